@@ -1,0 +1,359 @@
+/*
+ * CPU oracle for the quantized KV cache -- TEST INFRASTRUCTURE ONLY.
+ * See kvq_oracle.h for the sources cited below ([KIVI], [HF], [INNERQ] ...).
+ *
+ * Build: cc -O2 -std=c11 -ffp-contract=off -fno-fast-math -fPIC -shared.
+ * float arithmetic is IEEE single precision with round-to-nearest-even and
+ * no fused multiply-add, so every quantization decision below is the plain
+ * fp32 formula evaluated one operation at a time.
+ */
+#include "kvq_oracle.h"
+
+#include <fenv.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+int orc_rounding_is_nearest(void) { return fegetround() == FE_TONEAREST; }
+
+/* IEEE binary16 -> binary32, exact. */
+float orc_half_to_float(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int expo = (h >> 10) & 0x1f;
+  int man = h & 0x3ff;
+  float v;
+  if (expo == 0)
+    v = ldexpf((float)man, -24); /* zero or subnormal: man * 2^-24 */
+  else if (expo == 31)
+    v = man ? NAN : INFINITY;
+  else
+    v = ldexpf((float)(man | 0x400), expo - 25); /* (1024 + man) * 2^(e-25) */
+  return sign ? -v : v;
+}
+
+static void min_max(const float *x, int n, float *mn, float *mx) {
+  float lo = x[0], hi = x[0];
+  for (int i = 1; i < n; ++i) {
+    if (x[i] < lo) lo = x[i];
+    if (x[i] > hi) hi = x[i];
+  }
+  /* -0 and +0 compare equal; keep the result independent of their order. */
+  *mn = lo + 0.0f;
+  *mx = hi + 0.0f;
+}
+
+/*
+ * Asymmetric uniform quantizer of one group ([HF] §2.1: X_Q = round(X/S) - Z
+ * with scale S and zero offset Z; [KIVI] 2-bit asymmetric).  Written in the
+ * min/scale form: scale = (max - min) / (2^b - 1), zero = min,
+ * u = clamp(rint((x - min) / scale), 0, 2^b - 1), dequantized u*scale + zero.
+ * A constant group (max == min) stores scale 0 and all codes 0.
+ */
+void orc_quant_asym(const float *x, int n, int bits, float *scale, float *zero,
+                    uint8_t *u, int64_t ustride) {
+  const float top = (float)((1 << bits) - 1);
+  float mn, mx;
+  min_max(x, n, &mn, &mx);
+  *zero = mn;
+  if (mx == mn) {
+    *scale = 0.0f;
+    for (int i = 0; i < n; ++i) u[i * ustride] = 0;
+    return;
+  }
+  const float s = (mx - mn) / top;
+  *scale = s;
+  for (int i = 0; i < n; ++i) {
+    float r = rintf((x[i] - mn) / s);
+    if (r < 0.0f) r = 0.0f;
+    if (r > top) r = top;
+    u[i * ustride] = (uint8_t)r;
+  }
+}
+
+/*
+ * Symmetric quantizer of one group ([HF] §2.1: range symmetric about zero;
+ * [INNERQ] 方法论 2).  a = max(|min|, |max|), scale = a / (2^(b-1) - 1),
+ * q = clamp(rint(x / scale), -(2^(b-1) - 1), 2^(b-1) - 1).  Stored as the
+ * unsigned code u = q + 2^(b-1) with zero = -2^(b-1) * scale, so that
+ * u*scale + zero = q*scale dequantizes both modes with one formula.
+ */
+void orc_quant_sym(const float *x, int n, int bits, float *scale, float *zero,
+                   uint8_t *u, int64_t ustride) {
+  const int half = 1 << (bits - 1);
+  const float lim = (float)(half - 1);
+  float mn, mx;
+  min_max(x, n, &mn, &mx);
+  const float a = fmaxf(fabsf(mn), fabsf(mx));
+  const float s = a / lim;
+  *scale = s;
+  *zero = -(float)half * s;
+  for (int i = 0; i < n; ++i) {
+    float r = rintf(x[i] / s);
+    if (r < -lim) r = -lim;
+    if (r > lim) r = lim;
+    u[i * ustride] = (uint8_t)((int)r + half);
+  }
+}
+
+/*
+ * Per-group choice between the two ([INNERQ] 方法论 2: symmetric when the group
+ * is centred at zero, asymmetric otherwise; the page gives no threshold).
+ * Reading used: symmetric iff the group is not constant and its midpoint
+ * (max + min) / 2 lies within half an asymmetric step of zero, i.e.
+ * |max + min| <= (max - min) / (2^b - 1).
+ */
+int orc_choose_symmetric(float mn, float mx, int bits) {
+  if (mx == mn) return 0;
+  const float step = (mx - mn) / (float)((1 << bits) - 1);
+  return fabsf(mx + mn) <= step;
+}
+
+/* ---- KIVI ------------------------------------------------------------- */
+
+/* Key group: G consecutive tokens (rows of src, stride d) quantized per
+ * channel ([KIVI] 工作原理: keys grouped every G tokens, quantized along the
+ * channel dimension).  Destination: tokens t0 .. t0+G-1, t0 a multiple of G. */
+static void kivi_quant_key_group(orc_head *s, const uint16_t *src, int64_t t0) {
+  const int d = s->d, G = s->k_group;
+  float *x = (float *)malloc(sizeof(float) * (size_t)G);
+  for (int c = 0; c < d; ++c) {
+    for (int i = 0; i < G; ++i) x[i] = orc_half_to_float(src[(int64_t)i * d + c]);
+    orc_quant_asym(x, G, s->bits, &s->k_scale[(t0 / G) * d + c],
+                   &s->k_zero[(t0 / G) * d + c], &s->k_u[t0 * d + c], d);
+  }
+  free(x);
+}
+
+/* Value token: quantized per token in groups of v_group channels
+ * ([KIVI] 为什么…: values per token). */
+static void kivi_quant_value_token(orc_head *s, const uint16_t *src, int64_t t) {
+  const int d = s->d, Gv = s->v_group, ng = d / Gv;
+  float x[256];
+  for (int j = 0; j < ng; ++j) {
+    for (int i = 0; i < Gv; ++i) x[i] = orc_half_to_float(src[j * Gv + i]);
+    orc_quant_asym(x, Gv, s->bits, &s->v_scale[t * ng + j], &s->v_zero[t * ng + j],
+                   &s->v_u[t * d + j * Gv], 1);
+  }
+}
+
+/* ---- InnerQ ----------------------------------------------------------- */
+
+/* One token, groups of `group` consecutive channels along the inner (head)
+ * dimension, each group symmetric or asymmetric ([INNERQ] 方法论 1-2). */
+static void innerq_quant_token(const orc_head *s, const uint16_t *src, int group,
+                               int64_t t, uint8_t *u, float *scale, float *zero,
+                               uint8_t *sym) {
+  const int d = s->d, ng = d / group;
+  float x[256];
+  for (int j = 0; j < ng; ++j) {
+    for (int i = 0; i < group; ++i) x[i] = orc_half_to_float(src[j * group + i]);
+    float mn, mx;
+    min_max(x, group, &mn, &mx);
+    const int is_sym = orc_choose_symmetric(mn, mx, s->bits);
+    sym[t * ng + j] = (uint8_t)is_sym;
+    if (is_sym)
+      orc_quant_sym(x, group, s->bits, &scale[t * ng + j], &zero[t * ng + j],
+                    &u[t * d + j * group], 1);
+    else
+      orc_quant_asym(x, group, s->bits, &scale[t * ng + j], &zero[t * ng + j],
+                     &u[t * d + j * group], 1);
+  }
+}
+
+static void innerq_quant_kv(orc_head *s, const uint16_t *k, const uint16_t *v, int64_t t) {
+  innerq_quant_token(s, k, s->k_group, t, s->k_u, s->k_scale, s->k_zero, s->k_sym);
+  innerq_quant_token(s, v, s->v_group, t, s->v_u, s->v_scale, s->v_zero, s->v_sym);
+}
+
+/* ---- cache state machine ---------------------------------------------- */
+
+/*
+ * Prefill of one head's prompt K, V ([T][d] fp16).
+ * KIVI ([KIVI] 工作原理): the first l - r tokens, l - r a multiple of R (hence
+ *   of G), are quantized; the last r = T mod R stay fp16 in the residual.
+ * InnerQ ([INNERQ] 方法论 4; [KVQ5]): the first S tokens stay fp16 as sinks,
+ *   the last W as the recent window, the tokens between are quantized.
+ * Returns 0, or -1 when the quantized region would exceed the capacity.
+ */
+int orc_prefill(orc_head *s, const uint16_t *K, const uint16_t *V, int64_t T) {
+  const int d = s->d;
+  s->n_flush = 0;
+  if (s->scheme == ORC_KIVI) {
+    const int R = s->residual, G = s->k_group;
+    const int64_t nq = T - T % R;
+    if (nq > s->cap) return -1;
+    for (int64_t g = 0; g < nq / G; ++g) kivi_quant_key_group(s, K + g * G * d, g * G);
+    for (int64_t t = 0; t < nq; ++t) kivi_quant_value_token(s, V + t * d, t);
+    memcpy(s->k_res, K + nq * d, sizeof(uint16_t) * (size_t)((T - nq) * d));
+    memcpy(s->v_res, V + nq * d, sizeof(uint16_t) * (size_t)((T - nq) * d));
+    s->n_quant = nq;
+    s->n_resid = T - nq;
+    s->n_sink_used = 0;
+    return 0;
+  }
+  const int64_t ns = T < s->n_sink ? T : s->n_sink;
+  const int64_t rest = T - ns;
+  const int64_t nw = rest < s->residual ? rest : s->residual;
+  const int64_t nq = rest - nw;
+  if (nq > s->cap) return -1;
+  memcpy(s->k_sink, K, sizeof(uint16_t) * (size_t)(ns * d));
+  memcpy(s->v_sink, V, sizeof(uint16_t) * (size_t)(ns * d));
+  for (int64_t t = 0; t < nq; ++t) innerq_quant_kv(s, K + (ns + t) * d, V + (ns + t) * d, t);
+  memcpy(s->k_res, K + (T - nw) * d, sizeof(uint16_t) * (size_t)(nw * d));
+  memcpy(s->v_res, V + (T - nw) * d, sizeof(uint16_t) * (size_t)(nw * d));
+  s->n_sink_used = ns;
+  s->n_quant = nq;
+  s->n_resid = nw;
+  return 0;
+}
+
+/*
+ * One decode token (k, v: [d] fp16).
+ * KIVI ([KIVI] 工作原理; [HF] §3.1): the token joins the fp16 residual; when the
+ *   residual reaches R tokens all R are quantized (keys as R/G groups, values
+ *   per token), appended to the quantized region, and the residual empties.
+ * InnerQ ([INNERQ] 方法论 4): sinks fill first, then the window; once the
+ *   window holds W tokens its oldest token is quantized and appended to the
+ *   quantized region, and the new token takes its place.
+ * Returns 0, or -1 (state unchanged) when the quantized region is full.
+ */
+int orc_append(orc_head *s, const uint16_t *k, const uint16_t *v) {
+  const int d = s->d;
+  const size_t row = sizeof(uint16_t) * (size_t)d;
+  if (s->scheme == ORC_KIVI) {
+    const int R = s->residual, G = s->k_group;
+    if (s->n_resid + 1 == R && s->n_quant + R > s->cap) return -1;
+    memcpy(s->k_res + s->n_resid * d, k, row);
+    memcpy(s->v_res + s->n_resid * d, v, row);
+    s->n_resid += 1;
+    if (s->n_resid == R) {
+      for (int g = 0; g < R / G; ++g)
+        kivi_quant_key_group(s, s->k_res + (int64_t)g * G * d, s->n_quant + (int64_t)g * G);
+      for (int t = 0; t < R; ++t) kivi_quant_value_token(s, s->v_res + (int64_t)t * d, s->n_quant + t);
+      s->n_quant += R;
+      s->n_resid = 0;
+      s->n_flush += 1;
+    }
+    return 0;
+  }
+  if (s->n_sink_used < s->n_sink) {
+    memcpy(s->k_sink + s->n_sink_used * d, k, row);
+    memcpy(s->v_sink + s->n_sink_used * d, v, row);
+    s->n_sink_used += 1;
+    return 0;
+  }
+  if (s->n_resid < s->residual) {
+    memcpy(s->k_res + s->n_resid * d, k, row);
+    memcpy(s->v_res + s->n_resid * d, v, row);
+    s->n_resid += 1;
+    return 0;
+  }
+  if (s->n_quant + 1 > s->cap) return -1;
+  if (s->residual == 0) { /* no window: the token itself is quantized */
+    innerq_quant_kv(s, k, v, s->n_quant);
+    s->n_quant += 1;
+    return 0;
+  }
+  innerq_quant_kv(s, s->k_res, s->v_res, s->n_quant);
+  s->n_quant += 1;
+  memmove(s->k_res, s->k_res + d, row * (size_t)(s->residual - 1));
+  memmove(s->v_res, s->v_res + d, row * (size_t)(s->residual - 1));
+  memcpy(s->k_res + (int64_t)(s->residual - 1) * d, k, row);
+  memcpy(s->v_res + (int64_t)(s->residual - 1) * d, v, row);
+  return 0;
+}
+
+/* Dequantized key / value element of quantized token t, channel c, in fp64. */
+static double key_hat(const orc_head *s, int64_t t, int c) {
+  const int d = s->d;
+  const double u = (double)s->k_u[t * d + c];
+  if (s->scheme == ORC_KIVI) {
+    const int64_t i = (t / s->k_group) * d + c;
+    return u * (double)s->k_scale[i] + (double)s->k_zero[i];
+  }
+  const int64_t i = t * (d / s->k_group) + c / s->k_group;
+  return u * (double)s->k_scale[i] + (double)s->k_zero[i];
+}
+
+static double value_hat(const orc_head *s, int64_t t, int c) {
+  const int d = s->d;
+  const int64_t i = t * (d / s->v_group) + c / s->v_group;
+  return (double)s->v_u[t * d + c] * (double)s->v_scale[i] + (double)s->v_zero[i];
+}
+
+/*
+ * Decode attention of one query head q ([d] fp16) over the whole cache in
+ * fp64: softmax(tau * q . k) . v over the fp16 sink tokens, the dequantized
+ * tokens and the fp16 residual / window tokens ([IKV]: fp16 tokens joined
+ * with the dequantized cache; [KIVI] 背景: every decode step reads the whole
+ * cache).  Max-subtracted softmax.  An empty cache gives a zero output.
+ * Returns 0, or -1 on allocation failure.
+ */
+int orc_attend(const orc_head *s, const uint16_t *q, double tau, double *out) {
+  const int d = s->d;
+  const int64_t n = s->n_sink_used + s->n_quant + s->n_resid;
+  for (int c = 0; c < d; ++c) out[c] = 0.0;
+  if (n == 0) return 0;
+  double *sc = (double *)malloc(sizeof(double) * (size_t)n);
+  double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+  if (!sc || !qd) { free(sc); free(qd); return -1; }
+  for (int c = 0; c < d; ++c) qd[c] = (double)orc_half_to_float(q[c]);
+
+  int64_t i = 0;
+  for (int64_t t = 0; t < s->n_sink_used; ++t, ++i) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += qd[c] * (double)orc_half_to_float(s->k_sink[t * d + c]);
+    sc[i] = tau * acc;
+  }
+  for (int64_t t = 0; t < s->n_quant; ++t, ++i) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += qd[c] * key_hat(s, t, c);
+    sc[i] = tau * acc;
+  }
+  for (int64_t t = 0; t < s->n_resid; ++t, ++i) {
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += qd[c] * (double)orc_half_to_float(s->k_res[t * d + c]);
+    sc[i] = tau * acc;
+  }
+
+  double m = sc[0];
+  for (int64_t j = 1; j < n; ++j) if (sc[j] > m) m = sc[j];
+  double l = 0.0;
+  for (int64_t j = 0; j < n; ++j) { sc[j] = exp(sc[j] - m); l += sc[j]; }
+
+  i = 0;
+  for (int64_t t = 0; t < s->n_sink_used; ++t, ++i)
+    for (int c = 0; c < d; ++c) out[c] += sc[i] * (double)orc_half_to_float(s->v_sink[t * d + c]);
+  for (int64_t t = 0; t < s->n_quant; ++t, ++i)
+    for (int c = 0; c < d; ++c) out[c] += sc[i] * value_hat(s, t, c);
+  for (int64_t t = 0; t < s->n_resid; ++t, ++i)
+    for (int c = 0; c < d; ++c) out[c] += sc[i] * (double)orc_half_to_float(s->v_res[t * d + c]);
+  for (int c = 0; c < d; ++c) out[c] /= l;
+
+  free(sc);
+  free(qd);
+  return 0;
+}
+
+/*
+ * Bit packing of code rows ([n_rows][d], one code per byte) into
+ * [n_rows][d*bits/8] bytes: along the channels of a token, little-endian
+ * within each byte, channel c at bits (c mod (8/bits))*bits of byte
+ * c / (8/bits).  The pages fix no layout; this one is the library's.
+ */
+void orc_pack(const uint8_t *u, int64_t n_rows, int d, int bits, uint8_t *out) {
+  const int per = 8 / bits;
+  const int rb = d / per;
+  memset(out, 0, (size_t)(n_rows * rb));
+  for (int64_t t = 0; t < n_rows; ++t)
+    for (int c = 0; c < d; ++c)
+      out[t * rb + c / per] |= (uint8_t)(u[t * d + c] << ((c % per) * bits));
+}
+
+/* Mode flags (one per group, token-major) as bits: flag i is bit i % 32 of
+ * word i / 32.  `out` holds ceil(n / 32) words. */
+void orc_pack_modes(const uint8_t *sym, int64_t n, uint32_t *out) {
+  memset(out, 0, sizeof(uint32_t) * (size_t)((n + 31) / 32));
+  for (int64_t i = 0; i < n; ++i)
+    if (sym[i]) out[i / 32] |= (uint32_t)1 << (i % 32);
+}

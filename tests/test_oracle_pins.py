@@ -1,0 +1,467 @@
+"""Pins of the CPU oracle against facts fixed outside it (no GPU).
+
+Each pin checks the oracle against something other than its own code: the
+hand-worked rows and the page-printed numbers under tests/golden/, numpy's
+IEEE fp16 conversion, closed-form round-trip bounds, grid-exact data (where
+quantization is lossless, so attention must equal a library softmax-attention
+call on the raw fp16 data), torch's scaled_dot_product_attention in fp64,
+perturbation bounds, and the residual-flush cadence.  The last test plants
+mistakes in copies of the oracle's C file and checks that every one of them
+fails at least one pin.
+"""
+import math
+import os
+import shutil
+import tempfile
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_kv_cache_14_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+# --------------------------------------------------------------------------
+# scalar pins
+# --------------------------------------------------------------------------
+
+def pin_half_to_float():
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    for b in list(range(0, 1 << 16, 97)) + [0, 1, 0x3ff, 0x400, 0x3c00, 0x7bff, 0x8001, 0xfbff]:
+        got = np.float32(oracle.half_to_float(int(b)))
+        r = ref[b]
+        assert (np.isnan(got) and np.isnan(r)) or got.tobytes() == r.tobytes(), hex(b)
+
+
+def pin_worked_examples():
+    for row in _golden_rows("asym_worked_examples.txt"):
+        head, xs, scale, zero, codes = [c.strip() for c in row.split("|")]
+        mode, bits = head.split()
+        x = np.array([float(v) for v in xs.split()], np.float32)
+        fn = oracle.quant_asym if mode == "asym" else oracle.quant_sym
+        s, z, u = fn(x, int(bits))
+        assert s == np.float32(float(scale)), (row, s)
+        assert z == np.float32(float(zero)), (row, z)
+        assert list(u) == [int(c) for c in codes.split()], (row, u)
+
+
+def pin_mode_choice():
+    # midpoint 0 -> symmetric; far from zero -> asymmetric; equality -> symmetric
+    assert oracle.choose_symmetric(-1.0, 1.0, 4)
+    assert not oracle.choose_symmetric(0.0, 3.0, 2)
+    assert oracle.choose_symmetric(-1.0, 2.0, 2)        # |1| <= 3/3
+    assert not oracle.choose_symmetric(-1.0, 2.25, 2)   # |1.25| > 3.25/3
+    assert not oracle.choose_symmetric(2.0, 2.0, 4)     # constant group
+
+
+def pin_pack_layout():
+    for row in _golden_rows("pack_layout_example.txt"):
+        bits, codes, hexes = [c.strip() for c in row.split("|")]
+        u = np.array([[int(c) for c in codes.split()]], np.uint8)
+        got = oracle.pack(u, int(bits))[0]
+        assert [int(h, 16) for h in hexes.split()] == list(got), row
+
+
+def pin_llama2_bytes_per_token():
+    # layers * (K and V) * heads * bytes of one packed head row (codes only);
+    # the 16-bit row is the fp16 residual row the cache keeps unquantized.
+    L, H, d = 32, 32, 128
+    for row in _golden_rows("llama2_7b_bytes_per_token.txt"):
+        bits, expect = map(int, row.split())
+        if bits == 16:
+            row_bytes = d * np.dtype(np.float16).itemsize
+        else:
+            row_bytes = oracle.pack(np.zeros((1, d), np.uint8), bits).nbytes
+        assert L * 2 * H * row_bytes == expect
+    # "10k tokens about 5 GB" for fp16
+    assert abs(10_000 * 524288 / 1e9 - 5.0) < 0.3
+
+
+def _rand_groups(rng, n_groups, n, bits):
+    x = rng.standard_normal((n_groups, n)).astype(np.float16).astype(np.float32)
+    x[::7] *= 20.0
+    x[1::5] += 3.0
+    return x
+
+
+def pin_round_trip_bound():
+    rng = np.random.default_rng(11)
+    for bits in (2, 4, 8):
+        for n in (4, 32, 64):
+            for x in _rand_groups(rng, 60, n, bits):
+                for fn in (oracle.quant_asym, oracle.quant_sym):
+                    s, z, u = fn(x, bits)
+                    xh = u.astype(np.float64) * np.float64(s) + np.float64(z)
+                    amax = float(np.max(np.abs(x)))
+                    slack = 4 * np.spacing(np.float32(amax))
+                    assert np.all(np.abs(x - xh) <= float(s) / 2 + slack), (fn, bits, n)
+
+
+def pin_endpoints():
+    rng = np.random.default_rng(12)
+    for bits in (2, 4):
+        top, lim = (1 << bits) - 1, (1 << (bits - 1)) - 1
+        for x in _rand_groups(rng, 50, 32, bits):
+            s, z, u = oracle.quant_asym(x, bits)
+            assert u[np.argmin(x)] == 0 and u[np.argmax(x)] == top
+            assert z == x.min()
+            s, z, u = oracle.quant_sym(x, bits)
+            i = np.argmax(np.abs(x))
+            assert int(u[i]) - (1 << (bits - 1)) == (lim if x[i] > 0 else -lim)
+
+
+def pin_grid_exact_round_trip():
+    rng = np.random.default_rng(13)
+    for bits in (2, 4):
+        top = (1 << bits) - 1
+        for _ in range(200):
+            e = int(rng.integers(1, 6))
+            step = 2.0 ** -e
+            base = float(rng.integers(-40, 40)) * step
+            u = rng.integers(0, top + 1, 32)
+            u[rng.integers(0, 16)] = 0
+            u[16 + rng.integers(0, 16)] = top
+            x = (base + u * step).astype(np.float32)
+            s, z, got = oracle.quant_asym(x, bits)
+            assert s == np.float32(step) and z == np.float32(base)
+            assert np.array_equal(got, u)
+
+
+# --------------------------------------------------------------------------
+# cache state machine pins
+# --------------------------------------------------------------------------
+
+def _randn16(rng, *shape, scale=1.0):
+    return (rng.standard_normal(shape) * scale).astype(np.float16)
+
+
+def pin_kivi_flush_cadence():
+    rng = np.random.default_rng(14)
+    d, G, R = 16, 8, 32
+    for T in (0, 5, 31, 32, 100, 120):
+        h = oracle.OracleHead(d, 2, oracle.KIVI, G, 8, R, 0, 1024)
+        K, V = _randn16(rng, T, d), _randn16(rng, T, d)
+        h.prefill(K, V)
+        assert h.n_resid == T % R and h.n_quant == T - T % R
+        n0 = h.n_resid
+        for n in range(1, 140):
+            h.append(_randn16(rng, d), _randn16(rng, d))
+            assert h.n_flush == (n0 + n) // R
+            assert 0 <= h.n_resid < R and h.n_quant % G == 0
+            assert h.n_quant + h.n_resid == T + n
+        # the residual always holds the newest tokens, oldest first
+        kr, _ = h.residual_tokens()
+        assert kr.shape[0] == (T + 139) % R
+
+
+def pin_kivi_residual_is_exact_and_tail():
+    rng = np.random.default_rng(15)
+    d, G, R, T = 16, 8, 32, 77
+    K, V = _randn16(rng, T, d), _randn16(rng, T, d)
+    h = oracle.OracleHead(d, 2, oracle.KIVI, G, 8, R, 0, 256)
+    h.prefill(K, V)
+    kr, vr = h.residual_tokens()
+    assert np.array_equal(kr.view(np.uint16), K[64:].view(np.uint16))
+    assert np.array_equal(vr.view(np.uint16), V[64:].view(np.uint16))
+
+
+def pin_kivi_cache_round_trip():
+    """Every quantized element of a prefilled + appended cache reconstructs
+    within scale/2 through the storage layout (key meta per (G-token group,
+    channel), value meta per (token, channel group))."""
+    rng = np.random.default_rng(16)
+    d, G, Gv, R, T, n_app = 32, 8, 16, 16, 64, 40
+    K, V = _randn16(rng, T + n_app, d, scale=2.0), _randn16(rng, T + n_app, d)
+    for bits in (2, 4):
+        h = oracle.OracleHead(d, bits, oracle.KIVI, G, Gv, R, 0, 256)
+        h.prefill(K[:T], V[:T])
+        for i in range(T, T + n_app):
+            h.append(K[i], V[i])
+        n = h.n_quant
+        t = np.arange(n)
+        ks = h.k_scale[t // G]                       # [n][d]
+        kz = h.k_zero[t // G]
+        kh = h.k_u[:n] * ks.astype(np.float64) + kz
+        vs = np.repeat(h.v_scale[:n], Gv, axis=1)
+        vz = np.repeat(h.v_zero[:n], Gv, axis=1)
+        vh = h.v_u[:n] * vs.astype(np.float64) + vz
+        kx, vx = K[:n].astype(np.float64), V[:n].astype(np.float64)
+        assert np.all(np.abs(kx - kh) <= ks / 2 + 1e-5)
+        assert np.all(np.abs(vx - vh) <= vs / 2 + 1e-5)
+        # key groups: code 0 at the channel minimum of each group
+        kg = K[:n].astype(np.float32).reshape(n // G, G, d)
+        assert np.array_equal(h.k_zero[: n // G], kg.min(axis=1))
+
+
+def pin_innerq_windows():
+    rng = np.random.default_rng(17)
+    d, S, W = 128, 4, 8
+    for T in (0, 2, 4, 9, 12, 50):
+        K, V = _randn16(rng, T + 30, d), _randn16(rng, T + 30, d)
+        h = oracle.OracleHead(d, 4, oracle.INNERQ, 64, 64, W, S, 256)
+        h.prefill(K[:T], V[:T])
+        for i in range(T, T + 30):
+            h.append(K[i], V[i])
+            n = i + 1
+            assert h.n_sink_used == min(S, n)
+            assert h.n_resid == min(W, max(0, n - S))
+            assert h.n_quant == max(0, n - S - W)
+        ks, _ = h.sink_tokens()
+        kw, vw = h.residual_tokens()
+        n = T + 30
+        assert np.array_equal(ks.view(np.uint16), K[:S].view(np.uint16))
+        assert np.array_equal(kw.view(np.uint16), K[n - W:n].view(np.uint16))
+        assert np.array_equal(vw.view(np.uint16), V[n - W:n].view(np.uint16))
+        # quantized tokens are S .. n-W-1 in order: each reconstructs within scale/2
+        q = h.n_quant
+        src = K[S:S + q].astype(np.float64)
+        sc = np.repeat(h.k_scale[:q], 64, axis=1).astype(np.float64)
+        zz = np.repeat(h.k_zero[:q], 64, axis=1).astype(np.float64)
+        assert np.all(np.abs(src - (h.k_u[:q] * sc + zz)) <= sc / 2 + 1e-5)
+
+
+def pin_innerq_modes():
+    """Group modes follow the min/max rule, codes reach the symmetric limits."""
+    rng = np.random.default_rng(18)
+    d = 128
+    K = _randn16(rng, 40, d)
+    K[:, 64:] += np.float16(3.0)     # second group is far from zero: asymmetric
+    V = _randn16(rng, 40, d)
+    h = oracle.OracleHead(d, 4, oracle.INNERQ, 64, 64, 0, 0, 64)
+    h.prefill(K, V)
+    assert h.n_quant == 40
+    x = K.astype(np.float32)
+    for t in range(40):
+        for j in range(2):
+            g = x[t, 64 * j:64 * j + 64]
+            mn, mx = g.min(), g.max()
+            sym = abs(np.float32(mx + mn)) <= np.float32((mx - mn) / np.float32(15))
+            assert bool(h.k_sym[t, j]) == bool(sym)
+        assert h.k_sym[t, 1] == 0
+
+
+# --------------------------------------------------------------------------
+# attention pins
+# --------------------------------------------------------------------------
+
+def _sdpa(q, K, V, tau):
+    """torch scaled_dot_product_attention in fp64 on the CPU, one query."""
+    qt = torch.from_numpy(q.astype(np.float64))[None, None, None, :]
+    kt = torch.from_numpy(K.astype(np.float64))[None, None]
+    vt = torch.from_numpy(V.astype(np.float64))[None, None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=tau)
+    return o[0, 0, 0].numpy()
+
+
+def pin_attention_unquantized_is_sdpa():
+    rng = np.random.default_rng(19)
+    d, T = 64, 50
+    K, V = _randn16(rng, T + 20, d, scale=2.0), _randn16(rng, T + 20, d)
+    q = _randn16(rng, d)
+    h = oracle.OracleHead(d, 2, oracle.KIVI, 32, 32, 128, 0, 256)   # R > T + steps
+    h.prefill(K[:T], V[:T])
+    for i in range(T, T + 20):
+        h.append(K[i], V[i])
+    assert h.n_quant == 0
+    tau = 1 / math.sqrt(d)
+    np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K, V, tau), rtol=0, atol=1e-12)
+
+
+def _grid_tokens(rng, T, d, bits, k_rows, v_cols, sym_groups=False):
+    """fp16 tokens that every group quantizes losslessly.  Keys: groups of
+    k_rows consecutive tokens per channel (k_rows=1: per token over v_cols
+    channels, like values).  Values: per token, groups of v_cols channels."""
+    top = (1 << bits) - 1
+
+    def grid(n):
+        e = int(rng.integers(1, 5))
+        step = 2.0 ** -e
+        if sym_groups and rng.integers(0, 2):
+            lim = (1 << (bits - 1)) - 1
+            u = rng.integers(-lim, lim + 1, n)
+            u[0], u[-1] = -lim, lim
+            return rng.permutation(u) * step
+        base = float(rng.integers(-24, 24)) * step
+        if sym_groups:
+            base = abs(base) + 4.0          # clearly off-centre: asymmetric
+        u = rng.integers(0, top + 1, n)
+        u[0], u[-1] = 0, top
+        return base + rng.permutation(u) * step
+
+    K = np.empty((T, d), np.float64)
+    V = np.empty((T, d), np.float64)
+    if k_rows > 1:
+        for g in range(T // k_rows):
+            for c in range(d):
+                K[g * k_rows:(g + 1) * k_rows, c] = grid(k_rows)
+    else:
+        for t in range(T):
+            for j in range(d // v_cols):
+                K[t, j * v_cols:(j + 1) * v_cols] = grid(v_cols)
+    for t in range(T):
+        for j in range(d // v_cols):
+            V[t, j * v_cols:(j + 1) * v_cols] = grid(v_cols)
+    K16, V16 = K.astype(np.float16), V.astype(np.float16)
+    assert np.array_equal(K16.astype(np.float64), K) and np.array_equal(V16.astype(np.float64), V)
+    return K16, V16
+
+
+def pin_attention_grid_exact_kivi():
+    rng = np.random.default_rng(20)
+    d, G, Gv, R = 32, 8, 16, 16
+    for bits in (2, 4):
+        T = 64 + 7
+        K, V = _grid_tokens(rng, 64 + 16, d, bits, G, Gv)
+        Kx, Vx = _randn16(rng, 40, d), _randn16(rng, 40, d)
+        h = oracle.OracleHead(d, bits, oracle.KIVI, G, Gv, R, 0, 256)
+        h.prefill(K[:T], V[:T])              # 64 quantized, 7 residual
+        for i in range(T, 80):
+            h.append(K[i], V[i])             # flush at 80: all 80 quantized
+        assert h.n_quant == 80 and h.n_resid == 0
+        q = _randn16(rng, d)
+        tau = 1 / math.sqrt(d)
+        np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K[:80], V[:80], tau),
+                                   rtol=0, atol=1e-12)
+        # with a non-empty fp16 residual next to the quantized part
+        h.append(Kx[0], Vx[0])
+        Kall = np.concatenate([K[:80], Kx[:1]])
+        Vall = np.concatenate([V[:80], Vx[:1]])
+        np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, Kall, Vall, tau),
+                                   rtol=0, atol=1e-12)
+
+
+def pin_attention_grid_exact_innerq():
+    rng = np.random.default_rng(21)
+    d, S, W, T = 128, 4, 8, 60
+    K, V = _grid_tokens(rng, T, d, 4, 1, 64, sym_groups=True)
+    K[0] *= np.float16(8)                      # loud sink token, kept fp16
+    h = oracle.OracleHead(d, 4, oracle.INNERQ, 64, 64, W, S, 256)
+    h.prefill(K, V)
+    assert h.n_quant == T - S - W
+    assert 0 < h.k_sym[:h.n_quant].sum() < h.k_sym[:h.n_quant].size
+    q = _randn16(rng, d)
+    tau = 1 / math.sqrt(d)
+    np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K, V, tau), rtol=0, atol=1e-12)
+
+
+def pin_attention_identical_keys_mean():
+    rng = np.random.default_rng(22)
+    d, G, Gv, R, T = 32, 8, 8, 16, 48
+    krow = _randn16(rng, d)
+    K = np.repeat(krow[None], T + 3, axis=0)
+    V = _randn16(rng, T + 3, d)
+    h = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 128)
+    h.prefill(K[:T], V[:T])
+    for i in range(T, T + 3):
+        h.append(K[i], V[i])
+    n = h.n_quant
+    # constant key groups are lossless; output = mean of the values as stored
+    vh = h.v_u[:n] * np.repeat(h.v_scale[:n], Gv, axis=1).astype(np.float64) \
+        + np.repeat(h.v_zero[:n], Gv, axis=1)
+    _, vr = h.residual_tokens()
+    expect = np.concatenate([vh, vr.astype(np.float64)]).mean(axis=0)
+    np.testing.assert_allclose(h.attend(_randn16(rng, d), 0.3), expect, rtol=0, atol=1e-12)
+
+
+def pin_attention_error_bound():
+    """Random data: the quantized-cache output stays within the perturbation
+    bound implied by |x - x_hat| <= scale/2 of the fp64 attention over the
+    raw fp16 cache."""
+    rng = np.random.default_rng(23)
+    d, G, Gv, R, T = 64, 16, 16, 32, 200
+    for bits in (2, 4):
+        K, V = _randn16(rng, T, d), _randn16(rng, T, d)
+        h = oracle.OracleHead(d, bits, oracle.KIVI, G, Gv, R, 0, 256)
+        h.prefill(K, V)
+        n = h.n_quant
+        q = _randn16(rng, d)
+        tau = 1 / math.sqrt(d)
+        ks = h.k_scale[np.arange(n) // G].astype(np.float64)
+        delta = tau * (np.abs(q.astype(np.float64))[None, :] * ks / 2).sum(axis=1).max()
+        vs = np.repeat(h.v_scale[:n], Gv, axis=1).astype(np.float64)
+        vmax = np.abs(V.astype(np.float64)).max() + vs.max() / 2
+        bound = (math.exp(2 * delta) - 1) * vmax + vs.max() / 2 + 1e-9
+        err = np.abs(h.attend(q, tau) - _sdpa(q, K, V, tau)).max()
+        assert err <= bound, (bits, err, bound)
+        assert err > 0
+
+
+def pin_workload_shapes():
+    """The named workloads have the shapes their descriptions give."""
+    w = synth.WORKLOADS["llama2_7b_2bit"]
+    assert (w.batch, w.n_kv_heads, w.head_dim, w.ctx, w.bits, w.k_group, w.residual) == \
+        (8, 32, 128, 4096, 2, 32, 128)
+    assert w.n_outliers() == 82
+    assert synth.WORKLOADS["gqa_2bit"].n_outliers() == 20
+    assert synth.WORKLOADS["innerq_1m"].ctx == 1048576
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each must fail at least one pin
+# --------------------------------------------------------------------------
+
+MUTANTS = [
+    ("ties away from zero", "float r = rintf((x[i] - mn) / s);", "float r = roundf((x[i] - mn) / s);"),
+    ("zero = max", "*zero = mn;\n  if (mx == mn)", "*zero = mx;\n  if (mx == mn)"),
+    ("2^b levels", "const float s = (mx - mn) / top;", "const float s = (mx - mn) / (top + 1.0f);"),
+    ("sym zero off by one", "*zero = -(float)half * s;", "*zero = -(float)(half - 1) * s;"),
+    ("strict mode rule", "return fabsf(mx + mn) <= step;", "return fabsf(mx + mn) < step;"),
+    ("key meta by token", "const int64_t i = (t / s->k_group) * d + c;", "const int64_t i = (t % s->k_group) * d + c;"),
+    ("value zero dropped", "return (double)s->v_u[t * d + c] * (double)s->v_scale[i] + (double)s->v_zero[i];",
+     "return (double)s->v_u[t * d + c] * (double)s->v_scale[i];"),
+    ("flush one early", "if (s->n_resid == R) {", "if (s->n_resid == R - 1) {"),
+    ("prefill split by G", "const int64_t nq = T - T % R;", "const int64_t nq = T - T % G;"),
+    ("softmax sign", "sc[j] = exp(sc[j] - m);", "sc[j] = exp(m - sc[j]);"),
+    ("tau dropped", "for (int c = 0; c < d; ++c) acc += qd[c] * key_hat(s, t, c);\n    sc[i] = tau * acc;",
+     "for (int c = 0; c < d; ++c) acc += qd[c] * key_hat(s, t, c);\n    sc[i] = acc;"),
+    ("big-endian pack", "<< ((c % per) * bits)", "<< ((per - 1 - c % per) * bits)"),
+    ("evict newest", "innerq_quant_kv(s, s->k_res, s->v_res, s->n_quant);", "innerq_quant_kv(s, k, v, s->n_quant);"),
+    ("half exponent bias", "expo - 25", "expo - 24"),
+    ("value group transposed", "x[i] = orc_half_to_float(src[j * Gv + i]);", "x[i] = orc_half_to_float(src[i * (d / Gv) + j]);"),
+]
+
+
+def test_planted_mistakes_are_caught():
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "kvq_oracle.c")).read()
+    tmp = tempfile.mkdtemp(prefix="orc_mut_")
+    try:
+        survivors = []
+        for i, (name, old, new) in enumerate(MUTANTS):
+            assert src.count(old) == 1, name
+            path = os.path.join(tmp, "m%d.c" % i)
+            with open(path, "w") as f:
+                f.write(src.replace(old, new))
+            so = oracle.build(force=True, src=path, out=os.path.join(tmp, "m%d.so" % i))
+            failed = False
+            with oracle.using_library(so):
+                for pin in PINS:
+                    try:
+                        pin()
+                    except (AssertionError, ValueError):
+                        failed = True
+                        break
+            if not failed:
+                survivors.append(name)
+        assert not survivors, "mutants not caught: %s" % survivors
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
