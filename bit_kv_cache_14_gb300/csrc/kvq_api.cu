@@ -1,0 +1,305 @@
+// C ABI of libkvq: validation, buffer sizes, host counters, launches.
+// Declarations and contracts: include/kvq.h.
+#include <string.h>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+thread_local int t_last_launches = 0;
+
+bool pow2_group(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int num_sms_cached() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+}  // namespace
+
+void note_launch(int n) { t_last_launches = n; }
+
+int resolve(const kvq_config *cfg, Geometry *g) {
+  if (!cfg || !g) return KVQ_EINVAL;
+  const kvq_config &c = *cfg;
+  if (c.batch < 1 || c.n_kv_heads < 1 || c.n_q_heads < 1 || c.max_ctx < 1) return KVQ_EINVAL;
+  if (c.n_q_heads % c.n_kv_heads != 0) return KVQ_EINVAL;
+  if (c.scheme != KVQ_KIVI && c.scheme != KVQ_INNERQ) return KVQ_EINVAL;
+  if (c.residual < 0 || c.n_sink < 0 || c.k_group < 1 || c.v_group < 1) return KVQ_EINVAL;
+  const int rg = c.n_q_heads / c.n_kv_heads;
+  if (rg != 1 && rg != 2 && rg != 4 && rg != 8) return KVQ_EUNSUPPORTED;
+  if (c.head_dim != 64 && c.head_dim != 128) return KVQ_EUNSUPPORTED;
+  if (c.bits != 2 && c.bits != 4) return KVQ_EUNSUPPORTED;
+  if ((int64_t)c.batch * c.n_kv_heads > 65535) return KVQ_EUNSUPPORTED;
+  if (!pow2_group(c.v_group) || c.head_dim % c.v_group != 0) return KVQ_EUNSUPPORTED;
+  if (c.residual > kMaxResidual || c.n_sink > kMaxResidual) return KVQ_EUNSUPPORTED;
+  if (c.scheme == KVQ_KIVI) {
+    if (c.n_sink != 0) return KVQ_EINVAL;
+    if (c.residual < 1 || c.residual % c.k_group != 0) return KVQ_EINVAL;
+    if (!pow2_group(c.k_group)) return KVQ_EUNSUPPORTED;
+  } else {
+    if (!pow2_group(c.k_group) || c.head_dim % c.k_group != 0) return KVQ_EUNSUPPORTED;
+  }
+  g->B = c.batch;
+  g->H = c.n_kv_heads;
+  g->Hq = c.n_q_heads;
+  g->d = c.head_dim;
+  g->bits = c.bits;
+  g->scheme = c.scheme;
+  g->k_group = c.k_group;
+  g->v_group = c.v_group;
+  g->residual = c.residual;
+  g->n_sink = c.n_sink;
+  g->max_ctx = c.max_ctx;
+  g->row_bytes = c.head_dim * c.bits / 8;
+  g->v_meta_cols = c.head_dim / c.v_group;
+  if (c.scheme == KVQ_KIVI) {
+    g->k_meta_cols = c.head_dim;
+    g->k_meta_rows = (c.max_ctx + c.k_group - 1) / c.k_group;
+    g->mode_words = 0;
+  } else {
+    g->k_meta_cols = c.head_dim / c.k_group;
+    g->k_meta_rows = c.max_ctx;
+    g->mode_words = (c.max_ctx * (c.head_dim / c.k_group) + 31) / 32;
+    const int64_t vw = (c.max_ctx * (c.head_dim / c.v_group) + 31) / 32;
+    if (vw > g->mode_words) g->mode_words = vw;
+  }
+  return KVQ_OK;
+}
+
+CachePtrs ptrs_of(const kvq_cache *c) {
+  CachePtrs p;
+  p.k_codes = static_cast<uint8_t *>(c->k_codes);
+  p.v_codes = static_cast<uint8_t *>(c->v_codes);
+  p.k_scale = c->k_scale;
+  p.k_zero = c->k_zero;
+  p.v_scale = c->v_scale;
+  p.v_zero = c->v_zero;
+  p.k_mode = c->k_mode;
+  p.v_mode = c->v_mode;
+  p.k_res = reinterpret_cast<__half *>(c->k_res);
+  p.v_res = reinterpret_cast<__half *>(c->v_res);
+  p.k_sink = reinterpret_cast<__half *>(c->k_sink);
+  p.v_sink = reinterpret_cast<__half *>(c->v_sink);
+  p.status = c->dev_status;
+  return p;
+}
+
+// The buffers a configuration uses must be present and 16-byte aligned.
+static int check_cache(const Geometry &g, const kvq_cache *c) {
+  if (!c) return KVQ_EINVAL;
+  const void *need[] = {c->k_codes, c->v_codes, c->k_scale, c->k_zero, c->v_scale, c->v_zero};
+  for (const void *p : need) {
+    if (!p) return KVQ_EINVAL;
+    if (!aligned16(p)) return KVQ_EALIGN;
+  }
+  if (g.residual > 0) {
+    if (!c->k_res || !c->v_res) return KVQ_EINVAL;
+    if (!aligned16(c->k_res) || !aligned16(c->v_res)) return KVQ_EALIGN;
+  }
+  if (g.scheme == KVQ_INNERQ) {
+    if (!c->k_mode || !c->v_mode) return KVQ_EINVAL;
+    if (!aligned16(c->k_mode) || !aligned16(c->v_mode)) return KVQ_EALIGN;
+    if (g.n_sink > 0) {
+      if (!c->k_sink || !c->v_sink) return KVQ_EINVAL;
+      if (!aligned16(c->k_sink) || !aligned16(c->v_sink)) return KVQ_EALIGN;
+    }
+  }
+  if (c->n_quant < 0 || c->n_resid < 0 || c->n_sink < 0 || c->ring_head < 0) return KVQ_EINVAL;
+  return KVQ_OK;
+}
+
+static int from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA; }
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out) {
+  if (!out) return KVQ_EINVAL;
+  Geometry g;
+  const int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  memset(out, 0, sizeof(*out));
+  const size_t BH = (size_t)g.B * g.H;
+  out->k_codes = out->v_codes = BH * (size_t)g.max_ctx * g.row_bytes;
+  out->k_scale = out->k_zero = BH * (size_t)g.k_meta_rows * g.k_meta_cols * sizeof(float);
+  out->v_scale = out->v_zero = BH * (size_t)g.max_ctx * g.v_meta_cols * sizeof(float);
+  if (g.scheme == KVQ_INNERQ) out->k_mode = out->v_mode = BH * (size_t)g.mode_words * 4;
+  out->k_res = out->v_res = BH * (size_t)g.residual * g.d * 2;
+  out->k_sink = out->v_sink = BH * (size_t)g.n_sink * g.d * 2;
+  out->status = sizeof(int32_t);
+  return KVQ_OK;
+}
+
+int kvq_workspace_bytes(const kvq_config *cfg, size_t *bytes) {
+  if (!bytes) return KVQ_EINVAL;
+  Geometry g;
+  const int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  *bytes = decode_workspace_bytes(g);
+  return KVQ_OK;
+}
+
+int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K,
+                         const uint16_t *V, int64_t T, void *stream) {
+  Geometry g;
+  int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if (T < 0) return KVQ_EINVAL;
+  if (T > 0 && (!K || !V)) return KVQ_EINVAL;
+  if (T > 0 && (!aligned16(K) || !aligned16(V))) return KVQ_EALIGN;
+  if (T > g.max_ctx) return KVQ_ECAPACITY;
+  int64_t nq, nr, ns;
+  if (g.scheme == KVQ_KIVI) {
+    nq = T - T % g.residual;
+    nr = T - nq;
+    ns = 0;
+  } else {
+    ns = T < g.n_sink ? T : g.n_sink;
+    const int64_t rest = T - ns;
+    nr = rest < g.residual ? rest : g.residual;
+    nq = rest - nr;
+  }
+  int launches = 0;
+  r = from_cuda(launch_prefill(g, ptrs_of(cache), reinterpret_cast<const __half *>(K),
+                               reinterpret_cast<const __half *>(V), T, nq, nr, ns,
+                               static_cast<cudaStream_t>(stream), &launches));
+  if (r != KVQ_OK) return r;
+  cache->n_quant = nq;
+  cache->n_resid = nr;
+  cache->n_sink = ns;
+  cache->ring_head = 0;
+  note_launch(launches);
+  return KVQ_OK;
+}
+
+int kvq_append(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k, const uint16_t *v,
+               void *stream) {
+  Geometry g;
+  int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if (!k || !v) return KVQ_EINVAL;
+  if (!aligned16(k) || !aligned16(v)) return KVQ_EALIGN;
+  if (cache->n_quant + cache->n_resid + cache->n_sink + 1 > g.max_ctx) return KVQ_ECAPACITY;
+  if (g.scheme == KVQ_KIVI && cache->n_resid >= g.residual) return KVQ_EINVAL;
+  if (g.scheme == KVQ_INNERQ && g.residual > 0 && cache->ring_head >= g.residual) return KVQ_EINVAL;
+  r = from_cuda(launch_append(g, ptrs_of(cache), reinterpret_cast<const __half *>(k),
+                              reinterpret_cast<const __half *>(v), cache->n_quant,
+                              cache->n_resid, cache->n_sink, cache->ring_head,
+                              static_cast<cudaStream_t>(stream)));
+  if (r != KVQ_OK) return r;
+  if (g.scheme == KVQ_KIVI) {
+    if (cache->n_resid + 1 == g.residual) {
+      cache->n_quant += g.residual;
+      cache->n_resid = 0;
+    } else {
+      cache->n_resid += 1;
+    }
+  } else if (cache->n_sink < g.n_sink) {
+    cache->n_sink += 1;
+  } else if (cache->n_resid < g.residual) {
+    cache->n_resid += 1;
+  } else {
+    cache->n_quant += 1;
+    if (g.residual > 0) cache->ring_head = (cache->ring_head + 1) % g.residual;
+  }
+  note_launch(1);
+  return KVQ_OK;
+}
+
+int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
+                         float *out, float softmax_scale, void *ws, size_t ws_bytes,
+                         void *stream) {
+  Geometry g;
+  int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if (!q || !out || !ws) return KVQ_EINVAL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(ws)) return KVQ_EALIGN;
+  if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
+  if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
+  const DecodePlan plan =
+      plan_decode(g, cache->n_quant, cache->n_resid + cache->n_sink, num_sms_cached());
+  r = from_cuda(launch_decode(g, ptrs_of(cache), plan, cache->n_quant, cache->n_resid,
+                              cache->n_sink, cache->ring_head,
+                              reinterpret_cast<const __half *>(q), out, softmax_scale, ws,
+                              static_cast<cudaStream_t>(stream)));
+  if (r != KVQ_OK) return r;
+  note_launch(1);
+  return KVQ_OK;
+}
+
+int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *h_k,
+                         const uint16_t *h_v, const uint16_t *h_q, float *h_out, uint16_t *d_k,
+                         uint16_t *d_v, uint16_t *d_q, float *d_out, float softmax_scale,
+                         void *ws, size_t ws_bytes, void *stream) {
+  Geometry g;
+  int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  if (!h_k || !h_v || !h_q || !h_out || !d_k || !d_v || !d_q || !d_out) return KVQ_EINVAL;
+  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if (cache->n_quant + cache->n_resid + cache->n_sink + 1 > g.max_ctx) return KVQ_ECAPACITY;
+  if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t kv_bytes = (size_t)g.B * g.H * g.d * 2, q_bytes = (size_t)g.B * g.Hq * g.d * 2;
+  const size_t o_bytes = (size_t)g.B * g.Hq * g.d * 4;
+  if (cudaMemcpyAsync(d_k, h_k, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d_v, h_v, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(d_q, h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return KVQ_ECUDA;
+  if ((r = kvq_append(cfg, cache, d_k, d_v, stream)) != KVQ_OK) return r;
+  if ((r = kvq_decode_attention(cfg, cache, d_q, d_out, softmax_scale, ws, ws_bytes, stream)) !=
+      KVQ_OK)
+    return r;
+  if (cudaMemcpyAsync(h_out, d_out, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return KVQ_ECUDA;
+  note_launch(2);
+  return KVQ_OK;
+}
+
+int kvq_get_device_status(kvq_cache *cache, void *stream) {
+  if (!cache || !cache->dev_status) return KVQ_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KVQ_ECUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, cache->dev_status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KVQ_ECUDA;
+  if (v != 0) {
+    const int32_t zero = 0;
+    if (cudaMemcpy(cache->dev_status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return KVQ_ECUDA;
+  }
+  return v == 0 ? KVQ_OK : (int)v;
+}
+
+int kvq_last_launch_count(void) { return t_last_launches; }
+
+const char *kvq_strerror(int code) {
+  switch (code) {
+    case KVQ_OK: return "ok";
+    case KVQ_EINVAL: return "invalid argument";
+    case KVQ_EUNSUPPORTED: return "unsupported configuration";
+    case KVQ_ECAPACITY: return "capacity exceeded (max_ctx or workspace)";
+    case KVQ_EALIGN: return "device buffer not 16-byte aligned";
+    case KVQ_ECUDA: return "CUDA error";
+    case KVQ_ETIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown error";
+}
+
+}  // extern "C"

@@ -1,0 +1,98 @@
+// Internal declarations shared by the libkvq translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kMaxHeadDim = 128;
+constexpr int kMaxResidual = 1024;
+
+// Geometry of one cache, resolved on the host from kvq_config and copied by
+// value into every kernel.
+struct Geometry {
+  int B, H, Hq, d, bits, scheme, k_group, v_group, residual, n_sink;
+  int64_t max_ctx;
+  int row_bytes;      // packed bytes per token row: d * bits / 8
+  int k_meta_cols;    // KIVI: d; InnerQ: d / k_group
+  int v_meta_cols;    // d / v_group
+  int64_t k_meta_rows;  // per head: KIVI ceil(max_ctx / G); InnerQ max_ctx
+  int64_t mode_words;   // per head, InnerQ only
+};
+
+// Device pointers of a cache (same meaning as kvq_cache).
+struct CachePtrs {
+  uint8_t *k_codes, *v_codes;
+  float *k_scale, *k_zero, *v_scale, *v_zero;
+  uint32_t *k_mode, *v_mode;
+  __half *k_res, *v_res, *k_sink, *v_sink;
+  int32_t *status;
+};
+
+int resolve(const kvq_config *cfg, Geometry *g);
+CachePtrs ptrs_of(const kvq_cache *c);
+void note_launch(int n);
+
+// ---- launchers (return cudaError_t of the launch) ------------------------
+cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *K,
+                           const __half *V, int64_t T, int64_t n_quant, int64_t n_resid,
+                           int64_t n_sink, cudaStream_t st, int *launches);
+cudaError_t launch_append(const Geometry &g, const CachePtrs &p, const __half *k,
+                          const __half *v, int64_t n_quant, int64_t n_resid,
+                          int64_t n_sink, int64_t ring_head, cudaStream_t st);
+
+struct DecodePlan {
+  int n_qsplit;        // splits over the quantized region
+  int n_split;         // n_qsplit + (fp16 segment present ? 1 : 0)
+  int64_t chunk;       // quantized tokens per split
+};
+size_t decode_workspace_bytes(const Geometry &g);
+DecodePlan plan_decode(const Geometry &g, int64_t n_quant, int64_t n_fp16, int num_sms);
+cudaError_t launch_decode(const Geometry &g, const CachePtrs &p, const DecodePlan &plan,
+                          int64_t n_quant, int64_t n_resid, int64_t n_sink,
+                          int64_t ring_head, const __half *q, float *out, float scale,
+                          void *ws, cudaStream_t st);
+
+// ---- quantization arithmetic (bit-exact contract with the formula) -------
+// Asymmetric: scale = (max - min) / (2^b - 1), zero = min,
+// code = clamp(rint((x - min) / scale), 0, 2^b - 1); constant group: 0, 0.
+__device__ __forceinline__ float canon_zero(float x) { return __fadd_rn(x, 0.0f); }
+
+__device__ __forceinline__ float asym_scale(float mn, float mx, int bits) {
+  return mx == mn ? 0.0f : __fdiv_rn(__fsub_rn(mx, mn), (float)((1 << bits) - 1));
+}
+
+__device__ __forceinline__ uint32_t asym_code(float x, float mn, float scale, int bits) {
+  if (scale == 0.0f) return 0u;
+  float r = rintf(__fdiv_rn(__fsub_rn(x, mn), scale));
+  const float top = (float)((1 << bits) - 1);
+  r = fminf(fmaxf(r, 0.0f), top);
+  return (uint32_t)r;
+}
+
+// Symmetric: scale = max(|min|, |max|) / (2^(b-1) - 1),
+// code = clamp(rint(x / scale), -lim, lim) + 2^(b-1), zero = -2^(b-1) * scale.
+__device__ __forceinline__ float sym_scale(float mn, float mx, int bits) {
+  return __fdiv_rn(fmaxf(fabsf(mn), fabsf(mx)), (float)((1 << (bits - 1)) - 1));
+}
+
+__device__ __forceinline__ uint32_t sym_code(float x, float scale, int bits) {
+  const int half = 1 << (bits - 1);
+  const float lim = (float)(half - 1);
+  float r = rintf(__fdiv_rn(x, scale));
+  r = fminf(fmaxf(r, -lim), lim);
+  return (uint32_t)((int)r + half);
+}
+
+// InnerQ mode rule: symmetric iff not constant and |max + min| <= (max - min)/(2^b - 1).
+__device__ __forceinline__ bool choose_symmetric(float mn, float mx, int bits) {
+  if (mx == mn) return false;
+  const float step = __fdiv_rn(__fsub_rn(mx, mn), (float)((1 << bits) - 1));
+  return fabsf(__fadd_rn(mx, mn)) <= step;
+}
+
+}  // namespace kvq

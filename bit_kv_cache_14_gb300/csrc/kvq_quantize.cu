@@ -1,0 +1,431 @@
+// Prefill quantize+pack and append/flush kernels.
+//
+// Method: keys per channel over G-token groups, values per token over channel
+// groups ("大模型量化技术原理：KIVI、IntactKV、KVQuant", KIVI / 工作原理); residual
+// flushed in one batch when it holds R tokens (pgsm.cn how-to §3.1); InnerQ
+// per-token groups along the head dimension with a per-group symmetric /
+// asymmetric choice, fp16 sinks and recent window (InnerQ page, 方法论 1-4).
+//
+// Work mapping: one thread owns 8 consecutive channels of one token (one
+// 16-byte fp16 load, 2 or 4 packed output bytes), so a warp reads whole
+// 256-byte token rows and writes whole packed rows.  Per-token group min/max
+// is a butterfly over the lanes of the group; per-channel key statistics are
+// one thread per channel walking the G tokens of the group.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kQuantBlock = 256;
+
+__device__ __forceinline__ void load8(const __half *p, float (&x)[8]) {
+  const uint4 raw = *reinterpret_cast<const uint4 *>(p);
+  const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(h[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+// Store the packed codes of one 8-channel chunk: 2 bytes (2-bit) or 4 (4-bit).
+__device__ __forceinline__ void store_chunk(uint8_t *row, int chunk, uint32_t w, int bits) {
+  if (bits == 2)
+    reinterpret_cast<uint16_t *>(row)[chunk] = (uint16_t)w;
+  else
+    reinterpret_cast<uint32_t *>(row)[chunk] = w;
+}
+
+__device__ __forceinline__ uint8_t *code_row(uint8_t *base, const Geometry &g, int64_t bh,
+                                             int64_t slot) {
+  return base + (bh * g.max_ctx + slot) * (int64_t)g.row_bytes;
+}
+
+// One key group (G tokens of src, row stride d) quantized per channel into
+// token slots [t0, t0 + G), t0 a multiple of G.  All threads of the block call
+// it; s_scale / s_mn are d-float shared arrays.
+__device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int64_t bh,
+                                      const __half *src, int64_t t0, float *s_scale,
+                                      float *s_mn) {
+  const int d = g.d, G = g.k_group;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float mn = __half2float(src[c]), mx = mn;
+    for (int i = 1; i < G; ++i) {
+      const float x = __half2float(src[(int64_t)i * d + c]);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    mn = canon_zero(mn);
+    mx = canon_zero(mx);
+    const float sc = asym_scale(mn, mx, g.bits);
+    s_scale[c] = sc;
+    s_mn[c] = mn;
+    const int64_t mi = (bh * g.k_meta_rows + t0 / G) * d + c;
+    p.k_scale[mi] = sc;
+    p.k_zero[mi] = mn;
+  }
+  __syncthreads();
+  const int chunks = d / 8;
+  for (int it = threadIdx.x; it < G * chunks; it += blockDim.x) {
+    const int i = it / chunks, j = it - i * chunks;
+    float x[8];
+    load8(src + (int64_t)i * d + 8 * j, x);
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = 8 * j + k;
+      w |= asym_code(x[k], s_mn[c], s_scale[c], g.bits) << (k * g.bits);
+    }
+    store_chunk(code_row(p.k_codes, g, bh, t0 + i), j, w, g.bits);
+  }
+  __syncthreads();
+}
+
+// Result of quantizing one 8-channel chunk inside a per-token group.
+struct ChunkQ {
+  uint32_t codes;
+  float scale, zero;
+  bool sym;
+};
+
+// Per-token group quantization of the 8 values x of this lane; the group is
+// `lanes` consecutive, aligned lanes (lanes = group / 8, a power of two <= 16;
+// it may differ between lanes of a warp).  Every lane of the warp must call it:
+// the butterfly always runs its four full-mask rounds and each lane only
+// combines the rounds inside its own group.
+__device__ __forceinline__ ChunkQ quant_chunk(const float (&x)[8], int lanes, int bits,
+                                              bool allow_sym) {
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k) {
+    mn = fminf(mn, x[k]);
+    mx = fmaxf(mx, x[k]);
+  }
+#pragma unroll
+  for (int off = 1; off < 16; off <<= 1) {
+    const float omn = __shfl_xor_sync(0xffffffffu, mn, off);
+    const float omx = __shfl_xor_sync(0xffffffffu, mx, off);
+    if (off < lanes) {
+      mn = fminf(mn, omn);
+      mx = fmaxf(mx, omx);
+    }
+  }
+  mn = canon_zero(mn);
+  mx = canon_zero(mx);
+  ChunkQ r;
+  r.sym = allow_sym && choose_symmetric(mn, mx, bits);
+  r.codes = 0;
+  if (r.sym) {
+    r.scale = sym_scale(mn, mx, bits);
+    r.zero = __fmul_rn(-(float)(1 << (bits - 1)), r.scale);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r.codes |= sym_code(x[k], r.scale, bits) << (k * bits);
+  } else {
+    r.scale = asym_scale(mn, mx, bits);
+    r.zero = mn;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r.codes |= asym_code(x[k], mn, r.scale, bits) << (k * bits);
+  }
+  return r;
+}
+
+// Where one per-token quantization writes: codes, meta, optional mode bits.
+struct TokenDst {
+  uint8_t *codes;
+  float *scale, *zero;
+  uint32_t *mode;  // nullptr for KIVI values
+  int group;       // channels per group
+  int meta_cols;   // d / group
+};
+
+__device__ __forceinline__ TokenDst key_dst(const Geometry &g, const CachePtrs &p) {
+  return TokenDst{p.k_codes, p.k_scale, p.k_zero, p.k_mode, g.k_group, g.d / g.k_group};
+}
+__device__ __forceinline__ TokenDst value_dst(const Geometry &g, const CachePtrs &p) {
+  return TokenDst{p.v_codes, p.v_scale, p.v_zero, g.scheme == KVQ_INNERQ ? p.v_mode : nullptr,
+                  g.v_group, g.d / g.v_group};
+}
+
+// Prefill, per-token groups: tokens [src0, src0 + n_tok) of every head of
+// X [B*H][T][d] quantized into slots [0, n_tok).  blockIdx.y = head,
+// blockIdx.z = 0 keys / 1 values (keys only under InnerQ).
+__global__ void __launch_bounds__(kQuantBlock)
+    per_token_prefill_kernel(Geometry g, CachePtrs p, const __half *K, const __half *V,
+                             int64_t T, int64_t src0, int64_t n_tok) {
+  const bool is_key = blockIdx.z == 0 && g.scheme == KVQ_INNERQ;
+  const TokenDst dst = is_key ? key_dst(g, p) : value_dst(g, p);
+  const __half *X = is_key ? K : V;
+  const int64_t bh = blockIdx.y;
+  const int chunks = g.d / 8;
+  const int tpb = kQuantBlock / chunks;  // tokens per block
+  const int64_t tok0 = (int64_t)blockIdx.x * tpb;
+  const int lt = threadIdx.x / chunks, j = threadIdx.x - lt * chunks;
+  const int64_t t = tok0 + lt;
+  const bool valid = t < n_tok;
+  const int lanes = dst.group / 8;
+
+  // Mode bits of this block's tokens, assembled in shared memory.
+  __shared__ uint32_t s_bits[kQuantBlock / 8 + 2];
+  const int ng = dst.meta_cols;
+  const int64_t bit0 = tok0 * ng;
+  const int64_t wbase = bit0 >> 5;
+  if (dst.mode) {
+    for (int i = threadIdx.x; i < kQuantBlock / 8 + 2; i += blockDim.x) s_bits[i] = 0;
+    __syncthreads();
+  }
+
+  float x[8];
+  if (valid) {
+    load8(X + (bh * T + src0 + t) * g.d + 8 * j, x);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = 0.0f;
+  }
+  const ChunkQ q = quant_chunk(x, lanes, g.bits, dst.mode != nullptr);
+  if (valid) {
+    store_chunk(code_row(dst.codes, g, bh, t), j, q.codes, g.bits);
+    if ((j & (lanes - 1)) == 0) {
+      const int gi = j / lanes;
+      const int64_t mi = (bh * g.max_ctx + t) * ng + gi;
+      dst.scale[mi] = q.scale;
+      dst.zero[mi] = q.zero;
+      if (dst.mode && q.sym) {
+        const int64_t bit = t * ng + gi;
+        atomicOr(&s_bits[(bit >> 5) - wbase], 1u << (bit & 31));
+      }
+    }
+  }
+  if (!dst.mode) return;
+  __syncthreads();
+  // Write back the words this block owns.  Blocks own disjoint bit ranges;
+  // the block holding the last token also owns the rest of its last word.
+  const int64_t tok_end = min(tok0 + tpb, n_tok);
+  if (tok_end <= tok0) return;
+  int64_t bit1 = tok_end * ng;
+  if (tok_end == n_tok) bit1 = (bit1 + 31) & ~(int64_t)31;
+  const int64_t wlast = (bit1 - 1) >> 5;
+  uint32_t *words = dst.mode + bh * g.mode_words;
+  for (int64_t w = wbase + threadIdx.x; w <= wlast; w += blockDim.x) {
+    const int64_t lo = max(bit0, w * 32) - w * 32, hi = min(bit1, w * 32 + 32) - w * 32;
+    const uint32_t mask = (hi - lo == 32) ? 0xffffffffu : (((1u << (hi - lo)) - 1u) << lo);
+    const uint32_t bits = s_bits[w - wbase] & mask;
+    if (mask == 0xffffffffu) {
+      words[w] = bits;
+    } else {
+      atomicAnd(&words[w], ~mask);
+      atomicOr(&words[w], bits);
+    }
+  }
+}
+
+// Prefill, KIVI keys: one block per (G-token group, head).
+__global__ void __launch_bounds__(kQuantBlock)
+    kivi_key_prefill_kernel(Geometry g, CachePtrs p, const __half *K, int64_t T) {
+  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim];
+  const int64_t bh = blockIdx.y;
+  const int64_t t0 = (int64_t)blockIdx.x * g.k_group;
+  key_group_per_channel(g, p, bh, K + (bh * T + t0) * g.d, t0, s_scale, s_mn);
+}
+
+// fp16 row copy: rows [src0, src0 + n) of every head of X [B*H][T][d] into
+// rows [0, n) of dst [B*H][dst_rows][d].  blockIdx.z: 0 keys, 1 values.
+__global__ void copy_rows_kernel(const __half *K, const __half *V, int64_t T, int64_t src0,
+                                 int64_t n, __half *dk, __half *dv, int64_t dst_rows, int d,
+                                 int64_t n_heads) {
+  const __half *X = blockIdx.z == 0 ? K : V;
+  __half *D = blockIdx.z == 0 ? dk : dv;
+  const int vec = d / 8;
+  const int64_t total = n_heads * n * vec;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t bh = i / (n * vec);
+    const int64_t r = (i / vec) % n;
+    const int j = (int)(i % vec);
+    const uint4 v = *reinterpret_cast<const uint4 *>(X + (bh * T + src0 + r) * d + 8 * j);
+    *reinterpret_cast<uint4 *>(D + (bh * dst_rows + r) * d + 8 * j) = v;
+  }
+}
+
+// KIVI append: token into residual slot `slot`; on `flush` the whole residual
+// (R tokens) is quantized into slots [n_quant, n_quant + R).  One block per head.
+__global__ void __launch_bounds__(kQuantBlock)
+    kivi_append_kernel(Geometry g, CachePtrs p, const __half *k, const __half *v,
+                       int64_t slot, int flush, int64_t n_quant) {
+  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim];
+  const int64_t bh = blockIdx.x;
+  const int d = g.d, R = g.residual;
+  __half *kr = p.k_res + bh * R * d, *vr = p.v_res + bh * R * d;
+  for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
+    reinterpret_cast<uint4 *>(kr + slot * d)[c] = reinterpret_cast<const uint4 *>(k + bh * d)[c];
+    reinterpret_cast<uint4 *>(vr + slot * d)[c] = reinterpret_cast<const uint4 *>(v + bh * d)[c];
+  }
+  if (!flush) return;
+  __syncthreads();
+  for (int grp = 0; grp < R / g.k_group; ++grp)
+    key_group_per_channel(g, p, bh, kr + (int64_t)grp * g.k_group * d,
+                          n_quant + (int64_t)grp * g.k_group, s_scale, s_mn);
+  const TokenDst dst = value_dst(g, p);
+  const int chunks = d / 8, lanes = g.v_group / 8, ng = dst.meta_cols;
+  const int items = R * chunks;
+  const int rounds = (items + blockDim.x - 1) / blockDim.x;
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int it = rd * blockDim.x + threadIdx.x;
+    const bool valid = it < items;
+    const int t = valid ? it / chunks : 0, j = valid ? it - t * chunks : 0;
+    float x[8];
+    load8(vr + (int64_t)t * d + 8 * j, x);
+    const ChunkQ q = quant_chunk(x, lanes, g.bits, false);
+    if (valid) {
+      store_chunk(code_row(dst.codes, g, bh, n_quant + t), j, q.codes, g.bits);
+      if ((j & (lanes - 1)) == 0) {
+        const int64_t mi = (bh * g.max_ctx + n_quant + t) * ng + j / lanes;
+        dst.scale[mi] = q.scale;
+        dst.zero[mi] = q.zero;
+      }
+    }
+  }
+}
+
+// InnerQ append.  action 0: token into sink slot; 1: into window slot;
+// 2: quantize the token in window slot `slot` (the oldest; or the new token
+// itself when there is no window) into quantized slot n_quant, then put the
+// new token in that window slot.  One warp per head.
+__global__ void __launch_bounds__(32)
+    innerq_append_kernel(Geometry g, CachePtrs p, const __half *k, const __half *v, int action,
+                         int64_t slot, int64_t n_quant) {
+  const int64_t bh = blockIdx.x;
+  const int d = g.d, W = g.residual, S = g.n_sink;
+  const uint4 *kn = reinterpret_cast<const uint4 *>(k + bh * d);
+  const uint4 *vn = reinterpret_cast<const uint4 *>(v + bh * d);
+  const int lane = threadIdx.x;
+  if (action == 0 || action == 1) {
+    __half *dk = action == 0 ? p.k_sink + (bh * S + slot) * d : p.k_res + (bh * W + slot) * d;
+    __half *dv = action == 0 ? p.v_sink + (bh * S + slot) * d : p.v_res + (bh * W + slot) * d;
+    for (int c = lane; c < d / 8; c += 32) {
+      reinterpret_cast<uint4 *>(dk)[c] = kn[c];
+      reinterpret_cast<uint4 *>(dv)[c] = vn[c];
+    }
+    return;
+  }
+  const __half *srck = W > 0 ? p.k_res + (bh * W + slot) * d : k + bh * d;
+  const __half *srcv = W > 0 ? p.v_res + (bh * W + slot) * d : v + bh * d;
+  const int chunks = d / 8;
+  for (int it0 = 0; it0 < 2 * chunks; it0 += 32) {
+    const int it = it0 + lane;
+    const bool valid = it < 2 * chunks;
+    const bool is_key = it < chunks;
+    const int j = is_key ? it : it - chunks;
+    const TokenDst dst = is_key ? key_dst(g, p) : value_dst(g, p);
+    float x[8];
+    if (valid) {
+      load8((is_key ? srck : srcv) + 8 * j, x);
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) x[kk] = 0.0f;
+    }
+    // Keys and values may use different group sizes: lanes of one group are
+    // consecutive and never straddle the key/value boundary (chunks is a
+    // multiple of both group widths).
+    const int lanes = (valid ? dst.group : 8) / 8;
+    const ChunkQ q = quant_chunk(x, lanes, g.bits, true);
+    if (valid) {
+      store_chunk(code_row(dst.codes, g, bh, n_quant), j, q.codes, g.bits);
+      if ((j & (lanes - 1)) == 0) {
+        const int ng = dst.meta_cols, gi = j / lanes;
+        const int64_t mi = (bh * g.max_ctx + n_quant) * ng + gi;
+        dst.scale[mi] = q.scale;
+        dst.zero[mi] = q.zero;
+        const int64_t bit = n_quant * ng + gi;
+        uint32_t *word = dst.mode + bh * g.mode_words + (bit >> 5);
+        if (q.sym)
+          atomicOr(word, 1u << (bit & 31));
+        else
+          atomicAnd(word, ~(1u << (bit & 31)));
+      }
+    }
+  }
+  if (W == 0) return;
+  __syncwarp();
+  __half *dk = p.k_res + (bh * W + slot) * d, *dv = p.v_res + (bh * W + slot) * d;
+  for (int c = lane; c < d / 8; c += 32) {
+    reinterpret_cast<uint4 *>(dk)[c] = kn[c];
+    reinterpret_cast<uint4 *>(dv)[c] = vn[c];
+  }
+}
+
+int copy_blocks(int64_t total_vec) {
+  int64_t b = (total_vec + 255) / 256;
+  return (int)(b < 1 ? 1 : (b > 65535 ? 65535 : b));
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *K,
+                           const __half *V, int64_t T, int64_t n_quant, int64_t n_resid,
+                           int64_t n_sink, cudaStream_t st, int *launches) {
+  const int64_t BH = (int64_t)g.B * g.H;
+  const int chunks = g.d / 8;
+  const int tpb = kQuantBlock / chunks;
+  int n = 0;
+  if (g.scheme == KVQ_KIVI) {
+    if (n_quant > 0) {
+      kivi_key_prefill_kernel<<<dim3((unsigned)(n_quant / g.k_group), (unsigned)BH), kQuantBlock, 0,
+                                st>>>(g, p, K, T);
+      per_token_prefill_kernel<<<dim3((unsigned)((n_quant + tpb - 1) / tpb), (unsigned)BH, 1),
+                                 kQuantBlock, 0, st>>>(g, p, K, V, T, 0, n_quant);
+      n += 2;
+    }
+    if (n_resid > 0) {
+      copy_rows_kernel<<<dim3(copy_blocks(BH * n_resid * chunks), 1, 2), 256, 0, st>>>(
+          K, V, T, n_quant, n_resid, p.k_res, p.v_res, g.residual, g.d, BH);
+      ++n;
+    }
+  } else {
+    if (n_sink > 0) {
+      copy_rows_kernel<<<dim3(copy_blocks(BH * n_sink * chunks), 1, 2), 256, 0, st>>>(
+          K, V, T, 0, n_sink, p.k_sink, p.v_sink, g.n_sink, g.d, BH);
+      ++n;
+    }
+    if (n_quant > 0) {
+      per_token_prefill_kernel<<<dim3((unsigned)((n_quant + tpb - 1) / tpb), (unsigned)BH, 2),
+                                 kQuantBlock, 0, st>>>(g, p, K, V, T, n_sink, n_quant);
+      ++n;
+    }
+    if (n_resid > 0) {
+      copy_rows_kernel<<<dim3(copy_blocks(BH * n_resid * chunks), 1, 2), 256, 0, st>>>(
+          K, V, T, T - n_resid, n_resid, p.k_res, p.v_res, g.residual, g.d, BH);
+      ++n;
+    }
+  }
+  *launches = n;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const Geometry &g, const CachePtrs &p, const __half *k,
+                          const __half *v, int64_t n_quant, int64_t n_resid, int64_t n_sink,
+                          int64_t ring_head, cudaStream_t st) {
+  const unsigned BH = (unsigned)(g.B * g.H);
+  if (g.scheme == KVQ_KIVI) {
+    const int flush = (n_resid + 1 == g.residual) ? 1 : 0;
+    kivi_append_kernel<<<BH, kQuantBlock, 0, st>>>(g, p, k, v, n_resid, flush, n_quant);
+  } else {
+    int action;
+    int64_t slot;
+    if (n_sink < g.n_sink) {
+      action = 0;
+      slot = n_sink;
+    } else if (n_resid < g.residual) {
+      action = 1;
+      slot = n_resid;
+    } else {
+      action = 2;
+      slot = ring_head;
+    }
+    innerq_append_kernel<<<BH, 32, 0, st>>>(g, p, k, v, action, slot, n_quant);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,238 @@
+"""Python binding of libkvq (argument marshalling only).
+
+Every call goes through the C ABI declared in include/kvq.h; all arithmetic
+runs in the library's CUDA kernels.  PyTorch provides device memory and the
+current stream.  There is no fallback: if ``_build/libkvq.so`` is missing the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkvq.so")
+
+KVQ_OK = 0
+KVQ_EINVAL = -1
+KVQ_EUNSUPPORTED = -2
+KVQ_ECAPACITY = -3
+KVQ_EALIGN = -4
+KVQ_ECUDA = -5
+KVQ_ETIMEOUT = -6
+KIVI = 0
+INNERQ = 1
+
+# Every entry point declared in include/kvq.h.
+EXPORTS = (
+    "kvq_cache_sizes", "kvq_workspace_bytes", "kvq_quantize_prefill", "kvq_append",
+    "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
+    "kvq_last_launch_count", "kvq_strerror",
+)
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "n_q_heads", "n_kv_heads", "head_dim", "bits", "scheme", "k_group",
+        "v_group", "residual", "n_sink")] + [("max_ctx", ctypes.c_int64)]
+
+
+class Sizes(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_mode", "v_mode",
+        "k_res", "v_res", "k_sink", "v_sink", "status")]
+
+
+class Cache(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_mode", "v_mode",
+        "k_res", "v_res", "k_sink", "v_sink")] + [
+        (n, ctypes.c_int64) for n in ("n_quant", "n_resid", "n_sink", "ring_head")] + [
+        ("dev_status", ctypes.c_void_p)]
+
+
+class KVQError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s: %s (%d)" % (what, strerror(code), code))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libkvq is not built (%s missing); run "
+                                   "python -m bit_kv_cache_14_gb300.build_lib" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            P, I64, C = ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(Config)
+            CA = ctypes.POINTER(Cache)
+            L.kvq_cache_sizes.argtypes = [C, ctypes.POINTER(Sizes)]
+            L.kvq_workspace_bytes.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
+            L.kvq_quantize_prefill.argtypes = [C, CA, P, P, I64, P]
+            L.kvq_append.argtypes = [C, CA, P, P, P]
+            L.kvq_decode_attention.argtypes = [C, CA, P, P, ctypes.c_float, P, ctypes.c_size_t, P]
+            L.kvq_decode_step_host.argtypes = [C, CA, P, P, P, P, P, P, P, P, ctypes.c_float, P,
+                                               ctypes.c_size_t, P]
+            L.kvq_get_device_status.argtypes = [CA, P]
+            L.kvq_last_launch_count.argtypes = []
+            L.kvq_strerror.argtypes = [ctypes.c_int]
+            L.kvq_strerror.restype = ctypes.c_char_p
+            for name in EXPORTS:
+                if name != "kvq_strerror":
+                    getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().kvq_strerror(int(code)).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != KVQ_OK:
+        raise KVQError(code, what)
+
+
+def make_config(batch, n_q_heads, n_kv_heads, head_dim, bits, scheme, k_group, v_group,
+                residual, n_sink, max_ctx) -> Config:
+    return Config(batch, n_q_heads, n_kv_heads, head_dim, bits, scheme, k_group, v_group,
+                  residual, n_sink, max_ctx)
+
+
+def config_of(w, max_ctx: int | None = None) -> Config:
+    """Config of a synth.Workload (max_ctx defaults to prompt + streamed tokens)."""
+    return make_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.bits, w.scheme,
+                       w.k_group, w.v_group, w.residual, w.n_sink,
+                       w.max_ctx() if max_ctx is None else max_ctx)
+
+
+def cache_sizes(cfg: Config) -> Sizes:
+    s = Sizes()
+    _check(lib().kvq_cache_sizes(ctypes.byref(cfg), ctypes.byref(s)), "kvq_cache_sizes")
+    return s
+
+
+def workspace_bytes(cfg: Config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().kvq_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "kvq_workspace_bytes")
+    return n.value
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptr(t: torch.Tensor) -> int:
+    assert t.is_contiguous()
+    return t.data_ptr()
+
+
+class QuantizedKVCache:
+    """Device buffers (torch-allocated) of one quantized cache plus its C view."""
+
+    _BUFS = ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_mode",
+             "v_mode", "k_res", "v_res", "k_sink", "v_sink")
+
+    def __init__(self, cfg: Config, device="cuda"):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        sizes = cache_sizes(cfg)
+        self.bufs = {}
+        view = Cache()
+        for name in self._BUFS:
+            n = getattr(sizes, name)
+            t = torch.zeros(max(n, 16), dtype=torch.uint8, device=self.device)
+            self.bufs[name] = t
+            setattr(view, name, t.data_ptr() if n else None)
+        self.status = torch.zeros(4, dtype=torch.int32, device=self.device)
+        view.dev_status = self.status.data_ptr()
+        self.view = view
+        self.ws_bytes = workspace_bytes(cfg)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
+        self.sizes = sizes
+
+    # counters
+    n_quant = property(lambda self: self.view.n_quant)
+    n_resid = property(lambda self: self.view.n_resid)
+    n_sink = property(lambda self: self.view.n_sink)
+    ring_head = property(lambda self: self.view.ring_head)
+
+    def prefill(self, K: torch.Tensor, V: torch.Tensor, stream=None) -> None:
+        """K, V: fp16 [B][H][T][d] on the device."""
+        assert K.dtype == torch.float16 and V.dtype == torch.float16 and K.shape == V.shape
+        _check(lib().kvq_quantize_prefill(ctypes.byref(self.cfg), ctypes.byref(self.view),
+                                          _ptr(K), _ptr(V), K.shape[2], _stream(stream)),
+               "kvq_quantize_prefill")
+
+    def append(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        """k, v: fp16 [B][H][d] on the device."""
+        assert k.dtype == torch.float16 and v.dtype == torch.float16
+        _check(lib().kvq_append(ctypes.byref(self.cfg), ctypes.byref(self.view), _ptr(k),
+                                _ptr(v), _stream(stream)), "kvq_append")
+
+    def decode(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
+               stream=None) -> torch.Tensor:
+        """q: fp16 [B][Hq][d]; returns fp32 [B][Hq][d]."""
+        assert q.dtype == torch.float16
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.cfg.head_dim)
+        _check(lib().kvq_decode_attention(ctypes.byref(self.cfg), ctypes.byref(self.view),
+                                          _ptr(q), _ptr(out), float(scale), self.ws.data_ptr(),
+                                          self.ws_bytes, _stream(stream)),
+               "kvq_decode_attention")
+        return out
+
+    def decode_step_host(self, h_k, h_v, h_q, h_out, d_k, d_v, d_q, d_out, scale=None,
+                         stream=None) -> None:
+        """One append + decode from pinned host tensors through device staging tensors."""
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.cfg.head_dim)
+        _check(lib().kvq_decode_step_host(
+            ctypes.byref(self.cfg), ctypes.byref(self.view), _ptr(h_k), _ptr(h_v), _ptr(h_q),
+            _ptr(h_out), _ptr(d_k), _ptr(d_v), _ptr(d_q), _ptr(d_out), float(scale),
+            self.ws.data_ptr(), self.ws_bytes, _stream(stream)), "kvq_decode_step_host")
+
+    def device_status(self, stream=None) -> int:
+        return lib().kvq_get_device_status(ctypes.byref(self.view), _stream(stream))
+
+    # ---- typed views of the buffers (for tests and inspection) ------------
+    def _geom(self):
+        c = self.cfg
+        return c.batch, c.n_kv_heads, c.max_ctx, c.head_dim
+
+    def codes(self, which: str) -> torch.Tensor:
+        B, H, T, d = self._geom()
+        rb = d * self.cfg.bits // 8
+        return self.bufs[which + "_codes"][: B * H * T * rb].view(B, H, T, rb)
+
+    def meta(self, name: str) -> torch.Tensor:
+        B, H, T, d = self._geom()
+        n = getattr(self.sizes, name) // 4
+        return self.bufs[name][: n * 4].view(torch.float32).view(B, H, -1)
+
+    def modes(self, which: str) -> torch.Tensor:
+        B, H, _, _ = self._geom()
+        n = getattr(self.sizes, which + "_mode") // 4
+        return self.bufs[which + "_mode"][: n * 4].view(torch.int32).view(B, H, -1)
+
+    def fp16_rows(self, name: str, rows: int) -> torch.Tensor:
+        B, H, _, d = self._geom()
+        n = getattr(self.sizes, name) // 2
+        return self.bufs[name][: n * 2].view(torch.float16).view(B, H, rows, d)
+
+    def last_launch_count(self) -> int:
+        return lib().kvq_last_launch_count()

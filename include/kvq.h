@@ -1,0 +1,208 @@
+/*
+ * libkvq -- quantized KV cache with fused decode attention, for GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only; no CUDA or framework types in the
+ * signatures (a stream is passed as `void *`, meaning a cudaStream_t; NULL is
+ * the legacy default stream).  Every device buffer is allocated and owned by
+ * the caller; the library never allocates device or host memory.  Calls are
+ * asynchronous on the given stream unless stated otherwise.
+ *
+ * Method (page title, section):
+ *   [KIVI]   "大模型量化技术原理：KIVI、IntactKV、KVQuant" (juejin.cn), KIVI /
+ *            背景 and 工作原理: keys quantized per channel in groups of G
+ *            tokens, values per token; the newest tokens stay fp16 in a
+ *            residual that is quantized and appended every R tokens.
+ *   [HF]     pgsm.cn KV-cache quantization how-to, §2.1 (asymmetric form
+ *            X_Q = round(X/S) - Z) and §3.1 (fp16 residual buffer, quantized
+ *            as a batch when full).
+ *   [INNERQ] "【论文】InnerQ：硬件感知免调优KV缓存量化用于大语言模型"
+ *            (euno.news), 方法论 1-5: groups along the inner (head) dimension,
+ *            per-group symmetric/asymmetric choice, fp16 sink and recent
+ *            windows, dequantization fused into the GEMV.
+ *   [KVQ5]   the juejin page, KVQuant / 技术原理 五: first token kept fp16.
+ *   [IKV]    the juejin page, IntactKV / KV Cache量化: fp16 tokens joined
+ *            with the dequantized cache at attention time.
+ *
+ * Quantization formula (asymmetric, fp32, IEEE round-to-nearest-even):
+ *   scale = (max - min) / (2^b - 1), zero = min,
+ *   code  = clamp(rint((x - min) / scale), 0, 2^b - 1); x_hat = code*scale + zero.
+ *   A constant group stores scale 0 and code 0.
+ * Symmetric (InnerQ groups whose midpoint |max + min| <= (max - min)/(2^b - 1)):
+ *   scale = max(|min|, |max|) / (2^(b-1) - 1), q = clamp(rint(x / scale)),
+ *   code = q + 2^(b-1), zero = -2^(b-1) * scale (same dequantization formula).
+ *
+ * Packed layout (all buffers token-major per (batch, kv head)):
+ *   codes   u8 [B][H][max_ctx][d*bits/8]; channel c of a token at bits
+ *           (c mod (8/bits))*bits of byte c/(8/bits).
+ *   KIVI:   k_scale, k_zero f32 [B][H][ceil(max_ctx/G)][d]   (per G-token group, channel)
+ *           v_scale, v_zero f32 [B][H][max_ctx][d/v_group]   (per token, channel group)
+ *           k_res, v_res   fp16 [B][H][R][d]                 (residual, oldest first)
+ *   InnerQ: k_scale, k_zero f32 [B][H][max_ctx][d/k_group]   (per token, channel group)
+ *           v_scale, v_zero f32 [B][H][max_ctx][d/v_group]
+ *           k_mode, v_mode  u32 [B][H][ceil(max_ctx*(d/group)/32)]  bit i = group
+ *                           i % (d/group) of token i / (d/group); 1 = symmetric
+ *           k_res, v_res   fp16 [B][H][W][d]   recent window, a ring (see ring_head)
+ *           k_sink, v_sink fp16 [B][H][S][d]   first S tokens
+ *   Quantized tokens occupy slots [0, n_quant) in arrival order.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  Validation happens before any launch; on a negative return
+ * no cache state (host counters or device buffers) has changed. */
+#define KVQ_OK 0
+#define KVQ_EINVAL (-1)       /* null pointer, negative size, inconsistent config */
+#define KVQ_EUNSUPPORTED (-2) /* valid but not built: head_dim, bits, group sizes */
+#define KVQ_ECAPACITY (-3)    /* the call would exceed max_ctx or the workspace */
+#define KVQ_EALIGN (-4)       /* a device buffer is not 16-byte aligned */
+#define KVQ_ECUDA (-5)        /* a CUDA launch or copy failed */
+#define KVQ_ETIMEOUT (-6)     /* a bounded device-side wait gave up (status word) */
+
+#define KVQ_KIVI 0
+#define KVQ_INNERQ 1
+
+/*
+ * Cache configuration.
+ *   batch, n_q_heads, n_kv_heads: n_q_heads % n_kv_heads == 0; query head hq
+ *     reads KV head hq / (n_q_heads / n_kv_heads) (GQA; MHA when equal).
+ *   head_dim d: 64 or 128.   bits: 2 or 4.
+ *   scheme KVQ_KIVI: k_group = G tokens per key group (16, 32, 64 or 128),
+ *     v_group = channels per value group (multiple of 16 dividing d),
+ *     residual = R (multiple of G, <= 1024), n_sink must be 0.
+ *   scheme KVQ_INNERQ: k_group and v_group = channels per group (multiples of
+ *     16 dividing d), residual = W recent fp16 tokens (0..1024), n_sink = S
+ *     fp16 sink tokens (0..1024).
+ *   max_ctx: most tokens one sequence will hold (prompt + appended).
+ */
+typedef struct kvq_config {
+  int32_t batch;
+  int32_t n_q_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t bits;
+  int32_t scheme;
+  int32_t k_group;
+  int32_t v_group;
+  int32_t residual;
+  int32_t n_sink;
+  int64_t max_ctx;
+} kvq_config;
+
+/* Byte sizes of the cache buffers for a configuration (0 = unused). */
+typedef struct kvq_sizes {
+  size_t k_codes, v_codes;
+  size_t k_scale, k_zero, v_scale, v_zero;
+  size_t k_mode, v_mode;
+  size_t k_res, v_res;
+  size_t k_sink, v_sink;
+  size_t status; /* one int32 status word */
+} kvq_sizes;
+
+/*
+ * Cache view.  The caller allocates every buffer (sizes from kvq_cache_sizes,
+ * 16-byte aligned), zero-fills `dev_status` once, and keeps this struct; the
+ * library updates the host counters below.  Lengths are uniform across the
+ * batch.  Copying the struct together with the buffers checkpoints the cache.
+ *   n_quant   tokens in the quantized region (slots [0, n_quant))
+ *   n_resid   KIVI: fp16 residual tokens (< R); InnerQ: window tokens (<= W)
+ *   n_sink    InnerQ: sink tokens held (<= S)
+ *   ring_head InnerQ: window slot of the oldest token once the window is full
+ */
+typedef struct kvq_cache {
+  void *k_codes, *v_codes;
+  float *k_scale, *k_zero, *v_scale, *v_zero;
+  uint32_t *k_mode, *v_mode;
+  uint16_t *k_res, *v_res, *k_sink, *v_sink;
+  int64_t n_quant, n_resid, n_sink, ring_head;
+  int32_t *dev_status;
+} kvq_cache;
+
+/* Fills *out with the byte size of each cache buffer.  Returns KVQ_OK,
+ * KVQ_EINVAL or KVQ_EUNSUPPORTED.  Host only, no CUDA call. */
+int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out);
+
+/* Bytes of scratch (device) that kvq_decode_attention needs for any cache
+ * state of this configuration.  The scratch must be zero-filled before its
+ * first use; every decode call leaves its counters at zero again.  It must
+ * not be shared by decode calls that can run at the same time. */
+int kvq_workspace_bytes(const kvq_config *cfg, size_t *bytes);
+
+/*
+ * Prefill: quantize a prompt of T tokens into an empty cache.
+ * K, V: device fp16 [B][H][T][d], contiguous.  Resets the cache counters.
+ * KIVI ([KIVI] 工作原理): tokens [0, T - T mod R) are quantized (keys per
+ *   channel in groups of G tokens, values per token in groups of v_group
+ *   channels); the last T mod R tokens go to the fp16 residual.
+ * InnerQ ([INNERQ] 方法论 1-4): the first min(S, T) tokens go to the sink,
+ *   the last min(W, T - S) to the window, the rest are quantized per token in
+ *   groups of k_group / v_group channels with a per-group mode.
+ * Errors: KVQ_EINVAL (null, T < 0), KVQ_ECAPACITY (T > max_ctx), KVQ_EALIGN,
+ *   KVQ_EUNSUPPORTED, KVQ_ECUDA.
+ */
+int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K,
+                         const uint16_t *V, int64_t T, void *stream);
+
+/*
+ * Append one decode token per (batch, kv head).  k, v: device fp16 [B][H][d].
+ * KIVI ([KIVI] 工作原理; [HF] §3.1): the token enters residual slot n_resid;
+ *   when the residual reaches R tokens the same launch quantizes all R of them
+ *   to slots [n_quant, n_quant + R) and empties the residual.
+ * InnerQ: the sink fills first, then the window; once the window holds W
+ *   tokens its oldest token is quantized to slot n_quant and the new token
+ *   takes its ring slot.
+ * Errors: KVQ_EINVAL, KVQ_ECAPACITY (total tokens would exceed max_ctx),
+ *   KVQ_EALIGN, KVQ_ECUDA.
+ */
+int kvq_append(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k,
+               const uint16_t *v, void *stream);
+
+/*
+ * Fused decode attention over the packed cache ([KIVI] 背景: each decode
+ * step reads the whole cache; [INNERQ] 方法论 3: dequantization folded into
+ * the q.K^T and P.V GEMVs; [IKV]: fp16 sink / residual tokens joined with
+ * the quantized ones by an online-softmax merge).
+ *   q:   device fp16 [B][n_q_heads][d]
+ *   out: device fp32 [B][n_q_heads][d] = softmax(softmax_scale * q.K^T) V over
+ *        every token held (sink, quantized, residual / window).  An empty
+ *        cache yields zeros.
+ *   ws:  device scratch of ws_bytes >= kvq_workspace_bytes (see there).
+ * A decode step is kvq_append followed by kvq_decode_attention.
+ * Errors: KVQ_EINVAL, KVQ_ECAPACITY (ws too small), KVQ_EALIGN, KVQ_ECUDA.
+ */
+int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
+                         float *out, float softmax_scale, void *ws, size_t ws_bytes,
+                         void *stream);
+
+/*
+ * One decode step from HOST buffers: copies h_k, h_v ([B][H][d] fp16) and h_q
+ * ([B][n_q_heads][d] fp16) to the device staging buffers d_k, d_v, d_q,
+ * appends, attends, and copies the result to h_out ([B][n_q_heads][d] fp32)
+ * through d_out -- all enqueued on `stream`, no synchronization.  Host
+ * buffers should be pinned for the copies to be asynchronous.
+ */
+int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *h_k,
+                         const uint16_t *h_v, const uint16_t *h_q, float *h_out,
+                         uint16_t *d_k, uint16_t *d_v, uint16_t *d_q, float *d_out,
+                         float softmax_scale, void *ws, size_t ws_bytes, void *stream);
+
+/* Synchronizes `stream`, reads and clears the cache's device status word.
+ * Returns KVQ_OK, or the error a kernel recorded (KVQ_ETIMEOUT), or KVQ_ECUDA. */
+int kvq_get_device_status(kvq_cache *cache, void *stream);
+
+/* Number of kernel launches the last successful call of this thread enqueued. */
+int kvq_last_launch_count(void);
+
+/* Static description of a return code. */
+const char *kvq_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

@@ -1,0 +1,133 @@
+"""Shared helpers of the GPU parity tests: drive the CUDA path (through the C
+ABI binding) and the CPU oracle on the same seeded inputs and compare.
+
+Bit-exact: packed codes, scales, zeros, mode bits, fp16 residual / sink /
+window rows.  Attention output: max-abs error against the oracle's fp64
+result <= ATOL (fp32 accumulation on the device).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from bit_kv_cache_14_gb300 import kvq, synth
+
+ATOL = 2e-3
+
+
+def new_cache(w, max_ctx=None):
+    return kvq.QuantizedKVCache(kvq.config_of(w, max_ctx), "cuda")
+
+
+def oracle_head(w, b, h, max_ctx):
+    head = oracle.OracleHead.for_workload(w, cap=max_ctx)
+    K, V = synth.head_tokens(w, b, h, 0, w.ctx)
+    head.prefill(K, V)
+    return head
+
+
+def check_head_state(cache, w, b, h, head):
+    """Byte-for-byte comparison of one head's cache contents with the oracle."""
+    assert cache.n_quant == head.n_quant, (cache.n_quant, head.n_quant)
+    assert cache.n_resid == head.n_resid
+    n = head.n_quant
+    kc = cache.codes("k")[b, h, :n].cpu().numpy()
+    vc = cache.codes("v")[b, h, :n].cpu().numpy()
+    assert np.array_equal(kc, head.packed_k()), "key codes differ (b=%d h=%d)" % (b, h)
+    assert np.array_equal(vc, head.packed_v()), "value codes differ (b=%d h=%d)" % (b, h)
+    ks_o, kz_o = head.k_meta()
+    vs_o, vz_o = head.v_meta()
+    ks = cache.meta("k_scale")[b, h, : ks_o.size].cpu().numpy()
+    kz = cache.meta("k_zero")[b, h, : kz_o.size].cpu().numpy()
+    vs = cache.meta("v_scale")[b, h, : vs_o.size].cpu().numpy()
+    vz = cache.meta("v_zero")[b, h, : vz_o.size].cpu().numpy()
+    for got, exp, name in ((ks, ks_o, "k_scale"), (kz, kz_o, "k_zero"), (vs, vs_o, "v_scale"),
+                           (vz, vz_o, "v_zero")):
+        assert np.array_equal(got.view(np.uint32), exp.reshape(-1).view(np.uint32)), \
+            "%s differs (b=%d h=%d)" % (name, b, h)
+    kr_o, vr_o = head.residual_tokens()
+    nr = head.n_resid
+    if w.scheme == synth.KIVI:
+        kr = cache.fp16_rows("k_res", w.residual)[b, h, :nr].cpu().numpy()
+        vr = cache.fp16_rows("v_res", w.residual)[b, h, :nr].cpu().numpy()
+    else:
+        # window ring: slot (ring_head + i) % W holds the i-th oldest token
+        W = w.residual
+        order = [(cache.ring_head + i) % W for i in range(nr)] if nr == W else list(range(nr))
+        kr = cache.fp16_rows("k_res", max(W, 1))[b, h].cpu().numpy()[order]
+        vr = cache.fp16_rows("v_res", max(W, 1))[b, h].cpu().numpy()[order]
+        ns = head.n_sink_used
+        assert cache.n_sink == ns
+        if ns:
+            ksk_o, vsk_o = head.sink_tokens()
+            ksk = cache.fp16_rows("k_sink", w.n_sink)[b, h, :ns].cpu().numpy()
+            vsk = cache.fp16_rows("v_sink", w.n_sink)[b, h, :ns].cpu().numpy()
+            assert np.array_equal(ksk.view(np.uint16), ksk_o.view(np.uint16))
+            assert np.array_equal(vsk.view(np.uint16), vsk_o.view(np.uint16))
+        for which, ng, sym in (("k", w.head_dim // w.k_group, head.k_sym),
+                               ("v", w.head_dim // w.v_group, head.v_sym)):
+            nbits = n * ng
+            words = cache.modes(which)[b, h].cpu().numpy().view(np.uint32)
+            exp = oracle.pack_modes(sym[:n, :ng].reshape(-1))
+            full = nbits // 32
+            assert np.array_equal(words[:full], exp[:full]), "%s mode bits differ" % which
+            if nbits % 32:
+                mask = np.uint32((1 << (nbits % 32)) - 1)
+                assert (words[full] & mask) == (exp[full] & mask), "%s mode tail" % which
+    assert np.array_equal(kr.view(np.uint16), kr_o.view(np.uint16)), "key residual differs"
+    assert np.array_equal(vr.view(np.uint16), vr_o.view(np.uint16)), "value residual differs"
+
+
+def check_decode(out, q, w, b, h, head, tau):
+    """Attention output of the query heads of KV head (b, h) vs the oracle."""
+    rg = w.group_ratio
+    worst = 0.0
+    for hq in range(h * rg, (h + 1) * rg):
+        exp = head.attend(q[b, hq], tau)
+        got = out[b, hq].astype(np.float64)
+        err = float(np.max(np.abs(got - exp)))
+        worst = max(worst, err)
+        assert err <= ATOL, "attention error %.3g > %g (b=%d hq=%d)" % (err, ATOL, b, hq)
+    return worst
+
+
+def run_workload(w, heads=None, n_append=None, decode_every=None, max_ctx=None,
+                 check_steps=None):
+    """Prefill + appends + decodes on the GPU; oracle on `heads` (default: all).
+    Returns the worst attention error seen."""
+    n_append = w.n_append if n_append is None else n_append
+    max_ctx = w.ctx + n_append if max_ctx is None else max_ctx
+    if heads is None:
+        heads = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
+    K, V = synth.prompt(w)
+    cache = new_cache(w, max_ctx)
+    cache.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    del K, V
+    heads_o = {bh: oracle_head(w, bh[0], bh[1], max_ctx) for bh in heads}
+    torch.cuda.synchronize()
+    for (b, h), ho in heads_o.items():
+        check_head_state(cache, w, b, h, ho)
+    tau = 1.0 / math.sqrt(w.head_dim)
+    worst = 0.0
+    Ks, Vs = synth.streamed(w, n_append) if n_append else (None, None)
+    steps = set(check_steps or [])
+    if decode_every is None:
+        steps |= {n_append}
+    else:
+        steps |= set(range(0, n_append + 1, decode_every)) | {n_append}
+    for s in range(n_append + 1):
+        if s > 0:
+            cache.append(torch.from_numpy(Ks[s - 1]).cuda(), torch.from_numpy(Vs[s - 1]).cuda())
+            for (b, h), ho in heads_o.items():
+                ho.append(Ks[s - 1, b, h], Vs[s - 1, b, h])
+        if s in steps:
+            q = synth.queries(w, s)
+            out = cache.decode(torch.from_numpy(q).cuda()).cpu().numpy()
+            for (b, h), ho in heads_o.items():
+                check_head_state(cache, w, b, h, ho)
+                worst = max(worst, check_decode(out, q, w, b, h, ho, tau))
+    assert cache.device_status() == 0
+    return worst

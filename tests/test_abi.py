@@ -1,0 +1,127 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point
+that include/kvq.h declares, and its host-side logic (sizes, validation,
+error strings) behaves as documented.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from bit_kv_cache_14_gb300 import build_lib, kvq, synth
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "kvq.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_lib.build()
+    yield
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 9
+    L = ctypes.CDLL(kvq.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(kvq.EXPORTS) == names
+
+
+def _cfg(**kw):
+    base = dict(batch=8, n_q_heads=32, n_kv_heads=32, head_dim=128, bits=2, scheme=kvq.KIVI,
+                k_group=32, v_group=32, residual=128, n_sink=0, max_ctx=4352)
+    base.update(kw)
+    return kvq.make_config(**base)
+
+
+def test_sizes_follow_layout():
+    s = kvq.cache_sizes(_cfg())
+    BH, T, d = 8 * 32, 4352, 128
+    assert s.k_codes == BH * T * d * 2 // 8
+    assert s.k_scale == BH * (T // 32) * d * 4
+    assert s.v_scale == BH * T * (d // 32) * 4
+    assert s.k_res == BH * 128 * d * 2
+    assert s.k_mode == 0 and s.k_sink == 0
+    si = kvq.cache_sizes(_cfg(scheme=kvq.INNERQ, bits=4, k_group=64, v_group=64, residual=32,
+                              n_sink=4, batch=1, max_ctx=1 << 20))
+    assert si.k_codes == 32 * (1 << 20) * 64
+    assert si.k_scale == 32 * (1 << 20) * 2 * 4
+    assert si.k_mode == 32 * ((1 << 20) * 2 // 32) * 4
+    assert si.k_sink == 32 * 4 * 128 * 2
+
+
+def test_per_token_bytes_match_llama2_table():
+    # codes of one token, all 32 layers x 32 heads, keys and values
+    for bits, expect in ((2, 65536), (4, 131072)):
+        s = kvq.cache_sizes(_cfg(bits=bits, batch=1, max_ctx=1))
+        assert 32 * (s.k_codes + s.v_codes) == expect
+
+
+def test_workspace_bytes():
+    n = kvq.workspace_bytes(_cfg())
+    assert n > 8 * 32 * 3 * 130 * 4
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=96), kvq.KVQ_EUNSUPPORTED),
+    (dict(bits=3), kvq.KVQ_EUNSUPPORTED),
+    (dict(residual=100), kvq.KVQ_EINVAL),
+    (dict(n_q_heads=30), kvq.KVQ_EINVAL),
+    (dict(n_q_heads=96), kvq.KVQ_EUNSUPPORTED),
+    (dict(n_sink=4), kvq.KVQ_EINVAL),
+    (dict(v_group=24), kvq.KVQ_EUNSUPPORTED),
+    (dict(batch=0), kvq.KVQ_EINVAL),
+    (dict(max_ctx=0), kvq.KVQ_EINVAL),
+    (dict(scheme=7), kvq.KVQ_EINVAL),
+    (dict(scheme=kvq.INNERQ, k_group=48), kvq.KVQ_EUNSUPPORTED),
+])
+def test_config_validation(kw, code):
+    with pytest.raises(kvq.KVQError) as e:
+        kvq.cache_sizes(_cfg(**kw))
+    assert e.value.code == code
+
+
+def test_calls_validate_before_touching_the_device():
+    L = kvq.lib()
+    cfg = _cfg()
+    empty = kvq.Cache()
+    assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(empty), None, None, 0,
+                                  None) == kvq.KVQ_EINVAL
+    assert L.kvq_append(ctypes.byref(cfg), None, None, None, None) == kvq.KVQ_EINVAL
+    assert L.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(empty), None, None, 1.0, None,
+                                  0, None) == kvq.KVQ_EINVAL
+    bad = _cfg(head_dim=80)
+    assert L.kvq_append(ctypes.byref(bad), ctypes.byref(empty), None, None,
+                        None) == kvq.KVQ_EUNSUPPORTED
+    # misaligned cache buffer pointers are rejected before any launch
+    c = kvq.Cache()
+    for name in ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_res",
+                 "v_res"):
+        setattr(c, name, 0x1000)
+    c.k_codes = 0x1001
+    assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), None, None, 0,
+                                  None) == kvq.KVQ_EALIGN
+    c.k_codes = 0x1000
+    assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), ctypes.c_void_p(0x2000),
+                                  ctypes.c_void_p(0x2000), 5000, None) == kvq.KVQ_ECAPACITY
+    assert L.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(c), ctypes.c_void_p(0x2000),
+                                  ctypes.c_void_p(0x3000), 1.0, ctypes.c_void_p(0x4000), 16,
+                                  None) == kvq.KVQ_ECAPACITY
+
+
+def test_strerror():
+    assert kvq.strerror(0) == "ok"
+    assert "capacity" in kvq.strerror(kvq.KVQ_ECAPACITY)
+    assert kvq.strerror(12345) == "unknown error"
+
+
+def test_workload_configs_are_accepted():
+    for w in synth.WORKLOADS.values():
+        kvq.cache_sizes(kvq.config_of(w))

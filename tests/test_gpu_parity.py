@@ -1,0 +1,184 @@
+"""CUDA path vs the CPU oracle, through the C ABI (needs a GB300).
+
+Small cases run the oracle on every head; they span several key tiles and
+decode splits, ragged residuals, flushes, and the degenerate cache states.
+The full-size cases use the five named workloads at their own sizes, in the
+launch configuration the benchmark times, and compare sampled heads.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_14_gb300 import kvq, synth
+from parity_util import ATOL, check_decode, check_head_state, new_cache, run_workload
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+S = synth.scaled
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+
+
+SMALL = {
+    "tiny": W["tiny"],
+    "llama_small": S(W["llama2_7b_2bit"], batch=2, n_q_heads=3, n_kv_heads=3, ctx=1000,
+                     n_append=300),
+    "kivi4_small": S(W["kivi_4bit"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=777, n_append=200),
+    "gqa_small": S(W["gqa_2bit"], batch=2, n_q_heads=16, n_kv_heads=4, ctx=1500, n_append=140),
+    "innerq_small": S(W["innerq_1m"], batch=1, n_q_heads=4, n_kv_heads=4, ctx=3000, n_append=60),
+    "kivi_d64_g16": S(W["llama2_7b_2bit"], batch=1, n_q_heads=2, n_kv_heads=2, head_dim=64,
+                      ctx=600, k_group=16, v_group=16, residual=48, n_append=100),
+    "kivi_g128_r128": S(W["kivi_4bit"], batch=1, n_q_heads=2, n_kv_heads=1, ctx=700,
+                        k_group=128, v_group=128, residual=128, n_append=140),
+    "kivi_r_eq_g": S(W["llama2_7b_2bit"], batch=1, n_q_heads=8, n_kv_heads=1, ctx=333,
+                     k_group=32, residual=32, n_append=70),
+    "innerq_d64_g16_2bit": S(W["innerq_1m"], batch=2, n_q_heads=2, n_kv_heads=2, head_dim=64,
+                             bits=2, k_group=16, v_group=32, ctx=500, n_sink=3, residual=8,
+                             n_append=20),
+    "innerq_gqa": S(W["innerq_1m"], batch=1, n_q_heads=8, n_kv_heads=2, ctx=900, n_append=40),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_workload_all_heads(name):
+    w = SMALL[name]
+    worst = run_workload(w, decode_every=max(1, w.n_append // 4))
+    assert worst <= ATOL
+
+
+EDGE = {
+    # nothing quantized: the residual holds everything (textbook attention)
+    "kivi_short_prompt": S(W["llama2_7b_2bit"], batch=1, n_q_heads=2, n_kv_heads=2, ctx=100,
+                           n_append=20),
+    # empty prompt, every token streamed in (first flush at R)
+    "kivi_empty_prompt": S(W["llama2_7b_2bit"], batch=1, n_q_heads=1, n_kv_heads=1, ctx=0,
+                           n_append=260),
+    # prompt exactly R: no residual left after prefill
+    "kivi_prompt_eq_r": S(W["llama2_7b_2bit"], batch=1, n_q_heads=1, n_kv_heads=1, ctx=128,
+                          n_append=3),
+    # InnerQ prompt shorter than the sinks
+    "innerq_prompt_lt_sink": S(W["innerq_1m"], batch=1, n_q_heads=2, n_kv_heads=2, ctx=2,
+                               n_append=50),
+    # InnerQ without a recent window: every token past the sinks is quantized
+    "innerq_no_window": S(W["innerq_1m"], batch=1, n_q_heads=2, n_kv_heads=2, ctx=300,
+                          residual=0, n_append=10),
+    # InnerQ without sinks
+    "innerq_no_sink": S(W["innerq_1m"], batch=1, n_q_heads=2, n_kv_heads=2, ctx=300, n_sink=0,
+                        n_append=10),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(name):
+    w = EDGE[name]
+    run_workload(w, decode_every=max(1, w.n_append // 5))
+
+
+def test_empty_cache_decodes_to_zero():
+    w = S(W["tiny"], ctx=0)
+    cache = new_cache(w, 64)
+    q = torch.from_numpy(synth.queries(w)).cuda()
+    cache.prefill(torch.zeros(1, 1, 0, 64, dtype=torch.float16, device="cuda"),
+                  torch.zeros(1, 1, 0, 64, dtype=torch.float16, device="cuda"))
+    out = cache.decode(q)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
+
+
+def test_grid_exact_equals_sdpa():
+    """Lossless data: the fused kernel equals plain fp64 softmax attention on
+    the raw fp16 keys and values (independent of the oracle)."""
+    rng = np.random.default_rng(5)
+    B, H, T, d, G = 2, 2, 512, 128, 32
+    K = np.empty((B, H, T, d), np.float64)
+    V = np.empty((B, H, T, d), np.float64)
+    for b in range(B):
+        for h in range(H):
+            for g in range(T // G):
+                for c in range(d):
+                    u = rng.integers(0, 4, G)
+                    u[0], u[1] = 0, 3
+                    K[b, h, g * G:(g + 1) * G, c] = float(rng.integers(-8, 8)) / 4 + u / 4.0
+            for t in range(T):
+                for j in range(d // 32):
+                    u = rng.integers(0, 4, 32)
+                    u[0], u[1] = 0, 3
+                    V[b, h, t, j * 32:(j + 1) * 32] = float(rng.integers(-8, 8)) / 8 + u / 8.0
+    w = S(W["llama2_7b_2bit"], batch=B, n_q_heads=H, n_kv_heads=H, ctx=T, n_append=0)
+    cache = new_cache(w, T)
+    cache.prefill(torch.from_numpy(K.astype(np.float16)).cuda(),
+                  torch.from_numpy(V.astype(np.float16)).cuda())
+    q = rng.standard_normal((B, H, d)).astype(np.float16)
+    out = cache.decode(torch.from_numpy(q).cuda()).cpu().double()
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q.astype(np.float64))[:, :, None, :], torch.from_numpy(K),
+        torch.from_numpy(V), scale=1 / math.sqrt(d))[:, :, 0, :]
+    assert (out - ref).abs().max().item() <= ATOL
+
+
+def test_decode_step_host_matches_device_path():
+    w = S(W["llama2_7b_2bit"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=600, n_append=4)
+    K, V = synth.prompt(w)
+    Ks, Vs = synth.streamed(w, 4)
+    a, b = new_cache(w), new_cache(w)
+    for c in (a, b):
+        c.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    shape_q = (w.batch, w.n_q_heads, w.head_dim)
+    d_k = torch.empty(w.batch, w.n_kv_heads, w.head_dim, dtype=torch.float16, device="cuda")
+    d_v, d_q = torch.empty_like(d_k), torch.empty(shape_q, dtype=torch.float16, device="cuda")
+    d_out = torch.empty(shape_q, dtype=torch.float32, device="cuda")
+    h_out = torch.empty(shape_q, dtype=torch.float32).pin_memory()
+    for s in range(4):
+        q = synth.queries(w, s)
+        hk = torch.from_numpy(Ks[s]).pin_memory()
+        hv = torch.from_numpy(Vs[s]).pin_memory()
+        hq = torch.from_numpy(q).pin_memory()
+        a.decode_step_host(hk, hv, hq, h_out, d_k, d_v, d_q, d_out)
+        torch.cuda.synchronize()
+        b.append(torch.from_numpy(Ks[s]).cuda(), torch.from_numpy(Vs[s]).cuda())
+        ref = b.decode(torch.from_numpy(q).cuda()).cpu()
+        assert torch.equal(h_out, ref)
+
+
+def test_errors_leave_state_unchanged():
+    w = S(W["tiny"], ctx=64)
+    cache = new_cache(w, 64)
+    K, V = synth.prompt(w)
+    cache.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    k = torch.zeros(1, 1, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(kvq.KVQError) as e:
+        cache.append(k, k)                     # cache is full (max_ctx = 64)
+    assert e.value.code == kvq.KVQ_ECAPACITY
+    assert cache.n_quant == 64 and cache.n_resid == 0
+    with pytest.raises(kvq.KVQError) as e:
+        cache.append(k[..., 1:], k[..., 1:])   # misaligned device pointer
+    assert e.value.code in (kvq.KVQ_EALIGN, kvq.KVQ_ECAPACITY)
+    assert cache.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled heads
+# ---------------------------------------------------------------------------
+
+def _sample_heads(w, n=3):
+    B, H = w.batch, w.n_kv_heads
+    picks = [(0, 0), (B - 1, H - 1), (B // 2, H // 2)]
+    return sorted(set(picks))[:n]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama2_7b_2bit", "kivi_4bit", "gqa_2bit", "innerq_1m"])
+def test_full_size_sampled(name):
+    w = W[name]
+    heads = _sample_heads(w, 2 if name == "innerq_1m" else 3)
+    n_append = w.n_append
+    steps = [1, n_append] if n_append > 1 else [n_append]
+    run_workload(w, heads=heads, n_append=n_append, decode_every=None, check_steps=steps)
