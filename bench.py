@@ -1,0 +1,500 @@
+"""Decode-step benchmark of the quantized KV cache on GB300.
+
+One step = one pass of the decode hot path over the whole batch:
+kvq_append (the new token; the residual flush every R tokens is part of it)
+followed by kvq_decode_attention over the packed cache.  The prompt is
+quantized once per cache before timing (kvq_quantize_prefill, also timed
+separately and reported under "prefill").
+
+Workload (default): the Llama-2-7B-shaped layer -- batch 8, 32 heads,
+head_dim 128, 4096-token prompt, 2-bit, G=32, v_group=32, R=128, then 256
+streamed appends, each followed by a decode.  The appended steps replay in
+epochs of 256: a CUDA graph holds one epoch for every cache copy with the
+counters of that epoch, so every replay rewrites the same residual slots and
+flushes (the cache returns to its post-prompt state, context 4097..4352).
+Several cache copies are used in rotation so the bytes touched between two
+uses of one copy exceed 3x the L2 size (no L2 flush needed).
+
+Prints one JSON line.  --impl reference times the CPU oracle instead (the
+plain C reference of the method, on the host cores, bounded sample).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_kv_cache_14_gb300 import synth  # noqa: E402
+
+METRIC = "quantized-KV decode attention: KV GB/s read (% of GB300 HBM peak), µs/step"
+EPOCH = 256  # streamed appends per replayed epoch
+
+
+# ---------------------------------------------------------------------------
+# bytes of one decode step (algorithmic: what the kernel must read)
+# ---------------------------------------------------------------------------
+
+def decode_bytes(w, n_quant, n_resid, n_sink):
+    """Codes + fp32 scale/zero + fp16 residual/sink rows, all heads."""
+    BH, d, b = w.batch * w.n_kv_heads, w.head_dim, w.bits
+    codes = 2 * n_quant * d * b // 8
+    if w.scheme == synth.KIVI:
+        kmeta = (n_quant // w.k_group) * d * 8
+    else:
+        kmeta = n_quant * (d // w.k_group) * 8
+    vmeta = n_quant * (d // w.v_group) * 8
+    fp16 = (n_resid + n_sink) * d * 2 * 2
+    return BH * (codes + kmeta + vmeta + fp16)
+
+
+def kivi_states(w, n0, r0, steps):
+    """(n_quant, n_resid) after each append, starting from (n0, r0)."""
+    out, nq, nr = [], n0, r0
+    for _ in range(steps):
+        if nr + 1 == w.residual:
+            nq, nr = nq + w.residual, 0
+        else:
+            nr += 1
+        out.append((nq, nr))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [l for t, l in self.lines if t0 - 0.15 <= t <= t1 + 0.15] or [l for _, l in self.lines]
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def decode_source_sha():
+    h = hashlib.sha256()
+    for name in ("kvq_decode.cu", "kvq_internal.cuh"):
+        with open(os.path.join(ROOT, "bit_kv_cache_14_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, per_launch_units):
+    """DRAM bytes per decode launch from the committed ncu summary, or None when
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "decode_%s.md" % workload)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not tb or sha.group(1) != decode_source_sha():
+        return None
+    return float(tb.group(1))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_decode_rate(w, seconds=12.0, n_heads=None):
+    """Times the CPU oracle's decode step (append + fp64 attention) on a sample
+    of KV heads for about `seconds`; returns (bytes/s scaled to the whole
+    batch, threads, description)."""
+    import oracle  # only the CPU-baseline leg imports the oracle
+    from concurrent.futures import ThreadPoolExecutor
+
+    threads = max(1, len(os.sched_getaffinity(0)))
+    BH = w.batch * w.n_kv_heads
+    n_heads = min(BH, n_heads or max(threads, 16))
+    heads = [(i // w.n_kv_heads, i % w.n_kv_heads) for i in
+             np.linspace(0, BH - 1, n_heads).astype(int)]
+    cap = w.ctx + EPOCH
+    objs = {}
+
+    def make(bh):
+        b, h = bh
+        o = oracle.OracleHead.for_workload(w, cap=cap)
+        K, V = synth.head_tokens(w, b, h, 0, w.ctx)
+        o.prefill(K, V)
+        k, v = synth.head_tokens(w, b, h, 1, EPOCH, first_token=w.ctx)
+        objs[bh] = (o, k, v)
+
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(make, heads))
+    tau = 1.0 / math.sqrt(w.head_dim)
+    rg = w.group_ratio
+    qs = [synth.queries(w, s) for s in range(4)]
+
+    def one_step(bh, s):
+        o, k, v = objs[bh]
+        o.append(k[s], v[s])
+        b, h = bh
+        for hq in range(h * rg, (h + 1) * rg):
+            o.attend(qs[s % 4][b, hq], tau)
+
+    steps, t0 = 0, time.perf_counter()
+    byte_sum = 0.0
+    with ThreadPoolExecutor(threads) as ex:
+        while time.perf_counter() - t0 < seconds and steps < EPOCH:
+            list(ex.map(lambda bh: one_step(bh, steps), heads))
+            o0 = objs[heads[0]][0]
+            byte_sum += decode_bytes(w, o0.n_quant, o0.n_resid, o0.n_sink_used) * n_heads / BH
+            steps += 1
+    dt = time.perf_counter() - t0
+    desc = ("%d decode steps (append + fp64 attention) of %d of the %d KV heads "
+            "(%d query heads each), %d threads, scaled to the whole batch by bytes"
+            % (steps, n_heads, BH, rg, threads))
+    return byte_sum / dt, threads, desc, steps
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, w, rank, world):
+    import torch
+    from bit_kv_cache_14_gb300 import kvq
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    max_ctx = w.ctx + EPOCH
+    cfg = kvq.config_of(w, max_ctx)
+    K, V = synth.prompt(w)
+    Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
+    del K, V
+    prompt_bytes_in = 2 * Kd.numel() * 2
+
+    one = kvq.QuantizedKVCache(cfg, dev)
+    cache_bytes = sum(t.numel() for t in one.bufs.values())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    copies = max(2, math.ceil(3 * l2 / max(1, decode_bytes(w, w.ctx, 0, 0))) + 1)
+    caches = [one] + [kvq.QuantizedKVCache(cfg, dev) for _ in range(copies - 1)]
+
+    # prefill (timed once per copy, plain launches)
+    pre_ms = []
+    with torch.cuda.stream(stream):
+        for c in caches:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            c.prefill(Kd, Vd, stream)
+            e1.record(stream)
+            e1.synchronize()
+            pre_ms.append(e0.elapsed_time(e1))
+    del Kd, Vd
+    n0, r0, s0 = caches[0].n_quant, caches[0].n_resid, caches[0].n_sink
+    states = [(c.n_quant, c.n_resid, c.n_sink, c.ring_head) for c in caches]
+
+    Ks, Vs = synth.streamed(w, EPOCH)
+    ks = torch.from_numpy(Ks).to(dev)
+    vs = torch.from_numpy(Vs).to(dev)
+    qs = torch.from_numpy(np.stack([synth.queries(w, s) for s in range(8)])).to(dev)
+    outs = [torch.empty(qs.shape[1:], dtype=torch.float32, device=dev) for _ in caches]
+    scale = 1.0 / math.sqrt(w.head_dim)
+
+    def restore():
+        for c, st in zip(caches, states):
+            c.view.n_quant, c.view.n_resid, c.view.n_sink, c.view.ring_head = st
+
+    def step(i):
+        c = i % copies
+        e = (i // copies) % EPOCH
+        caches[c].append(ks[e], vs[e], stream)
+        caches[c].decode(qs[e % 8], outs[c], scale, stream)
+
+    # per-step algorithmic bytes over one epoch (identical for every copy)
+    if w.scheme == synth.KIVI:
+        ep_states = kivi_states(w, n0, r0, EPOCH)
+        ep_bytes = [decode_bytes(w, nq, nr, 0) for nq, nr in ep_states]
+    else:
+        ep_bytes = [decode_bytes(w, n0 + i + 1, r0, s0) for i in range(EPOCH)]
+
+    # graph of one epoch for every copy: EPOCH * copies steps
+    P = EPOCH * copies
+    graph = torch.cuda.CUDAGraph()
+    restore()
+    with torch.cuda.stream(stream):
+        step(0)  # warm the library (function attributes) outside capture
+    stream.synchronize()
+    restore()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(P):
+            step(i)
+    restore()
+
+    K_steps, W_steps = args.steps, args.warmup
+    n_full, rem = divmod(K_steps, P)
+    rem_graph = None
+    if rem:
+        rem_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rem_graph, stream=stream):
+            for i in range(rem):
+                step(i)
+        restore()
+
+    # warm-up: at least W steps, in whole epochs
+    warm_replays = max(1, math.ceil(W_steps / P))
+    with torch.cuda.stream(stream):
+        for _ in range(warm_replays):
+            graph.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_full):
+            graph.replay()
+        if rem_graph is not None:
+            rem_graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+
+    # bytes of exactly the K timed steps
+    total_bytes = sum(ep_bytes[(i // copies) % EPOCH] for i in range(K_steps))
+
+    # decode kernel alone: a graph of decode launches over the copies (state:
+    # post-prompt + one appended token), timed with events on the same stream
+    restore()
+    with torch.cuda.stream(stream):
+        for c in caches:
+            c.append(ks[0], vs[0], stream)
+    stream.synchronize()
+    dstate_bytes = decode_bytes(w, caches[0].n_quant, caches[0].n_resid, caches[0].n_sink)
+    M = max(copies * 32, 256)
+    dgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(dgraph, stream=stream):
+        for i in range(M):
+            caches[i % copies].decode(qs[i % 8], outs[i % copies], scale, stream)
+    with torch.cuda.stream(stream):
+        dgraph.replay()
+        stream.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(4):
+            dgraph.replay()
+        d1.record(stream)
+    d1.synchronize()
+    decode_ms = d0.elapsed_time(d1) / (4 * M)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # plain launches (no graph), one step per Python call: host-launch cost
+    restore()
+    n_plain = min(K_steps, 2 * P) if K_steps >= 8 else K_steps
+    with torch.cuda.stream(stream):
+        stream.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for i in range(n_plain):
+            if i % P == 0:
+                restore()
+            step(i)
+        p1.record(stream)
+    p1.synchronize()
+    plain_ms = p0.elapsed_time(p1) / max(1, n_plain)
+
+    # end to end through the host-buffer entry point (pinned host memory in,
+    # host result out, every step)
+    restore()
+    c0 = caches[0]
+    d_k = torch.empty(ks.shape[1:], dtype=torch.float16, device=dev)
+    d_v, d_q = torch.empty_like(d_k), torch.empty(qs.shape[1:], dtype=torch.float16, device=dev)
+    d_out = torch.empty(qs.shape[1:], dtype=torch.float32, device=dev)
+    h_k = torch.from_numpy(Ks).pin_memory()
+    h_v = torch.from_numpy(Vs).pin_memory()
+    h_q = qs.cpu().pin_memory()
+    h_out = torch.empty(qs.shape[1:], dtype=torch.float32).pin_memory()
+    n_e2e = min(EPOCH, max(K_steps, 16))
+    with torch.cuda.stream(stream):
+        for i in range(8):  # warm-up
+            c0.decode_step_host(h_k[i], h_v[i], h_q[i % 8], h_out, d_k, d_v, d_q, d_out, scale,
+                                stream)
+        stream.synchronize()
+        restore()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        e2e_bytes = 0
+        for i in range(n_e2e):
+            c0.decode_step_host(h_k[i], h_v[i], h_q[i % 8], h_out, d_k, d_v, d_q, d_out, scale,
+                                stream)
+            e2e_bytes += ep_bytes[i]
+        x1.record(stream)
+    x1.synchronize()
+    e2e_ms = x0.elapsed_time(x1)
+    h2d = 2 * ks[0].numel() * 2 + qs[0].numel() * 2
+    d2h = qs[0].numel() * 4
+    assert c0.device_status() == 0
+    return dict(warmup_steps=warm_replays * P, elapsed_ms=elapsed_ms, total_bytes=total_bytes, decode_ms=decode_ms,
+                dstate_bytes=dstate_bytes, plain_ms=plain_ms, e2e_ms=e2e_ms,
+                e2e_bytes=e2e_bytes, n_e2e=n_e2e, h2d=h2d, d2h=d2h, clocks=clocks,
+                copies=copies, cache_bytes=cache_bytes, prefill_ms=float(np.median(pre_ms)),
+                prompt_bytes_in=prompt_bytes_in, l2=l2,
+                ws_cache_total=cache_bytes * copies)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=512)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--workload", default="llama2_7b_2bit", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--skip-cpu", action="store_true", help="omit the cpu_baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.workload]
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    peak, peak_kind = measured_peak()
+    config = {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads,
+              "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "ctx": w.ctx, "bits": w.bits,
+              "k_group": w.k_group, "v_group": w.v_group, "residual": w.residual,
+              "n_sink": w.n_sink, "appends_per_epoch": EPOCH}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        rate, threads, desc, steps = oracle_decode_rate(w, seconds=args.cpu_seconds)
+        gbs = rate / 1e9
+        bytes_step = decode_bytes(w, w.ctx, 1, 0)
+        line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": steps, "warmup": 0, "ms_per_step": bytes_step / rate * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "config": config,
+                "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    r = run_gpu(args, w, rank, world)
+    elapsed = torch.tensor([r["elapsed_ms"]], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
+    elapsed_ms = float(elapsed.item())
+    value = r["total_bytes"] * world / (elapsed_ms * 1e-3) / 1e9
+    decode_gbs = r["dstate_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
+    traffic = profiled_traffic(w.name, 1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": r["warmup_steps"], "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": dict(config, l2_policy="rotating %d cache copies (%.0f MB touched between "
+                       "uses of one copy vs %.0f MB L2)" % (
+                           r["copies"], (r["copies"] - 1) * decode_bytes(w, w.ctx, 0, 0) / 1e6,
+                           r["l2"] / 1e6),
+                       storage="%d-bit codes + fp32 scale/zero" % w.bits,
+                       parallelism="replicas" if world > 1 else "single"),
+        "us_per_step": elapsed_ms / args.steps * 1e3,
+        "roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": decode_gbs / peak, "traffic": traffic,
+                     "kernel": "decode_kernel", "kernel_us": r["decode_ms"] * 1e3,
+                     "algorithmic_bytes_per_launch": r["dstate_bytes"],
+                     "peak_kind": peak_kind},
+        "plain_launch_us_per_step": r["plain_ms"] * 1e3,
+        "prefill": {"ms": r["prefill_ms"], "bytes_in": r["prompt_bytes_in"],
+                    "gbs_in": r["prompt_bytes_in"] / (r["prefill_ms"] * 1e-3) / 1e9},
+        "e2e": {"value": r["e2e_bytes"] / (r["e2e_ms"] * 1e-3) / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "us_per_step": r["e2e_ms"] / r["n_e2e"] * 1e3, "steps": r["n_e2e"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": r["clocks"],
+    }
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        rate, threads, desc, _ = oracle_decode_rate(w, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate / 1e9, "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

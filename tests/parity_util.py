@@ -57,8 +57,11 @@ def check_head_state(cache, w, b, h, head):
         # window ring: slot (ring_head + i) % W holds the i-th oldest token
         W = w.residual
         order = [(cache.ring_head + i) % W for i in range(nr)] if nr == W else list(range(nr))
-        kr = cache.fp16_rows("k_res", max(W, 1))[b, h].cpu().numpy()[order]
-        vr = cache.fp16_rows("v_res", max(W, 1))[b, h].cpu().numpy()[order]
+        if W > 0:
+            kr = cache.fp16_rows("k_res", W)[b, h].cpu().numpy()[order]
+            vr = cache.fp16_rows("v_res", W)[b, h].cpu().numpy()[order]
+        else:
+            kr = vr = np.zeros((0, w.head_dim), np.float16)
         ns = head.n_sink_used
         assert cache.n_sink == ns
         if ns:
