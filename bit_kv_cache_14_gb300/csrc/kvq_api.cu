@@ -61,17 +61,18 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   g->residual = c.residual;
   g->n_sink = c.n_sink;
   g->max_ctx = c.max_ctx;
+  g->cap = (c.max_ctx + kCapAlign - 1) / kCapAlign * kCapAlign;
   g->row_bytes = c.head_dim * c.bits / 8;
   g->v_meta_cols = c.head_dim / c.v_group;
   if (c.scheme == KVQ_KIVI) {
     g->k_meta_cols = c.head_dim;
-    g->k_meta_rows = (c.max_ctx + c.k_group - 1) / c.k_group;
+    g->k_meta_rows = g->cap / c.k_group;
     g->mode_words = 0;
   } else {
     g->k_meta_cols = c.head_dim / c.k_group;
-    g->k_meta_rows = c.max_ctx;
-    g->mode_words = (c.max_ctx * (c.head_dim / c.k_group) + 31) / 32;
-    const int64_t vw = (c.max_ctx * (c.head_dim / c.v_group) + 31) / 32;
+    g->k_meta_rows = g->cap;
+    g->mode_words = g->cap * (c.head_dim / c.k_group) / 32;
+    const int64_t vw = g->cap * (c.head_dim / c.v_group) / 32;
     if (vw > g->mode_words) g->mode_words = vw;
   }
   return KVQ_OK;
@@ -134,9 +135,10 @@ int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out) {
   if (r != KVQ_OK) return r;
   memset(out, 0, sizeof(*out));
   const size_t BH = (size_t)g.B * g.H;
-  out->k_codes = out->v_codes = BH * (size_t)g.max_ctx * g.row_bytes;
-  out->k_scale = out->k_zero = BH * (size_t)g.k_meta_rows * g.k_meta_cols * sizeof(float);
-  out->v_scale = out->v_zero = BH * (size_t)g.max_ctx * g.v_meta_cols * sizeof(float);
+  out->k_codes = out->v_codes = BH * (size_t)g.cap * g.row_bytes;
+  out->k_scale = out->k_zero =
+      BH * (size_t)g.k_meta_rows * g.k_meta_cols * sizeof(float) + kMetaPad;
+  out->v_scale = out->v_zero = BH * (size_t)g.cap * g.v_meta_cols * sizeof(float) + kMetaPad;
   if (g.scheme == KVQ_INNERQ) out->k_mode = out->v_mode = BH * (size_t)g.mode_words * 4;
   out->k_res = out->v_res = BH * (size_t)g.residual * g.d * 2;
   out->k_sink = out->v_sink = BH * (size_t)g.n_sink * g.d * 2;
@@ -238,7 +240,7 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
   r = from_cuda(launch_decode(g, ptrs_of(cache), plan, cache->n_quant, cache->n_resid,
                               cache->n_sink, cache->ring_head,
                               reinterpret_cast<const __half *>(q), out, softmax_scale, ws,
-                              static_cast<cudaStream_t>(stream)));
+                              num_sms_cached(), static_cast<cudaStream_t>(stream)));
   if (r != KVQ_OK) return r;
   note_launch(1);
   return KVQ_OK;
@@ -288,6 +290,10 @@ int kvq_get_device_status(kvq_cache *cache, void *stream) {
 }
 
 int kvq_last_launch_count(void) { return t_last_launches; }
+
+void kvq_debug_stall_waits(int64_t iterations) {
+  set_debug_stall(iterations < 0 ? 0 : (long long)iterations);
+}
 
 const char *kvq_strerror(int code) {
   switch (code) {

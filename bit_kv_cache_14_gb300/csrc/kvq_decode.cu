@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
       if (i < n_tok) {
         const int gl = tid / G;
         const uint4 *row = reinterpret_cast<const uint4 *>(
-            a.p.k_codes + (bh * g.max_ctx + t0 + i) * (int64_t)g.row_bytes);
+            a.p.k_codes + (bh * g.cap + t0 + i) * (int64_t)g.row_bytes);
         float s[RG];
 #pragma unroll
         for (int hh = 0; hh < RG; ++hh) s[hh] = bias_s[gl * RG + hh];
@@ -215,9 +215,9 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     for (int64_t i = tid; i < n_tok; i += kBlock) {
       const int64_t t = t0 + i;
       const uint32_t *row =
-          reinterpret_cast<const uint32_t *>(a.p.k_codes + (bh * g.max_ctx + t) * (int64_t)g.row_bytes);
-      const float *ks = a.p.k_scale + (bh * g.max_ctx + t) * ngk;
-      const float *kz = a.p.k_zero + (bh * g.max_ctx + t) * ngk;
+          reinterpret_cast<const uint32_t *>(a.p.k_codes + (bh * g.cap + t) * (int64_t)g.row_bytes);
+      const float *ks = a.p.k_scale + (bh * g.cap + t) * ngk;
+      const float *kz = a.p.k_zero + (bh * g.cap + t) * ngk;
       float s[RG] = {};
       for (int j = 0; j < ngk; ++j) {
         float part[RG] = {};
@@ -290,11 +290,11 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     const int gv = (8 * j) / g.v_group;
     for (int64_t i = tl; i < n_tok; i += TL) {
       const int64_t t = t0 + i;
-      const uint8_t *row = a.p.v_codes + (bh * g.max_ctx + t) * (int64_t)g.row_bytes;
+      const uint8_t *row = a.p.v_codes + (bh * g.cap + t) * (int64_t)g.row_bytes;
       const uint32_t word = BITS == 2 ? (uint32_t)reinterpret_cast<const uint16_t *>(row)[j]
                                       : reinterpret_cast<const uint32_t *>(row)[j];
-      const float vs = a.p.v_scale[(bh * g.max_ctx + t) * ngv + gv];
-      const float vz = a.p.v_zero[(bh * g.max_ctx + t) * ngv + gv];
+      const float vs = a.p.v_scale[(bh * g.cap + t) * ngv + gv];
+      const float vz = a.p.v_zero[(bh * g.cap + t) * ngv + gv];
 #pragma unroll
       for (int hh = 0; hh < RG; ++hh) {
         const float pv = sc[hh * a.sc_max + i];
@@ -405,9 +405,7 @@ int sc_slots(const Geometry &g) {
   return (int)s;
 }
 
-int s_max_of(const Geometry &g) {
-  return (int)((g.max_ctx + kTile - 1) / kTile) + 2;
-}
+int s_max_of(const Geometry &g) { return part_slots(g); }
 
 }  // namespace
 
@@ -437,8 +435,11 @@ DecodePlan plan_decode(const Geometry &g, int64_t n_quant, int64_t n_fp16, int n
 
 cudaError_t launch_decode(const Geometry &g, const CachePtrs &p, const DecodePlan &plan,
                           int64_t n_quant, int64_t n_resid, int64_t n_sink, int64_t ring_head,
-                          const __half *q, float *out, float scale, void *ws, cudaStream_t st) {
+                          const __half *q, float *out, float scale, void *ws, int num_sms,
+                          cudaStream_t st) {
   (void)ring_head;  // attention does not depend on the order of window tokens
+  if (n_quant > 0 && tc_decode_supported(g))
+    return launch_decode_tc(g, p, n_quant, n_resid, n_sink, q, out, scale, ws, num_sms, st);
   DecodeArgs a;
   a.g = g;
   a.p = p;

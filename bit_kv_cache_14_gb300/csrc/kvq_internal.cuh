@@ -11,16 +11,19 @@ namespace kvq {
 
 constexpr int kMaxHeadDim = 128;
 constexpr int kMaxResidual = 1024;
+constexpr int kCapAlign = 128;     // token-stride granularity of the cache layout
+constexpr int kMetaPad = 64;       // slack bytes after each metadata buffer
 
 // Geometry of one cache, resolved on the host from kvq_config and copied by
 // value into every kernel.
 struct Geometry {
   int B, H, Hq, d, bits, scheme, k_group, v_group, residual, n_sink;
   int64_t max_ctx;
+  int64_t cap;        // per-head token stride of every buffer: max_ctx rounded up to kCapAlign
   int row_bytes;      // packed bytes per token row: d * bits / 8
   int k_meta_cols;    // KIVI: d; InnerQ: d / k_group
   int v_meta_cols;    // d / v_group
-  int64_t k_meta_rows;  // per head: KIVI ceil(max_ctx / G); InnerQ max_ctx
+  int64_t k_meta_rows;  // per head: KIVI cap / G; InnerQ cap
   int64_t mode_words;   // per head, InnerQ only
 };
 
@@ -45,6 +48,10 @@ cudaError_t launch_append(const Geometry &g, const CachePtrs &p, const __half *k
                           const __half *v, int64_t n_quant, int64_t n_resid,
                           int64_t n_sink, int64_t ring_head, cudaStream_t st);
 
+// Partial (m, l, o) slots per head in the decode workspace: enough for one
+// per 128 quantized tokens plus the fp16 segment.
+inline int part_slots(const Geometry &g) { return (int)(g.cap / kCapAlign) + 2; }
+
 struct DecodePlan {
   int n_qsplit;        // splits over the quantized region
   int n_split;         // n_qsplit + (fp16 segment present ? 1 : 0)
@@ -55,7 +62,14 @@ DecodePlan plan_decode(const Geometry &g, int64_t n_quant, int64_t n_fp16, int n
 cudaError_t launch_decode(const Geometry &g, const CachePtrs &p, const DecodePlan &plan,
                           int64_t n_quant, int64_t n_resid, int64_t n_sink,
                           int64_t ring_head, const __half *q, float *out, float scale,
-                          void *ws, cudaStream_t st);
+                          void *ws, int num_sms, cudaStream_t st);
+
+// Tensor-core decode path (MHA, head_dim 128, 2 or 4 value groups).
+bool tc_decode_supported(const Geometry &g);
+cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_quant,
+                             int64_t n_resid, int64_t n_sink, const __half *q, float *out,
+                             float scale, void *ws, int num_sms, cudaStream_t st);
+void set_debug_stall(long long iterations);
 
 // ---- quantization arithmetic (bit-exact contract with the formula) -------
 // Asymmetric: scale = (max - min) / (2^b - 1), zero = min,

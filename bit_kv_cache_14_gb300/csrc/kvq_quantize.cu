@@ -40,7 +40,7 @@ __device__ __forceinline__ void store_chunk(uint8_t *row, int chunk, uint32_t w,
 
 __device__ __forceinline__ uint8_t *code_row(uint8_t *base, const Geometry &g, int64_t bh,
                                              int64_t slot) {
-  return base + (bh * g.max_ctx + slot) * (int64_t)g.row_bytes;
+  return base + (bh * g.cap + slot) * (int64_t)g.row_bytes;
 }
 
 // One key group (G tokens of src, row stride d) quantized per channel into
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kQuantBlock)
     store_chunk(code_row(dst.codes, g, bh, t), j, q.codes, g.bits);
     if ((j & (lanes - 1)) == 0) {
       const int gi = j / lanes;
-      const int64_t mi = (bh * g.max_ctx + t) * ng + gi;
+      const int64_t mi = (bh * g.cap + t) * ng + gi;
       dst.scale[mi] = q.scale;
       dst.zero[mi] = q.zero;
       if (dst.mode && q.sym) {
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kQuantBlock)
     if (valid) {
       store_chunk(code_row(dst.codes, g, bh, n_quant + t), j, q.codes, g.bits);
       if ((j & (lanes - 1)) == 0) {
-        const int64_t mi = (bh * g.max_ctx + n_quant + t) * ng + j / lanes;
+        const int64_t mi = (bh * g.cap + n_quant + t) * ng + j / lanes;
         dst.scale[mi] = q.scale;
         dst.zero[mi] = q.zero;
       }
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(32)
       store_chunk(code_row(dst.codes, g, bh, n_quant), j, q.codes, g.bits);
       if ((j & (lanes - 1)) == 0) {
         const int ng = dst.meta_cols, gi = j / lanes;
-        const int64_t mi = (bh * g.max_ctx + n_quant) * ng + gi;
+        const int64_t mi = (bh * g.cap + n_quant) * ng + gi;
         dst.scale[mi] = q.scale;
         dst.zero[mi] = q.zero;
         const int64_t bit = n_quant * ng + gi;

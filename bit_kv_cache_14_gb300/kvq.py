@@ -26,12 +26,13 @@ KVQ_ECUDA = -5
 KVQ_ETIMEOUT = -6
 KIVI = 0
 INNERQ = 1
+CAP_ALIGN = 128  # token-stride granularity of the cache layout
 
 # Every entry point declared in include/kvq.h.
 EXPORTS = (
     "kvq_cache_sizes", "kvq_workspace_bytes", "kvq_quantize_prefill", "kvq_append",
     "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
-    "kvq_last_launch_count", "kvq_strerror",
+    "kvq_last_launch_count", "kvq_strerror", "kvq_debug_stall_waits",
 )
 
 
@@ -85,10 +86,12 @@ def lib():
                                                ctypes.c_size_t, P]
             L.kvq_get_device_status.argtypes = [CA, P]
             L.kvq_last_launch_count.argtypes = []
+            L.kvq_debug_stall_waits.argtypes = [ctypes.c_int64]
+            L.kvq_debug_stall_waits.restype = None
             L.kvq_strerror.argtypes = [ctypes.c_int]
             L.kvq_strerror.restype = ctypes.c_char_p
             for name in EXPORTS:
-                if name != "kvq_strerror":
+                if name not in ("kvq_strerror", "kvq_debug_stall_waits"):
                     getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -207,32 +210,53 @@ class QuantizedKVCache:
             self.ws.data_ptr(), self.ws_bytes, _stream(stream)), "kvq_decode_step_host")
 
     def device_status(self, stream=None) -> int:
-        return lib().kvq_get_device_status(ctypes.byref(self.view), _stream(stream))
+        """Synchronizes, reads and clears the status word.  After an error the
+        decode workspace is zero-filled again (its counters are undefined)."""
+        code = lib().kvq_get_device_status(ctypes.byref(self.view), _stream(stream))
+        if code != KVQ_OK:
+            self.ws.zero_()
+            torch.cuda.synchronize(self.device)
+        return code
 
     # ---- typed views of the buffers (for tests and inspection) ------------
-    def _geom(self):
-        c = self.cfg
-        return c.batch, c.n_kv_heads, c.max_ctx, c.head_dim
+    @property
+    def cap(self) -> int:
+        """Per-head token stride of every buffer: max_ctx rounded up to 128."""
+        return (self.cfg.max_ctx + CAP_ALIGN - 1) // CAP_ALIGN * CAP_ALIGN
 
     def codes(self, which: str) -> torch.Tensor:
-        B, H, T, d = self._geom()
-        rb = d * self.cfg.bits // 8
-        return self.bufs[which + "_codes"][: B * H * T * rb].view(B, H, T, rb)
+        c = self.cfg
+        rb = c.head_dim * c.bits // 8
+        n = c.batch * c.n_kv_heads * self.cap * rb
+        return self.bufs[which + "_codes"][:n].view(c.batch, c.n_kv_heads, self.cap, rb)
 
     def meta(self, name: str) -> torch.Tensor:
-        B, H, T, d = self._geom()
-        n = getattr(self.sizes, name) // 4
-        return self.bufs[name][: n * 4].view(torch.float32).view(B, H, -1)
+        """scale / zero buffer as fp32 [B][H][rows * cols] (padding excluded)."""
+        c = self.cfg
+        if name.startswith("k") and c.scheme == KIVI:
+            per_head = self.cap // c.k_group * c.head_dim
+        elif name.startswith("k"):
+            per_head = self.cap * (c.head_dim // c.k_group)
+        else:
+            per_head = self.cap * (c.head_dim // c.v_group)
+        n = c.batch * c.n_kv_heads * per_head
+        return self.bufs[name][: n * 4].view(torch.float32).view(c.batch, c.n_kv_heads, per_head)
 
     def modes(self, which: str) -> torch.Tensor:
-        B, H, _, _ = self._geom()
+        c = self.cfg
         n = getattr(self.sizes, which + "_mode") // 4
-        return self.bufs[which + "_mode"][: n * 4].view(torch.int32).view(B, H, -1)
+        return self.bufs[which + "_mode"][: n * 4].view(torch.int32).view(c.batch, c.n_kv_heads, -1)
 
     def fp16_rows(self, name: str, rows: int) -> torch.Tensor:
-        B, H, _, d = self._geom()
+        c = self.cfg
         n = getattr(self.sizes, name) // 2
-        return self.bufs[name][: n * 2].view(torch.float16).view(B, H, rows, d)
+        return self.bufs[name][: n * 2].view(torch.float16).view(c.batch, c.n_kv_heads, rows,
+                                                                 c.head_dim)
 
     def last_launch_count(self) -> int:
         return lib().kvq_last_launch_count()
+
+
+def debug_stall_waits(iterations: int) -> None:
+    """Force the decode kernel's timeout path (iterations > 0) or switch it off (0)."""
+    lib().kvq_debug_stall_waits(int(iterations))

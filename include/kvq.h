@@ -31,16 +31,18 @@
  *   scale = max(|min|, |max|) / (2^(b-1) - 1), q = clamp(rint(x / scale)),
  *   code = q + 2^(b-1), zero = -2^(b-1) * scale (same dequantization formula).
  *
- * Packed layout (all buffers token-major per (batch, kv head)):
- *   codes   u8 [B][H][max_ctx][d*bits/8]; channel c of a token at bits
+ * Packed layout (all buffers token-major per (batch, kv head); cap = max_ctx
+ * rounded up to a multiple of 128 is the per-head token stride):
+ *   codes   u8 [B][H][cap][d*bits/8]; channel c of a token at bits
  *           (c mod (8/bits))*bits of byte c/(8/bits).
- *   KIVI:   k_scale, k_zero f32 [B][H][ceil(max_ctx/G)][d]   (per G-token group, channel)
- *           v_scale, v_zero f32 [B][H][max_ctx][d/v_group]   (per token, channel group)
- *           k_res, v_res   fp16 [B][H][R][d]                 (residual, oldest first)
- *   InnerQ: k_scale, k_zero f32 [B][H][max_ctx][d/k_group]   (per token, channel group)
- *           v_scale, v_zero f32 [B][H][max_ctx][d/v_group]
- *           k_mode, v_mode  u32 [B][H][ceil(max_ctx*(d/group)/32)]  bit i = group
+ *   KIVI:   k_scale, k_zero f32 [B][H][cap/G][d]         (per G-token group, channel)
+ *           v_scale, v_zero f32 [B][H][cap][d/v_group]   (per token, channel group)
+ *           k_res, v_res   fp16 [B][H][R][d]             (residual, oldest first)
+ *   InnerQ: k_scale, k_zero f32 [B][H][cap][d/k_group]   (per token, channel group)
+ *           v_scale, v_zero f32 [B][H][cap][d/v_group]
+ *           k_mode, v_mode  u32 [B][H][cap*(d/group)/32]  bit i = group
  *                           i % (d/group) of token i / (d/group); 1 = symmetric
+ *   The scale / zero buffers carry 64 bytes of slack after the last head.
  *           k_res, v_res   fp16 [B][H][W][d]   recent window, a ring (see ring_head)
  *           k_sink, v_sink fp16 [B][H][S][d]   first S tokens
  *   Quantized tokens occupy slots [0, n_quant) in arrival order.
@@ -195,6 +197,17 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
 /* Synchronizes `stream`, reads and clears the cache's device status word.
  * Returns KVQ_OK, or the error a kernel recorded (KVQ_ETIMEOUT), or KVQ_ECUDA. */
 int kvq_get_device_status(kvq_cache *cache, void *stream);
+
+/* Debug switch for the failure path of the decode kernel's bounded waits.
+ * Every wait of the shared-memory pipeline gives up after a fixed poll cap
+ * (2^24 polls, about a second or more), records KVQ_ETIMEOUT in the status
+ * word, waits (bounded) for the block's own copies in flight and returns.
+ * With iterations > 0, each block of later tensor-core decode launches first
+ * waits, with that cap, on a barrier that nothing completes, so the timeout
+ * path runs for certain; 0 switches it off.  After a timeout the output and
+ * the workspace counters are undefined: zero-fill the workspace again.
+ * Process-wide; not for production use. */
+void kvq_debug_stall_waits(int64_t iterations);
 
 /* Number of kernel launches the last successful call of this thread enqueued. */
 int kvq_last_launch_count(void);

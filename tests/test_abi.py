@@ -42,17 +42,17 @@ def _cfg(**kw):
 
 
 def test_sizes_follow_layout():
-    s = kvq.cache_sizes(_cfg())
-    BH, T, d = 8 * 32, 4352, 128
+    s = kvq.cache_sizes(_cfg(max_ctx=4300))
+    BH, T, d = 8 * 32, 4352, 128      # per-head stride: 4300 rounded up to 128
     assert s.k_codes == BH * T * d * 2 // 8
-    assert s.k_scale == BH * (T // 32) * d * 4
-    assert s.v_scale == BH * T * (d // 32) * 4
+    assert s.k_scale == BH * (T // 32) * d * 4 + 64
+    assert s.v_scale == BH * T * (d // 32) * 4 + 64
     assert s.k_res == BH * 128 * d * 2
     assert s.k_mode == 0 and s.k_sink == 0
     si = kvq.cache_sizes(_cfg(scheme=kvq.INNERQ, bits=4, k_group=64, v_group=64, residual=32,
                               n_sink=4, batch=1, max_ctx=1 << 20))
     assert si.k_codes == 32 * (1 << 20) * 64
-    assert si.k_scale == 32 * (1 << 20) * 2 * 4
+    assert si.k_scale == 32 * (1 << 20) * 2 * 4 + 64
     assert si.k_mode == 32 * ((1 << 20) * 2 // 32) * 4
     assert si.k_sink == 32 * 4 * 128 * 2
 
@@ -60,8 +60,8 @@ def test_sizes_follow_layout():
 def test_per_token_bytes_match_llama2_table():
     # codes of one token, all 32 layers x 32 heads, keys and values
     for bits, expect in ((2, 65536), (4, 131072)):
-        s = kvq.cache_sizes(_cfg(bits=bits, batch=1, max_ctx=1))
-        assert 32 * (s.k_codes + s.v_codes) == expect
+        s = kvq.cache_sizes(_cfg(bits=bits, batch=1, max_ctx=128))
+        assert 32 * (s.k_codes + s.v_codes) // 128 == expect
 
 
 def test_workspace_bytes():

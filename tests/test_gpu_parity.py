@@ -44,6 +44,13 @@ SMALL = {
                              bits=2, k_group=16, v_group=32, ctx=500, n_sink=3, residual=8,
                              n_append=20),
     "innerq_gqa": S(W["innerq_1m"], batch=1, n_q_heads=8, n_kv_heads=2, ctx=900, n_append=40),
+    # head_dim 128 MHA shapes that take the tensor-core decode path
+    "kivi_g16_mha": S(W["llama2_7b_2bit"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=1100,
+                      k_group=16, residual=64, n_append=90),
+    "kivi_g128_mha_4bit": S(W["kivi_4bit"], batch=1, n_q_heads=3, n_kv_heads=3, ctx=1500,
+                            k_group=128, v_group=32, residual=128, n_append=140),
+    "innerq_g32_2bit": S(W["innerq_1m"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, bits=2,
+                         k_group=32, v_group=32, n_append=30),
 }
 
 
@@ -182,3 +189,25 @@ def test_full_size_sampled(name):
     n_append = w.n_append
     steps = [1, n_append] if n_append > 1 else [n_append]
     run_workload(w, heads=heads, n_append=n_append, decode_every=None, check_steps=steps)
+
+
+def test_forced_timeout_is_reported_and_recoverable():
+    """The decode kernel's bounded pipeline wait gives up on a barrier that
+    nothing completes, records KVQ_ETIMEOUT, drains its own copies and
+    returns; the context stays usable and the next decode is correct."""
+    w = S(W["llama2_7b_2bit"], batch=1, n_q_heads=2, n_kv_heads=2, ctx=512, n_append=0)
+    K, V = synth.prompt(w)
+    cache = new_cache(w, 512)
+    cache.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    q = torch.from_numpy(synth.queries(w)).cuda()
+    good = cache.decode(q).clone()
+    assert cache.device_status() == 0
+    try:
+        kvq.debug_stall_waits(1000)
+        cache.decode(q)
+        assert cache.device_status() == kvq.KVQ_ETIMEOUT
+    finally:
+        kvq.debug_stall_waits(0)
+    again = cache.decode(q)
+    assert cache.device_status() == 0
+    assert torch.equal(again, good)
