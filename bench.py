@@ -137,10 +137,18 @@ def measured_peak():
 
 def decode_source_sha():
     h = hashlib.sha256()
-    for name in ("kvq_decode.cu", "kvq_internal.cuh"):
+    for name in ("kvq_decode.cu", "kvq_decode_tc.cu", "kvq_internal.cuh"):
         with open(os.path.join(ROOT, "bit_kv_cache_14_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def decode_kernel_name(w):
+    """Which decode kernel the library launches for this shape (head_dim 128,
+    MHA, 2 or 4 value groups -> the tensor-core kernel)."""
+    if w.head_dim == 128 and w.n_q_heads == w.n_kv_heads and 128 // w.v_group in (2, 4):
+        return "tc_decode_kernel"
+    return "decode_kernel"
 
 
 def profiled_traffic(workload, per_launch_units):
@@ -474,7 +482,7 @@ def main():
         "us_per_step": elapsed_ms / args.steps * 1e3,
         "roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": peak, "unit": "GB/s",
                      "frac": decode_gbs / peak, "traffic": traffic,
-                     "kernel": "decode_kernel", "kernel_us": r["decode_ms"] * 1e3,
+                     "kernel": decode_kernel_name(w), "kernel_us": r["decode_ms"] * 1e3,
                      "algorithmic_bytes_per_launch": r["dstate_bytes"],
                      "peak_kind": peak_kind},
         "plain_launch_us_per_step": r["plain_ms"] * 1e3,
