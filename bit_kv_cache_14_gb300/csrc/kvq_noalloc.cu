@@ -1,0 +1,56 @@
+// Decode attention whose scratch lives in a fixed device array, for callers
+// that cannot allocate device memory (see kvq_decode_attention_noalloc in
+// include/kvq.h).  Nothing here allocates: the scratch is a file-scope device
+// array that exists on every GPU that loads the library, and its device
+// address is looked up once per device.
+#include <mutex>
+
+#include "kvq_internal.cuh"
+
+// The shared scratch.  Host code only sees a stand-in symbol; its device
+// address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char kvq_noalloc_scratch[KVQ_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void *g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch on the current device; looked up on the
+// first call made with that device current.
+int scratch_address(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return KVQ_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, kvq_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return KVQ_ECUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" int kvq_decode_attention_noalloc(const kvq_config *cfg, const kvq_cache *cache,
+                                            const uint16_t *q, float *out,
+                                            float softmax_scale, void *stream) {
+  if (!cache || !q || !out) return KVQ_EINVAL;
+  size_t need = 0;
+  int r = kvq_workspace_bytes(cfg, &need);
+  if (r != KVQ_OK) return r;
+  if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ECAPACITY;
+  void *ws = nullptr;
+  if ((r = scratch_address(&ws)) != KVQ_OK) return r;
+  // The per-head tickets at the start of the scratch must read zero when a
+  // decode starts; clear them (another call may have stopped early).
+  const size_t tickets = ((size_t)cfg->batch * cfg->n_kv_heads * sizeof(int) + 255) & ~(size_t)255;
+  if (cudaMemsetAsync(ws, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return KVQ_ECUDA;
+  return kvq_decode_attention(cfg, cache, q, out, softmax_scale, ws,
+                              (size_t)KVQ_NOALLOC_SCRATCH_BYTES, stream);
+}

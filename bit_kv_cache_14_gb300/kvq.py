@@ -33,6 +33,7 @@ EXPORTS = (
     "kvq_cache_sizes", "kvq_workspace_bytes", "kvq_quantize_prefill", "kvq_append",
     "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
     "kvq_last_launch_count", "kvq_strerror", "kvq_debug_stall_waits",
+    "kvq_decode_attention_noalloc",
 )
 
 
@@ -84,6 +85,7 @@ def lib():
             L.kvq_decode_attention.argtypes = [C, CA, P, P, ctypes.c_float, P, ctypes.c_size_t, P]
             L.kvq_decode_step_host.argtypes = [C, CA, P, P, P, P, P, P, P, P, ctypes.c_float, P,
                                                ctypes.c_size_t, P]
+            L.kvq_decode_attention_noalloc.argtypes = [C, CA, P, P, ctypes.c_float, P]
             L.kvq_get_device_status.argtypes = [CA, P]
             L.kvq_last_launch_count.argtypes = []
             L.kvq_debug_stall_waits.argtypes = [ctypes.c_int64]

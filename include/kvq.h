@@ -194,6 +194,33 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
                          uint16_t *d_k, uint16_t *d_v, uint16_t *d_q, float *d_out,
                          float softmax_scale, void *ws, size_t ws_bytes, void *stream);
 
+/*
+ * Decode attention that allocates nothing, not even its scratch.  The pages
+ * have no counterpart: this is a deployment convenience of the library.
+ *
+ * For callers that cannot hand the library a device buffer for scratch: code
+ * that runs where no device allocator may be called (a plugin or callback
+ * handed only its input and output tensors, a real-time or certified path
+ * that forbids run-time device allocation, a process whose device memory is
+ * entirely owned by another pool).  Same arguments, result and errors as
+ * kvq_decode_attention minus ws / ws_bytes.
+ *
+ * The scratch is one file-scope device array of KVQ_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) that every GPU which loads the library holds until the process
+ * exits.  Configurations whose kvq_workspace_bytes exceeds it are rejected
+ * with KVQ_ECAPACITY before anything is enqueued.  The first call on a device
+ * (with that device current) looks up the array's device address with
+ * cudaGetSymbolAddress; make that first call before any stream capture.
+ * Each call clears the part of the scratch that must start at zero (an
+ * asynchronous memset on `stream`), then launches the decode.  All calls share
+ * the one array: calls whose work can overlap on the GPU (different streams,
+ * different caches) race and give wrong results; serialize them.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+int kvq_decode_attention_noalloc(const kvq_config *cfg, const kvq_cache *cache,
+                                 const uint16_t *q, float *out, float softmax_scale,
+                                 void *stream);
+
 /* Synchronizes `stream`, reads and clears the cache's device status word.
  * Returns KVQ_OK, or the error a kernel recorded (KVQ_ETIMEOUT), or KVQ_ECUDA. */
 int kvq_get_device_status(kvq_cache *cache, void *stream);

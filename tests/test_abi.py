@@ -116,6 +116,16 @@ def test_calls_validate_before_touching_the_device():
                                   None) == kvq.KVQ_ECAPACITY
 
 
+def test_noalloc_decode_rejects_oversized_configs_on_the_host():
+    L = kvq.lib()
+    big = kvq.config_of(synth.WORKLOADS["kivi_4bit"])
+    assert kvq.workspace_bytes(big) > (16 << 20)
+    c = kvq.Cache()
+    assert L.kvq_decode_attention_noalloc(ctypes.byref(big), ctypes.byref(c),
+                                          ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000),
+                                          1.0, None) == kvq.KVQ_ECAPACITY
+
+
 def test_strerror():
     assert kvq.strerror(0) == "ok"
     assert "capacity" in kvq.strerror(kvq.KVQ_ECAPACITY)
