@@ -4,22 +4,29 @@
 // cache, dequantization folded into both GEMVs -- "大模型量化技术原理：KIVI、
 // IntactKV、KVQuant", KIVI / 背景; InnerQ page, 方法论 3), arranged for GB300:
 //
-//  * Persistent, stream-K: the (head, 128-token stage) list of the whole batch,
-//    plus one fp16 item per head (sink + residual / window tokens), is cut into
-//    equal contiguous ranges, one per resident block.  A head split across
-//    blocks leaves one partial (m, l, o) per block; the last block to finish a
-//    head (atomic ticket, no spinning) merges them with the log-sum-exp rule.
-//  * Each 128-token stage (codes + scale/zero of K and V) is fetched with 1-D
-//    cp.async.bulk into a 4-slot shared-memory ring completed on mbarriers.
-//    Every wait is bounded; a timeout sets the status word and the block
-//    drains its own copies before it returns.
-//  * Both GEMVs run as mma.sync m16n8k16 (fp16 in, fp32 accumulate).  2/4-bit
-//    codes become exact fp16 integers with one LOP3 per two codes (the code
-//    bits are OR-ed into the mantissa of 1024.0) and one HSUB2; the position
-//    of a code inside its 16-bit half multiplies it by a power of two that the
-//    other operand (or the final output row) divides out exactly.  The channel
-//    order inside each MMA is a permutation chosen so a thread consumes whole
-//    32-bit code words; the matching operand uses the same permutation.
+//  * Persistent, stream-K: the (head, 128-token unit) list of the whole batch,
+//    plus one cost-weighted fp16 item per head (sink + residual / window
+//    tokens), is cut into equal contiguous ranges, one per resident block.  A
+//    head split across blocks leaves one partial (m, l, o) per block; the last
+//    block to finish a head (atomic ticket, no spinning) merges them with the
+//    log-sum-exp rule.
+//  * Warp-autonomous consumers: inside a block, the 32-token tiles of each
+//    head segment go round-robin to the warps.  Each warp owns a small ring of
+//    shared-memory slots that its lane 0 fills with 1-D cp.async.bulk copies
+//    (codes + scale/zero of K and V of one tile) completed on the warp's own
+//    mbarriers, and keeps its own online-softmax state; the block synchronises
+//    only at head-segment ends, to merge the warps.  The ring runs ahead across
+//    segment ends, so the copies never stop.  Every wait is bounded; a timeout
+//    sets the status word and the warp drains its own copies before the block
+//    returns.
+//  * Both GEMVs run as mma.sync m16n8k16 (fp16 in, fp32 accumulate), two
+//    independent 16-token MMA tiles per warp tile.  2/4-bit codes become exact
+//    fp16 integers with one LOP3 per two codes (the code bits are OR-ed into
+//    the mantissa of 1024.0) and one HSUB2; the position of a code inside its
+//    16-bit half multiplies it by a power of two that the other operand (or the
+//    final output row) divides out exactly.  The channel order inside each MMA
+//    is a permutation chosen so a thread consumes whole 32-bit code words; the
+//    matching operand uses the same permutation.
 //      keys   D[token][n] = sum_c code_tc * B[c][n],  B = q~ = q*scale split
 //             into fp16 hi + lo (n = hi, lo); KIVI: rebuilt per G-token group,
 //             InnerQ: q per channel group j (n = (j, hi/lo)), scale applied after.
@@ -38,10 +45,10 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTT = 128;      // tokens per stage (one 16-token MMA tile per warp)
-constexpr int kStages = 4;
+constexpr int kUnit = 128;    // tokens per stream-K work unit
+constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
 constexpr int kD = 128;
-constexpr int kScrFloats = 4096 + 64;  // fp16 item: 2048 scores + 16x128 reduce
+constexpr int kScrStride = kD + 4;        // floats per warp in the merge scratch
 constexpr uint32_t kMagic = 0x64006400u;  // half2(1024, 1024)
 constexpr long long kDrainLimit = 1LL << 26;
 
@@ -52,9 +59,10 @@ struct TcArgs {
   float *out;
   float scale_log2;
   int64_t n_quant, n_fp16, n_sink;
-  int S_h, F_h, U;  // quantized stages, fp16 units, units per head
-  int64_t total;    // BH * U
+  int S_h, F_h, U;  // quantized units, fp16 units, units per head
+  int total;        // BH * U
   int nc;           // resident blocks
+  int nslot;        // ring slots per warp
   int slot_bytes, off_vc, off_ks, off_kz, off_vs, off_vz;
   float *ws_ml, *ws_o;
   int *ws_cnt;
@@ -64,21 +72,21 @@ struct TcArgs {
 };
 
 struct TcLayout {
-  int ring, sB, sBias, sQf, sScr, sFlag, bars, total;
+  int ring, sB, sQf, sScr, sFlag, bars, total;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int slot_bytes) {
+__host__ __device__ inline TcLayout tc_layout(int slot_bytes, int nslot) {
   TcLayout L;
   L.ring = 0;
-  L.sB = L.ring + kStages * slot_bytes;       // 8 key groups x 128 u32
-  L.sBias = L.sB + 8 * 128 * 4;               // [8 groups][2] floats
-  L.sQf = L.sBias + 16 * 4;                   // [128] floats
-  L.sScr = L.sQf + kD * 4;                    // scratch floats
-  L.sFlag = L.sScr + kScrFloats * 4;          // [8] ints / floats
-  L.bars = L.sFlag + 8 * 4;                   // kStages mbarriers + 1 never completed
-  L.total = L.bars + (kStages + 1) * 8;
+  L.sB = L.ring + kWarps * nslot * slot_bytes;  // per warp: 2 key groups x 128 u32
+  L.sQf = L.sB + kWarps * 2 * 128 * 4;          // [128] floats
+  L.sScr = L.sQf + kD * 4;                      // [warps][kScrStride] floats
+  L.sFlag = L.sScr + kWarps * kScrStride * 4;   // [16] ints / floats
+  L.bars = L.sFlag + 16 * 4;                    // warps * nslot + 1 mbarriers
+  L.total = L.bars + (kWarps * nslot + 1) * 8;
   return L;
 }
+
 
 // ---- PTX helpers --------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -196,25 +204,25 @@ __device__ __forceinline__ void key_pair(int tig, int kb, int reg, int &c_lo, in
   }
 }
 
-__device__ __forceinline__ int64_t owner_of(int64_t x, int64_t total, int nc) {
-  return ((x + 1) * nc - 1) / total;
+__device__ __forceinline__ int owner_of(int x, int total, int nc) {
+  return (int)(((int64_t)(x + 1) * nc - 1) / total);
 }
 
-// Number of partials head bh produces, and the index of the fp16 one.
-__device__ __forceinline__ void head_parts(const TcArgs &a, int64_t bh, int &nseg, int &nparts) {
-  const int64_t base = bh * a.U;
-  nseg = a.S_h > 0 ? (int)(owner_of(base + a.S_h - 1, a.total, a.nc) -
-                           owner_of(base, a.total, a.nc) + 1)
+// Number of quantized-segment partials of head bh and the total partial count
+// (the fp16 partial, if any, has index nseg).
+__device__ __forceinline__ void head_parts(const TcArgs &a, int bh, int &nseg, int &nparts) {
+  const int base = bh * a.U;
+  nseg = a.S_h > 0 ? owner_of(base + a.S_h - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1
                    : 0;
   nparts = nseg + (a.F_h > 0 ? 1 : 0);
 }
 
-// Threads 0..127 hold (M, L, O_c) of one partial of head bh in registers;
-// publish it, take a ticket, and let the last block of the head merge.
-__device__ void publish(const TcArgs &a, int64_t bh, int slot, float M, float L, float O,
+// Threads 0..127 hold (M, L, O_c) of one partial of head bh; publish it, take
+// a ticket, and let the last block of the head merge all of its partials.
+__device__ void publish(const TcArgs &a, int bh, int slot, float M, float L, float O,
                         int *sflag) {
   const int tid = threadIdx.x;
-  const int64_t pi = bh * a.part_stride + slot;
+  const int64_t pi = (int64_t)bh * a.part_stride + slot;
   if (tid < kD) a.ws_o[pi * kD + tid] = O;
   if (tid == 0) {
     a.ws_ml[pi * 2] = M;
@@ -229,20 +237,20 @@ __device__ void publish(const TcArgs &a, int64_t bh, int slot, float M, float L,
   if (sflag[1]) {
     __threadfence();
     if (tid < kD) {
+      const int64_t base = (int64_t)bh * a.part_stride;
       float Mx = -INFINITY;
-      for (int s = 0; s < nparts; ++s) Mx = fmaxf(Mx, __ldcg(&a.ws_ml[(bh * a.part_stride + s) * 2]));
+      for (int s = 0; s < nparts; ++s) Mx = fmaxf(Mx, __ldcg(&a.ws_ml[(base + s) * 2]));
       float Ls = 0.0f, Os = 0.0f;
       if (Mx != -INFINITY) {
         for (int s = 0; s < nparts; ++s) {
-          const int64_t q = bh * a.part_stride + s;
-          const float ms = __ldcg(&a.ws_ml[q * 2]);
+          const float ms = __ldcg(&a.ws_ml[(base + s) * 2]);
           if (ms == -INFINITY) continue;
           const float w = exp2f(ms - Mx);
-          Ls += w * __ldcg(&a.ws_ml[q * 2 + 1]);
-          Os += w * __ldcg(&a.ws_o[q * kD + tid]);
+          Ls += w * __ldcg(&a.ws_ml[(base + s) * 2 + 1]);
+          Os += w * __ldcg(&a.ws_o[(base + s) * kD + tid]);
         }
       }
-      const int b = (int)(bh / a.g.H), h = (int)(bh % a.g.H);
+      const int b = bh / a.g.H, h = bh % a.g.H;
       a.out[((int64_t)b * a.g.Hq + h) * kD + tid] = Ls > 0.0f ? Os / Ls : 0.0f;
     }
     if (tid == 0) a.ws_cnt[bh] = 0;
@@ -250,78 +258,72 @@ __device__ void publish(const TcArgs &a, int64_t bh, int slot, float M, float L,
   __syncthreads();
 }
 
-// fp16 sink + residual / window tokens of head bh on CUDA cores (<= 2048
-// tokens); publishes partial `slot`.
-__device__ void fp16_item(const TcArgs &a, int64_t bh, int slot, const float *sQf, float *scr,
+// Every warp has written (m, l, o[128]) to scr; merge them (block-wide) and
+// publish the result as partial `slot` of head bh.
+__device__ void merge_and_publish(const TcArgs &a, int bh, int slot, const float *scr,
+                                  int *sflag) {
+  const int tid = threadIdx.x;
+  float M = -INFINITY, L = 0.0f, O = 0.0f;
+  if (tid < kD) {
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, scr[w * kScrStride]);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = scr[w * kScrStride];
+        if (mw == -INFINITY) continue;
+        const float s = exp2f(mw - M);
+        L += s * scr[w * kScrStride + 1];
+        O += s * scr[w * kScrStride + 2 + tid];
+      }
+    }
+  }
+  publish(a, bh, slot, M, L, O, sflag);
+}
+
+// fp16 sink + residual / window tokens of head bh (<= 2048): each warp takes
+// every 8th token with its own online softmax (a lane owns 4 channels), then
+// the warps are merged and published as partial `slot`.
+__device__ void fp16_item(const TcArgs &a, int bh, int slot, const float *sQf, float *scr,
                           int *sflag) {
   const Geometry &g = a.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = (int)a.n_fp16, ns = (int)a.n_sink;
-  float *sc = scr;          // [2048]
-  float *red = scr + 2048;  // [16][128]
-  float *wred = scr + 4096; // [8]
-  float mloc = -INFINITY;
-  for (int i = tid; i < n; i += kThreads) {
-    const __half *row = i < ns ? a.p.k_sink + (bh * g.n_sink + i) * kD
-                               : a.p.k_res + (bh * g.residual + (i - ns)) * kD;
-    float s = 0.0f;
-#pragma unroll 4
-    for (int c8 = 0; c8 < kD / 8; ++c8) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(row) + c8);
-      const __half2 *hv = reinterpret_cast<const __half2 *>(&raw);
+  float q4[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __half22float2(hv[k]);
-        s = fmaf(sQf[8 * c8 + 2 * k], f.x, s);
-        s = fmaf(sQf[8 * c8 + 2 * k + 1], f.y, s);
-      }
-    }
-    sc[i] = s;
-    mloc = fmaxf(mloc, s);
+  for (int j = 0; j < 4; ++j) q4[j] = sQf[4 * lane + j];
+  float m = -INFINITY, l = 0.0f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int i = warp; i < n; i += kWarps) {
+    const int64_t kr = i < ns ? ((int64_t)bh * g.n_sink + i) : ((int64_t)bh * g.residual + (i - ns));
+    const __half *krow = (i < ns ? a.p.k_sink : a.p.k_res) + kr * kD;
+    const __half *vrow = (i < ns ? a.p.v_sink : a.p.v_res) + kr * kD;
+    const uint2 kw = __ldg(reinterpret_cast<const uint2 *>(krow) + lane);
+    const uint2 vw = __ldg(reinterpret_cast<const uint2 *>(vrow) + lane);
+    const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
+    const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
+    const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+    const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+    float s = fmaf(q4[0], k01.x, fmaf(q4[1], k01.y, fmaf(q4[2], k23.x, q4[3] * k23.y)));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    const float mn = fmaxf(m, s);
+    const float al = exp2f(m - mn), p = exp2f(s - mn);
+    l = fmaf(l, al, p);
+    acc[0] = fmaf(acc[0], al, p * v01.x);
+    acc[1] = fmaf(acc[1], al, p * v01.y);
+    acc[2] = fmaf(acc[2], al, p * v23.x);
+    acc[3] = fmaf(acc[3], al, p * v23.y);
+    m = mn;
+  }
+  float *ws = scr + warp * kScrStride;
+  if (lane == 0) {
+    ws[0] = m;
+    ws[1] = l;
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-  if (lane == 0) wred[warp] = mloc;
+  for (int j = 0; j < 4; ++j) ws[2 + 4 * lane + j] = acc[j];
   __syncthreads();
-  float M = wred[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) M = fmaxf(M, wred[w]);
-  __syncthreads();
-  float lloc = 0.0f;
-  for (int i = tid; i < n; i += kThreads) {
-    const float p = exp2f(sc[i] - M);
-    sc[i] = p;
-    lloc += p;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
-  if (lane == 0) wred[warp] = lloc;
-  __syncthreads();
-  float L = 0.0f;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) L += wred[w];
-  const int j = tid & 15, tl = tid >> 4;
-  float acc[8] = {};
-  for (int i = tl; i < n; i += 16) {
-    const __half *row = i < ns ? a.p.v_sink + (bh * g.n_sink + i) * kD
-                               : a.p.v_res + (bh * g.residual + (i - ns)) * kD;
-    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(row) + j);
-    const __half2 *hv = reinterpret_cast<const __half2 *>(&raw);
-    const float p = sc[i];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __half22float2(hv[k]);
-      acc[2 * k] = fmaf(p, f.x, acc[2 * k]);
-      acc[2 * k + 1] = fmaf(p, f.y, acc[2 * k + 1]);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 8; ++k) red[tl * kD + 8 * j + k] = acc[k];
-  __syncthreads();
-  float O = 0.0f;
-  if (tid < kD)
-    for (int r = 0; r < 16; ++r) O += red[r * kD + tid];
-  publish(a, bh, slot, n > 0 ? M : -INFINITY, n > 0 ? L : 0.0f, O, sflag);
+  merge_and_publish(a, bh, slot, scr, sflag);
 }
 
 template <int BITS, int SCHEME, int NGV, int NGK>
@@ -329,10 +331,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   extern __shared__ __align__(128) uint8_t smem[];
   constexpr int RB = kD * BITS / 8;  // packed bytes per token row
   const Geometry &g = a.g;
-  const TcLayout Ly = tc_layout(a.slot_bytes);
-  uint8_t *ring = smem + Ly.ring;
-  uint32_t *sB = reinterpret_cast<uint32_t *>(smem + Ly.sB);
-  float *sBias = reinterpret_cast<float *>(smem + Ly.sBias);
+  const int nslot = a.nslot;
+  const TcLayout Ly = tc_layout(a.slot_bytes, nslot);
   float *sQf = reinterpret_cast<float *>(smem + Ly.sQf);
   float *sScr = reinterpret_cast<float *>(smem + Ly.sScr);
   int *sFlag = reinterpret_cast<int *>(smem + Ly.sFlag);
@@ -340,100 +340,120 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly.bars);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-  const int64_t x0 = (int64_t)blockIdx.x * a.total / a.nc;
-  const int64_t x1 = (int64_t)(blockIdx.x + 1) * a.total / a.nc;
+  uint8_t *wring = smem + Ly.ring + warp * nslot * a.slot_bytes;
+  uint64_t *wbars = bars + warp * nslot;
+  uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB) + warp * 256;
 
-  // zero the ring once so stale bytes are always finite; barriers
-  for (int i = tid; i < kStages * a.slot_bytes / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(ring)[i] = make_uint4(0, 0, 0, 0);
+  const int x0 = (int)((int64_t)blockIdx.x * a.total / a.nc);
+  const int x1 = (int)((int64_t)(blockIdx.x + 1) * a.total / a.nc);
+  const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
+
+  // zero the rings once so stale bytes are always finite; barriers
+  for (int i = tid; i < kWarps * nslot * a.slot_bytes / 16; i += kThreads)
+    reinterpret_cast<uint4 *>(smem + Ly.ring)[i] = make_uint4(0, 0, 0, 0);
   if (tid == 0) {
-    for (int s = 0; s <= kStages; ++s) bar_init(&bars[s], 1);
+    for (int s = 0; s <= kWarps * nslot; ++s) bar_init(&bars[s], 1);
     sFlag[0] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
 
-  // ---- producer (thread 0): next quantized unit to fetch -----------------
-  int64_t px = x0;
-  int issued = 0;
+  // quantized token range [tq0, tq1) of head bh inside this block's units
+  auto seg_of = [&](int bh, int &tq0, int &tq1) {
+    const int base = bh * a.U;
+    const int ua = max(x0, base) - base;
+    const int ub = min(min(x1, base + a.U) - base, a.S_h);
+    tq0 = ua * kUnit;
+    tq1 = ua < ub ? (int)min((int64_t)ub * kUnit, a.n_quant) : tq0;
+  };
+
+  // ---- producer (lane 0 of each warp): this warp's tiles, in the order the
+  // consumer loop below visits them ------------------------------------------
+  int pc_bh = -1, pc_tq0 = 0, pc_tq1 = 0, pc_lt = 0, issued = 0;
+  auto pc_settle = [&]() {
+    while (pc_bh >= 0 && pc_tq0 + kTile * pc_lt >= pc_tq1) {
+      if (++pc_bh > bh_last) {
+        pc_bh = -1;
+        return;
+      }
+      seg_of(pc_bh, pc_tq0, pc_tq1);
+      pc_lt = warp;
+    }
+  };
   auto issue_next = [&]() {
-    while (px < x1 && (int)(px % a.U) >= a.S_h) ++px;
-    if (px >= x1) return;
-    const int64_t bh = px / a.U;
-    const int u = (int)(px % a.U);
-    const int64_t tok0 = (int64_t)u * kTT;
-    const int n = (int)min((int64_t)kTT, a.n_quant - tok0);
-    uint8_t *dst = ring + (issued % kStages) * a.slot_bytes;
-    uint64_t *bar = &bars[issued % kStages];
+    if (pc_bh < 0) return;
+    const int tok0 = pc_tq0 + kTile * pc_lt;
+    const int n = min(kTile, pc_tq1 - tok0);
+    const int s = issued % nslot;
+    uint8_t *dst = wring + s * a.slot_bytes;
+    uint64_t *bar = &wbars[s];
+    const int64_t row0 = (int64_t)pc_bh * g.cap + tok0;
     const uint32_t cb = (uint32_t)(n * RB);
-    uint32_t kmb, vmb = (uint32_t)((n * NGV * 4 + 15) & ~15);
+    const uint32_t vmb = (uint32_t)((n * NGV * 4 + 15) & ~15);
+    uint32_t kmb;
     const float *ks, *kz;
     if (SCHEME == KVQ_KIVI) {
-      kmb = (uint32_t)((n / g.k_group) * kD * 4);
-      ks = a.p.k_scale + (bh * g.k_meta_rows + tok0 / g.k_group) * kD;
-      kz = a.p.k_zero + (bh * g.k_meta_rows + tok0 / g.k_group) * kD;
+      const int g0 = tok0 / g.k_group, g1 = (tok0 + n - 1) / g.k_group;
+      kmb = (uint32_t)((g1 - g0 + 1) * kD * 4);
+      ks = a.p.k_scale + ((int64_t)pc_bh * g.k_meta_rows + g0) * kD;
+      kz = a.p.k_zero + ((int64_t)pc_bh * g.k_meta_rows + g0) * kD;
     } else {
       kmb = (uint32_t)((n * NGK * 4 + 15) & ~15);
-      ks = a.p.k_scale + (bh * g.cap + tok0) * NGK;
-      kz = a.p.k_zero + (bh * g.cap + tok0) * NGK;
+      ks = a.p.k_scale + row0 * NGK;
+      kz = a.p.k_zero + row0 * NGK;
     }
     bar_expect_tx(bar, 2 * cb + 2 * kmb + 2 * vmb);
-    bulk_g2s(dst, a.p.k_codes + (bh * g.cap + tok0) * RB, cb, bar);
-    bulk_g2s(dst + a.off_vc, a.p.v_codes + (bh * g.cap + tok0) * RB, cb, bar);
+    bulk_g2s(dst, a.p.k_codes + row0 * RB, cb, bar);
+    bulk_g2s(dst + a.off_vc, a.p.v_codes + row0 * RB, cb, bar);
     bulk_g2s(dst + a.off_ks, ks, kmb, bar);
     bulk_g2s(dst + a.off_kz, kz, kmb, bar);
-    bulk_g2s(dst + a.off_vs, a.p.v_scale + (bh * g.cap + tok0) * NGV, vmb, bar);
-    bulk_g2s(dst + a.off_vz, a.p.v_zero + (bh * g.cap + tok0) * NGV, vmb, bar);
+    bulk_g2s(dst + a.off_vs, a.p.v_scale + row0 * NGV, vmb, bar);
+    bulk_g2s(dst + a.off_vz, a.p.v_zero + row0 * NGV, vmb, bar);
     ++issued;
-    ++px;
+    pc_lt += kWarps;
+    pc_settle();
   };
-  if (tid == 0)
-    for (int s = 0; s < kStages - 1; ++s) issue_next();
+  if (lane == 0) {
+    pc_bh = bh_first;
+    seg_of(pc_bh, pc_tq0, pc_tq1);
+    pc_lt = warp;
+    pc_settle();
+    for (int s = 0; s < nslot; ++s) issue_next();
+  }
 
   // ---- per-head constants --------------------------------------------------
   float pow2E = 1.0f;  // scores = raw * 2^E (q normalised by 2^-E)
-  // KIVI key-operand build: this thread's channel pair (ip = tid % 64)
-  const int ip = tid & 63;
-  int bW, bp, b_clo, b_chi, b_tig, b_kb, b_reg;
-  if (BITS == 2) {
-    bW = ip >> 3;
-    bp = ip & 7;
-    b_clo = 16 * bW + bp;
-    b_chi = b_clo + 8;
-    b_tig = bW >> 1;
-    b_kb = 4 * (bW & 1) + (bp >> 1);
-  } else {
-    bW = ip >> 2;
-    bp = ip & 3;
-    b_clo = 8 * bW + bp;
-    b_chi = b_clo + 4;
-    b_tig = bW >> 2;
-    b_kb = 2 * (bW & 3) + (bp >> 1);
+  // KIVI key operand: this lane builds channel pairs ip = lane and lane + 32
+  constexpr int kHalf = BITS == 2 ? 8 : 4;  // channel offset of the high half of a pair
+  int b_clo[2], b_sidx[2];
+  float qn_lo[2], qn_hi[2], qf_lo[2], qf_hi[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int ip = lane + 32 * r;
+    int W, p, tg, kb;
+    if (BITS == 2) {
+      W = ip >> 3;
+      p = ip & 7;
+      b_clo[r] = 16 * W + p;
+      tg = W >> 1;
+      kb = 4 * (W & 1) + (p >> 1);
+    } else {
+      W = ip >> 2;
+      p = ip & 3;
+      b_clo[r] = 8 * W + p;
+      tg = W >> 2;
+      kb = 2 * (W & 3) + (p >> 1);
+    }
+    b_sidx[r] = tg * 16 + kb * 2 + (p & 1);
+    qn_lo[r] = qn_hi[r] = qf_lo[r] = qf_hi[r] = 0.0f;
   }
-  b_reg = bp & 1;
-  float qn_lo = 0.f, qn_hi = 0.f, qf_lo = 0.f, qf_hi = 0.f;
   // InnerQ: fixed key operand and per-group sums of q
   uint32_t bqi[8][2];
   float Qj[NGK];
 
-  // ---- per-warp online-softmax state --------------------------------------
-  float m_run = -INFINITY, l_lane = 0.0f, z_lane[NGV];
-  float dv[8][4];
-  auto reset_state = [&]() {
-    m_run = -INFINITY;
-    l_lane = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NGV; ++j) z_lane[j] = 0.0f;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) dv[mt][r] = 0.0f;
-  };
-  reset_state();
-
-  auto start_head = [&](int64_t bh) {
-    const int b = (int)(bh / g.H), h = (int)(bh % g.H);
+  auto start_head = [&](int bh) {
+    const int b = bh / g.H, h = bh % g.H;
     float v = 0.0f;
     if (tid < kD) {
       v = __half2float(a.q[((int64_t)b * g.Hq + h) * kD + tid]) * a.scale_log2;
@@ -450,11 +470,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     pow2E = ldexpf(1.0f, E);
     const float inv = ldexpf(1.0f, -E);
     if (SCHEME == KVQ_KIVI) {
-      const float f = pos_factor<BITS>(bp);
-      qf_lo = sQf[b_clo];
-      qf_hi = sQf[b_chi];
-      qn_lo = qf_lo * inv / f;
-      qn_hi = qf_hi * inv / f;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int p = BITS == 2 ? (b_clo[r] & 7) : (b_clo[r] & 3);
+        const float invf = inv / pos_factor<BITS>(p);
+        qf_lo[r] = sQf[b_clo[r]];
+        qf_hi[r] = sQf[b_clo[r] + kHalf];
+        qn_lo[r] = qf_lo[r] * invf;
+        qn_hi[r] = qf_hi[r] * invf;
+      }
     } else {
       const int GK = kD / NGK;
 #pragma unroll
@@ -471,9 +495,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         for (int r = 0; r < 2; ++r) {
           int clo, chi, p;
           key_pair<BITS>(tig, kb, r, clo, chi, p);
-          const float f = pos_factor<BITS>(p);
-          const float vlo = (clo / GK == jn) ? sQf[clo] * inv / f : 0.0f;
-          const float vhi = (chi / GK == jn) ? sQf[chi] * inv / f : 0.0f;
+          const float invf = inv / pos_factor<BITS>(p);
+          const float vlo = (clo / GK == jn) ? sQf[clo] * invf : 0.0f;
+          const float vhi = (chi / GK == jn) ? sQf[chi] * invf : 0.0f;
           uint32_t hi, lo;
           split2(vlo, vhi, hi, lo);
           bqi[kb][r] = gid < 2 * NGK ? (part ? lo : hi) : 0u;
@@ -482,8 +506,24 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     __syncthreads();
   };
 
-  // Warp states -> one partial for head bh (slot = segment index).
-  auto flush = [&](int64_t bh) {
+  // ---- per-warp online-softmax state ----------------------------------------
+  float m_run = -INFINITY, l_lane = 0.0f, z_lane[NGV];
+  float dv[8][4];
+  auto reset_state = [&]() {
+    m_run = -INFINITY;
+    l_lane = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NGV; ++j) z_lane[j] = 0.0f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) dv[mt][r] = 0.0f;
+  };
+  reset_state();
+
+  // Warp state -> merge scratch.  Lanes hold one token each, so every lane
+  // counts.  Returns false when a warp of the block gave up (timeout).
+  auto flush = [&](int bh) -> bool {
     float l = l_lane;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
@@ -495,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
       Z[j] = z;
     }
-    float *ws = sScr + warp * (kD + 2);
+    float *ws = sScr + warp * kScrStride;
     const int gc = (gid * NGV) >> 3;  // value group of this thread's 16 channels
     if (tig == gc) {
       float zc = Z[0];
@@ -505,8 +545,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float invf = 1.0f / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
-        ws[2 + 16 * gid + mt] = (dv[mt][0] + dv[mt][1]) * invf + zc;
-        ws[2 + 16 * gid + 8 + mt] = (dv[mt][2] + dv[mt][3]) * invf + zc;
+        ws[2 + 16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
+        ws[2 + 16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
       }
     }
     if (lane == 0) {
@@ -514,264 +554,305 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       ws[1] = l;
     }
     __syncthreads();
-    float M = -INFINITY, L = 0.0f, O = 0.0f;
-    if (tid < kD) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sScr[w * (kD + 2)]);
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float mw = sScr[w * (kD + 2)];
-          if (mw == -INFINITY) continue;
-          const float s = exp2f(mw - M);
-          L += s * sScr[w * (kD + 2) + 1];
-          O += s * sScr[w * (kD + 2) + 2 + tid];
-        }
-      }
-    }
-    const int seg = (int)(blockIdx.x - owner_of(bh * a.U, a.total, a.nc));
-    publish(a, bh, seg, M, L, O, sFlag);
+    if (sFlag[0]) return false;
+    const int seg = (int)blockIdx.x - owner_of(bh * a.U, a.total, a.nc);
+    merge_and_publish(a, bh, seg, sScr, sFlag);
     reset_state();
+    return true;
   };
 
-  int qi = 0;
-  int64_t cur = -1;
-  bool seg_open = false;
-  bool aborted = false;
-  for (int64_t x = x0; x < x1; ++x) {
-    const int64_t bh = x / a.U;
-    const int u = (int)(x % a.U);
-    if (bh != cur) {
-      if (seg_open) flush(cur);
-      seg_open = false;
-      start_head(bh);
-      cur = bh;
-    }
-    if (u >= a.S_h) {
-      if (u == a.S_h) {
-        if (seg_open) flush(bh);
-        seg_open = false;
-        int nseg, nparts;
-        head_parts(a, bh, nseg, nparts);
-        fp16_item(a, bh, nseg, sQf, sScr, sFlag);
-      }
-      continue;
-    }
-    seg_open = true;
-    if (tid == 0) issue_next();
-    const int s = qi % kStages;
-    const uint8_t *slot = ring + s * a.slot_bytes;
-    bool ok = true;
-    if (qi == 0 && a.stall_limit > 0) ok = bar_wait(&bars[kStages], 0u, a.stall_limit);
-    if (!ok || !bar_wait(&bars[s], (uint32_t)((qi / kStages) & 1), a.wait_limit)) {
-      sFlag[0] = 1;
-      if (a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
-    }
-    const int n_stage = (int)min((int64_t)kTT, a.n_quant - (int64_t)u * kTT);
+  int ck = 0, done = 0;  // tiles visited / tiles whose copies completed
+  bool wabort = false;
+  bool stop = false;
+  for (int bh = bh_first; bh <= bh_last && !stop; ++bh) {
+    int tq0, tq1;
+    seg_of(bh, tq0, tq1);
+    const int base = bh * a.U;
+    const bool own_fp16 = a.F_h > 0 && x0 <= base + a.S_h && base + a.S_h < x1;
+    if (tq1 <= tq0 && !own_fp16) continue;
+    start_head(bh);
+    if (tq1 > tq0) {
+      const int nt = (tq1 - tq0 + kTile - 1) / kTile;
+      for (int lt = warp; lt < nt; lt += kWarps, ++ck) {
+        const int s = ck % nslot;
+        if (!wabort) {
+          bool ok = true;
+          if (ck == 0 && a.stall_limit > 0) ok = bar_wait(&bars[kWarps * nslot], 0u, a.stall_limit);
+          if (!ok || !bar_wait(&wbars[s], (uint32_t)((ck / nslot) & 1), a.wait_limit)) {
+            wabort = true;
+            sFlag[0] = 1;
+            if (a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+          } else {
+            ++done;
+          }
+        }
+        if (wabort) continue;
+        const uint8_t *slot = wring + s * a.slot_bytes;
+        const int tok0 = tq0 + kTile * lt;
+        const int n = min(kTile, tq1 - tok0);
+        const uint8_t *kc = slot;
+        const uint8_t *vc = slot + a.off_vc;
 
-    if (SCHEME == KVQ_KIVI) {
-      // q~ = q * scale (normalised, position factor divided out) as fp16
-      // hi/lo in the B-fragment order, and q . zero per group.
-      const int ngs = n_stage / g.k_group;
-      const float *ks = reinterpret_cast<const float *>(slot + a.off_ks);
-      const float *kz = reinterpret_cast<const float *>(slot + a.off_kz);
-      for (int it = tid; it < ngs * 64; it += kThreads) {
-        const int gl = it >> 6;
-        const float v_lo = qn_lo * ks[gl * kD + b_clo], v_hi = qn_hi * ks[gl * kD + b_chi];
-        uint32_t hi, lo;
-        split2(v_lo, v_hi, hi, lo);
-        uint32_t *dstB = sB + gl * 128;
-        dstB[(0 * 4 + b_tig) * 16 + b_kb * 2 + b_reg] = hi;
-        dstB[(1 * 4 + b_tig) * 16 + b_kb * 2 + b_reg] = lo;
-        float bz = fmaf(qf_lo, kz[gl * kD + b_clo], qf_hi * kz[gl * kD + b_chi]);
+        // ------------- keys: two 16-token MMA tiles ------------------------
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        float bias0 = 0.0f, bias1 = 0.0f;
+        uint32_t bk[8][2];
+        auto load_bk = [&](int gl) {
+          if (SCHEME == KVQ_KIVI) {
+            if (gid < 2) {
+              const uint4 *src = reinterpret_cast<const uint4 *>(sBw + gl * 128 + (gid * 4 + tig) * 16);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
-        if (lane == 0) sBias[gl * 2 + ((it >> 5) & 1)] = bz;
-      }
-    }
-    __syncthreads();
-    if (sFlag[0]) {
-      aborted = true;
-      break;
-    }
-
-    const int r0 = warp * 16;
-    if (r0 < n_stage) {
-      const uint8_t *kc = slot;
-      const uint8_t *vc = slot + a.off_vc;
-      // ---------------- keys: D[token][n] --------------------------------
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t bk[8][2];
-      if (SCHEME == KVQ_KIVI) {
-        const int gl = r0 / g.k_group;
-        if (gid < 2) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(sB + gl * 128 + (gid * 4 + tig) * 16);
+              for (int i = 0; i < 4; ++i) {
+                const uint4 v4 = src[i];
+                bk[2 * i][0] = v4.x;
+                bk[2 * i][1] = v4.y;
+                bk[2 * i + 1][0] = v4.z;
+                bk[2 * i + 1][1] = v4.w;
+              }
+            } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 v4 = src[i];
-            bk[2 * i][0] = v4.x;
-            bk[2 * i][1] = v4.y;
-            bk[2 * i + 1][0] = v4.z;
-            bk[2 * i + 1][1] = v4.w;
+              for (int kb = 0; kb < 8; ++kb) bk[kb][0] = bk[kb][1] = 0u;
+            }
+          } else {
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+              bk[kb][0] = bqi[kb][0];
+              bk[kb][1] = bqi[kb][1];
+            }
+          }
+        };
+        bool two_groups = false;
+        if (SCHEME == KVQ_KIVI) {
+          // q~ = q * scale (normalised, position factor divided out) as fp16
+          // hi/lo in B-fragment order, and q . zero, per key group of the tile
+          const float *ks = reinterpret_cast<const float *>(slot + a.off_ks);
+          const float *kz = reinterpret_cast<const float *>(slot + a.off_kz);
+          two_groups = g.k_group == 16 && n > 16;
+          const int ngb = two_groups ? 2 : 1;
+          for (int gl = 0; gl < ngb; ++gl) {
+            float bz = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int clo = b_clo[r], chi = b_clo[r] + kHalf;
+              uint32_t hi, lo;
+              split2(qn_lo[r] * ks[gl * kD + clo], qn_hi[r] * ks[gl * kD + chi], hi, lo);
+              sBw[gl * 128 + b_sidx[r]] = hi;
+              sBw[gl * 128 + 64 + b_sidx[r]] = lo;
+              bz = fmaf(qf_lo[r], kz[gl * kD + clo], fmaf(qf_hi[r], kz[gl * kD + chi], bz));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
+            if (gl == 0) bias0 = bz;
+            bias1 = bz;
+          }
+          __syncwarp();
+        }
+        load_bk(0);
+        if (BITS == 2) {
+          const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
+          const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
+          const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
+          const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
+          if (!two_groups) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
+              const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
+              const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
+              const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                mma16816(d0, ext<2>(w00, s00, 2 * j), ext<2>(w01, s01, 2 * j),
+                         ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1),
+                         bk[4 * m + j][0], bk[4 * m + j][1]);
+                mma16816(d1, ext<2>(w10, s10, 2 * j), ext<2>(w11, s11, 2 * j),
+                         ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1),
+                         bk[4 * m + j][0], bk[4 * m + j][1]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int t2 = 0; t2 < 2; ++t2) {
+              if (t2 == 1) load_bk(1);
+              const uint2 wa = t2 ? wa1 : wa0, wb = t2 ? wb1 : wb0;
+#pragma unroll
+              for (int m = 0; m < 2; ++m) {
+                const uint32_t w0 = m ? wa.y : wa.x, w1 = m ? wb.y : wb.x;
+                const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  if (t2 == 0)
+                    mma16816(d0, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
+                             ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
+                             bk[4 * m + j][0], bk[4 * m + j][1]);
+                  else
+                    mma16816(d1, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
+                             ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
+                             bk[4 * m + j][0], bk[4 * m + j][1]);
+                }
+              }
+            }
           }
         } else {
+          // 4-bit keys: G >= 32 always gives one key group per tile here
+          // (the 4-bit group-16 case takes the same path with two groups)
 #pragma unroll
-          for (int kb = 0; kb < 8; ++kb) bk[kb][0] = bk[kb][1] = 0u;
-        }
-      } else {
+          for (int t2 = 0; t2 < 2; ++t2) {
+            if (two_groups && t2 == 1) load_bk(1);
+            const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid) * RB + 16 * tig);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid + 8) * RB + 16 * tig);
+            const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          bk[kb][0] = bqi[kb][0];
-          bk[kb][1] = bqi[kb][1];
-        }
-      }
-      if (BITS == 2) {
-        const uint2 wa = *reinterpret_cast<const uint2 *>(kc + (r0 + gid) * RB + 8 * tig);
-        const uint2 wb = *reinterpret_cast<const uint2 *>(kc + (r0 + gid + 8) * RB + 8 * tig);
+            for (int m = 0; m < 4; ++m) {
+              const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          const uint32_t w0 = m ? wa.y : wa.x, w1 = m ? wb.y : wb.x;
-          const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            mma16816(d, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j), ext<2>(w0, s0, 2 * j + 1),
-                     ext<2>(w1, s1, 2 * j + 1), bk[4 * m + j][0], bk[4 * m + j][1]);
+              for (int j = 0; j < 2; ++j) {
+                if (t2 == 0)
+                  mma16816(d0, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
+                           ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
+                           bk[2 * m + j][0], bk[2 * m + j][1]);
+                else
+                  mma16816(d1, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
+                           ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
+                           bk[2 * m + j][0], bk[2 * m + j][1]);
+              }
+            }
           }
         }
-      } else {
-        const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (r0 + gid) * RB + 16 * tig);
-        const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (r0 + gid + 8) * RB + 16 * tig);
-        const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
+        // ------------- scores -> one token per lane ------------------------
+        float ra0, rb0, ra1, rb1;
+        if (SCHEME == KVQ_KIVI) {
+          ra0 = d0[0] + d0[1];
+          rb0 = d0[2] + d0[3];
+          ra1 = d1[0] + d1[1];
+          rb1 = d1[2] + d1[3];
+        } else {
+          const float *ks = reinterpret_cast<const float *>(slot + a.off_ks);
+          const float *kz = reinterpret_cast<const float *>(slot + a.off_kz);
+          const int jj = tig < NGK ? tig : NGK - 1;
+          float qj = Qj[0];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
+          for (int j = 1; j < NGK; ++j)
+            if (j == jj) qj = Qj[j];
+          auto term = [&](int row, float dd) {
+            return fmaf(ks[row * NGK + jj], dd * pow2E, kz[row * NGK + jj] * qj);
+          };
+          ra0 = term(gid, d0[0] + d0[1]);
+          rb0 = term(gid + 8, d0[2] + d0[3]);
+          ra1 = term(gid + 16, d1[0] + d1[1]);
+          rb1 = term(gid + 24, d1[2] + d1[3]);
+          if (tig >= NGK) ra0 = rb0 = ra1 = rb1 = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            mma16816(d, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                     ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
-                     bk[2 * m + j][0], bk[2 * m + j][1]);
+          for (int off = 1; off < NGK; off <<= 1) {
+            ra0 += __shfl_xor_sync(0xffffffffu, ra0, off);
+            rb0 += __shfl_xor_sync(0xffffffffu, rb0, off);
+            ra1 += __shfl_xor_sync(0xffffffffu, ra1, off);
+            rb1 += __shfl_xor_sync(0xffffffffu, rb1, off);
           }
         }
-      }
-      // ---------------- scores -> one token per lane (t = lane & 15) ------
-      float ra, rb;
-      if (SCHEME == KVQ_KIVI) {
-        ra = d[0] + d[1];
-        rb = d[2] + d[3];
-      } else {
-        const float *ks = reinterpret_cast<const float *>(slot + a.off_ks);
-        const float *kz = reinterpret_cast<const float *>(slot + a.off_kz);
-        const int jj = tig < NGK ? tig : NGK - 1;
-        float qj = Qj[0];
+        const int t = lane;
+        const int src = 4 * (t & 7);
+        const float xa0 = __shfl_sync(0xffffffffu, ra0, src), xb0 = __shfl_sync(0xffffffffu, rb0, src);
+        const float xa1 = __shfl_sync(0xffffffffu, ra1, src), xb1 = __shfl_sync(0xffffffffu, rb1, src);
+        float score = t < 16 ? ((t & 8) ? xb0 : xa0) : ((t & 8) ? xb1 : xa1);
+        if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
+        const bool valid = t < n;
+        score = valid ? score : -INFINITY;
+        float mt_ = score;
 #pragma unroll
-        for (int j = 1; j < NGK; ++j)
-          if (j == jj) qj = Qj[j];
-        ra = fmaf(ks[(r0 + gid) * NGK + jj], (d[0] + d[1]) * pow2E, kz[(r0 + gid) * NGK + jj] * qj);
-        rb = fmaf(ks[(r0 + gid + 8) * NGK + jj], (d[2] + d[3]) * pow2E,
-                  kz[(r0 + gid + 8) * NGK + jj] * qj);
-        if (tig >= NGK) ra = rb = 0.0f;
+        for (int off = 1; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
+        if (mt_ > m_run) {
+          const float alpha = exp2f(m_run - mt_);
+          l_lane *= alpha;
 #pragma unroll
-        for (int off = 1; off < NGK; off <<= 1) {
-          ra += __shfl_xor_sync(0xffffffffu, ra, off);
-          rb += __shfl_xor_sync(0xffffffffu, rb, off);
+          for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
+          m_run = mt_;
         }
-      }
-      const int t = lane & 15;
-      const float xa = __shfl_sync(0xffffffffu, ra, 4 * (t & 7));
-      const float xb = __shfl_sync(0xffffffffu, rb, 4 * (t & 7));
-      float score = (t & 8) ? xb : xa;
-      if (SCHEME == KVQ_KIVI) {
-        const int gl = r0 / g.k_group;
-        score = fmaf(score, pow2E, sBias[gl * 2] + sBias[gl * 2 + 1]);
-      }
-      const bool valid = r0 + t < n_stage;
-      score = valid ? score : -INFINITY;
-      float mt_ = score;
+        const float p = exp2f(score - m_run);
+        l_lane += p;
+        {
+          const float *vz = reinterpret_cast<const float *>(slot + a.off_vz);
 #pragma unroll
-      for (int off = 1; off < 16; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
-      if (mt_ > m_run) {
-        const float alpha = exp2f(m_run - mt_);
-        l_lane *= alpha;
-#pragma unroll
-        for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
-        m_run = mt_;
-      }
-      const float p = exp2f(score - m_run);
-      const float pc = (lane < 16 && valid) ? p : 0.0f;
-      l_lane += pc;
-      {
-        const float *vz = reinterpret_cast<const float *>(slot + a.off_vz);
-#pragma unroll
-        for (int j = 0; j < NGV; ++j)
-          z_lane[j] = pc > 0.0f ? fmaf(pc, vz[(r0 + t) * NGV + j], z_lane[j]) : z_lane[j];
-      }
-      // ---------------- values: B = p * scale (hi/lo), A = codes ----------
-      const float *vs = reinterpret_cast<const float *>(slot + a.off_vs);
-      const int jg = (gid >> 1) < NGV ? (gid >> 1) : NGV - 1;
-      const int tk0 = 2 * tig, tk1 = 2 * tig + 1, tk2 = 2 * tig + 8, tk3 = 2 * tig + 9;
-      const float p0 = __shfl_sync(0xffffffffu, p, tk0), p1 = __shfl_sync(0xffffffffu, p, tk1);
-      const float p2 = __shfl_sync(0xffffffffu, p, tk2), p3 = __shfl_sync(0xffffffffu, p, tk3);
-      const float x0 = p0 > 0.0f ? p0 * vs[(r0 + tk0) * NGV + jg] : 0.0f;
-      const float x1 = p1 > 0.0f ? p1 * vs[(r0 + tk1) * NGV + jg] : 0.0f;
-      const float x2 = p2 > 0.0f ? p2 * vs[(r0 + tk2) * NGV + jg] : 0.0f;
-      const float x3 = p3 > 0.0f ? p3 * vs[(r0 + tk3) * NGV + jg] : 0.0f;
-      uint32_t h01, l01, h23, l23;
-      split2(x0, x1, h01, l01);
-      split2(x2, x3, h23, l23);
-      const bool bact = gid < 2 * NGV;
-      const uint32_t bv0 = bact ? ((gid & 1) ? l01 : h01) : 0u;
-      const uint32_t bv1 = bact ? ((gid & 1) ? l23 : h23) : 0u;
-      if (BITS == 2) {
-        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + (r0 + tk0) * RB + 4 * gid);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + (r0 + tk1) * RB + 4 * gid);
-        const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vc + (r0 + tk2) * RB + 4 * gid);
-        const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vc + (r0 + tk3) * RB + 4 * gid);
-        const uint32_t xa_ = __byte_perm(w0, w1, 0x5410), ya_ = __byte_perm(w0, w1, 0x7632);
-        const uint32_t xb_ = __byte_perm(w2, w3, 0x5410), yb_ = __byte_perm(w2, w3, 0x7632);
-        const uint32_t xas = shifted<2>(xa_), yas = shifted<2>(ya_);
-        const uint32_t xbs = shifted<2>(xb_), ybs = shifted<2>(yb_);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-          mma16816(dv[mt], ext<2>(xa_, xas, mt), ext<2>(ya_, yas, mt), ext<2>(xb_, xbs, mt),
-                   ext<2>(yb_, ybs, mt), bv0, bv1);
-      } else {
-        const uint2 w0 = *reinterpret_cast<const uint2 *>(vc + (r0 + tk0) * RB + 8 * gid);
-        const uint2 w1 = *reinterpret_cast<const uint2 *>(vc + (r0 + tk1) * RB + 8 * gid);
-        const uint2 w2 = *reinterpret_cast<const uint2 *>(vc + (r0 + tk2) * RB + 8 * gid);
-        const uint2 w3 = *reinterpret_cast<const uint2 *>(vc + (r0 + tk3) * RB + 8 * gid);
-        // [0]: channels 16gid+0..3, [1]: +4..7, [2]: +8..11, [3]: +12..15
-        const uint32_t xa4[4] = {__byte_perm(w0.x, w1.x, 0x5410), __byte_perm(w0.x, w1.x, 0x7632),
-                                 __byte_perm(w0.y, w1.y, 0x5410), __byte_perm(w0.y, w1.y, 0x7632)};
-        const uint32_t xb4[4] = {__byte_perm(w2.x, w3.x, 0x5410), __byte_perm(w2.x, w3.x, 0x7632),
-                                 __byte_perm(w2.y, w3.y, 0x5410), __byte_perm(w2.y, w3.y, 0x7632)};
-        uint32_t sa4[4], sb4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          sa4[i] = shifted<4>(xa4[i]);
-          sb4[i] = shifted<4>(xb4[i]);
+          for (int j = 0; j < NGV; ++j)
+            z_lane[j] = p > 0.0f ? fmaf(p, vz[t * NGV + j], z_lane[j]) : z_lane[j];
         }
+        // ------------- values: B = p * scale (hi/lo), A = codes ------------
+        const float *vs = reinterpret_cast<const float *>(slot + a.off_vs);
+        const int jg = (gid >> 1) < NGV ? (gid >> 1) : NGV - 1;
+        const bool bact = gid < 2 * NGV;
+        const int nkb = n > 16 ? 2 : 1;
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int tk0 = 16 * kb + 2 * tig, tk1 = tk0 + 1, tk2 = tk0 + 8, tk3 = tk0 + 9;
+          const float p0 = __shfl_sync(0xffffffffu, p, tk0), p1 = __shfl_sync(0xffffffffu, p, tk1);
+          const float p2 = __shfl_sync(0xffffffffu, p, tk2), p3 = __shfl_sync(0xffffffffu, p, tk3);
+          const float x0 = p0 > 0.0f ? p0 * vs[tk0 * NGV + jg] : 0.0f;
+          const float x1 = p1 > 0.0f ? p1 * vs[tk1 * NGV + jg] : 0.0f;
+          const float x2 = p2 > 0.0f ? p2 * vs[tk2 * NGV + jg] : 0.0f;
+          const float x3 = p3 > 0.0f ? p3 * vs[tk3 * NGV + jg] : 0.0f;
+          uint32_t h01, l01, h23, l23;
+          split2(x0, x1, h01, l01);
+          split2(x2, x3, h23, l23);
+          const uint32_t bv0 = bact ? ((gid & 1) ? l01 : h01) : 0u;
+          const uint32_t bv1 = bact ? ((gid & 1) ? l23 : h23) : 0u;
+          if (BITS == 2) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * gid);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * gid);
+            const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vc + tk2 * RB + 4 * gid);
+            const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vc + tk3 * RB + 4 * gid);
+            const uint32_t xa_ = __byte_perm(w0, w1, 0x5410), ya_ = __byte_perm(w0, w1, 0x7632);
+            const uint32_t xb_ = __byte_perm(w2, w3, 0x5410), yb_ = __byte_perm(w2, w3, 0x7632);
+            const uint32_t xas = shifted<2>(xa_), yas = shifted<2>(ya_);
+            const uint32_t xbs = shifted<2>(xb_), ybs = shifted<2>(yb_);
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int lo = mt < 4 ? 0 : 1, hi = mt < 4 ? 2 : 3, pos = mt & 3;
-          mma16816(dv[mt], ext<4>(xa4[lo], sa4[lo], pos), ext<4>(xa4[hi], sa4[hi], pos),
-                   ext<4>(xb4[lo], sb4[lo], pos), ext<4>(xb4[hi], sb4[hi], pos), bv0, bv1);
+            for (int mt = 0; mt < 8; ++mt)
+              mma16816(dv[mt], ext<2>(xa_, xas, mt), ext<2>(ya_, yas, mt), ext<2>(xb_, xbs, mt),
+                       ext<2>(yb_, ybs, mt), bv0, bv1);
+          } else {
+            const uint2 w0 = *reinterpret_cast<const uint2 *>(vc + tk0 * RB + 8 * gid);
+            const uint2 w1 = *reinterpret_cast<const uint2 *>(vc + tk1 * RB + 8 * gid);
+            const uint2 w2 = *reinterpret_cast<const uint2 *>(vc + tk2 * RB + 8 * gid);
+            const uint2 w3 = *reinterpret_cast<const uint2 *>(vc + tk3 * RB + 8 * gid);
+            // [0]: channels 16gid+0..3, [1]: +4..7, [2]: +8..11, [3]: +12..15
+            const uint32_t xa4[4] = {__byte_perm(w0.x, w1.x, 0x5410), __byte_perm(w0.x, w1.x, 0x7632),
+                                     __byte_perm(w0.y, w1.y, 0x5410), __byte_perm(w0.y, w1.y, 0x7632)};
+            const uint32_t xb4[4] = {__byte_perm(w2.x, w3.x, 0x5410), __byte_perm(w2.x, w3.x, 0x7632),
+                                     __byte_perm(w2.y, w3.y, 0x5410), __byte_perm(w2.y, w3.y, 0x7632)};
+            uint32_t sa4[4], sb4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              sa4[i] = shifted<4>(xa4[i]);
+              sb4[i] = shifted<4>(xb4[i]);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              const int lo = mt < 4 ? 0 : 1, hi = mt < 4 ? 2 : 3, pos = mt & 3;
+              mma16816(dv[mt], ext<4>(xa4[lo], sa4[lo], pos), ext<4>(xa4[hi], sa4[hi], pos),
+                       ext<4>(xb4[lo], sb4[lo], pos), ext<4>(xb4[hi], sb4[hi], pos), bv0, bv1);
+            }
+          }
         }
+        __syncwarp();
+        if (lane == 0) issue_next();  // refill the slot just consumed
+      }
+      if (!flush(bh)) {
+        stop = true;
+        break;
       }
     }
-    __syncthreads();
-    ++qi;
+    if (own_fp16) {
+      int nseg, nparts;
+      head_parts(a, bh, nseg, nparts);
+      fp16_item(a, bh, nseg, sQf, sScr, sFlag);
+    }
   }
-  if (aborted) {
-    if (tid == 0)
-      for (int i = qi; i < issued; ++i)
-        bar_wait(&bars[i % kStages], (uint32_t)((i / kStages) & 1), kDrainLimit);
-    return;
-  }
-  if (seg_open) flush(cur);
+  // copies still in flight (only after a timeout) complete before exit
+  if (lane == 0)
+    for (int i = done; i < issued; ++i)
+      bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
 }
 
 template <int BITS, int SCHEME, int NGV, int NGK>
@@ -802,12 +883,12 @@ cudaError_t launch_tc_v(TcArgs &a, int smem, int num_sms, cudaStream_t st) {
     return ngv == 4 ? launch_tc_t<BITS, SCHEME, 4, 1>(a, smem, num_sms, st)
                     : launch_tc_t<BITS, SCHEME, 2, 1>(a, smem, num_sms, st);
   } else {
-  const int ngk = kD / a.g.k_group;
-  if (ngv == 4)
-    return ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4>(a, smem, num_sms, st)
-                    : launch_tc_t<BITS, SCHEME, 4, 2>(a, smem, num_sms, st);
-  return ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4>(a, smem, num_sms, st)
-                  : launch_tc_t<BITS, SCHEME, 2, 2>(a, smem, num_sms, st);
+    const int ngk = kD / a.g.k_group;
+    if (ngv == 4)
+      return ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4>(a, smem, num_sms, st)
+                      : launch_tc_t<BITS, SCHEME, 4, 2>(a, smem, num_sms, st);
+    return ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4>(a, smem, num_sms, st)
+                    : launch_tc_t<BITS, SCHEME, 2, 2>(a, smem, num_sms, st);
   }
 }
 
@@ -840,19 +921,27 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.n_sink = n_sink;
   const int RB = kD * g.bits / 8;
   const int ngv = kD / g.v_group;
-  const int kmb = g.scheme == KVQ_KIVI ? (kTT / g.k_group) * kD * 4 : kTT * (kD / g.k_group) * 4;
-  const int vmb = kTT * ngv * 4;
-  a.off_vc = kTT * RB;
-  a.off_ks = 2 * kTT * RB;
+  const int kmb = g.scheme == KVQ_KIVI ? (g.k_group == 16 ? 2 : 1) * kD * 4
+                                       : kTile * (kD / g.k_group) * 4;
+  const int vmb = kTile * ngv * 4;
+  a.off_vc = kTile * RB;
+  a.off_ks = 2 * kTile * RB;
   a.off_kz = a.off_ks + kmb;
   a.off_vs = a.off_kz + kmb;
   a.off_vz = a.off_vs + vmb;
   a.slot_bytes = (a.off_vz + vmb + 127) & ~127;
-  a.S_h = (int)((n_quant + kTT - 1) / kTT);
-  const int64_t payload = 2LL * kTT * RB + 2 * kmb + 2 * vmb;
-  a.F_h = a.n_fp16 > 0 ? (int)((a.n_fp16 * kD * 2 * 2 * 2 + payload - 1) / payload) : 0;
+  a.nslot = tc_layout(a.slot_bytes, 3).total <= 110 * 1024 ? 3 : 2;
+  a.S_h = (int)((n_quant + kUnit - 1) / kUnit);
+  // fp16 item weight in units: its bytes against a unit's bytes, x2 for the
+  // CUDA-core path
+  const int64_t unit_bytes = 2LL * kUnit * RB + 2LL * kUnit * ngv * 4 +
+                             (g.scheme == KVQ_KIVI ? 2LL * (kUnit / g.k_group) * kD * 4
+                                                   : 2LL * kUnit * (kD / g.k_group) * 4);
+  a.F_h = a.n_fp16 > 0 ? (int)((a.n_fp16 * kD * 2 * 2 * 2 + unit_bytes - 1) / unit_bytes) : 0;
   a.U = a.S_h + a.F_h;
-  a.total = (int64_t)g.B * g.H * a.U;
+  const int64_t total = (int64_t)g.B * g.H * a.U;
+  if (total >= (1LL << 31)) return cudaErrorInvalidValue;
+  a.total = (int)total;
   a.part_stride = part_slots(g);
   const int64_t BH = (int64_t)g.B * g.H;
   char *base = static_cast<char *>(ws);
@@ -862,7 +951,7 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * 2;
   a.wait_limit = 1LL << 24;
   a.stall_limit = g_stall_limit;
-  const int smem = tc_layout(a.slot_bytes).total;
+  const int smem = tc_layout(a.slot_bytes, a.nslot).total;
   if (g.bits == 2)
     return g.scheme == KVQ_KIVI ? launch_tc_v<2, KVQ_KIVI>(a, smem, num_sms, st)
                                 : launch_tc_v<2, KVQ_INNERQ>(a, smem, num_sms, st);
