@@ -410,8 +410,11 @@ int s_max_of(const Geometry &g) { return part_slots(g); }
 }  // namespace
 
 size_t decode_workspace_bytes(const Geometry &g) {
+  // the larger of the two decode paths' partial arrays
   const int64_t BH = (int64_t)g.B * g.H, rg = g.Hq / g.H;
-  const int64_t parts = BH * s_max_of(g) * rg;
+  int64_t parts = BH * s_max_of(g) * rg;
+  const int64_t tc_parts = BH * tc_part_slots(g);
+  if (tc_parts > parts) parts = tc_parts;
   size_t cnt = ((size_t)BH * sizeof(int) + 255) & ~(size_t)255;
   return cnt + (size_t)parts * 2 * sizeof(float) + (size_t)parts * g.d * sizeof(float) + 256;
 }

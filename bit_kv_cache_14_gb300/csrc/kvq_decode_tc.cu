@@ -37,6 +37,8 @@
 //    can overflow (|q| <= 1, scales <= 65504).
 #include <math.h>
 
+#include <type_traits>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -48,9 +50,9 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kUnit = 128;    // tokens per stream-K work unit
 constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
 constexpr int kD = 128;
-constexpr int kScrStride = kD + 4;        // floats per warp in the merge scratch
+constexpr int kSBWords = 2 * 128 + 16;  // per-warp key operands (2 groups) + a zero block
 constexpr uint32_t kMagic = 0x64006400u;  // half2(1024, 1024)
-constexpr long long kDrainLimit = 1LL << 26;
+constexpr int kDrainLimit = 1 << 26;
 
 struct TcArgs {
   Geometry g;
@@ -62,30 +64,42 @@ struct TcArgs {
   int S_h, F_h, U;  // quantized units, fp16 units, units per head
   int total;        // BH * U
   int nc;           // resident blocks
-  int nslot;        // ring slots per warp
-  int slot_bytes, off_vc, off_ks, off_kz, off_vs, off_vz;
   float *ws_ml, *ws_o;
   int *ws_cnt;
   int part_stride;
-  long long wait_limit;   // poll cap of every pipeline wait
-  long long stall_limit;  // debug: > 0 = first wait on a barrier nothing completes
+  int wait_limit;   // poll cap of every pipeline wait
+  int stall_limit;  // debug: > 0 = first wait on a barrier nothing completes
 };
 
 struct TcLayout {
-  int ring, sB, sQf, sScr, sFlag, bars, total;
+  int ring, sB, bars, total;
 };
 
-__host__ __device__ inline TcLayout tc_layout(int slot_bytes, int nslot) {
-  TcLayout L;
+__host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot) {
+  TcLayout L{};
   L.ring = 0;
-  L.sB = L.ring + kWarps * nslot * slot_bytes;  // per warp: 2 key groups x 128 u32
-  L.sQf = L.sB + kWarps * 2 * 128 * 4;          // [128] floats
-  L.sScr = L.sQf + kD * 4;                      // [warps][kScrStride] floats
-  L.sFlag = L.sScr + kWarps * kScrStride * 4;   // [16] ints / floats
-  L.bars = L.sFlag + 16 * 4;                    // warps * nslot + 1 mbarriers
-  L.total = L.bars + (kWarps * nslot + 1) * 8;
+  L.sB = L.ring + kWarps * nslot * slot_bytes;  // per warp: 2 key groups x 128 u32 + 16 zeros
+  L.bars = L.sB + kWarps * kSBWords * 4;        // per warp: nslot + 1 mbarriers
+  L.total = L.bars + kWarps * (nslot + 1) * 8;
   return L;
 }
+
+// Compile-time layout of one warp-ring slot (one 32-token tile): K codes,
+// V codes, K scale, K zero, V scale, V zero.
+template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
+struct SlotCfg {
+  static constexpr int RB = kD * BITS / 8;
+  static constexpr int KMB = SCHEME == KVQ_KIVI ? (G16 ? 2 : 1) * kD * 4 : kTile * NGK * 4;
+  static constexpr int VMB = kTile * NGV * 4;
+  static constexpr int off_vc = kTile * RB;
+  static constexpr int off_ks = 2 * kTile * RB;
+  static constexpr int off_kz = off_ks + KMB;
+  static constexpr int off_vs = off_kz + KMB;
+  static constexpr int off_vz = off_vs + VMB;
+  static constexpr int bytes = (off_vz + VMB + 127) & ~127;
+  static constexpr int nslot = tc_layout(bytes, 3).total <= 110 * 1024 ? 3 : 2;
+  static constexpr int smem = tc_layout(bytes, nslot).total;
+};
 
 
 // ---- PTX helpers --------------------------------------------------------
@@ -115,11 +129,11 @@ __device__ __forceinline__ bool bar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, long long limit) {
-  for (long long it = 0;; ++it) {
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, int limit) {
+  if (bar_try_wait(bar, parity)) return true;
+  for (int it = 0; it < limit; ++it)
     if (bar_try_wait(bar, parity)) return true;
-    if (it >= limit) return false;
-  }
+  return false;
 }
 
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
@@ -170,7 +184,7 @@ __host__ __device__ __forceinline__ float pos_factor(int p) {
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -208,156 +222,93 @@ __device__ __forceinline__ int owner_of(int x, int total, int nc) {
   return (int)(((int64_t)(x + 1) * nc - 1) / total);
 }
 
-// Number of quantized-segment partials of head bh and the total partial count
-// (the fp16 partial, if any, has index nseg).
+// Quantized segments of head bh (one per block touching its quantized units)
+// and the head's partial count: every warp of every such block leaves one
+// partial, and so does every warp of the block owning the fp16 item.
 __device__ __forceinline__ void head_parts(const TcArgs &a, int bh, int &nseg, int &nparts) {
   const int base = bh * a.U;
   nseg = a.S_h > 0 ? owner_of(base + a.S_h - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1
                    : 0;
-  nparts = nseg + (a.F_h > 0 ? 1 : 0);
+  nparts = kWarps * (nseg + (a.F_h > 0 ? 1 : 0));
 }
 
-// Threads 0..127 hold (M, L, O_c) of one partial of head bh; publish it, take
-// a ticket, and let the last block of the head merge all of its partials.
-__device__ void publish(const TcArgs &a, int bh, int slot, float M, float L, float O,
-                        int *sflag) {
-  const int tid = threadIdx.x;
-  const int64_t pi = (int64_t)bh * a.part_stride + slot;
-  if (tid < kD) a.ws_o[pi * kD + tid] = O;
-  if (tid == 0) {
-    a.ws_ml[pi * 2] = M;
-    a.ws_ml[pi * 2 + 1] = L;
+// One warp publishes partial `slot` of head bh (its o values are already
+// stored), takes a ticket, and if it is the head's last partial, merges all
+// of them with the log-sum-exp rule and writes the output row.
+__device__ void warp_publish(const TcArgs &a, int bh, int slot, float m, float l) {
+  const int lane = threadIdx.x & 31;
+  const int64_t base = (int64_t)bh * a.part_stride;
+  if (lane == 0) {
+    a.ws_ml[(base + slot) * 2] = m;
+    a.ws_ml[(base + slot) * 2 + 1] = l;
   }
   int nseg, nparts;
   head_parts(a, bh, nseg, nparts);
   __threadfence();
-  __syncthreads();
-  if (tid == 0) sflag[1] = atomicAdd(&a.ws_cnt[bh], 1) == nparts - 1;
-  __syncthreads();
-  if (sflag[1]) {
-    __threadfence();
-    if (tid < kD) {
-      const int64_t base = (int64_t)bh * a.part_stride;
-      float Mx = -INFINITY;
-      for (int s = 0; s < nparts; ++s) Mx = fmaxf(Mx, __ldcg(&a.ws_ml[(base + s) * 2]));
-      float Ls = 0.0f, Os = 0.0f;
-      if (Mx != -INFINITY) {
-        for (int s = 0; s < nparts; ++s) {
-          const float ms = __ldcg(&a.ws_ml[(base + s) * 2]);
-          if (ms == -INFINITY) continue;
-          const float w = exp2f(ms - Mx);
-          Ls += w * __ldcg(&a.ws_ml[(base + s) * 2 + 1]);
-          Os += w * __ldcg(&a.ws_o[(base + s) * kD + tid]);
-        }
-      }
-      const int b = bh / a.g.H, h = bh % a.g.H;
-      a.out[((int64_t)b * a.g.Hq + h) * kD + tid] = Ls > 0.0f ? Os / Ls : 0.0f;
-    }
-    if (tid == 0) a.ws_cnt[bh] = 0;
-  }
-  __syncthreads();
-}
-
-// Every warp has written (m, l, o[128]) to scr; merge them (block-wide) and
-// publish the result as partial `slot` of head bh.
-__device__ void merge_and_publish(const TcArgs &a, int bh, int slot, const float *scr,
-                                  int *sflag) {
-  const int tid = threadIdx.x;
-  float M = -INFINITY, L = 0.0f, O = 0.0f;
-  if (tid < kD) {
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(&a.ws_cnt[bh], 1) == nparts - 1;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  float Mx = -INFINITY;
+  for (int s = lane; s < nparts; s += 32) Mx = fmaxf(Mx, __ldcg(&a.ws_ml[(base + s) * 2]));
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, scr[w * kScrStride]);
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = scr[w * kScrStride];
-        if (mw == -INFINITY) continue;
-        const float s = exp2f(mw - M);
-        L += s * scr[w * kScrStride + 1];
-        O += s * scr[w * kScrStride + 2 + tid];
-      }
+  for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+  float Ls = 0.0f, O[4] = {0.f, 0.f, 0.f, 0.f};
+  if (Mx != -INFINITY) {
+    for (int s = 0; s < nparts; ++s) {
+      const float ms = __ldcg(&a.ws_ml[(base + s) * 2]);
+      if (ms == -INFINITY) continue;
+      const float w = exp2f(ms - Mx);
+      Ls = fmaf(w, __ldcg(&a.ws_ml[(base + s) * 2 + 1]), Ls);
+      const float4 o = __ldcg(reinterpret_cast<const float4 *>(a.ws_o + (base + s) * kD) + lane);
+      O[0] = fmaf(w, o.x, O[0]);
+      O[1] = fmaf(w, o.y, O[1]);
+      O[2] = fmaf(w, o.z, O[2]);
+      O[3] = fmaf(w, o.w, O[3]);
     }
   }
-  publish(a, bh, slot, M, L, O, sflag);
+  const int b = bh / a.g.H, h = bh % a.g.H;
+  const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+  float4 r;
+  r.x = O[0] * inv;
+  r.y = O[1] * inv;
+  r.z = O[2] * inv;
+  r.w = O[3] * inv;
+  reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h) * kD)[lane] = r;
+  if (lane == 0) a.ws_cnt[bh] = 0;
 }
 
-// fp16 sink + residual / window tokens of head bh (<= 2048): each warp takes
-// every 8th token with its own online softmax (a lane owns 4 channels), then
-// the warps are merged and published as partial `slot`.
-__device__ void fp16_item(const TcArgs &a, int bh, int slot, const float *sQf, float *scr,
-                          int *sflag) {
-  const Geometry &g = a.g;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = (int)a.n_fp16, ns = (int)a.n_sink;
-  float q4[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) q4[j] = sQf[4 * lane + j];
-  float m = -INFINITY, l = 0.0f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int i = warp; i < n; i += kWarps) {
-    const int64_t kr = i < ns ? ((int64_t)bh * g.n_sink + i) : ((int64_t)bh * g.residual + (i - ns));
-    const __half *krow = (i < ns ? a.p.k_sink : a.p.k_res) + kr * kD;
-    const __half *vrow = (i < ns ? a.p.v_sink : a.p.v_res) + kr * kD;
-    const uint2 kw = __ldg(reinterpret_cast<const uint2 *>(krow) + lane);
-    const uint2 vw = __ldg(reinterpret_cast<const uint2 *>(vrow) + lane);
-    const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
-    const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
-    const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
-    const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
-    float s = fmaf(q4[0], k01.x, fmaf(q4[1], k01.y, fmaf(q4[2], k23.x, q4[3] * k23.y)));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    const float mn = fmaxf(m, s);
-    const float al = exp2f(m - mn), p = exp2f(s - mn);
-    l = fmaf(l, al, p);
-    acc[0] = fmaf(acc[0], al, p * v01.x);
-    acc[1] = fmaf(acc[1], al, p * v01.y);
-    acc[2] = fmaf(acc[2], al, p * v23.x);
-    acc[3] = fmaf(acc[3], al, p * v23.y);
-    m = mn;
-  }
-  float *ws = scr + warp * kScrStride;
-  if (lane == 0) {
-    ws[0] = m;
-    ws[1] = l;
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) ws[2 + 4 * lane + j] = acc[j];
-  __syncthreads();
-  merge_and_publish(a, bh, slot, scr, sflag);
-}
-
-template <int BITS, int SCHEME, int NGV, int NGK>
+template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
 __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  constexpr int RB = kD * BITS / 8;  // packed bytes per token row
+  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, G16>;
+  constexpr int RB = SC::RB;  // packed bytes per token row
+  constexpr int nslot = SC::nslot;
+  constexpr int SLOT = SC::bytes;
   const Geometry &g = a.g;
-  const int nslot = a.nslot;
-  const TcLayout Ly = tc_layout(a.slot_bytes, nslot);
-  float *sQf = reinterpret_cast<float *>(smem + Ly.sQf);
-  float *sScr = reinterpret_cast<float *>(smem + Ly.sScr);
-  int *sFlag = reinterpret_cast<int *>(smem + Ly.sFlag);
-  float *sFlagF = reinterpret_cast<float *>(smem + Ly.sFlag);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Ly.bars);
+  constexpr TcLayout Ly = tc_layout(SLOT, nslot);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-  uint8_t *wring = smem + Ly.ring + warp * nslot * a.slot_bytes;
-  uint64_t *wbars = bars + warp * nslot;
-  uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB) + warp * 256;
+  uint8_t *wring = smem + Ly.ring + warp * nslot * SLOT;
+  uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
+  uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB) + warp * kSBWords;
 
   const int x0 = (int)((int64_t)blockIdx.x * a.total / a.nc);
   const int x1 = (int)((int64_t)(blockIdx.x + 1) * a.total / a.nc);
   const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
 
-  // zero the rings once so stale bytes are always finite; barriers
-  for (int i = tid; i < kWarps * nslot * a.slot_bytes / 16; i += kThreads)
-    reinterpret_cast<uint4 *>(smem + Ly.ring)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) {
-    for (int s = 0; s <= kWarps * nslot; ++s) bar_init(&bars[s], 1);
-    sFlag[0] = 0;
+  // Each warp owns its ring and barriers; nothing below synchronises warps.
+  for (int i = lane; i < nslot * SLOT / 16; i += 32)
+    reinterpret_cast<uint4 *>(wring)[i] = make_uint4(0, 0, 0, 0);
+  if (lane < 16) sBw[256 + lane] = 0u;
+  if (lane == 0) {
+    for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncthreads();
+  __syncwarp();
 
   // quantized token range [tq0, tq1) of head bh inside this block's units
   auto seg_of = [&](int bh, int &tq0, int &tq1) {
@@ -368,9 +319,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     tq1 = ua < ub ? (int)min((int64_t)ub * kUnit, a.n_quant) : tq0;
   };
 
-  // ---- producer (lane 0 of each warp): this warp's tiles, in the order the
-  // consumer loop below visits them ------------------------------------------
-  int pc_bh = -1, pc_tq0 = 0, pc_tq1 = 0, pc_lt = 0, issued = 0;
+  // ---- producer: this warp's tiles in the order the consumer visits them --
+  int pc_bh = -1, pc_tq0 = 0, pc_tq1 = 0, pc_lt = 0, issued = 0, ps = 0;
   auto pc_settle = [&]() {
     while (pc_bh >= 0 && pc_tq0 + kTile * pc_lt >= pc_tq1) {
       if (++pc_bh > bh_last) {
@@ -381,49 +331,56 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       pc_lt = warp;
     }
   };
+  // Called by the whole warp: lane 0 posts the byte count, lanes 0..5 each
+  // issue one of the six copies of the next tile of this warp.
   auto issue_next = [&]() {
     if (pc_bh < 0) return;
     const int tok0 = pc_tq0 + kTile * pc_lt;
     const int n = min(kTile, pc_tq1 - tok0);
-    const int s = issued % nslot;
-    uint8_t *dst = wring + s * a.slot_bytes;
-    uint64_t *bar = &wbars[s];
+    uint8_t *dst = wring + ps * SLOT;
+    uint64_t *bar = &wbars[ps];
+    ps = ps + 1 == nslot ? 0 : ps + 1;
     const int64_t row0 = (int64_t)pc_bh * g.cap + tok0;
     const uint32_t cb = (uint32_t)(n * RB);
     const uint32_t vmb = (uint32_t)((n * NGV * 4 + 15) & ~15);
     uint32_t kmb;
-    const float *ks, *kz;
+    int64_t krow;
     if (SCHEME == KVQ_KIVI) {
-      const int g0 = tok0 / g.k_group, g1 = (tok0 + n - 1) / g.k_group;
-      kmb = (uint32_t)((g1 - g0 + 1) * kD * 4);
-      ks = a.p.k_scale + ((int64_t)pc_bh * g.k_meta_rows + g0) * kD;
-      kz = a.p.k_zero + ((int64_t)pc_bh * g.k_meta_rows + g0) * kD;
+      kmb = (uint32_t)((G16 && n > 16 ? 2 : 1) * kD * 4);
+      krow = ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * kD;
     } else {
       kmb = (uint32_t)((n * NGK * 4 + 15) & ~15);
-      ks = a.p.k_scale + row0 * NGK;
-      kz = a.p.k_zero + row0 * NGK;
+      krow = row0 * NGK;
     }
-    bar_expect_tx(bar, 2 * cb + 2 * kmb + 2 * vmb);
-    bulk_g2s(dst, a.p.k_codes + row0 * RB, cb, bar);
-    bulk_g2s(dst + a.off_vc, a.p.v_codes + row0 * RB, cb, bar);
-    bulk_g2s(dst + a.off_ks, ks, kmb, bar);
-    bulk_g2s(dst + a.off_kz, kz, kmb, bar);
-    bulk_g2s(dst + a.off_vs, a.p.v_scale + row0 * NGV, vmb, bar);
-    bulk_g2s(dst + a.off_vz, a.p.v_zero + row0 * NGV, vmb, bar);
+    if (lane == 0) bar_expect_tx(bar, 2 * cb + 2 * kmb + 2 * vmb);
+    __syncwarp();
+    if (lane < 6) {
+      const float *fsrc = lane == 2 ? a.p.k_scale + krow
+                        : lane == 3 ? a.p.k_zero + krow
+                        : lane == 4 ? a.p.v_scale + row0 * NGV
+                                    : a.p.v_zero + row0 * NGV;
+      const void *src = lane == 0 ? (const void *)(a.p.k_codes + row0 * RB)
+                      : lane == 1 ? (const void *)(a.p.v_codes + row0 * RB)
+                                  : (const void *)fsrc;
+      const uint32_t off = lane == 0 ? 0u : lane == 1 ? (uint32_t)SC::off_vc
+                         : lane == 2 ? (uint32_t)SC::off_ks : lane == 3 ? (uint32_t)SC::off_kz
+                         : lane == 4 ? (uint32_t)SC::off_vs : (uint32_t)SC::off_vz;
+      const uint32_t bytes = lane < 2 ? cb : lane < 4 ? kmb : vmb;
+      bulk_g2s(dst + off, src, bytes, bar);
+    }
     ++issued;
     pc_lt += kWarps;
     pc_settle();
   };
-  if (lane == 0) {
-    pc_bh = bh_first;
-    seg_of(pc_bh, pc_tq0, pc_tq1);
-    pc_lt = warp;
-    pc_settle();
-    for (int s = 0; s < nslot; ++s) issue_next();
-  }
+  pc_bh = bh_first;
+  seg_of(pc_bh, pc_tq0, pc_tq1);
+  pc_lt = warp;
+  pc_settle();
+  for (int s = 0; s < nslot; ++s) issue_next();
 
-  // ---- per-head constants --------------------------------------------------
+  // ---- per-head constants (each warp for itself) --------------------------
   float pow2E = 1.0f;  // scores = raw * 2^E (q normalised by 2^-E)
+  float q4[4];         // q of channels 4*lane .. 4*lane+3 (exp2 domain)
   // KIVI key operand: this lane builds channel pairs ip = lane and lane + 32
   constexpr int kHalf = BITS == 2 ? 8 : 4;  // channel offset of the high half of a pair
   int b_clo[2], b_sidx[2];
@@ -453,39 +410,41 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   float Qj[NGK];
 
   auto start_head = [&](int bh) {
-    const int b = bh / g.H, h = bh % g.H;
-    float v = 0.0f;
-    if (tid < kD) {
-      v = __half2float(a.q[((int64_t)b * g.Hq + h) * kD + tid]) * a.scale_log2;
-      sQf[tid] = v;
-    }
-    float mx = fabsf(v);
+    const __half *qh = a.q + ((int64_t)(bh / g.H) * g.Hq + bh % g.H) * kD;
+    const uint2 qr = __ldg(reinterpret_cast<const uint2 *>(qh) + lane);
+    const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
+    const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
+    q4[0] = q01.x * a.scale_log2;
+    q4[1] = q01.y * a.scale_log2;
+    q4[2] = q23.x * a.scale_log2;
+    q4[3] = q23.y * a.scale_log2;
+    float mx = fmaxf(fmaxf(fabsf(q4[0]), fabsf(q4[1])), fmaxf(fabsf(q4[2]), fabsf(q4[3])));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0 && warp < 4) sFlagF[4 + warp] = mx;
-    __syncthreads();
-    mx = fmaxf(fmaxf(sFlagF[4], sFlagF[5]), fmaxf(sFlagF[6], sFlagF[7]));
     int E = 0;
     if (mx > 0.0f && mx < INFINITY) frexpf(mx, &E);
     pow2E = ldexpf(1.0f, E);
     const float inv = ldexpf(1.0f, -E);
+    auto qf = [&](int c) { return __half2float(__ldg(qh + c)) * a.scale_log2; };
     if (SCHEME == KVQ_KIVI) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int p = BITS == 2 ? (b_clo[r] & 7) : (b_clo[r] & 3);
         const float invf = inv / pos_factor<BITS>(p);
-        qf_lo[r] = sQf[b_clo[r]];
-        qf_hi[r] = sQf[b_clo[r] + kHalf];
+        qf_lo[r] = qf(b_clo[r]);
+        qf_hi[r] = qf(b_clo[r] + kHalf);
         qn_lo[r] = qf_lo[r] * invf;
         qn_hi[r] = qf_hi[r] * invf;
       }
     } else {
       const int GK = kD / NGK;
+      const float s4 = (q4[0] + q4[1]) + (q4[2] + q4[3]);
 #pragma unroll
       for (int j = 0; j < NGK; ++j) {
-        float s = 0.0f;
-        for (int c = j * GK; c < (j + 1) * GK; ++c) s += sQf[c];
-        Qj[j] = s;
+        float sj = (4 * lane) / GK == j ? s4 : 0.0f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sj += __shfl_xor_sync(0xffffffffu, sj, off);
+        Qj[j] = sj;
       }
       // columns n = gid = (group j = gid/2, part = gid%2); zero for gid >= 2*NGK
       const int jn = gid >> 1, part = gid & 1;
@@ -496,14 +455,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           int clo, chi, p;
           key_pair<BITS>(tig, kb, r, clo, chi, p);
           const float invf = inv / pos_factor<BITS>(p);
-          const float vlo = (clo / GK == jn) ? sQf[clo] * invf : 0.0f;
-          const float vhi = (chi / GK == jn) ? sQf[chi] * invf : 0.0f;
+          const float vlo = (clo / GK == jn) ? qf(clo) * invf : 0.0f;
+          const float vhi = (chi / GK == jn) ? qf(chi) * invf : 0.0f;
           uint32_t hi, lo;
           split2(vlo, vhi, hi, lo);
           bqi[kb][r] = gid < 2 * NGK ? (part ? lo : hi) : 0u;
         }
     }
-    __syncthreads();
   };
 
   // ---- per-warp online-softmax state ----------------------------------------
@@ -521,9 +479,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   };
   reset_state();
 
-  // Warp state -> merge scratch.  Lanes hold one token each, so every lane
-  // counts.  Returns false when a warp of the block gave up (timeout).
-  auto flush = [&](int bh) -> bool {
+  // Warp state -> partial `slot` of head bh (lanes hold one token each, so
+  // every lane counts).
+  auto flush = [&](int bh, int slot) {
     float l = l_lane;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
@@ -535,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
       Z[j] = z;
     }
-    float *ws = sScr + warp * kScrStride;
+    float *wo = a.ws_o + ((int64_t)bh * a.part_stride + slot) * kD;
     const int gc = (gid * NGV) >> 3;  // value group of this thread's 16 channels
     if (tig == gc) {
       float zc = Z[0];
@@ -545,26 +503,55 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float invf = 1.0f / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
-        ws[2 + 16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
-        ws[2 + 16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
+        wo[16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
+        wo[16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
       }
     }
-    if (lane == 0) {
-      ws[0] = m_run;
-      ws[1] = l;
-    }
-    __syncthreads();
-    if (sFlag[0]) return false;
-    const int seg = (int)blockIdx.x - owner_of(bh * a.U, a.total, a.nc);
-    merge_and_publish(a, bh, seg, sScr, sFlag);
+    warp_publish(a, bh, slot, m_run, l);
     reset_state();
-    return true;
   };
 
-  int ck = 0, done = 0;  // tiles visited / tiles whose copies completed
-  bool wabort = false;
-  bool stop = false;
-  for (int bh = bh_first; bh <= bh_last && !stop; ++bh) {
+  // fp16 sink + residual / window tokens of head bh: this warp takes every
+  // kWarps-th token (a lane owns 4 channels) and publishes partial `slot`.
+  auto fp16_item = [&](int bh, int slot) {
+    const int n = (int)a.n_fp16, ns = (int)a.n_sink;
+    float m = -INFINITY, l = 0.0f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i = warp; i < n; i += kWarps) {
+      const int64_t kr = i < ns ? ((int64_t)bh * g.n_sink + i) : ((int64_t)bh * g.residual + (i - ns));
+      const __half *krow = (i < ns ? a.p.k_sink : a.p.k_res) + kr * kD;
+      const __half *vrow = (i < ns ? a.p.v_sink : a.p.v_res) + kr * kD;
+      const uint2 kw = __ldg(reinterpret_cast<const uint2 *>(krow) + lane);
+      const uint2 vw = __ldg(reinterpret_cast<const uint2 *>(vrow) + lane);
+      const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
+      const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
+      const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+      const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+      float sc = fmaf(q4[0], k01.x, fmaf(q4[1], k01.y, fmaf(q4[2], k23.x, q4[3] * k23.y)));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+      const float mn = fmaxf(m, sc);
+      const float al = exp2f(m - mn), pp = exp2f(sc - mn);
+      l = fmaf(l, al, pp);
+      acc[0] = fmaf(acc[0], al, pp * v01.x);
+      acc[1] = fmaf(acc[1], al, pp * v01.y);
+      acc[2] = fmaf(acc[2], al, pp * v23.x);
+      acc[3] = fmaf(acc[3], al, pp * v23.y);
+      m = mn;
+    }
+    float4 o;
+    o.x = acc[0];
+    o.y = acc[1];
+    o.z = acc[2];
+    o.w = acc[3];
+    reinterpret_cast<float4 *>(a.ws_o + ((int64_t)bh * a.part_stride + slot) * kD)[lane] = o;
+    warp_publish(a, bh, slot, m, l);
+  };
+
+  int done = 0;          // tiles whose copies completed
+  int cs = 0;            // ring slot of the next tile
+  uint32_t cph = 0;      // its barrier phase parity
+  bool first = true;
+  for (int bh = bh_first; bh <= bh_last; ++bh) {
     int tq0, tq1;
     seg_of(bh, tq0, tq1);
     const int base = bh * a.U;
@@ -573,35 +560,42 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     start_head(bh);
     if (tq1 > tq0) {
       const int nt = (tq1 - tq0 + kTile - 1) / kTile;
-      for (int lt = warp; lt < nt; lt += kWarps, ++ck) {
-        const int s = ck % nslot;
-        if (!wabort) {
-          bool ok = true;
-          if (ck == 0 && a.stall_limit > 0) ok = bar_wait(&bars[kWarps * nslot], 0u, a.stall_limit);
-          if (!ok || !bar_wait(&wbars[s], (uint32_t)((ck / nslot) & 1), a.wait_limit)) {
-            wabort = true;
-            sFlag[0] = 1;
-            if (a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
-          } else {
-            ++done;
-          }
+      bool aborted = false;
+      for (int lt = warp; lt < nt; lt += kWarps) {
+        const int s = cs;
+        const uint32_t par = cph;
+        if (++cs == nslot) {
+          cs = 0;
+          cph ^= 1u;
         }
-        if (wabort) continue;
-        const uint8_t *slot = wring + s * a.slot_bytes;
+        bool ok = true;
+        if (first && a.stall_limit > 0) ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
+        first = false;
+        if (ok) ok = bar_wait(&wbars[s], par, a.wait_limit);
+        // one verdict per warp: every lane takes the same path from here
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+          aborted = true;
+          break;
+        }
+        ++done;
+        const uint8_t *slot = wring + s * SLOT;
         const int tok0 = tq0 + kTile * lt;
         const int n = min(kTile, tq1 - tok0);
-        const uint8_t *kc = slot;
-        const uint8_t *vc = slot + a.off_vc;
-
-        // ------------- keys: two 16-token MMA tiles ------------------------
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-        float bias0 = 0.0f, bias1 = 0.0f;
-        uint32_t bk[8][2];
-        auto load_bk = [&](int gl) {
-          if (SCHEME == KVQ_KIVI) {
-            if (gid < 2) {
-              const uint4 *src = reinterpret_cast<const uint4 *>(sBw + gl * 128 + (gid * 4 + tig) * 16);
-#pragma unroll
+        auto tile = [&](auto full_c) {
+          constexpr bool FULL = decltype(full_c)::value;
+          const uint8_t *kc = slot;
+          const uint8_t *vc = slot + SC::off_vc;
+          // ------------- keys: two 16-token MMA tiles ------------------------
+          float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+          float bias0 = 0.0f, bias1 = 0.0f;
+          uint32_t bk[8][2];
+          auto load_bk = [&](int gl) {
+            if (SCHEME == KVQ_KIVI) {
+              // lanes of columns >= 2 read a zero block: no divergent branch
+              const uint4 *src = reinterpret_cast<const uint4 *>(
+                  gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + 256);
+  #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint4 v4 = src[i];
                 bk[2 * i][0] = v4.x;
@@ -610,265 +604,268 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
                 bk[2 * i + 1][1] = v4.w;
               }
             } else {
-#pragma unroll
-              for (int kb = 0; kb < 8; ++kb) bk[kb][0] = bk[kb][1] = 0u;
+  #pragma unroll
+              for (int kb = 0; kb < 8; ++kb) {
+                bk[kb][0] = bqi[kb][0];
+                bk[kb][1] = bqi[kb][1];
+              }
             }
-          } else {
-#pragma unroll
-            for (int kb = 0; kb < 8; ++kb) {
-              bk[kb][0] = bqi[kb][0];
-              bk[kb][1] = bqi[kb][1];
+          };
+          bool two_groups = false;
+          if (SCHEME == KVQ_KIVI) {
+            // q~ = q * scale (normalised, position factor divided out) as fp16
+            // hi/lo in B-fragment order, and q . zero, per key group of the tile
+            const float *ks = reinterpret_cast<const float *>(slot + SC::off_ks);
+            const float *kz = reinterpret_cast<const float *>(slot + SC::off_kz);
+            two_groups = G16 && (FULL || n > 16);
+            const int ngb = two_groups ? 2 : 1;
+            for (int gl = 0; gl < ngb; ++gl) {
+              float bz = 0.0f;
+  #pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const int clo = b_clo[r], chi = b_clo[r] + kHalf;
+                uint32_t hi, lo;
+                split2(qn_lo[r] * ks[gl * kD + clo], qn_hi[r] * ks[gl * kD + chi], hi, lo);
+                sBw[gl * 128 + b_sidx[r]] = hi;
+                sBw[gl * 128 + 64 + b_sidx[r]] = lo;
+                bz = fmaf(qf_lo[r], kz[gl * kD + clo], fmaf(qf_hi[r], kz[gl * kD + chi], bz));
+              }
+  #pragma unroll
+              for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
+              if (gl == 0) bias0 = bz;
+              bias1 = bz;
             }
+            __syncwarp();
           }
-        };
-        bool two_groups = false;
-        if (SCHEME == KVQ_KIVI) {
-          // q~ = q * scale (normalised, position factor divided out) as fp16
-          // hi/lo in B-fragment order, and q . zero, per key group of the tile
-          const float *ks = reinterpret_cast<const float *>(slot + a.off_ks);
-          const float *kz = reinterpret_cast<const float *>(slot + a.off_kz);
-          two_groups = g.k_group == 16 && n > 16;
-          const int ngb = two_groups ? 2 : 1;
-          for (int gl = 0; gl < ngb; ++gl) {
-            float bz = 0.0f;
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const int clo = b_clo[r], chi = b_clo[r] + kHalf;
-              uint32_t hi, lo;
-              split2(qn_lo[r] * ks[gl * kD + clo], qn_hi[r] * ks[gl * kD + chi], hi, lo);
-              sBw[gl * 128 + b_sidx[r]] = hi;
-              sBw[gl * 128 + 64 + b_sidx[r]] = lo;
-              bz = fmaf(qf_lo[r], kz[gl * kD + clo], fmaf(qf_hi[r], kz[gl * kD + chi], bz));
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
-            if (gl == 0) bias0 = bz;
-            bias1 = bz;
-          }
-          __syncwarp();
-        }
-        load_bk(0);
-        if (BITS == 2) {
-          const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
-          const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
-          const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
-          const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
-          if (!two_groups) {
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
-              const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
-              const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
-              const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                mma16816(d0, ext<2>(w00, s00, 2 * j), ext<2>(w01, s01, 2 * j),
-                         ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1),
-                         bk[4 * m + j][0], bk[4 * m + j][1]);
-                mma16816(d1, ext<2>(w10, s10, 2 * j), ext<2>(w11, s11, 2 * j),
-                         ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1),
-                         bk[4 * m + j][0], bk[4 * m + j][1]);
+          load_bk(0);
+          if (BITS == 2) {
+            const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
+            const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
+            const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
+            const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
+            if (!two_groups) {
+  #pragma unroll
+              for (int m = 0; m < 2; ++m) {
+                const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
+                const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
+                const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
+                const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  mma16816(d0, ext<2>(w00, s00, 2 * j), ext<2>(w01, s01, 2 * j),
+                           ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1),
+                           bk[4 * m + j][0], bk[4 * m + j][1]);
+                  mma16816(d1, ext<2>(w10, s10, 2 * j), ext<2>(w11, s11, 2 * j),
+                           ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1),
+                           bk[4 * m + j][0], bk[4 * m + j][1]);
+                }
+              }
+            } else {
+  #pragma unroll
+              for (int t2 = 0; t2 < 2; ++t2) {
+                if (t2 == 1) load_bk(1);
+                const uint2 wa = t2 ? wa1 : wa0, wb = t2 ? wb1 : wb0;
+  #pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                  const uint32_t w0 = m ? wa.y : wa.x, w1 = m ? wb.y : wb.x;
+                  const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
+  #pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    if (t2 == 0)
+                      mma16816(d0, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
+                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
+                               bk[4 * m + j][0], bk[4 * m + j][1]);
+                    else
+                      mma16816(d1, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
+                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
+                               bk[4 * m + j][0], bk[4 * m + j][1]);
+                  }
+                }
               }
             }
           } else {
-#pragma unroll
+            // 4-bit keys: G >= 32 always gives one key group per tile here
+            // (the 4-bit group-16 case takes the same path with two groups)
+  #pragma unroll
             for (int t2 = 0; t2 < 2; ++t2) {
-              if (t2 == 1) load_bk(1);
-              const uint2 wa = t2 ? wa1 : wa0, wb = t2 ? wb1 : wb0;
-#pragma unroll
-              for (int m = 0; m < 2; ++m) {
-                const uint32_t w0 = m ? wa.y : wa.x, w1 = m ? wb.y : wb.x;
-                const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
+              if (two_groups && t2 == 1) load_bk(1);
+              const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid) * RB + 16 * tig);
+              const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid + 8) * RB + 16 * tig);
+              const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
+  #pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
+  #pragma unroll
+                for (int j = 0; j < 2; ++j) {
                   if (t2 == 0)
-                    mma16816(d0, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                             ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
-                             bk[4 * m + j][0], bk[4 * m + j][1]);
+                    mma16816(d0, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
+                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
+                             bk[2 * m + j][0], bk[2 * m + j][1]);
                   else
-                    mma16816(d1, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                             ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
-                             bk[4 * m + j][0], bk[4 * m + j][1]);
+                    mma16816(d1, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
+                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
+                             bk[2 * m + j][0], bk[2 * m + j][1]);
                 }
               }
             }
           }
-        } else {
-          // 4-bit keys: G >= 32 always gives one key group per tile here
-          // (the 4-bit group-16 case takes the same path with two groups)
-#pragma unroll
-          for (int t2 = 0; t2 < 2; ++t2) {
-            if (two_groups && t2 == 1) load_bk(1);
-            const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid) * RB + 16 * tig);
-            const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid + 8) * RB + 16 * tig);
-            const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                if (t2 == 0)
-                  mma16816(d0, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                           ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
-                           bk[2 * m + j][0], bk[2 * m + j][1]);
-                else
-                  mma16816(d1, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                           ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
-                           bk[2 * m + j][0], bk[2 * m + j][1]);
+          // ------------- scores -> one token per lane ------------------------
+          float ra0, rb0, ra1, rb1;
+          if (SCHEME == KVQ_KIVI) {
+            ra0 = d0[0] + d0[1];
+            rb0 = d0[2] + d0[3];
+            ra1 = d1[0] + d1[1];
+            rb1 = d1[2] + d1[3];
+          } else {
+            const float *ks = reinterpret_cast<const float *>(slot + SC::off_ks);
+            const float *kz = reinterpret_cast<const float *>(slot + SC::off_kz);
+            const int jj = tig < NGK ? tig : NGK - 1;
+            float qj = Qj[0];
+  #pragma unroll
+            for (int j = 1; j < NGK; ++j)
+              if (j == jj) qj = Qj[j];
+            auto term = [&](int row, float dd) {
+              return fmaf(ks[row * NGK + jj], dd * pow2E, kz[row * NGK + jj] * qj);
+            };
+            ra0 = term(gid, d0[0] + d0[1]);
+            rb0 = term(gid + 8, d0[2] + d0[3]);
+            ra1 = term(gid + 16, d1[0] + d1[1]);
+            rb1 = term(gid + 24, d1[2] + d1[3]);
+            if (tig >= NGK) ra0 = rb0 = ra1 = rb1 = 0.0f;
+  #pragma unroll
+            for (int off = 1; off < NGK; off <<= 1) {
+              ra0 += __shfl_xor_sync(0xffffffffu, ra0, off);
+              rb0 += __shfl_xor_sync(0xffffffffu, rb0, off);
+              ra1 += __shfl_xor_sync(0xffffffffu, ra1, off);
+              rb1 += __shfl_xor_sync(0xffffffffu, rb1, off);
+            }
+          }
+          const int t = lane;
+          const int src = 4 * (t & 7);
+          const float xa0 = __shfl_sync(0xffffffffu, ra0, src), xb0 = __shfl_sync(0xffffffffu, rb0, src);
+          const float xa1 = __shfl_sync(0xffffffffu, ra1, src), xb1 = __shfl_sync(0xffffffffu, rb1, src);
+          float score = t < 16 ? ((t & 8) ? xb0 : xa0) : ((t & 8) ? xb1 : xa1);
+          if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
+          const bool valid = FULL || t < n;
+          score = valid ? score : -INFINITY;
+          float mt_ = score;
+  #pragma unroll
+          for (int off = 1; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
+          if (mt_ > m_run) {
+            const float alpha = exp2f(m_run - mt_);
+            l_lane *= alpha;
+  #pragma unroll
+            for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
+  #pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+  #pragma unroll
+              for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
+            m_run = mt_;
+          }
+          const float p = exp2f(score - m_run);
+          l_lane += p;
+          {
+            const float *vz = reinterpret_cast<const float *>(slot + SC::off_vz);
+  #pragma unroll
+            for (int j = 0; j < NGV; ++j)
+              z_lane[j] = (FULL || p > 0.0f) ? fmaf(p, vz[t * NGV + j], z_lane[j]) : z_lane[j];
+          }
+          // ------------- values: B = p * scale (hi/lo), A = codes ------------
+          const float *vs = reinterpret_cast<const float *>(slot + SC::off_vs);
+          const int jg = (gid >> 1) < NGV ? (gid >> 1) : NGV - 1;
+          const bool bact = gid < 2 * NGV;
+          const int nkb = (FULL || n > 16) ? 2 : 1;
+          for (int kb = 0; kb < nkb; ++kb) {
+            const int tk0 = 16 * kb + 2 * tig, tk1 = tk0 + 1, tk2 = tk0 + 8, tk3 = tk0 + 9;
+            const float p0 = __shfl_sync(0xffffffffu, p, tk0), p1 = __shfl_sync(0xffffffffu, p, tk1);
+            const float p2 = __shfl_sync(0xffffffffu, p, tk2), p3 = __shfl_sync(0xffffffffu, p, tk3);
+            const float x0 = (FULL || p0 > 0.0f) ? p0 * vs[tk0 * NGV + jg] : 0.0f;
+            const float x1 = (FULL || p1 > 0.0f) ? p1 * vs[tk1 * NGV + jg] : 0.0f;
+            const float x2 = (FULL || p2 > 0.0f) ? p2 * vs[tk2 * NGV + jg] : 0.0f;
+            const float x3 = (FULL || p3 > 0.0f) ? p3 * vs[tk3 * NGV + jg] : 0.0f;
+            uint32_t h01, l01, h23, l23;
+            split2(x0, x1, h01, l01);
+            split2(x2, x3, h23, l23);
+            const uint32_t bv0 = bact ? ((gid & 1) ? l01 : h01) : 0u;
+            const uint32_t bv1 = bact ? ((gid & 1) ? l23 : h23) : 0u;
+            if (BITS == 2) {
+              const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * gid);
+              const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * gid);
+              const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vc + tk2 * RB + 4 * gid);
+              const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vc + tk3 * RB + 4 * gid);
+              const uint32_t xa_ = __byte_perm(w0, w1, 0x5410), ya_ = __byte_perm(w0, w1, 0x7632);
+              const uint32_t xb_ = __byte_perm(w2, w3, 0x5410), yb_ = __byte_perm(w2, w3, 0x7632);
+              const uint32_t xas = shifted<2>(xa_), yas = shifted<2>(ya_);
+              const uint32_t xbs = shifted<2>(xb_), ybs = shifted<2>(yb_);
+  #pragma unroll
+              for (int mt = 0; mt < 8; ++mt)
+                mma16816(dv[mt], ext<2>(xa_, xas, mt), ext<2>(ya_, yas, mt), ext<2>(xb_, xbs, mt),
+                         ext<2>(yb_, ybs, mt), bv0, bv1);
+            } else {
+              const uint2 w0 = *reinterpret_cast<const uint2 *>(vc + tk0 * RB + 8 * gid);
+              const uint2 w1 = *reinterpret_cast<const uint2 *>(vc + tk1 * RB + 8 * gid);
+              const uint2 w2 = *reinterpret_cast<const uint2 *>(vc + tk2 * RB + 8 * gid);
+              const uint2 w3 = *reinterpret_cast<const uint2 *>(vc + tk3 * RB + 8 * gid);
+              // [0]: channels 16gid+0..3, [1]: +4..7, [2]: +8..11, [3]: +12..15
+              const uint32_t xa4[4] = {__byte_perm(w0.x, w1.x, 0x5410), __byte_perm(w0.x, w1.x, 0x7632),
+                                       __byte_perm(w0.y, w1.y, 0x5410), __byte_perm(w0.y, w1.y, 0x7632)};
+              const uint32_t xb4[4] = {__byte_perm(w2.x, w3.x, 0x5410), __byte_perm(w2.x, w3.x, 0x7632),
+                                       __byte_perm(w2.y, w3.y, 0x5410), __byte_perm(w2.y, w3.y, 0x7632)};
+              uint32_t sa4[4], sb4[4];
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                sa4[i] = shifted<4>(xa4[i]);
+                sb4[i] = shifted<4>(xb4[i]);
+              }
+  #pragma unroll
+              for (int mt = 0; mt < 8; ++mt) {
+                const int lo = mt < 4 ? 0 : 1, hi = mt < 4 ? 2 : 3, pos = mt & 3;
+                mma16816(dv[mt], ext<4>(xa4[lo], sa4[lo], pos), ext<4>(xa4[hi], sa4[hi], pos),
+                         ext<4>(xb4[lo], sb4[lo], pos), ext<4>(xb4[hi], sb4[hi], pos), bv0, bv1);
               }
             }
           }
-        }
-        // ------------- scores -> one token per lane ------------------------
-        float ra0, rb0, ra1, rb1;
-        if (SCHEME == KVQ_KIVI) {
-          ra0 = d0[0] + d0[1];
-          rb0 = d0[2] + d0[3];
-          ra1 = d1[0] + d1[1];
-          rb1 = d1[2] + d1[3];
-        } else {
-          const float *ks = reinterpret_cast<const float *>(slot + a.off_ks);
-          const float *kz = reinterpret_cast<const float *>(slot + a.off_kz);
-          const int jj = tig < NGK ? tig : NGK - 1;
-          float qj = Qj[0];
-#pragma unroll
-          for (int j = 1; j < NGK; ++j)
-            if (j == jj) qj = Qj[j];
-          auto term = [&](int row, float dd) {
-            return fmaf(ks[row * NGK + jj], dd * pow2E, kz[row * NGK + jj] * qj);
-          };
-          ra0 = term(gid, d0[0] + d0[1]);
-          rb0 = term(gid + 8, d0[2] + d0[3]);
-          ra1 = term(gid + 16, d1[0] + d1[1]);
-          rb1 = term(gid + 24, d1[2] + d1[3]);
-          if (tig >= NGK) ra0 = rb0 = ra1 = rb1 = 0.0f;
-#pragma unroll
-          for (int off = 1; off < NGK; off <<= 1) {
-            ra0 += __shfl_xor_sync(0xffffffffu, ra0, off);
-            rb0 += __shfl_xor_sync(0xffffffffu, rb0, off);
-            ra1 += __shfl_xor_sync(0xffffffffu, ra1, off);
-            rb1 += __shfl_xor_sync(0xffffffffu, rb1, off);
-          }
-        }
-        const int t = lane;
-        const int src = 4 * (t & 7);
-        const float xa0 = __shfl_sync(0xffffffffu, ra0, src), xb0 = __shfl_sync(0xffffffffu, rb0, src);
-        const float xa1 = __shfl_sync(0xffffffffu, ra1, src), xb1 = __shfl_sync(0xffffffffu, rb1, src);
-        float score = t < 16 ? ((t & 8) ? xb0 : xa0) : ((t & 8) ? xb1 : xa1);
-        if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
-        const bool valid = t < n;
-        score = valid ? score : -INFINITY;
-        float mt_ = score;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
-        if (mt_ > m_run) {
-          const float alpha = exp2f(m_run - mt_);
-          l_lane *= alpha;
-#pragma unroll
-          for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
-          m_run = mt_;
-        }
-        const float p = exp2f(score - m_run);
-        l_lane += p;
-        {
-          const float *vz = reinterpret_cast<const float *>(slot + a.off_vz);
-#pragma unroll
-          for (int j = 0; j < NGV; ++j)
-            z_lane[j] = p > 0.0f ? fmaf(p, vz[t * NGV + j], z_lane[j]) : z_lane[j];
-        }
-        // ------------- values: B = p * scale (hi/lo), A = codes ------------
-        const float *vs = reinterpret_cast<const float *>(slot + a.off_vs);
-        const int jg = (gid >> 1) < NGV ? (gid >> 1) : NGV - 1;
-        const bool bact = gid < 2 * NGV;
-        const int nkb = n > 16 ? 2 : 1;
-        for (int kb = 0; kb < nkb; ++kb) {
-          const int tk0 = 16 * kb + 2 * tig, tk1 = tk0 + 1, tk2 = tk0 + 8, tk3 = tk0 + 9;
-          const float p0 = __shfl_sync(0xffffffffu, p, tk0), p1 = __shfl_sync(0xffffffffu, p, tk1);
-          const float p2 = __shfl_sync(0xffffffffu, p, tk2), p3 = __shfl_sync(0xffffffffu, p, tk3);
-          const float x0 = p0 > 0.0f ? p0 * vs[tk0 * NGV + jg] : 0.0f;
-          const float x1 = p1 > 0.0f ? p1 * vs[tk1 * NGV + jg] : 0.0f;
-          const float x2 = p2 > 0.0f ? p2 * vs[tk2 * NGV + jg] : 0.0f;
-          const float x3 = p3 > 0.0f ? p3 * vs[tk3 * NGV + jg] : 0.0f;
-          uint32_t h01, l01, h23, l23;
-          split2(x0, x1, h01, l01);
-          split2(x2, x3, h23, l23);
-          const uint32_t bv0 = bact ? ((gid & 1) ? l01 : h01) : 0u;
-          const uint32_t bv1 = bact ? ((gid & 1) ? l23 : h23) : 0u;
-          if (BITS == 2) {
-            const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * gid);
-            const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * gid);
-            const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vc + tk2 * RB + 4 * gid);
-            const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vc + tk3 * RB + 4 * gid);
-            const uint32_t xa_ = __byte_perm(w0, w1, 0x5410), ya_ = __byte_perm(w0, w1, 0x7632);
-            const uint32_t xb_ = __byte_perm(w2, w3, 0x5410), yb_ = __byte_perm(w2, w3, 0x7632);
-            const uint32_t xas = shifted<2>(xa_), yas = shifted<2>(ya_);
-            const uint32_t xbs = shifted<2>(xb_), ybs = shifted<2>(yb_);
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-              mma16816(dv[mt], ext<2>(xa_, xas, mt), ext<2>(ya_, yas, mt), ext<2>(xb_, xbs, mt),
-                       ext<2>(yb_, ybs, mt), bv0, bv1);
-          } else {
-            const uint2 w0 = *reinterpret_cast<const uint2 *>(vc + tk0 * RB + 8 * gid);
-            const uint2 w1 = *reinterpret_cast<const uint2 *>(vc + tk1 * RB + 8 * gid);
-            const uint2 w2 = *reinterpret_cast<const uint2 *>(vc + tk2 * RB + 8 * gid);
-            const uint2 w3 = *reinterpret_cast<const uint2 *>(vc + tk3 * RB + 8 * gid);
-            // [0]: channels 16gid+0..3, [1]: +4..7, [2]: +8..11, [3]: +12..15
-            const uint32_t xa4[4] = {__byte_perm(w0.x, w1.x, 0x5410), __byte_perm(w0.x, w1.x, 0x7632),
-                                     __byte_perm(w0.y, w1.y, 0x5410), __byte_perm(w0.y, w1.y, 0x7632)};
-            const uint32_t xb4[4] = {__byte_perm(w2.x, w3.x, 0x5410), __byte_perm(w2.x, w3.x, 0x7632),
-                                     __byte_perm(w2.y, w3.y, 0x5410), __byte_perm(w2.y, w3.y, 0x7632)};
-            uint32_t sa4[4], sb4[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              sa4[i] = shifted<4>(xa4[i]);
-              sb4[i] = shifted<4>(xb4[i]);
-            }
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              const int lo = mt < 4 ? 0 : 1, hi = mt < 4 ? 2 : 3, pos = mt & 3;
-              mma16816(dv[mt], ext<4>(xa4[lo], sa4[lo], pos), ext<4>(xa4[hi], sa4[hi], pos),
-                       ext<4>(xb4[lo], sb4[lo], pos), ext<4>(xb4[hi], sb4[hi], pos), bv0, bv1);
-            }
-          }
-        }
+        };
+        if (n == kTile)
+          tile(std::true_type{});
+        else
+          tile(std::false_type{});
         __syncwarp();
-        if (lane == 0) issue_next();  // refill the slot just consumed
+        issue_next();  // refill the slot just consumed
       }
-      if (!flush(bh)) {
-        stop = true;
-        break;
+      if (aborted) {
+        // give up this block's work for this warp; its copies complete first
+        if (lane == 0)
+          for (int i = done; i < issued; ++i)
+            bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
+        return;
       }
+      const int seg = (int)blockIdx.x - owner_of(base, a.total, a.nc);
+      flush(bh, seg * kWarps + warp);
     }
     if (own_fp16) {
       int nseg, nparts;
       head_parts(a, bh, nseg, nparts);
-      fp16_item(a, bh, nseg, sQf, sScr, sFlag);
+      fp16_item(bh, nseg * kWarps + warp);
     }
   }
-  // copies still in flight (only after a timeout) complete before exit
-  if (lane == 0)
-    for (int i = done; i < issued; ++i)
-      bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
 }
 
-template <int BITS, int SCHEME, int NGV, int NGK>
-cudaError_t launch_tc_t(TcArgs &a, int smem, int num_sms, cudaStream_t st) {
-  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK>;
-  static int configured = 0;
+template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
+cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
+  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, G16>;
+  constexpr int smem = SlotCfg<BITS, SCHEME, NGV, NGK, G16>::smem;
   static int occ = 0;
-  if (configured != smem) {
+  if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads, smem);
     if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-    configured = smem;
+    occ = o < 1 ? 1 : o;
   }
   int64_t nc = (int64_t)num_sms * occ;
+  if (nc > kTcMaxBlocks) nc = kTcMaxBlocks;
   if (nc > a.total) nc = a.total;
   if (nc < 1) nc = 1;
   a.nc = (int)nc;
@@ -877,26 +874,30 @@ cudaError_t launch_tc_t(TcArgs &a, int smem, int num_sms, cudaStream_t st) {
 }
 
 template <int BITS, int SCHEME>
-cudaError_t launch_tc_v(TcArgs &a, int smem, int num_sms, cudaStream_t st) {
+cudaError_t launch_tc_v(TcArgs &a, int num_sms, cudaStream_t st) {
   const int ngv = kD / a.g.v_group;
   if constexpr (SCHEME == KVQ_KIVI) {
-    return ngv == 4 ? launch_tc_t<BITS, SCHEME, 4, 1>(a, smem, num_sms, st)
-                    : launch_tc_t<BITS, SCHEME, 2, 1>(a, smem, num_sms, st);
+    const bool g16 = a.g.k_group == 16;
+    if (ngv == 4)
+      return g16 ? launch_tc_t<BITS, SCHEME, 4, 1, true>(a, num_sms, st)
+                 : launch_tc_t<BITS, SCHEME, 4, 1, false>(a, num_sms, st);
+    return g16 ? launch_tc_t<BITS, SCHEME, 2, 1, true>(a, num_sms, st)
+               : launch_tc_t<BITS, SCHEME, 2, 1, false>(a, num_sms, st);
   } else {
     const int ngk = kD / a.g.k_group;
     if (ngv == 4)
-      return ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4>(a, smem, num_sms, st)
-                      : launch_tc_t<BITS, SCHEME, 4, 2>(a, smem, num_sms, st);
-    return ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4>(a, smem, num_sms, st)
-                    : launch_tc_t<BITS, SCHEME, 2, 2>(a, smem, num_sms, st);
+      return ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, false>(a, num_sms, st)
+                      : launch_tc_t<BITS, SCHEME, 4, 2, false>(a, num_sms, st);
+    return ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, false>(a, num_sms, st)
+                    : launch_tc_t<BITS, SCHEME, 2, 2, false>(a, num_sms, st);
   }
 }
 
-long long g_stall_limit = 0;
+int g_stall_limit = 0;
 
 }  // namespace
 
-void set_debug_stall(long long n) { g_stall_limit = n; }
+void set_debug_stall(long long n) { g_stall_limit = n > (1 << 30) ? (1 << 30) : (int)n; }
 
 bool tc_decode_supported(const Geometry &g) {
   if (g.d != kD || g.Hq != g.H) return false;
@@ -921,16 +922,6 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.n_sink = n_sink;
   const int RB = kD * g.bits / 8;
   const int ngv = kD / g.v_group;
-  const int kmb = g.scheme == KVQ_KIVI ? (g.k_group == 16 ? 2 : 1) * kD * 4
-                                       : kTile * (kD / g.k_group) * 4;
-  const int vmb = kTile * ngv * 4;
-  a.off_vc = kTile * RB;
-  a.off_ks = 2 * kTile * RB;
-  a.off_kz = a.off_ks + kmb;
-  a.off_vs = a.off_kz + kmb;
-  a.off_vz = a.off_vs + vmb;
-  a.slot_bytes = (a.off_vz + vmb + 127) & ~127;
-  a.nslot = tc_layout(a.slot_bytes, 3).total <= 110 * 1024 ? 3 : 2;
   a.S_h = (int)((n_quant + kUnit - 1) / kUnit);
   // fp16 item weight in units: its bytes against a unit's bytes, x2 for the
   // CUDA-core path
@@ -942,21 +933,20 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   const int64_t total = (int64_t)g.B * g.H * a.U;
   if (total >= (1LL << 31)) return cudaErrorInvalidValue;
   a.total = (int)total;
-  a.part_stride = part_slots(g);
+  a.part_stride = tc_part_slots(g);
   const int64_t BH = (int64_t)g.B * g.H;
   char *base = static_cast<char *>(ws);
   const size_t cnt = ((size_t)BH * sizeof(int) + 255) & ~(size_t)255;
   a.ws_cnt = reinterpret_cast<int *>(base);
   a.ws_ml = reinterpret_cast<float *>(base + cnt);
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * 2;
-  a.wait_limit = 1LL << 24;
+  a.wait_limit = 1 << 24;
   a.stall_limit = g_stall_limit;
-  const int smem = tc_layout(a.slot_bytes, a.nslot).total;
   if (g.bits == 2)
-    return g.scheme == KVQ_KIVI ? launch_tc_v<2, KVQ_KIVI>(a, smem, num_sms, st)
-                                : launch_tc_v<2, KVQ_INNERQ>(a, smem, num_sms, st);
-  return g.scheme == KVQ_KIVI ? launch_tc_v<4, KVQ_KIVI>(a, smem, num_sms, st)
-                              : launch_tc_v<4, KVQ_INNERQ>(a, smem, num_sms, st);
+    return g.scheme == KVQ_KIVI ? launch_tc_v<2, KVQ_KIVI>(a, num_sms, st)
+                                : launch_tc_v<2, KVQ_INNERQ>(a, num_sms, st);
+  return g.scheme == KVQ_KIVI ? launch_tc_v<4, KVQ_KIVI>(a, num_sms, st)
+                              : launch_tc_v<4, KVQ_INNERQ>(a, num_sms, st);
 }
 
 }  // namespace kvq

@@ -52,6 +52,17 @@ cudaError_t launch_append(const Geometry &g, const CachePtrs &p, const __half *k
 // per 128 quantized tokens plus the fp16 segment.
 inline int part_slots(const Geometry &g) { return (int)(g.cap / kCapAlign) + 2; }
 
+// The tensor-core decode kernel leaves one partial per warp (8 per block) for
+// every block that touches a head, plus 8 for the fp16 item; it never uses
+// more than kTcMaxBlocks blocks.
+constexpr int kTcWarps = 8;
+constexpr int kTcMaxBlocks = 1024;
+inline int tc_part_slots(const Geometry &g) {
+  int64_t u = g.cap / kCapAlign;
+  if (u > kTcMaxBlocks) u = kTcMaxBlocks;
+  return (int)(kTcWarps * (u + 1));
+}
+
 struct DecodePlan {
   int n_qsplit;        // splits over the quantized region
   int n_split;         // n_qsplit + (fp16 segment present ? 1 : 0)
