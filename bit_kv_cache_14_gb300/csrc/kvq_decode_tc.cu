@@ -21,10 +21,11 @@
 //    returns.
 //  * Both GEMVs run as mma.sync m16n8k16 (fp16 in, fp32 accumulate), two
 //    independent 16-token MMA tiles per warp tile.  2/4-bit codes become exact
-//    fp16 integers with one LOP3 per two codes (the code bits are OR-ed into
-//    the mantissa of 1024.0) and one HSUB2; the position of a code inside its
-//    16-bit half multiplies it by a power of two that the other operand (or the
-//    final output row) divides out exactly.  The channel order inside each MMA
+//    fp16 operands with one AND per two codes: the masked code bits, left in
+//    place in the low ten bits of a 16-bit half, read as the subnormal
+//    code * 2^(position bits) * 2^-24.  The position power of two is divided
+//    out of the other operand (or the final output row) and the 2^-24 out of
+//    the fp32 result, both exactly.  The channel order inside each MMA
 //    is a permutation chosen so a thread consumes whole 32-bit code words; the
 //    matching operand uses the same permutation.
 //      keys   D[token][n] = sum_c code_tc * B[c][n],  B = q~ = q*scale split
@@ -51,7 +52,7 @@ constexpr int kUnit = 128;    // tokens per stream-K work unit
 constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
 constexpr int kD = 128;
 constexpr int kSBWords = 2 * 128 + 16;  // per-warp key operands (2 groups) + a zero block
-constexpr uint32_t kMagic = 0x64006400u;  // half2(1024, 1024)
+constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
 constexpr int kDrainLimit = 1 << 26;
 
 struct TcArgs {
@@ -145,29 +146,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
-__device__ __forceinline__ uint32_t lop_or_and(uint32_t a, uint32_t mask, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(c));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t hsub_magic(uint32_t x) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(x), "r"(kMagic));
-  return d;
-}
-
 // Code pair at position p of a word holding two 16-bit halves of codes:
-// returns half2(code_lo * f, code_hi * f) exactly, f = 4^p' / 16^p' below.
+// returns half2(code_lo * f, code_hi * f) * 2^-24 exactly, f = 4^p' (2-bit)
+// or 16^p' (4-bit).  The masked bits sit in the low ten bits of each half, so
+// each half reads as the fp16 subnormal (code * f) * 2^-24: one AND per pair.
 // ws = w >> 10 (2-bit) or w >> 8 (4-bit), precomputed by the caller.
 template <int BITS>
 __device__ __forceinline__ uint32_t ext(uint32_t w, uint32_t ws, int p) {
-  if (BITS == 2) {
-    return p <= 4 ? hsub_magic(lop_or_and(w, 0x00030003u << (2 * p), kMagic))
-                  : hsub_magic(lop_or_and(ws, 0x00030003u << (2 * (p - 5)), kMagic));
-  }
-  return p <= 1 ? hsub_magic(lop_or_and(w, 0x000F000Fu << (4 * p), kMagic))
-                : hsub_magic(lop_or_and(ws, 0x000F000Fu << (4 * (p - 2)), kMagic));
+  if (BITS == 2) return p <= 4 ? (w & (0x00030003u << (2 * p))) : (ws & (0x00030003u << (2 * (p - 5))));
+  return p <= 1 ? (w & (0x000F000Fu << (4 * p))) : (ws & (0x000F000Fu << (4 * (p - 2))));
 }
 
 template <int BITS>
@@ -379,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   for (int s = 0; s < nslot; ++s) issue_next();
 
   // ---- per-head constants (each warp for itself) --------------------------
-  float pow2E = 1.0f;  // scores = raw * 2^E (q normalised by 2^-E)
+  float pow2E = 1.0f;  // scores = raw * 2^(E+24) (q normalised by 2^-E, codes by 2^-24)
   float q4[4];         // q of channels 4*lane .. 4*lane+3 (exp2 domain)
   // KIVI key operand: this lane builds channel pairs ip = lane and lane + 32
   constexpr int kHalf = BITS == 2 ? 8 : 4;  // channel offset of the high half of a pair
@@ -423,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     int E = 0;
     if (mx > 0.0f && mx < INFINITY) frexpf(mx, &E);
-    pow2E = ldexpf(1.0f, E);
+    pow2E = ldexpf(1.0f, E) * kSub;
     const float inv = ldexpf(1.0f, -E);
     auto qf = [&](int c) { return __half2float(__ldg(qh + c)) * a.scale_log2; };
     if (SCHEME == KVQ_KIVI) {
@@ -502,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         if (j == gc) zc = Z[j];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const float invf = 1.0f / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
+        const float invf = kSub / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
         wo[16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
         wo[16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
       }
