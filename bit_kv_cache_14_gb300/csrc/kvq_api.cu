@@ -75,17 +75,26 @@ int resolve(const kvq_config *cfg, Geometry *g) {
     const int64_t vw = g->cap * (c.head_dim / c.v_group) / 32;
     if (vw > g->mode_words) g->mode_words = vw;
   }
+  const int vmeta = kBlockTokens * g->v_meta_cols * (int)sizeof(float);
+  g->blk_vc = kBlockTokens * g->row_bytes;
+  g->blk_vs = 2 * kBlockTokens * g->row_bytes;
+  g->blk_vz = g->blk_vs + vmeta;
+  g->blk_ks = g->blk_vz + vmeta;
+  if (c.scheme == KVQ_INNERQ) {
+    const int kmeta = kBlockTokens * g->k_meta_cols * (int)sizeof(float);
+    g->blk_kz = g->blk_ks + kmeta;
+    g->block_bytes = g->blk_kz + kmeta;
+  } else {
+    g->blk_kz = g->blk_ks;
+    g->block_bytes = g->blk_ks;
+  }
   return KVQ_OK;
 }
 
 CachePtrs ptrs_of(const kvq_cache *c) {
   CachePtrs p;
-  p.k_codes = static_cast<uint8_t *>(c->k_codes);
-  p.v_codes = static_cast<uint8_t *>(c->v_codes);
-  p.k_scale = c->k_scale;
-  p.k_zero = c->k_zero;
-  p.v_scale = c->v_scale;
-  p.v_zero = c->v_zero;
+  p.blocks = static_cast<uint8_t *>(c->blocks);
+  p.k_meta = c->k_meta;
   p.k_mode = c->k_mode;
   p.v_mode = c->v_mode;
   p.k_res = reinterpret_cast<__half *>(c->k_res);
@@ -99,10 +108,11 @@ CachePtrs ptrs_of(const kvq_cache *c) {
 // The buffers a configuration uses must be present and 16-byte aligned.
 static int check_cache(const Geometry &g, const kvq_cache *c) {
   if (!c) return KVQ_EINVAL;
-  const void *need[] = {c->k_codes, c->v_codes, c->k_scale, c->k_zero, c->v_scale, c->v_zero};
-  for (const void *p : need) {
-    if (!p) return KVQ_EINVAL;
-    if (!aligned16(p)) return KVQ_EALIGN;
+  if (!c->blocks) return KVQ_EINVAL;
+  if (!aligned16(c->blocks)) return KVQ_EALIGN;
+  if (g.scheme == KVQ_KIVI) {
+    if (!c->k_meta) return KVQ_EINVAL;
+    if (!aligned16(c->k_meta)) return KVQ_EALIGN;
   }
   if (g.residual > 0) {
     if (!c->k_res || !c->v_res) return KVQ_EINVAL;
@@ -135,10 +145,9 @@ int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out) {
   if (r != KVQ_OK) return r;
   memset(out, 0, sizeof(*out));
   const size_t BH = (size_t)g.B * g.H;
-  out->k_codes = out->v_codes = BH * (size_t)g.cap * g.row_bytes;
-  out->k_scale = out->k_zero =
-      BH * (size_t)g.k_meta_rows * g.k_meta_cols * sizeof(float) + kMetaPad;
-  out->v_scale = out->v_zero = BH * (size_t)g.cap * g.v_meta_cols * sizeof(float) + kMetaPad;
+  out->blocks = BH * (size_t)(g.cap / kBlockTokens) * g.block_bytes;
+  if (g.scheme == KVQ_KIVI)
+    out->k_meta = BH * (size_t)g.k_meta_rows * 2 * g.d * sizeof(float) + kMetaPad;
   if (g.scheme == KVQ_INNERQ) out->k_mode = out->v_mode = BH * (size_t)g.mode_words * 4;
   out->k_res = out->v_res = BH * (size_t)g.residual * g.d * 2;
   out->k_sink = out->v_sink = BH * (size_t)g.n_sink * g.d * 2;

@@ -167,14 +167,14 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
       const int ng_here = (int)min((int64_t)ngt, (n_tok - tt + G - 1) / G);
       for (int i = tid; i < ng_here * D; i += kBlock) {
         const int gl = i / D, c = i % D;
-        const float sk = a.p.k_scale[(bh * g.k_meta_rows + g0 + gl) * D + c];
+        const float sk = kivi_key_meta(g, a.p, bh, g0 + gl)[c];
 #pragma unroll
         for (int hh = 0; hh < RG; ++hh) u_s[(gl * RG + hh) * D + c] = q_s[hh * D + c] * sk;
       }
       const int lane = tid & 31, wid = tid >> 5;
       for (int pr = wid; pr < ng_here * RG; pr += kBlock / 32) {
         const int gl = pr / RG, hh = pr % RG;
-        const float *zr = a.p.k_zero + (bh * g.k_meta_rows + g0 + gl) * D;
+        const float *zr = kivi_key_meta(g, a.p, bh, g0 + gl) + D;
         float s = 0.0f;
         for (int c = lane; c < D; c += 32) s += q_s[hh * D + c] * zr[c];
 #pragma unroll
@@ -185,8 +185,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
       const int64_t i = tt + tid;
       if (i < n_tok) {
         const int gl = tid / G;
-        const uint4 *row = reinterpret_cast<const uint4 *>(
-            a.p.k_codes + (bh * g.cap + t0 + i) * (int64_t)g.row_bytes);
+        const uint4 *row = reinterpret_cast<const uint4 *>(code_row(g, a.p, bh, t0 + i, 0));
         float s[RG];
 #pragma unroll
         for (int hh = 0; hh < RG; ++hh) s[hh] = bias_s[gl * RG + hh];
@@ -214,10 +213,9 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     const int GK = g.k_group;
     for (int64_t i = tid; i < n_tok; i += kBlock) {
       const int64_t t = t0 + i;
-      const uint32_t *row =
-          reinterpret_cast<const uint32_t *>(a.p.k_codes + (bh * g.cap + t) * (int64_t)g.row_bytes);
-      const float *ks = a.p.k_scale + (bh * g.cap + t) * ngk;
-      const float *kz = a.p.k_zero + (bh * g.cap + t) * ngk;
+      const uint32_t *row = reinterpret_cast<const uint32_t *>(code_row(g, a.p, bh, t, 0));
+      const float *ks = tok_meta(g, a.p, bh, t, g.blk_ks, ngk);
+      const float *kz = tok_meta(g, a.p, bh, t, g.blk_kz, ngk);
       float s[RG] = {};
       for (int j = 0; j < ngk; ++j) {
         float part[RG] = {};
@@ -290,11 +288,11 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     const int gv = (8 * j) / g.v_group;
     for (int64_t i = tl; i < n_tok; i += TL) {
       const int64_t t = t0 + i;
-      const uint8_t *row = a.p.v_codes + (bh * g.cap + t) * (int64_t)g.row_bytes;
+      const uint8_t *row = code_row(g, a.p, bh, t, g.blk_vc);
       const uint32_t word = BITS == 2 ? (uint32_t)reinterpret_cast<const uint16_t *>(row)[j]
                                       : reinterpret_cast<const uint32_t *>(row)[j];
-      const float vs = a.p.v_scale[(bh * g.cap + t) * ngv + gv];
-      const float vz = a.p.v_zero[(bh * g.cap + t) * ngv + gv];
+      const float vs = tok_meta(g, a.p, bh, t, g.blk_vs, ngv)[gv];
+      const float vz = tok_meta(g, a.p, bh, t, g.blk_vz, ngv)[gv];
 #pragma unroll
       for (int hh = 0; hh < RG; ++hh) {
         const float pv = sc[hh * a.sc_max + i];

@@ -51,7 +51,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kUnit = 128;    // tokens per stream-K work unit
 constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
 constexpr int kD = 128;
-constexpr int kSBWords = 2 * 128 + 16;  // per-warp key operands (2 groups) + a zero block
 constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
 constexpr int kDrainLimit = 1 << 26;
 
@@ -73,32 +72,38 @@ struct TcArgs {
 };
 
 struct TcLayout {
-  int ring, sB, bars, total;
+  int ring, bars, total;
 };
 
 __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot) {
   TcLayout L{};
   L.ring = 0;
-  L.sB = L.ring + kWarps * nslot * slot_bytes;  // per warp: 2 key groups x 128 u32 + 16 zeros
-  L.bars = L.sB + kWarps * kSBWords * 4;        // per warp: nslot + 1 mbarriers
+  L.bars = L.ring + kWarps * nslot * slot_bytes;  // per warp: nslot + 1 mbarriers
   L.total = L.bars + kWarps * (nslot + 1) * 8;
   return L;
 }
 
-// Compile-time layout of one warp-ring slot (one 32-token tile): K codes,
-// V codes, K scale, K zero, V scale, V zero.
+// Compile-time layout of one warp-ring slot (one 32-token tile).  The first
+// BB bytes are a copy of the cache block (K codes, V codes, V scale, V zero,
+// InnerQ K scale, K zero); then the KIVI key statistics of the tile's group(s)
+// (scale row, zero row per group; the key MMA operand is later built in
+// place of them), the query row on the first tile of a head, and 64 bytes
+// that stay zero.
 template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
 struct SlotCfg {
   static constexpr int RB = kD * BITS / 8;
-  static constexpr int KMB = SCHEME == KVQ_KIVI ? (G16 ? 2 : 1) * kD * 4 : kTile * NGK * 4;
-  static constexpr int VMB = kTile * NGV * 4;
   static constexpr int off_vc = kTile * RB;
-  static constexpr int off_ks = 2 * kTile * RB;
-  static constexpr int off_kz = off_ks + KMB;
-  static constexpr int off_vs = off_kz + KMB;
-  static constexpr int off_vz = off_vs + VMB;
-  static constexpr int bytes = (off_vz + VMB + 127) & ~127;
-  static constexpr int nslot = tc_layout(bytes, 3).total <= 110 * 1024 ? 3 : 2;
+  static constexpr int off_vs = 2 * kTile * RB;
+  static constexpr int off_vz = off_vs + kTile * NGV * 4;
+  static constexpr int off_ks = off_vz + kTile * NGV * 4;  // InnerQ
+  static constexpr int off_kz = off_ks + kTile * NGK * 4;  // InnerQ
+  static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks : off_kz + kTile * NGK * 4;
+  static constexpr int KMB = SCHEME == KVQ_KIVI ? (G16 ? 2 : 1) * 2 * kD * 4 : 0;
+  static constexpr int off_km = BB;
+  static constexpr int off_q = BB + KMB;
+  static constexpr int off_zero = off_q + kD * 2;
+  static constexpr int bytes = (off_zero + 64 + 127) & ~127;
+  static constexpr int nslot = tc_layout(bytes, 3).total <= 112 * 1024 ? 3 : 2;
   static constexpr int smem = tc_layout(bytes, nslot).total;
 };
 
@@ -280,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   uint8_t *wring = smem + Ly.ring + warp * nslot * SLOT;
   uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
-  uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB) + warp * kSBWords;
 
   const int x0 = (int)((int64_t)blockIdx.x * a.total / a.nc);
   const int x1 = (int)((int64_t)(blockIdx.x + 1) * a.total / a.nc);
@@ -289,7 +293,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // Each warp owns its ring and barriers; nothing below synchronises warps.
   for (int i = lane; i < nslot * SLOT / 16; i += 32)
     reinterpret_cast<uint4 *>(wring)[i] = make_uint4(0, 0, 0, 0);
-  if (lane < 16) sBw[256 + lane] = 0u;
   if (lane == 0) {
     for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -318,42 +321,33 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       pc_lt = warp;
     }
   };
-  // Called by the whole warp: lane 0 posts the byte count, lanes 0..5 each
-  // issue one of the six copies of the next tile of this warp.
+  // Called by the whole warp; lane 0 posts the byte count and issues the
+  // copies of the next tile of this warp: its cache block, the KIVI key
+  // statistics of its group(s), and the query row on the first tile of a head.
   auto issue_next = [&]() {
     if (pc_bh < 0) return;
     const int tok0 = pc_tq0 + kTile * pc_lt;
-    const int n = min(kTile, pc_tq1 - tok0);
+    const bool first = pc_lt == warp;
     uint8_t *dst = wring + ps * SLOT;
     uint64_t *bar = &wbars[ps];
     ps = ps + 1 == nslot ? 0 : ps + 1;
-    const int64_t row0 = (int64_t)pc_bh * g.cap + tok0;
-    const uint32_t cb = (uint32_t)(n * RB);
-    const uint32_t vmb = (uint32_t)((n * NGV * 4 + 15) & ~15);
-    uint32_t kmb;
-    int64_t krow;
     if (SCHEME == KVQ_KIVI) {
-      kmb = (uint32_t)((G16 && n > 16 ? 2 : 1) * kD * 4);
-      krow = ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * kD;
-    } else {
-      kmb = (uint32_t)((n * NGK * 4 + 15) & ~15);
-      krow = row0 * NGK;
+      // the key operand was written into this slot by the generic proxy:
+      // order those writes before the copy that overwrites the slot
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
     }
-    if (lane == 0) bar_expect_tx(bar, 2 * cb + 2 * kmb + 2 * vmb);
-    __syncwarp();
-    if (lane < 6) {
-      const float *fsrc = lane == 2 ? a.p.k_scale + krow
-                        : lane == 3 ? a.p.k_zero + krow
-                        : lane == 4 ? a.p.v_scale + row0 * NGV
-                                    : a.p.v_zero + row0 * NGV;
-      const void *src = lane == 0 ? (const void *)(a.p.k_codes + row0 * RB)
-                      : lane == 1 ? (const void *)(a.p.v_codes + row0 * RB)
-                                  : (const void *)fsrc;
-      const uint32_t off = lane == 0 ? 0u : lane == 1 ? (uint32_t)SC::off_vc
-                         : lane == 2 ? (uint32_t)SC::off_ks : lane == 3 ? (uint32_t)SC::off_kz
-                         : lane == 4 ? (uint32_t)SC::off_vs : (uint32_t)SC::off_vz;
-      const uint32_t bytes = lane < 2 ? cb : lane < 4 ? kmb : vmb;
-      bulk_g2s(dst + off, src, bytes, bar);
+    if (lane == 0) {
+      bar_expect_tx(bar, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)));
+      bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
+               SC::BB, bar);
+      if (SCHEME == KVQ_KIVI)
+        bulk_g2s(dst + SC::off_km,
+                 a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
+                 SC::KMB, bar);
+      if (first)
+        bulk_g2s(dst + SC::off_q, a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD,
+                 kD * 2, bar);
     }
     ++issued;
     pc_lt += kWarps;
@@ -396,9 +390,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   uint32_t bqi[8][2];
   float Qj[NGK];
 
-  auto start_head = [&](int bh) {
-    const __half *qh = a.q + ((int64_t)(bh / g.H) * g.Hq + bh % g.H) * kD;
-    const uint2 qr = __ldg(reinterpret_cast<const uint2 *>(qh) + lane);
+  // Per-head constants from the query row that rode along with the head's
+  // first tile of this warp.
+  auto start_head = [&](const uint8_t *slot) {
+    const __half *qh = reinterpret_cast<const __half *>(slot + SC::off_q);
+    const uint2 qr = reinterpret_cast<const uint2 *>(qh)[lane];
     const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
     const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
     q4[0] = q01.x * a.scale_log2;
@@ -412,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     if (mx > 0.0f && mx < INFINITY) frexpf(mx, &E);
     pow2E = ldexpf(1.0f, E) * kSub;
     const float inv = ldexpf(1.0f, -E);
-    auto qf = [&](int c) { return __half2float(__ldg(qh + c)) * a.scale_log2; };
+    auto qf = [&](int c) { return __half2float(qh[c]) * a.scale_log2; };
     if (SCHEME == KVQ_KIVI) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
@@ -502,6 +498,17 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // kWarps-th token (a lane owns 4 channels) and publishes partial `slot`.
   auto fp16_item = [&](int bh, int slot) {
     const int n = (int)a.n_fp16, ns = (int)a.n_sink;
+    float qq[4];
+    {
+      const uint2 qr = __ldg(reinterpret_cast<const uint2 *>(
+                                 a.q + ((int64_t)(bh / g.H) * g.Hq + bh % g.H) * kD) + lane);
+      const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
+      const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
+      qq[0] = q01.x * a.scale_log2;
+      qq[1] = q01.y * a.scale_log2;
+      qq[2] = q23.x * a.scale_log2;
+      qq[3] = q23.y * a.scale_log2;
+    }
     float m = -INFINITY, l = 0.0f, acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int i = warp; i < n; i += kWarps) {
       const int64_t kr = i < ns ? ((int64_t)bh * g.n_sink + i) : ((int64_t)bh * g.residual + (i - ns));
@@ -513,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
       const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
       const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
-      float sc = fmaf(q4[0], k01.x, fmaf(q4[1], k01.y, fmaf(q4[2], k23.x, q4[3] * k23.y)));
+      float sc = fmaf(qq[0], k01.x, fmaf(qq[1], k01.y, fmaf(qq[2], k23.x, qq[3] * k23.y)));
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
       const float mn = fmaxf(m, sc);
@@ -544,7 +551,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     const int base = bh * a.U;
     const bool own_fp16 = a.F_h > 0 && x0 <= base + a.S_h && base + a.S_h < x1;
     if (tq1 <= tq0 && !own_fp16) continue;
-    start_head(bh);
     if (tq1 > tq0) {
       const int nt = (tq1 - tq0 + kTile - 1) / kTile;
       bool aborted = false;
@@ -567,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         }
         ++done;
         const uint8_t *slot = wring + s * SLOT;
+        if (lt == warp) start_head(slot);
         const int tok0 = tq0 + kTile * lt;
         const int n = min(kTile, tq1 - tok0);
         auto tile = [&](auto full_c) {
@@ -577,11 +584,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
           float bias0 = 0.0f, bias1 = 0.0f;
           uint32_t bk[8][2];
+          // KIVI key operand, built in place of the tile's key statistics
+          uint32_t *sBw = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(slot) + SC::off_km);
           auto load_bk = [&](int gl) {
             if (SCHEME == KVQ_KIVI) {
-              // lanes of columns >= 2 read a zero block: no divergent branch
+              // lanes of columns >= 2 read the zero block: no divergent branch
               const uint4 *src = reinterpret_cast<const uint4 *>(
-                  gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + 256);
+                  gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16
+                          : reinterpret_cast<const uint32_t *>(slot + SC::off_zero));
   #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint4 v4 = src[i];
@@ -601,26 +611,36 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           bool two_groups = false;
           if (SCHEME == KVQ_KIVI) {
             // q~ = q * scale (normalised, position factor divided out) as fp16
-            // hi/lo in B-fragment order, and q . zero, per key group of the tile
-            const float *ks = reinterpret_cast<const float *>(slot + SC::off_ks);
-            const float *kz = reinterpret_cast<const float *>(slot + SC::off_kz);
+            // hi/lo in B-fragment order, and q . zero, per key group of the
+            // tile.  All statistics are read before the operand overwrites them.
+            const float *km = reinterpret_cast<const float *>(slot + SC::off_km);
             two_groups = G16 && (FULL || n > 16);
-            const int ngb = two_groups ? 2 : 1;
-            for (int gl = 0; gl < ngb; ++gl) {
+            uint32_t whi[2][2], wlo[2][2];
+  #pragma unroll
+            for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
+              if (gl == 1 && !two_groups) break;
+              const float *ks = km + gl * 2 * kD, *kz = ks + kD;
               float bz = 0.0f;
   #pragma unroll
               for (int r = 0; r < 2; ++r) {
                 const int clo = b_clo[r], chi = b_clo[r] + kHalf;
-                uint32_t hi, lo;
-                split2(qn_lo[r] * ks[gl * kD + clo], qn_hi[r] * ks[gl * kD + chi], hi, lo);
-                sBw[gl * 128 + b_sidx[r]] = hi;
-                sBw[gl * 128 + 64 + b_sidx[r]] = lo;
-                bz = fmaf(qf_lo[r], kz[gl * kD + clo], fmaf(qf_hi[r], kz[gl * kD + chi], bz));
+                split2(qn_lo[r] * ks[clo], qn_hi[r] * ks[chi], whi[gl][r], wlo[gl][r]);
+                bz = fmaf(qf_lo[r], kz[clo], fmaf(qf_hi[r], kz[chi], bz));
               }
   #pragma unroll
               for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
               if (gl == 0) bias0 = bz;
               bias1 = bz;
+            }
+            __syncwarp();
+  #pragma unroll
+            for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
+              if (gl == 1 && !two_groups) break;
+  #pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                sBw[gl * 128 + b_sidx[r]] = whi[gl][r];
+                sBw[gl * 128 + 64 + b_sidx[r]] = wlo[gl][r];
+              }
             }
             __syncwarp();
           }
@@ -842,6 +862,7 @@ template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
 cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, G16>;
   constexpr int smem = SlotCfg<BITS, SCHEME, NGV, NGK, G16>::smem;
+  if (a.g.block_bytes != SlotCfg<BITS, SCHEME, NGV, NGK, G16>::BB) return cudaErrorInvalidValue;
   static int occ = 0;
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

@@ -12,29 +12,57 @@ namespace kvq {
 constexpr int kMaxHeadDim = 128;
 constexpr int kMaxResidual = 1024;
 constexpr int kCapAlign = 128;     // token-stride granularity of the cache layout
-constexpr int kMetaPad = 64;       // slack bytes after each metadata buffer
+constexpr int kMetaPad = 64;       // slack bytes after the KIVI key-statistics buffer
+constexpr int kBlockTokens = 32;   // tokens per block of the quantized region
 
 // Geometry of one cache, resolved on the host from kvq_config and copied by
 // value into every kernel.
 struct Geometry {
   int B, H, Hq, d, bits, scheme, k_group, v_group, residual, n_sink;
   int64_t max_ctx;
-  int64_t cap;        // per-head token stride of every buffer: max_ctx rounded up to kCapAlign
+  int64_t cap;        // per-head token capacity: max_ctx rounded up to kCapAlign
   int row_bytes;      // packed bytes per token row: d * bits / 8
   int k_meta_cols;    // KIVI: d; InnerQ: d / k_group
   int v_meta_cols;    // d / v_group
-  int64_t k_meta_rows;  // per head: KIVI cap / G; InnerQ cap
+  int64_t k_meta_rows;  // KIVI: cap / G key groups per head; InnerQ: cap
   int64_t mode_words;   // per head, InnerQ only
+  int block_bytes;      // one 32-token block
+  int blk_vc, blk_vs, blk_vz, blk_ks, blk_kz;  // byte offsets inside a block
 };
 
 // Device pointers of a cache (same meaning as kvq_cache).
 struct CachePtrs {
-  uint8_t *k_codes, *v_codes;
-  float *k_scale, *k_zero, *v_scale, *v_zero;
+  uint8_t *blocks;
+  float *k_meta;
   uint32_t *k_mode, *v_mode;
   __half *k_res, *v_res, *k_sink, *v_sink;
   int32_t *status;
 };
+
+// ---- addressing of the block layout (include/kvq.h, "Packed layout") ------
+__host__ __device__ __forceinline__ int64_t block_index(const Geometry &g, int64_t bh,
+                                                        int64_t t) {
+  return bh * (g.cap / kBlockTokens) + t / kBlockTokens;
+}
+__device__ __forceinline__ uint8_t *tok_block(const Geometry &g, const CachePtrs &p, int64_t bh,
+                                              int64_t t) {
+  return p.blocks + block_index(g, bh, t) * g.block_bytes;
+}
+// Packed code row of token t (off = 0 for keys, g.blk_vc for values).
+__device__ __forceinline__ uint8_t *code_row(const Geometry &g, const CachePtrs &p, int64_t bh,
+                                             int64_t t, int off) {
+  return tok_block(g, p, bh, t) + off + (int)(t % kBlockTokens) * g.row_bytes;
+}
+// Per-token statistics row of token t: `cols` floats at block offset `off`.
+__device__ __forceinline__ float *tok_meta(const Geometry &g, const CachePtrs &p, int64_t bh,
+                                           int64_t t, int off, int cols) {
+  return reinterpret_cast<float *>(tok_block(g, p, bh, t) + off) + (int)(t % kBlockTokens) * cols;
+}
+// KIVI key group grp of head bh: scale row (d floats); the zero row follows.
+__device__ __forceinline__ float *kivi_key_meta(const Geometry &g, const CachePtrs &p, int64_t bh,
+                                                int64_t grp) {
+  return p.k_meta + (bh * g.k_meta_rows + grp) * 2 * g.d;
+}
 
 int resolve(const kvq_config *cfg, Geometry *g);
 CachePtrs ptrs_of(const kvq_cache *c);

@@ -38,11 +38,6 @@ __device__ __forceinline__ void store_chunk(uint8_t *row, int chunk, uint32_t w,
     reinterpret_cast<uint32_t *>(row)[chunk] = w;
 }
 
-__device__ __forceinline__ uint8_t *code_row(uint8_t *base, const Geometry &g, int64_t bh,
-                                             int64_t slot) {
-  return base + (bh * g.cap + slot) * (int64_t)g.row_bytes;
-}
-
 // One key group (G tokens of src, row stride d) quantized per channel into
 // token slots [t0, t0 + G), t0 a multiple of G.  All threads of the block call
 // it; s_scale / s_mn are d-float shared arrays.
@@ -62,9 +57,9 @@ __device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int
     const float sc = asym_scale(mn, mx, g.bits);
     s_scale[c] = sc;
     s_mn[c] = mn;
-    const int64_t mi = (bh * g.k_meta_rows + t0 / G) * d + c;
-    p.k_scale[mi] = sc;
-    p.k_zero[mi] = mn;
+    float *km = kivi_key_meta(g, p, bh, t0 / G);
+    km[c] = sc;
+    km[d + c] = mn;
   }
   __syncthreads();
   const int chunks = d / 8;
@@ -78,7 +73,7 @@ __device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int
       const int c = 8 * j + k;
       w |= asym_code(x[k], s_mn[c], s_scale[c], g.bits) << (k * g.bits);
     }
-    store_chunk(code_row(p.k_codes, g, bh, t0 + i), j, w, g.bits);
+    store_chunk(code_row(g, p, bh, t0 + i, 0), j, w, g.bits);
   }
   __syncthreads();
 }
@@ -131,21 +126,32 @@ __device__ __forceinline__ ChunkQ quant_chunk(const float (&x)[8], int lanes, in
   return r;
 }
 
-// Where one per-token quantization writes: codes, meta, optional mode bits.
+// Where one per-token quantization writes: block offsets of the code rows
+// and of the scale / zero rows, optional mode bits.
 struct TokenDst {
-  uint8_t *codes;
-  float *scale, *zero;
+  int off_codes, off_scale, off_zero;
   uint32_t *mode;  // nullptr for KIVI values
   int group;       // channels per group
   int meta_cols;   // d / group
 };
 
 __device__ __forceinline__ TokenDst key_dst(const Geometry &g, const CachePtrs &p) {
-  return TokenDst{p.k_codes, p.k_scale, p.k_zero, p.k_mode, g.k_group, g.d / g.k_group};
+  return TokenDst{0, g.blk_ks, g.blk_kz, p.k_mode, g.k_group, g.d / g.k_group};
 }
 __device__ __forceinline__ TokenDst value_dst(const Geometry &g, const CachePtrs &p) {
-  return TokenDst{p.v_codes, p.v_scale, p.v_zero, g.scheme == KVQ_INNERQ ? p.v_mode : nullptr,
+  return TokenDst{g.blk_vc, g.blk_vs, g.blk_vz, g.scheme == KVQ_INNERQ ? p.v_mode : nullptr,
                   g.v_group, g.d / g.v_group};
+}
+
+__device__ __forceinline__ void store_token(const Geometry &g, const CachePtrs &p,
+                                            const TokenDst &dst, int64_t bh, int64_t t, int j,
+                                            int lanes, const ChunkQ &q) {
+  store_chunk(code_row(g, p, bh, t, dst.off_codes), j, q.codes, g.bits);
+  if ((j & (lanes - 1)) == 0) {
+    const int gi = j / lanes;
+    tok_meta(g, p, bh, t, dst.off_scale, dst.meta_cols)[gi] = q.scale;
+    tok_meta(g, p, bh, t, dst.off_zero, dst.meta_cols)[gi] = q.zero;
+  }
 }
 
 // Prefill, per-token groups: tokens [src0, src0 + n_tok) of every head of
@@ -185,12 +191,9 @@ __global__ void __launch_bounds__(kQuantBlock)
   }
   const ChunkQ q = quant_chunk(x, lanes, g.bits, dst.mode != nullptr);
   if (valid) {
-    store_chunk(code_row(dst.codes, g, bh, t), j, q.codes, g.bits);
+    store_token(g, p, dst, bh, t, j, lanes, q);
     if ((j & (lanes - 1)) == 0) {
       const int gi = j / lanes;
-      const int64_t mi = (bh * g.cap + t) * ng + gi;
-      dst.scale[mi] = q.scale;
-      dst.zero[mi] = q.zero;
       if (dst.mode && q.sym) {
         const int64_t bit = t * ng + gi;
         atomicOr(&s_bits[(bit >> 5) - wbase], 1u << (bit & 31));
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kQuantBlock)
     key_group_per_channel(g, p, bh, kr + (int64_t)grp * g.k_group * d,
                           n_quant + (int64_t)grp * g.k_group, s_scale, s_mn);
   const TokenDst dst = value_dst(g, p);
-  const int chunks = d / 8, lanes = g.v_group / 8, ng = dst.meta_cols;
+  const int chunks = d / 8, lanes = g.v_group / 8;
   const int items = R * chunks;
   const int rounds = (items + blockDim.x - 1) / blockDim.x;
   for (int rd = 0; rd < rounds; ++rd) {
@@ -277,14 +280,7 @@ __global__ void __launch_bounds__(kQuantBlock)
     float x[8];
     load8(vr + (int64_t)t * d + 8 * j, x);
     const ChunkQ q = quant_chunk(x, lanes, g.bits, false);
-    if (valid) {
-      store_chunk(code_row(dst.codes, g, bh, n_quant + t), j, q.codes, g.bits);
-      if ((j & (lanes - 1)) == 0) {
-        const int64_t mi = (bh * g.cap + n_quant + t) * ng + j / lanes;
-        dst.scale[mi] = q.scale;
-        dst.zero[mi] = q.zero;
-      }
-    }
+    if (valid) store_token(g, p, dst, bh, n_quant + t, j, lanes, q);
   }
 }
 
@@ -331,12 +327,9 @@ __global__ void __launch_bounds__(32)
     const int lanes = (valid ? dst.group : 8) / 8;
     const ChunkQ q = quant_chunk(x, lanes, g.bits, true);
     if (valid) {
-      store_chunk(code_row(dst.codes, g, bh, n_quant), j, q.codes, g.bits);
+      store_token(g, p, dst, bh, n_quant, j, lanes, q);
       if ((j & (lanes - 1)) == 0) {
         const int ng = dst.meta_cols, gi = j / lanes;
-        const int64_t mi = (bh * g.cap + n_quant) * ng + gi;
-        dst.scale[mi] = q.scale;
-        dst.zero[mi] = q.zero;
         const int64_t bit = n_quant * ng + gi;
         uint32_t *word = dst.mode + bh * g.mode_words + (bit >> 5);
         if (q.sym)

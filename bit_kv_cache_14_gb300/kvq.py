@@ -45,14 +45,12 @@ class Config(ctypes.Structure):
 
 class Sizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_mode", "v_mode",
-        "k_res", "v_res", "k_sink", "v_sink", "status")]
+        "blocks", "k_meta", "k_mode", "v_mode", "k_res", "v_res", "k_sink", "v_sink", "status")]
 
 
 class Cache(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
-        "k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_mode", "v_mode",
-        "k_res", "v_res", "k_sink", "v_sink")] + [
+        "blocks", "k_meta", "k_mode", "v_mode", "k_res", "v_res", "k_sink", "v_sink")] + [
         (n, ctypes.c_int64) for n in ("n_quant", "n_resid", "n_sink", "ring_head")] + [
         ("dev_status", ctypes.c_void_p)]
 
@@ -147,8 +145,7 @@ def _ptr(t: torch.Tensor) -> int:
 class QuantizedKVCache:
     """Device buffers (torch-allocated) of one quantized cache plus its C view."""
 
-    _BUFS = ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_mode",
-             "v_mode", "k_res", "v_res", "k_sink", "v_sink")
+    _BUFS = ("blocks", "k_meta", "k_mode", "v_mode", "k_res", "v_res", "k_sink", "v_sink")
 
     def __init__(self, cfg: Config, device="cuda"):
         self.cfg = cfg
@@ -226,23 +223,46 @@ class QuantizedKVCache:
         """Per-head token stride of every buffer: max_ctx rounded up to 128."""
         return (self.cfg.max_ctx + CAP_ALIGN - 1) // CAP_ALIGN * CAP_ALIGN
 
-    def codes(self, which: str) -> torch.Tensor:
+    # Byte offsets inside a 32-token block (include/kvq.h, "Packed layout").
+    def _block_layout(self):
         c = self.cfg
         rb = c.head_dim * c.bits // 8
-        n = c.batch * c.n_kv_heads * self.cap * rb
-        return self.bufs[which + "_codes"][:n].view(c.batch, c.n_kv_heads, self.cap, rb)
+        ngv = c.head_dim // c.v_group
+        ngk = c.head_dim // c.k_group if c.scheme == INNERQ else 0
+        off = {"k_codes": 0, "v_codes": 32 * rb, "v_scale": 64 * rb}
+        off["v_zero"] = off["v_scale"] + 128 * ngv
+        off["k_scale"] = off["v_zero"] + 128 * ngv
+        off["k_zero"] = off["k_scale"] + 128 * ngk
+        return off, off["k_zero"] + 128 * ngk, rb, ngv, ngk
+
+    def _block_field(self, name: str, width: int) -> torch.Tensor:
+        """Bytes [off, off + 32*width) of every block as [B][H][cap][width] (a copy)."""
+        c = self.cfg
+        off, bb, _, _, _ = self._block_layout()
+        nb = self.cap // 32
+        blocks = self.bufs["blocks"][: c.batch * c.n_kv_heads * nb * bb]
+        f = blocks.view(c.batch, c.n_kv_heads, nb, bb)[..., off[name]: off[name] + 32 * width]
+        return f.reshape(c.batch, c.n_kv_heads, self.cap, width)
+
+    def codes(self, which: str) -> torch.Tensor:
+        """Packed code rows as u8 [B][H][cap][d*bits/8] (a copy)."""
+        _, _, rb, _, _ = self._block_layout()
+        return self._block_field(which + "_codes", rb)
 
     def meta(self, name: str) -> torch.Tensor:
-        """scale / zero buffer as fp32 [B][H][rows * cols] (padding excluded)."""
+        """scale / zero statistics as fp32 [B][H][rows * cols] (a copy): KIVI keys
+        [cap/G][d], per-token statistics [cap][groups]."""
         c = self.cfg
         if name.startswith("k") and c.scheme == KIVI:
-            per_head = self.cap // c.k_group * c.head_dim
-        elif name.startswith("k"):
-            per_head = self.cap * (c.head_dim // c.k_group)
-        else:
-            per_head = self.cap * (c.head_dim // c.v_group)
-        n = c.batch * c.n_kv_heads * per_head
-        return self.bufs[name][: n * 4].view(torch.float32).view(c.batch, c.n_kv_heads, per_head)
+            rows = self.cap // c.k_group
+            n = c.batch * c.n_kv_heads * rows * 2 * c.head_dim
+            km = self.bufs["k_meta"][: n * 4].view(torch.float32)
+            km = km.view(c.batch, c.n_kv_heads, rows, 2, c.head_dim)
+            return km[:, :, :, 0 if name == "k_scale" else 1, :].reshape(c.batch, c.n_kv_heads, -1)
+        _, _, _, ngv, ngk = self._block_layout()
+        cols = ngk if name.startswith("k") else ngv
+        f = self._block_field(name, 4 * cols).contiguous().view(torch.float32)
+        return f.reshape(c.batch, c.n_kv_heads, -1)
 
     def modes(self, which: str) -> torch.Tensor:
         c = self.cfg

@@ -31,18 +31,27 @@
  *   scale = max(|min|, |max|) / (2^(b-1) - 1), q = clamp(rint(x / scale)),
  *   code = q + 2^(b-1), zero = -2^(b-1) * scale (same dequantization formula).
  *
- * Packed layout (all buffers token-major per (batch, kv head); cap = max_ctx
- * rounded up to a multiple of 128 is the per-head token stride):
- *   codes   u8 [B][H][cap][d*bits/8]; channel c of a token at bits
- *           (c mod (8/bits))*bits of byte c/(8/bits).
- *   KIVI:   k_scale, k_zero f32 [B][H][cap/G][d]         (per G-token group, channel)
- *           v_scale, v_zero f32 [B][H][cap][d/v_group]   (per token, channel group)
- *           k_res, v_res   fp16 [B][H][R][d]             (residual, oldest first)
- *   InnerQ: k_scale, k_zero f32 [B][H][cap][d/k_group]   (per token, channel group)
- *           v_scale, v_zero f32 [B][H][cap][d/v_group]
- *           k_mode, v_mode  u32 [B][H][cap*(d/group)/32]  bit i = group
+ * Packed layout.  cap = max_ctx rounded up to a multiple of 128 is the
+ * per-head token capacity.  Every per-token quantity of the quantized region
+ * lives in 32-token blocks, so one contiguous read fetches everything a
+ * 32-token tile needs except the KIVI key statistics:
+ *   blocks  u8 [B][H][cap/32][block_bytes]; block j of a head holds tokens
+ *           32j .. 32j+31 (token t at row i = t mod 32) as
+ *             K codes  [32][d*bits/8]    channel c of a row at bits
+ *             V codes  [32][d*bits/8]    (c mod (8/bits))*bits of byte c/(8/bits)
+ *             V scale  f32 [32][d/v_group]   (per token, channel group)
+ *             V zero   f32 [32][d/v_group]
+ *             InnerQ only:
+ *             K scale  f32 [32][d/k_group]   (per token, channel group)
+ *             K zero   f32 [32][d/k_group]
+ *           block_bytes = 64*d*bits/8 + 256*(d/v_group + (InnerQ ? d/k_group : 0)),
+ *           a multiple of 128.
+ *   KIVI:   k_meta  f32 [B][H][cap/G][2][d]  per G-token group: scale row,
+ *                   then zero (= min) row, one value per channel
+ *           (the buffer carries 64 bytes of slack after the last head)
+ *           k_res, v_res   fp16 [B][H][R][d]  residual, oldest first
+ *   InnerQ: k_mode, v_mode  u32 [B][H][cap*(d/group)/32]  bit i = group
  *                           i % (d/group) of token i / (d/group); 1 = symmetric
- *   The scale / zero buffers carry 64 bytes of slack after the last head.
  *           k_res, v_res   fp16 [B][H][W][d]   recent window, a ring (see ring_head)
  *           k_sink, v_sink fp16 [B][H][S][d]   first S tokens
  *   Quantized tokens occupy slots [0, n_quant) in arrival order.
@@ -99,8 +108,8 @@ typedef struct kvq_config {
 
 /* Byte sizes of the cache buffers for a configuration (0 = unused). */
 typedef struct kvq_sizes {
-  size_t k_codes, v_codes;
-  size_t k_scale, k_zero, v_scale, v_zero;
+  size_t blocks;  /* 32-token blocks of codes and per-token statistics */
+  size_t k_meta;  /* KIVI key statistics (0 under InnerQ) */
   size_t k_mode, v_mode;
   size_t k_res, v_res;
   size_t k_sink, v_sink;
@@ -118,8 +127,8 @@ typedef struct kvq_sizes {
  *   ring_head InnerQ: window slot of the oldest token once the window is full
  */
 typedef struct kvq_cache {
-  void *k_codes, *v_codes;
-  float *k_scale, *k_zero, *v_scale, *v_zero;
+  void *blocks;
+  float *k_meta;
   uint32_t *k_mode, *v_mode;
   uint16_t *k_res, *v_res, *k_sink, *v_sink;
   int64_t n_quant, n_resid, n_sink, ring_head;

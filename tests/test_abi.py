@@ -43,16 +43,17 @@ def _cfg(**kw):
 
 def test_sizes_follow_layout():
     s = kvq.cache_sizes(_cfg(max_ctx=4300))
-    BH, T, d = 8 * 32, 4352, 128      # per-head stride: 4300 rounded up to 128
-    assert s.k_codes == BH * T * d * 2 // 8
-    assert s.k_scale == BH * (T // 32) * d * 4 + 64
-    assert s.v_scale == BH * T * (d // 32) * 4 + 64
+    BH, T, d = 8 * 32, 4352, 128      # per-head capacity: 4300 rounded up to 128
+    # a 32-token block: K codes, V codes (32 B a row), V scale, V zero (4 groups)
+    assert s.blocks == BH * (T // 32) * (2 * 32 * 32 + 2 * 32 * 4 * 4)
+    assert s.k_meta == BH * (T // 32) * 2 * d * 4 + 64
     assert s.k_res == BH * 128 * d * 2
     assert s.k_mode == 0 and s.k_sink == 0
     si = kvq.cache_sizes(_cfg(scheme=kvq.INNERQ, bits=4, k_group=64, v_group=64, residual=32,
                               n_sink=4, batch=1, max_ctx=1 << 20))
-    assert si.k_codes == 32 * (1 << 20) * 64
-    assert si.k_scale == 32 * (1 << 20) * 2 * 4 + 64
+    # 4-bit rows of 64 B; two value groups and two key groups per token
+    assert si.blocks == 32 * ((1 << 20) // 32) * (2 * 32 * 64 + 4 * 32 * 2 * 4)
+    assert si.k_meta == 0
     assert si.k_mode == 32 * ((1 << 20) * 2 // 32) * 4
     assert si.k_sink == 32 * 4 * 128 * 2
 
@@ -60,8 +61,9 @@ def test_sizes_follow_layout():
 def test_per_token_bytes_match_llama2_table():
     # codes of one token, all 32 layers x 32 heads, keys and values
     for bits, expect in ((2, 65536), (4, 131072)):
-        s = kvq.cache_sizes(_cfg(bits=bits, batch=1, max_ctx=128))
-        assert 32 * (s.k_codes + s.v_codes) // 128 == expect
+        s = kvq.cache_sizes(_cfg(bits=bits, batch=1, max_ctx=128, v_group=128))
+        meta = 128 * 32 * 2 * 4            # one value group: scale + zero per token
+        assert 32 * (s.blocks - meta) // 128 == expect
 
 
 def test_workspace_bytes():
@@ -102,13 +104,16 @@ def test_calls_validate_before_touching_the_device():
                         None) == kvq.KVQ_EUNSUPPORTED
     # misaligned cache buffer pointers are rejected before any launch
     c = kvq.Cache()
-    for name in ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_res",
-                 "v_res"):
+    for name in ("blocks", "k_meta", "k_res", "v_res"):
         setattr(c, name, 0x1000)
-    c.k_codes = 0x1001
+    c.blocks = 0x1001
     assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), None, None, 0,
                                   None) == kvq.KVQ_EALIGN
-    c.k_codes = 0x1000
+    c.blocks = 0x1000
+    c.k_meta = None
+    assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), None, None, 0,
+                                  None) == kvq.KVQ_EINVAL
+    c.k_meta = 0x1000
     assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), ctypes.c_void_p(0x2000),
                                   ctypes.c_void_p(0x2000), 5000, None) == kvq.KVQ_ECAPACITY
     assert L.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(c), ctypes.c_void_p(0x2000),
