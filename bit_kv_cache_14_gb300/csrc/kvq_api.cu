@@ -85,8 +85,11 @@ int resolve(const kvq_config *cfg, Geometry *g) {
     g->blk_kz = g->blk_ks + kmeta;
     g->block_bytes = g->blk_kz + kmeta;
   } else {
+    // G <= 32: the statistics of the block's 32 / G key groups end the block
     g->blk_kz = g->blk_ks;
-    g->block_bytes = g->blk_ks;
+    g->block_bytes = g->blk_ks + (c.k_group <= kBlockTokens
+                                      ? (kBlockTokens / c.k_group) * 2 * c.head_dim * (int)sizeof(float)
+                                      : 0);
   }
   return KVQ_OK;
 }
@@ -110,7 +113,7 @@ static int check_cache(const Geometry &g, const kvq_cache *c) {
   if (!c) return KVQ_EINVAL;
   if (!c->blocks) return KVQ_EINVAL;
   if (!aligned16(c->blocks)) return KVQ_EALIGN;
-  if (g.scheme == KVQ_KIVI) {
+  if (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens) {
     if (!c->k_meta) return KVQ_EINVAL;
     if (!aligned16(c->k_meta)) return KVQ_EALIGN;
   }
@@ -146,7 +149,7 @@ int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out) {
   memset(out, 0, sizeof(*out));
   const size_t BH = (size_t)g.B * g.H;
   out->blocks = BH * (size_t)(g.cap / kBlockTokens) * g.block_bytes;
-  if (g.scheme == KVQ_KIVI)
+  if (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens)
     out->k_meta = BH * (size_t)g.k_meta_rows * 2 * g.d * sizeof(float) + kMetaPad;
   if (g.scheme == KVQ_INNERQ) out->k_mode = out->v_mode = BH * (size_t)g.mode_words * 4;
   out->k_res = out->v_res = BH * (size_t)g.residual * g.d * 2;

@@ -89,7 +89,10 @@ __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot) {
 // (scale row, zero row per group; the key MMA operand is later built in
 // place of them), the query row on the first tile of a head, and 64 bytes
 // that stay zero.
-template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
+// KM (KIVI): 2 = G 16, two key groups per tile, statistics inside the block;
+// 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
+// from the separate key-statistics array.
+template <int BITS, int SCHEME, int NGV, int NGK, int KM>
 struct SlotCfg {
   static constexpr int RB = kD * BITS / 8;
   static constexpr int off_vc = kTile * RB;
@@ -97,9 +100,11 @@ struct SlotCfg {
   static constexpr int off_vz = off_vs + kTile * NGV * 4;
   static constexpr int off_ks = off_vz + kTile * NGV * 4;  // InnerQ
   static constexpr int off_kz = off_ks + kTile * NGK * 4;  // InnerQ
-  static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks : off_kz + kTile * NGK * 4;
-  static constexpr int KMB = SCHEME == KVQ_KIVI ? (G16 ? 2 : 1) * 2 * kD * 4 : 0;
-  static constexpr int off_km = BB;
+  static constexpr bool KIN = SCHEME == KVQ_KIVI && KM >= 1;
+  static constexpr int KGB = (KM == 2 ? 2 : 1) * 2 * kD * 4;  // KIVI key statistics of a tile
+  static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks + (KIN ? KGB : 0) : off_kz + kTile * NGK * 4;
+  static constexpr int KMB = SCHEME == KVQ_KIVI && !KIN ? KGB : 0;  // separate copy
+  static constexpr int off_km = KIN ? off_ks : BB;
   static constexpr int off_q = BB + KMB;
   static constexpr int off_zero = off_q + kD * 2;
   static constexpr int bytes = (off_zero + 64 + 127) & ~127;
@@ -272,10 +277,11 @@ __device__ void warp_publish(const TcArgs &a, int bh, int slot, float m, float l
   if (lane == 0) a.ws_cnt[bh] = 0;
 }
 
-template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
+template <int BITS, int SCHEME, int NGV, int NGK, int KM>
 __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, G16>;
+  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM>;
+  constexpr bool G16 = SCHEME == KVQ_KIVI && KM == 2;
   constexpr int RB = SC::RB;  // packed bytes per token row
   constexpr int nslot = SC::nslot;
   constexpr int SLOT = SC::bytes;
@@ -341,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       bar_expect_tx(bar, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)));
       bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
                SC::BB, bar);
-      if (SCHEME == KVQ_KIVI)
+      if (SCHEME == KVQ_KIVI && !SC::KIN)
         bulk_g2s(dst + SC::off_km,
                  a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
                  SC::KMB, bar);
@@ -858,11 +864,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   }
 }
 
-template <int BITS, int SCHEME, int NGV, int NGK, bool G16>
+template <int BITS, int SCHEME, int NGV, int NGK, int KM>
 cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
-  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, G16>;
-  constexpr int smem = SlotCfg<BITS, SCHEME, NGV, NGK, G16>::smem;
-  if (a.g.block_bytes != SlotCfg<BITS, SCHEME, NGV, NGK, G16>::BB) return cudaErrorInvalidValue;
+  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM>;
+  constexpr int smem = SlotCfg<BITS, SCHEME, NGV, NGK, KM>::smem;
+  if (a.g.block_bytes != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::BB) return cudaErrorInvalidValue;
   static int occ = 0;
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -885,19 +891,21 @@ template <int BITS, int SCHEME>
 cudaError_t launch_tc_v(TcArgs &a, int num_sms, cudaStream_t st) {
   const int ngv = kD / a.g.v_group;
   if constexpr (SCHEME == KVQ_KIVI) {
-    const bool g16 = a.g.k_group == 16;
+    const int G = a.g.k_group;
     if (ngv == 4)
-      return g16 ? launch_tc_t<BITS, SCHEME, 4, 1, true>(a, num_sms, st)
-                 : launch_tc_t<BITS, SCHEME, 4, 1, false>(a, num_sms, st);
-    return g16 ? launch_tc_t<BITS, SCHEME, 2, 1, true>(a, num_sms, st)
-               : launch_tc_t<BITS, SCHEME, 2, 1, false>(a, num_sms, st);
+      return G == 16 ? launch_tc_t<BITS, SCHEME, 4, 1, 2>(a, num_sms, st)
+           : G == 32 ? launch_tc_t<BITS, SCHEME, 4, 1, 1>(a, num_sms, st)
+                     : launch_tc_t<BITS, SCHEME, 4, 1, 0>(a, num_sms, st);
+    return G == 16 ? launch_tc_t<BITS, SCHEME, 2, 1, 2>(a, num_sms, st)
+         : G == 32 ? launch_tc_t<BITS, SCHEME, 2, 1, 1>(a, num_sms, st)
+                   : launch_tc_t<BITS, SCHEME, 2, 1, 0>(a, num_sms, st);
   } else {
     const int ngk = kD / a.g.k_group;
     if (ngv == 4)
-      return ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, false>(a, num_sms, st)
-                      : launch_tc_t<BITS, SCHEME, 4, 2, false>(a, num_sms, st);
-    return ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, false>(a, num_sms, st)
-                    : launch_tc_t<BITS, SCHEME, 2, 2, false>(a, num_sms, st);
+      return ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, 0>(a, num_sms, st)
+                      : launch_tc_t<BITS, SCHEME, 4, 2, 0>(a, num_sms, st);
+    return ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, 0>(a, num_sms, st)
+                    : launch_tc_t<BITS, SCHEME, 2, 2, 0>(a, num_sms, st);
   }
 }
 

@@ -59,8 +59,14 @@ __device__ __forceinline__ float *tok_meta(const Geometry &g, const CachePtrs &p
   return reinterpret_cast<float *>(tok_block(g, p, bh, t) + off) + (int)(t % kBlockTokens) * cols;
 }
 // KIVI key group grp of head bh: scale row (d floats); the zero row follows.
+// G <= 32: at the end of the group's block; G >= 64: in the k_meta array.
 __device__ __forceinline__ float *kivi_key_meta(const Geometry &g, const CachePtrs &p, int64_t bh,
                                                 int64_t grp) {
+  if (g.k_group <= kBlockTokens) {
+    const int64_t t0 = grp * g.k_group;
+    return reinterpret_cast<float *>(tok_block(g, p, bh, t0) + g.blk_ks) +
+           (int)((t0 % kBlockTokens) / g.k_group) * 2 * g.d;
+  }
   return p.k_meta + (bh * g.k_meta_rows + grp) * 2 * g.d;
 }
 

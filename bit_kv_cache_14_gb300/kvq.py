@@ -233,7 +233,11 @@ class QuantizedKVCache:
         off["v_zero"] = off["v_scale"] + 128 * ngv
         off["k_scale"] = off["v_zero"] + 128 * ngv
         off["k_zero"] = off["k_scale"] + 128 * ngk
-        return off, off["k_zero"] + 128 * ngk, rb, ngv, ngk
+        bb = off["k_zero"] + 128 * ngk
+        if c.scheme == KIVI and c.k_group <= 32:
+            off["k_stats"] = off["k_scale"]          # 32/G groups x (scale row, zero row)
+            bb = off["k_stats"] + (32 // c.k_group) * 2 * c.head_dim * 4
+        return off, bb, rb, ngv, ngk
 
     def _block_field(self, name: str, width: int) -> torch.Tensor:
         """Bytes [off, off + 32*width) of every block as [B][H][cap][width] (a copy)."""
@@ -255,10 +259,17 @@ class QuantizedKVCache:
         c = self.cfg
         if name.startswith("k") and c.scheme == KIVI:
             rows = self.cap // c.k_group
+            which = 0 if name == "k_scale" else 1
+            if c.k_group <= 32:
+                per = 32 // c.k_group
+                f = self._block_field("k_stats", per * 2 * c.head_dim * 4 // 32)
+                f = f.contiguous().view(torch.float32)
+                f = f.reshape(c.batch, c.n_kv_heads, self.cap // 32, per, 2, c.head_dim)
+                return f[:, :, :, :, which, :].reshape(c.batch, c.n_kv_heads, -1)
             n = c.batch * c.n_kv_heads * rows * 2 * c.head_dim
             km = self.bufs["k_meta"][: n * 4].view(torch.float32)
             km = km.view(c.batch, c.n_kv_heads, rows, 2, c.head_dim)
-            return km[:, :, :, 0 if name == "k_scale" else 1, :].reshape(c.batch, c.n_kv_heads, -1)
+            return km[:, :, :, which, :].reshape(c.batch, c.n_kv_heads, -1)
         _, _, _, ngv, ngk = self._block_layout()
         cols = ngk if name.startswith("k") else ngv
         f = self._block_field(name, 4 * cols).contiguous().view(torch.float32)

@@ -44,12 +44,15 @@
  *             InnerQ only:
  *             K scale  f32 [32][d/k_group]   (per token, channel group)
  *             K zero   f32 [32][d/k_group]
- *           block_bytes = 64*d*bits/8 + 256*(d/v_group + (InnerQ ? d/k_group : 0)),
- *           a multiple of 128.
- *   KIVI:   k_meta  f32 [B][H][cap/G][2][d]  per G-token group: scale row,
- *                   then zero (= min) row, one value per channel
+ *             KIVI with G <= 32 only:
+ *             K stats  f32 [32/G][2][d]  per key group of the block: scale
+ *                      row, then zero (= min) row, one value per channel
+ *           block_bytes = 64*d*bits/8 + 256*(d/v_group + (InnerQ ? d/k_group : 0))
+ *                         + (KIVI, G <= 32 ? (32/G)*8*d : 0), a multiple of 128.
+ *   KIVI with G >= 64:
+ *           k_meta  f32 [B][H][cap/G][2][d]  the same two rows per key group
  *           (the buffer carries 64 bytes of slack after the last head)
- *           k_res, v_res   fp16 [B][H][R][d]  residual, oldest first
+ *   KIVI:   k_res, v_res   fp16 [B][H][R][d]  residual, oldest first
  *   InnerQ: k_mode, v_mode  u32 [B][H][cap*(d/group)/32]  bit i = group
  *                           i % (d/group) of token i / (d/group); 1 = symmetric
  *           k_res, v_res   fp16 [B][H][W][d]   recent window, a ring (see ring_head)
@@ -109,7 +112,7 @@ typedef struct kvq_config {
 /* Byte sizes of the cache buffers for a configuration (0 = unused). */
 typedef struct kvq_sizes {
   size_t blocks;  /* 32-token blocks of codes and per-token statistics */
-  size_t k_meta;  /* KIVI key statistics (0 under InnerQ) */
+  size_t k_meta;  /* KIVI key statistics for G >= 64 (0 otherwise) */
   size_t k_mode, v_mode;
   size_t k_res, v_res;
   size_t k_sink, v_sink;

@@ -44,9 +44,13 @@ def _cfg(**kw):
 def test_sizes_follow_layout():
     s = kvq.cache_sizes(_cfg(max_ctx=4300))
     BH, T, d = 8 * 32, 4352, 128      # per-head capacity: 4300 rounded up to 128
-    # a 32-token block: K codes, V codes (32 B a row), V scale, V zero (4 groups)
-    assert s.blocks == BH * (T // 32) * (2 * 32 * 32 + 2 * 32 * 4 * 4)
-    assert s.k_meta == BH * (T // 32) * 2 * d * 4 + 64
+    # a 32-token block: K codes, V codes (32 B a row), V scale, V zero (4 groups),
+    # then the scale and zero rows of its one 32-token key group
+    assert s.blocks == BH * (T // 32) * (2 * 32 * 32 + 2 * 32 * 4 * 4 + 2 * d * 4)
+    assert s.k_meta == 0
+    s64 = kvq.cache_sizes(_cfg(max_ctx=4300, k_group=64))
+    assert s64.blocks == BH * (T // 32) * (2 * 32 * 32 + 2 * 32 * 4 * 4)
+    assert s64.k_meta == BH * (T // 64) * 2 * d * 4 + 64
     assert s.k_res == BH * 128 * d * 2
     assert s.k_mode == 0 and s.k_sink == 0
     si = kvq.cache_sizes(_cfg(scheme=kvq.INNERQ, bits=4, k_group=64, v_group=64, residual=32,
@@ -62,7 +66,7 @@ def test_per_token_bytes_match_llama2_table():
     # codes of one token, all 32 layers x 32 heads, keys and values
     for bits, expect in ((2, 65536), (4, 131072)):
         s = kvq.cache_sizes(_cfg(bits=bits, batch=1, max_ctx=128, v_group=128))
-        meta = 128 * 32 * 2 * 4            # one value group: scale + zero per token
+        meta = 32 * (128 * 2 * 4 + 4 * 2 * 128 * 4)  # 32 heads: value + key statistics
         assert 32 * (s.blocks - meta) // 128 == expect
 
 
@@ -110,10 +114,10 @@ def test_calls_validate_before_touching_the_device():
     assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), None, None, 0,
                                   None) == kvq.KVQ_EALIGN
     c.blocks = 0x1000
-    c.k_meta = None
-    assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), None, None, 0,
+    c.k_meta = None          # needed only for key groups longer than a block
+    cfg64 = _cfg(k_group=64)
+    assert L.kvq_quantize_prefill(ctypes.byref(cfg64), ctypes.byref(c), None, None, 0,
                                   None) == kvq.KVQ_EINVAL
-    c.k_meta = 0x1000
     assert L.kvq_quantize_prefill(ctypes.byref(cfg), ctypes.byref(c), ctypes.c_void_p(0x2000),
                                   ctypes.c_void_p(0x2000), 5000, None) == kvq.KVQ_ECAPACITY
     assert L.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(c), ctypes.c_void_p(0x2000),
