@@ -72,22 +72,24 @@ struct TcArgs {
 };
 
 struct TcLayout {
-  int ring, bars, total;
+  int ring, sB, bars, total;
 };
 
-__host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot) {
+__host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int sb_bytes) {
   TcLayout L{};
   L.ring = 0;
-  L.bars = L.ring + kWarps * nslot * slot_bytes;  // per warp: nslot + 1 mbarriers
+  L.sB = L.ring + kWarps * nslot * slot_bytes;  // per warp: key operand + zero block
+  L.bars = L.sB + kWarps * sb_bytes;            // per warp: nslot + 1 mbarriers
   L.total = L.bars + kWarps * (nslot + 1) * 8;
   return L;
 }
 
 // Compile-time layout of one warp-ring slot (one 32-token tile).  The first
 // BB bytes are a copy of the cache block (K codes, V codes, V scale, V zero,
-// InnerQ K scale, K zero); then the KIVI key statistics of the tile's group(s)
-// (scale row, zero row per group; the key MMA operand is later built in
-// place of them), the query row on the first tile of a head, and 64 bytes
+// InnerQ K scale, K zero; KIVI G <= 32 key statistics); for KIVI G >= 64 the
+// statistics of the tile's key group (scale row, zero row); the query row
+// on the first tile of a head.  Outside the ring each warp keeps its KIVI key
+// operand (fp16 hi/lo words in fragment order, per key group) and 64 bytes
 // that stay zero.
 // KM (KIVI): 2 = G 16, two key groups per tile, statistics inside the block;
 // 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
@@ -106,10 +108,11 @@ struct SlotCfg {
   static constexpr int KMB = SCHEME == KVQ_KIVI && !KIN ? KGB : 0;  // separate copy
   static constexpr int off_km = KIN ? off_ks : BB;
   static constexpr int off_q = BB + KMB;
-  static constexpr int off_zero = off_q + kD * 2;
-  static constexpr int bytes = (off_zero + 64 + 127) & ~127;
-  static constexpr int nslot = tc_layout(bytes, 3).total <= 112 * 1024 ? 3 : 2;
-  static constexpr int smem = tc_layout(bytes, nslot).total;
+  static constexpr int bytes = off_q + kD * 2;
+  static constexpr int SBB = (SCHEME == KVQ_KIVI ? (KM == 2 ? 2 : 1) * 512 : 0) + 64;
+  static constexpr int sb_zero = SBB / 4 - 16;  // word offset of the zero block
+  static constexpr int nslot = tc_layout(bytes, 3, SBB).total <= 112 * 1024 ? 3 : 2;
+  static constexpr int smem = tc_layout(bytes, nslot, SBB).total;
 };
 
 
@@ -286,11 +289,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   constexpr int nslot = SC::nslot;
   constexpr int SLOT = SC::bytes;
   const Geometry &g = a.g;
-  constexpr TcLayout Ly = tc_layout(SLOT, nslot);
+  constexpr TcLayout Ly = tc_layout(SLOT, nslot, SC::SBB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   uint8_t *wring = smem + Ly.ring + warp * nslot * SLOT;
   uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
+  uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB + warp * SC::SBB);
 
   const int x0 = (int)((int64_t)blockIdx.x * a.total / a.nc);
   const int x1 = (int)((int64_t)(blockIdx.x + 1) * a.total / a.nc);
@@ -299,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // Each warp owns its ring and barriers; nothing below synchronises warps.
   for (int i = lane; i < nslot * SLOT / 16; i += 32)
     reinterpret_cast<uint4 *>(wring)[i] = make_uint4(0, 0, 0, 0);
+  if (lane < 16) sBw[SC::sb_zero + lane] = 0u;
   if (lane == 0) {
     for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -337,12 +342,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     uint8_t *dst = wring + ps * SLOT;
     uint64_t *bar = &wbars[ps];
     ps = ps + 1 == nslot ? 0 : ps + 1;
-    if (SCHEME == KVQ_KIVI) {
-      // the key operand was written into this slot by the generic proxy:
-      // order those writes before the copy that overwrites the slot
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-    }
     if (lane == 0) {
       bar_expect_tx(bar, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)));
       bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
@@ -590,14 +589,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
           float bias0 = 0.0f, bias1 = 0.0f;
           uint32_t bk[8][2];
-          // KIVI key operand, built in place of the tile's key statistics
-          uint32_t *sBw = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(slot) + SC::off_km);
           auto load_bk = [&](int gl) {
             if (SCHEME == KVQ_KIVI) {
               // lanes of columns >= 2 read the zero block: no divergent branch
               const uint4 *src = reinterpret_cast<const uint4 *>(
-                  gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16
-                          : reinterpret_cast<const uint32_t *>(slot + SC::off_zero));
+                  gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + SC::sb_zero);
   #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const uint4 v4 = src[i];
@@ -617,11 +613,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           bool two_groups = false;
           if (SCHEME == KVQ_KIVI) {
             // q~ = q * scale (normalised, position factor divided out) as fp16
-            // hi/lo in B-fragment order, and q . zero, per key group of the
-            // tile.  All statistics are read before the operand overwrites them.
+            // hi/lo in B-fragment order, and q . zero, per key group of the tile
             const float *km = reinterpret_cast<const float *>(slot + SC::off_km);
             two_groups = G16 && (FULL || n > 16);
-            uint32_t whi[2][2], wlo[2][2];
   #pragma unroll
             for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
               if (gl == 1 && !two_groups) break;
@@ -630,23 +624,16 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   #pragma unroll
               for (int r = 0; r < 2; ++r) {
                 const int clo = b_clo[r], chi = b_clo[r] + kHalf;
-                split2(qn_lo[r] * ks[clo], qn_hi[r] * ks[chi], whi[gl][r], wlo[gl][r]);
+                uint32_t hi, lo;
+                split2(qn_lo[r] * ks[clo], qn_hi[r] * ks[chi], hi, lo);
+                sBw[gl * 128 + b_sidx[r]] = hi;
+                sBw[gl * 128 + 64 + b_sidx[r]] = lo;
                 bz = fmaf(qf_lo[r], kz[clo], fmaf(qf_hi[r], kz[chi], bz));
               }
   #pragma unroll
               for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
               if (gl == 0) bias0 = bz;
               bias1 = bz;
-            }
-            __syncwarp();
-  #pragma unroll
-            for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
-              if (gl == 1 && !two_groups) break;
-  #pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                sBw[gl * 128 + b_sidx[r]] = whi[gl][r];
-                sBw[gl * 128 + 64 + b_sidx[r]] = wlo[gl][r];
-              }
             }
             __syncwarp();
           }
@@ -778,10 +765,22 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           const float p = exp2f(score - m_run);
           l_lane += p;
           {
-            const float *vz = reinterpret_cast<const float *>(slot + SC::off_vz);
+            const float *vz = reinterpret_cast<const float *>(slot + SC::off_vz) + t * NGV;
+            float zr[NGV];
+            if (NGV == 4) {
+              const float4 z4 = *reinterpret_cast<const float4 *>(vz);
+              zr[0] = z4.x;
+              zr[1] = z4.y;
+              zr[2 % NGV] = z4.z;
+              zr[3 % NGV] = z4.w;
+            } else {
+              const float2 z2 = *reinterpret_cast<const float2 *>(vz);
+              zr[0] = z2.x;
+              zr[1 % NGV] = z2.y;
+            }
   #pragma unroll
             for (int j = 0; j < NGV; ++j)
-              z_lane[j] = (FULL || p > 0.0f) ? fmaf(p, vz[t * NGV + j], z_lane[j]) : z_lane[j];
+              z_lane[j] = (FULL || p > 0.0f) ? fmaf(p, zr[j], z_lane[j]) : z_lane[j];
           }
           // ------------- values: B = p * scale (hi/lo), A = codes ------------
           const float *vs = reinterpret_cast<const float *>(slot + SC::off_vs);
@@ -789,7 +788,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           const bool bact = gid < 2 * NGV;
           const int nkb = (FULL || n > 16) ? 2 : 1;
           for (int kb = 0; kb < nkb; ++kb) {
-            const int tk0 = 16 * kb + 2 * tig, tk1 = tk0 + 1, tk2 = tk0 + 8, tk3 = tk0 + 9;
+            // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) carry tokens
+            // tig + {0, 4} and tig + {8, 12}: rows 4 apart hit distinct banks
+            const int tk0 = 16 * kb + tig, tk1 = tk0 + 4, tk2 = tk0 + 8, tk3 = tk0 + 12;
             const float p0 = __shfl_sync(0xffffffffu, p, tk0), p1 = __shfl_sync(0xffffffffu, p, tk1);
             const float p2 = __shfl_sync(0xffffffffu, p, tk2), p3 = __shfl_sync(0xffffffffu, p, tk3);
             const float x0 = (FULL || p0 > 0.0f) ? p0 * vs[tk0 * NGV + jg] : 0.0f;
