@@ -62,6 +62,8 @@ struct TcArgs {
   float scale_log2;
   int64_t n_quant, n_fp16, n_sink;
   int S_h, F_h, U;  // quantized units, fp16 units, units per head
+  int CPU;          // fp16 chunks per fp16 unit
+  int nch;          // fp16 chunks per head
   int total;        // BH * U
   int nc;           // resident blocks
   float *ws_ml, *ws_o;
@@ -89,8 +91,8 @@ __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int 
 // InnerQ K scale, K zero; KIVI G <= 32 key statistics); for KIVI G >= 64 the
 // statistics of the tile's key group (scale row, zero row); the query row
 // on the first tile of a head.  Outside the ring each warp keeps its KIVI key
-// operand (fp16 hi/lo words in fragment order, per key group) and 64 bytes
-// that stay zero.
+// operand (fp16 hi/lo words in fragment order, per key group), reused to
+// transpose the output row at a head's end, and 64 bytes that stay zero.
 // KM (KIVI): 2 = G 16, two key groups per tile, statistics inside the block;
 // 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
 // from the separate key-statistics array.
@@ -109,7 +111,10 @@ struct SlotCfg {
   static constexpr int off_km = KIN ? off_ks : BB;
   static constexpr int off_q = BB + KMB;
   static constexpr int bytes = off_q + kD * 2;
-  static constexpr int SBB = (SCHEME == KVQ_KIVI ? (KM == 2 ? 2 : 1) * 512 : 0) + 64;
+  static constexpr int CH = off_q / (4 * kD) < 8 ? off_q / (4 * kD) : 8;  // fp16 tokens per chunk
+  // per warp: KIVI key operand (512 B per group; also the 512 B output
+  // transpose at a head's end) + 64 zero bytes
+  static constexpr int SBB = (SCHEME == KVQ_KIVI && KM == 2 ? 1024 : 512) + 64;
   static constexpr int sb_zero = SBB / 4 - 16;  // word offset of the zero block
   static constexpr int nslot = tc_layout(bytes, 3, SBB).total <= 112 * 1024 ? 3 : 2;
   static constexpr int smem = tc_layout(bytes, nslot, SBB).total;
@@ -222,14 +227,36 @@ __device__ __forceinline__ int owner_of(int x, int total, int nc) {
   return (int)(((int64_t)(x + 1) * nc - 1) / total);
 }
 
-// Quantized segments of head bh (one per block touching its quantized units)
-// and the head's partial count: every warp of every such block leaves one
-// partial, and so does every warp of the block owning the fp16 item.
-__device__ __forceinline__ void head_parts(const TcArgs &a, int bh, int &nseg, int &nparts) {
+// Unit range [x0, x1) of block x.
+__device__ __forceinline__ void block_range(const TcArgs &a, int x, int &x0, int &x1) {
+  x0 = (int)((int64_t)x * a.total / a.nc);
+  x1 = (int)((int64_t)(x + 1) * a.total / a.nc);
+}
+
+// What block range [x0, x1) holds of head bh: quantized tokens [tq0, tq1)
+// (from its units [0, S_h)) and fp16 chunks [c0, c1) (from its units
+// [S_h, U), CPU chunks each).
+struct Seg {
+  int tq0, tq1, c0, c1;
+};
+__device__ __forceinline__ Seg seg_in(const TcArgs &a, int bh, int x0, int x1) {
+  Seg s;
   const int base = bh * a.U;
-  nseg = a.S_h > 0 ? owner_of(base + a.S_h - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1
-                   : 0;
-  nparts = kWarps * (nseg + (a.F_h > 0 ? 1 : 0));
+  const int ua = max(x0, base) - base;
+  const int ub = min(min(x1, base + a.U) - base, a.S_h);
+  s.tq0 = ua * kUnit;
+  s.tq1 = ua < ub ? (int)min((int64_t)ub * kUnit, a.n_quant) : s.tq0;
+  const int fa = max(x0 - base - a.S_h, 0), fb = min(x1 - base - a.S_h, a.F_h);
+  s.c0 = fa * a.CPU;
+  s.c1 = fa < fb ? min(fb * a.CPU, a.nch) : s.c0;
+  return s;
+}
+
+// Partials of head bh: one per warp of every block whose units touch it
+// (quantized or fp16), slot 8 * (block - first such block) + warp.
+__device__ __forceinline__ int head_nparts(const TcArgs &a, int bh) {
+  const int base = bh * a.U;
+  return kWarps * (owner_of(base + a.U - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1);
 }
 
 // One warp publishes partial `slot` of head bh (its o values are already
@@ -242,8 +269,7 @@ __device__ void warp_publish(const TcArgs &a, int bh, int slot, float m, float l
     a.ws_ml[(base + slot) * 2] = m;
     a.ws_ml[(base + slot) * 2 + 1] = l;
   }
-  int nseg, nparts;
-  head_parts(a, bh, nseg, nparts);
+  const int nparts = head_nparts(a, bh);
   __threadfence();
   __syncwarp();
   int last = 0;
@@ -296,9 +322,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
   uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB + warp * SC::SBB);
 
-  const int x0 = (int)((int64_t)blockIdx.x * a.total / a.nc);
-  const int x1 = (int)((int64_t)(blockIdx.x + 1) * a.total / a.nc);
+  int x0, x1;
+  block_range(a, blockIdx.x, x0, x1);
   const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
+  // fp16 tokens per chunk: a chunk's K and V rows fill the slot up to the query
+  constexpr int CH = SC::CH;
 
   // Each warp owns its ring and barriers; nothing below synchronises warps.
   for (int i = lane; i < nslot * SLOT / 16; i += 32)
@@ -311,56 +339,76 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncwarp();
 
-  // quantized token range [tq0, tq1) of head bh inside this block's units
-  auto seg_of = [&](int bh, int &tq0, int &tq1) {
-    const int base = bh * a.U;
-    const int ua = max(x0, base) - base;
-    const int ub = min(min(x1, base + a.U) - base, a.S_h);
-    tq0 = ua * kUnit;
-    tq1 = ua < ub ? (int)min((int64_t)ub * kUnit, a.n_quant) : tq0;
-  };
-
-  // ---- producer: this warp's tiles in the order the consumer visits them --
-  int pc_bh = -1, pc_tq0 = 0, pc_tq1 = 0, pc_lt = 0, issued = 0, ps = 0;
+  // ---- producer: this warp's items in the order the consumer visits them:
+  // per head, its quantized tiles lt = warp, warp + 8, ..., then its fp16
+  // chunks lt = warp, warp + 8, ... of this block's segments.
+  int pc_bh = bh_first, pc_ph = 0, pc_lt = warp, pc_n = 0, issued = 0, ps = 0;
+  Seg pc_seg = seg_in(a, pc_bh, x0, x1);
+  pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
   auto pc_settle = [&]() {
-    while (pc_bh >= 0 && pc_tq0 + kTile * pc_lt >= pc_tq1) {
-      if (++pc_bh > bh_last) {
-        pc_bh = -1;
-        return;
+    while (pc_bh >= 0 && pc_lt >= pc_n) {
+      if (pc_ph == 0) {
+        pc_ph = 1;
+        pc_n = pc_seg.c1 - pc_seg.c0;
+      } else {
+        if (++pc_bh > bh_last) {
+          pc_bh = -1;
+          return;
+        }
+        pc_ph = 0;
+        pc_seg = seg_in(a, pc_bh, x0, x1);
+        pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
       }
-      seg_of(pc_bh, pc_tq0, pc_tq1);
       pc_lt = warp;
     }
   };
   // Called by the whole warp; lane 0 posts the byte count and issues the
-  // copies of the next tile of this warp: its cache block, the KIVI key
-  // statistics of its group(s), and the query row on the first tile of a head.
+  // copies of the next item of this warp.  A quantized tile: its cache block
+  // and, for KIVI G >= 64, its key group's statistics.  An fp16 chunk: its K
+  // rows, then its V rows (sink rows before residual / window rows).  The
+  // query row rides along with the warp's first item of each phase of a head.
   auto issue_next = [&]() {
     if (pc_bh < 0) return;
-    const int tok0 = pc_tq0 + kTile * pc_lt;
     const bool first = pc_lt == warp;
     uint8_t *dst = wring + ps * SLOT;
     uint64_t *bar = &wbars[ps];
     ps = ps + 1 == nslot ? 0 : ps + 1;
     if (lane == 0) {
-      bar_expect_tx(bar, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)));
-      bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
-               SC::BB, bar);
-      if (SCHEME == KVQ_KIVI && !SC::KIN)
-        bulk_g2s(dst + SC::off_km,
-                 a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
-                 SC::KMB, bar);
-      if (first)
-        bulk_g2s(dst + SC::off_q, a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD,
-                 kD * 2, bar);
+      const __half *qrow = a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD;
+      if (pc_ph == 0) {
+        const int tok0 = pc_seg.tq0 + kTile * pc_lt;
+        bar_expect_tx(bar, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)));
+        bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
+                 SC::BB, bar);
+        if (SCHEME == KVQ_KIVI && !SC::KIN)
+          bulk_g2s(dst + SC::off_km,
+                   a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
+                   SC::KMB, bar);
+      } else {
+        const int ns = (int)a.n_sink;
+        const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
+        const int s0 = min(i0, ns), s1 = min(i1, ns);            // sink rows
+        const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;  // residual / window rows
+        bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2 + (first ? kD * 2 : 0)));
+        if (s1 > s0) {
+          const int64_t row = (int64_t)pc_bh * g.n_sink + s0;
+          bulk_g2s(dst, a.p.k_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+          bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+        }
+        if (r1 > r0) {
+          const int64_t row = (int64_t)pc_bh * g.residual + r0;
+          const int o = (s1 - s0) * kD * 2;
+          bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((r1 - r0) * kD * 2), bar);
+          bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD, (uint32_t)((r1 - r0) * kD * 2),
+                   bar);
+        }
+      }
+      if (first) bulk_g2s(dst + SC::off_q, qrow, kD * 2, bar);
     }
     ++issued;
     pc_lt += kWarps;
     pc_settle();
   };
-  pc_bh = bh_first;
-  seg_of(pc_bh, pc_tq0, pc_tq1);
-  pc_lt = warp;
   pc_settle();
   for (int s = 0; s < nslot; ++s) issue_next();
 
@@ -467,9 +515,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   };
   reset_state();
 
-  // Warp state -> partial `slot` of head bh (lanes hold one token each, so
-  // every lane counts).
-  auto flush = [&](int bh, int slot) {
+  // Warp state -> partial `slot` of head bh.  The quantized-token state
+  // (online softmax over MMA fragments; lanes hold one token each for l and
+  // z) and the fp16-token state (mf, lf, af: a lane owns channels 4*lane ..
+  // 4*lane + 3) are joined with the log-sum-exp rule; the quantized output
+  // row goes through the warp's operand area to reach the lane layout.
+  auto flush = [&](int bh, int slot, float mf, float lf, const float (&af)[4]) {
     float l = l_lane;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
@@ -481,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
       Z[j] = z;
     }
-    float *wo = a.ws_o + ((int64_t)bh * a.part_stride + slot) * kD;
+    float *so = reinterpret_cast<float *>(sBw);
     const int gc = (gid * NGV) >> 3;  // value group of this thread's 16 channels
     if (tig == gc) {
       float zc = Z[0];
@@ -491,92 +542,64 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const float invf = kSub / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
-        wo[16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
-        wo[16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
+        so[16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
+        so[16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
       }
     }
-    warp_publish(a, bh, slot, m_run, l);
+    __syncwarp();
+    const float4 oq = reinterpret_cast<const float4 *>(so)[lane];
+    __syncwarp();
+    const float m = fmaxf(m_run, mf);
+    const float wq = m_run == -INFINITY ? 0.0f : exp2f(m_run - m);
+    const float wf = mf == -INFINITY ? 0.0f : exp2f(mf - m);
+    float4 o;
+    o.x = fmaf(oq.x, wq, af[0] * wf);
+    o.y = fmaf(oq.y, wq, af[1] * wf);
+    o.z = fmaf(oq.z, wq, af[2] * wf);
+    o.w = fmaf(oq.w, wq, af[3] * wf);
+    reinterpret_cast<float4 *>(a.ws_o + ((int64_t)bh * a.part_stride + slot) * kD)[lane] = o;
+    warp_publish(a, bh, slot, m, fmaf(l, wq, lf * wf));
     reset_state();
   };
 
-  // fp16 sink + residual / window tokens of head bh: this warp takes every
-  // kWarps-th token (a lane owns 4 channels) and publishes partial `slot`.
-  auto fp16_item = [&](int bh, int slot) {
-    const int n = (int)a.n_fp16, ns = (int)a.n_sink;
-    float qq[4];
-    {
-      const uint2 qr = __ldg(reinterpret_cast<const uint2 *>(
-                                 a.q + ((int64_t)(bh / g.H) * g.Hq + bh % g.H) * kD) + lane);
-      const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
-      const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
-      qq[0] = q01.x * a.scale_log2;
-      qq[1] = q01.y * a.scale_log2;
-      qq[2] = q23.x * a.scale_log2;
-      qq[3] = q23.y * a.scale_log2;
-    }
-    float m = -INFINITY, l = 0.0f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = warp; i < n; i += kWarps) {
-      const int64_t kr = i < ns ? ((int64_t)bh * g.n_sink + i) : ((int64_t)bh * g.residual + (i - ns));
-      const __half *krow = (i < ns ? a.p.k_sink : a.p.k_res) + kr * kD;
-      const __half *vrow = (i < ns ? a.p.v_sink : a.p.v_res) + kr * kD;
-      const uint2 kw = __ldg(reinterpret_cast<const uint2 *>(krow) + lane);
-      const uint2 vw = __ldg(reinterpret_cast<const uint2 *>(vrow) + lane);
-      const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
-      const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
-      const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
-      const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
-      float sc = fmaf(qq[0], k01.x, fmaf(qq[1], k01.y, fmaf(qq[2], k23.x, qq[3] * k23.y)));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
-      const float mn = fmaxf(m, sc);
-      const float al = exp2f(m - mn), pp = exp2f(sc - mn);
-      l = fmaf(l, al, pp);
-      acc[0] = fmaf(acc[0], al, pp * v01.x);
-      acc[1] = fmaf(acc[1], al, pp * v01.y);
-      acc[2] = fmaf(acc[2], al, pp * v23.x);
-      acc[3] = fmaf(acc[3], al, pp * v23.y);
-      m = mn;
-    }
-    float4 o;
-    o.x = acc[0];
-    o.y = acc[1];
-    o.z = acc[2];
-    o.w = acc[3];
-    reinterpret_cast<float4 *>(a.ws_o + ((int64_t)bh * a.part_stride + slot) * kD)[lane] = o;
-    warp_publish(a, bh, slot, m, l);
-  };
-
-  int done = 0;          // tiles whose copies completed
-  int cs = 0;            // ring slot of the next tile
+  int done = 0;          // items whose copies completed
+  int cs = 0;            // ring slot of the next item
   uint32_t cph = 0;      // its barrier phase parity
   bool first = true;
-  for (int bh = bh_first; bh <= bh_last; ++bh) {
-    int tq0, tq1;
-    seg_of(bh, tq0, tq1);
+  // Waits for the next ring slot.  One verdict per warp: every lane takes
+  // the same path; false (status word set) on timeout.
+  auto wait_slot = [&](int &s_out) -> bool {
+    const int s = cs;
+    const uint32_t par = cph;
+    if (++cs == nslot) {
+      cs = 0;
+      cph ^= 1u;
+    }
+    bool ok = true;
+    if (first && a.stall_limit > 0) ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
+    first = false;
+    if (ok) ok = bar_wait(&wbars[s], par, a.wait_limit);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+      return false;
+    }
+    ++done;
+    s_out = s;
+    return true;
+  };
+  bool aborted = false;
+  for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
+    const Seg sg = seg_in(a, bh, x0, x1);
+    const int tq0 = sg.tq0, tq1 = sg.tq1;
     const int base = bh * a.U;
-    const bool own_fp16 = a.F_h > 0 && x0 <= base + a.S_h && base + a.S_h < x1;
-    if (tq1 <= tq0 && !own_fp16) continue;
     if (tq1 > tq0) {
       const int nt = (tq1 - tq0 + kTile - 1) / kTile;
-      bool aborted = false;
       for (int lt = warp; lt < nt; lt += kWarps) {
-        const int s = cs;
-        const uint32_t par = cph;
-        if (++cs == nslot) {
-          cs = 0;
-          cph ^= 1u;
-        }
-        bool ok = true;
-        if (first && a.stall_limit > 0) ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
-        first = false;
-        if (ok) ok = bar_wait(&wbars[s], par, a.wait_limit);
-        // one verdict per warp: every lane takes the same path from here
-        if (!__all_sync(0xffffffffu, ok)) {
-          if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+        int s;
+        if (!wait_slot(s)) {
           aborted = true;
           break;
         }
-        ++done;
         const uint8_t *slot = wring + s * SLOT;
         if (lt == warp) start_head(slot);
         const int tok0 = tq0 + kTile * lt;
@@ -847,21 +870,109 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         __syncwarp();
         issue_next();  // refill the slot just consumed
       }
-      if (aborted) {
-        // give up this block's work for this warp; its copies complete first
-        if (lane == 0)
-          for (int i = done; i < issued; ++i)
-            bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
-        return;
+      if (aborted) break;
+    }
+    // fp16 sink + residual / window chunks of this block's segment: chunk
+    // lt goes to warp lt mod 8; a lane owns channels 4*lane .. 4*lane + 3.
+    const int nchk = sg.c1 - sg.c0;
+    if (tq1 <= tq0 && nchk <= 0) continue;
+    float mf = -INFINITY, lf = 0.0f, af[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      for (int lt = warp; lt < nchk; lt += kWarps) {
+        int s;
+        if (!wait_slot(s)) {
+          aborted = true;
+          break;
+        }
+        const uint8_t *slot = wring + s * SLOT;
+        if (lt == warp) {
+          const uint2 qr = reinterpret_cast<const uint2 *>(slot + SC::off_q)[lane];
+          const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
+          const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
+          q4[0] = q01.x * a.scale_log2;
+          q4[1] = q01.y * a.scale_log2;
+          q4[2] = q23.x * a.scale_log2;
+          q4[3] = q23.y * a.scale_log2;
+        }
+        const int i0 = (sg.c0 + lt) * CH;
+        const int nv = min(CH, (int)a.n_fp16 - i0);  // valid rows of the chunk
+        const uint2 *kr = reinterpret_cast<const uint2 *>(slot);
+        const uint2 *vr = reinterpret_cast<const uint2 *>(slot + CH * kD * 2);
+        // partial dot products of the lane's 4 channels, then a reduce-scatter:
+        // after it lane L holds the score of row (L >> 2) & 7 of the chunk
+        float sp[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          sp[t] = 0.0f;
+          if (t < CH && t < nv) {
+            const uint2 kw = kr[t * (kD / 4) + lane];
+            const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
+            const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
+            sp[t] = fmaf(q4[0], k01.x, fmaf(q4[1], k01.y, fmaf(q4[2], k23.x, q4[3] * k23.y)));
+          }
+        }
+        {
+          const bool h4 = lane & 16;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float mine = h4 ? sp[j + 4] : sp[j], other = h4 ? sp[j] : sp[j + 4];
+            sp[j] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
+          }
+          const bool h3 = lane & 8;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float mine = h3 ? sp[j + 2] : sp[j], other = h3 ? sp[j] : sp[j + 2];
+            sp[j] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+          }
+          const bool h2 = lane & 4;
+          const float mine = h2 ? sp[1] : sp[0], other = h2 ? sp[0] : sp[1];
+          sp[0] = mine + __shfl_xor_sync(0xffffffffu, other, 4);
+          sp[0] += __shfl_xor_sync(0xffffffffu, sp[0], 2);
+          sp[0] += __shfl_xor_sync(0xffffffffu, sp[0], 1);
+        }
+        const int row = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+        const float sc = row < nv ? sp[0] : -INFINITY;
+        float mc = sc;
+        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 4));
+        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 8));
+        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
+        const float mn = fmaxf(mf, mc);
+        const float al = exp2f(mf - mn);
+        const float pr = exp2f(sc - mn);  // 0 for rows past the chunk's end
+        float ps_ = pr;
+        ps_ += __shfl_xor_sync(0xffffffffu, ps_, 4);
+        ps_ += __shfl_xor_sync(0xffffffffu, ps_, 8);
+        ps_ += __shfl_xor_sync(0xffffffffu, ps_, 16);
+        lf = fmaf(lf, al, ps_);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) af[i] *= al;
+        mf = mn;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          if (t < CH && t < nv) {
+            // row t's probability sits in lanes whose bits 4,3,2 spell t
+            const float pt = __shfl_sync(0xffffffffu, pr, ((t >> 2) << 4) | (((t >> 1) & 1) << 3) | ((t & 1) << 2));
+            const uint2 vw = vr[t * (kD / 4) + lane];
+            const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+            const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+            af[0] = fmaf(pt, v01.x, af[0]);
+            af[1] = fmaf(pt, v01.y, af[1]);
+            af[2] = fmaf(pt, v23.x, af[2]);
+            af[3] = fmaf(pt, v23.y, af[3]);
+          }
+        }
+        __syncwarp();
+        issue_next();
       }
-      const int seg = (int)blockIdx.x - owner_of(base, a.total, a.nc);
-      flush(bh, seg * kWarps + warp);
+      if (aborted) break;
     }
-    if (own_fp16) {
-      int nseg, nparts;
-      head_parts(a, bh, nseg, nparts);
-      fp16_item(bh, nseg * kWarps + warp);
-    }
+    flush(bh, kWarps * ((int)blockIdx.x - owner_of(base, a.total, a.nc)) + warp, mf, lf, af);
+  }
+  if (aborted) {
+    // give up this block's work for this warp; its copies complete first
+    if (lane == 0)
+      for (int i = done; i < issued; ++i)
+        bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
   }
 }
 
@@ -869,7 +980,9 @@ template <int BITS, int SCHEME, int NGV, int NGK, int KM>
 cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM>;
   constexpr int smem = SlotCfg<BITS, SCHEME, NGV, NGK, KM>::smem;
-  if (a.g.block_bytes != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::BB) return cudaErrorInvalidValue;
+  if (a.g.block_bytes != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::BB ||
+      tc_fp16_chunk(a.g) != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::CH)
+    return cudaErrorInvalidValue;
   static int occ = 0;
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -937,15 +1050,17 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.n_quant = n_quant;
   a.n_fp16 = n_resid + n_sink;
   a.n_sink = n_sink;
-  const int RB = kD * g.bits / 8;
-  const int ngv = kD / g.v_group;
   a.S_h = (int)((n_quant + kUnit - 1) / kUnit);
-  // fp16 item weight in units: its bytes against a unit's bytes, x2 for the
-  // CUDA-core path
-  const int64_t unit_bytes = 2LL * kUnit * RB + 2LL * kUnit * ngv * 4 +
-                             (g.scheme == KVQ_KIVI ? 2LL * (kUnit / g.k_group) * kD * 4
-                                                   : 2LL * kUnit * (kD / g.k_group) * 4);
-  a.F_h = a.n_fp16 > 0 ? (int)((a.n_fp16 * kD * 2 * 2 * 2 + unit_bytes - 1) / unit_bytes) : 0;
+  // fp16 rows travel in chunks of CH tokens (K and V rows fill a ring slot up
+  // to its query row; the kernel's SlotCfg::CH is the same expression), and
+  // CPU chunks -- about a unit's bytes -- make one work unit.
+  const int kmb = (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens) ? 2 * kD * 4 : 0;
+  const int CH = tc_fp16_chunk(g);
+  const int64_t unit_bytes = (int64_t)(kUnit / kBlockTokens) * (g.block_bytes + kmb);
+  a.CPU = (int)(unit_bytes / (CH * 4 * kD));
+  if (a.CPU < 1) a.CPU = 1;
+  a.nch = (int)((a.n_fp16 + CH - 1) / CH);
+  a.F_h = (a.nch + a.CPU - 1) / a.CPU;
   a.U = a.S_h + a.F_h;
   const int64_t total = (int64_t)g.B * g.H * a.U;
   if (total >= (1LL << 31)) return cudaErrorInvalidValue;

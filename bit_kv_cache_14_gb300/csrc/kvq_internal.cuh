@@ -86,14 +86,22 @@ cudaError_t launch_append(const Geometry &g, const CachePtrs &p, const __half *k
 // per 128 quantized tokens plus the fp16 segment.
 inline int part_slots(const Geometry &g) { return (int)(g.cap / kCapAlign) + 2; }
 
-// The tensor-core decode kernel leaves one partial per warp (8 per block) for
-// every block that touches a head, plus 8 for the fp16 item; it never uses
-// more than kTcMaxBlocks blocks.
+// The tensor-core decode kernel cuts each head into 128-token units of
+// quantized tokens plus units of fp16 chunks (tc_fp16_chunk tokens each,
+// at least one chunk per unit) and leaves one partial per warp (8 per block)
+// for every block that touches a head's units; it never uses more than
+// kTcMaxBlocks blocks.
 constexpr int kTcWarps = 8;
 constexpr int kTcMaxBlocks = 1024;
+inline int tc_fp16_chunk(const Geometry &g) {
+  const int kmb = (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens) ? 2 * g.d * 4 : 0;
+  const int ch = (g.block_bytes + kmb) / (4 * g.d);
+  return ch < 8 ? ch : 8;
+}
 inline int tc_part_slots(const Geometry &g) {
-  int64_t u = g.cap / kCapAlign;
-  if (u > kTcMaxBlocks) u = kTcMaxBlocks;
+  const int ch = tc_fp16_chunk(g) > 0 ? tc_fp16_chunk(g) : 1;
+  int64_t u = g.cap / kCapAlign + (g.residual + g.n_sink + ch - 1) / ch + 1;
+  if (u > kTcMaxBlocks + 1) u = kTcMaxBlocks + 1;
   return (int)(kTcWarps * (u + 1));
 }
 
