@@ -52,6 +52,12 @@ constexpr int kUnit = 128;    // tokens per stream-K work unit
 constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
 constexpr int kD = 128;
 constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
+// Lazy online softmax: probabilities are taken against a running reference
+// that may sit up to kSlack (log2 units) below the true maximum, so p <= 2^8;
+// the value operand carries p * 2^-8 and the output row multiplies it back.
+constexpr float kSlack = 8.0f;
+constexpr float kSlackScale = 256.0f;
+constexpr float kInvSlack = 1.0f / 256.0f;
 constexpr int kDrainLimit = 1 << 26;
 
 struct TcArgs {
@@ -541,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         if (j == gc) zc = Z[j];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const float invf = kSub / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
+        const float invf = kSub * kSlackScale / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
         so[16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
         so[16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
       }
@@ -611,26 +617,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           // ------------- keys: two 16-token MMA tiles ------------------------
           float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
           float bias0 = 0.0f, bias1 = 0.0f;
-          uint32_t bk[8][2];
-          auto load_bk = [&](int gl) {
+          // key operand words of MMA k-block kb for key group gl (loaded next
+          // to their use to keep few registers live)
+          auto bk_at = [&](int gl, int kb) -> uint2 {
             if (SCHEME == KVQ_KIVI) {
               // lanes of columns >= 2 read the zero block: no divergent branch
-              const uint4 *src = reinterpret_cast<const uint4 *>(
-                  gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + SC::sb_zero);
-  #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint4 v4 = src[i];
-                bk[2 * i][0] = v4.x;
-                bk[2 * i][1] = v4.y;
-                bk[2 * i + 1][0] = v4.z;
-                bk[2 * i + 1][1] = v4.w;
-              }
+              const uint32_t *src = gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + SC::sb_zero;
+              return *reinterpret_cast<const uint2 *>(src + 2 * kb);
             } else {
-  #pragma unroll
-              for (int kb = 0; kb < 8; ++kb) {
-                bk[kb][0] = bqi[kb][0];
-                bk[kb][1] = bqi[kb][1];
-              }
+              return make_uint2(bqi[kb][0], bqi[kb][1]);
             }
           };
           bool two_groups = false;
@@ -660,7 +655,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             }
             __syncwarp();
           }
-          load_bk(0);
           if (BITS == 2) {
             const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
             const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
@@ -675,18 +669,16 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
                 const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
   #pragma unroll
                 for (int j = 0; j < 4; ++j) {
+                  const uint2 b = bk_at(0, 4 * m + j);
                   mma16816(d0, ext<2>(w00, s00, 2 * j), ext<2>(w01, s01, 2 * j),
-                           ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1),
-                           bk[4 * m + j][0], bk[4 * m + j][1]);
+                           ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1), b.x, b.y);
                   mma16816(d1, ext<2>(w10, s10, 2 * j), ext<2>(w11, s11, 2 * j),
-                           ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1),
-                           bk[4 * m + j][0], bk[4 * m + j][1]);
+                           ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1), b.x, b.y);
                 }
               }
             } else {
   #pragma unroll
               for (int t2 = 0; t2 < 2; ++t2) {
-                if (t2 == 1) load_bk(1);
                 const uint2 wa = t2 ? wa1 : wa0, wb = t2 ? wb1 : wb0;
   #pragma unroll
                 for (int m = 0; m < 2; ++m) {
@@ -694,14 +686,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
                   const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
   #pragma unroll
                   for (int j = 0; j < 4; ++j) {
+                    const uint2 b = bk_at(t2, 4 * m + j);
                     if (t2 == 0)
                       mma16816(d0, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
-                               bk[4 * m + j][0], bk[4 * m + j][1]);
+                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
                     else
                       mma16816(d1, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1),
-                               bk[4 * m + j][0], bk[4 * m + j][1]);
+                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
                   }
                 }
               }
@@ -711,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             // (the 4-bit group-16 case takes the same path with two groups)
   #pragma unroll
             for (int t2 = 0; t2 < 2; ++t2) {
-              if (two_groups && t2 == 1) load_bk(1);
+              const int gl = two_groups ? t2 : 0;
               const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid) * RB + 16 * tig);
               const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid + 8) * RB + 16 * tig);
               const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
@@ -720,14 +711,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
                 const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
   #pragma unroll
                 for (int j = 0; j < 2; ++j) {
+                  const uint2 b = bk_at(gl, 2 * m + j);
                   if (t2 == 0)
                     mma16816(d0, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
-                             bk[2 * m + j][0], bk[2 * m + j][1]);
+                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
                   else
                     mma16816(d1, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1),
-                             bk[2 * m + j][0], bk[2 * m + j][1]);
+                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
                 }
               }
             }
@@ -771,10 +761,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
           const bool valid = FULL || t < n;
           score = valid ? score : -INFINITY;
-          float mt_ = score;
+          // lazy rescaling: the reference m_run moves only when a score passes
+          // it by more than kSlack (one vote, no reduction on most tiles)
+          if (__any_sync(0xffffffffu, score > m_run + kSlack)) {
+            float mt_ = score;
   #pragma unroll
-          for (int off = 1; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
-          if (mt_ > m_run) {
+            for (int off = 1; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
             const float alpha = exp2f(m_run - mt_);
             l_lane *= alpha;
   #pragma unroll
@@ -785,7 +777,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
               for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
             m_run = mt_;
           }
-          const float p = exp2f(score - m_run);
+          const float p = exp2f(score - m_run);  // <= 2^kSlack
+          const float pv = p * kInvSlack;          // value operand scale: stays in fp16 range
           l_lane += p;
           {
             const float *vz = reinterpret_cast<const float *>(slot + SC::off_vz) + t * NGV;
@@ -814,8 +807,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) carry tokens
             // tig + {0, 4} and tig + {8, 12}: rows 4 apart hit distinct banks
             const int tk0 = 16 * kb + tig, tk1 = tk0 + 4, tk2 = tk0 + 8, tk3 = tk0 + 12;
-            const float p0 = __shfl_sync(0xffffffffu, p, tk0), p1 = __shfl_sync(0xffffffffu, p, tk1);
-            const float p2 = __shfl_sync(0xffffffffu, p, tk2), p3 = __shfl_sync(0xffffffffu, p, tk3);
+            const float p0 = __shfl_sync(0xffffffffu, pv, tk0), p1 = __shfl_sync(0xffffffffu, pv, tk1);
+            const float p2 = __shfl_sync(0xffffffffu, pv, tk2), p3 = __shfl_sync(0xffffffffu, pv, tk3);
             const float x0 = (FULL || p0 > 0.0f) ? p0 * vs[tk0 * NGV + jg] : 0.0f;
             const float x1 = (FULL || p1 > 0.0f) ? p1 * vs[tk1 * NGV + jg] : 0.0f;
             const float x2 = (FULL || p2 > 0.0f) ? p2 * vs[tk2 * NGV + jg] : 0.0f;
