@@ -358,6 +358,11 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     }
     a.out[((int64_t)b * g.Hq + h * RG + hh) * D + c] = Lsum > 0.0f ? O / Lsum : 0.0f;
   }
+  // leave the workspace zero, as the tensor-core path expects it
+  __syncthreads();
+  const int64_t p0 = (int64_t)bh * a.s_max * RG;
+  for (int i = tid; i < a.n_split * RG * D; i += kBlock) a.ws_o[p0 * D + i] = 0.0f;
+  for (int i = tid; i < a.n_split * RG * 2; i += kBlock) a.ws_ml[p0 * 2 + i] = 0.0f;
   if (tid == 0) a.ws_cnt[bh] = 0;
 }
 

@@ -265,41 +265,111 @@ __device__ __forceinline__ int head_nparts(const TcArgs &a, int bh) {
   return kWarps * (owner_of(base + a.U - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1);
 }
 
-// One warp publishes partial `slot` of head bh (its o values are already
-// stored), takes a ticket, and if it is the head's last partial, merges all
-// of them with the log-sum-exp rule and writes the output row.
-__device__ void warp_publish(const TcArgs &a, int bh, int slot, float m, float l) {
+// Partials are stored XOR-ed with kEnc: no float that arithmetic produces
+// (kEnc is a signalling NaN) encodes to 0, so a zero word means "not
+// written yet" and the zero-filled workspace starts empty.  Writers publish
+// without any fence: they store their partial and take a ticket with a
+// relaxed atomic whose result they look at only later.  The warp that took
+// the head's last ticket polls (bounded) until every partial is visible,
+// merges them with the log-sum-exp rule, writes the output row and zeroes
+// the partials and the ticket again.
+constexpr uint32_t kEnc = 0x7fbadbadu;
+constexpr int kMergePolls = 1 << 22;
+
+__device__ __forceinline__ uint4 enc4(float4 v) {
+  return make_uint4(__float_as_uint(v.x) ^ kEnc, __float_as_uint(v.y) ^ kEnc,
+                    __float_as_uint(v.z) ^ kEnc, __float_as_uint(v.w) ^ kEnc);
+}
+
+// Stores partial `slot` of head bh: the lane's 4 output channels and (lane 0)
+// m, l.  Returns the ticket of lane 0's relaxed atomic (read it later).
+__device__ __forceinline__ int publish_partial(const TcArgs &a, int bh, int slot, float4 o,
+                                               float m, float l) {
   const int lane = threadIdx.x & 31;
-  const int64_t base = (int64_t)bh * a.part_stride;
+  const int64_t row = (int64_t)bh * a.part_stride + slot;
+  reinterpret_cast<uint4 *>(a.ws_o + row * kD)[lane] = enc4(o);
+  int ticket = 0;
   if (lane == 0) {
-    a.ws_ml[(base + slot) * 2] = m;
-    a.ws_ml[(base + slot) * 2 + 1] = l;
+    reinterpret_cast<uint2 *>(a.ws_ml)[row] =
+        make_uint2(__float_as_uint(m) ^ kEnc, __float_as_uint(l) ^ kEnc);
+    ticket = atomicAdd(&a.ws_cnt[bh], 1);
   }
+  return ticket;
+}
+
+// Called by the whole warp with lane 0's ticket for head bh: if it was the
+// head's last, merge.  Returns false if the partials did not all appear
+// within the poll bound (status word set).
+__device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
+  const int lane = threadIdx.x & 31;
   const int nparts = head_nparts(a, bh);
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) last = atomicAdd(&a.ws_cnt[bh], 1) == nparts - 1;
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
+  if (__shfl_sync(0xffffffffu, ticket, 0) != nparts - 1) return true;
+  const int64_t base = (int64_t)bh * a.part_stride;
+  const uint2 *ml = reinterpret_cast<const uint2 *>(a.ws_ml) + base;
+  const uint4 *wo = reinterpret_cast<const uint4 *>(a.ws_o + base * kD);
+  // (m, l) of partial s sits in lane s % 32; every load is re-polled
+  // (bounded) until its words are non-zero
+  auto ml_of = [&](int s) -> uint2 {
+    uint2 v = __ldcg(ml + s);
+    for (int it = 0; it < kMergePolls && (v.x == 0u || v.y == 0u); ++it) {
+      __nanosleep(32);
+      v = __ldcg(ml + s);
+    }
+    return v;
+  };
+  bool ok = true;
   float Mx = -INFINITY;
-  for (int s = lane; s < nparts; s += 32) Mx = fmaxf(Mx, __ldcg(&a.ws_ml[(base + s) * 2]));
+  for (int s = lane; s < nparts; s += 32) {
+    const uint2 v = ml_of(s);
+    ok = ok && v.x != 0u && v.y != 0u;
+    Mx = fmaxf(Mx, __uint_as_float(v.x ^ kEnc));
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
   float Ls = 0.0f, O[4] = {0.f, 0.f, 0.f, 0.f};
-  if (Mx != -INFINITY) {
-    for (int s = 0; s < nparts; ++s) {
-      const float ms = __ldcg(&a.ws_ml[(base + s) * 2]);
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - Mx);
-      Ls = fmaf(w, __ldcg(&a.ws_ml[(base + s) * 2 + 1]), Ls);
-      const float4 o = __ldcg(reinterpret_cast<const float4 *>(a.ws_o + (base + s) * kD) + lane);
-      O[0] = fmaf(w, o.x, O[0]);
-      O[1] = fmaf(w, o.y, O[1]);
-      O[2] = fmaf(w, o.z, O[2]);
-      O[3] = fmaf(w, o.w, O[3]);
+  for (int s0 = 0; s0 < nparts && ok; s0 += 32) {
+    float w = 0.0f;
+    if (s0 + lane < nparts) {
+      const uint2 v = __ldcg(ml + s0 + lane);
+      const float ms = __uint_as_float(v.x ^ kEnc);
+      if (ms != -INFINITY) {
+        w = exp2f(ms - Mx);
+        Ls = fmaf(w, __uint_as_float(v.y ^ kEnc), Ls);
+      }
     }
+    const int nb = min(32, nparts - s0);
+    for (int j0 = 0; j0 < nb; j0 += 4) {
+      uint4 o[4];
+      bool ready = false;
+      for (int it = 0; it < kMergePolls && !ready; ++it) {
+        bool mine = true;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          o[j] = j0 + j < nb ? __ldcg(wo + (int64_t)(s0 + j0 + j) * (kD / 4) + lane)
+                             : make_uint4(1, 1, 1, 1);
+          mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
+        }
+        ready = __all_sync(0xffffffffu, mine);
+        if (!ready) __nanosleep(32);
+      }
+      ok = ok && ready;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+        if (j0 + j < nb && wj != 0.0f) {
+          O[0] = fmaf(wj, __uint_as_float(o[j].x ^ kEnc), O[0]);
+          O[1] = fmaf(wj, __uint_as_float(o[j].y ^ kEnc), O[1]);
+          O[2] = fmaf(wj, __uint_as_float(o[j].z ^ kEnc), O[2]);
+          O[3] = fmaf(wj, __uint_as_float(o[j].w ^ kEnc), O[3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+  if (!__all_sync(0xffffffffu, ok)) {
+    if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+    return false;
   }
   const int b = bh / a.g.H, h = bh % a.g.H;
   const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
@@ -309,7 +379,12 @@ __device__ void warp_publish(const TcArgs &a, int bh, int slot, float m, float l
   r.z = O[2] * inv;
   r.w = O[3] * inv;
   reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h) * kD)[lane] = r;
+  // leave the workspace as found: partials and ticket zero
+  for (int s = 0; s < nparts; ++s)
+    reinterpret_cast<uint4 *>(a.ws_o + base * kD)[(int64_t)s * (kD / 4) + lane] = make_uint4(0, 0, 0, 0);
+  for (int s = lane; s < nparts; s += 32) reinterpret_cast<uint2 *>(a.ws_ml)[base + s] = make_uint2(0, 0);
   if (lane == 0) a.ws_cnt[bh] = 0;
+  return true;
 }
 
 template <int BITS, int SCHEME, int NGV, int NGK, int KM>
@@ -526,7 +601,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // z) and the fp16-token state (mf, lf, af: a lane owns channels 4*lane ..
   // 4*lane + 3) are joined with the log-sum-exp rule; the quantized output
   // row goes through the warp's operand area to reach the lane layout.
-  auto flush = [&](int bh, int slot, float mf, float lf, const float (&af)[4]) {
+  int pend_bh = -1, pend_ticket = 0;  // last published head, lane 0's ticket for it
+  auto flush = [&](int bh, int slot, float mf, float lf, const float (&af)[4]) -> bool {
     float l = l_lane;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
@@ -563,9 +639,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     o.y = fmaf(oq.y, wq, af[1] * wf);
     o.z = fmaf(oq.z, wq, af[2] * wf);
     o.w = fmaf(oq.w, wq, af[3] * wf);
-    reinterpret_cast<float4 *>(a.ws_o + ((int64_t)bh * a.part_stride + slot) * kD)[lane] = o;
-    warp_publish(a, bh, slot, m, fmaf(l, wq, lf * wf));
+    const float lt = fmaf(l, wq, lf * wf);
     reset_state();
+    // the previous head's ticket has long arrived: act on it, then publish
+    if (pend_bh >= 0 && !finish_head(a, pend_bh, pend_ticket)) return false;
+    pend_ticket = publish_partial(a, bh, slot, o, m, lt);
+    pend_bh = bh;
+    return true;
   };
 
   int done = 0;          // items whose copies completed
@@ -959,8 +1039,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       }
       if (aborted) break;
     }
-    flush(bh, kWarps * ((int)blockIdx.x - owner_of(base, a.total, a.nc)) + warp, mf, lf, af);
+    if (!flush(bh, kWarps * ((int)blockIdx.x - owner_of(base, a.total, a.nc)) + warp, mf, lf, af)) {
+      aborted = true;
+      break;
+    }
   }
+  if (!aborted && pend_bh >= 0 && !finish_head(a, pend_bh, pend_ticket)) aborted = true;
   if (aborted) {
     // give up this block's work for this warp; its copies complete first
     if (lane == 0)

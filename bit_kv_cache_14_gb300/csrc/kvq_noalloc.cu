@@ -46,10 +46,10 @@ extern "C" int kvq_decode_attention_noalloc(const kvq_config *cfg, const kvq_cac
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ECAPACITY;
   void *ws = nullptr;
   if ((r = scratch_address(&ws)) != KVQ_OK) return r;
-  // The per-head tickets at the start of the scratch must read zero when a
-  // decode starts; clear them (another call may have stopped early).
-  const size_t tickets = ((size_t)cfg->batch * cfg->n_kv_heads * sizeof(int) + 255) & ~(size_t)255;
-  if (cudaMemsetAsync(ws, 0, tickets, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // The scratch must read zero when a decode starts; a successful decode
+  // leaves it so, but another call may have stopped early: clear the part
+  // this configuration uses.
+  if (cudaMemsetAsync(ws, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return KVQ_ECUDA;
   return kvq_decode_attention(cfg, cache, q, out, softmax_scale, ws,
                               (size_t)KVQ_NOALLOC_SCRATCH_BYTES, stream);

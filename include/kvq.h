@@ -144,7 +144,7 @@ int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out);
 
 /* Bytes of scratch (device) that kvq_decode_attention needs for any cache
  * state of this configuration.  The scratch must be zero-filled before its
- * first use; every decode call leaves its counters at zero again.  It must
+ * first use; every decode call that succeeds leaves it zero again.  It must
  * not be shared by decode calls that can run at the same time. */
 int kvq_workspace_bytes(const kvq_config *cfg, size_t *bytes);
 
@@ -223,8 +223,9 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
  * with KVQ_ECAPACITY before anything is enqueued.  The first call on a device
  * (with that device current) looks up the array's device address with
  * cudaGetSymbolAddress; make that first call before any stream capture.
- * Each call clears the part of the scratch that must start at zero (an
- * asynchronous memset on `stream`), then launches the decode.  All calls share
+ * Each call clears the part of the scratch its configuration uses (an
+ * asynchronous memset of kvq_workspace_bytes on `stream`), then launches the
+ * decode.  All calls share
  * the one array: calls whose work can overlap on the GPU (different streams,
  * different caches) race and give wrong results; serialize them.
  */
@@ -244,7 +245,7 @@ int kvq_get_device_status(kvq_cache *cache, void *stream);
  * With iterations > 0, each block of later tensor-core decode launches first
  * waits, with that cap, on a barrier that nothing completes, so the timeout
  * path runs for certain; 0 switches it off.  After a timeout the output and
- * the workspace counters are undefined: zero-fill the workspace again.
+ * the workspace are undefined: zero-fill the workspace again.
  * Process-wide; not for production use. */
 void kvq_debug_stall_waits(int64_t iterations);
 
