@@ -410,8 +410,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   constexpr int CH = SC::CH;
 
   // Each warp owns its ring and barriers; nothing below synchronises warps.
-  for (int i = lane; i < nslot * SLOT / 16; i += 32)
-    reinterpret_cast<uint4 *>(wring)[i] = make_uint4(0, 0, 0, 0);
+  // Ring bytes are only read where a copy wrote them (rows past a segment's
+  // end are masked), so the ring needs no clearing; the zero block does.
   if (lane < 16) sBw[SC::sb_zero + lane] = 0u;
   if (lane == 0) {
     for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
