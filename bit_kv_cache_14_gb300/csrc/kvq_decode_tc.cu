@@ -338,13 +338,13 @@ __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
       }
     }
     const int nb = min(32, nparts - s0);
-    for (int j0 = 0; j0 < nb; j0 += 4) {
-      uint4 o[4];
+    for (int j0 = 0; j0 < nb; j0 += 8) {
+      uint4 o[8];
       bool ready = false;
       for (int it = 0; it < kMergePolls && !ready; ++it) {
         bool mine = true;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
           o[j] = j0 + j < nb ? __ldcg(wo + (int64_t)(s0 + j0 + j) * (kD / 4) + lane)
                              : make_uint4(1, 1, 1, 1);
           mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
@@ -354,7 +354,7 @@ __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
       }
       ok = ok && ready;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
         const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
         if (j0 + j < nb && wj != 0.0f) {
           O[0] = fmaf(wj, __uint_as_float(o[j].x ^ kEnc), O[0]);
@@ -1143,6 +1143,9 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   if (total >= (1LL << 31)) return cudaErrorInvalidValue;
   a.total = (int)total;
   a.part_stride = tc_part_slots(g);
+  // ws_o must stay 16-byte aligned (uint4 rows): BH * part_stride * 8 bytes
+  // past ws_ml, so the stride is even
+  if (a.part_stride & 1) return cudaErrorInvalidValue;
   const int64_t BH = (int64_t)g.B * g.H;
   char *base = static_cast<char *>(ws);
   const size_t cnt = ((size_t)BH * sizeof(int) + 255) & ~(size_t)255;
