@@ -271,10 +271,11 @@ def run_gpu(args, w, rank, world):
             c.view.n_quant, c.view.n_resid, c.view.n_sink, c.view.ring_head = st
 
     def step(i):
+        """One decode step (append + attend); returns the kernels it launched."""
         c = i % copies
         e = (i // copies) % EPOCH
-        caches[c].append(ks[e], vs[e], stream)
-        caches[c].decode(qs[e % 8], outs[c], scale, stream)
+        caches[c].append_decode(ks[e], vs[e], qs[e % 8], outs[c], scale, stream)
+        return caches[c].last_launch_count()
 
     # per-step algorithmic bytes over one epoch (identical for every copy)
     if w.scheme == synth.KIVI:
@@ -291,20 +292,23 @@ def run_gpu(args, w, rank, world):
         step(0)  # warm the library (function attributes) outside capture
     stream.synchronize()
     restore()
+    ep_launches = 0
     with torch.cuda.graph(graph, stream=stream):
         for i in range(P):
-            step(i)
+            ep_launches += step(i)
     restore()
 
     K_steps, W_steps = args.steps, args.warmup
     n_full, rem = divmod(K_steps, P)
     rem_graph = None
+    rem_launches = 0
     if rem:
         rem_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(rem_graph, stream=stream):
             for i in range(rem):
-                step(i)
+                rem_launches += step(i)
         restore()
+    timed_launches = n_full * ep_launches + rem_launches
 
     # warm-up: at least W steps, in whole epochs
     warm_replays = max(1, math.ceil(W_steps / P))
@@ -410,7 +414,8 @@ def run_gpu(args, w, rank, world):
     h2d = 2 * ks[0].numel() * 2 + qs[0].numel() * 2
     d2h = qs[0].numel() * 4
     assert c0.device_status() == 0
-    return dict(warmup_steps=warm_replays * P, elapsed_ms=elapsed_ms, total_bytes=total_bytes, decode_ms=decode_ms,
+    return dict(warmup_steps=warm_replays * P, elapsed_ms=elapsed_ms, total_bytes=total_bytes,
+                decode_ms=decode_ms, timed_launches=timed_launches,
                 dstate_bytes=dstate_bytes, plain_ms=plain_ms, e2e_ms=e2e_ms,
                 e2e_bytes=e2e_bytes, n_e2e=n_e2e, h2d=h2d, d2h=d2h, clocks=clocks,
                 copies=copies, cache_bytes=cache_bytes, prefill_ms=float(np.median(pre_ms)),
@@ -491,7 +496,7 @@ def main():
         "e2e": {"value": r["e2e_bytes"] / (r["e2e_ms"] * 1e-3) / 1e9 * world, "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "us_per_step": r["e2e_ms"] / r["n_e2e"] * 1e3, "steps": r["n_e2e"]},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": r["timed_launches"],
         "clocks": r["clocks"],
     }
     if rank == 0 and world == 1 and not args.skip_cpu:

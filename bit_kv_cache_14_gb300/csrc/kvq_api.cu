@@ -258,6 +258,43 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
   return KVQ_OK;
 }
 
+int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k,
+                      const uint16_t *v, const uint16_t *q, float *out, float softmax_scale,
+                      void *ws, size_t ws_bytes, void *stream) {
+  Geometry g;
+  int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if (!k || !v || !q || !out || !ws) return KVQ_EINVAL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out) || !aligned16(ws))
+    return KVQ_EALIGN;
+  if (cache->n_quant + cache->n_resid + cache->n_sink + 1 > g.max_ctx) return KVQ_ECAPACITY;
+  if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
+  if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
+  // One launch when the append only stores the new token (KIVI, no flush)
+  // and the decode runs on the tensor-core path; two launches otherwise.
+  const bool fuse = g.scheme == KVQ_KIVI && cache->n_resid + 1 < g.residual &&
+                    cache->n_quant > 0 && tc_decode_supported(g);
+  if (!fuse) {
+    if ((r = kvq_append(cfg, cache, k, v, stream)) != KVQ_OK) return r;
+    if ((r = kvq_decode_attention(cfg, cache, q, out, softmax_scale, ws, ws_bytes, stream)) !=
+        KVQ_OK)
+      return r;
+    note_launch(2);
+    return KVQ_OK;
+  }
+  r = from_cuda(launch_decode_tc(g, ptrs_of(cache), cache->n_quant, cache->n_resid + 1,
+                                 cache->n_sink, reinterpret_cast<const __half *>(q), out,
+                                 softmax_scale, ws, num_sms_cached(),
+                                 static_cast<cudaStream_t>(stream),
+                                 reinterpret_cast<const __half *>(k),
+                                 reinterpret_cast<const __half *>(v)));
+  if (r != KVQ_OK) return r;
+  cache->n_resid += 1;
+  note_launch(1);
+  return KVQ_OK;
+}
+
 int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *h_k,
                          const uint16_t *h_v, const uint16_t *h_q, float *h_out, uint16_t *d_k,
                          uint16_t *d_v, uint16_t *d_q, float *d_out, float softmax_scale,
@@ -276,13 +313,13 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
       cudaMemcpyAsync(d_v, h_v, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
       cudaMemcpyAsync(d_q, h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return KVQ_ECUDA;
-  if ((r = kvq_append(cfg, cache, d_k, d_v, stream)) != KVQ_OK) return r;
-  if ((r = kvq_decode_attention(cfg, cache, d_q, d_out, softmax_scale, ws, ws_bytes, stream)) !=
-      KVQ_OK)
+  if ((r = kvq_append_decode(cfg, cache, d_k, d_v, d_q, d_out, softmax_scale, ws, ws_bytes,
+                             stream)) != KVQ_OK)
     return r;
+  const int launches = kvq_last_launch_count();
   if (cudaMemcpyAsync(h_out, d_out, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return KVQ_ECUDA;
-  note_launch(2);
+  note_launch(launches);
   return KVQ_OK;
 }
 

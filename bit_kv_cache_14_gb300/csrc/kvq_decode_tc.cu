@@ -65,6 +65,8 @@ struct TcArgs {
   CachePtrs p;
   const __half *q;
   float *out;
+  const __half *k_new, *v_new;  // fused append: the step's new K, V rows [B][H][d]
+  int new_row;                  // their residual row (the last one), or -1
   float scale_log2;
   int64_t n_quant, n_fp16, n_sink;
   int S_h, F_h, U;  // quantized units, fp16 units, units per head
@@ -477,11 +479,21 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
         }
         if (r1 > r0) {
+          // a fused append's new row is not in the residual yet: it comes from
+          // the step's input rows
+          const int rn = (a.new_row >= 0 && r1 - 1 == a.new_row) ? r1 - 1 : r1;
           const int64_t row = (int64_t)pc_bh * g.residual + r0;
           const int o = (s1 - s0) * kD * 2;
-          bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((r1 - r0) * kD * 2), bar);
-          bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD, (uint32_t)((r1 - r0) * kD * 2),
-                   bar);
+          if (rn > r0) {
+            bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((rn - r0) * kD * 2), bar);
+            bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD,
+                     (uint32_t)((rn - r0) * kD * 2), bar);
+          }
+          if (rn < r1) {
+            const int on = o + (rn - r0) * kD * 2;
+            bulk_g2s(dst + on, a.k_new + (int64_t)pc_bh * kD, kD * 2, bar);
+            bulk_g2s(dst + CH * kD * 2 + on, a.v_new + (int64_t)pc_bh * kD, kD * 2, bar);
+          }
         }
       }
       if (first) bulk_g2s(dst + SC::off_q, qrow, kD * 2, bar);
@@ -969,6 +981,16 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         }
         const int i0 = (sg.c0 + lt) * CH;
         const int nv = min(CH, (int)a.n_fp16 - i0);  // valid rows of the chunk
+        if (a.new_row >= 0) {
+          // fused append: the warp holding the new token stores it in the residual
+          const int tn = (int)a.n_sink + a.new_row - i0;
+          if (tn >= 0 && tn < nv) {
+            const int half = lane >> 4, j = lane & 15;
+            const uint4 v4 = reinterpret_cast<const uint4 *>(slot + half * CH * kD * 2 + tn * kD * 2)[j];
+            __half *dstrow = (half ? a.p.v_res : a.p.k_res) + ((int64_t)bh * g.residual + a.new_row) * kD;
+            reinterpret_cast<uint4 *>(dstrow)[j] = v4;
+          }
+        }
         const uint2 *kr = reinterpret_cast<const uint2 *>(slot);
         const uint2 *vr = reinterpret_cast<const uint2 *>(slot + CH * kD * 2);
         // partial dot products of the lane's 4 channels, then a reduce-scatter:
@@ -1117,12 +1139,16 @@ bool tc_decode_supported(const Geometry &g) {
 
 cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_quant,
                              int64_t n_resid, int64_t n_sink, const __half *q, float *out,
-                             float scale, void *ws, int num_sms, cudaStream_t st) {
+                             float scale, void *ws, int num_sms, cudaStream_t st,
+                             const __half *k_new, const __half *v_new) {
   TcArgs a;
   a.g = g;
   a.p = p;
   a.q = q;
   a.out = out;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.new_row = k_new ? (int)n_resid - 1 : -1;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.n_quant = n_quant;
   a.n_fp16 = n_resid + n_sink;

@@ -119,9 +119,13 @@ cudaError_t launch_decode(const Geometry &g, const CachePtrs &p, const DecodePla
 
 // Tensor-core decode path (MHA, head_dim 128, 2 or 4 value groups).
 bool tc_decode_supported(const Geometry &g);
+// k_new, v_new non-null: fused append -- the last of the n_resid residual
+// rows is the step's new token, read from k_new / v_new ([B][H][d]) and
+// stored into the residual by the kernel.
 cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_quant,
                              int64_t n_resid, int64_t n_sink, const __half *q, float *out,
-                             float scale, void *ws, int num_sms, cudaStream_t st);
+                             float scale, void *ws, int num_sms, cudaStream_t st,
+                             const __half *k_new = nullptr, const __half *v_new = nullptr);
 void set_debug_stall(long long iterations);
 
 // ---- quantization arithmetic (bit-exact contract with the formula) -------

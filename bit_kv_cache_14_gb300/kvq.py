@@ -33,7 +33,7 @@ EXPORTS = (
     "kvq_cache_sizes", "kvq_workspace_bytes", "kvq_quantize_prefill", "kvq_append",
     "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
     "kvq_last_launch_count", "kvq_strerror", "kvq_debug_stall_waits",
-    "kvq_decode_attention_noalloc",
+    "kvq_decode_attention_noalloc", "kvq_append_decode",
 )
 
 
@@ -84,6 +84,8 @@ def lib():
             L.kvq_decode_step_host.argtypes = [C, CA, P, P, P, P, P, P, P, P, ctypes.c_float, P,
                                                ctypes.c_size_t, P]
             L.kvq_decode_attention_noalloc.argtypes = [C, CA, P, P, ctypes.c_float, P]
+            L.kvq_append_decode.argtypes = [C, CA, P, P, P, P, ctypes.c_float, P,
+                                            ctypes.c_size_t, P]
             L.kvq_get_device_status.argtypes = [CA, P]
             L.kvq_last_launch_count.argtypes = []
             L.kvq_debug_stall_waits.argtypes = [ctypes.c_int64]
@@ -196,6 +198,22 @@ class QuantizedKVCache:
                                           _ptr(q), _ptr(out), float(scale), self.ws.data_ptr(),
                                           self.ws_bytes, _stream(stream)),
                "kvq_decode_attention")
+        return out
+
+    def append_decode(self, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,
+                      out: torch.Tensor | None = None, scale: float | None = None,
+                      stream=None) -> torch.Tensor:
+        """One decode step on device tensors: append k, v ([B][H][d] fp16), then
+        attend with q; a single launch when the append needs no flush."""
+        assert k.dtype == torch.float16 and v.dtype == torch.float16 and q.dtype == torch.float16
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.cfg.head_dim)
+        _check(lib().kvq_append_decode(ctypes.byref(self.cfg), ctypes.byref(self.view), _ptr(k),
+                                       _ptr(v), _ptr(q), _ptr(out), float(scale),
+                                       self.ws.data_ptr(), self.ws_bytes, _stream(stream)),
+               "kvq_append_decode")
         return out
 
     def decode_step_host(self, h_k, h_v, h_q, h_out, d_k, d_v, d_q, d_out, scale=None,

@@ -195,9 +195,22 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
                          void *stream);
 
 /*
+ * One decode step on device buffers: kvq_append(k, v) then
+ * kvq_decode_attention(q) with the same arguments, results and errors.  When
+ * the append only stores the new token (KIVI without a flush) and the decode
+ * runs on the tensor-core path (head_dim 128, MHA), both happen in ONE kernel
+ * launch: the decode reads the new token's rows from k, v directly and stores
+ * them into the residual; otherwise it is the two launches.
+ */
+int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k,
+                      const uint16_t *v, const uint16_t *q, float *out, float softmax_scale,
+                      void *ws, size_t ws_bytes, void *stream);
+
+/*
  * One decode step from HOST buffers: copies h_k, h_v ([B][H][d] fp16) and h_q
  * ([B][n_q_heads][d] fp16) to the device staging buffers d_k, d_v, d_q,
- * appends, attends, and copies the result to h_out ([B][n_q_heads][d] fp32)
+ * appends and attends (kvq_append_decode), and copies the result to h_out
+ * ([B][n_q_heads][d] fp32)
  * through d_out -- all enqueued on `stream`, no synchronization.  Host
  * buffers should be pinned for the copies to be asynchronous.
  */

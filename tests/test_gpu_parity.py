@@ -155,6 +155,38 @@ def test_decode_step_host_matches_device_path():
         assert torch.equal(h_out, ref)
 
 
+def test_fused_append_decode_matches_two_launches():
+    """kvq_append_decode (one launch unless the append flushes) leaves the same
+    cache and returns the same output as kvq_append + kvq_decode_attention."""
+    w = S(W["llama2_7b_2bit"], batch=2, n_q_heads=3, n_kv_heads=3, ctx=600, residual=64,
+          n_append=70)
+    K, V = synth.prompt(w)
+    Ks, Vs = synth.streamed(w, w.n_append)
+    a, b = new_cache(w), new_cache(w)
+    for c in (a, b):
+        c.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    fused = flushed = 0
+    for s in range(w.n_append):
+        q = torch.from_numpy(synth.queries(w, s)).cuda()
+        k, v = torch.from_numpy(Ks[s]).cuda(), torch.from_numpy(Vs[s]).cuda()
+        will_flush = a.n_resid + 1 == w.residual
+        got = a.append_decode(k, v, q)
+        n = a.last_launch_count()
+        assert n == (2 if will_flush else 1)
+        fused += n == 1
+        flushed += n == 2
+        b.append(k, v)
+        ref = b.decode(q)
+        assert torch.equal(got, ref), s
+        assert (a.n_quant, a.n_resid) == (b.n_quant, b.n_resid)
+    assert fused > 0 and flushed > 0
+    torch.cuda.synchronize()
+    for name in ("k_res", "v_res"):
+        assert torch.equal(a.bufs[name], b.bufs[name])
+    assert torch.equal(a.bufs["blocks"], b.bufs["blocks"])
+    assert a.device_status() == 0
+
+
 def test_errors_leave_state_unchanged():
     w = S(W["tiny"], ctx=64)
     cache = new_cache(w, 64)
