@@ -137,7 +137,10 @@ def measured_peak():
 
 def decode_source_sha():
     h = hashlib.sha256()
-    for name in ("kvq_decode.cu", "kvq_decode_tc.cu", "kvq_internal.cuh"):
+    for name in ("kvq_decode.cu", "kvq_decode_tc.cu", "kvq_decode_gqa.cu", "kvq_tc_common.cuh",
+                 "kvq_internal.cuh"):
+        if not os.path.exists(os.path.join(ROOT, "bit_kv_cache_14_gb300", "csrc", name)):
+            continue
         with open(os.path.join(ROOT, "bit_kv_cache_14_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

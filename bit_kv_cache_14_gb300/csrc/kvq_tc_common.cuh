@@ -1,0 +1,366 @@
+// Shared pieces of the tensor-core decode kernels (MHA: kvq_decode_tc.cu,
+// grouped-query: kvq_decode_gqa.cu): launch arguments, PTX wrappers (mbarriers,
+// bulk copies, mma.sync), the code-extraction helpers, the stream-K work
+// split and the fence-free merge of partials.  Everything sits in an unnamed
+// namespace: each translation unit gets its own internal copy.
+#pragma once
+
+#include <math.h>
+
+#include <type_traits>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnit = 128;    // tokens per stream-K work unit
+constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
+constexpr int kD = 128;
+constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
+// Lazy online softmax: probabilities are taken against a running reference
+// that may sit up to kSlack (log2 units) below the true maximum, so p <= 2^8;
+// the value operand carries p * 2^-8 and the output row multiplies it back.
+constexpr float kSlack = 8.0f;
+constexpr float kSlackScale = 256.0f;
+constexpr float kInvSlack = 1.0f / 256.0f;
+constexpr int kDrainLimit = 1 << 26;
+
+struct TcArgs {
+  Geometry g;
+  CachePtrs p;
+  const __half *q;
+  float *out;
+  const __half *k_new, *v_new;  // fused append: the step's new K, V rows [B][H][d]
+  int new_row;                  // their residual row (the last one), or -1
+  float scale_log2;
+  int64_t n_quant, n_fp16, n_sink;
+  int S_h, F_h, U;  // quantized units, fp16 units, units per head
+  int CPU;          // fp16 chunks per fp16 unit
+  int nch;          // fp16 chunks per head
+  int total;        // BH * U
+  int nc;           // resident blocks
+  float *ws_ml, *ws_o;
+  int *ws_cnt;
+  int part_stride;
+  int wait_limit;   // poll cap of every pipeline wait
+  int stall_limit;  // debug: > 0 = first wait on a barrier nothing completes
+};
+
+struct TcLayout {
+  int ring, sB, bars, total;
+};
+
+__host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int sb_bytes) {
+  TcLayout L{};
+  L.ring = 0;
+  L.sB = L.ring + kWarps * nslot * slot_bytes;  // per warp: key operand + zero block
+  L.bars = L.sB + kWarps * sb_bytes;            // per warp: nslot + 1 mbarriers
+  L.total = L.bars + kWarps * (nslot + 1) * 8;
+  return L;
+}
+
+// Compile-time layout of one warp-ring slot (one 32-token tile).  The first
+// BB bytes are a copy of the cache block (K codes, V codes, V scale, V zero,
+// InnerQ K scale, K zero; KIVI G <= 32 key statistics); for KIVI G >= 64 the
+// statistics of the tile's key group (scale row, zero row); the query row
+// on the first tile of a head.  Outside the ring each warp keeps its KIVI key
+// operand (fp16 hi/lo words in fragment order, per key group), reused to
+// transpose the output row at a head's end, and 64 bytes that stay zero.
+// KM (KIVI): 2 = G 16, two key groups per tile, statistics inside the block;
+// 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
+// from the separate key-statistics array.
+template <int BITS, int SCHEME, int NGV, int NGK, int KM>
+struct SlotCfg {
+  static constexpr int RB = kD * BITS / 8;
+  static constexpr int off_vc = kTile * RB;
+  static constexpr int off_vs = 2 * kTile * RB;
+  static constexpr int off_vz = off_vs + kTile * NGV * 4;
+  static constexpr int off_ks = off_vz + kTile * NGV * 4;  // InnerQ
+  static constexpr int off_kz = off_ks + kTile * NGK * 4;  // InnerQ
+  static constexpr bool KIN = SCHEME == KVQ_KIVI && KM >= 1;
+  static constexpr int KGB = (KM == 2 ? 2 : 1) * 2 * kD * 4;  // KIVI key statistics of a tile
+  static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks + (KIN ? KGB : 0) : off_kz + kTile * NGK * 4;
+  static constexpr int KMB = SCHEME == KVQ_KIVI && !KIN ? KGB : 0;  // separate copy
+  static constexpr int off_km = KIN ? off_ks : BB;
+  static constexpr int off_q = BB + KMB;
+  static constexpr int bytes = off_q + kD * 2;
+  static constexpr int CH = off_q / (4 * kD) < 8 ? off_q / (4 * kD) : 8;  // fp16 tokens per chunk
+  // per warp: KIVI key operand (512 B per group; also the 512 B output
+  // transpose at a head's end) + 64 zero bytes
+  static constexpr int SBB = (SCHEME == KVQ_KIVI && KM == 2 ? 1024 : 512) + 64;
+  static constexpr int sb_zero = SBB / 4 - 16;  // word offset of the zero block
+  static constexpr int nslot = tc_layout(bytes, 3, SBB).total <= 112 * 1024 ? 3 : 2;
+  static constexpr int smem = tc_layout(bytes, nslot, SBB).total;
+};
+
+
+// ---- PTX helpers --------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void bar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void bar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool bar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity; false on timeout.
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, int limit) {
+  if (bar_try_wait(bar, parity)) return true;
+  for (int it = 0; it < limit; ++it)
+    if (bar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Code pair at position p of a word holding two 16-bit halves of codes:
+// returns half2(code_lo * f, code_hi * f) * 2^-24 exactly, f = 4^p' (2-bit)
+// or 16^p' (4-bit).  The masked bits sit in the low ten bits of each half, so
+// each half reads as the fp16 subnormal (code * f) * 2^-24: one AND per pair.
+// ws = w >> 10 (2-bit) or w >> 8 (4-bit), precomputed by the caller.
+template <int BITS>
+__device__ __forceinline__ uint32_t ext(uint32_t w, uint32_t ws, int p) {
+  if (BITS == 2) return p <= 4 ? (w & (0x00030003u << (2 * p))) : (ws & (0x00030003u << (2 * (p - 5))));
+  return p <= 1 ? (w & (0x000F000Fu << (4 * p))) : (ws & (0x000F000Fu << (4 * (p - 2))));
+}
+
+template <int BITS>
+__device__ __forceinline__ uint32_t shifted(uint32_t w) {
+  return BITS == 2 ? (w >> 10) : (w >> 8);
+}
+
+// Multiplier carried by the code at position p (see ext).
+template <int BITS>
+__host__ __device__ __forceinline__ float pos_factor(int p) {
+  if (BITS == 2) return (float)(1 << (2 * (p <= 4 ? p : p - 5)));
+  return (p & 1) ? 16.0f : 1.0f;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+
+// fp16 hi + lo split of two fp32 values (hi = rn(x), lo = rn(x - hi)).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  hi = h2u(h);
+  lo = h2u(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+}
+
+// Key-operand channel pair (c_lo, c_hi = c_lo + half word) of MMA column pair
+// (tig, kb, reg); see the key extraction in process_tile.
+template <int BITS>
+__device__ __forceinline__ void key_pair(int tig, int kb, int reg, int &c_lo, int &c_hi, int &p) {
+  if (BITS == 2) {
+    const int W = 2 * tig + (kb >> 2);
+    p = 2 * (kb & 3) + reg;
+    c_lo = 16 * W + p;
+    c_hi = c_lo + 8;
+  } else {
+    const int W = 4 * tig + (kb >> 1);
+    p = 2 * (kb & 1) + reg;
+    c_lo = 8 * W + p;
+    c_hi = c_lo + 4;
+  }
+}
+
+__device__ __forceinline__ int owner_of(int x, int total, int nc) {
+  return (int)(((int64_t)(x + 1) * nc - 1) / total);
+}
+
+// Unit range [x0, x1) of block x.
+__device__ __forceinline__ void block_range(const TcArgs &a, int x, int &x0, int &x1) {
+  x0 = (int)((int64_t)x * a.total / a.nc);
+  x1 = (int)((int64_t)(x + 1) * a.total / a.nc);
+}
+
+// What block range [x0, x1) holds of head bh: quantized tokens [tq0, tq1)
+// (from its units [0, S_h)) and fp16 chunks [c0, c1) (from its units
+// [S_h, U), CPU chunks each).
+struct Seg {
+  int tq0, tq1, c0, c1;
+};
+__device__ __forceinline__ Seg seg_in(const TcArgs &a, int bh, int x0, int x1) {
+  Seg s;
+  const int base = bh * a.U;
+  const int ua = max(x0, base) - base;
+  const int ub = min(min(x1, base + a.U) - base, a.S_h);
+  s.tq0 = ua * kUnit;
+  s.tq1 = ua < ub ? (int)min((int64_t)ub * kUnit, a.n_quant) : s.tq0;
+  const int fa = max(x0 - base - a.S_h, 0), fb = min(x1 - base - a.S_h, a.F_h);
+  s.c0 = fa * a.CPU;
+  s.c1 = fa < fb ? min(fb * a.CPU, a.nch) : s.c0;
+  return s;
+}
+
+// Partials of head bh: one per warp of every block whose units touch it
+// (quantized or fp16), slot 8 * (block - first such block) + warp.
+__device__ __forceinline__ int head_nparts(const TcArgs &a, int bh) {
+  const int base = bh * a.U;
+  return kWarps * (owner_of(base + a.U - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1);
+}
+
+// Partials are stored XOR-ed with kEnc: no float that arithmetic produces
+// (kEnc is a signalling NaN) encodes to 0, so a zero word means "not
+// written yet" and the zero-filled workspace starts empty.  Writers publish
+// without any fence: they store their partial and take a ticket with a
+// relaxed atomic whose result they look at only later.  The warp that took
+// the head's last ticket polls (bounded) until every partial is visible,
+// merges them with the log-sum-exp rule, writes the output row and zeroes
+// the partials and the ticket again.
+constexpr uint32_t kEnc = 0x7fbadbadu;
+constexpr int kMergePolls = 1 << 22;
+
+__device__ __forceinline__ uint4 enc4(float4 v) {
+  return make_uint4(__float_as_uint(v.x) ^ kEnc, __float_as_uint(v.y) ^ kEnc,
+                    __float_as_uint(v.z) ^ kEnc, __float_as_uint(v.w) ^ kEnc);
+}
+
+// Stores partial `slot` of head bh: the lane's 4 output channels and (lane 0)
+// m, l.  Returns the ticket of lane 0's relaxed atomic (read it later).
+__device__ __forceinline__ int publish_partial(const TcArgs &a, int bh, int slot, float4 o,
+                                               float m, float l) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)bh * a.part_stride + slot;
+  reinterpret_cast<uint4 *>(a.ws_o + row * kD)[lane] = enc4(o);
+  int ticket = 0;
+  if (lane == 0) {
+    reinterpret_cast<uint2 *>(a.ws_ml)[row] =
+        make_uint2(__float_as_uint(m) ^ kEnc, __float_as_uint(l) ^ kEnc);
+    ticket = atomicAdd(&a.ws_cnt[bh], 1);
+  }
+  return ticket;
+}
+
+// Called by the whole warp with lane 0's ticket for head bh: if it was the
+// head's last, merge.  Returns false if the partials did not all appear
+// within the poll bound (status word set).
+__device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
+  const int lane = threadIdx.x & 31;
+  const int nparts = head_nparts(a, bh);
+  if (__shfl_sync(0xffffffffu, ticket, 0) != nparts - 1) return true;
+  const int64_t base = (int64_t)bh * a.part_stride;
+  const uint2 *ml = reinterpret_cast<const uint2 *>(a.ws_ml) + base;
+  const uint4 *wo = reinterpret_cast<const uint4 *>(a.ws_o + base * kD);
+  // (m, l) of partial s sits in lane s % 32; every load is re-polled
+  // (bounded) until its words are non-zero
+  auto ml_of = [&](int s) -> uint2 {
+    uint2 v = __ldcg(ml + s);
+    for (int it = 0; it < kMergePolls && (v.x == 0u || v.y == 0u); ++it) {
+      __nanosleep(32);
+      v = __ldcg(ml + s);
+    }
+    return v;
+  };
+  bool ok = true;
+  float Mx = -INFINITY;
+  for (int s = lane; s < nparts; s += 32) {
+    const uint2 v = ml_of(s);
+    ok = ok && v.x != 0u && v.y != 0u;
+    Mx = fmaxf(Mx, __uint_as_float(v.x ^ kEnc));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
+  float Ls = 0.0f, O[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s0 = 0; s0 < nparts && ok; s0 += 32) {
+    float w = 0.0f;
+    if (s0 + lane < nparts) {
+      const uint2 v = __ldcg(ml + s0 + lane);
+      const float ms = __uint_as_float(v.x ^ kEnc);
+      if (ms != -INFINITY) {
+        w = exp2f(ms - Mx);
+        Ls = fmaf(w, __uint_as_float(v.y ^ kEnc), Ls);
+      }
+    }
+    const int nb = min(32, nparts - s0);
+    for (int j0 = 0; j0 < nb; j0 += 8) {
+      uint4 o[8];
+      bool ready = false;
+      for (int it = 0; it < kMergePolls && !ready; ++it) {
+        bool mine = true;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          o[j] = j0 + j < nb ? __ldcg(wo + (int64_t)(s0 + j0 + j) * (kD / 4) + lane)
+                             : make_uint4(1, 1, 1, 1);
+          mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
+        }
+        ready = __all_sync(0xffffffffu, mine);
+        if (!ready) __nanosleep(32);
+      }
+      ok = ok && ready;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+        if (j0 + j < nb && wj != 0.0f) {
+          O[0] = fmaf(wj, __uint_as_float(o[j].x ^ kEnc), O[0]);
+          O[1] = fmaf(wj, __uint_as_float(o[j].y ^ kEnc), O[1]);
+          O[2] = fmaf(wj, __uint_as_float(o[j].z ^ kEnc), O[2]);
+          O[3] = fmaf(wj, __uint_as_float(o[j].w ^ kEnc), O[3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+  if (!__all_sync(0xffffffffu, ok)) {
+    if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+    return false;
+  }
+  const int b = bh / a.g.H, h = bh % a.g.H;
+  const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+  float4 r;
+  r.x = O[0] * inv;
+  r.y = O[1] * inv;
+  r.z = O[2] * inv;
+  r.w = O[3] * inv;
+  reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h) * kD)[lane] = r;
+  // leave the workspace as found: partials and ticket zero
+  for (int s = 0; s < nparts; ++s)
+    reinterpret_cast<uint4 *>(a.ws_o + base * kD)[(int64_t)s * (kD / 4) + lane] = make_uint4(0, 0, 0, 0);
+  for (int s = lane; s < nparts; s += 32) reinterpret_cast<uint2 *>(a.ws_ml)[base + s] = make_uint2(0, 0);
+  if (lane == 0) a.ws_cnt[bh] = 0;
+  return true;
+}
+
+}  // namespace
+
+// Poll cap of the debug stall (kvq_debug_stall_waits); 0 = off.
+int debug_stall_limit();
+
+}  // namespace kvq
