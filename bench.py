@@ -147,10 +147,15 @@ def decode_source_sha():
 
 
 def decode_kernel_name(w):
-    """Which decode kernel the library launches for this shape (head_dim 128,
-    MHA, 2 or 4 value groups -> the tensor-core kernel)."""
-    if w.head_dim == 128 and w.n_q_heads == w.n_kv_heads and 128 // w.v_group in (2, 4):
-        return "tc_decode_kernel"
+    """Which decode kernel the library launches for this shape: head_dim 128
+    with 2 or 4 value groups -> the tensor-core kernels (MHA; grouped-query for
+    2-bit KIVI, G >= 32, 2 or 4 query heads per KV head), else the general one."""
+    if w.head_dim == 128 and 128 // w.v_group in (2, 4):
+        if w.n_q_heads == w.n_kv_heads:
+            return "tc_decode_kernel"
+        if (w.bits == 2 and w.scheme == synth.KIVI and w.k_group >= 32
+                and w.n_q_heads // w.n_kv_heads in (2, 4)):
+            return "tc_gqa_kernel"
     return "decode_kernel"
 
 

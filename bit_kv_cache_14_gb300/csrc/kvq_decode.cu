@@ -416,7 +416,7 @@ size_t decode_workspace_bytes(const Geometry &g) {
   // the larger of the two decode paths' partial arrays
   const int64_t BH = (int64_t)g.B * g.H, rg = g.Hq / g.H;
   int64_t parts = BH * s_max_of(g) * rg;
-  const int64_t tc_parts = BH * tc_part_slots(g);
+  const int64_t tc_parts = BH * tc_part_slots(g) * rg;  // the grouped-query kernel: rg rows a slot
   if (tc_parts > parts) parts = tc_parts;
   size_t cnt = ((size_t)BH * sizeof(int) + 255) & ~(size_t)255;
   return cnt + (size_t)parts * 2 * sizeof(float) + (size_t)parts * g.d * sizeof(float) + 256;
@@ -446,6 +446,8 @@ cudaError_t launch_decode(const Geometry &g, const CachePtrs &p, const DecodePla
   (void)ring_head;  // attention does not depend on the order of window tokens
   if (n_quant > 0 && tc_decode_supported(g))
     return launch_decode_tc(g, p, n_quant, n_resid, n_sink, q, out, scale, ws, num_sms, st);
+  if (n_quant > 0 && gqa_decode_supported(g))
+    return launch_decode_gqa(g, p, n_quant, n_resid, n_sink, q, out, scale, ws, num_sms, st);
   DecodeArgs a;
   a.g = g;
   a.p = p;

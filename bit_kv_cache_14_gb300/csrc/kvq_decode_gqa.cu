@@ -1,0 +1,751 @@
+// Grouped-query decode attention on the tensor cores: head_dim 128, 2-bit
+// KIVI codes, RG = 2 or 4 query heads per KV head.
+//
+// Same computation as the MHA kernel (softmax(scale * q.K^T) V over the
+// packed cache, dequantization folded into both GEMVs -- "大模型量化技术原理：
+// KIVI、IntactKV、KVQuant", KIVI / 背景; GQA maps query head hq to KV head
+// hq / RG), arranged so one pass over the cache serves all RG query heads:
+//
+//  * Keys: D[token][n] = sum_c code * B[c][n] with the 8 MMA columns n =
+//    (query head r, fp16 hi/lo) -- every column carries data.  The operand
+//    is rebuilt per key group from a per-warp table of the normalised
+//    queries.  A lane of the accumulator holds head tig's scores for 4
+//    tokens, so the online softmax runs per lane with no transposition.
+//  * Values: each 16-row MMA tile holds channels of ONE value group (word
+//    W = group * words-per-group + gid mod words-per-group, code position
+//    chosen per lane by a shift), so its operand is that group's columns
+//    n = (r, hi/lo) of p_tr * scale_tj and every accumulator entry is used:
+//    lane (gid, tig) accumulates head tig.
+//  * fp16 sink / residual tokens ride the same ring in 8-token chunks and are
+//    folded on CUDA cores one head at a time into a second partial.
+//  * Work split, rings, bounded waits and the fence-free merge are those of
+//    the MHA kernel (kvq_tc_common.cuh); a partial here is RG rows.
+#include "kvq_tc_common.cuh"
+
+namespace kvq {
+
+namespace {
+
+template <int NGV, int KM, int RG>
+struct GqaCfg {
+  static constexpr int RB = kD * 2 / 8;  // 32 bytes per 2-bit row
+  static constexpr int off_vc = kTile * RB;
+  static constexpr int off_vs = 2 * kTile * RB;
+  static constexpr int off_vz = off_vs + kTile * NGV * 4;
+  static constexpr int off_ks = off_vz + kTile * NGV * 4;
+  static constexpr bool KIN = KM >= 1;  // G = 32: key statistics inside the block
+  static constexpr int KGB = 2 * kD * 4;
+  static constexpr int BB = off_ks + (KIN ? KGB : 0);
+  static constexpr int KMB = KIN ? 0 : KGB;
+  static constexpr int off_km = KIN ? off_ks : BB;
+  static constexpr int bytes = BB + KMB;  // one slot (no query rows in the ring)
+  static constexpr int CH = bytes / (4 * kD) < 8 ? bytes / (4 * kD) : 8;
+  static constexpr int WPG = 8 / NGV;     // 16-channel code words per value group
+  // per warp: key operand (8 columns x 64 words, also the output transpose of
+  // RG x 128 floats) + 64 zero bytes; query table [c][4] fp32 + 2^E per head
+  static constexpr int SBB = 8 * 64 * 4 + 64;
+  static constexpr int sb_zero = SBB / 4 - 16;
+  static constexpr int QTB = kD * 4 * 4 + 16;
+  __host__ __device__ static constexpr int lay(int nslot, int what) {
+    // what: 0 sB offset, 1 QT offset, 2 bars offset, 3 total
+    return what == 0 ? kWarps * nslot * bytes
+         : what == 1 ? kWarps * nslot * bytes + kWarps * SBB
+         : what == 2 ? kWarps * nslot * bytes + kWarps * (SBB + QTB)
+                     : kWarps * nslot * bytes + kWarps * (SBB + QTB) + kWarps * (nslot + 1) * 8;
+  }
+  static constexpr int nslot = lay(3, 3) <= 112 * 1024 ? 3 : 2;
+  static constexpr int smem = lay(nslot, 3);
+};
+
+// Partial slots of head bh (RG rows each): 8 per block holding quantized
+// units of it (every warp, by block order), then one per warp with at least
+// one of the block's fp16 chunks (by block order, no gaps).  gqa_slot0(a, bh,
+// xe) is the first fp16 slot of block xe; for xe past the last block it is
+// the head's slot count.
+__device__ __forceinline__ int gqa_slot0(const TcArgs &a, int bh, int xe) {
+  const int base = bh * a.U;
+  int np = 0;
+  if (a.S_h > 0)
+    np = kWarps * (owner_of(base + a.S_h - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1);
+  if (a.F_h > 0) {
+    const int xa = owner_of(base + a.S_h, a.total, a.nc);
+    const int xb = min(owner_of(base + a.U - 1, a.total, a.nc), xe - 1);
+    for (int x = xa; x <= xb; ++x) {
+      int x0, x1;
+      block_range(a, x, x0, x1);
+      const Seg sg = seg_in(a, bh, x0, x1);
+      np += min(kWarps, sg.c1 - sg.c0);
+    }
+  }
+  return np;
+}
+
+// Merge of n encoded partial rows row0, row0 + stride, ... (see merge in
+// kvq_tc_common.cuh): (M, L, O) for this lane's 4 channels; rows zeroed.
+__device__ bool merge_strided(const TcArgs &a, int64_t row0, int stride, int n, float &M,
+                              float &L, float4 &O) {
+  const int lane = threadIdx.x & 31;
+  const uint2 *ml = reinterpret_cast<const uint2 *>(a.ws_ml);
+  const uint4 *wo = reinterpret_cast<const uint4 *>(a.ws_o);
+  bool ok = true;
+  M = -INFINITY;
+  for (int s = lane; s < n; s += 32) {
+    const int64_t row = row0 + (int64_t)s * stride;
+    uint2 v = __ldcg(ml + row);
+    for (int it = 0; it < kMergePolls && (v.x == 0u || v.y == 0u); ++it) {
+      __nanosleep(32);
+      v = __ldcg(ml + row);
+    }
+    ok = ok && v.x != 0u && v.y != 0u;
+    M = fmaxf(M, __uint_as_float(v.x ^ kEnc));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  L = 0.0f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s0 = 0; s0 < n && ok; s0 += 32) {
+    float w = 0.0f;
+    if (s0 + lane < n) {
+      const uint2 v = __ldcg(ml + row0 + (int64_t)(s0 + lane) * stride);
+      const float ms = __uint_as_float(v.x ^ kEnc);
+      if (ms != -INFINITY) {
+        w = exp2f(ms - M);
+        L = fmaf(w, __uint_as_float(v.y ^ kEnc), L);
+      }
+    }
+    const int nb = min(32, n - s0);
+    for (int j0 = 0; j0 < nb; j0 += 8) {
+      uint4 o[8];
+      bool ready = false;
+      for (int it = 0; it < kMergePolls && !ready; ++it) {
+        bool mine = true;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          o[j] = j0 + j < nb
+                     ? __ldcg(wo + (row0 + (int64_t)(s0 + j0 + j) * stride) * (kD / 4) + lane)
+                     : make_uint4(1, 1, 1, 1);
+          mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
+        }
+        ready = __all_sync(0xffffffffu, mine);
+        if (!ready) __nanosleep(32);
+      }
+      ok = ok && ready;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+        if (j0 + j < nb && wj != 0.0f) {
+          acc[0] = fmaf(wj, __uint_as_float(o[j].x ^ kEnc), acc[0]);
+          acc[1] = fmaf(wj, __uint_as_float(o[j].y ^ kEnc), acc[1]);
+          acc[2] = fmaf(wj, __uint_as_float(o[j].z ^ kEnc), acc[2]);
+          acc[3] = fmaf(wj, __uint_as_float(o[j].w ^ kEnc), acc[3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  O = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  for (int s = 0; s < n; ++s)
+    reinterpret_cast<uint4 *>(a.ws_o)[(row0 + (int64_t)s * stride) * (kD / 4) + lane] =
+        make_uint4(0, 0, 0, 0);
+  for (int s = lane; s < n; s += 32)
+    reinterpret_cast<uint2 *>(a.ws_ml)[row0 + (int64_t)s * stride] = make_uint2(0, 0);
+  if (!__all_sync(0xffffffffu, ok)) {
+    if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+    return false;
+  }
+  return true;
+}
+
+// The warp holding head bh's last ticket merges its partials, head by head.
+template <int RG>
+__device__ bool gqa_finish(const TcArgs &a, int bh, int ticket) {
+  const int lane = threadIdx.x & 31;
+  const int nparts = gqa_slot0(a, bh, a.nc);
+  if (__shfl_sync(0xffffffffu, ticket, 0) != nparts - 1) return true;
+  const int b = bh / a.g.H, h = bh % a.g.H;
+  for (int r = 0; r < RG; ++r) {
+    float M, L;
+    float4 O;
+    if (!merge_strided(a, (int64_t)bh * a.part_stride * RG + r, RG, nparts, M, L, O))
+      return false;
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h * RG + r) * kD)[lane] =
+        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+  }
+  if (lane == 0) a.ws_cnt[bh] = 0;
+  return true;
+}
+
+template <int NGV, int KM, int RG>
+__global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using C = GqaCfg<NGV, KM, RG>;
+  constexpr int RB = C::RB;
+  constexpr int nslot = C::nslot;
+  constexpr int SLOT = C::bytes;
+  constexpr int CH = C::CH;
+  constexpr int WPG = C::WPG;
+  const Geometry &g = a.g;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  uint8_t *wring = smem + warp * nslot * SLOT;
+  uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + C::lay(nslot, 0) + warp * C::SBB);
+  float *QT = reinterpret_cast<float *>(smem + C::lay(nslot, 1) + warp * C::QTB);
+  uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + C::lay(nslot, 2)) + warp * (nslot + 1);
+
+  int x0, x1;
+  block_range(a, blockIdx.x, x0, x1);
+  const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
+
+  if (lane < 16) sBw[C::sb_zero + lane] = 0u;
+  if (lane == 0) {
+    for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+
+  // ---- producer: per head, quantized tiles lt = warp, warp + 8, ..., then
+  // fp16 chunks lt = warp, warp + 8, ... of this block's segments
+  int pc_bh = bh_first, pc_ph = 0, pc_lt = warp, pc_n = 0, issued = 0, ps = 0;
+  Seg pc_seg = seg_in(a, pc_bh, x0, x1);
+  pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
+  auto pc_settle = [&]() {
+    while (pc_bh >= 0 && pc_lt >= pc_n) {
+      if (pc_ph == 0) {
+        pc_ph = 1;
+        pc_n = pc_seg.c1 - pc_seg.c0;
+      } else {
+        if (++pc_bh > bh_last) {
+          pc_bh = -1;
+          return;
+        }
+        pc_ph = 0;
+        pc_seg = seg_in(a, pc_bh, x0, x1);
+        pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
+      }
+      pc_lt = warp;
+    }
+  };
+  auto issue_next = [&]() {
+    if (pc_bh < 0) return;
+    uint8_t *dst = wring + ps * SLOT;
+    uint64_t *bar = &wbars[ps];
+    ps = ps + 1 == nslot ? 0 : ps + 1;
+    if (lane == 0) {
+      if (pc_ph == 0) {
+        const int tok0 = pc_seg.tq0 + kTile * pc_lt;
+        bar_expect_tx(bar, (uint32_t)(C::BB + C::KMB));
+        bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * C::BB,
+                 C::BB, bar);
+        if constexpr (!C::KIN)
+          bulk_g2s(dst + C::off_km,
+                   a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
+                   C::KMB, bar);
+      } else {
+        const int ns = (int)a.n_sink;
+        const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
+        const int s0 = min(i0, ns), s1 = min(i1, ns);
+        const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;
+        bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2));
+        if (s1 > s0) {
+          const int64_t row = (int64_t)pc_bh * g.n_sink + s0;
+          bulk_g2s(dst, a.p.k_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+          bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+        }
+        if (r1 > r0) {
+          const int64_t row = (int64_t)pc_bh * g.residual + r0;
+          const int o = (s1 - s0) * kD * 2;
+          bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((r1 - r0) * kD * 2), bar);
+          bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD, (uint32_t)((r1 - r0) * kD * 2),
+                   bar);
+        }
+      }
+    }
+    ++issued;
+    pc_lt += kWarps;
+    pc_settle();
+  };
+  pc_settle();
+  for (int s = 0; s < nslot; ++s) issue_next();
+
+  // ---- per-head query table: QT[c][r] = q_r[c] * scale_log2 * 2^-E_r, and
+  // 2^E_r; loaded with plain loads when the warp starts a head
+  float pow2 = 1.0f;  // 2^E of this lane's softmax head (tig)
+  int q_head = -1;
+  auto load_q = [&](int bh) {
+    const int b = bh / g.H, h = bh % g.H;
+    float qv[RG][4];
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+      const uint2 qr = __ldg(reinterpret_cast<const uint2 *>(
+                                 a.q + ((int64_t)b * g.Hq + h * RG + r) * kD) + lane);
+      const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
+      const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
+      qv[r][0] = q01.x * a.scale_log2;
+      qv[r][1] = q01.y * a.scale_log2;
+      qv[r][2] = q23.x * a.scale_log2;
+      qv[r][3] = q23.y * a.scale_log2;
+    }
+    float e2[RG];
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+      float mx = fmaxf(fmaxf(fabsf(qv[r][0]), fabsf(qv[r][1])), fmaxf(fabsf(qv[r][2]), fabsf(qv[r][3])));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      int E = 0;
+      if (mx > 0.0f && mx < INFINITY) frexpf(mx, &E);
+      e2[r] = ldexpf(1.0f, E);
+      const float inv = ldexpf(1.0f, -E);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qv[r][i] *= inv;
+    }
+    __syncwarp();  // the previous head's readers are done with the table
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float4 t;
+      t.x = qv[0][i];
+      t.y = RG > 1 ? qv[RG > 1 ? 1 : 0][i] : 0.0f;
+      t.z = RG > 2 ? qv[RG > 2 ? 2 : 0][i] : 0.0f;
+      t.w = RG > 3 ? qv[RG > 3 ? 3 : 0][i] : 0.0f;
+      reinterpret_cast<float4 *>(QT)[4 * lane + i] = t;
+    }
+    if (lane < RG) QT[4 * kD + lane] = e2[lane < RG ? lane : 0];
+    __syncwarp();
+    pow2 = tig < RG ? QT[4 * kD + tig] : 1.0f;
+    q_head = bh;
+  };
+
+  // key-operand channel pairs this lane builds (as in the MHA kernel)
+  int b_clo[2], b_sidx[2];
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int ip = lane + 32 * m;
+    const int W = ip >> 3, p = ip & 7;
+    b_clo[m] = 16 * W + p;
+    b_sidx[m] = (W >> 1) * 16 + (4 * (W & 1) + (p >> 1)) * 2 + (p & 1);
+  }
+
+  // ---- online-softmax state: lane (gid, tig) holds head tig ---------------
+  float m_run = -INFINITY, l_lane = 0.0f, z_lane[NGV];
+  float dv[8][4];
+  auto reset_state = [&]() {
+    m_run = -INFINITY;
+    l_lane = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NGV; ++j) z_lane[j] = 0.0f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) dv[mt][r] = 0.0f;
+  };
+  reset_state();
+
+  int pend_bh = -1, pend_ticket = 0;
+  auto publish = [&](int bh, int slot, const float4 (&o)[RG], const float (&m)[RG],
+                     const float (&l)[RG]) -> bool {
+    if (pend_bh >= 0 && !gqa_finish<RG>(a, pend_bh, pend_ticket)) return false;
+    const int64_t row0 = ((int64_t)bh * a.part_stride + slot) * RG;
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+      reinterpret_cast<uint4 *>(a.ws_o + (row0 + r) * kD)[lane] = enc4(o[r]);
+      if (lane == 0)
+        reinterpret_cast<uint2 *>(a.ws_ml)[row0 + r] =
+            make_uint2(__float_as_uint(m[r]) ^ kEnc, __float_as_uint(l[r]) ^ kEnc);
+    }
+    pend_ticket = 0;
+    if (lane == 0) pend_ticket = atomicAdd(&a.ws_cnt[bh], 1);
+    pend_bh = bh;
+    return true;
+  };
+
+  // quantized state -> partial `slot` of head bh
+  auto flush_quant = [&](int bh, int slot) -> bool {
+    float l = l_lane, Z[NGV];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+#pragma unroll
+    for (int j = 0; j < NGV; ++j) {
+      float z = z_lane[j];
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      Z[j] = z;
+    }
+    float *so = reinterpret_cast<float *>(sBw);
+    __syncwarp();
+    if (tig < RG) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int j = mt / WPG, m = mt % WPG;
+        const int W = j * WPG + gid % WPG, p = m * NGV + gid / WPG;
+        const int P = m * NGV;  // extraction position of this tile
+        const float f = kSub * kSlackScale / pos_factor<2>(P);
+        so[tig * kD + 16 * W + p] = fmaf(dv[mt][0] + dv[mt][1], f, Z[j]);
+        so[tig * kD + 16 * W + 8 + p] = fmaf(dv[mt][2] + dv[mt][3], f, Z[j]);
+      }
+    }
+    __syncwarp();
+    float4 o[RG];
+    float mm[RG], ll[RG];
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+      o[r] = reinterpret_cast<const float4 *>(so)[r * (kD / 4) + lane];
+      mm[r] = __shfl_sync(0xffffffffu, m_run, r);
+      ll[r] = __shfl_sync(0xffffffffu, l, r);
+    }
+    __syncwarp();
+    reset_state();
+    return publish(bh, slot, o, mm, ll);
+  };
+
+  int cs = 0, done = 0;
+  uint32_t cph = 0;
+  bool first = true;
+  auto wait_slot = [&](int &s_out) -> bool {
+    bool ok = true;
+    if (first && a.stall_limit > 0) ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
+    first = false;
+    if (ok) ok = bar_wait(&wbars[cs], cph, a.wait_limit);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+      return false;
+    }
+    s_out = cs;
+    if (++cs == nslot) {
+      cs = 0;
+      cph ^= 1u;
+    }
+    ++done;
+    return true;
+  };
+
+  bool aborted = false;
+  for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
+    const Seg sg = seg_in(a, bh, x0, x1);
+    const int base = bh * a.U;
+    const int tq0 = sg.tq0, tq1 = sg.tq1;
+    if (tq1 > tq0) {
+      if (q_head != bh) load_q(bh);
+      const int nt = (tq1 - tq0 + kTile - 1) / kTile;
+      for (int lt = warp; lt < nt; lt += kWarps) {
+        int s;
+        if (!wait_slot(s)) {
+          aborted = true;
+          break;
+        }
+        const uint8_t *slot = wring + s * SLOT;
+        const int tok0 = tq0 + kTile * lt;
+        const int n = min(kTile, tq1 - tok0);
+        const uint8_t *kc = slot;
+        const uint8_t *vc = slot + C::off_vc;
+        // ---- key operand: columns (r, hi/lo) of QT * scale / 4^p, and the
+        // per-head bias sum_c QT * zero, for this tile's key group
+        const float *ks = reinterpret_cast<const float *>(slot + C::off_km), *kz = ks + kD;
+        float bpart[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const int clo = b_clo[m], chi = clo + 8;
+          const float ipf = 1.0f / pos_factor<2>(clo & 7);
+          const float slo = ks[clo] * ipf, shi = ks[chi] * ipf;
+          const float zlo = kz[clo], zhi = kz[chi];
+          const float4 ql = reinterpret_cast<const float4 *>(QT)[clo];
+          const float4 qh = reinterpret_cast<const float4 *>(QT)[chi];
+          const float qlo[4] = {ql.x, ql.y, ql.z, ql.w}, qhi[4] = {qh.x, qh.y, qh.z, qh.w};
+#pragma unroll
+          for (int r = 0; r < RG; ++r) {
+            uint32_t hi, lo;
+            split2(qlo[r] * slo, qhi[r] * shi, hi, lo);
+            sBw[(2 * r) * 64 + b_sidx[m]] = hi;
+            sBw[(2 * r + 1) * 64 + b_sidx[m]] = lo;
+            bpart[r] = fmaf(qlo[r], zlo, fmaf(qhi[r], zhi, bpart[r]));
+          }
+        }
+        // reduce-scatter of the 4 bias sums: lane L ends with head (L >> 3)
+        {
+          const bool h4 = lane & 16;
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float mine = h4 ? bpart[j + 2] : bpart[j], other = h4 ? bpart[j] : bpart[j + 2];
+            bpart[j] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
+          }
+          const bool h3 = lane & 8;
+          const float mine = h3 ? bpart[1] : bpart[0], other = h3 ? bpart[0] : bpart[1];
+          bpart[0] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+          bpart[0] += __shfl_xor_sync(0xffffffffu, bpart[0], 4);
+          bpart[0] += __shfl_xor_sync(0xffffffffu, bpart[0], 2);
+          bpart[0] += __shfl_xor_sync(0xffffffffu, bpart[0], 1);
+        }
+        const float bias = __shfl_sync(0xffffffffu, bpart[0], (tig & 3) << 3);
+        __syncwarp();
+        // ---- keys: D[token][(r, hi/lo)]
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+          const uint32_t *bsrc = gid < 2 * RG ? sBw + gid * 64 + tig * 16 : sBw + C::sb_zero;
+          const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
+          const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
+          const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
+          const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {
+            const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
+            const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
+            const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
+            const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const uint2 b = *reinterpret_cast<const uint2 *>(bsrc + 2 * (4 * m + jj));
+              mma16816(d0, ext<2>(w00, s00, 2 * jj), ext<2>(w01, s01, 2 * jj),
+                       ext<2>(w00, s00, 2 * jj + 1), ext<2>(w01, s01, 2 * jj + 1), b.x, b.y);
+              mma16816(d1, ext<2>(w10, s10, 2 * jj), ext<2>(w11, s11, 2 * jj),
+                       ext<2>(w10, s10, 2 * jj + 1), ext<2>(w11, s11, 2 * jj + 1), b.x, b.y);
+            }
+          }
+        }
+        // ---- scores of head tig for tokens gid, gid + 8, gid + 16, gid + 24
+        float sc[4];
+        sc[0] = fmaf(d0[0] + d0[1], kSub, bias) * pow2;
+        sc[1] = fmaf(d0[2] + d0[3], kSub, bias) * pow2;
+        sc[2] = fmaf(d1[0] + d1[1], kSub, bias) * pow2;
+        sc[3] = fmaf(d1[2] + d1[3], kSub, bias) * pow2;
+        bool grow = false;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const bool valid = tig < RG && gid + 8 * i < n;
+          sc[i] = valid ? sc[i] : -INFINITY;
+          grow = grow || sc[i] > m_run + kSlack;
+        }
+        if (__any_sync(0xffffffffu, grow)) {
+          float mt_ = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
+          if (mt_ > m_run) {
+            const float alpha = exp2f(m_run - mt_);
+            l_lane *= alpha;
+#pragma unroll
+            for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+              for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
+            m_run = mt_;
+          }
+        }
+        float pv[4];
+        {
+          const float *vz = reinterpret_cast<const float *>(slot + C::off_vz);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float p = sc[i] == -INFINITY ? 0.0f : exp2f(sc[i] - m_run);
+            pv[i] = p * kInvSlack;
+            l_lane += p;
+            if (p > 0.0f) {
+              const float *zr = vz + (gid + 8 * i) * NGV;
+#pragma unroll
+              for (int j = 0; j < NGV; ++j) z_lane[j] = fmaf(p, zr[j], z_lane[j]);
+            }
+          }
+        }
+        // ---- values: per value group j, its 16-row tiles and columns (r, hi/lo)
+        {
+          const float *vs = reinterpret_cast<const float *>(slot + C::off_vs);
+          const int r = gid >> 1;
+          const bool bact = r < RG;
+          const int src0 = 4 * tig + (bact ? r : 0), src1 = 4 * (tig + 4) + (bact ? r : 0);
+          const int sh = 2 * (gid / WPG);  // this lane's code position offset
+          const int nkb = n > 16 ? 2 : 1;
+          for (int kb = 0; kb < nkb; ++kb) {
+            const int tk0 = 16 * kb + tig, tk1 = tk0 + 4, tk2 = tk0 + 8, tk3 = tk0 + 12;
+            const float plo = kb ? pv[2] : pv[0], phi = kb ? pv[3] : pv[1];
+            const float p0 = __shfl_sync(0xffffffffu, plo, src0);
+            const float p1 = __shfl_sync(0xffffffffu, plo, src1);
+            const float p2 = __shfl_sync(0xffffffffu, phi, src0);
+            const float p3 = __shfl_sync(0xffffffffu, phi, src1);
+#pragma unroll
+            for (int j = 0; j < NGV; ++j) {
+              const float x0 = p0 > 0.0f ? p0 * vs[tk0 * NGV + j] : 0.0f;
+              const float x1 = p1 > 0.0f ? p1 * vs[tk1 * NGV + j] : 0.0f;
+              const float x2 = p2 > 0.0f ? p2 * vs[tk2 * NGV + j] : 0.0f;
+              const float x3 = p3 > 0.0f ? p3 * vs[tk3 * NGV + j] : 0.0f;
+              uint32_t h01, l01, h23, l23;
+              split2(x0, x1, h01, l01);
+              split2(x2, x3, h23, l23);
+              const uint32_t bv0 = bact ? ((gid & 1) ? l01 : h01) : 0u;
+              const uint32_t bv1 = bact ? ((gid & 1) ? l23 : h23) : 0u;
+              const int W = j * WPG + gid % WPG;
+              const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * W);
+              const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * W);
+              const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vc + tk2 * RB + 4 * W);
+              const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vc + tk3 * RB + 4 * W);
+              const uint32_t ya = __byte_perm(w0, w1, 0x5410) >> sh, yb = __byte_perm(w0, w1, 0x7632) >> sh;
+              const uint32_t yc = __byte_perm(w2, w3, 0x5410) >> sh, yd = __byte_perm(w2, w3, 0x7632) >> sh;
+              const uint32_t sa = shifted<2>(ya), sb = shifted<2>(yb);
+              const uint32_t sc_ = shifted<2>(yc), sd = shifted<2>(yd);
+#pragma unroll
+              for (int m = 0; m < WPG; ++m) {
+                const int P = m * NGV;
+                mma16816(dv[j * WPG + m], ext<2>(ya, sa, P), ext<2>(yb, sb, P), ext<2>(yc, sc_, P),
+                         ext<2>(yd, sd, P), bv0, bv1);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        issue_next();
+      }
+      if (aborted) break;
+      if (!flush_quant(bh, kWarps * ((int)blockIdx.x - owner_of(base, a.total, a.nc)) + warp)) {
+        aborted = true;
+        break;
+      }
+    }
+    // ---- fp16 chunks of this block's segment, one head at a time ----------
+    const int nchk = sg.c1 - sg.c0;
+    if (warp < nchk) {
+      if (q_head != bh) load_q(bh);
+      float qq[RG][4], mf[RG], lf[RG], af[RG][4];
+#pragma unroll
+      for (int r = 0; r < RG; ++r) {
+        const float e = QT[4 * kD + r];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qq[r][i] = QT[4 * (4 * lane + i) + r] * e;
+        mf[r] = -INFINITY;
+        lf[r] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) af[r][i] = 0.0f;
+      }
+      for (int lt = warp; lt < nchk; lt += kWarps) {
+        int s;
+        if (!wait_slot(s)) {
+          aborted = true;
+          break;
+        }
+        const uint8_t *slot = wring + s * SLOT;
+        const int i0 = (sg.c0 + lt) * CH;
+        const int nv = min(CH, (int)a.n_fp16 - i0);
+        const uint2 *kr = reinterpret_cast<const uint2 *>(slot);
+        const uint2 *vr = reinterpret_cast<const uint2 *>(slot + CH * kD * 2);
+        for (int t = 0; t < nv; ++t) {
+          const uint2 kw = kr[t * (kD / 4) + lane], vw = vr[t * (kD / 4) + lane];
+          const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
+          const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
+          const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+          const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+#pragma unroll
+          for (int r = 0; r < RG; ++r) {
+            float sc_ = fmaf(qq[r][0], k01.x, fmaf(qq[r][1], k01.y, fmaf(qq[r][2], k23.x, qq[r][3] * k23.y)));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sc_ += __shfl_xor_sync(0xffffffffu, sc_, off);
+            const float mn = fmaxf(mf[r], sc_);
+            const float al = exp2f(mf[r] - mn), pp = exp2f(sc_ - mn);
+            lf[r] = fmaf(lf[r], al, pp);
+            af[r][0] = fmaf(af[r][0], al, pp * v01.x);
+            af[r][1] = fmaf(af[r][1], al, pp * v01.y);
+            af[r][2] = fmaf(af[r][2], al, pp * v23.x);
+            af[r][3] = fmaf(af[r][3], al, pp * v23.y);
+            mf[r] = mn;
+          }
+        }
+        __syncwarp();
+        issue_next();
+      }
+      if (aborted) break;
+      float4 o[RG];
+#pragma unroll
+      for (int r = 0; r < RG; ++r) o[r] = make_float4(af[r][0], af[r][1], af[r][2], af[r][3]);
+      if (!publish(bh, gqa_slot0(a, bh, blockIdx.x) + warp, o, mf, lf)) {
+        aborted = true;
+        break;
+      }
+    }
+  }
+  if (!aborted && pend_bh >= 0 && !gqa_finish<RG>(a, pend_bh, pend_ticket)) aborted = true;
+  if (aborted && lane == 0)
+    for (int i = done; i < issued; ++i)
+      bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
+}
+
+template <int NGV, int KM, int RG>
+cudaError_t launch_gqa_t(TcArgs &a, int num_sms, cudaStream_t st) {
+  using C = GqaCfg<NGV, KM, RG>;
+  auto kern = tc_gqa_kernel<NGV, KM, RG>;
+  if (a.g.block_bytes != C::BB || tc_fp16_chunk(a.g) != C::CH) return cudaErrorInvalidValue;
+  static int occ = 0;
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem);
+    if (e != cudaSuccess) return e;
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads, C::smem);
+    if (e != cudaSuccess) return e;
+    occ = o < 1 ? 1 : o;
+  }
+  int64_t nc = (int64_t)num_sms * occ;
+  if (nc > kTcMaxBlocks) nc = kTcMaxBlocks;
+  if (nc > a.total) nc = a.total;
+  if (nc < 1) nc = 1;
+  a.nc = (int)nc;
+  kern<<<(unsigned)nc, kThreads, C::smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int RG>
+cudaError_t launch_gqa_r(TcArgs &a, int num_sms, cudaStream_t st) {
+  const int ngv = kD / a.g.v_group;
+  const int km = a.g.k_group == 32 ? 1 : 0;
+  if (ngv == 4) return km ? launch_gqa_t<4, 1, RG>(a, num_sms, st) : launch_gqa_t<4, 0, RG>(a, num_sms, st);
+  return km ? launch_gqa_t<2, 1, RG>(a, num_sms, st) : launch_gqa_t<2, 0, RG>(a, num_sms, st);
+}
+
+}  // namespace
+
+bool gqa_decode_supported(const Geometry &g) {
+  if (g.d != kD || g.bits != 2 || g.scheme != KVQ_KIVI) return false;
+  const int rg = g.Hq / g.H;
+  if (rg != 2 && rg != 4) return false;
+  const int ngv = kD / g.v_group;
+  if (ngv != 2 && ngv != 4) return false;
+  return g.k_group >= 32 && g.k_group <= 128;
+}
+
+cudaError_t launch_decode_gqa(const Geometry &g, const CachePtrs &p, int64_t n_quant,
+                              int64_t n_resid, int64_t n_sink, const __half *q, float *out,
+                              float scale, void *ws, int num_sms, cudaStream_t st) {
+  TcArgs a;
+  a.g = g;
+  a.p = p;
+  a.q = q;
+  a.out = out;
+  a.k_new = nullptr;
+  a.v_new = nullptr;
+  a.new_row = -1;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.n_quant = n_quant;
+  a.n_fp16 = n_resid + n_sink;
+  a.n_sink = n_sink;
+  a.S_h = (int)((n_quant + kUnit - 1) / kUnit);
+  const int kmb = g.k_group > kBlockTokens ? 2 * kD * 4 : 0;
+  const int CH = tc_fp16_chunk(g);
+  const int64_t unit_bytes = (int64_t)(kUnit / kBlockTokens) * (g.block_bytes + kmb);
+  a.CPU = (int)(unit_bytes / (CH * 4 * kD));
+  if (a.CPU < 1) a.CPU = 1;
+  a.nch = (int)((a.n_fp16 + CH - 1) / CH);
+  a.F_h = (a.nch + a.CPU - 1) / a.CPU;
+  a.U = a.S_h + a.F_h;
+  const int64_t total = (int64_t)g.B * g.H * a.U;
+  if (total >= (1LL << 31)) return cudaErrorInvalidValue;
+  a.total = (int)total;
+  a.part_stride = tc_part_slots(g);
+  if (a.part_stride & 1) return cudaErrorInvalidValue;  // keeps ws_o 16-byte aligned
+  const int rg = g.Hq / g.H;
+  const int64_t BH = (int64_t)g.B * g.H;
+  char *base = static_cast<char *>(ws);
+  const size_t cnt = ((size_t)BH * sizeof(int) + 255) & ~(size_t)255;
+  a.ws_cnt = reinterpret_cast<int *>(base);
+  a.ws_ml = reinterpret_cast<float *>(base + cnt);
+  a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * rg * 2;
+  a.wait_limit = 1 << 24;
+  a.stall_limit = debug_stall_limit();
+  return rg == 4 ? launch_gqa_r<4>(a, num_sms, st) : launch_gqa_r<2>(a, num_sms, st);
+}
+
+}  // namespace kvq

@@ -128,6 +128,13 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
                              const __half *k_new = nullptr, const __half *v_new = nullptr);
 void set_debug_stall(long long iterations);
 
+// Tensor-core grouped-query path (head_dim 128, 2-bit KIVI, G >= 32, 2 or 4
+// query heads per KV head, 2 or 4 value groups).
+bool gqa_decode_supported(const Geometry &g);
+cudaError_t launch_decode_gqa(const Geometry &g, const CachePtrs &p, int64_t n_quant,
+                              int64_t n_resid, int64_t n_sink, const __half *q, float *out,
+                              float scale, void *ws, int num_sms, cudaStream_t st);
+
 // ---- quantization arithmetic (bit-exact contract with the formula) -------
 // Asymmetric: scale = (max - min) / (2^b - 1), zero = min,
 // code = clamp(rint((x - min) / scale), 0, 2^b - 1); constant group: 0, 0.

@@ -51,6 +51,10 @@ SMALL = {
                             k_group=128, v_group=32, residual=128, n_append=140),
     "innerq_g32_2bit": S(W["innerq_1m"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, bits=2,
                          k_group=32, v_group=32, n_append=30),
+    # grouped-query tensor-core path: 2 query heads per KV head, G 64, two
+    # value groups (the gqa_small case covers 4 heads per KV head, G 32)
+    "gqa_rg2_g64": S(W["gqa_2bit"], batch=2, n_q_heads=8, n_kv_heads=4, ctx=900, k_group=64,
+                     v_group=64, residual=128, n_append=150),
 }
 
 
