@@ -307,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     const float lt = fmaf(l, wq, lf * wf);
     reset_state();
     // the previous head's ticket has long arrived: act on it, then publish
-    if (pend_bh >= 0 && !finish_head(a, pend_bh, pend_ticket)) return false;
+    if (pend_bh >= 0 && !finish_head<8>(a, pend_bh, pend_ticket)) return false;
     pend_ticket = publish_partial(a, bh, slot, o, m, lt);
     pend_bh = bh;
     return true;
@@ -719,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       break;
     }
   }
-  if (!aborted && pend_bh >= 0 && !finish_head(a, pend_bh, pend_ticket)) aborted = true;
+  if (!aborted && pend_bh >= 0 && !finish_head<24>(a, pend_bh, pend_ticket)) aborted = true;
   if (aborted) {
     // give up this block's work for this warp; its copies complete first
     if (lane == 0)

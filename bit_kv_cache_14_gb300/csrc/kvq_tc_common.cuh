@@ -271,6 +271,10 @@ __device__ __forceinline__ int publish_partial(const TcArgs &a, int bh, int slot
 // Called by the whole warp with lane 0's ticket for head bh: if it was the
 // head's last, merge.  Returns false if the partials did not all appear
 // within the poll bound (status word set).
+// MB: partial rows fetched in one round of loads on the fast path (the
+// kernel's last call can afford many registers; calls inside the tile loop
+// use few).
+template <int MB>
 __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
   const int lane = threadIdx.x & 31;
   const int nparts = head_nparts(a, bh);
@@ -278,6 +282,48 @@ __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
   const int64_t base = (int64_t)bh * a.part_stride;
   const uint2 *ml = reinterpret_cast<const uint2 *>(a.ws_ml) + base;
   const uint4 *wo = reinterpret_cast<const uint4 *>(a.ws_o + base * kD);
+  const int b = bh / a.g.H, h = bh % a.g.H;
+  if (nparts <= MB) {
+    // fast path: every (m, l) and o row loaded in one round; taken when all
+    // of them are already visible (the usual case: the tickets came last)
+    const uint2 v = lane < nparts ? __ldcg(ml + lane) : make_uint2(1u, 1u);
+    uint4 o[MB];
+#pragma unroll
+    for (int j = 0; j < MB; ++j)
+      o[j] = j < nparts ? __ldcg(wo + (int64_t)j * (kD / 4) + lane) : make_uint4(1, 1, 1, 1);
+    bool mine = v.x != 0u && v.y != 0u;
+#pragma unroll
+    for (int j = 0; j < MB; ++j) mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
+    if (__all_sync(0xffffffffu, mine)) {
+      const float ms = lane < nparts ? __uint_as_float(v.x ^ kEnc) : -INFINITY;
+      float M = ms;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float w = ms != -INFINITY ? exp2f(ms - M) : 0.0f;
+      float L = w * (lane < nparts ? __uint_as_float(v.y ^ kEnc) : 0.0f);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+      float O[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < MB; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, w, j & 31);
+        if (j < nparts && wj != 0.0f) {
+          O[0] = fmaf(wj, __uint_as_float(o[j].x ^ kEnc), O[0]);
+          O[1] = fmaf(wj, __uint_as_float(o[j].y ^ kEnc), O[1]);
+          O[2] = fmaf(wj, __uint_as_float(o[j].z ^ kEnc), O[2]);
+          O[3] = fmaf(wj, __uint_as_float(o[j].w ^ kEnc), O[3]);
+        }
+      }
+      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+      reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h) * kD)[lane] =
+          make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+      for (int s = 0; s < nparts; ++s)
+        reinterpret_cast<uint4 *>(a.ws_o + base * kD)[(int64_t)s * (kD / 4) + lane] = make_uint4(0, 0, 0, 0);
+      if (lane < nparts) reinterpret_cast<uint2 *>(a.ws_ml)[base + lane] = make_uint2(0, 0);
+      if (lane == 0) a.ws_cnt[bh] = 0;
+      return true;
+    }
+  }
   // (m, l) of partial s sits in lane s % 32; every load is re-polled
   // (bounded) until its words are non-zero
   auto ml_of = [&](int s) -> uint2 {
@@ -342,7 +388,6 @@ __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
     if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
     return false;
   }
-  const int b = bh / a.g.H, h = bh % a.g.H;
   const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
   float4 r;
   r.x = O[0] * inv;
