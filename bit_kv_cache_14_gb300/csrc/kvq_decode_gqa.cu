@@ -731,6 +731,9 @@ cudaError_t launch_decode_gqa(const Geometry &g, const CachePtrs &p, int64_t n_q
   a.nch = (int)((a.n_fp16 + CH - 1) / CH);
   a.F_h = (a.nch + a.CPU - 1) / a.CPU;
   a.U = a.S_h + a.F_h;
+  a.HU = 0;
+  a.nw = 0;
+  a.UPC = 0;
   const int64_t total = (int64_t)g.B * g.H * a.U;
   if (total >= (1LL << 31)) return cudaErrorInvalidValue;
   a.total = (int)total;

@@ -42,6 +42,29 @@ namespace kvq {
 
 namespace {
 
+// Work units: a quantized tile is one unit, an fp16 chunk kChunkUnits (its
+// dot products run on the CUDA cores in a long dependent chain), and every
+// head has kHeadUnits units that hold no data (they stand for the cost of a
+// head change, so a warp that changes heads gets less data).
+constexpr int kHeadUnits = 1;
+constexpr int kChunkUnits = 2;
+
+// What unit range [x0, x1) holds of head bh: its U units are HU empty ones,
+// S_h quantized tiles of kTile tokens, then F_h = nch * UPC fp16 units; a
+// chunk belongs to the warp that holds its first unit.
+__device__ __forceinline__ Seg warp_seg(const TcArgs &a, int bh, int x0, int x1) {
+  Seg s;
+  const int base = bh * a.U;
+  const int ua = max(x0, base) - base, ub = min(x1, base + a.U) - base;
+  const int qa = max(ua - a.HU, 0), qb = min(ub - a.HU, a.S_h);
+  s.tq0 = qa * kTile;
+  s.tq1 = qa < qb ? (int)min((int64_t)qb * kTile, a.n_quant) : s.tq0;
+  const int fa = max(ua - a.HU - a.S_h, 0), fb = min(ub - a.HU - a.S_h, a.F_h);
+  s.c0 = (fa + a.UPC - 1) / a.UPC;
+  s.c1 = fa < fb ? min((fb + a.UPC - 1) / a.UPC, a.nch) : s.c0;
+  return s;
+}
+
 template <int BITS, int SCHEME, int NGV, int NGK, int KM>
 __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -58,8 +81,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
   uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB + warp * SC::SBB);
 
-  int x0, x1;
-  block_range(a, blockIdx.x, x0, x1);
+  // Warp-level stream-K: warp gw of the grid owns units [x0, x1) of the
+  // concatenated per-head unit lists (units of one tile or fp16 chunk).
+  const int gw = (int)blockIdx.x * kWarps + warp;
+  if (gw >= a.nw) return;
+  const int x0 = (int)((int64_t)gw * a.total / a.nw);
+  const int x1 = (int)((int64_t)(gw + 1) * a.total / a.nw);
   const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
   // fp16 tokens per chunk: a chunk's K and V rows fill the slot up to the query
   constexpr int CH = SC::CH;
@@ -76,10 +103,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   __syncwarp();
 
   // ---- producer: this warp's items in the order the consumer visits them:
-  // per head, its quantized tiles lt = warp, warp + 8, ..., then its fp16
-  // chunks lt = warp, warp + 8, ... of this block's segments.
-  int pc_bh = bh_first, pc_ph = 0, pc_lt = warp, pc_n = 0, issued = 0, ps = 0;
-  Seg pc_seg = seg_in(a, pc_bh, x0, x1);
+  // per head, its quantized tiles, then its fp16 chunks.
+  int pc_bh = bh_first, pc_ph = 0, pc_lt = 0, pc_n = 0, issued = 0, ps = 0;
+  Seg pc_seg = warp_seg(a, pc_bh, x0, x1);
   pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
   auto pc_settle = [&]() {
     while (pc_bh >= 0 && pc_lt >= pc_n) {
@@ -92,10 +118,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           return;
         }
         pc_ph = 0;
-        pc_seg = seg_in(a, pc_bh, x0, x1);
+        pc_seg = warp_seg(a, pc_bh, x0, x1);
         pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
       }
-      pc_lt = warp;
+      pc_lt = 0;
     }
   };
   // Called by the whole warp; lane 0 posts the byte count and issues the
@@ -105,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // query row rides along with the warp's first item of each phase of a head.
   auto issue_next = [&]() {
     if (pc_bh < 0) return;
-    const bool first = pc_lt == warp;
+    const bool first = pc_lt == 0;
     uint8_t *dst = wring + ps * SLOT;
     uint64_t *bar = &wbars[ps];
     ps = ps + 1 == nslot ? 0 : ps + 1;
@@ -152,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       if (first) bulk_g2s(dst + SC::off_q, qrow, kD * 2, bar);
     }
     ++issued;
-    pc_lt += kWarps;
+    ++pc_lt;
     pc_settle();
   };
   pc_settle();
@@ -308,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     reset_state();
     // the previous head's ticket has long arrived: act on it, then publish
     if (pend_bh >= 0 && !finish_head<8>(a, pend_bh, pend_ticket)) return false;
-    pend_ticket = publish_partial(a, bh, slot, o, m, lt);
+    publish_partial(a, bh, slot, o, m, lt);
+    pend_ticket = take_ticket(a, bh);
     pend_bh = bh;
     return true;
   };
@@ -340,19 +367,21 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   };
   bool aborted = false;
   for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
-    const Seg sg = seg_in(a, bh, x0, x1);
+    const Seg sg = warp_seg(a, bh, x0, x1);
     const int tq0 = sg.tq0, tq1 = sg.tq1;
+    // fp16 sink + residual / window chunks of this warp's segment
+    const int nchk = sg.c1 - sg.c0;
     const int base = bh * a.U;
     if (tq1 > tq0) {
       const int nt = (tq1 - tq0 + kTile - 1) / kTile;
-      for (int lt = warp; lt < nt; lt += kWarps) {
+      for (int lt = 0; lt < nt; ++lt) {
         int s;
         if (!wait_slot(s)) {
           aborted = true;
           break;
         }
         const uint8_t *slot = wring + s * SLOT;
-        if (lt == warp) start_head(slot);
+        if (lt == 0) start_head(slot);
         const int tok0 = tq0 + kTile * lt;
         const int n = min(kTile, tq1 - tok0);
         auto tile = [&](auto full_c) {
@@ -610,20 +639,19 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       }
       if (aborted) break;
     }
-    // fp16 sink + residual / window chunks of this block's segment: chunk
-    // lt goes to warp lt mod 8; a lane owns channels 4*lane .. 4*lane + 3.
-    const int nchk = sg.c1 - sg.c0;
-    if (tq1 <= tq0 && nchk <= 0) continue;
+    // fp16 chunks; a lane owns channels 4*lane .. 4*lane + 3.  A warp whose
+    // range holds only a head's empty unit still publishes (an empty
+    // partial): the head's partial count includes every warp it touches.
     float mf = -INFINITY, lf = 0.0f, af[4] = {0.f, 0.f, 0.f, 0.f};
     {
-      for (int lt = warp; lt < nchk; lt += kWarps) {
+      for (int lt = 0; lt < nchk; ++lt) {
         int s;
         if (!wait_slot(s)) {
           aborted = true;
           break;
         }
         const uint8_t *slot = wring + s * SLOT;
-        if (lt == warp) {
+        if (lt == 0) {
           const uint2 qr = reinterpret_cast<const uint2 *>(slot + SC::off_q)[lane];
           const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
           const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
@@ -714,14 +742,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       }
       if (aborted) break;
     }
-    if (!flush(bh, kWarps * ((int)blockIdx.x - owner_of(base, a.total, a.nc)) + warp, mf, lf, af)) {
+    if (!flush(bh, gw - owner_of(base, a.total, a.nw), mf, lf, af)) {
       aborted = true;
       break;
     }
   }
   if (!aborted && pend_bh >= 0 && !finish_head<24>(a, pend_bh, pend_ticket)) aborted = true;
   if (aborted) {
-    // give up this block's work for this warp; its copies complete first
+    // give up this warp's work; its copies complete first
     if (lane == 0)
       for (int i = done; i < issued; ++i)
         bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
@@ -746,9 +774,13 @@ cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   }
   int64_t nc = (int64_t)num_sms * occ;
   if (nc > kTcMaxBlocks) nc = kTcMaxBlocks;
-  if (nc > a.total) nc = a.total;
-  if (nc < 1) nc = 1;
+  // every working warp gets at least one unit
+  int64_t nw = nc * kWarps;
+  if (nw > a.total) nw = a.total;
+  if (nw < 1) nw = 1;
+  nc = (nw + kWarps - 1) / kWarps;
   a.nc = (int)nc;
+  a.nw = (int)nw;
   kern<<<(unsigned)nc, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -807,18 +839,18 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.n_quant = n_quant;
   a.n_fp16 = n_resid + n_sink;
   a.n_sink = n_sink;
-  a.S_h = (int)((n_quant + kUnit - 1) / kUnit);
+  a.S_h = (int)((n_quant + kTile - 1) / kTile);
   // fp16 rows travel in chunks of CH tokens (K and V rows fill a ring slot up
-  // to its query row; the kernel's SlotCfg::CH is the same expression), and
-  // CPU chunks -- about a unit's bytes -- make one work unit.
-  const int kmb = (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens) ? 2 * kD * 4 : 0;
+  // to its query row; the kernel's SlotCfg::CH is the same expression)
   const int CH = tc_fp16_chunk(g);
-  const int64_t unit_bytes = (int64_t)(kUnit / kBlockTokens) * (g.block_bytes + kmb);
-  a.CPU = (int)(unit_bytes / (CH * 4 * kD));
-  if (a.CPU < 1) a.CPU = 1;
+  a.CPU = 1;
+  a.UPC = kChunkUnits;
   a.nch = (int)((a.n_fp16 + CH - 1) / CH);
-  a.F_h = (a.nch + a.CPU - 1) / a.CPU;
-  a.U = a.S_h + a.F_h;
+  a.F_h = a.nch * a.UPC;
+  // a head change costs a warp about one tile's time (its flush, the next
+  // head's query setup): one empty unit per head
+  a.HU = kHeadUnits;
+  a.U = a.HU + a.S_h + a.F_h;
   const int64_t total = (int64_t)g.B * g.H * a.U;
   if (total >= (1LL << 31)) return cudaErrorInvalidValue;
   a.total = (int)total;

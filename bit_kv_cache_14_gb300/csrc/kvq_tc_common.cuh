@@ -17,7 +17,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnit = 128;    // tokens per stream-K work unit
+constexpr int kUnit = 128;    // tokens per stream-K work unit (grouped-query kernel)
 constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
 constexpr int kD = 128;
 constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
@@ -39,10 +39,13 @@ struct TcArgs {
   float scale_log2;
   int64_t n_quant, n_fp16, n_sink;
   int S_h, F_h, U;  // quantized units, fp16 units, units per head
-  int CPU;          // fp16 chunks per fp16 unit
+  int CPU;          // fp16 chunks per fp16 unit (grouped-query kernel)
+  int UPC;          // units per fp16 chunk (warp-level split)
   int nch;          // fp16 chunks per head
   int total;        // BH * U
   int nc;           // resident blocks
+  int HU;           // leading units of a head that hold no data (a head change's cost)
+  int nw;           // warps given work (warp-level split; 0 where work is split by block)
   float *ws_ml, *ws_o;
   int *ws_cnt;
   int part_stride;
@@ -229,11 +232,11 @@ __device__ __forceinline__ Seg seg_in(const TcArgs &a, int bh, int x0, int x1) {
   return s;
 }
 
-// Partials of head bh: one per warp of every block whose units touch it
-// (quantized or fp16), slot 8 * (block - first such block) + warp.
+// Partials of head bh under the warp-level split: one per warp whose unit
+// range touches the head, slot (warp - first such warp).
 __device__ __forceinline__ int head_nparts(const TcArgs &a, int bh) {
   const int base = bh * a.U;
-  return kWarps * (owner_of(base + a.U - 1, a.total, a.nc) - owner_of(base, a.total, a.nc) + 1);
+  return owner_of(base + a.U - 1, a.total, a.nw) - owner_of(base, a.total, a.nw) + 1;
 }
 
 // Partials are stored XOR-ed with kEnc: no float that arithmetic produces
@@ -252,20 +255,21 @@ __device__ __forceinline__ uint4 enc4(float4 v) {
                     __float_as_uint(v.z) ^ kEnc, __float_as_uint(v.w) ^ kEnc);
 }
 
+// Lane 0's ticket for head bh (a relaxed atomic; read the result later).
+__device__ __forceinline__ int take_ticket(const TcArgs &a, int bh) {
+  return (threadIdx.x & 31) == 0 ? atomicAdd(&a.ws_cnt[bh], 1) : 0;
+}
+
 // Stores partial `slot` of head bh: the lane's 4 output channels and (lane 0)
-// m, l.  Returns the ticket of lane 0's relaxed atomic (read it later).
-__device__ __forceinline__ int publish_partial(const TcArgs &a, int bh, int slot, float4 o,
-                                               float m, float l) {
+// m, l.
+__device__ __forceinline__ void publish_partial(const TcArgs &a, int bh, int slot, float4 o,
+                                                float m, float l) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)bh * a.part_stride + slot;
   reinterpret_cast<uint4 *>(a.ws_o + row * kD)[lane] = enc4(o);
-  int ticket = 0;
-  if (lane == 0) {
+  if (lane == 0)
     reinterpret_cast<uint2 *>(a.ws_ml)[row] =
         make_uint2(__float_as_uint(m) ^ kEnc, __float_as_uint(l) ^ kEnc);
-    ticket = atomicAdd(&a.ws_cnt[bh], 1);
-  }
-  return ticket;
 }
 
 // Called by the whole warp with lane 0's ticket for head bh: if it was the
@@ -284,17 +288,27 @@ __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
   const uint4 *wo = reinterpret_cast<const uint4 *>(a.ws_o + base * kD);
   const int b = bh / a.g.H, h = bh % a.g.H;
   if (nparts <= MB) {
-    // fast path: every (m, l) and o row loaded in one round; taken when all
-    // of them are already visible (the usual case: the tickets came last)
-    const uint2 v = lane < nparts ? __ldcg(ml + lane) : make_uint2(1u, 1u);
+    // every (m, l) and o row loaded in one round, repeated (bounded) until
+    // all of them are visible
+    uint2 v;
     uint4 o[MB];
+    bool all = false;
+    for (int it = 0; it < kMergePolls && !all; ++it) {
+      if (it > 0) __nanosleep(32);
+      v = lane < nparts ? __ldcg(ml + lane) : make_uint2(1u, 1u);
 #pragma unroll
-    for (int j = 0; j < MB; ++j)
-      o[j] = j < nparts ? __ldcg(wo + (int64_t)j * (kD / 4) + lane) : make_uint4(1, 1, 1, 1);
-    bool mine = v.x != 0u && v.y != 0u;
+      for (int j = 0; j < MB; ++j)
+        o[j] = j < nparts ? __ldcg(wo + (int64_t)j * (kD / 4) + lane) : make_uint4(1, 1, 1, 1);
+      bool mine = v.x != 0u && v.y != 0u;
 #pragma unroll
-    for (int j = 0; j < MB; ++j) mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
-    if (__all_sync(0xffffffffu, mine)) {
+      for (int j = 0; j < MB; ++j) mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
+      all = __all_sync(0xffffffffu, mine);
+    }
+    if (!all) {
+      if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+      return false;
+    }
+    {
       const float ms = lane < nparts ? __uint_as_float(v.x ^ kEnc) : -INFINITY;
       float M = ms;
 #pragma unroll
