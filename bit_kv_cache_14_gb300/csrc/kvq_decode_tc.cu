@@ -44,9 +44,10 @@ namespace {
 
 // Work units: a quantized tile is one unit, an fp16 chunk kChunkUnits (its
 // dot products run on the CUDA cores in a long dependent chain), and every
-// head has kHeadUnits units that hold no data (they stand for the cost of a
-// head change, so a warp that changes heads gets less data).
-constexpr int kHeadUnits = 1;
+// head starts with kHeadUnits units that hold no data.  They fall to the
+// warp that holds the head's first unit: the warp that changes heads there
+// and merges the head's partials at the end, both costs of about a tile.
+constexpr int kHeadUnits = 2;
 constexpr int kChunkUnits = 2;
 
 // What unit range [x0, x1) holds of head bh: its U units are HU empty ones,
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // z) and the fp16-token state (mf, lf, af: a lane owns channels 4*lane ..
   // 4*lane + 3) are joined with the log-sum-exp rule; the quantized output
   // row goes through the warp's operand area to reach the lane layout.
-  int pend_bh = -1, pend_ticket = 0;  // last published head, lane 0's ticket for it
+  int pend_bh = -1;  // head this warp merges (slot 0), once it has published
   auto flush = [&](int bh, int slot, float mf, float lf, const float (&af)[4]) -> bool {
     float l = l_lane;
 #pragma unroll
@@ -333,10 +334,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     const float lt = fmaf(l, wq, lf * wf);
     reset_state();
     // the previous head's ticket has long arrived: act on it, then publish
-    if (pend_bh >= 0 && !finish_head<8>(a, pend_bh, pend_ticket)) return false;
+    // a merge still owed (a head this warp held whole) comes first; the
+    // merge of the warp's last head waits until after the tile loop
+    if (pend_bh >= 0 && !merge_head<8>(a, pend_bh)) return false;
     publish_partial(a, bh, slot, o, m, lt);
-    pend_ticket = take_ticket(a, bh);
-    pend_bh = bh;
+    pend_bh = slot == 0 ? bh : -1;
     return true;
   };
 
@@ -747,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       break;
     }
   }
-  if (!aborted && pend_bh >= 0 && !finish_head<24>(a, pend_bh, pend_ticket)) aborted = true;
+  if (!aborted && pend_bh >= 0 && !merge_head<24>(a, pend_bh)) aborted = true;
   if (aborted) {
     // give up this warp's work; its copies complete first
     if (lane == 0)
@@ -847,8 +849,6 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.UPC = kChunkUnits;
   a.nch = (int)((a.n_fp16 + CH - 1) / CH);
   a.F_h = a.nch * a.UPC;
-  // a head change costs a warp about one tile's time (its flush, the next
-  // head's query setup): one empty unit per head
   a.HU = kHeadUnits;
   a.U = a.HU + a.S_h + a.F_h;
   const int64_t total = (int64_t)g.B * g.H * a.U;

@@ -242,11 +242,11 @@ __device__ __forceinline__ int head_nparts(const TcArgs &a, int bh) {
 // Partials are stored XOR-ed with kEnc: no float that arithmetic produces
 // (kEnc is a signalling NaN) encodes to 0, so a zero word means "not
 // written yet" and the zero-filled workspace starts empty.  Writers publish
-// without any fence: they store their partial and take a ticket with a
-// relaxed atomic whose result they look at only later.  The warp that took
-// the head's last ticket polls (bounded) until every partial is visible,
-// merges them with the log-sum-exp rule, writes the output row and zeroes
-// the partials and the ticket again.
+// without any fence or atomic.  The head's merger is fixed in advance: the
+// warp in slot 0, whose range holds the head's first unit and so ends in
+// this head (or holds all of it).  After publishing its own partial it polls
+// (bounded) until the others are visible, merges them with the log-sum-exp
+// rule, writes the output row and zeroes the partials again.
 constexpr uint32_t kEnc = 0x7fbadbadu;
 constexpr int kMergePolls = 1 << 22;
 
@@ -255,9 +255,8 @@ __device__ __forceinline__ uint4 enc4(float4 v) {
                     __float_as_uint(v.z) ^ kEnc, __float_as_uint(v.w) ^ kEnc);
 }
 
-// Lane 0's ticket for head bh (a relaxed atomic; read the result later).
-__device__ __forceinline__ int take_ticket(const TcArgs &a, int bh) {
-  return (threadIdx.x & 31) == 0 ? atomicAdd(&a.ws_cnt[bh], 1) : 0;
+__device__ __forceinline__ bool vis4(uint4 v) {
+  return v.x != 0u && v.y != 0u && v.z != 0u && v.w != 0u;
 }
 
 // Stores partial `slot` of head bh: the lane's 4 output channels and (lane 0)
@@ -272,52 +271,46 @@ __device__ __forceinline__ void publish_partial(const TcArgs &a, int bh, int slo
         make_uint2(__float_as_uint(m) ^ kEnc, __float_as_uint(l) ^ kEnc);
 }
 
-// Called by the whole warp with lane 0's ticket for head bh: if it was the
-// head's last, merge.  Returns false if the partials did not all appear
-// within the poll bound (status word set).
-// MB: partial rows fetched in one round of loads on the fast path (the
-// kernel's last call can afford many registers; calls inside the tile loop
-// use few).
+// Run by the whole warp in slot 0 of head bh after it published its own
+// partial (a lane reads back only what it wrote itself there): merges the
+// head's partials and writes the output row.  Returns false if they did not
+// all appear within the poll bound (status word set).
+// MB: partial rows fetched in one round of loads when nparts <= MB (the
+// kernel's last call can afford many registers).
 template <int MB>
-__device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
+__device__ bool merge_head(const TcArgs &a, int bh) {
   const int lane = threadIdx.x & 31;
   const int nparts = head_nparts(a, bh);
-  if (__shfl_sync(0xffffffffu, ticket, 0) != nparts - 1) return true;
   const int64_t base = (int64_t)bh * a.part_stride;
   const uint2 *ml = reinterpret_cast<const uint2 *>(a.ws_ml) + base;
   const uint4 *wo = reinterpret_cast<const uint4 *>(a.ws_o + base * kD);
-  const int b = bh / a.g.H, h = bh % a.g.H;
+  bool ok = true;
+  float Ls = 0.0f, O[4] = {0.f, 0.f, 0.f, 0.f};
   if (nparts <= MB) {
-    // every (m, l) and o row loaded in one round, repeated (bounded) until
-    // all of them are visible
-    uint2 v;
+    // every (m, l) and o row in one round of loads, repeated until all are
+    // visible
+    uint2 v = make_uint2(1u, 1u);
     uint4 o[MB];
     bool all = false;
     for (int it = 0; it < kMergePolls && !all; ++it) {
       if (it > 0) __nanosleep(32);
       v = lane < nparts ? __ldcg(ml + lane) : make_uint2(1u, 1u);
-#pragma unroll
-      for (int j = 0; j < MB; ++j)
-        o[j] = j < nparts ? __ldcg(wo + (int64_t)j * (kD / 4) + lane) : make_uint4(1, 1, 1, 1);
       bool mine = v.x != 0u && v.y != 0u;
 #pragma unroll
-      for (int j = 0; j < MB; ++j) mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
+      for (int j = 0; j < MB; ++j) {
+        o[j] = j < nparts ? __ldcg(wo + (int64_t)j * (kD / 4) + lane) : make_uint4(1, 1, 1, 1);
+        mine = mine && vis4(o[j]);
+      }
       all = __all_sync(0xffffffffu, mine);
     }
-    if (!all) {
-      if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
-      return false;
-    }
-    {
+    ok = all;
+    if (ok) {
       const float ms = lane < nparts ? __uint_as_float(v.x ^ kEnc) : -INFINITY;
       float M = ms;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
       const float w = ms != -INFINITY ? exp2f(ms - M) : 0.0f;
-      float L = w * (lane < nparts ? __uint_as_float(v.y ^ kEnc) : 0.0f);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-      float O[4] = {0.f, 0.f, 0.f, 0.f};
+      Ls = w * (lane < nparts ? __uint_as_float(v.y ^ kEnc) : 0.0f);
 #pragma unroll
       for (int j = 0; j < MB; ++j) {
         const float wj = __shfl_sync(0xffffffffu, w, j & 31);
@@ -328,70 +321,62 @@ __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
           O[3] = fmaf(wj, __uint_as_float(o[j].w ^ kEnc), O[3]);
         }
       }
-      const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-      reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h) * kD)[lane] =
-          make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
-      for (int s = 0; s < nparts; ++s)
-        reinterpret_cast<uint4 *>(a.ws_o + base * kD)[(int64_t)s * (kD / 4) + lane] = make_uint4(0, 0, 0, 0);
-      if (lane < nparts) reinterpret_cast<uint2 *>(a.ws_ml)[base + lane] = make_uint2(0, 0);
-      if (lane == 0) a.ws_cnt[bh] = 0;
-      return true;
     }
-  }
-  // (m, l) of partial s sits in lane s % 32; every load is re-polled
-  // (bounded) until its words are non-zero
-  auto ml_of = [&](int s) -> uint2 {
-    uint2 v = __ldcg(ml + s);
-    for (int it = 0; it < kMergePolls && (v.x == 0u || v.y == 0u); ++it) {
-      __nanosleep(32);
-      v = __ldcg(ml + s);
-    }
-    return v;
-  };
-  bool ok = true;
-  float Mx = -INFINITY;
-  for (int s = lane; s < nparts; s += 32) {
-    const uint2 v = ml_of(s);
-    ok = ok && v.x != 0u && v.y != 0u;
-    Mx = fmaxf(Mx, __uint_as_float(v.x ^ kEnc));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, off));
-  float Ls = 0.0f, O[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int s0 = 0; s0 < nparts && ok; s0 += 32) {
-    float w = 0.0f;
-    if (s0 + lane < nparts) {
-      const uint2 v = __ldcg(ml + s0 + lane);
-      const float ms = __uint_as_float(v.x ^ kEnc);
-      if (ms != -INFINITY) {
-        w = exp2f(ms - Mx);
-        Ls = fmaf(w, __uint_as_float(v.y ^ kEnc), Ls);
+  } else {
+    // (m, l) of partial s sits in lane s % 32; every load is re-polled
+    // (bounded) until its words are non-zero
+    auto ml_of = [&](int s) -> uint2 {
+      uint2 v = __ldcg(ml + s);
+      for (int it = 0; it < kMergePolls && (v.x == 0u || v.y == 0u); ++it) {
+        __nanosleep(32);
+        v = __ldcg(ml + s);
       }
+      return v;
+    };
+    float M = -INFINITY;
+    for (int s = lane; s < nparts; s += 32) {
+      const uint2 v = ml_of(s);
+      ok = ok && v.x != 0u && v.y != 0u;
+      M = fmaxf(M, __uint_as_float(v.x ^ kEnc));
     }
-    const int nb = min(32, nparts - s0);
-    for (int j0 = 0; j0 < nb; j0 += 8) {
-      uint4 o[8];
-      bool ready = false;
-      for (int it = 0; it < kMergePolls && !ready; ++it) {
-        bool mine = true;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    ok = __all_sync(0xffffffffu, ok);
+    for (int s0 = 0; s0 < nparts && ok; s0 += 32) {
+      float w = 0.0f;
+      if (s0 + lane < nparts) {
+        const uint2 v = __ldcg(ml + s0 + lane);
+        const float ms = __uint_as_float(v.x ^ kEnc);
+        if (ms != -INFINITY) {
+          w = exp2f(ms - M);
+          Ls = fmaf(w, __uint_as_float(v.y ^ kEnc), Ls);
+        }
+      }
+      const int nb = min(32, nparts - s0);
+      for (int j0 = 0; j0 < nb; j0 += 8) {
+        uint4 o[8];
+        bool ready = false;
+        for (int it = 0; it < kMergePolls && !ready; ++it) {
+          bool mine = true;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            o[j] = j0 + j < nb ? __ldcg(wo + (int64_t)(s0 + j0 + j) * (kD / 4) + lane)
+                               : make_uint4(1, 1, 1, 1);
+            mine = mine && vis4(o[j]);
+          }
+          ready = __all_sync(0xffffffffu, mine);
+          if (!ready) __nanosleep(32);
+        }
+        ok = ok && ready;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          o[j] = j0 + j < nb ? __ldcg(wo + (int64_t)(s0 + j0 + j) * (kD / 4) + lane)
-                             : make_uint4(1, 1, 1, 1);
-          mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
-        }
-        ready = __all_sync(0xffffffffu, mine);
-        if (!ready) __nanosleep(32);
-      }
-      ok = ok && ready;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
-        if (j0 + j < nb && wj != 0.0f) {
-          O[0] = fmaf(wj, __uint_as_float(o[j].x ^ kEnc), O[0]);
-          O[1] = fmaf(wj, __uint_as_float(o[j].y ^ kEnc), O[1]);
-          O[2] = fmaf(wj, __uint_as_float(o[j].z ^ kEnc), O[2]);
-          O[3] = fmaf(wj, __uint_as_float(o[j].w ^ kEnc), O[3]);
+          const float wj = __shfl_sync(0xffffffffu, w, (j0 + j) & 31);
+          if (j0 + j < nb && wj != 0.0f) {
+            O[0] = fmaf(wj, __uint_as_float(o[j].x ^ kEnc), O[0]);
+            O[1] = fmaf(wj, __uint_as_float(o[j].y ^ kEnc), O[1]);
+            O[2] = fmaf(wj, __uint_as_float(o[j].z ^ kEnc), O[2]);
+            O[3] = fmaf(wj, __uint_as_float(o[j].w ^ kEnc), O[3]);
+          }
         }
       }
     }
@@ -403,17 +388,12 @@ __device__ bool finish_head(const TcArgs &a, int bh, int ticket) {
     return false;
   }
   const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-  float4 r;
-  r.x = O[0] * inv;
-  r.y = O[1] * inv;
-  r.z = O[2] * inv;
-  r.w = O[3] * inv;
-  reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h) * kD)[lane] = r;
-  // leave the workspace as found: partials and ticket zero
+  reinterpret_cast<float4 *>(a.out + ((int64_t)(bh / a.g.H) * a.g.Hq + bh % a.g.H) * kD)[lane] =
+      make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
+  // leave the workspace as found: partials zero
   for (int s = 0; s < nparts; ++s)
     reinterpret_cast<uint4 *>(a.ws_o + base * kD)[(int64_t)s * (kD / 4) + lane] = make_uint4(0, 0, 0, 0);
   for (int s = lane; s < nparts; s += 32) reinterpret_cast<uint2 *>(a.ws_ml)[base + s] = make_uint2(0, 0);
-  if (lane == 0) a.ws_cnt[bh] = 0;
   return true;
 }
 
