@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // ---- producer: this warp's items in the order the consumer visits them:
   // per head, its quantized tiles, then its fp16 chunks.
   int pc_bh = bh_first, pc_ph = 0, pc_lt = 0, pc_n = 0, issued = 0, ps = 0;
+  const uint64_t pol_once = l2_evict_first();  // cache blocks are read once
   Seg pc_seg = warp_seg(a, pc_bh, x0, x1);
   pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
   auto pc_settle = [&]() {
@@ -141,8 +142,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       if (pc_ph == 0) {
         const int tok0 = pc_seg.tq0 + kTile * pc_lt;
         bar_expect_tx(bar, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)));
-        bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
-                 SC::BB, bar);
+        bulk_g2s_hint(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
+                      SC::BB, bar, pol_once);
         if (SCHEME == KVQ_KIVI && !SC::KIN)
           bulk_g2s(dst + SC::off_km,
                    a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
