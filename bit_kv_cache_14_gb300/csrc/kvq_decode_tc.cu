@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   uint8_t *wring = smem + Ly.ring + warp * nslot * SLOT;
   uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
   uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB + warp * SC::SBB);
+  const uint32_t wring_s = smem_u32(wring), wbars_s = smem_u32(wbars);  // shared-window addresses
 
   // Warp-level stream-K: warp gw of the grid owns units [x0, x1) of the
   // concatenated per-head unit lists (units of one tile or fp16 chunk).
@@ -136,45 +137,48 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     const bool first = pc_lt == 0;
     uint8_t *dst = wring + ps * SLOT;
     uint64_t *bar = &wbars[ps];
+    const uint32_t dst_s = wring_s + ps * SLOT, bar_s = wbars_s + 8 * ps;
     ps = ps + 1 == nslot ? 0 : ps + 1;
-    if (lane == 0) {
+    if (pc_ph == 0) {
+      // a cache block: the common case, issued without a branch on the lane
+      const int tok0 = pc_seg.tq0 + kTile * pc_lt;
+      bulk_g2s_pred(lane == 0, bar_s, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)), dst_s,
+                    a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB, SC::BB,
+                    pol_once);
+      if (SCHEME == KVQ_KIVI && !SC::KIN && lane == 0)
+        bulk_g2s(dst + SC::off_km,
+                 a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
+                 SC::KMB, bar);
+      if (first && lane == 0)
+        bulk_g2s(dst + SC::off_q, a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD, kD * 2,
+                 bar);
+    } else if (lane == 0) {
       const __half *qrow = a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD;
-      if (pc_ph == 0) {
-        const int tok0 = pc_seg.tq0 + kTile * pc_lt;
-        bar_expect_tx(bar, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)));
-        bulk_g2s_hint(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB,
-                      SC::BB, bar, pol_once);
-        if (SCHEME == KVQ_KIVI && !SC::KIN)
-          bulk_g2s(dst + SC::off_km,
-                   a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
-                   SC::KMB, bar);
-      } else {
-        const int ns = (int)a.n_sink;
-        const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
-        const int s0 = min(i0, ns), s1 = min(i1, ns);            // sink rows
-        const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;  // residual / window rows
-        bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2 + (first ? kD * 2 : 0)));
-        if (s1 > s0) {
-          const int64_t row = (int64_t)pc_bh * g.n_sink + s0;
-          bulk_g2s(dst, a.p.k_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
-          bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+      const int ns = (int)a.n_sink;
+      const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
+      const int s0 = min(i0, ns), s1 = min(i1, ns);            // sink rows
+      const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;  // residual / window rows
+      bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2 + (first ? kD * 2 : 0)));
+      if (s1 > s0) {
+        const int64_t row = (int64_t)pc_bh * g.n_sink + s0;
+        bulk_g2s(dst, a.p.k_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+        bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+      }
+      if (r1 > r0) {
+        // a fused append's new row is not in the residual yet: it comes from
+        // the step's input rows
+        const int rn = (a.new_row >= 0 && r1 - 1 == a.new_row) ? r1 - 1 : r1;
+        const int64_t row = (int64_t)pc_bh * g.residual + r0;
+        const int o = (s1 - s0) * kD * 2;
+        if (rn > r0) {
+          bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((rn - r0) * kD * 2), bar);
+          bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD,
+                   (uint32_t)((rn - r0) * kD * 2), bar);
         }
-        if (r1 > r0) {
-          // a fused append's new row is not in the residual yet: it comes from
-          // the step's input rows
-          const int rn = (a.new_row >= 0 && r1 - 1 == a.new_row) ? r1 - 1 : r1;
-          const int64_t row = (int64_t)pc_bh * g.residual + r0;
-          const int o = (s1 - s0) * kD * 2;
-          if (rn > r0) {
-            bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((rn - r0) * kD * 2), bar);
-            bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD,
-                     (uint32_t)((rn - r0) * kD * 2), bar);
-          }
-          if (rn < r1) {
-            const int on = o + (rn - r0) * kD * 2;
-            bulk_g2s(dst + on, a.k_new + (int64_t)pc_bh * kD, kD * 2, bar);
-            bulk_g2s(dst + CH * kD * 2 + on, a.v_new + (int64_t)pc_bh * kD, kD * 2, bar);
-          }
+        if (rn < r1) {
+          const int on = o + (rn - r0) * kD * 2;
+          bulk_g2s(dst + on, a.k_new + (int64_t)pc_bh * kD, kD * 2, bar);
+          bulk_g2s(dst + CH * kD * 2 + on, a.v_new + (int64_t)pc_bh * kD, kD * 2, bar);
         }
       }
       if (first) bulk_g2s(dst + SC::off_q, qrow, kD * 2, bar);
@@ -359,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     bool ok = true;
     if (first && a.stall_limit > 0) ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
     first = false;
-    if (ok) ok = bar_wait(&wbars[s], par, a.wait_limit);
+    if (ok) ok = bar_wait(wbars_s + 8 * s, par, a.wait_limit);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
       return false;

@@ -116,23 +116,28 @@ __device__ __forceinline__ void bar_expect_tx(uint64_t *bar, uint32_t bytes) {
                : "memory");
 }
 
-__device__ __forceinline__ bool bar_try_wait(uint64_t *bar, uint32_t parity) {
+// Barrier waits on a shared-window address (bar_s) or a pointer.
+__device__ __forceinline__ bool bar_try_wait(uint32_t bar_s, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(bar_s), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
 // Bounded wait for the phase with the given parity; false on timeout.
-__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, int limit) {
-  if (bar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool bar_wait(uint32_t bar_s, uint32_t parity, int limit) {
+  if (bar_try_wait(bar_s, parity)) return true;
   for (int it = 0; it < limit; ++it)
-    if (bar_try_wait(bar, parity)) return true;
+    if (bar_try_wait(bar_s, parity)) return true;
   return false;
+}
+
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, int limit) {
+  return bar_wait(smem_u32(bar), parity, limit);
 }
 
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
@@ -152,13 +157,17 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   return pol;
 }
 
-// bulk_g2s with an L2 cache policy.
-__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes,
-                                              uint64_t *bar, uint64_t pol) {
+// Predicated on `on` (one lane), without a branch: posts tx expected bytes on
+// the barrier at bar_s and copies `bytes` from src to dst_s (shared-window
+// addresses) with L2 policy pol.
+__device__ __forceinline__ void bulk_g2s_pred(bool on, uint32_t bar_s, uint32_t tx, uint32_t dst_s,
+                                              const void *src, uint32_t bytes, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
-      "%2, [%3], %4;" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      "{\n .reg .pred p;\n setp.ne.b32 p, %0, 0;\n"
+      " @p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%1], %2;\n"
+      " @p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%3], "
+      "[%4], %5, [%1], %6;\n}\n" ::"r"((int)on),
+      "r"(bar_s), "r"(tx), "r"(dst_s), "l"(src), "r"(bytes), "l"(pol)
       : "memory");
 }
 
