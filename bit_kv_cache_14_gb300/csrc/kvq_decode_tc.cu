@@ -193,29 +193,30 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // ---- per-head constants (each warp for itself) --------------------------
   float pow2E = 1.0f;  // scores = raw * 2^(E+24) (q normalised by 2^-E, codes by 2^-24)
   float q4[4];         // q of channels 4*lane .. 4*lane+3 (exp2 domain)
-  // KIVI key operand: this lane builds channel pairs ip = lane and lane + 32
+  // KIVI key operand: this lane builds the channel pairs (c, c + kHalf) of
+  // c = b_clo and c = b_clo + 1 (even positions p and p + 1 of word W), whose
+  // B-fragment words sit next to each other at b_sidx, b_sidx + 1
   constexpr int kHalf = BITS == 2 ? 8 : 4;  // channel offset of the high half of a pair
-  int b_clo[2], b_sidx[2];
+  int b_clo, b_sidx;
   float qn_lo[2], qn_hi[2], qf_lo[2], qf_hi[2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int ip = lane + 32 * r;
+  {
     int W, p, tg, kb;
     if (BITS == 2) {
-      W = ip >> 3;
-      p = ip & 7;
-      b_clo[r] = 16 * W + p;
+      W = lane >> 2;
+      p = 2 * (lane & 3);
+      b_clo = 16 * W + p;
       tg = W >> 1;
       kb = 4 * (W & 1) + (p >> 1);
     } else {
-      W = ip >> 2;
-      p = ip & 3;
-      b_clo[r] = 8 * W + p;
+      W = lane >> 1;
+      p = 2 * (lane & 1);
+      b_clo = 8 * W + p;
       tg = W >> 2;
       kb = 2 * (W & 3) + (p >> 1);
     }
-    b_sidx[r] = tg * 16 + kb * 2 + (p & 1);
-    qn_lo[r] = qn_hi[r] = qf_lo[r] = qf_hi[r] = 0.0f;
+    b_sidx = tg * 16 + kb * 2;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) qn_lo[r] = qn_hi[r] = qf_lo[r] = qf_hi[r] = 0.0f;
   }
   // InnerQ: fixed key operand and per-group sums of q
   uint32_t bqi[8][2];
@@ -243,10 +244,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     if (SCHEME == KVQ_KIVI) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int p = BITS == 2 ? (b_clo[r] & 7) : (b_clo[r] & 3);
-        const float invf = inv / pos_factor<BITS>(p);
-        qf_lo[r] = qf(b_clo[r]);
-        qf_hi[r] = qf(b_clo[r] + kHalf);
+        const int c = b_clo + r;
+        const int p = BITS == 2 ? (c & 7) : (c & 3);
+        const float invf = inv * inv_pos_factor<BITS>(p);
+        qf_lo[r] = qf(c);
+        qf_hi[r] = qf(c + kHalf);
         qn_lo[r] = qf_lo[r] * invf;
         qn_hi[r] = qf_hi[r] * invf;
       }
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         for (int r = 0; r < 2; ++r) {
           int clo, chi, p;
           key_pair<BITS>(tig, kb, r, clo, chi, p);
-          const float invf = inv / pos_factor<BITS>(p);
+          const float invf = inv * inv_pos_factor<BITS>(p);
           const float vlo = (clo / GK == jn) ? qf(clo) * invf : 0.0f;
           const float vhi = (chi / GK == jn) ? qf(chi) * invf : 0.0f;
           uint32_t hi, lo;
@@ -419,16 +421,16 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
               if (gl == 1 && !two_groups) break;
               const float *ks = km + gl * 2 * kD, *kz = ks + kD;
-              float bz = 0.0f;
-  #pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                const int clo = b_clo[r], chi = b_clo[r] + kHalf;
-                uint32_t hi, lo;
-                split2(qn_lo[r] * ks[clo], qn_hi[r] * ks[chi], hi, lo);
-                sBw[gl * 128 + b_sidx[r]] = hi;
-                sBw[gl * 128 + 64 + b_sidx[r]] = lo;
-                bz = fmaf(qf_lo[r], kz[clo], fmaf(qf_hi[r], kz[chi], bz));
-              }
+              const float2 s_lo = *reinterpret_cast<const float2 *>(ks + b_clo);
+              const float2 s_hi = *reinterpret_cast<const float2 *>(ks + b_clo + kHalf);
+              const float2 z_lo = *reinterpret_cast<const float2 *>(kz + b_clo);
+              const float2 z_hi = *reinterpret_cast<const float2 *>(kz + b_clo + kHalf);
+              uint32_t h0, l0, h1, l1;
+              split2(qn_lo[0] * s_lo.x, qn_hi[0] * s_hi.x, h0, l0);
+              split2(qn_lo[1] * s_lo.y, qn_hi[1] * s_hi.y, h1, l1);
+              *reinterpret_cast<uint2 *>(sBw + gl * 128 + b_sidx) = make_uint2(h0, h1);
+              *reinterpret_cast<uint2 *>(sBw + gl * 128 + 64 + b_sidx) = make_uint2(l0, l1);
+              float bz = fmaf(qf_lo[0], z_lo.x, fmaf(qf_hi[0], z_hi.x, fmaf(qf_lo[1], z_lo.y, qf_hi[1] * z_hi.y)));
   #pragma unroll
               for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
               if (gl == 0) bias0 = bz;

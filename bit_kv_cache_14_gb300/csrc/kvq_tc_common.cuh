@@ -194,6 +194,13 @@ __host__ __device__ __forceinline__ float pos_factor(int p) {
   return (p & 1) ? 16.0f : 1.0f;
 }
 
+// 1 / pos_factor(p), exact (a power of two).
+template <int BITS>
+__device__ __forceinline__ float inv_pos_factor(int p) {
+  const int e = BITS == 2 ? 2 * (p <= 4 ? p : p - 5) : ((p & 1) ? 4 : 0);
+  return __int_as_float((127 - e) << 23);
+}
+
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm(
