@@ -582,25 +582,46 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
               z_lane[j] = (FULL || p > 0.0f) ? fmaf(p, zr[j], z_lane[j]) : z_lane[j];
           }
           // ------------- values: B = p * scale (hi/lo), A = codes ------------
-          const float *vs = reinterpret_cast<const float *>(slot + SC::off_vs);
-          const int jg = (gid >> 1) < NGV ? (gid >> 1) : NGV - 1;
+          // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) of k-block kb carry
+          // tokens 16kb + tig + {0, 4} and + {8, 12} (code rows 4 apart hit
+          // distinct banks).  Each token's lane writes its operand row
+          // B[t][(j, hi/lo)] = p_t * scale_tj * 2^-8 as fp16 hi + lo into the
+          // warp's operand area (the key operand is consumed by now), laid out
+          // [column][kb][tig][4 tokens] so each lane then loads the fragment of
+          // a k-block with one 64-bit load.
+          {
+            const float *vsr = reinterpret_cast<const float *>(slot + SC::off_vs) + t * NGV;
+            float sv[NGV];
+            if (NGV == 4) {
+              const float4 s4 = *reinterpret_cast<const float4 *>(vsr);
+              sv[0] = s4.x;
+              sv[1] = s4.y;
+              sv[2 % NGV] = s4.z;
+              sv[3 % NGV] = s4.w;
+            } else {
+              const float2 s2 = *reinterpret_cast<const float2 *>(vsr);
+              sv[0] = s2.x;
+              sv[1 % NGV] = s2.y;
+            }
+            __syncwarp();  // every lane's key-operand loads are done
+            __half *orow = reinterpret_cast<__half *>(sBw) + 16 * (t >> 4) + 4 * (t & 3) + ((t & 15) >> 2);
+  #pragma unroll
+            for (int j = 0; j < NGV; ++j) {
+              const float x = valid ? pv * sv[j] : 0.0f;
+              const __half h = __float2half_rn(x);
+              orow[64 * j] = h;
+              orow[64 * j + 32] = __float2half_rn(x - __half2float(h));
+            }
+            __syncwarp();
+          }
           const bool bact = gid < 2 * NGV;
+          const uint32_t *bsrc = sBw + 16 * gid + 2 * tig;
           const int nkb = (FULL || n > 16) ? 2 : 1;
           for (int kb = 0; kb < nkb; ++kb) {
-            // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) carry tokens
-            // tig + {0, 4} and tig + {8, 12}: rows 4 apart hit distinct banks
             const int tk0 = 16 * kb + tig, tk1 = tk0 + 4, tk2 = tk0 + 8, tk3 = tk0 + 12;
-            const float p0 = __shfl_sync(0xffffffffu, pv, tk0), p1 = __shfl_sync(0xffffffffu, pv, tk1);
-            const float p2 = __shfl_sync(0xffffffffu, pv, tk2), p3 = __shfl_sync(0xffffffffu, pv, tk3);
-            const float x0 = (FULL || p0 > 0.0f) ? p0 * vs[tk0 * NGV + jg] : 0.0f;
-            const float x1 = (FULL || p1 > 0.0f) ? p1 * vs[tk1 * NGV + jg] : 0.0f;
-            const float x2 = (FULL || p2 > 0.0f) ? p2 * vs[tk2 * NGV + jg] : 0.0f;
-            const float x3 = (FULL || p3 > 0.0f) ? p3 * vs[tk3 * NGV + jg] : 0.0f;
-            uint32_t h01, l01, h23, l23;
-            split2(x0, x1, h01, l01);
-            split2(x2, x3, h23, l23);
-            const uint32_t bv0 = bact ? ((gid & 1) ? l01 : h01) : 0u;
-            const uint32_t bv1 = bact ? ((gid & 1) ? l23 : h23) : 0u;
+            const uint2 bw = *reinterpret_cast<const uint2 *>(bsrc + 8 * kb);
+            const uint32_t bv0 = bact ? bw.x : 0u;
+            const uint32_t bv1 = bact ? bw.y : 0u;
             if (BITS == 2) {
               const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * gid);
               const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * gid);
