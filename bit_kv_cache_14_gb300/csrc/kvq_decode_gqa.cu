@@ -209,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
   // ---- producer: per head, quantized tiles lt = warp, warp + 8, ..., then
   // fp16 chunks lt = warp, warp + 8, ... of this block's segments
   int pc_bh = bh_first, pc_ph = 0, pc_lt = warp, pc_n = 0, issued = 0, ps = 0;
+  const uint64_t pol_once = l2_evict_first();  // cache blocks are read once
+  const uint32_t wring_s = smem_u32(wring), wbars_s = smem_u32(wbars);
   Seg pc_seg = seg_in(a, pc_bh, x0, x1);
   pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
   auto pc_settle = [&]() {
@@ -232,35 +234,36 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
     if (pc_bh < 0) return;
     uint8_t *dst = wring + ps * SLOT;
     uint64_t *bar = &wbars[ps];
+    const uint32_t dst_s = wring_s + ps * SLOT, bar_s = wbars_s + 8 * ps;
     ps = ps + 1 == nslot ? 0 : ps + 1;
-    if (lane == 0) {
-      if (pc_ph == 0) {
-        const int tok0 = pc_seg.tq0 + kTile * pc_lt;
-        bar_expect_tx(bar, (uint32_t)(C::BB + C::KMB));
-        bulk_g2s(dst, a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * C::BB,
-                 C::BB, bar);
-        if constexpr (!C::KIN)
+    if (pc_ph == 0) {
+      // a cache block: posted by one lane without a branch
+      const int tok0 = pc_seg.tq0 + kTile * pc_lt;
+      bulk_g2s_pred(lane == 0, bar_s, (uint32_t)(C::BB + C::KMB), dst_s,
+                    a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * C::BB, C::BB,
+                    pol_once);
+      if constexpr (!C::KIN)
+        if (lane == 0)
           bulk_g2s(dst + C::off_km,
                    a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
                    C::KMB, bar);
-      } else {
-        const int ns = (int)a.n_sink;
-        const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
-        const int s0 = min(i0, ns), s1 = min(i1, ns);
-        const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;
-        bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2));
-        if (s1 > s0) {
-          const int64_t row = (int64_t)pc_bh * g.n_sink + s0;
-          bulk_g2s(dst, a.p.k_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
-          bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
-        }
-        if (r1 > r0) {
-          const int64_t row = (int64_t)pc_bh * g.residual + r0;
-          const int o = (s1 - s0) * kD * 2;
-          bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((r1 - r0) * kD * 2), bar);
-          bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD, (uint32_t)((r1 - r0) * kD * 2),
-                   bar);
-        }
+    } else if (lane == 0) {
+      const int ns = (int)a.n_sink;
+      const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
+      const int s0 = min(i0, ns), s1 = min(i1, ns);
+      const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;
+      bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2));
+      if (s1 > s0) {
+        const int64_t row = (int64_t)pc_bh * g.n_sink + s0;
+        bulk_g2s(dst, a.p.k_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+        bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
+      }
+      if (r1 > r0) {
+        const int64_t row = (int64_t)pc_bh * g.residual + r0;
+        const int o = (s1 - s0) * kD * 2;
+        bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((r1 - r0) * kD * 2), bar);
+        bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD, (uint32_t)((r1 - r0) * kD * 2),
+                 bar);
       }
     }
     ++issued;
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
     bool ok = true;
     if (first && a.stall_limit > 0) ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
     first = false;
-    if (ok) ok = bar_wait(&wbars[cs], cph, a.wait_limit);
+    if (ok) ok = bar_wait(wbars_s + 8 * cs, cph, a.wait_limit);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
       return false;
