@@ -550,31 +550,45 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
           }
         }
         // ---- values: per value group j, its 16-row tiles and columns (r, hi/lo)
+        // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) of k-block kb carry
+        // tokens 16kb + tig + {0, 8} and + {4, 12}.  The operand B[t][(r,
+        // hi/lo)] = p_tr * scale_tj * 2^-8 is written once, by the lane that
+        // holds p_tr (head tig, tokens gid + 8i): a token pair (t, t + 8) of one
+        // column is one 32-bit word, at [j][kb][column][tig'][2 words] in the
+        // warp's operand area (the key operand is consumed by now); each lane
+        // then loads its fragment of (kb, j) with one 64-bit load.
         {
           const float *vs = reinterpret_cast<const float *>(slot + C::off_vs);
-          const int r = gid >> 1;
-          const bool bact = r < RG;
-          const int src0 = 4 * tig + (bact ? r : 0), src1 = 4 * (tig + 4) + (bact ? r : 0);
+          const int wofs = 2 * (gid & 3) + (gid >> 2);  // word of token pair (gid, gid + 8)
+          __syncwarp();  // every lane's key-operand loads are done
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const float pa = pv[2 * kb], pb = pv[2 * kb + 1];
+            const float *sa = vs + (gid + 16 * kb) * NGV, *sb = sa + 8 * NGV;
+#pragma unroll
+            for (int j = 0; j < NGV; ++j) {
+              const float xa = pa > 0.0f ? pa * sa[j] : 0.0f;
+              const float xb = pb > 0.0f ? pb * sb[j] : 0.0f;
+              uint32_t h, l;
+              split2(xa, xb, h, l);
+              uint32_t *cell = sBw + ((j * 2 + kb) * 8 + 2 * tig) * 8 + wofs;
+              cell[0] = h;
+              cell[8] = l;
+            }
+          }
+          __syncwarp();
+        }
+        {
+          const bool bact = gid < 2 * RG;
           const int sh = 2 * (gid / WPG);  // this lane's code position offset
           const int nkb = n > 16 ? 2 : 1;
           for (int kb = 0; kb < nkb; ++kb) {
-            const int tk0 = 16 * kb + tig, tk1 = tk0 + 4, tk2 = tk0 + 8, tk3 = tk0 + 12;
-            const float plo = kb ? pv[2] : pv[0], phi = kb ? pv[3] : pv[1];
-            const float p0 = __shfl_sync(0xffffffffu, plo, src0);
-            const float p1 = __shfl_sync(0xffffffffu, plo, src1);
-            const float p2 = __shfl_sync(0xffffffffu, phi, src0);
-            const float p3 = __shfl_sync(0xffffffffu, phi, src1);
+            const int tk0 = 16 * kb + tig, tk1 = tk0 + 8, tk2 = tk0 + 4, tk3 = tk0 + 12;
 #pragma unroll
             for (int j = 0; j < NGV; ++j) {
-              const float x0 = p0 > 0.0f ? p0 * vs[tk0 * NGV + j] : 0.0f;
-              const float x1 = p1 > 0.0f ? p1 * vs[tk1 * NGV + j] : 0.0f;
-              const float x2 = p2 > 0.0f ? p2 * vs[tk2 * NGV + j] : 0.0f;
-              const float x3 = p3 > 0.0f ? p3 * vs[tk3 * NGV + j] : 0.0f;
-              uint32_t h01, l01, h23, l23;
-              split2(x0, x1, h01, l01);
-              split2(x2, x3, h23, l23);
-              const uint32_t bv0 = bact ? ((gid & 1) ? l01 : h01) : 0u;
-              const uint32_t bv1 = bact ? ((gid & 1) ? l23 : h23) : 0u;
+              const uint2 bw = *reinterpret_cast<const uint2 *>(sBw + ((j * 2 + kb) * 8 + gid) * 8 + 2 * tig);
+              const uint32_t bv0 = bact ? bw.x : 0u;
+              const uint32_t bv1 = bact ? bw.y : 0u;
               const int W = j * WPG + gid % WPG;
               const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * W);
               const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * W);
