@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
           const int clo = b_clo[m], chi = clo + 8;
-          const float ipf = 1.0f / pos_factor<2>(clo & 7);
+          const float ipf = inv_pos_factor<2>(clo & 7);
           const float slo = ks[clo] * ipf, shi = ks[chi] * ipf;
           const float zlo = kz[clo], zhi = kz[chi];
           const float4 ql = reinterpret_cast<const float4 *>(QT)[clo];
