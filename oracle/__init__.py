@@ -202,6 +202,20 @@ class OracleHead:
                    w.n_sink, cap)
 
     # counters
+    def save_state(self):
+        """The counters and fp16 residual/window rows (enough to rewind appends:
+        the rows they overwrite are rewritten in the same order)."""
+        s = self._s
+        return ((s.n_quant, s.n_resid, s.n_sink_used, s.n_flush),
+                self.k_res.copy(), self.v_res.copy())
+
+    def load_state(self, state) -> None:
+        (nq, nr, ns, nf), kr, vr = state
+        s = self._s
+        s.n_quant, s.n_resid, s.n_sink_used, s.n_flush = nq, nr, ns, nf
+        self.k_res[...] = kr
+        self.v_res[...] = vr
+
     n_quant = property(lambda self: self._s.n_quant)
     n_resid = property(lambda self: self._s.n_resid)
     n_sink_used = property(lambda self: self._s.n_sink_used)
