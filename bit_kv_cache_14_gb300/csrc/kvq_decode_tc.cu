@@ -673,6 +673,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     // range holds only a head's empty unit still publishes (an empty
     // partial): the head's partial count includes every warp it touches.
     float mf = -INFINITY, lf = 0.0f, af[4] = {0.f, 0.f, 0.f, 0.f};
+    float pow2F = 1.0f;  // fp16 scores = MMA result * 2^F (q normalised by 2^-F)
     {
       for (int lt = 0; lt < nchk; ++lt) {
         int s;
@@ -689,6 +690,24 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           q4[1] = q01.y * a.scale_log2;
           q4[2] = q23.x * a.scale_log2;
           q4[3] = q23.y * a.scale_log2;
+          // key-score operand of the fp16 rows: q / 2^F as fp16 hi/lo.  With
+          // channels 16kb + 4tig .. + 3 on k-pairs (2tig, 2tig+1), (2tig+8,
+          // 2tig+9) of k-block kb, lane L's own 4 channels are the B words of
+          // (kb, tig) = (L >> 2, L & 3).
+          float mx = fmaxf(fmaxf(fabsf(q4[0]), fabsf(q4[1])), fmaxf(fabsf(q4[2]), fabsf(q4[3])));
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+          int F = 0;
+          if (mx > 0.0f && mx < INFINITY) frexpf(mx, &F);
+          pow2F = ldexpf(1.0f, F);
+          const float inv = ldexpf(1.0f, -F);
+          uint32_t h0, l0, h1, l1;
+          split2(q4[0] * inv, q4[1] * inv, h0, l0);
+          split2(q4[2] * inv, q4[3] * inv, h1, l1);
+          __syncwarp();  // the quantized tiles' operand loads are done
+          *reinterpret_cast<uint2 *>(sBw + (lane & 3) * 16 + 2 * (lane >> 2)) = make_uint2(h0, h1);
+          *reinterpret_cast<uint2 *>(sBw + (4 + (lane & 3)) * 16 + 2 * (lane >> 2)) = make_uint2(l0, l1);
+          __syncwarp();
         }
         const int i0 = (sg.c0 + lt) * CH;
         const int nv = min(CH, (int)a.n_fp16 - i0);  // valid rows of the chunk
@@ -702,42 +721,25 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             reinterpret_cast<uint4 *>(dstrow)[j] = v4;
           }
         }
-        const uint2 *kr = reinterpret_cast<const uint2 *>(slot);
         const uint2 *vr = reinterpret_cast<const uint2 *>(slot + CH * kD * 2);
-        // partial dot products of the lane's 4 channels, then a reduce-scatter:
-        // after it lane L holds the score of row (L >> 2) & 7 of the chunk
-        float sp[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          sp[t] = 0.0f;
-          if (t < CH && t < nv) {
-            const uint2 kw = kr[t * (kD / 4) + lane];
-            const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
-            const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
-            sp[t] = fmaf(q4[0], k01.x, fmaf(q4[1], k01.y, fmaf(q4[2], k23.x, q4[3] * k23.y)));
-          }
-        }
+        // scores on the tensor cores: A = the chunk's K rows (token rows 0..7;
+        // rows 8..15 zero), B = the query operand; rows past the chunk's valid
+        // ones are masked below.  Lane (gid, 0) ends with token gid's score.
+        float sp;
         {
-          const bool h4 = lane & 16;
+          const uint2 *ka = reinterpret_cast<const uint2 *>(slot + gid * kD * 2) + tig;
+          const uint32_t *bq = gid < 2 ? sBw + (gid * 4 + tig) * 16 : sBw + SC::sb_zero;
+          float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float mine = h4 ? sp[j + 4] : sp[j], other = h4 ? sp[j] : sp[j + 4];
-            sp[j] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
+          for (int kb = 0; kb < 8; ++kb) {
+            const uint2 av = ka[4 * kb];
+            const uint2 bv = *reinterpret_cast<const uint2 *>(bq + 2 * kb);
+            mma16816((kb & 1) ? e1 : e0, av.x, 0u, av.y, 0u, bv.x, bv.y);
           }
-          const bool h3 = lane & 8;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const float mine = h3 ? sp[j + 2] : sp[j], other = h3 ? sp[j] : sp[j + 2];
-            sp[j] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
-          }
-          const bool h2 = lane & 4;
-          const float mine = h2 ? sp[1] : sp[0], other = h2 ? sp[0] : sp[1];
-          sp[0] = mine + __shfl_xor_sync(0xffffffffu, other, 4);
-          sp[0] += __shfl_xor_sync(0xffffffffu, sp[0], 2);
-          sp[0] += __shfl_xor_sync(0xffffffffu, sp[0], 1);
+          sp = __shfl_sync(0xffffffffu, (e0[0] + e0[1]) + (e1[0] + e1[1]), lane & ~3) * pow2F;
         }
-        const int row = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-        const float sc = row < nv ? sp[0] : -INFINITY;
+        const int row = gid;
+        const float sc = row < nv ? sp : -INFINITY;
         float mc = sc;
         mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 4));
         mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 8));
