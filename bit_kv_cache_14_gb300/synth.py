@@ -58,6 +58,7 @@ class Workload:
     k_offset_sigma: float = 0.0    # per-(head, channel) key offset ~ N(0, sigma)
     data_scale: float = 1.0          # multiplier on every key and value
     first_token_k_mult: float = 1.0
+    k_norm: bool = False             # InnerQ: one-shot per-channel key normalization
 
     @property
     def group_ratio(self) -> int:

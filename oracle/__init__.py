@@ -51,7 +51,7 @@ class _Head(ctypes.Structure):
     _fields_ = [
         ("d", ctypes.c_int32), ("bits", ctypes.c_int32), ("scheme", ctypes.c_int32),
         ("k_group", ctypes.c_int32), ("v_group", ctypes.c_int32),
-        ("residual", ctypes.c_int32), ("n_sink", ctypes.c_int32), ("pad_", ctypes.c_int32),
+        ("residual", ctypes.c_int32), ("n_sink", ctypes.c_int32), ("k_normalize", ctypes.c_int32),
         ("cap", ctypes.c_int64), ("n_quant", ctypes.c_int64), ("n_resid", ctypes.c_int64),
         ("n_sink_used", ctypes.c_int64), ("n_flush", ctypes.c_int64),
         ("k_u", ctypes.c_void_p), ("v_u", ctypes.c_void_p),
@@ -60,6 +60,7 @@ class _Head(ctypes.Structure):
         ("k_sym", ctypes.c_void_p), ("v_sym", ctypes.c_void_p),
         ("k_res", ctypes.c_void_p), ("v_res", ctypes.c_void_p),
         ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p),
+        ("k_norm", ctypes.c_void_p),
     ]
 
 
@@ -164,9 +165,11 @@ def pack_modes(sym: np.ndarray, n_words: int | None = None) -> np.ndarray:
 class OracleHead:
     """Cache state of one head, driven through the C oracle."""
 
-    def __init__(self, d, bits, scheme, k_group, v_group, residual, n_sink, cap):
+    def __init__(self, d, bits, scheme, k_group, v_group, residual, n_sink, cap, k_norm=False):
         if d > 256 or bits not in (2, 4, 8) or d % (8 // bits):
             raise ValueError("unsupported head_dim / bits")
+        if k_norm and scheme != INNERQ:
+            raise ValueError("key normalization is an InnerQ option")
         self.d, self.bits, self.scheme = d, bits, scheme
         self.k_group, self.v_group = k_group, v_group
         self.residual, self.n_sink, self.cap = residual, n_sink, cap
@@ -186,12 +189,14 @@ class OracleHead:
         self.v_res = np.zeros((max(residual, 1), d), np.uint16)
         self.k_sink = np.zeros((max(n_sink, 1), d), np.uint16)
         self.v_sink = np.zeros((max(n_sink, 1), d), np.uint16)
+        self.k_norm = np.ones(d, np.float32)  # per-channel key factors (InnerQ option)
         s = _Head()
         s.d, s.bits, s.scheme = d, bits, scheme
         s.k_group, s.v_group, s.residual, s.n_sink = k_group, v_group, residual, n_sink
         s.cap = cap
+        s.k_normalize = 1 if k_norm else 0
         for name in ("k_u", "v_u", "k_scale", "k_zero", "v_scale", "v_zero", "k_sym",
-                     "v_sym", "k_res", "v_res", "k_sink", "v_sink"):
+                     "v_sym", "k_res", "v_res", "k_sink", "v_sink", "k_norm"):
             setattr(s, name, _ptr(getattr(self, name)))
         self._s = s
 
@@ -199,7 +204,7 @@ class OracleHead:
     def for_workload(cls, w, cap=None):
         cap = w.max_ctx() if cap is None else cap
         return cls(w.head_dim, w.bits, w.scheme, w.k_group, w.v_group, w.residual,
-                   w.n_sink, cap)
+                   w.n_sink, cap, k_norm=getattr(w, "k_norm", False))
 
     # counters
     def save_state(self):
@@ -253,6 +258,10 @@ class OracleHead:
         """(scale, zero) of the quantized keys: KIVI [n_quant/G][d], InnerQ [n_quant][d/G]."""
         rows = self.n_quant // self.k_group if self.scheme == KIVI else self.n_quant
         return self.k_scale[:rows], self.k_zero[:rows]
+
+    def key_norms(self) -> np.ndarray:
+        """Per-channel key factors of the one-shot normalization ([d] fp32)."""
+        return self.k_norm.copy()
 
     def v_meta(self):
         return self.v_scale[: self.n_quant], self.v_zero[: self.n_quant]

@@ -139,14 +139,22 @@ static void kivi_quant_value_token(orc_head *s, const uint16_t *src, int64_t t) 
 /* ---- InnerQ ----------------------------------------------------------- */
 
 /* One token, groups of `group` consecutive channels along the inner (head)
- * dimension, each group symmetric or asymmetric ([INNERQ] 方法论 1-2). */
+ * dimension, each group symmetric or asymmetric ([INNERQ] 方法论 1-2).  With
+ * `norm` (keys under the one-shot normalization) channel c is first scaled
+ * by 1 / norm[c]: the fp32 reciprocal, then one fp32 product. */
 static void innerq_quant_token(const orc_head *s, const uint16_t *src, int group,
                                int64_t t, uint8_t *u, float *scale, float *zero,
-                               uint8_t *sym) {
+                               uint8_t *sym, const float *norm) {
   const int d = s->d, ng = d / group;
   float x[256];
   for (int j = 0; j < ng; ++j) {
-    for (int i = 0; i < group; ++i) x[i] = orc_half_to_float(src[j * group + i]);
+    for (int i = 0; i < group; ++i) {
+      x[i] = orc_half_to_float(src[j * group + i]);
+      if (norm) {
+        const float r = 1.0f / norm[j * group + i];
+        x[i] = x[i] * r;
+      }
+    }
     float mn, mx;
     min_max(x, group, &mn, &mx);
     const int is_sym = orc_choose_symmetric(mn, mx, s->bits);
@@ -161,8 +169,26 @@ static void innerq_quant_token(const orc_head *s, const uint16_t *src, int group
 }
 
 static void innerq_quant_kv(orc_head *s, const uint16_t *k, const uint16_t *v, int64_t t) {
-  innerq_quant_token(s, k, s->k_group, t, s->k_u, s->k_scale, s->k_zero, s->k_sym);
-  innerq_quant_token(s, v, s->v_group, t, s->v_u, s->v_scale, s->v_zero, s->v_sym);
+  innerq_quant_token(s, k, s->k_group, t, s->k_u, s->k_scale, s->k_zero, s->k_sym,
+                     s->k_normalize ? s->k_norm : 0);
+  innerq_quant_token(s, v, s->v_group, t, s->v_u, s->v_scale, s->v_zero, s->v_sym, 0);
+}
+
+/* One-shot per-channel key normalization ([INNERQ] 关键贡献, 方法论 4): the
+ * prompt's keys are scaled once per channel and the factor is folded into
+ * the query.  The pages fix no statistic; the factor of channel c is the
+ * largest |K[t][c]| over the T prompt tokens (sinks and window included), 1
+ * when that is 0 (or T = 0).  Keys appended later use the same factors. */
+static void innerq_key_norms(orc_head *s, const uint16_t *K, int64_t T) {
+  const int d = s->d;
+  for (int c = 0; c < d; ++c) {
+    float a = 0.0f;
+    for (int64_t t = 0; t < T; ++t) {
+      const float x = fabsf(orc_half_to_float(K[t * d + c]));
+      if (x > a) a = x;
+    }
+    s->k_norm[c] = a > 0.0f ? a : 1.0f;
+  }
 }
 
 /* ---- cache state machine ---------------------------------------------- */
@@ -196,6 +222,7 @@ int orc_prefill(orc_head *s, const uint16_t *K, const uint16_t *V, int64_t T) {
   const int64_t nw = rest < s->residual ? rest : s->residual;
   const int64_t nq = rest - nw;
   if (nq > s->cap) return -1;
+  if (s->k_normalize) innerq_key_norms(s, K, T);
   memcpy(s->k_sink, K, sizeof(uint16_t) * (size_t)(ns * d));
   memcpy(s->v_sink, V, sizeof(uint16_t) * (size_t)(ns * d));
   for (int64_t t = 0; t < nq; ++t) innerq_quant_kv(s, K + (ns + t) * d, V + (ns + t) * d, t);
@@ -306,8 +333,10 @@ int orc_attend(const orc_head *s, const uint16_t *q, double tau, double *out) {
     sc[i] = tau * acc;
   }
   for (int64_t t = 0; t < s->n_quant; ++t, ++i) {
+    /* normalized keys: the factor is folded into the query */
     double acc = 0.0;
-    for (int c = 0; c < d; ++c) acc += qd[c] * key_hat(s, t, c);
+    for (int c = 0; c < d; ++c)
+      acc += qd[c] * (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, t, c);
     sc[i] = tau * acc;
   }
   for (int64_t t = 0; t < s->n_resid; ++t, ++i) {

@@ -18,7 +18,7 @@
  *   [HF]      pgsm.cn KV-cache quantization how-to, §2.1 量化基础概念,
  *             §3.1 残差缓存设计, §3.2 内存节省计算示例.
  *   [INNERQ]  "【论文】InnerQ：硬件感知免调优KV缓存量化用于大语言模型" (euno.news),
- *             方法论 1-4.
+ *             关键贡献, 方法论 1-4.
  */
 #ifndef KVQ_ORACLE_H
 #define KVQ_ORACLE_H
@@ -40,7 +40,7 @@ typedef struct orc_head {
   int32_t v_group;    /* channels per value group */
   int32_t residual;   /* KIVI: residual length R; InnerQ: recent window W */
   int32_t n_sink;     /* InnerQ: fp16 sink tokens S */
-  int32_t pad_;
+  int32_t k_normalize;/* InnerQ: 1 = one-shot per-channel key normalization */
   int64_t cap;        /* token capacity of the quantized region */
   int64_t n_quant;    /* tokens held quantized */
   int64_t n_resid;    /* KIVI: fp16 residual tokens; InnerQ: fp16 window tokens */
@@ -52,6 +52,7 @@ typedef struct orc_head {
   uint8_t *k_sym, *v_sym;     /* InnerQ [cap][d/group]: 1 = symmetric group */
   uint16_t *k_res, *v_res;    /* [residual][d] fp16, oldest first */
   uint16_t *k_sink, *v_sink;  /* [n_sink][d] fp16 */
+  float *k_norm;              /* InnerQ with k_normalize: [d] per-channel key factors */
 } orc_head;
 
 int orc_rounding_is_nearest(void);

@@ -252,6 +252,50 @@ def pin_innerq_modes():
         assert h.k_sym[t, 1] == 0
 
 
+def pin_innerq_key_norms():
+    """One-shot per-channel key normalization: the factor of channel c is the
+    largest |K[t][c]| over the whole prompt (1 for an all-zero channel or an
+    empty prompt), and scaling a key channel by a power of two scales its
+    factor and leaves every code, scale, zero and mode unchanged (appended
+    keys included)."""
+    rng = np.random.default_rng(23)
+    d, S, W = 128, 2, 8
+    for T in (0, 1, 40):
+        K, V = _randn16(rng, T + 20, d), _randn16(rng, T + 20, d)
+        if T:
+            K[:, 5] = 0                           # an all-zero channel
+            K[0, 7] = np.float16(-9.5)            # a channel whose extreme is a sink
+        e = rng.integers(0, 4, d)          # up-scaling: exact in fp16 (no subnormals)
+        K2 = (K.astype(np.float32) * np.exp2(e).astype(np.float32)).astype(np.float16)
+        assert np.array_equal(K2.astype(np.float32), K.astype(np.float32) * np.exp2(e))
+        hs = []
+        for KK in (K, K2):
+            h = oracle.OracleHead(d, 4, oracle.INNERQ, 32, 64, W, S, 128, k_norm=True)
+            h.prefill(KK[:T], V[:T])
+            for i in range(T, T + 20):
+                h.append(KK[i], V[i])
+            hs.append(h)
+        if T == 0:
+            assert np.array_equal(hs[0].key_norms(), np.ones(d, np.float32))
+            continue
+        amax = np.abs(K[:T].astype(np.float32)).max(axis=0)
+        want = np.where(amax > 0, amax, np.float32(1))
+        assert np.array_equal(hs[0].key_norms(), want)
+        assert want[5] == 1 and want[7] == np.float32(9.5)
+        want2 = np.where(amax > 0, want * np.exp2(e).astype(np.float32), np.float32(1))
+        assert np.array_equal(hs[1].key_norms(), want2)
+        n = hs[0].n_quant
+        assert n == hs[1].n_quant and n > 0
+        for a, b in ((hs[0].k_u, hs[1].k_u), (hs[0].k_scale, hs[1].k_scale),
+                     (hs[0].k_zero, hs[1].k_zero), (hs[0].k_sym, hs[1].k_sym)):
+            assert np.array_equal(a[:n], b[:n])
+        # the normalized keys reconstruct within half a step of K / factor
+        x = K[S:S + n].astype(np.float32) * (np.float32(1) / hs[0].key_norms())
+        sc = np.repeat(hs[0].k_scale[:n], 32, axis=1).astype(np.float64)
+        zz = np.repeat(hs[0].k_zero[:n], 32, axis=1).astype(np.float64)
+        assert np.all(np.abs(x - (hs[0].k_u[:n] * sc + zz)) <= sc / 2 + 1e-5)
+
+
 # --------------------------------------------------------------------------
 # attention pins
 # --------------------------------------------------------------------------
@@ -356,6 +400,26 @@ def pin_attention_grid_exact_innerq():
     np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K, V, tau), rtol=0, atol=1e-12)
 
 
+def pin_attention_grid_exact_innerq_key_norm():
+    """Normalized keys with power-of-two factors stay grid-exact, so attention
+    with the factor folded into q equals plain attention on the raw tokens."""
+    rng = np.random.default_rng(24)
+    d, S, W, T = 128, 2, 8, 60
+    K, V = _grid_tokens(rng, T, d, 4, 1, 64, sym_groups=True)
+    assert np.abs(K.astype(np.float32)).max() < 32
+    q = _randn16(rng, d)
+    # the sink carries each channel's extreme (factors 32 and 128) and scores
+    # far below the rest, so the quantized tokens decide the output
+    sgn = np.where(q.astype(np.float32) > 0, -1, 1)
+    K[0] = (np.repeat(np.float32([32, 128]), 64) * sgn).astype(np.float16)
+    h = oracle.OracleHead(d, 4, oracle.INNERQ, 64, 64, W, S, 256, k_norm=True)
+    h.prefill(K, V)
+    assert h.n_quant == T - S - W
+    assert np.array_equal(h.key_norms(), np.repeat(np.float32([32, 128]), 64))
+    tau = 1 / math.sqrt(d)
+    np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K, V, tau), rtol=0, atol=1e-12)
+
+
 def pin_attention_identical_keys_mean():
     rng = np.random.default_rng(22)
     d, G, Gv, R, T = 32, 8, 8, 16, 48
@@ -432,8 +496,12 @@ MUTANTS = [
     ("flush one early", "if (s->n_resid == R) {", "if (s->n_resid == R - 1) {"),
     ("prefill split by G", "const int64_t nq = T - T % R;", "const int64_t nq = T - T % G;"),
     ("softmax sign", "sc[j] = exp(sc[j] - m);", "sc[j] = exp(m - sc[j]);"),
-    ("tau dropped", "for (int c = 0; c < d; ++c) acc += qd[c] * key_hat(s, t, c);\n    sc[i] = tau * acc;",
-     "for (int c = 0; c < d; ++c) acc += qd[c] * key_hat(s, t, c);\n    sc[i] = acc;"),
+    ("tau dropped", "acc += qd[c] * (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, t, c);\n    sc[i] = tau * acc;",
+     "acc += qd[c] * (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, t, c);\n    sc[i] = acc;"),
+    ("key factor not folded into q", "(s->k_normalize ? (double)s->k_norm[c] : 1.0)", "1.0"),
+    ("key factor over the quantized tokens only", "for (int64_t t = 0; t < T; ++t) {\n      const float x = fabsf",
+     "for (int64_t t = s->n_sink < T ? s->n_sink : T; t < T; ++t) {\n      const float x = fabsf"),
+    ("zero channel factor 0", "s->k_norm[c] = a > 0.0f ? a : 1.0f;", "s->k_norm[c] = a;"),
     ("big-endian pack", "<< ((c % per) * bits)", "<< ((per - 1 - c % per) * bits)"),
     ("evict newest", "innerq_quant_kv(s, s->k_res, s->v_res, s->n_quant);", "innerq_quant_kv(s, k, v, s->n_quant);"),
     ("half exponent bias", "expo - 25", "expo - 24"),
