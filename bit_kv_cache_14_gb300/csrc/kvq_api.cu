@@ -34,7 +34,8 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   const kvq_config &c = *cfg;
   if (c.batch < 1 || c.n_kv_heads < 1 || c.n_q_heads < 1 || c.max_ctx < 1) return KVQ_EINVAL;
   if (c.n_q_heads % c.n_kv_heads != 0) return KVQ_EINVAL;
-  if (c.scheme != KVQ_KIVI && c.scheme != KVQ_INNERQ) return KVQ_EINVAL;
+  if (c.scheme != KVQ_KIVI && c.scheme != KVQ_INNERQ && c.scheme != KVQ_INNERQ_KNORM)
+    return KVQ_EINVAL;
   if (c.residual < 0 || c.n_sink < 0 || c.k_group < 1 || c.v_group < 1) return KVQ_EINVAL;
   const int rg = c.n_q_heads / c.n_kv_heads;
   if (rg != 1 && rg != 2 && rg != 4 && rg != 8) return KVQ_EUNSUPPORTED;
@@ -55,7 +56,9 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   g->Hq = c.n_q_heads;
   g->d = c.head_dim;
   g->bits = c.bits;
-  g->scheme = c.scheme;
+  // the normalization is an InnerQ option: internally the scheme is InnerQ
+  g->scheme = c.scheme == KVQ_INNERQ_KNORM ? KVQ_INNERQ : c.scheme;
+  g->knorm = c.scheme == KVQ_INNERQ_KNORM ? 1 : 0;
   g->k_group = c.k_group;
   g->v_group = c.v_group;
   g->residual = c.residual;
@@ -64,7 +67,7 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   g->cap = (c.max_ctx + kCapAlign - 1) / kCapAlign * kCapAlign;
   g->row_bytes = c.head_dim * c.bits / 8;
   g->v_meta_cols = c.head_dim / c.v_group;
-  if (c.scheme == KVQ_KIVI) {
+  if (g->scheme == KVQ_KIVI) {
     g->k_meta_cols = c.head_dim;
     g->k_meta_rows = g->cap / c.k_group;
     g->mode_words = 0;
@@ -80,7 +83,7 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   g->blk_vs = 2 * kBlockTokens * g->row_bytes;
   g->blk_vz = g->blk_vs + vmeta;
   g->blk_ks = g->blk_vz + vmeta;
-  if (c.scheme == KVQ_INNERQ) {
+  if (g->scheme == KVQ_INNERQ) {
     const int kmeta = kBlockTokens * g->k_meta_cols * (int)sizeof(float);
     g->blk_kz = g->blk_ks + kmeta;
     g->block_bytes = g->blk_kz + kmeta;
@@ -91,12 +94,14 @@ int resolve(const kvq_config *cfg, Geometry *g) {
                                       ? (kBlockTokens / c.k_group) * 2 * c.head_dim * (int)sizeof(float)
                                       : 0);
   }
+  g->knorm_off = (int64_t)g->B * g->H * (g->cap / kBlockTokens) * g->block_bytes;
   return KVQ_OK;
 }
 
-CachePtrs ptrs_of(const kvq_cache *c) {
+CachePtrs ptrs_of(const Geometry &g, const kvq_cache *c) {
   CachePtrs p;
   p.blocks = static_cast<uint8_t *>(c->blocks);
+  p.k_norm = g.knorm ? reinterpret_cast<float *>(p.blocks + g.knorm_off) : nullptr;
   p.k_meta = c->k_meta;
   p.k_mode = c->k_mode;
   p.v_mode = c->v_mode;
@@ -148,7 +153,8 @@ int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out) {
   if (r != KVQ_OK) return r;
   memset(out, 0, sizeof(*out));
   const size_t BH = (size_t)g.B * g.H;
-  out->blocks = BH * (size_t)(g.cap / kBlockTokens) * g.block_bytes;
+  out->blocks = BH * (size_t)(g.cap / kBlockTokens) * g.block_bytes +
+                (g.knorm ? BH * (size_t)g.d * sizeof(float) : 0);
   if (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens)
     out->k_meta = BH * (size_t)g.k_meta_rows * 2 * g.d * sizeof(float) + kMetaPad;
   if (g.scheme == KVQ_INNERQ) out->k_mode = out->v_mode = BH * (size_t)g.mode_words * 4;
@@ -189,7 +195,7 @@ int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t
     nq = rest - nr;
   }
   int launches = 0;
-  r = from_cuda(launch_prefill(g, ptrs_of(cache), reinterpret_cast<const __half *>(K),
+  r = from_cuda(launch_prefill(g, ptrs_of(g, cache), reinterpret_cast<const __half *>(K),
                                reinterpret_cast<const __half *>(V), T, nq, nr, ns,
                                static_cast<cudaStream_t>(stream), &launches));
   if (r != KVQ_OK) return r;
@@ -212,7 +218,7 @@ int kvq_append(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k, const
   if (cache->n_quant + cache->n_resid + cache->n_sink + 1 > g.max_ctx) return KVQ_ECAPACITY;
   if (g.scheme == KVQ_KIVI && cache->n_resid >= g.residual) return KVQ_EINVAL;
   if (g.scheme == KVQ_INNERQ && g.residual > 0 && cache->ring_head >= g.residual) return KVQ_EINVAL;
-  r = from_cuda(launch_append(g, ptrs_of(cache), reinterpret_cast<const __half *>(k),
+  r = from_cuda(launch_append(g, ptrs_of(g, cache), reinterpret_cast<const __half *>(k),
                               reinterpret_cast<const __half *>(v), cache->n_quant,
                               cache->n_resid, cache->n_sink, cache->ring_head,
                               static_cast<cudaStream_t>(stream)));
@@ -249,7 +255,7 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
   if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
   const DecodePlan plan =
       plan_decode(g, cache->n_quant, cache->n_resid + cache->n_sink, num_sms_cached());
-  r = from_cuda(launch_decode(g, ptrs_of(cache), plan, cache->n_quant, cache->n_resid,
+  r = from_cuda(launch_decode(g, ptrs_of(g, cache), plan, cache->n_quant, cache->n_resid,
                               cache->n_sink, cache->ring_head,
                               reinterpret_cast<const __half *>(q), out, softmax_scale, ws,
                               num_sms_cached(), static_cast<cudaStream_t>(stream)));
@@ -283,7 +289,7 @@ int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k
     note_launch(2);
     return KVQ_OK;
   }
-  r = from_cuda(launch_decode_tc(g, ptrs_of(cache), cache->n_quant, cache->n_resid + 1,
+  r = from_cuda(launch_decode_tc(g, ptrs_of(g, cache), cache->n_quant, cache->n_resid + 1,
                                  cache->n_sink, reinterpret_cast<const __half *>(q), out,
                                  softmax_scale, ws, num_sms_cached(),
                                  static_cast<cudaStream_t>(stream),

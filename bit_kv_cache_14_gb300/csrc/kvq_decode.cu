@@ -112,9 +112,12 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
   const int64_t bh = blockIdx.y;
   const int b = (int)(bh / g.H), h = (int)(bh % g.H);
 
+  const bool fp16_split = split == a.n_qsplit;
   for (int i = tid; i < RG * D; i += kBlock) {
     const int hq = h * RG + i / D;
     q_s[i] = __half2float(a.q[((int64_t)b * g.Hq + hq) * D + i % D]) * a.scale_log2;
+    // quantized keys are normalized per channel: the factor goes into q
+    if (SCHEME == KVQ_INNERQ && g.knorm && !fp16_split) q_s[i] *= a.p.k_norm[bh * D + i % D];
   }
   __syncthreads();
   if (SCHEME == KVQ_INNERQ) {
@@ -126,7 +129,6 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     }
   }
 
-  const bool fp16_split = split == a.n_qsplit;
   int64_t t0 = 0, n_tok;
   if (fp16_split) {
     n_tok = a.n_sink + a.n_resid;

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
 
   // Per-head constants from the query row that rode along with the head's
   // first tile of this warp.
-  auto start_head = [&](const uint8_t *slot) {
+  auto start_head = [&](const uint8_t *slot, int cur_bh) {
     const __half *qh = reinterpret_cast<const __half *>(slot + SC::off_q);
     const uint2 qr = reinterpret_cast<const uint2 *>(qh)[lane];
     const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
@@ -233,6 +233,16 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     q4[1] = q01.y * a.scale_log2;
     q4[2] = q23.x * a.scale_log2;
     q4[3] = q23.y * a.scale_log2;
+    // InnerQ with normalized keys: the per-channel factors go into q (the
+    // quantized tokens only; the fp16 rows reload the raw query)
+    const float *knr = SCHEME == KVQ_INNERQ && g.knorm ? a.p.k_norm + (int64_t)cur_bh * kD : nullptr;
+    if (knr) {
+      const float4 n4 = reinterpret_cast<const float4 *>(knr)[lane];
+      q4[0] *= n4.x;
+      q4[1] *= n4.y;
+      q4[2] *= n4.z;
+      q4[3] *= n4.w;
+    }
     float mx = fmaxf(fmaxf(fabsf(q4[0]), fabsf(q4[1])), fmaxf(fabsf(q4[2]), fabsf(q4[3])));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     if (mx > 0.0f && mx < INFINITY) frexpf(mx, &E);
     pow2E = ldexpf(1.0f, E) * kSub;
     const float inv = ldexpf(1.0f, -E);
-    auto qf = [&](int c) { return __half2float(qh[c]) * a.scale_log2; };
+    auto qf = [&](int c) { return __half2float(qh[c]) * a.scale_log2 * (knr ? knr[c] : 1.0f); };
     if (SCHEME == KVQ_KIVI) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           break;
         }
         const uint8_t *slot = wring + s * SLOT;
-        if (lt == 0) start_head(slot);
+        if (lt == 0) start_head(slot, bh);
         const int tok0 = tq0 + kTile * lt;
         const int n = min(kTile, tq1 - tok0);
         auto tile = [&](auto full_c) {

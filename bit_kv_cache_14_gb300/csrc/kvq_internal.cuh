@@ -28,6 +28,8 @@ struct Geometry {
   int64_t mode_words;   // per head, InnerQ only
   int block_bytes;      // one 32-token block
   int blk_vc, blk_vs, blk_vz, blk_ks, blk_kz;  // byte offsets inside a block
+  int knorm;            // InnerQ key normalization (KVQ_INNERQ_KNORM)
+  int64_t knorm_off;    // byte offset of the key factors f32 [B][H][d] in blocks
 };
 
 // Device pointers of a cache (same meaning as kvq_cache).
@@ -37,6 +39,7 @@ struct CachePtrs {
   uint32_t *k_mode, *v_mode;
   __half *k_res, *v_res, *k_sink, *v_sink;
   int32_t *status;
+  float *k_norm;  // key factors [B*H][d] (KVQ_INNERQ_KNORM), else nullptr
 };
 
 // ---- addressing of the block layout (include/kvq.h, "Packed layout") ------
@@ -71,7 +74,7 @@ __device__ __forceinline__ float *kivi_key_meta(const Geometry &g, const CachePt
 }
 
 int resolve(const kvq_config *cfg, Geometry *g);
-CachePtrs ptrs_of(const kvq_cache *c);
+CachePtrs ptrs_of(const Geometry &g, const kvq_cache *c);
 void note_launch(int n);
 
 // ---- launchers (return cudaError_t of the launch) ------------------------

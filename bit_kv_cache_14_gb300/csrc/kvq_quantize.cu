@@ -78,6 +78,53 @@ __device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int
   __syncthreads();
 }
 
+// One-shot per-channel key normalization ("InnerQ" summary, key
+// contributions and methodology 4): keys of channel c are multiplied by
+// r_c = 1 / n_c before they are quantized (fp32 division, then an fp32
+// product), n_c the largest |K[t][c]| of the prompt (1 if 0).
+__device__ __forceinline__ void normalize8(const float *k_norm_row, int c0, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4 *>(k_norm_row + c0)[0];
+  const float4 b = reinterpret_cast<const float4 *>(k_norm_row + c0)[1];
+  const float n[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) x[k] = __fmul_rn(x[k], __fdiv_rn(1.0f, n[k]));
+}
+
+// Key factors, pass 1: the largest |K[t][c]| of tokens [t0, t0 + kNormTokens)
+// of head blockIdx.y into n[bh][c] by an atomic max on the bit pattern
+// (non-negative floats order like their bits); n starts at 0.
+constexpr int kNormTokens = 4096;
+__global__ void __launch_bounds__(kQuantBlock)
+    key_absmax_kernel(const __half *K, int64_t T, int d, float *n) {
+  __shared__ unsigned int s_max[kMaxHeadDim];
+  const int64_t bh = blockIdx.y;
+  const int chunks = d / 8, rows = kQuantBlock / chunks;
+  const int j = threadIdx.x % chunks, r = threadIdx.x / chunks;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) s_max[c] = 0u;
+  __syncthreads();
+  const int64_t t0 = (int64_t)blockIdx.x * kNormTokens;
+  const int64_t t1 = min(t0 + kNormTokens, T);
+  float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int64_t t = t0 + r; t < t1; t += rows) {
+    float x[8];
+    load8(K + (bh * T + t) * d + 8 * j, x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], fabsf(x[k]));
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) atomicMax(&s_max[8 * j + k], __float_as_uint(m[k]));
+  __syncthreads();
+  for (int c = threadIdx.x; c < d; c += blockDim.x)
+    atomicMax(reinterpret_cast<unsigned int *>(n + bh * d + c), s_max[c]);
+}
+
+// Key factors, pass 2: an all-zero channel (or an empty prompt) gets 1.
+__global__ void key_norm_finish_kernel(float *n, int64_t count) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x)
+    if (!(n[i] > 0.0f)) n[i] = 1.0f;
+}
+
 // Result of quantizing one 8-channel chunk inside a per-token group.
 struct ChunkQ {
   uint32_t codes;
@@ -185,6 +232,7 @@ __global__ void __launch_bounds__(kQuantBlock)
   float x[8];
   if (valid) {
     load8(X + (bh * T + src0 + t) * g.d + 8 * j, x);
+    if (is_key && g.knorm) normalize8(p.k_norm + bh * g.d, 8 * j, x);
   } else {
 #pragma unroll
     for (int k = 0; k < 8; ++k) x[k] = 0.0f;
@@ -317,6 +365,7 @@ __global__ void __launch_bounds__(32)
     float x[8];
     if (valid) {
       load8((is_key ? srck : srcv) + 8 * j, x);
+      if (is_key && g.knorm) normalize8(p.k_norm + bh * d, 8 * j, x);
     } else {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) x[kk] = 0.0f;
@@ -376,6 +425,18 @@ cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *
       ++n;
     }
   } else {
+    if (g.knorm) {
+      // key factors over the whole prompt, before any key is quantized
+      const cudaError_t e = cudaMemsetAsync(p.k_norm, 0, sizeof(float) * BH * g.d, st);
+      if (e != cudaSuccess) return e;
+      if (T > 0) {
+        key_absmax_kernel<<<dim3((unsigned)((T + kNormTokens - 1) / kNormTokens), (unsigned)BH),
+                            kQuantBlock, 0, st>>>(K, T, g.d, p.k_norm);
+        ++n;
+      }
+      key_norm_finish_kernel<<<copy_blocks(BH * g.d), 256, 0, st>>>(p.k_norm, BH * g.d);
+      ++n;
+    }
     if (n_sink > 0) {
       copy_rows_kernel<<<dim3(copy_blocks(BH * n_sink * chunks), 1, 2), 256, 0, st>>>(
           K, V, T, 0, n_sink, p.k_sink, p.v_sink, g.n_sink, g.d, BH);

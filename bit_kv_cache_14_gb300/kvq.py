@@ -26,6 +26,7 @@ KVQ_ECUDA = -5
 KVQ_ETIMEOUT = -6
 KIVI = 0
 INNERQ = 1
+INNERQ_KNORM = 2  # InnerQ with the one-shot per-channel key normalization
 CAP_ALIGN = 128  # token-stride granularity of the cache layout
 
 # Every entry point declared in include/kvq.h.
@@ -116,7 +117,8 @@ def make_config(batch, n_q_heads, n_kv_heads, head_dim, bits, scheme, k_group, v
 
 def config_of(w, max_ctx: int | None = None) -> Config:
     """Config of a synth.Workload (max_ctx defaults to prompt + streamed tokens)."""
-    return make_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.bits, w.scheme,
+    scheme = INNERQ_KNORM if getattr(w, "k_norm", False) else w.scheme
+    return make_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.bits, scheme,
                        w.k_group, w.v_group, w.residual, w.n_sink,
                        w.max_ctx() if max_ctx is None else max_ctx)
 
@@ -246,7 +248,7 @@ class QuantizedKVCache:
         c = self.cfg
         rb = c.head_dim * c.bits // 8
         ngv = c.head_dim // c.v_group
-        ngk = c.head_dim // c.k_group if c.scheme == INNERQ else 0
+        ngk = c.head_dim // c.k_group if c.scheme in (INNERQ, INNERQ_KNORM) else 0
         off = {"k_codes": 0, "v_codes": 32 * rb, "v_scale": 64 * rb}
         off["v_zero"] = off["v_scale"] + 128 * ngv
         off["k_scale"] = off["v_zero"] + 128 * ngv
@@ -292,6 +294,18 @@ class QuantizedKVCache:
         cols = ngk if name.startswith("k") else ngv
         f = self._block_field(name, 4 * cols).contiguous().view(torch.float32)
         return f.reshape(c.batch, c.n_kv_heads, -1)
+
+    def key_norms(self) -> torch.Tensor:
+        """Per-channel key factors fp32 [B][H][d] (INNERQ_KNORM), stored after
+        the last head's blocks (a copy)."""
+        c = self.cfg
+        if c.scheme != INNERQ_KNORM:
+            raise ValueError("the configuration has no key normalization")
+        _, bb, _, _, _ = self._block_layout()
+        off = c.batch * c.n_kv_heads * (self.cap // 32) * bb
+        n = c.batch * c.n_kv_heads * c.head_dim
+        f = self.bufs["blocks"][off: off + 4 * n].view(torch.float32)
+        return f.reshape(c.batch, c.n_kv_heads, c.head_dim)
 
     def modes(self, which: str) -> torch.Tensor:
         c = self.cfg

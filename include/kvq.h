@@ -49,6 +49,8 @@
  *                      row, then zero (= min) row, one value per channel
  *           block_bytes = 64*d*bits/8 + 256*(d/v_group + (InnerQ ? d/k_group : 0))
  *                         + (KIVI, G <= 32 ? (32/G)*8*d : 0), a multiple of 128.
+ *           KVQ_INNERQ_KNORM: the blocks buffer ends with the key factors
+ *             f32 [B][H][d] (n_c above), after the last head's blocks.
  *   KIVI with G >= 64:
  *           k_meta  f32 [B][H][cap/G][2][d]  the same two rows per key group
  *           (the buffer carries 64 bytes of slack after the last head)
@@ -81,6 +83,7 @@ extern "C" {
 
 #define KVQ_KIVI 0
 #define KVQ_INNERQ 1
+#define KVQ_INNERQ_KNORM 2 /* InnerQ with the one-shot per-channel key normalization */
 
 /*
  * Cache configuration.
@@ -93,6 +96,15 @@ extern "C" {
  *   scheme KVQ_INNERQ: k_group and v_group = channels per group (multiples of
  *     16 dividing d), residual = W recent fp16 tokens (0..1024), n_sink = S
  *     fp16 sink tokens (0..1024).
+ *   scheme KVQ_INNERQ_KNORM: KVQ_INNERQ plus the one-shot per-channel key
+ *     normalization ("InnerQ" paper summary, key contributions and
+ *     methodology 4: keys scaled once per channel at prefill, the factor
+ *     folded into the query).  kvq_quantize_prefill sets the factor n_c of
+ *     channel c of every head to the largest |K[t][c]| over the T prompt
+ *     tokens (1 if that is 0 or T = 0); every key that is quantized (now or
+ *     when it later leaves the window) is first multiplied, in fp32, by
+ *     r_c = 1 / n_c (fp32 division); decode multiplies q by n_c for the
+ *     quantized tokens.  Sinks and window stay the raw fp16 keys.
  *   max_ctx: most tokens one sequence will hold (prompt + appended).
  */
 typedef struct kvq_config {

@@ -48,6 +48,10 @@ def check_head_state(cache, w, b, h, head):
                            (vz, vz_o, "v_zero")):
         assert np.array_equal(got.view(np.uint32), exp.reshape(-1).view(np.uint32)), \
             "%s differs (b=%d h=%d)" % (name, b, h)
+    if getattr(w, "k_norm", False):
+        kn = cache.key_norms()[b, h].cpu().numpy()
+        assert np.array_equal(kn.view(np.uint32), head.key_norms().view(np.uint32)), \
+            "key factors differ (b=%d h=%d)" % (b, h)
     kr_o, vr_o = head.residual_tokens()
     nr = head.n_resid
     if w.scheme == synth.KIVI:

@@ -60,6 +60,11 @@ def test_sizes_follow_layout():
     assert si.k_meta == 0
     assert si.k_mode == 32 * ((1 << 20) * 2 // 32) * 4
     assert si.k_sink == 32 * 4 * 128 * 2
+    # the key normalization adds the fp32 factors [B][H][d] after the blocks
+    sn = kvq.cache_sizes(_cfg(scheme=kvq.INNERQ_KNORM, bits=4, k_group=64, v_group=64,
+                              residual=32, n_sink=4, batch=1, max_ctx=1 << 20))
+    assert sn.blocks == si.blocks + 32 * 128 * 4
+    assert (sn.k_mode, sn.v_mode, sn.k_res, sn.k_sink) == (si.k_mode, si.v_mode, si.k_res, si.k_sink)
 
 
 def test_per_token_bytes_match_llama2_table():
@@ -87,6 +92,8 @@ def test_workspace_bytes():
     (dict(max_ctx=0), kvq.KVQ_EINVAL),
     (dict(scheme=7), kvq.KVQ_EINVAL),
     (dict(scheme=kvq.INNERQ, k_group=48), kvq.KVQ_EUNSUPPORTED),
+    (dict(scheme=kvq.INNERQ_KNORM, k_group=48), kvq.KVQ_EUNSUPPORTED),
+    (dict(scheme=3), kvq.KVQ_EINVAL),
 ])
 def test_config_validation(kw, code):
     with pytest.raises(kvq.KVQError) as e:

@@ -55,6 +55,14 @@ SMALL = {
     # value groups (the gqa_small case covers 4 heads per KV head, G 32)
     "gqa_rg2_g64": S(W["gqa_2bit"], batch=2, n_q_heads=8, n_kv_heads=4, ctx=900, k_group=64,
                      v_group=64, residual=128, n_append=150),
+    # InnerQ with the one-shot per-channel key normalization: MHA (tensor-core
+    # kernel), 2-bit with 32-channel key groups, and grouped-query (general kernel)
+    "innerq_knorm": S(W["innerq_1m"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=900, n_append=40,
+                      k_norm=True),
+    "innerq_knorm_2bit": S(W["innerq_1m"], batch=1, n_q_heads=3, n_kv_heads=3, ctx=700, bits=2,
+                           k_group=32, v_group=32, n_append=30, k_norm=True),
+    "innerq_knorm_gqa": S(W["innerq_1m"], batch=1, n_q_heads=8, n_kv_heads=2, ctx=600,
+                          n_append=40, k_norm=True),
 }
 
 
