@@ -362,7 +362,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   int done = 0;          // items whose copies completed
   int cs = 0;            // ring slot of the next item
   uint32_t cph = 0;      // its barrier phase parity
-  bool first = true;
   // Waits for the next ring slot.  One verdict per warp: every lane takes
   // the same path; false (status word set) on timeout.
   auto wait_slot = [&](int &s_out) -> bool {
@@ -372,10 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       cs = 0;
       cph ^= 1u;
     }
-    bool ok = true;
-    if (first && a.stall_limit > 0) ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
-    first = false;
-    if (ok) ok = bar_wait(wbars_s + 8 * s, par, a.wait_limit);
+    const bool ok = bar_wait(wbars_s + 8 * s, par, a.wait_limit);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
       return false;
@@ -385,6 +381,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     return true;
   };
   bool aborted = false;
+  if (a.stall_limit > 0) {
+    // debug: the warp's first wait is on a barrier nothing completes
+    const bool ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
+      aborted = true;
+    }
+  }
   for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
     const Seg sg = warp_seg(a, bh, x0, x1);
     const int tq0 = sg.tq0, tq1 = sg.tq1;
@@ -560,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             float mt_ = score;
   #pragma unroll
             for (int off = 1; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
-            const float alpha = exp2f(m_run - mt_);
+            const float alpha = exp2_approx(m_run - mt_);
             l_lane *= alpha;
   #pragma unroll
             for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
@@ -570,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
               for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
             m_run = mt_;
           }
-          const float p = exp2f(score - m_run);  // <= 2^kSlack
+          const float p = exp2_approx(score - m_run);  // <= 2^kSlack
           const float pv = p * kInvSlack;          // value operand scale: stays in fp16 range
           l_lane += p;
           {
@@ -755,8 +759,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 8));
         mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
         const float mn = fmaxf(mf, mc);
-        const float al = exp2f(mf - mn);
-        const float pr = exp2f(sc - mn);  // 0 for rows past the chunk's end
+        const float al = exp2_approx(mf - mn);
+        const float pr = exp2_approx(sc - mn);  // 0 for rows past the chunk's end
         float ps_ = pr;
         ps_ += __shfl_xor_sync(0xffffffffu, ps_, 4);
         ps_ += __shfl_xor_sync(0xffffffffu, ps_, 8);

@@ -187,6 +187,14 @@ __device__ __forceinline__ uint32_t shifted(uint32_t w) {
   return BITS == 2 ? (w >> 10) : (w >> 8);
 }
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz: relative error about
+// 2^-22; 2^-inf = 0).  Softmax weights only.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Multiplier carried by the code at position p (see ext).
 template <int BITS>
 __host__ __device__ __forceinline__ float pos_factor(int p) {
