@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
           if (mt_ > m_run) {
-            const float alpha = exp2f(m_run - mt_);
+            const float alpha = exp2_approx(m_run - mt_);
             l_lane *= alpha;
 #pragma unroll
             for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
@@ -539,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
           const float *vz = reinterpret_cast<const float *>(slot + C::off_vz);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float p = sc[i] == -INFINITY ? 0.0f : exp2f(sc[i] - m_run);
+            const float p = sc[i] == -INFINITY ? 0.0f : exp2_approx(sc[i] - m_run);
             pv[i] = p * kInvSlack;
             l_lane += p;
             if (p > 0.0f) {
@@ -654,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) sc_ += __shfl_xor_sync(0xffffffffu, sc_, off);
             const float mn = fmaxf(mf[r], sc_);
-            const float al = exp2f(mf[r] - mn), pp = exp2f(sc_ - mn);
+            const float al = exp2_approx(mf[r] - mn), pp = exp2_approx(sc_ - mn);
             lf[r] = fmaf(lf[r], al, pp);
             af[r][0] = fmaf(af[r][0], al, pp * v01.x);
             af[r][1] = fmaf(af[r][1], al, pp * v01.y);
