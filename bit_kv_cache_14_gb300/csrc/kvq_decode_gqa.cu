@@ -18,8 +18,12 @@
 //    lane (gid, tig) accumulates head tig.
 //  * fp16 sink / residual tokens ride the same ring in 8-token chunks and are
 //    folded on CUDA cores one head at a time into a second partial.
-//  * Work split, rings, bounded waits and the fence-free merge are those of
-//    the MHA kernel (kvq_tc_common.cuh); a partial here is RG rows.
+//  * Work split by block (each block an equal range of (head, 128-token unit)
+//    plus fp16 units; a segment's tiles go round-robin to the block's warps).
+//    Rings and bounded waits are the MHA kernel's (kvq_tc_common.cuh); a
+//    warp publishes its partial (RG rows) and takes a ticket with a relaxed
+//    atomic, and the last ticket's holder merges (fence-free, the same
+//    encoding as the MHA merge).
 #include "kvq_tc_common.cuh"
 
 namespace kvq {

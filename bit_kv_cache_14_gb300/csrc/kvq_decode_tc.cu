@@ -4,21 +4,21 @@
 // cache, dequantization folded into both GEMVs -- "大模型量化技术原理：KIVI、
 // IntactKV、KVQuant", KIVI / 背景; InnerQ page, 方法论 3), arranged for GB300:
 //
-//  * Persistent, stream-K: the (head, 128-token unit) list of the whole batch,
-//    plus one cost-weighted fp16 item per head (sink + residual / window
-//    tokens), is cut into equal contiguous ranges, one per resident block.  A
-//    head split across blocks leaves one partial (m, l, o) per block; the last
-//    block to finish a head (atomic ticket, no spinning) merges them with the
-//    log-sum-exp rule.
-//  * Warp-autonomous consumers: inside a block, the 32-token tiles of each
-//    head segment go round-robin to the warps.  Each warp owns a small ring of
-//    shared-memory slots that its lane 0 fills with 1-D cp.async.bulk copies
-//    (codes + scale/zero of K and V of one tile) completed on the warp's own
-//    mbarriers, and keeps its own online-softmax state; the block synchronises
-//    only at head-segment ends, to merge the warps.  The ring runs ahead across
-//    segment ends, so the copies never stop.  Every wait is bounded; a timeout
-//    sets the status word and the warp drains its own copies before the block
-//    returns.
+//  * Persistent, stream-K over warps: every head is a list of work units (a
+//    32-token tile is one unit, an 8-token fp16 chunk of sink / residual /
+//    window tokens two, plus two empty units at the head's start), and the
+//    list of the whole batch is cut into equal contiguous ranges, one per
+//    warp of the resident grid.  A warp leaves one partial (m, l, o) per head
+//    it touches; the warp holding a head's first unit (its range ends in that
+//    head, and the empty units give it less data) merges them with the
+//    log-sum-exp rule once they are all visible.  No atomics, no fences.
+//  * Warp-autonomous: each warp owns a small ring of shared-memory slots that
+//    one lane fills with 1-D cp.async.bulk copies (a tile's whole 32-token
+//    block, issued by a predicated instruction) completed on the warp's own
+//    mbarriers, and keeps its own online-softmax state; nothing synchronises
+//    the warps of a block.  The ring runs ahead across head ends, so the
+//    copies never stop.  Every wait is bounded; a timeout sets the status
+//    word and the warp drains its own copies before it returns.
 //  * Both GEMVs run as mma.sync m16n8k16 (fp16 in, fp32 accumulate), two
 //    independent 16-token MMA tiles per warp tile.  2/4-bit codes become exact
 //    fp16 operands with one AND per two codes: the masked code bits, left in
@@ -32,7 +32,8 @@
 //             into fp16 hi + lo (n = hi, lo); KIVI: rebuilt per G-token group,
 //             InnerQ: q per channel group j (n = (j, hi/lo)), scale applied after.
 //      values D[c][n] = sum_t code_tc * B[t][n],  B = p_t * scale_tj split into
-//             hi + lo, n = (value group j, hi/lo); row c keeps column j(c).
+//             hi + lo, n = (value group j, hi/lo), written once per token by
+//             the token's lane; row c keeps column j(c).
 //    zero points enter as q.zero per key group and sum_t p_t zero_tj per value
 //    group (CUDA cores).  q is normalised by a power of two so no fp16 operand
 //    can overflow (|q| <= 1, scales <= 65504).
@@ -341,8 +342,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     const float4 oq = reinterpret_cast<const float4 *>(so)[lane];
     __syncwarp();
     const float m = fmaxf(m_run, mf);
-    const float wq = m_run == -INFINITY ? 0.0f : exp2f(m_run - m);
-    const float wf = mf == -INFINITY ? 0.0f : exp2f(mf - m);
+    const float wq = m_run == -INFINITY ? 0.0f : exp2_approx(m_run - m);
+    const float wf = mf == -INFINITY ? 0.0f : exp2_approx(mf - m);
     float4 o;
     o.x = fmaf(oq.x, wq, af[0] * wf);
     o.y = fmaf(oq.y, wq, af[1] * wf);
@@ -350,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     o.w = fmaf(oq.w, wq, af[3] * wf);
     const float lt = fmaf(l, wq, lf * wf);
     reset_state();
-    // the previous head's ticket has long arrived: act on it, then publish
     // a merge still owed (a head this warp held whole) comes first; the
     // merge of the warp's last head waits until after the tile loop
     if (pend_bh >= 0 && !merge_head<8>(a, pend_bh)) return false;

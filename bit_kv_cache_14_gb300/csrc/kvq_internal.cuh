@@ -89,11 +89,14 @@ cudaError_t launch_append(const Geometry &g, const CachePtrs &p, const __half *k
 // per 128 quantized tokens plus the fp16 segment.
 inline int part_slots(const Geometry &g) { return (int)(g.cap / kCapAlign) + 2; }
 
-// The tensor-core decode kernel cuts each head into 128-token units of
-// quantized tokens plus units of fp16 chunks (tc_fp16_chunk tokens each,
-// at least one chunk per unit) and leaves one partial per warp (8 per block)
-// for every block that touches a head's units; it never uses more than
-// kTcMaxBlocks blocks.
+// Partial slots per head of the tensor-core decode kernels, a bound for both
+// splits.  The grouped-query kernel cuts each head into 128-token units plus
+// fp16 units and leaves one partial per warp (8 per block) for every block
+// that touches a head; the MHA kernel gives every warp an equal range of
+// 32-token tiles, fp16 chunks (tc_fp16_chunk tokens, two units each) and two
+// empty units per head, one partial per warp touching the head, i.e. at most
+// cap/32 + 2 * chunks + 3 per head (each warp holds at least one unit), which
+// 8 * (cap/128 + chunks + 2) covers.  At most kTcMaxBlocks blocks.
 constexpr int kTcWarps = 8;
 constexpr int kTcMaxBlocks = 1024;
 inline int tc_fp16_chunk(const Geometry &g) {

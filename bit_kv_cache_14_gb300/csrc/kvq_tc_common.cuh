@@ -351,7 +351,7 @@ __device__ bool merge_head(const TcArgs &a, int bh) {
       float M = ms;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      const float w = ms != -INFINITY ? exp2f(ms - M) : 0.0f;
+      const float w = ms != -INFINITY ? exp2_approx(ms - M) : 0.0f;
       Ls = w * (lane < nparts ? __uint_as_float(v.y ^ kEnc) : 0.0f);
 #pragma unroll
       for (int j = 0; j < MB; ++j) {
@@ -390,7 +390,7 @@ __device__ bool merge_head(const TcArgs &a, int bh) {
         const uint2 v = __ldcg(ml + s0 + lane);
         const float ms = __uint_as_float(v.x ^ kEnc);
         if (ms != -INFINITY) {
-          w = exp2f(ms - M);
+          w = exp2_approx(ms - M);
           Ls = fmaf(w, __uint_as_float(v.y ^ kEnc), Ls);
         }
       }
