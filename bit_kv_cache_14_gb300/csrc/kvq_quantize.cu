@@ -38,19 +38,53 @@ __device__ __forceinline__ void store_chunk(uint8_t *row, int chunk, uint32_t w,
     reinterpret_cast<uint32_t *>(row)[chunk] = w;
 }
 
+// Shared scratch of key_group_per_channel: per-row-lane partial minima and
+// maxima, [blockDim / (d / 8)][d] each (2048 floats for any d).
+constexpr int kKeyPart = kQuantBlock * 8;
+
 // One key group (G tokens of src, row stride d) quantized per channel into
 // token slots [t0, t0 + G), t0 a multiple of G.  All threads of the block call
-// it; s_scale / s_mn are d-float shared arrays.
+// it; s_scale / s_mn are d-float shared arrays, s_pmn / s_pmx kKeyPart-float
+// scratch.  A thread reads 8-channel chunks (16-byte loads) of rows r0, r0 +
+// lanes, ...; the per-channel minimum and maximum are then combined over the
+// row lanes (min / max are order-free, so the result is that of one pass).
 __device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int64_t bh,
                                       const __half *src, int64_t t0, float *s_scale,
-                                      float *s_mn) {
+                                      float *s_mn, float *s_pmn, float *s_pmx) {
   const int d = g.d, G = g.k_group;
+  {
+    const int chunks = d / 8, lanes = blockDim.x / chunks;
+    const int j = threadIdx.x % chunks, r0 = threadIdx.x / chunks;
+    float mn8[8], mx8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      mn8[k] = INFINITY;
+      mx8[k] = -INFINITY;
+    }
+    for (int i = r0; i < G; i += lanes) {
+      float x[8];
+      load8(src + (int64_t)i * d + 8 * j, x);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        mn8[k] = fminf(mn8[k], x[k]);
+        mx8[k] = fmaxf(mx8[k], x[k]);
+      }
+    }
+    if (r0 < lanes) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        s_pmn[r0 * d + 8 * j + k] = mn8[k];
+        s_pmx[r0 * d + 8 * j + k] = mx8[k];
+      }
+    }
+  }
+  __syncthreads();
+  const int lanes = blockDim.x / (d / 8);
   for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float mn = __half2float(src[c]), mx = mn;
-    for (int i = 1; i < G; ++i) {
-      const float x = __half2float(src[(int64_t)i * d + c]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
+    float mn = s_pmn[c], mx = s_pmx[c];
+    for (int r = 1; r < lanes; ++r) {
+      mn = fminf(mn, s_pmn[r * d + c]);
+      mx = fmaxf(mx, s_pmx[r * d + c]);
     }
     mn = canon_zero(mn);
     mx = canon_zero(mx);
@@ -203,7 +237,9 @@ __device__ __forceinline__ void store_token(const Geometry &g, const CachePtrs &
 
 // Prefill, per-token groups: tokens [src0, src0 + n_tok) of every head of
 // X [B*H][T][d] quantized into slots [0, n_tok).  blockIdx.y = head,
-// blockIdx.z = 0 keys / 1 values (keys only under InnerQ).
+// blockIdx.z = 0 keys / 1 values (keys only under InnerQ).  A block takes
+// kTokIter rounds of kQuantBlock / (d/8) tokens.
+constexpr int kTokIter = 4;
 __global__ void __launch_bounds__(kQuantBlock)
     per_token_prefill_kernel(Geometry g, CachePtrs p, const __half *K, const __half *V,
                              int64_t T, int64_t src0, int64_t n_tok) {
@@ -212,39 +248,42 @@ __global__ void __launch_bounds__(kQuantBlock)
   const __half *X = is_key ? K : V;
   const int64_t bh = blockIdx.y;
   const int chunks = g.d / 8;
-  const int tpb = kQuantBlock / chunks;  // tokens per block
-  const int64_t tok0 = (int64_t)blockIdx.x * tpb;
+  const int tpr = kQuantBlock / chunks;  // tokens per round
+  const int64_t tok0 = (int64_t)blockIdx.x * tpr * kTokIter;
   const int lt = threadIdx.x / chunks, j = threadIdx.x - lt * chunks;
-  const int64_t t = tok0 + lt;
-  const bool valid = t < n_tok;
   const int lanes = dst.group / 8;
 
-  // Mode bits of this block's tokens, assembled in shared memory.
-  __shared__ uint32_t s_bits[kQuantBlock / 8 + 2];
+  // Mode bits of this block's tokens, assembled in shared memory (at most
+  // kTokIter * kQuantBlock * 8 / 16 bits: groups of >= 16 channels).
+  __shared__ uint32_t s_bits[kTokIter * kQuantBlock / 64 + 2];
   const int ng = dst.meta_cols;
   const int64_t bit0 = tok0 * ng;
   const int64_t wbase = bit0 >> 5;
   if (dst.mode) {
-    for (int i = threadIdx.x; i < kQuantBlock / 8 + 2; i += blockDim.x) s_bits[i] = 0;
+    for (int i = threadIdx.x; i < kTokIter * kQuantBlock / 64 + 2; i += blockDim.x) s_bits[i] = 0;
     __syncthreads();
   }
 
-  float x[8];
-  if (valid) {
-    load8(X + (bh * T + src0 + t) * g.d + 8 * j, x);
-    if (is_key && g.knorm) normalize8(p.k_norm + bh * g.d, 8 * j, x);
-  } else {
+  for (int it = 0; it < kTokIter; ++it) {
+    const int64_t t = tok0 + (int64_t)it * tpr + lt;
+    const bool valid = t < n_tok;
+    float x[8];
+    if (valid) {
+      load8(X + (bh * T + src0 + t) * g.d + 8 * j, x);
+      if (is_key && g.knorm) normalize8(p.k_norm + bh * g.d, 8 * j, x);
+    } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) x[k] = 0.0f;
-  }
-  const ChunkQ q = quant_chunk(x, lanes, g.bits, dst.mode != nullptr);
-  if (valid) {
-    store_token(g, p, dst, bh, t, j, lanes, q);
-    if ((j & (lanes - 1)) == 0) {
-      const int gi = j / lanes;
-      if (dst.mode && q.sym) {
-        const int64_t bit = t * ng + gi;
-        atomicOr(&s_bits[(bit >> 5) - wbase], 1u << (bit & 31));
+      for (int k = 0; k < 8; ++k) x[k] = 0.0f;
+    }
+    const ChunkQ q = quant_chunk(x, lanes, g.bits, dst.mode != nullptr);
+    if (valid) {
+      store_token(g, p, dst, bh, t, j, lanes, q);
+      if ((j & (lanes - 1)) == 0) {
+        const int gi = j / lanes;
+        if (dst.mode && q.sym) {
+          const int64_t bit = t * ng + gi;
+          atomicOr(&s_bits[(bit >> 5) - wbase], 1u << (bit & 31));
+        }
       }
     }
   }
@@ -252,7 +291,7 @@ __global__ void __launch_bounds__(kQuantBlock)
   __syncthreads();
   // Write back the words this block owns.  Blocks own disjoint bit ranges;
   // the block holding the last token also owns the rest of its last word.
-  const int64_t tok_end = min(tok0 + tpb, n_tok);
+  const int64_t tok_end = min(tok0 + (int64_t)tpr * kTokIter, n_tok);
   if (tok_end <= tok0) return;
   int64_t bit1 = tok_end * ng;
   if (tok_end == n_tok) bit1 = (bit1 + 31) & ~(int64_t)31;
@@ -274,10 +313,10 @@ __global__ void __launch_bounds__(kQuantBlock)
 // Prefill, KIVI keys: one block per (G-token group, head).
 __global__ void __launch_bounds__(kQuantBlock)
     kivi_key_prefill_kernel(Geometry g, CachePtrs p, const __half *K, int64_t T) {
-  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim];
+  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim], s_pmn[kKeyPart], s_pmx[kKeyPart];
   const int64_t bh = blockIdx.y;
   const int64_t t0 = (int64_t)blockIdx.x * g.k_group;
-  key_group_per_channel(g, p, bh, K + (bh * T + t0) * g.d, t0, s_scale, s_mn);
+  key_group_per_channel(g, p, bh, K + (bh * T + t0) * g.d, t0, s_scale, s_mn, s_pmn, s_pmx);
 }
 
 // fp16 row copy: rows [src0, src0 + n) of every head of X [B*H][T][d] into
@@ -304,7 +343,7 @@ __global__ void copy_rows_kernel(const __half *K, const __half *V, int64_t T, in
 __global__ void __launch_bounds__(kQuantBlock)
     kivi_append_kernel(Geometry g, CachePtrs p, const __half *k, const __half *v,
                        int64_t slot, int flush, int64_t n_quant) {
-  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim];
+  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim], s_pmn[kKeyPart], s_pmx[kKeyPart];
   const int64_t bh = blockIdx.x;
   const int d = g.d, R = g.residual;
   __half *kr = p.k_res + bh * R * d, *vr = p.v_res + bh * R * d;
@@ -316,7 +355,7 @@ __global__ void __launch_bounds__(kQuantBlock)
   __syncthreads();
   for (int grp = 0; grp < R / g.k_group; ++grp)
     key_group_per_channel(g, p, bh, kr + (int64_t)grp * g.k_group * d,
-                          n_quant + (int64_t)grp * g.k_group, s_scale, s_mn);
+                          n_quant + (int64_t)grp * g.k_group, s_scale, s_mn, s_pmn, s_pmx);
   const TokenDst dst = value_dst(g, p);
   const int chunks = d / 8, lanes = g.v_group / 8;
   const int items = R * chunks;
@@ -415,7 +454,8 @@ cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *
     if (n_quant > 0) {
       kivi_key_prefill_kernel<<<dim3((unsigned)(n_quant / g.k_group), (unsigned)BH), kQuantBlock, 0,
                                 st>>>(g, p, K, T);
-      per_token_prefill_kernel<<<dim3((unsigned)((n_quant + tpb - 1) / tpb), (unsigned)BH, 1),
+      per_token_prefill_kernel<<<dim3((unsigned)((n_quant + tpb * kTokIter - 1) / (tpb * kTokIter)),
+                                      (unsigned)BH, 1),
                                  kQuantBlock, 0, st>>>(g, p, K, V, T, 0, n_quant);
       n += 2;
     }
@@ -443,7 +483,8 @@ cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *
       ++n;
     }
     if (n_quant > 0) {
-      per_token_prefill_kernel<<<dim3((unsigned)((n_quant + tpb - 1) / tpb), (unsigned)BH, 2),
+      per_token_prefill_kernel<<<dim3((unsigned)((n_quant + tpb * kTokIter - 1) / (tpb * kTokIter)),
+                                      (unsigned)BH, 2),
                                  kQuantBlock, 0, st>>>(g, p, K, V, T, n_sink, n_quant);
       ++n;
     }
