@@ -169,6 +169,8 @@ int kvq_workspace_bytes(const kvq_config *cfg, size_t *bytes);
  * InnerQ ([INNERQ] 方法论 1-4): the first min(S, T) tokens go to the sink,
  *   the last min(W, T - S) to the window, the rest are quantized per token in
  *   groups of k_group / v_group channels with a per-group mode.
+ *   KVQ_INNERQ_KNORM: the per-channel key factors are computed first over all
+ *   T tokens and the quantized keys are normalized by them (see the scheme).
  * Errors: KVQ_EINVAL (null, T < 0), KVQ_ECAPACITY (T > max_ctx), KVQ_EALIGN,
  *   KVQ_EUNSUPPORTED, KVQ_ECUDA.
  */
@@ -181,8 +183,9 @@ int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t
  *   when the residual reaches R tokens the same launch quantizes all R of them
  *   to slots [n_quant, n_quant + R) and empties the residual.
  * InnerQ: the sink fills first, then the window; once the window holds W
- *   tokens its oldest token is quantized to slot n_quant and the new token
- *   takes its ring slot.
+ *   tokens its oldest token is quantized to slot n_quant (normalized by the
+ *   prompt's key factors under KVQ_INNERQ_KNORM) and the new token takes its
+ *   ring slot.
  * Errors: KVQ_EINVAL, KVQ_ECAPACITY (total tokens would exceed max_ctx),
  *   KVQ_EALIGN, KVQ_ECUDA.
  */
