@@ -76,6 +76,8 @@ def _declare(L):
     L.orc_prefill.argtypes = [ctypes.POINTER(_Head), P, P, ctypes.c_int64]
     L.orc_append.argtypes = [ctypes.POINTER(_Head), P, P]
     L.orc_attend.argtypes = [ctypes.POINTER(_Head), P, ctypes.c_double, P]
+    L.orc_attend_rope.argtypes = [ctypes.POINTER(_Head), P, ctypes.c_double, ctypes.c_double,
+                                  ctypes.c_int64, P]
     L.orc_pack.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P]
     L.orc_pack_modes.argtypes = [P, ctypes.c_int64, P]
     if not L.orc_rounding_is_nearest():
@@ -244,6 +246,17 @@ class OracleHead:
         out = np.zeros(self.d, np.float64)
         if lib().orc_attend(ctypes.byref(self._s), _ptr(q.view(np.uint16)), float(tau),
                             _ptr(out)) != 0:
+            raise MemoryError("oracle attention")
+        return out
+
+    def attend_rope(self, q, tau: float, base: float, pos0: int = 0) -> np.ndarray:
+        """fp64 attention output [d] over keys cached before the rotary
+        embedding: the j-th token held sits at position pos0 + j, the query
+        (pre-RoPE, [d] fp16) at pos0 + n - 1."""
+        q = _f16(q)
+        out = np.zeros(self.d, np.float64)
+        if lib().orc_attend_rope(ctypes.byref(self._s), _ptr(q.view(np.uint16)), float(tau),
+                                 float(base), int(pos0), _ptr(out)) != 0:
             raise MemoryError("oracle attention")
         return out
 

@@ -365,6 +365,92 @@ int orc_attend(const orc_head *s, const uint16_t *q, double tau, double *out) {
 }
 
 /*
+ * Rotary position embedding of one vector x ([d], fp64) at position p.  The
+ * pages say only that RoPE turns pairs of channels by position-dependent
+ * amounts ([KVQ2]); the rotation itself is RoFormer's, as LLaMA applies it:
+ * channels 2i and 2i+1 form pair i, turned counter-clockwise by the angle
+ * p * theta_i with theta_i = base^(-2i/d).
+ */
+static void rope_rotate(double *x, int d, double base, double p) {
+  for (int i = 0; i < d / 2; ++i) {
+    const int ca = 2 * i, cb = 2 * i + 1;
+    const double theta = pow(base, -2.0 * i / d);
+    const double c = cos(p * theta), sn = sin(p * theta);
+    const double a = x[ca], b = x[cb];
+    x[ca] = a * c - b * sn;
+    x[cb] = a * sn + b * c;
+  }
+}
+
+/*
+ * Key (k != 0) or value row of the j-th token the cache holds, in arrival
+ * order: the fp16 sinks, the quantized tokens (dequantized in fp64; a
+ * normalized key is multiplied back by its channel factor), then the fp16
+ * residual / window tokens, oldest first.
+ */
+static void token_row(const orc_head *s, int64_t j, int k, double *row) {
+  const int d = s->d;
+  if (j < s->n_sink_used) {
+    const uint16_t *src = (k ? s->k_sink : s->v_sink) + j * d;
+    for (int c = 0; c < d; ++c) row[c] = (double)orc_half_to_float(src[c]);
+    return;
+  }
+  j -= s->n_sink_used;
+  if (j < s->n_quant) {
+    for (int c = 0; c < d; ++c)
+      row[c] = k ? (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, j, c)
+                 : value_hat(s, j, c);
+    return;
+  }
+  j -= s->n_quant;
+  const uint16_t *src = (k ? s->k_res : s->v_res) + j * d;
+  for (int c = 0; c < d; ++c) row[c] = (double)orc_half_to_float(src[c]);
+}
+
+/*
+ * Decode attention over keys cached BEFORE the rotary position embedding
+ * ([KVQ2]: keys quantized pre-RoPE, the embedding applied after
+ * dequantization, at attention time).  The j-th token held (arrival order,
+ * as token_row) sits at position pos0 + j; the query belongs to the newest
+ * token, position pos0 + n - 1.  Every key and the query are rotated
+ * (rope_rotate) and then attended exactly as orc_attend does, in fp64.
+ * Returns 0, or -1 on allocation failure.
+ */
+int orc_attend_rope(const orc_head *s, const uint16_t *q, double tau, double base,
+                    int64_t pos0, double *out) {
+  const int d = s->d;
+  const int64_t n = s->n_sink_used + s->n_quant + s->n_resid;
+  for (int c = 0; c < d; ++c) out[c] = 0.0;
+  if (n == 0) return 0;
+  double *sc = (double *)malloc(sizeof(double) * (size_t)n);
+  double *qd = (double *)malloc(sizeof(double) * (size_t)d);
+  double *row = (double *)malloc(sizeof(double) * (size_t)d);
+  if (!sc || !qd || !row) { free(sc); free(qd); free(row); return -1; }
+  for (int c = 0; c < d; ++c) qd[c] = (double)orc_half_to_float(q[c]);
+  rope_rotate(qd, d, base, (double)(pos0 + n - 1));
+  for (int64_t j = 0; j < n; ++j) {
+    token_row(s, j, 1, row);
+    rope_rotate(row, d, base, (double)(pos0 + j));
+    double acc = 0.0;
+    for (int c = 0; c < d; ++c) acc += qd[c] * row[c];
+    sc[j] = tau * acc;
+  }
+  double m = sc[0];
+  for (int64_t j = 1; j < n; ++j) if (sc[j] > m) m = sc[j];
+  double l = 0.0;
+  for (int64_t j = 0; j < n; ++j) { sc[j] = exp(sc[j] - m); l += sc[j]; }
+  for (int64_t j = 0; j < n; ++j) {
+    token_row(s, j, 0, row);
+    for (int c = 0; c < d; ++c) out[c] += sc[j] * row[c];
+  }
+  for (int c = 0; c < d; ++c) out[c] /= l;
+  free(sc);
+  free(qd);
+  free(row);
+  return 0;
+}
+
+/*
  * Bit packing of code rows ([n_rows][d], one code per byte) into
  * [n_rows][d*bits/8] bytes: along the channels of a token, little-endian
  * within each byte, channel c at bits (c mod (8/bits))*bits of byte

@@ -12,6 +12,8 @@
  * Sources (page title, section):
  *   [KIVI]    "大模型量化技术原理：KIVI、IntactKV、KVQuant" (juejin), KIVI / 背景,
  *             为什么键和值缓存应该沿着不同的维度进行量化, 工作原理.
+ *   [KVQ2]    same page, KVQuant / 技术原理 二 (keys quantized before the rotary
+ *             position embedding, the embedding applied after dequantization).
  *   [KVQ5]    same page, KVQuant / 技术原理 五、Attention Sink 感知量化.
  *   [IKV]     same page, IntactKV / KV Cache量化 (fp16 part concatenated with
  *             the dequantized cache at inference time).
@@ -67,6 +69,8 @@ int orc_choose_symmetric(float mn, float mx, int bits);
 int orc_prefill(orc_head *s, const uint16_t *K, const uint16_t *V, int64_t T);
 int orc_append(orc_head *s, const uint16_t *k, const uint16_t *v);
 int orc_attend(const orc_head *s, const uint16_t *q, double tau, double *out);
+int orc_attend_rope(const orc_head *s, const uint16_t *q, double tau, double base,
+                    int64_t pos0, double *out);
 
 void orc_pack(const uint8_t *u, int64_t n_rows, int d, int bits, uint8_t *out);
 void orc_pack_modes(const uint8_t *sym, int64_t n, uint32_t *out);

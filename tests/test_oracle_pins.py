@@ -462,6 +462,105 @@ def pin_attention_error_bound():
         assert err > 0
 
 
+# --------------------------------------------------------------------------
+# keys cached before the rotary position embedding
+# --------------------------------------------------------------------------
+
+def _rope_sdpa(q, K, V, tau, base, pos0=0):
+    """Attention with RoPE in complex form, independent of the oracle's code:
+    channel pair (2i, 2i+1) is the complex number x_2i + 1j*x_2i+1, multiplied
+    by exp(1j * p * base^(-2i/d)) at position p; a score is Re(sum z_q conj(z_k)).
+    Token t sits at pos0 + t, the query at pos0 + T - 1 (T tokens)."""
+    d, T = q.size, K.shape[0]
+    theta = float(base) ** (-2.0 * np.arange(d // 2) / d)
+    pos = pos0 + np.arange(T, dtype=np.float64)
+    K64, q64 = K.astype(np.float64), q.astype(np.float64)
+    zk = (K64[:, 0::2] + 1j * K64[:, 1::2]) * np.exp(1j * np.outer(pos, theta))
+    zq = (q64[0::2] + 1j * q64[1::2]) * np.exp(1j * (pos0 + T - 1) * theta)
+    sc = tau * np.real(zk.conj() @ zq)
+    p = np.exp(sc - sc.max())
+    return (p / p.sum()) @ V.astype(np.float64)
+
+
+def pin_rope_closed_form():
+    """Three fp16 tokens at positions 0, 1, 2, base 100 (theta = 1, 0.1 for
+    d = 4), query (1, 0, 1, 0) at position 2: the scores are sin 2 (pair 0
+    turned by 2 rad), sin 0.1 (pair 1 turned by one step of 0.1 rad) and 1
+    (same position); one-hot values read the softmax weights back."""
+    h = oracle.OracleHead(4, 2, oracle.KIVI, 4, 4, 8, 0, 8)      # R > T: all fp16
+    K = np.array([[0, 1, 0, 0], [0, 0, 0, 1], [0, 0, 1, 0]], np.float16)
+    V = np.eye(3, 4).astype(np.float16)
+    h.prefill(K, V)
+    q = np.array([1, 0, 1, 0], np.float16)
+    for tau in (1.0, 0.7):
+        sc = tau * np.array([math.sin(2.0), math.sin(0.1), 1.0])
+        p = np.exp(sc - sc.max())
+        expect = np.append(p / p.sum(), 0.0)
+        np.testing.assert_allclose(h.attend_rope(q, tau, 100.0), expect, rtol=0, atol=1e-12)
+
+
+def pin_rope_grid_exact_kivi():
+    """Lossless KIVI cache (quantized tokens, a flush, then an fp16 residual):
+    RoPE attention equals the complex-form attention on the raw tokens."""
+    rng = np.random.default_rng(30)
+    d, G, Gv, R = 32, 8, 16, 16
+    K, V = _grid_tokens(rng, 80, d, 2, G, Gv)
+    Kx, Vx = _randn16(rng, 5, d), _randn16(rng, 5, d)
+    h = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 256)
+    h.prefill(K[:71], V[:71])
+    for i in range(71, 80):
+        h.append(K[i], V[i])
+    for i in range(5):
+        h.append(Kx[i], Vx[i])
+    assert h.n_quant == 80 and h.n_resid == 5
+    Kall, Vall = np.concatenate([K, Kx]), np.concatenate([V, Vx])
+    q = _randn16(rng, d)
+    tau = 1 / math.sqrt(d)
+    for base in (10000.0, 50.0):
+        np.testing.assert_allclose(h.attend_rope(q, tau, base), _rope_sdpa(q, Kall, Vall, tau, base),
+                                   rtol=0, atol=1e-11)
+
+
+def pin_rope_grid_exact_innerq():
+    """Lossless InnerQ cache with sinks, quantized tokens and a window that
+    has wrapped (tokens evicted into the quantized region by appends), with
+    and without the key normalization (power-of-two factors)."""
+    rng = np.random.default_rng(31)
+    d, S, W, T, n_app = 128, 4, 8, 60, 13
+    for k_norm in (False, True):
+        K, V = _grid_tokens(rng, T + n_app, d, 4, 1, 64, sym_groups=True)
+        if k_norm:
+            K[0] = np.repeat(np.float16([32, 128]), 64) * np.where(rng.integers(0, 2, d), 1, -1)
+        h = oracle.OracleHead(d, 4, oracle.INNERQ, 64, 64, W, S, 256, k_norm=k_norm)
+        h.prefill(K[:T], V[:T])
+        for i in range(T, T + n_app):
+            h.append(K[i], V[i])
+        assert h.n_quant == T + n_app - S - W and h.n_resid == W
+        q = _randn16(rng, d)
+        tau = 1 / math.sqrt(d)
+        np.testing.assert_allclose(h.attend_rope(q, tau, 10000.0),
+                                   _rope_sdpa(q, K, V, tau, 10000.0), rtol=0, atol=1e-11)
+
+
+def pin_rope_shift_invariance():
+    """Scores depend on positions only through their differences: moving
+    every token and the query by the same offset leaves the output unchanged
+    (random, lossy data: quantized, sink and window tokens)."""
+    rng = np.random.default_rng(32)
+    d = 64
+    K, V = _randn16(rng, 200, d), _randn16(rng, 200, d)
+    q = _randn16(rng, d)
+    for head in (oracle.OracleHead(d, 2, oracle.KIVI, 16, 32, 32, 0, 256),
+                 oracle.OracleHead(d, 4, oracle.INNERQ, 32, 32, 16, 3, 256)):
+        head.prefill(K[:180], V[:180])
+        for i in range(180, 200):
+            head.append(K[i], V[i])
+        a = head.attend_rope(q, 0.125, 10000.0)
+        b = head.attend_rope(q, 0.125, 10000.0, pos0=12345)
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-9)
+        assert np.abs(a - head.attend(q, 0.125)).max() > 1e-3   # RoPE does change it
+
+
 def pin_workload_shapes():
     """The named workloads have the shapes their descriptions give."""
     w = synth.WORKLOADS["llama2_7b_2bit"]
@@ -495,16 +594,30 @@ MUTANTS = [
      "return (double)s->v_u[t * d + c] * (double)s->v_scale[i];"),
     ("flush one early", "if (s->n_resid == R) {", "if (s->n_resid == R - 1) {"),
     ("prefill split by G", "const int64_t nq = T - T % R;", "const int64_t nq = T - T % G;"),
-    ("softmax sign", "sc[j] = exp(sc[j] - m);", "sc[j] = exp(m - sc[j]);"),
+    ("softmax sign", "sc[j] = exp(sc[j] - m); l += sc[j]; }\n\n  i = 0;",
+     "sc[j] = exp(m - sc[j]); l += sc[j]; }\n\n  i = 0;"),
+    ("rope softmax sign", "sc[j] = exp(sc[j] - m); l += sc[j]; }\n  for (int64_t j = 0; j < n; ++j) {\n    token_row",
+     "sc[j] = exp(m - sc[j]); l += sc[j]; }\n  for (int64_t j = 0; j < n; ++j) {\n    token_row"),
     ("tau dropped", "acc += qd[c] * (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, t, c);\n    sc[i] = tau * acc;",
      "acc += qd[c] * (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, t, c);\n    sc[i] = acc;"),
-    ("key factor not folded into q", "(s->k_normalize ? (double)s->k_norm[c] : 1.0)", "1.0"),
+    ("key factor not folded into q", "acc += qd[c] * (s->k_normalize ? (double)s->k_norm[c] : 1.0)",
+     "acc += qd[c] * 1.0"),
     ("key factor over the quantized tokens only", "for (int64_t t = 0; t < T; ++t) {\n      const float x = fabsf",
      "for (int64_t t = s->n_sink < T ? s->n_sink : T; t < T; ++t) {\n      const float x = fabsf"),
     ("zero channel factor 0", "s->k_norm[c] = a > 0.0f ? a : 1.0f;", "s->k_norm[c] = a;"),
     ("big-endian pack", "<< ((c % per) * bits)", "<< ((per - 1 - c % per) * bits)"),
     ("evict newest", "innerq_quant_kv(s, s->k_res, s->v_res, s->n_quant);", "innerq_quant_kv(s, k, v, s->n_quant);"),
     ("half exponent bias", "expo - 25", "expo - 24"),
+    ("rope query one position late", "rope_rotate(qd, d, base, (double)(pos0 + n - 1));",
+     "rope_rotate(qd, d, base, (double)(pos0 + n));"),
+    ("rope pairs as halves", "const int ca = 2 * i, cb = 2 * i + 1;", "const int ca = i, cb = i + d / 2;"),
+    ("rope keys turned backwards", "rope_rotate(row, d, base, (double)(pos0 + j));",
+     "rope_rotate(row, d, base, -(double)(pos0 + j));"),
+    ("rope theta exponent", "pow(base, -2.0 * i / d)", "pow(base, -1.0 * i / d)"),
+    ("rope key factor dropped", "row[c] = k ? (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, j, c)",
+     "row[c] = k ? key_hat(s, j, c)"),
+    ("rope window newest first", "const uint16_t *src = (k ? s->k_res : s->v_res) + j * d;",
+     "const uint16_t *src = (k ? s->k_res : s->v_res) + (s->n_resid - 1 - j) * d;"),
     ("value group transposed", "x[i] = orc_half_to_float(src[j * Gv + i]);", "x[i] = orc_half_to_float(src[i * (d / Gv) + j]);"),
 ]
 
