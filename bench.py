@@ -135,10 +135,14 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def decode_source_sha():
+DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode_tc.cu", "kvq_decode_gqa.cu", "kvq_tc_common.cuh",
+                  "kvq_internal.cuh")
+ROPE_SOURCES = ("kvq_rope.cu", "kvq_rope.cuh", "kvq_internal.cuh")
+
+
+def decode_source_sha(names=DECODE_SOURCES):
     h = hashlib.sha256()
-    for name in ("kvq_decode.cu", "kvq_decode_tc.cu", "kvq_decode_gqa.cu", "kvq_tc_common.cuh",
-                 "kvq_internal.cuh"):
+    for name in names:
         if not os.path.exists(os.path.join(ROOT, "bit_kv_cache_14_gb300", "csrc", name)):
             continue
         with open(os.path.join(ROOT, "bit_kv_cache_14_gb300", "csrc", name), "rb") as f:
@@ -159,17 +163,19 @@ def decode_kernel_name(w):
     return "decode_kernel"
 
 
-def profiled_traffic(workload, per_launch_units):
+def profiled_traffic(workload, per_launch_units, rope=False):
     """DRAM bytes per decode launch from the committed ncu summary, or None when
     the kernel source changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "decode_%s.md" % workload)
+    path = os.path.join(ROOT, "profiles", ("decode_rope_%s.md" if rope else "decode_%s.md")
+                        % workload)
     try:
         text = open(path).read()
     except OSError:
         return None
     sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
     tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not sha or not tb or sha.group(1) != decode_source_sha():
+    if not sha or not tb or sha.group(1) != decode_source_sha(ROPE_SOURCES if rope
+                                                             else DECODE_SOURCES):
         return None
     return float(tb.group(1))
 
@@ -337,12 +343,19 @@ def run_gpu(args, w, rank, world):
         for c, st in zip(caches, states):
             c.view.n_quant, c.view.n_resid, c.view.n_sink, c.view.ring_head = st
 
+    rope = args.rope_base
+
     def step(i):
         """One decode step (append + attend); returns the kernels it launched."""
         c = i % copies
         e = (i // copies) % EPOCH
-        caches[c].append_decode(ks[e], vs[e], qs[e % 8], outs[c], scale, stream)
-        return caches[c].last_launch_count()
+        if rope is None:
+            caches[c].append_decode(ks[e], vs[e], qs[e % 8], outs[c], scale, stream)
+            return caches[c].last_launch_count()
+        caches[c].append(ks[e], vs[e], stream)
+        n = caches[c].last_launch_count()
+        caches[c].decode_rope(qs[e % 8], rope, outs[c], scale, stream)
+        return n + caches[c].last_launch_count()
 
     # per-step algorithmic bytes over one epoch (identical for every copy)
     if w.scheme == synth.KIVI:
@@ -421,7 +434,10 @@ def run_gpu(args, w, rank, world):
     dgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(dgraph, stream=stream):
         for i in range(M):
-            caches[i % copies].decode(qs[i % 8], outs[i % copies], scale, stream)
+            if rope is None:
+                caches[i % copies].decode(qs[i % 8], outs[i % copies], scale, stream)
+            else:
+                caches[i % copies].decode_rope(qs[i % 8], rope, outs[i % copies], scale, stream)
     with torch.cuda.stream(stream):
         dgraph.replay()
         stream.synchronize()
@@ -462,18 +478,30 @@ def run_gpu(args, w, rank, world):
     h_q = qs.cpu().pin_memory()
     h_out = torch.empty(qs.shape[1:], dtype=torch.float32).pin_memory()
     n_e2e = min(EPOCH, max(K_steps, 16))
-    with torch.cuda.stream(stream):
-        for i in range(8):  # warm-up
+
+    def host_step(i):
+        if rope is None:
             c0.decode_step_host(h_k[i], h_v[i], h_q[i % 8], h_out, d_k, d_v, d_q, d_out, scale,
                                 stream)
+            return
+        # the same copies around the binding's calls: pinned host in, host result out
+        d_k.copy_(h_k[i], non_blocking=True)
+        d_v.copy_(h_v[i], non_blocking=True)
+        d_q.copy_(h_q[i % 8], non_blocking=True)
+        c0.append(d_k, d_v, stream)
+        c0.decode_rope(d_q, rope, d_out, scale, stream)
+        h_out.copy_(d_out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(8):  # warm-up
+            host_step(i)
         stream.synchronize()
         restore()
         x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         x0.record(stream)
         e2e_bytes = 0
         for i in range(n_e2e):
-            c0.decode_step_host(h_k[i], h_v[i], h_q[i % 8], h_out, d_k, d_v, d_q, d_out, scale,
-                                stream)
+            host_step(i)
             e2e_bytes += ep_bytes[i]
         x1.record(stream)
     x1.synchronize()
@@ -499,6 +527,9 @@ def main():
     ap.add_argument("--workload", default="llama2_7b_2bit", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--skip-cpu", action="store_true", help="omit the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--rope-base", type=float, default=None,
+                    help="time the variant whose keys are cached before the rotary embedding "
+                         "(kvq_decode_attention_rope with this base) instead of the plain decode")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     args.warmup = max(3, args.warmup)
@@ -510,6 +541,9 @@ def main():
               "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "ctx": w.ctx, "bits": w.bits,
               "k_group": w.k_group, "v_group": w.v_group, "residual": w.residual,
               "n_sink": w.n_sink, "appends_per_epoch": EPOCH}
+    if args.rope_base is not None:
+        config["variant"] = ("keys cached before the rotary embedding (base %g), rotated inside "
+                             "the decode kernel" % args.rope_base)
 
     if args.impl == "reference":
         if rank != 0:
@@ -540,7 +574,8 @@ def main():
     elapsed_ms = float(elapsed.item())
     value = r["total_bytes"] * world / (elapsed_ms * 1e-3) / 1e9
     decode_gbs = r["dstate_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
-    traffic = profiled_traffic(w.name, 1)
+    rope = args.rope_base is not None
+    traffic = profiled_traffic(w.name, 1, rope=rope)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": r["warmup_steps"], "ms_per_step": elapsed_ms / args.steps,
@@ -557,7 +592,8 @@ def main():
         "us_per_step": elapsed_ms / args.steps * 1e3,
         "roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": peak, "unit": "GB/s",
                      "frac": decode_gbs / peak, "traffic": traffic,
-                     "kernel": decode_kernel_name(w), "kernel_us": r["decode_ms"] * 1e3,
+                     "kernel": "rope_decode_kernel" if rope else decode_kernel_name(w),
+                     "kernel_us": r["decode_ms"] * 1e3,
                      "algorithmic_bytes_per_launch": r["dstate_bytes"],
                      "peak_kind": peak_kind},
         "plain_launch_us_per_step": r["plain_ms"] * 1e3,
@@ -569,7 +605,7 @@ def main():
         "gpu_launches": r["timed_launches"],
         "clocks": r["clocks"],
     }
-    if rank == 0 and world == 1 and not args.skip_cpu:
+    if rank == 0 and world == 1 and not args.skip_cpu and not rope:
         rate, threads, desc, _ = oracle_decode_rate(w, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate / 1e9, "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": desc}

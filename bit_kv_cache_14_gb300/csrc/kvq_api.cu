@@ -2,7 +2,10 @@
 // Declarations and contracts: include/kvq.h.
 #include <string.h>
 
+#include <math.h>
+
 #include "kvq_internal.cuh"
+#include "kvq_rope.cuh"
 
 namespace kvq {
 
@@ -259,6 +262,29 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
                               cache->n_sink, cache->ring_head,
                               reinterpret_cast<const __half *>(q), out, softmax_scale, ws,
                               num_sms_cached(), static_cast<cudaStream_t>(stream)));
+  if (r != KVQ_OK) return r;
+  note_launch(1);
+  return KVQ_OK;
+}
+
+int kvq_decode_attention_rope(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
+                              float *out, float softmax_scale, double rope_base, void *ws,
+                              size_t ws_bytes, void *stream) {
+  Geometry g;
+  int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if (!q || !out || !ws) return KVQ_EINVAL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(ws)) return KVQ_EALIGN;
+  if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
+  if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
+  if (!(rope_base > 0.0) || !isfinite(rope_base)) return KVQ_EINVAL;
+  if (!rope_group_supported(g.Hq / g.H) || g.max_ctx > kRopeMaxPositions) return KVQ_EUNSUPPORTED;
+  r = from_cuda(launch_decode_rope(g, ptrs_of(g, cache), cache->n_quant, cache->n_resid,
+                                   cache->n_sink, cache->ring_head,
+                                   reinterpret_cast<const __half *>(q), out, softmax_scale,
+                                   rope_base, ws, num_sms_cached(),
+                                   static_cast<cudaStream_t>(stream)));
   if (r != KVQ_OK) return r;
   note_launch(1);
   return KVQ_OK;

@@ -34,7 +34,7 @@ EXPORTS = (
     "kvq_cache_sizes", "kvq_workspace_bytes", "kvq_quantize_prefill", "kvq_append",
     "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
     "kvq_last_launch_count", "kvq_strerror", "kvq_debug_stall_waits",
-    "kvq_decode_attention_noalloc", "kvq_append_decode",
+    "kvq_decode_attention_noalloc", "kvq_append_decode", "kvq_decode_attention_rope",
 )
 
 
@@ -84,6 +84,8 @@ def lib():
             L.kvq_decode_attention.argtypes = [C, CA, P, P, ctypes.c_float, P, ctypes.c_size_t, P]
             L.kvq_decode_step_host.argtypes = [C, CA, P, P, P, P, P, P, P, P, ctypes.c_float, P,
                                                ctypes.c_size_t, P]
+            L.kvq_decode_attention_rope.argtypes = [C, CA, P, P, ctypes.c_float, ctypes.c_double,
+                                                    P, ctypes.c_size_t, P]
             L.kvq_decode_attention_noalloc.argtypes = [C, CA, P, P, ctypes.c_float, P]
             L.kvq_append_decode.argtypes = [C, CA, P, P, P, P, ctypes.c_float, P,
                                             ctypes.c_size_t, P]
@@ -200,6 +202,23 @@ class QuantizedKVCache:
                                           _ptr(q), _ptr(out), float(scale), self.ws.data_ptr(),
                                           self.ws_bytes, _stream(stream)),
                "kvq_decode_attention")
+        return out
+
+    def decode_rope(self, q: torch.Tensor, base: float = 10000.0, out: torch.Tensor | None = None,
+                    scale: float | None = None, stream=None) -> torch.Tensor:
+        """Attention over keys cached before the rotary embedding: q (fp16
+        [B][Hq][d], un-rotated) belongs to the newest token; every key is
+        rotated by its position inside the kernel.  Returns fp32 [B][Hq][d]."""
+        assert q.dtype == torch.float16
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.cfg.head_dim)
+        _check(lib().kvq_decode_attention_rope(ctypes.byref(self.cfg), ctypes.byref(self.view),
+                                               _ptr(q), _ptr(out), float(scale), float(base),
+                                               self.ws.data_ptr(), self.ws_bytes,
+                                               _stream(stream)),
+               "kvq_decode_attention_rope")
         return out
 
     def append_decode(self, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,

@@ -210,6 +210,28 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
                          void *stream);
 
 /*
+ * Decode attention over keys cached BEFORE the rotary position embedding
+ * ("大模型量化技术原理：KIVI、IntactKV、KVQuant", KVQuant / 技术原理 二: keys
+ * are quantized pre-RoPE, and the embedding is applied after dequantization
+ * inside the q.K^T kernel).  The cache holds the keys exactly as they were
+ * given to kvq_quantize_prefill / kvq_append (un-rotated); q is un-rotated
+ * too.  RoPE (RoFormer's rotation; the pages do not spell it out): channels
+ * 2i and 2i+1 of a vector at position p are turned counter-clockwise by the
+ * angle p * theta_i, theta_i = rope_base^(-2i/d).  Positions: the tokens held
+ * are numbered 0, 1, ... in arrival order (sinks, quantized tokens,
+ * residual / window oldest first), and q belongs to the newest token.
+ *   out = softmax(softmax_scale * RoPE(q) . RoPE(K)^T) V, fp32, as
+ *   kvq_decode_attention (values are not rotated; an empty cache gives zeros).
+ *   ws: the decode scratch (kvq_workspace_bytes; zero-filled, left zero).
+ * Errors: as kvq_decode_attention; KVQ_EINVAL for rope_base <= 0 or not
+ *   finite; KVQ_EUNSUPPORTED for n_q_heads / n_kv_heads = 8 or max_ctx > 2^24
+ *   (positions are exact in fp32).
+ */
+int kvq_decode_attention_rope(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
+                              float *out, float softmax_scale, double rope_base, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/*
  * One decode step on device buffers: kvq_append(k, v) then
  * kvq_decode_attention(q) with the same arguments, results and errors.  When
  * the append only stores the new token (KIVI without a flush) and the decode

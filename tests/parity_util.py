@@ -88,12 +88,16 @@ def check_head_state(cache, w, b, h, head):
     assert np.array_equal(vr.view(np.uint16), vr_o.view(np.uint16)), "value residual differs"
 
 
-def check_decode(out, q, w, b, h, head, tau):
-    """Attention output of the query heads of KV head (b, h) vs the oracle."""
+def check_decode(out, q, w, b, h, head, tau, rope_base=None):
+    """Attention output of the query heads of KV head (b, h) vs the oracle
+    (keys cached before the rotary embedding when rope_base is given)."""
     rg = w.group_ratio
     worst = 0.0
     for hq in range(h * rg, (h + 1) * rg):
-        exp = head.attend(q[b, hq], tau)
+        if rope_base is None:
+            exp = head.attend(q[b, hq], tau)
+        else:
+            exp = head.attend_rope(q[b, hq], tau, rope_base)
         got = out[b, hq].astype(np.float64)
         err = float(np.max(np.abs(got - exp)))
         worst = max(worst, err)
@@ -102,9 +106,11 @@ def check_decode(out, q, w, b, h, head, tau):
 
 
 def run_workload(w, heads=None, n_append=None, decode_every=None, max_ctx=None,
-                 check_steps=None):
+                 check_steps=None, rope_base=None):
     """Prefill + appends + decodes on the GPU; oracle on `heads` (default: all).
-    Returns the worst attention error seen."""
+    With rope_base, the decodes are kvq_decode_attention_rope (keys and
+    queries cached / given before the rotary embedding).  Returns the worst
+    attention error seen."""
     n_append = w.n_append if n_append is None else n_append
     max_ctx = w.ctx + n_append if max_ctx is None else max_ctx
     if heads is None:
@@ -132,9 +138,11 @@ def run_workload(w, heads=None, n_append=None, decode_every=None, max_ctx=None,
                 ho.append(Ks[s - 1, b, h], Vs[s - 1, b, h])
         if s in steps:
             q = synth.queries(w, s)
-            out = cache.decode(torch.from_numpy(q).cuda()).cpu().numpy()
+            qd = torch.from_numpy(q).cuda()
+            out = (cache.decode(qd) if rope_base is None
+                   else cache.decode_rope(qd, rope_base)).cpu().numpy()
             for (b, h), ho in heads_o.items():
                 check_head_state(cache, w, b, h, ho)
-                worst = max(worst, check_decode(out, q, w, b, h, ho, tau))
+                worst = max(worst, check_decode(out, q, w, b, h, ho, tau, rope_base))
     assert cache.device_status() == 0
     return worst
