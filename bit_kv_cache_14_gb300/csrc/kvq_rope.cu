@@ -26,11 +26,16 @@
 // three-part constant (W. J. Cody, W. Waite, "Software Manual for the
 // Elementary Functions", 1980), and its cosine and sine come from __sincosf
 // of the reduced angle (|error| ~ 1e-6 rad in all).
-// Values are not rotated.  Work split: one block per (split, KV head); each
-// split is a range of quantized tokens, plus one split for the fp16 sink /
-// residual / window tokens (each with its own angle); the block's last
-// finisher merges the splits' (m, l, o) by log-sum-exp (IntactKV / KV
-// Cache量化 on the same page: fp16 tokens joined with the dequantized ones).
+// Values are not rotated; their codes use the same in-place conversion, the
+// power of two applied once to each accumulator at the end.
+// Work split: one block per (split, KV head); the quantized tokens are cut
+// into splits so that one wave of blocks fills every SM (blocks per SM from
+// the occupancy calculator), plus one split for the fp16 sink / residual /
+// window tokens (each with its own angle).  Each warp loads its sub-tile's
+// code rows before computing the sub-tile's weights, so the two loads'
+// latencies overlap.  The block that finishes a head last merges the splits'
+// (m, l, o) by log-sum-exp (IntactKV / KV Cache量化 on the same page: fp16
+// tokens joined with the dequantized ones).
 #include <math.h>
 
 #include "kvq_rope.cuh"
@@ -42,8 +47,9 @@ namespace {
 constexpr int kRBlock = 256;            // threads per block
 constexpr int kRWarps = kRBlock / 32;
 constexpr int kSub = 32;                // tokens per sub-tile: one per lane
-constexpr int kRChunkAlign = 256;       // quantized tokens per split: a multiple of this
+constexpr int kRChunkMin = 128;         // quantized tokens per split: at least this
 constexpr int kRChunkCap = 2048;        // ... and at most this
+constexpr int kRBlockFixed = 128;       // a block's fixed work, in token-equivalents
 constexpr float kInvTwoPi = 0.15915494309189535f;
 
 struct RopeArgs {
@@ -130,8 +136,13 @@ __device__ __forceinline__ void block_reduce(float (&v)[RG], bool is_max, float 
   __syncthreads();
 }
 
+// One query head per KV head (KIVI): registers capped so five blocks fit an SM.
+template <int RG, int SCHEME>
+constexpr int rope_min_blocks() { return (RG == 1 && SCHEME == KVQ_KIVI) ? 5 : 1; }
+
 template <int D, int BITS, int RG, int SCHEME>
-__global__ void __launch_bounds__(kRBlock) rope_decode_kernel(const RopeArgs a) {
+__global__ void __launch_bounds__(kRBlock, rope_min_blocks<RG, SCHEME>())
+    rope_decode_kernel(const RopeArgs a) {
   extern __shared__ float4 smem4[];
   float *smem = reinterpret_cast<float *>(smem4);
   constexpr int P = D / 2;              // channel pairs
@@ -219,6 +230,22 @@ __global__ void __launch_bounds__(kRBlock) rope_decode_kernel(const RopeArgs a) 
     for (int st = wid; st < n_sub; st += kRWarps) {
       const int64_t tb = t0 + (int64_t)st * kSub;
       const float delta0 = (float)(a.qpos - (pos_base + tb));
+      // the lane's code row is loaded first, so its latency overlaps the
+      // key statistics' and the weights' computation
+      const int j = lane;
+      const bool live = tb + j < t0 + n_tok;
+      uint32_t wd[NW];
+      if (live) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(code_row(g, a.p, bh, tb + j, 0));
+#pragma unroll
+        for (int v = 0; v < NW / 4; ++v) {
+          const uint4 x = row[v];
+          wd[4 * v] = x.x;
+          wd[4 * v + 1] = x.y;
+          wd[4 * v + 2] = x.z;
+          wd[4 * v + 3] = x.w;
+        }
+      }
       // per-pair weights of the anchor query A = R(delta0) q
 #pragma unroll
       for (int pp = 0; pp < (P + 31) / 32; ++pp) {
@@ -256,19 +283,8 @@ __global__ void __launch_bounds__(kRBlock) rope_decode_kernel(const RopeArgs a) 
         }
       }
       __syncwarp();
-      const int j = lane;
-      if (tb + j < t0 + n_tok) {
+      if (live) {
         const int64_t t = tb + j;
-        const uint4 *row = reinterpret_cast<const uint4 *>(code_row(g, a.p, bh, t, 0));
-        uint32_t wd[NW];
-#pragma unroll
-        for (int v = 0; v < NW / 4; ++v) {
-          const uint4 x = row[v];
-          wd[4 * v] = x.x;
-          wd[4 * v + 1] = x.y;
-          wd[4 * v + 2] = x.z;
-          wd[4 * v + 3] = x.w;
-        }
         const int gi = NGS > 1 ? (j >> lgk) : 0;
         const float4 *wt = w_me + gi * RG * P;
         const float2 *zt = z_me + gi * RG * P;
@@ -387,24 +403,43 @@ __global__ void __launch_bounds__(kRBlock) rope_decode_kernel(const RopeArgs a) 
       }
     }
   } else {
+    // Codes stay in place in their 16-bit half: acc[h][k] collects
+    // p * scale * (code << offset_k), and the power of two comes out once at
+    // the end.  Split starts are multiples of the 32-token block.
     const int ngv = D / g.v_group;
     const int gv = (8 * jc) / g.v_group;
-    for (int64_t i = tl; i < n_tok; i += TL) {
-      const int64_t t = t0 + i;
-      const uint8_t *row = code_row(g, a.p, bh, t, g.blk_vc);
-      const uint32_t word = BITS == 2 ? (uint32_t)reinterpret_cast<const uint16_t *>(row)[jc]
-                                      : reinterpret_cast<const uint32_t *>(row)[jc];
-      const float vs = tok_meta(g, a.p, bh, t, g.blk_vs, ngv)[gv];
-      const float vz = tok_meta(g, a.p, bh, t, g.blk_vz, ngv)[gv];
+    for (int64_t bt = 0; bt < n_tok; bt += kBlockTokens) {
+      const uint8_t *blk = tok_block(g, a.p, bh, t0 + bt);
+      const uint8_t *vrow = blk + g.blk_vc;
+      const float *vsr = reinterpret_cast<const float *>(blk + g.blk_vs);
+      const float *vzr = reinterpret_cast<const float *>(blk + g.blk_vz);
+      for (int r = tl; r < kBlockTokens; r += TL) {
+        if (bt + r >= n_tok) break;
+        const uint8_t *row = vrow + r * g.row_bytes;
+        const uint32_t word = BITS == 2 ? (uint32_t)reinterpret_cast<const uint16_t *>(row)[jc]
+                                        : reinterpret_cast<const uint32_t *>(row)[jc];
+        const float vs = vsr[r * ngv + gv];
+        const float vz = vzr[r * ngv + gv];
+        float cv[8];
 #pragma unroll
-      for (int hh = 0; hh < RG; ++hh) {
-        const float pv = sc[hh * a.sc_max + i];
-        const float ps = pv * vs;
-        zacc[hh] += pv * vz;
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t half = (k * BITS) >= 16 ? word >> 16 : word;
+          cv[k] = small_uint_to_float(half & (kMask << ((k * BITS) & 15)));
+        }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) acc[hh][k] += ps * (float)((word >> (k * BITS)) & kMask);
+        for (int hh = 0; hh < RG; ++hh) {
+          const float pv = sc[hh * a.sc_max + bt + r];
+          const float ps = pv * vs;
+          zacc[hh] = fmaf(pv, vz, zacc[hh]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[hh][k] = fmaf(ps, cv[k], acc[hh][k]);
+        }
       }
     }
+#pragma unroll
+    for (int hh = 0; hh < RG; ++hh)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[hh][k] *= __int_as_float((127 - ((k * BITS) & 15)) << 23);
   }
   // reduce the TL token lanes through shared memory (the weights are dead)
   __syncthreads();
@@ -470,32 +505,71 @@ __global__ void __launch_bounds__(kRBlock) rope_decode_kernel(const RopeArgs a) 
   if (tid == 0) a.ws_cnt[bh] = 0;
 }
 
+// Splits over the quantized tokens, plus the fp16 split.  A split's block
+// costs about its tokens plus a fixed part (kRBlockFixed token-equivalents:
+// the cos / sin table, the reductions, the partial row); blocks run in waves
+// of per_sm * num_sms, so the plan minimises waves * (chunk + fixed) over the
+// number of splits.  chunk: a multiple of 32 tokens (sub-tiles and blocks
+// start aligned), at least kRChunkMin (the partial slots per head suffice),
+// at most kRChunkCap (the score buffer).
+void plan_rope(RopeArgs &a, int per_sm, int num_sms) {
+  const int64_t BH = (int64_t)a.g.B * a.g.H;
+  const int64_t slots = (int64_t)per_sm * num_sms;
+  int64_t chunk = kRChunkMin, best = -1;
+  const int64_t s0 = (a.n_quant + kRChunkCap - 1) / kRChunkCap;
+  for (int64_t s = s0 > 0 ? s0 : 1; s < s0 + 64; ++s) {
+    int64_t c = (a.n_quant + s - 1) / s;
+    c = (c + kSub - 1) / kSub * kSub;
+    if (c < kRChunkMin) c = kRChunkMin;
+    if (c > kRChunkCap) continue;
+    const int64_t ns = (a.n_quant + c - 1) / c;
+    const int64_t cost = ((BH * ns + slots - 1) / slots) * (c + kRBlockFixed);
+    if (best < 0 || cost < best) {
+      best = cost;
+      chunk = c;
+    }
+  }
+  a.chunk = chunk;
+  a.n_qsplit = (int)((a.n_quant + chunk - 1) / chunk);
+  a.n_split = a.n_qsplit + (a.n_resid + a.n_sink > 0 ? 1 : 0);
+  if (a.n_split == 0) a.n_split = 1;  // empty cache: one empty split writes zeros
+}
+
 template <int D, int BITS, int RG, int SCHEME>
-cudaError_t launch_t(const RopeArgs &a, int smem_bytes, cudaStream_t st) {
-  static int configured = 0;
+cudaError_t launch_t(RopeArgs a, int smem_bytes, int num_sms, cudaStream_t st) {
+  static int configured = 0, occ_smem = -1, per_sm = 1;
   if (configured < smem_bytes) {
     cudaError_t e = cudaFuncSetAttribute(rope_decode_kernel<D, BITS, RG, SCHEME>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     configured = smem_bytes;
   }
+  if (occ_smem != smem_bytes) {
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &n, rope_decode_kernel<D, BITS, RG, SCHEME>, kRBlock, smem_bytes);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+    occ_smem = smem_bytes;
+  }
+  plan_rope(a, per_sm, num_sms);
   rope_decode_kernel<D, BITS, RG, SCHEME>
       <<<dim3((unsigned)a.n_split, (unsigned)(a.g.B * a.g.H)), kRBlock, smem_bytes, st>>>(a);
   return cudaGetLastError();
 }
 
 template <int D, int BITS, int RG>
-cudaError_t launch_s(const RopeArgs &a, int smem, cudaStream_t st) {
-  return a.g.scheme == KVQ_KIVI ? launch_t<D, BITS, RG, KVQ_KIVI>(a, smem, st)
-                                : launch_t<D, BITS, RG, KVQ_INNERQ>(a, smem, st);
+cudaError_t launch_s(const RopeArgs &a, int smem, int num_sms, cudaStream_t st) {
+  return a.g.scheme == KVQ_KIVI ? launch_t<D, BITS, RG, KVQ_KIVI>(a, smem, num_sms, st)
+                                : launch_t<D, BITS, RG, KVQ_INNERQ>(a, smem, num_sms, st);
 }
 
 template <int D, int BITS>
-cudaError_t launch_r(const RopeArgs &a, int rg, int smem, cudaStream_t st) {
+cudaError_t launch_r(const RopeArgs &a, int rg, int smem, int num_sms, cudaStream_t st) {
   switch (rg) {
-    case 1: return launch_s<D, BITS, 1>(a, smem, st);
-    case 2: return launch_s<D, BITS, 2>(a, smem, st);
-    case 4: return launch_s<D, BITS, 4>(a, smem, st);
+    case 1: return launch_s<D, BITS, 1>(a, smem, num_sms, st);
+    case 2: return launch_s<D, BITS, 2>(a, smem, num_sms, st);
+    case 4: return launch_s<D, BITS, 4>(a, smem, num_sms, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -519,18 +593,7 @@ cudaError_t launch_decode_rope(const Geometry &g, const CachePtrs &p, int64_t n_
   a.n_sink = n_sink;
   a.ring_head = ring_head;
   a.qpos = n_sink + n_quant + n_resid - 1;
-  // splits: about three blocks per SM over the quantized tokens, plus the fp16 split
   const int64_t BH = (int64_t)g.B * g.H;
-  int64_t want = (3LL * num_sms + BH - 1) / BH;
-  if (want < 1) want = 1;
-  int64_t chunk = (n_quant + want - 1) / want;
-  chunk = (chunk + kRChunkAlign - 1) / kRChunkAlign * kRChunkAlign;
-  if (chunk < kRChunkAlign) chunk = kRChunkAlign;
-  if (chunk > kRChunkCap) chunk = kRChunkCap;
-  a.chunk = chunk;
-  a.n_qsplit = (int)((n_quant + chunk - 1) / chunk);
-  a.n_split = a.n_qsplit + (n_resid + n_sink > 0 ? 1 : 0);
-  if (a.n_split == 0) a.n_split = 1;  // empty cache: one empty split writes zeros
   a.s_max = part_slots(g);
   a.sc_max = kRChunkCap > g.residual + g.n_sink ? kRChunkCap : g.residual + g.n_sink;
   // theta_i = base^(-2i/d) as hi + lo; 2 pi in three parts
@@ -552,9 +615,10 @@ cudaError_t launch_decode_rope(const Geometry &g, const CachePtrs &p, int64_t n_
   a.ws_o = a.ws_ml + parts * 2;
   const int ngs = (g.scheme == KVQ_KIVI && g.k_group < kSub) ? kSub / g.k_group : 1;
   const int smem = rope_smem(g.d, rg, ngs, a.sc_max).total * (int)sizeof(float);
-  if (g.d == 64) return g.bits == 2 ? launch_r<64, 2>(a, rg, smem, st)
-                                    : launch_r<64, 4>(a, rg, smem, st);
-  return g.bits == 2 ? launch_r<128, 2>(a, rg, smem, st) : launch_r<128, 4>(a, rg, smem, st);
+  if (g.d == 64) return g.bits == 2 ? launch_r<64, 2>(a, rg, smem, num_sms, st)
+                                    : launch_r<64, 4>(a, rg, smem, num_sms, st);
+  return g.bits == 2 ? launch_r<128, 2>(a, rg, smem, num_sms, st)
+                     : launch_r<128, 4>(a, rg, smem, num_sms, st);
 }
 
 }  // namespace kvq
