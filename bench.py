@@ -181,6 +181,26 @@ def profiled_traffic(workload, per_launch_units, rope=False):
 
 
 # ---------------------------------------------------------------------------
+# whole-job figures over ranks (one process per GPU, weak scaling)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(values, world, device):
+    """Each rank's timings -> their maxima over all ranks (one all_reduce MAX;
+    NCCL on the GPUs, gloo in the CPU tests)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(bytes_per_rank, world, elapsed_ms):
+    """Every rank streams bytes_per_rank (replicas: per-GPU work fixed as N
+    grows); the job lasts as long as its slowest rank."""
+    return bytes_per_rank * world / (elapsed_ms * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 
@@ -568,11 +588,8 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl")
     r = run_gpu(args, w, rank, world)
-    elapsed = torch.tensor([r["elapsed_ms"]], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(elapsed, op=torch.distributed.ReduceOp.MAX)
-    elapsed_ms = float(elapsed.item())
-    value = r["total_bytes"] * world / (elapsed_ms * 1e-3) / 1e9
+    elapsed_ms, e2e_ms = max_over_ranks([r["elapsed_ms"], r["e2e_ms"]], world, "cuda")
+    value = whole_job_gbs(r["total_bytes"], world, elapsed_ms)
     decode_gbs = r["dstate_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
     rope = args.rope_base is not None
     traffic = profiled_traffic(w.name, 1, rope=rope)
@@ -599,9 +616,9 @@ def main():
         "plain_launch_us_per_step": r["plain_ms"] * 1e3,
         "prefill": {"ms": r["prefill_ms"], "bytes_in": r["prompt_bytes_in"],
                     "gbs_in": r["prompt_bytes_in"] / (r["prefill_ms"] * 1e-3) / 1e9},
-        "e2e": {"value": r["e2e_bytes"] / (r["e2e_ms"] * 1e-3) / 1e9 * world, "unit": "GB/s",
+        "e2e": {"value": whole_job_gbs(r["e2e_bytes"], world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                "us_per_step": r["e2e_ms"] / r["n_e2e"] * 1e3, "steps": r["n_e2e"]},
+                "us_per_step": e2e_ms / r["n_e2e"] * 1e3, "steps": r["n_e2e"]},
         "gpu_launches": r["timed_launches"],
         "clocks": r["clocks"],
     }
