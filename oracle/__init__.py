@@ -61,6 +61,7 @@ class _Head(ctypes.Structure):
         ("k_res", ctypes.c_void_p), ("v_res", ctypes.c_void_p),
         ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p),
         ("k_norm", ctypes.c_void_p),
+        ("v_queue", ctypes.c_int32), ("n_vquant", ctypes.c_int64),
     ]
 
 
@@ -167,11 +168,14 @@ def pack_modes(sym: np.ndarray, n_words: int | None = None) -> np.ndarray:
 class OracleHead:
     """Cache state of one head, driven through the C oracle."""
 
-    def __init__(self, d, bits, scheme, k_group, v_group, residual, n_sink, cap, k_norm=False):
+    def __init__(self, d, bits, scheme, k_group, v_group, residual, n_sink, cap, k_norm=False,
+                 v_queue=False):
         if d > 256 or bits not in (2, 4, 8) or d % (8 // bits):
             raise ValueError("unsupported head_dim / bits")
         if k_norm and scheme != INNERQ:
             raise ValueError("key normalization is an InnerQ option")
+        if v_queue and scheme != KIVI:
+            raise ValueError("the value queue is a KIVI option")
         self.d, self.bits, self.scheme = d, bits, scheme
         self.k_group, self.v_group = k_group, v_group
         self.residual, self.n_sink, self.cap = residual, n_sink, cap
@@ -197,6 +201,7 @@ class OracleHead:
         s.k_group, s.v_group, s.residual, s.n_sink = k_group, v_group, residual, n_sink
         s.cap = cap
         s.k_normalize = 1 if k_norm else 0
+        s.v_queue = 1 if v_queue else 0
         for name in ("k_u", "v_u", "k_scale", "k_zero", "v_scale", "v_zero", "k_sym",
                      "v_sym", "k_res", "v_res", "k_sink", "v_sink", "k_norm"):
             setattr(s, name, _ptr(getattr(self, name)))
@@ -206,20 +211,21 @@ class OracleHead:
     def for_workload(cls, w, cap=None):
         cap = w.max_ctx() if cap is None else cap
         return cls(w.head_dim, w.bits, w.scheme, w.k_group, w.v_group, w.residual,
-                   w.n_sink, cap, k_norm=getattr(w, "k_norm", False))
+                   w.n_sink, cap, k_norm=getattr(w, "k_norm", False),
+                   v_queue=getattr(w, "v_queue", False))
 
     # counters
     def save_state(self):
         """The counters and fp16 residual/window rows (enough to rewind appends:
         the rows they overwrite are rewritten in the same order)."""
         s = self._s
-        return ((s.n_quant, s.n_resid, s.n_sink_used, s.n_flush),
+        return ((s.n_quant, s.n_resid, s.n_sink_used, s.n_flush, s.n_vquant),
                 self.k_res.copy(), self.v_res.copy())
 
     def load_state(self, state) -> None:
-        (nq, nr, ns, nf), kr, vr = state
+        (nq, nr, ns, nf, nvq), kr, vr = state
         s = self._s
-        s.n_quant, s.n_resid, s.n_sink_used, s.n_flush = nq, nr, ns, nf
+        s.n_quant, s.n_resid, s.n_sink_used, s.n_flush, s.n_vquant = nq, nr, ns, nf, nvq
         self.k_res[...] = kr
         self.v_res[...] = vr
 
@@ -227,6 +233,11 @@ class OracleHead:
     n_resid = property(lambda self: self._s.n_resid)
     n_sink_used = property(lambda self: self._s.n_sink_used)
     n_flush = property(lambda self: self._s.n_flush)
+
+    @property
+    def n_vquant(self) -> int:
+        """Values held quantized (the keys' count unless KIVI's value queue)."""
+        return self._s.n_vquant if self._s.v_queue else self._s.n_quant
 
     def prefill(self, K, V) -> None:
         K, V = _f16(K), _f16(V)
@@ -265,7 +276,7 @@ class OracleHead:
         return pack(self.k_u[: self.n_quant], self.bits)
 
     def packed_v(self) -> np.ndarray:
-        return pack(self.v_u[: self.n_quant], self.bits)
+        return pack(self.v_u[: self.n_vquant], self.bits)
 
     def k_meta(self):
         """(scale, zero) of the quantized keys: KIVI [n_quant/G][d], InnerQ [n_quant][d/G]."""
@@ -277,12 +288,18 @@ class OracleHead:
         return self.k_norm.copy()
 
     def v_meta(self):
-        return self.v_scale[: self.n_quant], self.v_zero[: self.n_quant]
+        return self.v_scale[: self.n_vquant], self.v_zero[: self.n_vquant]
 
     def residual_tokens(self):
-        """fp16 residual (KIVI) or window (InnerQ) keys and values, oldest first."""
+        """fp16 residual (KIVI) or window (InnerQ) keys and values, oldest first
+        (with KIVI's value queue the values are value_queue())."""
         n = self.n_resid
         return self.k_res[:n].view(np.float16), self.v_res[:n].view(np.float16)
+
+    def value_queue(self) -> np.ndarray:
+        """fp16 values not yet quantized, oldest first."""
+        n = self.n_quant + self.n_resid - self.n_vquant
+        return self.v_res[:n].view(np.float16)
 
     def sink_tokens(self):
         n = self.n_sink_used

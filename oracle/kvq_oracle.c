@@ -193,10 +193,19 @@ static void innerq_key_norms(orc_head *s, const uint16_t *K, int64_t T) {
 
 /* ---- cache state machine ---------------------------------------------- */
 
+/* Values held quantized: they follow the keys (batch flush), except for
+ * KIVI's value queue, which keeps its own count. */
+static int64_t values_quantized(const orc_head *s) {
+  return s->v_queue ? s->n_vquant : s->n_quant;
+}
+
 /*
  * Prefill of one head's prompt K, V ([T][d] fp16).
  * KIVI ([KIVI] 工作原理): the first l - r tokens, l - r a multiple of R (hence
  *   of G), are quantized; the last r = T mod R stay fp16 in the residual.
+ *   With v_queue the values are a queue instead (the page's value
+ *   paragraph): the last min(T, R - 1) values stay fp16, the rest are
+ *   quantized per token.
  * InnerQ ([INNERQ] 方法论 4; [KVQ5]): the first S tokens stay fp16 as sinks,
  *   the last W as the recent window, the tokens between are quantized.
  * Returns 0, or -1 when the quantized region would exceed the capacity.
@@ -207,13 +216,18 @@ int orc_prefill(orc_head *s, const uint16_t *K, const uint16_t *V, int64_t T) {
   if (s->scheme == ORC_KIVI) {
     const int R = s->residual, G = s->k_group;
     const int64_t nq = T - T % R;
-    if (nq > s->cap) return -1;
+    /* the value queue ([KIVI] 工作原理, value paragraph) holds the newest
+     * values until it reaches R, then its oldest is quantized: after the
+     * prompt it holds the last min(T, R - 1) values */
+    const int64_t nvq = !s->v_queue ? nq : (T >= R ? T - (R - 1) : 0);
+    if (nq > s->cap || nvq > s->cap) return -1;
     for (int64_t g = 0; g < nq / G; ++g) kivi_quant_key_group(s, K + g * G * d, g * G);
-    for (int64_t t = 0; t < nq; ++t) kivi_quant_value_token(s, V + t * d, t);
+    for (int64_t t = 0; t < nvq; ++t) kivi_quant_value_token(s, V + t * d, t);
     memcpy(s->k_res, K + nq * d, sizeof(uint16_t) * (size_t)((T - nq) * d));
-    memcpy(s->v_res, V + nq * d, sizeof(uint16_t) * (size_t)((T - nq) * d));
+    memcpy(s->v_res, V + nvq * d, sizeof(uint16_t) * (size_t)((T - nvq) * d));
     s->n_quant = nq;
     s->n_resid = T - nq;
+    s->n_vquant = nvq;
     s->n_sink_used = 0;
     return 0;
   }
@@ -239,6 +253,9 @@ int orc_prefill(orc_head *s, const uint16_t *K, const uint16_t *V, int64_t T) {
  * KIVI ([KIVI] 工作原理; [HF] §3.1): the token joins the fp16 residual; when the
  *   residual reaches R tokens all R are quantized (keys as R/G groups, values
  *   per token), appended to the quantized region, and the residual empties.
+ *   With v_queue only the keys flush so; the value is pushed onto the value
+ *   queue, and once the queue holds R values its oldest is quantized per
+ *   token and appended to the quantized values.
  * InnerQ ([INNERQ] 方法论 4): sinks fill first, then the window; once the
  *   window holds W tokens its oldest token is quantized and appended to the
  *   quantized region, and the new token takes its place.
@@ -249,17 +266,32 @@ int orc_append(orc_head *s, const uint16_t *k, const uint16_t *v) {
   const size_t row = sizeof(uint16_t) * (size_t)d;
   if (s->scheme == ORC_KIVI) {
     const int R = s->residual, G = s->k_group;
+    const int64_t held = s->n_quant + s->n_resid;  /* tokens before this one */
+    int64_t nv = held - s->n_vquant;               /* queued fp16 values (queue) */
     if (s->n_resid + 1 == R && s->n_quant + R > s->cap) return -1;
+    if (s->v_queue && nv + 1 == R && s->n_vquant + 1 > s->cap) return -1;
     memcpy(s->k_res + s->n_resid * d, k, row);
-    memcpy(s->v_res + s->n_resid * d, v, row);
+    if (!s->v_queue) memcpy(s->v_res + s->n_resid * d, v, row);
     s->n_resid += 1;
     if (s->n_resid == R) {
       for (int g = 0; g < R / G; ++g)
         kivi_quant_key_group(s, s->k_res + (int64_t)g * G * d, s->n_quant + (int64_t)g * G);
-      for (int t = 0; t < R; ++t) kivi_quant_value_token(s, s->v_res + (int64_t)t * d, s->n_quant + t);
+      if (!s->v_queue)
+        for (int t = 0; t < R; ++t)
+          kivi_quant_value_token(s, s->v_res + (int64_t)t * d, s->n_quant + t);
       s->n_quant += R;
       s->n_resid = 0;
       s->n_flush += 1;
+    }
+    if (s->v_queue) {
+      /* push the value; once the queue holds R, its oldest is quantized */
+      memcpy(s->v_res + nv * d, v, row);
+      nv += 1;
+      if (nv == R) {
+        kivi_quant_value_token(s, s->v_res, s->n_vquant);
+        s->n_vquant += 1;
+        memmove(s->v_res, s->v_res + d, row * (size_t)(R - 1));
+      }
     }
     return 0;
   }
@@ -353,9 +385,10 @@ int orc_attend(const orc_head *s, const uint16_t *q, double tau, double *out) {
   i = 0;
   for (int64_t t = 0; t < s->n_sink_used; ++t, ++i)
     for (int c = 0; c < d; ++c) out[c] += sc[i] * (double)orc_half_to_float(s->v_sink[t * d + c]);
-  for (int64_t t = 0; t < s->n_quant; ++t, ++i)
+  const int64_t nvq = values_quantized(s);
+  for (int64_t t = 0; t < nvq; ++t, ++i)
     for (int c = 0; c < d; ++c) out[c] += sc[i] * value_hat(s, t, c);
-  for (int64_t t = 0; t < s->n_resid; ++t, ++i)
+  for (int64_t t = 0; t < n - s->n_sink_used - nvq; ++t, ++i)
     for (int c = 0; c < d; ++c) out[c] += sc[i] * (double)orc_half_to_float(s->v_res[t * d + c]);
   for (int c = 0; c < d; ++c) out[c] /= l;
 
@@ -396,13 +429,14 @@ static void token_row(const orc_head *s, int64_t j, int k, double *row) {
     return;
   }
   j -= s->n_sink_used;
-  if (j < s->n_quant) {
+  const int64_t nq = k ? s->n_quant : values_quantized(s);
+  if (j < nq) {
     for (int c = 0; c < d; ++c)
       row[c] = k ? (s->k_normalize ? (double)s->k_norm[c] : 1.0) * key_hat(s, j, c)
                  : value_hat(s, j, c);
     return;
   }
-  j -= s->n_quant;
+  j -= nq;
   const uint16_t *src = (k ? s->k_res : s->v_res) + j * d;
   for (int c = 0; c < d; ++c) row[c] = (double)orc_half_to_float(src[c]);
 }

@@ -55,6 +55,8 @@ typedef struct orc_head {
   uint16_t *k_res, *v_res;    /* [residual][d] fp16, oldest first */
   uint16_t *k_sink, *v_sink;  /* [n_sink][d] fp16 */
   float *k_norm;              /* InnerQ with k_normalize: [d] per-channel key factors */
+  int32_t v_queue;            /* KIVI: 1 = values leave fp16 one at a time (a queue) */
+  int64_t n_vquant;           /* KIVI with v_queue: values held quantized */
 } orc_head;
 
 int orc_rounding_is_nearest(void);

@@ -463,6 +463,71 @@ def pin_attention_error_bound():
 
 
 # --------------------------------------------------------------------------
+# KIVI's value queue (values leave the fp16 queue one at a time)
+# --------------------------------------------------------------------------
+
+def pin_kivi_value_queue_cadence():
+    """After n tokens the queue holds the last min(n, R - 1) values in fp16
+    (oldest first) and the rest are quantized per token; the keys flush
+    exactly as in the batch reading; every value token quantized under both
+    readings has the same codes, scales and zeros."""
+    rng = np.random.default_rng(40)
+    d, G, Gv, R = 32, 8, 16, 16
+    for T in (0, 5, 15, 16, 17, 40, 48):
+        K, V = _randn16(rng, T + 40, d), _randn16(rng, T + 40, d)
+        hq = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 256, v_queue=True)
+        hb = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 256)
+        hq.prefill(K[:T], V[:T])
+        hb.prefill(K[:T], V[:T])
+        for n in range(T, T + 40):
+            if n > T:
+                hq.append(K[n - 1], V[n - 1])
+                hb.append(K[n - 1], V[n - 1])
+            assert hq.n_vquant == max(0, n - R + 1), (T, n, hq.n_vquant)
+            assert np.array_equal(hq.value_queue().view(np.uint16),
+                                  V[hq.n_vquant:n].view(np.uint16)), (T, n)
+            assert (hq.n_quant, hq.n_resid) == (hb.n_quant, hb.n_resid)
+            nq = hq.n_quant
+            assert np.array_equal(hq.k_u[:nq], hb.k_u[:nq])
+            m = min(hq.n_vquant, hb.n_vquant)
+            assert np.array_equal(hq.v_u[:m], hb.v_u[:m]), (T, n)
+            assert np.array_equal(hq.v_scale[:m].view(np.uint32), hb.v_scale[:m].view(np.uint32))
+            assert np.array_equal(hq.v_zero[:m].view(np.uint32), hb.v_zero[:m].view(np.uint32))
+
+
+def pin_kivi_value_queue_selector():
+    """One token whose score leads all others by hundreds of nats makes the
+    attention output that token's value as stored: the exact fp16 row while
+    it waits in the queue (also when its key is already quantized) and the
+    dequantized row once it has left.  Under the batch reading the same
+    token's value is already quantized (the two readings differ)."""
+    rng = np.random.default_rng(41)
+    d, G, Gv, R, T = 32, 8, 16, 16, 40       # keys: 32 quantized; values: 25
+    q = np.zeros(d, np.float16)
+    q[0] = 64
+    for sel, where in ((28, "queue, key quantized"), (36, "queue and residual"),
+                       (10, "quantized")):
+        K = (rng.standard_normal((T, d)) * 0.5).astype(np.float16)
+        K[sel, 0] = 8
+        V = _randn16(rng, T, d)
+        hq = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 64, v_queue=True)
+        hb = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 64)
+        hq.prefill(K, V)
+        hb.prefill(K, V)
+        assert (hq.n_quant, hq.n_vquant, hb.n_vquant) == (32, 25, 32)
+        out = hq.attend(q, 1.0)
+        if sel >= hq.n_vquant:
+            np.testing.assert_allclose(out, V[sel].astype(np.float64), rtol=0, atol=1e-12,
+                                       err_msg=where)
+        else:
+            vh = hq.v_u[sel] * np.repeat(hq.v_scale[sel], Gv).astype(np.float64) \
+                + np.repeat(hq.v_zero[sel], Gv)
+            np.testing.assert_allclose(out, vh, rtol=0, atol=1e-12, err_msg=where)
+        if 25 <= sel < 32:
+            assert np.abs(hb.attend(q, 1.0) - V[sel].astype(np.float64)).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
 # keys cached before the rotary position embedding
 # --------------------------------------------------------------------------
 
@@ -618,6 +683,10 @@ MUTANTS = [
      "row[c] = k ? key_hat(s, j, c)"),
     ("rope window newest first", "const uint16_t *src = (k ? s->k_res : s->v_res) + j * d;",
      "const uint16_t *src = (k ? s->k_res : s->v_res) + (s->n_resid - 1 - j) * d;"),
+    ("queue holds R values after the prompt", "(T >= R ? T - (R - 1) : 0)", "(T >= R ? T - R : 0)"),
+    ("queue pops newest", "kivi_quant_value_token(s, s->v_res, s->n_vquant);",
+     "kivi_quant_value_token(s, s->v_res + (int64_t)(R - 1) * d, s->n_vquant);"),
+    ("queue ignored by attention", "return s->v_queue ? s->n_vquant : s->n_quant;", "return s->n_quant;"),
     ("value group transposed", "x[i] = orc_half_to_float(src[j * Gv + i]);", "x[i] = orc_half_to_float(src[i * (d / Gv) + j]);"),
 ]
 
