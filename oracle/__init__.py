@@ -62,6 +62,7 @@ class _Head(ctypes.Structure):
         ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p),
         ("k_norm", ctypes.c_void_p),
         ("v_queue", ctypes.c_int32), ("n_vquant", ctypes.c_int64),
+        ("meta_f16", ctypes.c_int32),
     ]
 
 
@@ -70,6 +71,10 @@ def _declare(L):
     L.orc_rounding_is_nearest.restype = ctypes.c_int
     L.orc_half_to_float.argtypes = [ctypes.c_uint16]
     L.orc_half_to_float.restype = ctypes.c_float
+    L.orc_float_to_half.argtypes = [ctypes.c_float]
+    L.orc_float_to_half.restype = ctypes.c_uint16
+    L.orc_quant_asym_f16.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int64]
+    L.orc_quant_sym_f16.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int64]
     L.orc_quant_asym.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int64]
     L.orc_quant_sym.argtypes = [P, ctypes.c_int, ctypes.c_int, P, P, P, ctypes.c_int64]
     L.orc_choose_symmetric.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_int]
@@ -124,21 +129,28 @@ def half_to_float(h: int) -> float:
     return lib().orc_half_to_float(int(h))
 
 
-def quant_asym(x, bits: int):
+def float_to_half(f: float) -> int:
+    """IEEE binary32 -> binary16 bits, round to nearest even."""
+    return int(lib().orc_float_to_half(float(f)))
+
+
+def quant_asym(x, bits: int, meta_f16: bool = False):
     """Asymmetric quantization of one group x (float32): (scale, zero, codes)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     s, z = ctypes.c_float(), ctypes.c_float()
     u = np.zeros(x.size, dtype=np.uint8)
-    lib().orc_quant_asym(_ptr(x), x.size, bits, ctypes.addressof(s), ctypes.addressof(z), _ptr(u), 1)
+    fn = lib().orc_quant_asym_f16 if meta_f16 else lib().orc_quant_asym
+    fn(_ptr(x), x.size, bits, ctypes.addressof(s), ctypes.addressof(z), _ptr(u), 1)
     return np.float32(s.value), np.float32(z.value), u
 
 
-def quant_sym(x, bits: int):
+def quant_sym(x, bits: int, meta_f16: bool = False):
     """Symmetric quantization of one group x (float32): (scale, zero, codes)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     s, z = ctypes.c_float(), ctypes.c_float()
     u = np.zeros(x.size, dtype=np.uint8)
-    lib().orc_quant_sym(_ptr(x), x.size, bits, ctypes.addressof(s), ctypes.addressof(z), _ptr(u), 1)
+    fn = lib().orc_quant_sym_f16 if meta_f16 else lib().orc_quant_sym
+    fn(_ptr(x), x.size, bits, ctypes.addressof(s), ctypes.addressof(z), _ptr(u), 1)
     return np.float32(s.value), np.float32(z.value), u
 
 
@@ -169,7 +181,7 @@ class OracleHead:
     """Cache state of one head, driven through the C oracle."""
 
     def __init__(self, d, bits, scheme, k_group, v_group, residual, n_sink, cap, k_norm=False,
-                 v_queue=False):
+                 v_queue=False, meta_f16=False):
         if d > 256 or bits not in (2, 4, 8) or d % (8 // bits):
             raise ValueError("unsupported head_dim / bits")
         if k_norm and scheme != INNERQ:
@@ -202,6 +214,7 @@ class OracleHead:
         s.cap = cap
         s.k_normalize = 1 if k_norm else 0
         s.v_queue = 1 if v_queue else 0
+        s.meta_f16 = 1 if meta_f16 else 0
         for name in ("k_u", "v_u", "k_scale", "k_zero", "v_scale", "v_zero", "k_sym",
                      "v_sym", "k_res", "v_res", "k_sink", "v_sink", "k_norm"):
             setattr(s, name, _ptr(getattr(self, name)))

@@ -31,6 +31,34 @@ float orc_half_to_float(uint16_t h) {
   return sign ? -v : v;
 }
 
+/*
+ * IEEE binary32 -> binary16, round to nearest even; overflow gives infinity,
+ * NaN stays NaN.  Written from the two formats' definitions: 1 sign bit,
+ * 5 exponent bits (bias 15), 10 fraction bits; subnormals in units of 2^-24.
+ */
+uint16_t orc_float_to_half(float f) {
+  uint32_t x;
+  memcpy(&x, &f, sizeof(x));
+  const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  const uint32_t ax = x & 0x7fffffffu;
+  if (ax >= 0x7f800000u) return sign | (ax > 0x7f800000u ? 0x7e00u : 0x7c00u);
+  if (ax >= 0x477ff000u) return sign | 0x7c00u;  /* >= 65520: rounds past 65504 */
+  const int e = (int)(ax >> 23) - 127;           /* unbiased exponent */
+  if (e < -25) return sign;                      /* below 2^-25: rounds to zero */
+  const uint32_t m = (ax & 0x7fffffu) | 0x800000u;  /* 24-bit significand */
+  /* keep 11 significant bits for a normal result; a subnormal result counts
+   * units of 2^-24, i.e. m * 2^(e+1) */
+  const int shift = e >= -14 ? 13 : -(e + 1);
+  uint32_t q = m >> shift;
+  const uint32_t rem = m & ((1u << shift) - 1u), half = 1u << (shift - 1);
+  if (rem > half || (rem == half && (q & 1u))) q += 1;
+  if (e >= -14) /* q in [0x400, 0x800]; a carry to 0x800 moves to the next exponent */
+    return sign | (uint16_t)((((uint32_t)(e + 15)) << 10) + (q - 0x400u));
+  return sign | (uint16_t)q;                     /* 0x400 = the smallest normal */
+}
+
+static float round_to_half(float f) { return orc_half_to_float(orc_float_to_half(f)); }
+
 static void min_max(const float *x, int n, float *mn, float *mx) {
   float lo = x[0], hi = x[0];
   for (int i = 1; i < n; ++i) {
@@ -96,6 +124,48 @@ void orc_quant_sym(const float *x, int n, int bits, float *scale, float *zero,
 }
 
 /*
+ * fp16 metadata (a cache-format variant; the pages fix no storage precision
+ * for scales and zero points).  Reading: the fp32 scale and zero above are
+ * rounded once to fp16, and the codes are taken with the stored values, so
+ * dequantization u*scale + zero uses exactly what is stored.  A scale that
+ * rounds to 0 is a constant group (all codes 0, or q = 0 when symmetric).
+ */
+void orc_quant_asym_f16(const float *x, int n, int bits, float *scale, float *zero,
+                        uint8_t *u, int64_t ustride) {
+  const float top = (float)((1 << bits) - 1);
+  float mn, mx;
+  min_max(x, n, &mn, &mx);
+  const float z = round_to_half(mn);
+  const float s = mx == mn ? 0.0f : round_to_half((mx - mn) / top);
+  *zero = z;
+  *scale = s;
+  for (int i = 0; i < n; ++i) {
+    float r = s == 0.0f ? 0.0f : rintf((x[i] - z) / s);
+    if (r < 0.0f) r = 0.0f;
+    if (r > top) r = top;
+    u[i * ustride] = (uint8_t)r;
+  }
+}
+
+void orc_quant_sym_f16(const float *x, int n, int bits, float *scale, float *zero,
+                       uint8_t *u, int64_t ustride) {
+  const int half = 1 << (bits - 1);
+  const float lim = (float)(half - 1);
+  float mn, mx;
+  min_max(x, n, &mn, &mx);
+  const float a = fmaxf(fabsf(mn), fabsf(mx));
+  const float s = round_to_half(a / lim);
+  *scale = s;
+  *zero = -(float)half * s;
+  for (int i = 0; i < n; ++i) {
+    float r = s == 0.0f ? 0.0f : rintf(x[i] / s);
+    if (r < -lim) r = -lim;
+    if (r > lim) r = lim;
+    u[i * ustride] = (uint8_t)((int)r + half);
+  }
+}
+
+/*
  * Per-group choice between the two ([INNERQ] 方法论 2: symmetric when the group
  * is centred at zero, asymmetric otherwise; the page gives no threshold).
  * Reading used: symmetric iff the group is not constant and its midpoint
@@ -118,8 +188,9 @@ static void kivi_quant_key_group(orc_head *s, const uint16_t *src, int64_t t0) {
   float *x = (float *)malloc(sizeof(float) * (size_t)G);
   for (int c = 0; c < d; ++c) {
     for (int i = 0; i < G; ++i) x[i] = orc_half_to_float(src[(int64_t)i * d + c]);
-    orc_quant_asym(x, G, s->bits, &s->k_scale[(t0 / G) * d + c],
-                   &s->k_zero[(t0 / G) * d + c], &s->k_u[t0 * d + c], d);
+    (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(
+        x, G, s->bits, &s->k_scale[(t0 / G) * d + c], &s->k_zero[(t0 / G) * d + c],
+        &s->k_u[t0 * d + c], d);
   }
   free(x);
 }
@@ -131,8 +202,9 @@ static void kivi_quant_value_token(orc_head *s, const uint16_t *src, int64_t t) 
   float x[256];
   for (int j = 0; j < ng; ++j) {
     for (int i = 0; i < Gv; ++i) x[i] = orc_half_to_float(src[j * Gv + i]);
-    orc_quant_asym(x, Gv, s->bits, &s->v_scale[t * ng + j], &s->v_zero[t * ng + j],
-                   &s->v_u[t * d + j * Gv], 1);
+    (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(
+        x, Gv, s->bits, &s->v_scale[t * ng + j], &s->v_zero[t * ng + j], &s->v_u[t * d + j * Gv],
+        1);
   }
 }
 
@@ -160,11 +232,11 @@ static void innerq_quant_token(const orc_head *s, const uint16_t *src, int group
     const int is_sym = orc_choose_symmetric(mn, mx, s->bits);
     sym[t * ng + j] = (uint8_t)is_sym;
     if (is_sym)
-      orc_quant_sym(x, group, s->bits, &scale[t * ng + j], &zero[t * ng + j],
-                    &u[t * d + j * group], 1);
+      (s->meta_f16 ? orc_quant_sym_f16 : orc_quant_sym)(
+          x, group, s->bits, &scale[t * ng + j], &zero[t * ng + j], &u[t * d + j * group], 1);
     else
-      orc_quant_asym(x, group, s->bits, &scale[t * ng + j], &zero[t * ng + j],
-                     &u[t * d + j * group], 1);
+      (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(
+          x, group, s->bits, &scale[t * ng + j], &zero[t * ng + j], &u[t * d + j * group], 1);
   }
 }
 

@@ -57,16 +57,22 @@ typedef struct orc_head {
   float *k_norm;              /* InnerQ with k_normalize: [d] per-channel key factors */
   int32_t v_queue;            /* KIVI: 1 = values leave fp16 one at a time (a queue) */
   int64_t n_vquant;           /* KIVI with v_queue: values held quantized */
+  int32_t meta_f16;           /* 1 = scales and zeros stored in fp16 */
 } orc_head;
 
 int orc_rounding_is_nearest(void);
 float orc_half_to_float(uint16_t h);
+uint16_t orc_float_to_half(float f);
 
 void orc_quant_asym(const float *x, int n, int bits, float *scale, float *zero,
                     uint8_t *u, int64_t ustride);
 void orc_quant_sym(const float *x, int n, int bits, float *scale, float *zero,
                    uint8_t *u, int64_t ustride);
 int orc_choose_symmetric(float mn, float mx, int bits);
+void orc_quant_asym_f16(const float *x, int n, int bits, float *scale, float *zero,
+                        uint8_t *u, int64_t ustride);
+void orc_quant_sym_f16(const float *x, int n, int bits, float *scale, float *zero,
+                       uint8_t *u, int64_t ustride);
 
 int orc_prefill(orc_head *s, const uint16_t *K, const uint16_t *V, int64_t T);
 int orc_append(orc_head *s, const uint16_t *k, const uint16_t *v);

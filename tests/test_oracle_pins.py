@@ -57,6 +57,60 @@ def pin_worked_examples():
         assert list(u) == [int(c) for c in codes.split()], (row, u)
 
 
+def pin_float_to_half():
+    """fp32 -> fp16, nearest-even, against numpy's IEEE conversion: every
+    midpoint between consecutive halves (ties) and its two neighbours, both
+    signs, subnormals, the overflow boundary, infinities and zeros."""
+    h = np.arange(0, 0x7c00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mid = ((h[:-1] + h[1:]) / 2).astype(np.float32)
+    vals = np.concatenate([mid, np.nextafter(mid, np.float32(np.inf)),
+                           np.nextafter(mid, np.float32(0)),
+                           np.float32([0.0, 65504, 65519, 65520, 1e9, 2.0 ** -25, 2.0 ** -26,
+                                       1e-30, np.inf])])
+    vals = np.concatenate([vals, -vals])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    for i in list(range(0, vals.size, 7)) + list(range(vals.size - 20, vals.size)):
+        assert oracle.float_to_half(vals[i]) == ref[i], (vals[i], hex(ref[i]))
+
+
+def pin_f16_meta_worked_examples():
+    for row in _golden_rows("f16_meta_worked_examples.txt"):
+        head, xs, scale, zero, codes = [c.strip() for c in row.split("|")]
+        mode, bits = head.split()
+        x = np.array([float(v) for v in xs.split()], np.float32)
+        fn = oracle.quant_asym if mode == "asym" else oracle.quant_sym
+        s, z, u = fn(x, int(bits), meta_f16=True)
+        assert s == np.float32(float(scale)), (row, s)
+        assert z == np.float32(float(zero)), (row, z)
+        assert list(u) == [int(c) for c in codes.split()], (row, u)
+
+
+def pin_f16_meta_round_trip_bound():
+    """With fp16 metadata the stored scale and zero are fp16 values, and every
+    element reconstructs within half a stored step plus what rounding the
+    scale and the zero moved the grid: |x - x_hat| <= s16/2 + |min - z16| +
+    (2^b - 1)|s32 - s16| (+ fp32 slack), for fp16 and for arbitrary fp32
+    groups (normalized keys)."""
+    rng = np.random.default_rng(42)
+    for bits in (2, 4):
+        top = (1 << bits) - 1
+        for trial in range(400):
+            n = int(rng.integers(2, 70))
+            x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-3, 2)).astype(np.float32)
+            if trial % 2:
+                x = x.astype(np.float16).astype(np.float32)
+            s, z, u = oracle.quant_asym(x, bits, meta_f16=True)
+            assert np.float32(s).astype(np.float16).astype(np.float32) == s
+            assert np.float32(z).astype(np.float16).astype(np.float32) == z
+            mn, mx = float(x.min()), float(x.max())
+            s32 = (mx - mn) / top
+            xh = u.astype(np.float64) * float(s) + float(z)
+            bound = float(s) / 2 + abs(mn - float(z)) + top * abs(s32 - float(s)) \
+                + 4 * np.spacing(np.float32(max(abs(mn), abs(mx))))
+            assert np.abs(x.astype(np.float64) - xh).max() <= bound, (bits, trial)
+
+
 def pin_mode_choice():
     # midpoint 0 -> symmetric; far from zero -> asymmetric; equality -> symmetric
     assert oracle.choose_symmetric(-1.0, 1.0, 4)
@@ -420,6 +474,30 @@ def pin_attention_grid_exact_innerq_key_norm():
     np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K, V, tau), rtol=0, atol=1e-12)
 
 
+def pin_attention_grid_exact_f16_meta():
+    """Grid data has power-of-two steps and fp16 bases, which fp16 metadata
+    stores exactly: attention over KIVI and InnerQ caches with fp16 scales
+    and zeros equals torch's fp64 SDPA on the raw tokens."""
+    rng = np.random.default_rng(25)
+    d, G, Gv, R = 32, 8, 16, 16
+    K, V = _grid_tokens(rng, 80, d, 2, G, Gv)
+    h = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 256, meta_f16=True)
+    h.prefill(K[:71], V[:71])
+    for i in range(71, 80):
+        h.append(K[i], V[i])
+    q = _randn16(rng, d)
+    tau = 1 / math.sqrt(d)
+    np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K, V, tau), rtol=0, atol=1e-12)
+    d, S, W, T = 128, 4, 8, 60
+    K, V = _grid_tokens(rng, T, d, 4, 1, 64, sym_groups=True)
+    h = oracle.OracleHead(d, 4, oracle.INNERQ, 64, 64, W, S, 256, meta_f16=True)
+    h.prefill(K, V)
+    assert 0 < h.k_sym[:h.n_quant].sum() < h.k_sym[:h.n_quant].size
+    q = _randn16(rng, d)
+    tau = 1 / math.sqrt(d)
+    np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K, V, tau), rtol=0, atol=1e-12)
+
+
 def pin_attention_identical_keys_mean():
     rng = np.random.default_rng(22)
     d, G, Gv, R, T = 32, 8, 8, 16, 48
@@ -652,7 +730,8 @@ MUTANTS = [
     ("ties away from zero", "float r = rintf((x[i] - mn) / s);", "float r = roundf((x[i] - mn) / s);"),
     ("zero = max", "*zero = mn;\n  if (mx == mn)", "*zero = mx;\n  if (mx == mn)"),
     ("2^b levels", "const float s = (mx - mn) / top;", "const float s = (mx - mn) / (top + 1.0f);"),
-    ("sym zero off by one", "*zero = -(float)half * s;", "*zero = -(float)(half - 1) * s;"),
+    ("sym zero off by one", "*zero = -(float)half * s;\n  for (int i = 0; i < n; ++i) {\n    float r = rintf(x[i] / s);",
+     "*zero = -(float)(half - 1) * s;\n  for (int i = 0; i < n; ++i) {\n    float r = rintf(x[i] / s);"),
     ("strict mode rule", "return fabsf(mx + mn) <= step;", "return fabsf(mx + mn) < step;"),
     ("key meta by token", "const int64_t i = (t / s->k_group) * d + c;", "const int64_t i = (t % s->k_group) * d + c;"),
     ("value zero dropped", "return (double)s->v_u[t * d + c] * (double)s->v_scale[i] + (double)s->v_zero[i];",
@@ -687,6 +766,12 @@ MUTANTS = [
     ("queue pops newest", "kivi_quant_value_token(s, s->v_res, s->n_vquant);",
      "kivi_quant_value_token(s, s->v_res + (int64_t)(R - 1) * d, s->n_vquant);"),
     ("queue ignored by attention", "return s->v_queue ? s->n_vquant : s->n_quant;", "return s->n_quant;"),
+    ("f16 codes from the fp32 scale", "float r = s == 0.0f ? 0.0f : rintf((x[i] - z) / s);",
+     "float r = s == 0.0f ? 0.0f : rintf((x[i] - z) / ((mx - mn) / top));"),
+    ("f16 symmetric codes from the fp32 scale", "float r = s == 0.0f ? 0.0f : rintf(x[i] / s);",
+     "float r = s == 0.0f ? 0.0f : rintf(x[i] / (a / lim));"),
+    ("fp32 to fp16 truncates", "if (rem > half || (rem == half && (q & 1u))) q += 1;", "if (0) q += 1;"),
+    ("fp32 to fp16 ties away", "(rem == half && (q & 1u))", "(rem == half)"),
     ("value group transposed", "x[i] = orc_half_to_float(src[j * Gv + i]);", "x[i] = orc_half_to_float(src[i * (d / Gv) + j]);"),
 ]
 
