@@ -62,7 +62,9 @@ class _Head(ctypes.Structure):
         ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p),
         ("k_norm", ctypes.c_void_p),
         ("v_queue", ctypes.c_int32), ("n_vquant", ctypes.c_int64),
-        ("meta_f16", ctypes.c_int32),
+        ("meta_f16", ctypes.c_int32), ("outliers", ctypes.c_int32),
+        ("k_oidx", ctypes.c_void_p), ("v_oidx", ctypes.c_void_p),
+        ("k_oval", ctypes.c_void_p), ("v_oval", ctypes.c_void_p),
     ]
 
 
@@ -85,6 +87,7 @@ def _declare(L):
     L.orc_attend_rope.argtypes = [ctypes.POINTER(_Head), P, ctypes.c_double, ctypes.c_double,
                                   ctypes.c_int64, P]
     L.orc_pack.argtypes = [P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P]
+    L.orc_select_outliers.argtypes = [P, ctypes.c_int, ctypes.c_int, P]
     L.orc_pack_modes.argtypes = [P, ctypes.c_int64, P]
     if not L.orc_rounding_is_nearest():
         raise RuntimeError("oracle needs round-to-nearest-even")
@@ -158,6 +161,14 @@ def choose_symmetric(mn: float, mx: float, bits: int) -> bool:
     return bool(lib().orc_choose_symmetric(float(mn), float(mx), bits))
 
 
+def select_outliers(row, k: int) -> np.ndarray:
+    """Channels (ascending) of the k largest-magnitude elements of one fp16 row."""
+    row = _f16(row)
+    idx = np.zeros(k, np.uint16)
+    lib().orc_select_outliers(_ptr(row.view(np.uint16)), row.size, k, _ptr(idx))
+    return idx
+
+
 def pack(u: np.ndarray, bits: int) -> np.ndarray:
     """Pack code rows [n][d] (one code per byte) into [n][d*bits/8] bytes."""
     u = np.ascontiguousarray(u, dtype=np.uint8)
@@ -181,13 +192,15 @@ class OracleHead:
     """Cache state of one head, driven through the C oracle."""
 
     def __init__(self, d, bits, scheme, k_group, v_group, residual, n_sink, cap, k_norm=False,
-                 v_queue=False, meta_f16=False):
+                 v_queue=False, meta_f16=False, outliers=0):
         if d > 256 or bits not in (2, 4, 8) or d % (8 // bits):
             raise ValueError("unsupported head_dim / bits")
         if k_norm and scheme != INNERQ:
             raise ValueError("key normalization is an InnerQ option")
         if v_queue and scheme != KIVI:
             raise ValueError("the value queue is a KIVI option")
+        if outliers and (scheme != KIVI or not 0 < outliers <= 8 or outliers >= d):
+            raise ValueError("outliers: KIVI only, 1..8 per token")
         self.d, self.bits, self.scheme = d, bits, scheme
         self.k_group, self.v_group = k_group, v_group
         self.residual, self.n_sink, self.cap = residual, n_sink, cap
@@ -208,6 +221,11 @@ class OracleHead:
         self.k_sink = np.zeros((max(n_sink, 1), d), np.uint16)
         self.v_sink = np.zeros((max(n_sink, 1), d), np.uint16)
         self.k_norm = np.ones(d, np.float32)  # per-channel key factors (InnerQ option)
+        no = max(outliers, 1)
+        self.k_oidx = np.zeros((cap, no), np.uint16)   # per-token outlier channels
+        self.v_oidx = np.zeros((cap, no), np.uint16)
+        self.k_oval = np.zeros((cap, no), np.uint16)   # and their fp16 values
+        self.v_oval = np.zeros((cap, no), np.uint16)
         s = _Head()
         s.d, s.bits, s.scheme = d, bits, scheme
         s.k_group, s.v_group, s.residual, s.n_sink = k_group, v_group, residual, n_sink
@@ -215,8 +233,10 @@ class OracleHead:
         s.k_normalize = 1 if k_norm else 0
         s.v_queue = 1 if v_queue else 0
         s.meta_f16 = 1 if meta_f16 else 0
+        s.outliers = int(outliers)
         for name in ("k_u", "v_u", "k_scale", "k_zero", "v_scale", "v_zero", "k_sym",
-                     "v_sym", "k_res", "v_res", "k_sink", "v_sink", "k_norm"):
+                     "v_sym", "k_res", "v_res", "k_sink", "v_sink", "k_norm", "k_oidx", "v_oidx",
+                     "k_oval", "v_oval"):
             setattr(s, name, _ptr(getattr(self, name)))
         self._s = s
 

@@ -178,6 +178,71 @@ int orc_choose_symmetric(float mn, float mx, int bits) {
   return fabsf(mx + mn) <= step;
 }
 
+/* ---- dense-and-sparse outliers ([KVQ4]) -------------------------------- */
+
+/*
+ * The k elements of largest magnitude of one fp16 row ([d] bits): those are
+ * the row's outliers.  The page computes per-token outlier thresholds online
+ * and keeps about 1 % of the elements; read as a fixed count k per token
+ * (1 % of d rounded up, chosen by the caller), equal magnitudes going to the
+ * lower channel.  idx receives the k channels in ascending order.
+ */
+void orc_select_outliers(const uint16_t *row, int d, int k, uint16_t *idx) {
+  uint8_t taken[256] = {0};
+  for (int j = 0; j < k; ++j) {
+    int best = -1;
+    float bm = -1.0f;
+    for (int c = 0; c < d; ++c) {
+      const float m = fabsf(orc_half_to_float(row[c]));
+      if (!taken[c] && m > bm) {
+        bm = m;
+        best = c;
+      }
+    }
+    taken[best] = 1;
+  }
+  int n = 0;
+  for (int c = 0; c < d; ++c)
+    if (taken[c]) idx[n++] = (uint16_t)c;
+}
+
+/* Records the outliers of the token row src (fp16, [d]) as token t's list
+ * and marks them in is_out[d]. */
+static void record_outliers(const orc_head *s, const uint16_t *src, int64_t t,
+                            uint16_t *oidx, uint16_t *oval, uint8_t *is_out) {
+  const int k = s->outliers;
+  memset(is_out, 0, (size_t)s->d);
+  orc_select_outliers(src, s->d, k, oidx + t * k);
+  for (int j = 0; j < k; ++j) {
+    const int c = oidx[t * k + j];
+    oval[t * k + j] = src[c];
+    is_out[c] = 1;
+  }
+}
+
+/*
+ * Asymmetric quantization of the inliers of one group: the statistics come
+ * from the elements with is_out == 0 only ([KVQ4]: removing the outliers
+ * narrows the range the codes span); outlier positions store code 0 (the
+ * decode reads their fp16 value instead).  No inlier: scale 0, zero 0.
+ */
+static void quant_inliers(const orc_head *s, const float *x, const uint8_t *is_out, int n,
+                          float *scale, float *zero, uint8_t *u, int64_t ustride) {
+  float in[256];
+  uint8_t code[256];
+  int m = 0;
+  for (int i = 0; i < n; ++i)
+    if (!is_out[i]) in[m++] = x[i];
+  if (m == 0) {
+    *scale = 0.0f;
+    *zero = 0.0f;
+  } else {
+    (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(in, m, s->bits, scale, zero, code, 1);
+  }
+  m = 0;
+  for (int i = 0; i < n; ++i) u[i * ustride] = is_out[i] ? 0 : code[m++];
+}
+
 /* ---- KIVI ------------------------------------------------------------- */
 
 /* Key group: G consecutive tokens (rows of src, stride d) quantized per
@@ -186,25 +251,44 @@ int orc_choose_symmetric(float mn, float mx, int bits) {
 static void kivi_quant_key_group(orc_head *s, const uint16_t *src, int64_t t0) {
   const int d = s->d, G = s->k_group;
   float *x = (float *)malloc(sizeof(float) * (size_t)G);
+  /* with outliers: each token's are found over its own row ([KVQ4]: per
+   * token, online), and each channel's statistics skip the group's tokens
+   * that hold an outlier there */
+  uint8_t *mask = s->outliers ? (uint8_t *)malloc((size_t)G * (size_t)d) : 0, col[256];
+  if (mask)
+    for (int i = 0; i < G; ++i)
+      record_outliers(s, src + (int64_t)i * d, t0 + i, s->k_oidx, s->k_oval, mask + i * d);
   for (int c = 0; c < d; ++c) {
     for (int i = 0; i < G; ++i) x[i] = orc_half_to_float(src[(int64_t)i * d + c]);
-    (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(
-        x, G, s->bits, &s->k_scale[(t0 / G) * d + c], &s->k_zero[(t0 / G) * d + c],
-        &s->k_u[t0 * d + c], d);
+    float *scale = &s->k_scale[(t0 / G) * d + c], *zero = &s->k_zero[(t0 / G) * d + c];
+    if (mask) {
+      for (int i = 0; i < G; ++i) col[i] = mask[i * d + c];
+      quant_inliers(s, x, col, G, scale, zero, &s->k_u[t0 * d + c], d);
+    } else {
+      (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(x, G, s->bits, scale, zero,
+                                                           &s->k_u[t0 * d + c], d);
+    }
   }
+  free(mask);
   free(x);
 }
 
 /* Value token: quantized per token in groups of v_group channels
- * ([KIVI] 为什么…: values per token). */
+ * ([KIVI] 为什么…: values per token); with outliers, the token's are found
+ * over the whole row and each group's statistics skip them. */
 static void kivi_quant_value_token(orc_head *s, const uint16_t *src, int64_t t) {
   const int d = s->d, Gv = s->v_group, ng = d / Gv;
   float x[256];
+  uint8_t is_out[256];
+  if (s->outliers) record_outliers(s, src, t, s->v_oidx, s->v_oval, is_out);
   for (int j = 0; j < ng; ++j) {
     for (int i = 0; i < Gv; ++i) x[i] = orc_half_to_float(src[j * Gv + i]);
-    (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(
-        x, Gv, s->bits, &s->v_scale[t * ng + j], &s->v_zero[t * ng + j], &s->v_u[t * d + j * Gv],
-        1);
+    float *scale = &s->v_scale[t * ng + j], *zero = &s->v_zero[t * ng + j];
+    if (s->outliers)
+      quant_inliers(s, x, is_out + j * Gv, Gv, scale, zero, &s->v_u[t * d + j * Gv], 1);
+    else
+      (s->meta_f16 ? orc_quant_asym_f16 : orc_quant_asym)(x, Gv, s->bits, scale, zero,
+                                                           &s->v_u[t * d + j * Gv], 1);
   }
 }
 
@@ -394,9 +478,20 @@ int orc_append(orc_head *s, const uint16_t *k, const uint16_t *v) {
   return 0;
 }
 
-/* Dequantized key / value element of quantized token t, channel c, in fp64. */
+/* fp16 outlier of token t at channel c from its list, or -1 when c is an
+ * inlier ([KVQ4]: the sparse part holds the outliers at full precision). */
+static int outlier_slot(const orc_head *s, const uint16_t *oidx, int64_t t, int c) {
+  for (int j = 0; j < s->outliers; ++j)
+    if (oidx[t * s->outliers + j] == c) return j;
+  return -1;
+}
+
+/* Dequantized key / value element of quantized token t, channel c, in fp64
+ * (an outlier: its fp16 value). */
 static double key_hat(const orc_head *s, int64_t t, int c) {
   const int d = s->d;
+  const int o = s->outliers ? outlier_slot(s, s->k_oidx, t, c) : -1;
+  if (o >= 0) return (double)orc_half_to_float(s->k_oval[t * s->outliers + o]);
   const double u = (double)s->k_u[t * d + c];
   if (s->scheme == ORC_KIVI) {
     const int64_t i = (t / s->k_group) * d + c;
@@ -408,6 +503,8 @@ static double key_hat(const orc_head *s, int64_t t, int c) {
 
 static double value_hat(const orc_head *s, int64_t t, int c) {
   const int d = s->d;
+  const int o = s->outliers ? outlier_slot(s, s->v_oidx, t, c) : -1;
+  if (o >= 0) return (double)orc_half_to_float(s->v_oval[t * s->outliers + o]);
   const int64_t i = t * (d / s->v_group) + c / s->v_group;
   return (double)s->v_u[t * d + c] * (double)s->v_scale[i] + (double)s->v_zero[i];
 }

@@ -14,6 +14,9 @@
  *             为什么键和值缓存应该沿着不同的维度进行量化, 工作原理.
  *   [KVQ2]    same page, KVQuant / 技术原理 二 (keys quantized before the rotary
  *             position embedding, the embedding applied after dequantization).
+ *   [KVQ4]    same page, KVQuant / 技术原理 四 (per-vector dense-and-sparse:
+ *             each vector's outliers kept apart in fp16, the rest quantized
+ *             over a narrower range; per-token thresholds computed online).
  *   [KVQ5]    same page, KVQuant / 技术原理 五、Attention Sink 感知量化.
  *   [IKV]     same page, IntactKV / KV Cache量化 (fp16 part concatenated with
  *             the dequantized cache at inference time).
@@ -58,6 +61,9 @@ typedef struct orc_head {
   int32_t v_queue;            /* KIVI: 1 = values leave fp16 one at a time (a queue) */
   int64_t n_vquant;           /* KIVI with v_queue: values held quantized */
   int32_t meta_f16;           /* 1 = scales and zeros stored in fp16 */
+  int32_t outliers;           /* KIVI: fp16 outliers kept per token and tensor (0 = none) */
+  uint16_t *k_oidx, *v_oidx;  /* [cap][outliers] channels of each token's outliers, ascending */
+  uint16_t *k_oval, *v_oval;  /* [cap][outliers] their fp16 values */
 } orc_head;
 
 int orc_rounding_is_nearest(void);
@@ -80,6 +86,7 @@ int orc_attend(const orc_head *s, const uint16_t *q, double tau, double *out);
 int orc_attend_rope(const orc_head *s, const uint16_t *q, double tau, double base,
                     int64_t pos0, double *out);
 
+void orc_select_outliers(const uint16_t *row, int d, int k, uint16_t *idx);
 void orc_pack(const uint8_t *u, int64_t n_rows, int d, int bits, uint8_t *out);
 void orc_pack_modes(const uint8_t *sym, int64_t n, uint32_t *out);
 

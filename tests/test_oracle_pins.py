@@ -606,6 +606,144 @@ def pin_kivi_value_queue_selector():
 
 
 # --------------------------------------------------------------------------
+# dense-and-sparse outliers (KVQuant per-vector), KIVI layout
+# --------------------------------------------------------------------------
+
+def pin_outlier_selection():
+    """A token's outliers are its k largest magnitudes, equal magnitudes going
+    to the lower channel: numpy's stable sort agrees on rows full of ties."""
+    rng = np.random.default_rng(50)
+    for trial in range(300):
+        d = int(rng.choice([16, 32, 64, 128]))
+        k = int(rng.integers(1, 5))
+        row = (rng.integers(-6, 7, d) * 0.5).astype(np.float16)   # many ties, +-0
+        if trial % 3 == 0:
+            row = _randn16(rng, d, scale=3.0)
+        order = np.argsort(-np.abs(row.astype(np.float32)), kind="stable")[:k]
+        assert list(oracle.select_outliers(row, k)) == sorted(order.tolist()), (row, k)
+
+
+def _outlier_head(d, bits, G, Gv, R, k, cap=256):
+    return oracle.OracleHead(d, bits, oracle.KIVI, G, Gv, R, 0, cap, outliers=k)
+
+
+def pin_outlier_statistics():
+    """Every quantized token stores its own outliers (channels and exact fp16
+    values); each key group's per-channel statistics and each value group's
+    come from the inliers alone (the quantizer applied to the elements left
+    after removing the outliers); outlier positions hold code 0."""
+    rng = np.random.default_rng(51)
+    d, G, Gv, R, k = 32, 8, 16, 16, 2
+    T = 70
+    K, V = _randn16(rng, T + 20, d), _randn16(rng, T + 20, d)
+    for arr in (K, V):
+        for t in range(T + 20):
+            c = rng.integers(0, d, 3)
+            arr[t, c] = (rng.choice([-1, 1], 3) * rng.uniform(20, 60, 3)).astype(np.float16)
+    h = _outlier_head(d, 2, G, Gv, R, k)
+    h.prefill(K[:T], V[:T])
+    for i in range(T, T + 20):
+        h.append(K[i], V[i])
+    n = h.n_quant
+    assert n == 80
+    for name, X, oidx, oval in (("k", K, h.k_oidx, h.k_oval), ("v", V, h.v_oidx, h.v_oval)):
+        for t in range(n):
+            sel = oracle.select_outliers(X[t], k)
+            assert np.array_equal(oidx[t], sel), (name, t)
+            assert np.array_equal(oval[t], X[t, sel].view(np.uint16)), (name, t)
+    for g in range(n // G):
+        for c in range(d):
+            toks = [t for t in range(g * G, (g + 1) * G) if c not in h.k_oidx[t]]
+            s_, z_, u_ = oracle.quant_asym(K[toks, c].astype(np.float32), 2)
+            assert h.k_scale[g, c] == s_ and h.k_zero[g, c] == z_, (g, c)
+            assert list(h.k_u[toks, c]) == list(u_)
+            outs = [t for t in range(g * G, (g + 1) * G) if c in h.k_oidx[t]]
+            assert all(h.k_u[t, c] == 0 for t in outs)
+    for t in range(n):
+        for j in range(d // Gv):
+            chans = [c for c in range(j * Gv, (j + 1) * Gv) if c not in h.v_oidx[t]]
+            s_, z_, u_ = oracle.quant_asym(V[t, chans].astype(np.float32), 2)
+            assert h.v_scale[t, j] == s_ and h.v_zero[t, j] == z_, (t, j)
+            assert list(h.v_u[t, chans]) == list(u_)
+
+
+def pin_attention_grid_exact_outliers():
+    """Inliers on a grid that every group still spans after its outliers are
+    removed, plus one loud outlier per token and tensor: the dense part is
+    lossless and the outliers are restored exactly, so attention equals
+    torch's fp64 SDPA on the raw tokens (prompt, flushes, residual)."""
+    rng = np.random.default_rng(52)
+    d, G, Gv, R, k, top = 32, 8, 16, 16, 1, 3
+    T = 96
+    K = np.empty((T, d), np.float64)
+    V = np.empty((T, d), np.float64)
+    kout = np.empty(T, int)
+    for g in range(T // G):
+        while True:   # each channel keeps at least two inlier tokens in the group
+            cs = rng.integers(0, d, G)
+            if np.bincount(cs, minlength=d).max() <= G - 2:
+                break
+        kout[g * G:(g + 1) * G] = cs
+        for c in range(d):
+            step = 2.0 ** -int(rng.integers(1, 4))
+            u = rng.integers(0, top + 1, G)
+            inl = [i for i in range(G) if cs[i] != c]
+            u[inl[0]], u[inl[1]] = 0, top
+            K[g * G:(g + 1) * G, c] = float(rng.integers(-8, 8)) * step + u * step
+    for t in range(T):
+        K[t, kout[t]] = float(rng.choice([-1, 1])) * (64 + int(rng.integers(0, 64)))
+        vo = []
+        for j in range(d // Gv):
+            step = 2.0 ** -int(rng.integers(1, 4))
+            u = rng.integers(0, top + 1, Gv)
+            u[0], u[1] = 0, top
+            V[t, j * Gv:(j + 1) * Gv] = float(rng.integers(-8, 8)) * step + u * step
+            vo.append(j * Gv + int(rng.integers(2, Gv)))
+        V[t, vo[int(rng.integers(0, len(vo)))]] = float(rng.choice([-1, 1])) * 96
+    K16, V16 = K.astype(np.float16), V.astype(np.float16)
+    assert np.array_equal(K16.astype(np.float64), K) and np.array_equal(V16.astype(np.float64), V)
+    h = _outlier_head(d, 2, G, Gv, R, k)
+    h.prefill(K16[:75], V16[:75])
+    for i in range(75, 91):
+        h.append(K16[i], V16[i])
+    assert (h.n_quant, h.n_resid) == (80, 11)
+    q = (_randn16(rng, d).astype(np.float32) / 16).astype(np.float16)
+    tau = 1 / math.sqrt(d)
+    np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K16[:91], V16[:91], tau), rtol=0,
+                               atol=1e-12)
+
+
+def pin_outlier_isolation_bounds_the_error():
+    """Gaussian tokens with a few loud elements: keeping k outliers per token
+    apart bounds every other element's error by its group's inlier half-step,
+    and the largest error falls well below that of the plain cache."""
+    rng = np.random.default_rng(53)
+    d, G, Gv, R, k = 64, 16, 32, 32, 2
+    K, V = _randn16(rng, 64, d), _randn16(rng, 64, d)
+    for t in range(64):
+        c = rng.choice(d, 2, replace=False)
+        K[t, c] = (rng.choice([-1, 1], 2) * 40).astype(np.float16)
+        V[t, c] = (rng.choice([-1, 1], 2) * 40).astype(np.float16)
+    ho, hp = _outlier_head(d, 4, G, Gv, R, k), oracle.OracleHead(d, 4, oracle.KIVI, G, Gv, R, 0, 256)
+    ho.prefill(K, V)
+    hp.prefill(K, V)
+    err = {}
+    for name, h in (("sparse", ho), ("plain", hp)):
+        kh = h.k_u[:64] * np.repeat(h.k_scale[:4], G, axis=0).astype(np.float64) \
+            + np.repeat(h.k_zero[:4], G, axis=0)
+        if name == "sparse":
+            for t in range(64):
+                inl = np.ones(d, bool)
+                inl[h.k_oidx[t]] = False
+                sc = np.repeat(h.k_scale[:4], G, axis=0)[t].astype(np.float64)
+                e = np.abs(kh[t] - K[t].astype(np.float64))[inl]
+                assert np.all(e <= sc[inl] / 2 + 1e-5), t
+                kh[t, h.k_oidx[t]] = K[t, h.k_oidx[t]]
+        err[name] = np.abs(kh - K.astype(np.float64)).max()
+    assert err["sparse"] * 10 < err["plain"], err
+
+
+# --------------------------------------------------------------------------
 # keys cached before the rotary position embedding
 # --------------------------------------------------------------------------
 
@@ -772,6 +910,13 @@ MUTANTS = [
      "float r = s == 0.0f ? 0.0f : rintf(x[i] / (a / lim));"),
     ("fp32 to fp16 truncates", "if (rem > half || (rem == half && (q & 1u))) q += 1;", "if (0) q += 1;"),
     ("fp32 to fp16 ties away", "(rem == half && (q & 1u))", "(rem == half)"),
+    ("outliers are the smallest", "if (!taken[c] && m > bm) {", "if (!taken[c] && (bm < 0.0f || m < bm)) {"),
+    ("outlier ties to the higher channel", "if (!taken[c] && m > bm) {", "if (!taken[c] && m >= bm) {"),
+    ("outliers kept in the statistics", "if (!is_out[i]) in[m++] = x[i];", "in[m++] = x[i];"),
+    ("key outlier not restored", "if (o >= 0) return (double)orc_half_to_float(s->k_oval[t * s->outliers + o]);",
+     "if (0) return (double)orc_half_to_float(s->k_oval[t * s->outliers + o]);"),
+    ("value outlier not restored", "if (o >= 0) return (double)orc_half_to_float(s->v_oval[t * s->outliers + o]);",
+     "if (0) return (double)orc_half_to_float(s->v_oval[t * s->outliers + o]);"),
     ("value group transposed", "x[i] = orc_half_to_float(src[j * Gv + i]);", "x[i] = orc_half_to_float(src[i * (d / Gv) + j]);"),
 ]
 
