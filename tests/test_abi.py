@@ -151,3 +151,33 @@ def test_strerror():
 def test_workload_configs_are_accepted():
     for w in synth.WORKLOADS.values():
         kvq.cache_sizes(kvq.config_of(w))
+
+
+def test_rope_decode_validates_before_touching_the_device():
+    """kvq_decode_attention_rope: the decode's checks, then the base (finite,
+    > 0) and the supported shapes (1, 2 or 4 query heads per KV head;
+    max_ctx <= 2^24 so positions are exact in fp32), all on the host."""
+    L = kvq.lib()
+    cfg = _cfg()
+    c = kvq.Cache()
+    c.blocks, c.k_res, c.v_res = 0x1000, 0x1000, 0x1000
+    q, out = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    ws, ws_n = ctypes.c_void_p(0x4000), kvq.workspace_bytes(cfg)
+
+    def call(cfg_, base, n=ws_n):
+        return L.kvq_decode_attention_rope(ctypes.byref(cfg_), ctypes.byref(c), q, out, 1.0,
+                                           base, ws, n, None)
+
+    assert L.kvq_decode_attention_rope(ctypes.byref(cfg), ctypes.byref(kvq.Cache()), q, out, 1.0,
+                                       10000.0, ws, ws_n, None) == kvq.KVQ_EINVAL
+    assert call(cfg, 10000.0, 16) == kvq.KVQ_ECAPACITY
+    for base in (0.0, -2.0, float("inf"), float("nan")):
+        assert call(cfg, base) == kvq.KVQ_EINVAL, base
+    rg8 = _cfg(n_q_heads=32, n_kv_heads=4)
+    assert call(rg8, 10000.0, kvq.workspace_bytes(rg8)) == kvq.KVQ_EUNSUPPORTED
+    long_ctx = _cfg(batch=1, n_q_heads=1, n_kv_heads=1, max_ctx=(1 << 24) + 1)
+    assert call(long_ctx, 10000.0, kvq.workspace_bytes(long_ctx)) == kvq.KVQ_EUNSUPPORTED
+    bad = kvq.Cache()
+    bad.blocks, bad.k_res, bad.v_res = 0x1001, 0x1000, 0x1000
+    assert L.kvq_decode_attention_rope(ctypes.byref(cfg), ctypes.byref(bad), q, out, 1.0,
+                                       10000.0, ws, ws_n, None) == kvq.KVQ_EALIGN
