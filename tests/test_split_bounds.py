@@ -80,3 +80,62 @@ def test_tc_split_never_exceeds_the_partial_slots(w):
                 worst, nw, total = _max_parts(BH, n_quant, n_fp16, ch, blocks)
                 assert nw <= total
                 assert worst <= stride, (w.name, n_quant, n_fp16, blocks, worst, stride)
+
+
+def _gqa_max_parts(cfg, BH, n_quant, n_fp16, blocks):
+    """Partial slots the grouped-query kernel's block-level split gives its
+    busiest head: 8 per block holding quantized units of the head, plus one
+    per warp with at least one of a block's fp16 chunks (the kernel's own
+    count).  Units: 128 quantized tokens, or CPU fp16 chunks of CH tokens."""
+    s = kvq.cache_sizes(cfg)
+    cap = (cfg.max_ctx + 127) // 128 * 128
+    block_bytes = s.blocks // (BH * (cap // 32))
+    ch = _fp16_chunk(cfg)
+    kmb = 2 * 128 * 4 if cfg.k_group > 32 else 0
+    cpu = max(1, (128 // 32) * (block_bytes + kmb) // (ch * 4 * 128))
+    nch = -(-n_fp16 // ch) if n_fp16 else 0
+    S_h, F_h = -(-n_quant // 128), -(-nch // cpu)
+    U = S_h + F_h
+    total = BH * U
+    nc = max(1, min(blocks, 1024, total))
+
+    def owner(x):
+        return ((x + 1) * nc - 1) // total
+
+    worst = 0
+    for bh in range(BH):
+        base, npart = bh * U, 0
+        if S_h:
+            npart = 8 * (owner(base + S_h - 1) - owner(base) + 1)
+        if F_h:
+            for x in range(owner(base + S_h), owner(base + U - 1) + 1):
+                x0, x1 = x * total // nc, (x + 1) * total // nc
+                fa, fb = max(x0 - base - S_h, 0), min(x1 - base - S_h, F_h)
+                c0 = fa * cpu
+                c1 = min(fb * cpu, nch) if fa < fb else c0
+                npart += min(8, c1 - c0)
+        worst = max(worst, npart)
+    return worst
+
+
+GQA_CASES = [synth.WORKLOADS["gqa_2bit"],
+             synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=2, n_q_heads=8, n_kv_heads=4,
+                          ctx=900, k_group=64, v_group=64),
+             synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=1, n_q_heads=4, n_kv_heads=1,
+                          ctx=1 << 20)]
+
+
+@pytest.mark.parametrize("w", GQA_CASES, ids=lambda w: "%s_B%d_T%d" % (w.name, w.batch, w.ctx))
+def test_gqa_split_never_exceeds_the_partial_slots(w):
+    """Block counts up to 8 resident blocks on each of 152 SMs (the kernel
+    fits at most 2: 112 KB of shared memory per block)."""
+    cfg = kvq.config_of(w)
+    stride = _part_stride(cfg)
+    BH = cfg.batch * cfg.n_kv_heads
+    cap = (cfg.max_ctx + 127) // 128 * 128
+    quant = sorted({1, 127, 128, 129, cap // 3, cap - 1, cap} & set(range(1, cap + 1)))
+    for n_quant in quant:
+        for n_fp16 in (0, 1, 9, cfg.residual):
+            for blocks in (1, 7, 152, 304, 608, 1216):
+                worst = _gqa_max_parts(cfg, BH, n_quant, n_fp16, blocks)
+                assert worst <= stride, (n_quant, n_fp16, blocks, worst, stride)
