@@ -204,10 +204,11 @@ def whole_job_gbs(bytes_per_rank, world, elapsed_ms):
 # CPU oracle (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 
-def oracle_decode_rate(w, seconds=12.0, n_heads=None):
-    """Times the CPU oracle's decode step (append + fp64 attention) on a sample
-    of KV heads for about `seconds`; returns (bytes/s scaled to the whole
-    batch, threads, description)."""
+def oracle_decode_rate(w, seconds=12.0, n_heads=None, rope_base=None):
+    """Times the CPU oracle's decode step (append + fp64 attention; with
+    rope_base, attention over keys cached before the rotary embedding) on a
+    sample of KV heads for about `seconds`; returns (bytes/s scaled to the
+    whole batch, threads, description)."""
     import oracle  # only the CPU-baseline leg imports the oracle
     from concurrent.futures import ThreadPoolExecutor
 
@@ -238,7 +239,10 @@ def oracle_decode_rate(w, seconds=12.0, n_heads=None):
         o.append(k[s], v[s])
         b, h = bh
         for hq in range(h * rg, (h + 1) * rg):
-            o.attend(qs[s % 4][b, hq], tau)
+            if rope_base is None:
+                o.attend(qs[s % 4][b, hq], tau)
+            else:
+                o.attend_rope(qs[s % 4][b, hq], tau, rope_base)
 
     steps, t0 = 0, time.perf_counter()
     byte_sum = 0.0
@@ -249,13 +253,14 @@ def oracle_decode_rate(w, seconds=12.0, n_heads=None):
             byte_sum += decode_bytes(w, o0.n_quant, o0.n_resid, o0.n_sink_used) * n_heads / BH
             steps += 1
     dt = time.perf_counter() - t0
-    desc = ("%d decode steps (append + fp64 attention) of %d of the %d KV heads "
+    desc = ("%d decode steps (append + fp64 attention%s) of %d of the %d KV heads "
             "(%d query heads each), %d threads, scaled to the whole batch by bytes"
-            % (steps, n_heads, BH, rg, threads))
+            % (steps, "" if rope_base is None else " over keys rotated by position", n_heads,
+               BH, rg, threads))
     return byte_sum / dt, threads, desc, steps
 
 
-def oracle_reference_rate(w, steps, warmup):
+def oracle_reference_rate(w, steps, warmup, rope_base=None):
     """The reference arm: `warmup` untimed then `steps` timed decode steps of
     the CPU oracle.  A step is one append + fp64 attention on a bounded sample
     of KV heads, one head per host thread; the heads rewind to their prompt
@@ -291,7 +296,10 @@ def oracle_reference_rate(w, steps, warmup):
         o.append(k[e], v[e])
         b, h = bh
         for hq in range(h * rg, (h + 1) * rg):
-            o.attend(qs[e % 4][b, hq], tau)
+            if rope_base is None:
+                o.attend(qs[e % 4][b, hq], tau)
+            else:
+                o.attend_rope(qs[e % 4][b, hq], tau, rope_base)
 
     byte_sum, t0 = 0.0, None
     with ThreadPoolExecutor(threads) as ex:
@@ -568,7 +576,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        rate, threads, desc = oracle_reference_rate(w, args.steps, args.warmup)
+        rate, threads, desc = oracle_reference_rate(w, args.steps, args.warmup, args.rope_base)
         gbs = rate / 1e9
         bytes_step = decode_bytes(w, w.ctx, 1, 0)
         line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
@@ -622,8 +630,9 @@ def main():
         "gpu_launches": r["timed_launches"],
         "clocks": r["clocks"],
     }
-    if rank == 0 and world == 1 and not args.skip_cpu and not rope:
-        rate, threads, desc, _ = oracle_decode_rate(w, seconds=args.cpu_seconds)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        rate, threads, desc, _ = oracle_decode_rate(w, seconds=args.cpu_seconds,
+                                                    rope_base=args.rope_base)
         line["cpu_baseline"] = {"value": rate / 1e9, "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": desc}
     if rank == 0:
