@@ -204,7 +204,7 @@ def whole_job_gbs(bytes_per_rank, world, elapsed_ms):
 # CPU oracle (reference arm and cpu_baseline)
 # ---------------------------------------------------------------------------
 
-def oracle_decode_rate(w, seconds=12.0, n_heads=None, rope_base=None):
+def oracle_decode_rate(w, seconds=12.0, n_heads=None, rope_base=None, threads=None):
     """Times the CPU oracle's decode step (append + fp64 attention; with
     rope_base, attention over keys cached before the rotary embedding) on a
     sample of KV heads for about `seconds`; returns (bytes/s scaled to the
@@ -212,7 +212,7 @@ def oracle_decode_rate(w, seconds=12.0, n_heads=None, rope_base=None):
     import oracle  # only the CPU-baseline leg imports the oracle
     from concurrent.futures import ThreadPoolExecutor
 
-    threads = max(1, len(os.sched_getaffinity(0)))
+    threads = threads or max(1, len(os.sched_getaffinity(0)))
     BH = w.batch * w.n_kv_heads
     n_heads = min(BH, n_heads or max(threads, 16))
     heads = [(i // w.n_kv_heads, i % w.n_kv_heads) for i in
@@ -635,6 +635,12 @@ def main():
                                                     rope_base=args.rope_base)
         line["cpu_baseline"] = {"value": rate / 1e9, "unit": "GB/s", "cores": threads,
                                 "kind": "oracle", "sample": desc}
+        if threads > 1:
+            rate1, _, desc1, _ = oracle_decode_rate(w, seconds=args.cpu_seconds / 4,
+                                                    rope_base=args.rope_base, threads=1,
+                                                    n_heads=16)
+            line["cpu_baseline"]["single_thread"] = {"value": rate1 / 1e9, "unit": "GB/s",
+                                                     "sample": desc1}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
