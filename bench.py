@@ -537,10 +537,38 @@ def run_gpu(args, w, rank, world):
     h2d = 2 * ks[0].numel() * 2 + qs[0].numel() * 2
     d2h = qs[0].numel() * 4
     assert c0.device_status() == 0
+
+    # secondary figures: kvq_append alone, plain launches with events around
+    # each over one epoch per cache copy, split into steps that store the
+    # token and steps that flush (quantize) the residual.  Taken after every
+    # figure above; a failure here drops only these.
+    def time_appends():
+        restore()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = {"store": [], "flush": []}
+        with torch.cuda.stream(stream):
+            for e in range(EPOCH):
+                for c in caches:
+                    kind = ("flush" if w.scheme == synth.KIVI and c.n_resid + 1 == w.residual
+                            else "store")
+                    ev0.record(stream)
+                    c.append(ks[e], vs[e], stream)
+                    ev1.record(stream)
+                    ev1.synchronize()
+                    times[kind].append(ev0.elapsed_time(ev1) * 1e3)
+        restore()
+        return {k: {"us_median": float(np.median(v)), "launches": len(v)}
+                for k, v in times.items() if v}
+
+    try:
+        append_stats = time_appends()
+    except Exception as exc:  # noqa: BLE001 -- secondary figure only
+        append_stats = {"error": str(exc)[:200]}
     return dict(warmup_steps=warm_replays * P, elapsed_ms=elapsed_ms, total_bytes=total_bytes,
                 decode_ms=decode_ms, timed_launches=timed_launches,
                 dstate_bytes=dstate_bytes, plain_ms=plain_ms, e2e_ms=e2e_ms,
                 e2e_bytes=e2e_bytes, n_e2e=n_e2e, h2d=h2d, d2h=d2h, clocks=clocks,
+                append=append_stats,
                 copies=copies, cache_bytes=cache_bytes, prefill_ms=float(np.median(pre_ms)),
                 prompt_bytes_in=prompt_bytes_in, l2=l2,
                 ws_cache_total=cache_bytes * copies)
@@ -627,6 +655,7 @@ def main():
         "e2e": {"value": whole_job_gbs(r["e2e_bytes"], world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "us_per_step": e2e_ms / r["n_e2e"] * 1e3, "steps": r["n_e2e"]},
+        "append": r.get("append"),
         "gpu_launches": r["timed_launches"],
         "clocks": r["clocks"],
     }
