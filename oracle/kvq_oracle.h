@@ -24,6 +24,15 @@
  *             §3.1 残差缓存设计, §3.2 内存节省计算示例.
  *   [INNERQ]  "【论文】InnerQ：硬件感知免调优KV缓存量化用于大语言模型" (euno.news),
  *             关键贡献, 方法论 1-4.
+ *
+ * Parity unpinned: orc_choose_symmetric's threshold.  The InnerQ page asks
+ * for the symmetric mode when a group is centred at zero and gives no
+ * threshold; the rule here (midpoint within half an asymmetric step of zero)
+ * is a choice.  Its implementation is pinned by worked boundary cases, the
+ * rule itself by nothing on the pages.  The other readings where the pages
+ * are silent (the value queue's pop, fp16 metadata rounding, the outlier
+ * count and tie rule, the rotary pairing) are each pinned against their
+ * stated definition.
  */
 #ifndef KVQ_ORACLE_H
 #define KVQ_ORACLE_H
