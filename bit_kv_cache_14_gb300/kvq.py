@@ -144,8 +144,15 @@ def _stream(stream) -> int:
 
 
 def _ptr(t: torch.Tensor) -> int:
-    assert t.is_contiguous()
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous (the library reads plain row-major buffers)")
     return t.data_ptr()
+
+
+def _need_f16(*ts) -> None:
+    for t in ts:
+        if t.dtype != torch.float16:
+            raise TypeError("expected a float16 tensor, got %s" % t.dtype)
 
 
 class QuantizedKVCache:
@@ -179,21 +186,23 @@ class QuantizedKVCache:
 
     def prefill(self, K: torch.Tensor, V: torch.Tensor, stream=None) -> None:
         """K, V: fp16 [B][H][T][d] on the device."""
-        assert K.dtype == torch.float16 and V.dtype == torch.float16 and K.shape == V.shape
+        _need_f16(K, V)
+        if K.shape != V.shape:
+            raise ValueError("K and V shapes differ: %s vs %s" % (tuple(K.shape), tuple(V.shape)))
         _check(lib().kvq_quantize_prefill(ctypes.byref(self.cfg), ctypes.byref(self.view),
                                           _ptr(K), _ptr(V), K.shape[2], _stream(stream)),
                "kvq_quantize_prefill")
 
     def append(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         """k, v: fp16 [B][H][d] on the device."""
-        assert k.dtype == torch.float16 and v.dtype == torch.float16
+        _need_f16(k, v)
         _check(lib().kvq_append(ctypes.byref(self.cfg), ctypes.byref(self.view), _ptr(k),
                                 _ptr(v), _stream(stream)), "kvq_append")
 
     def decode(self, q: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
                stream=None) -> torch.Tensor:
         """q: fp16 [B][Hq][d]; returns fp32 [B][Hq][d]."""
-        assert q.dtype == torch.float16
+        _need_f16(q)
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         if scale is None:
@@ -209,7 +218,7 @@ class QuantizedKVCache:
         """Attention over keys cached before the rotary embedding: q (fp16
         [B][Hq][d], un-rotated) belongs to the newest token; every key is
         rotated by its position inside the kernel.  Returns fp32 [B][Hq][d]."""
-        assert q.dtype == torch.float16
+        _need_f16(q)
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         if scale is None:
@@ -226,7 +235,7 @@ class QuantizedKVCache:
                       stream=None) -> torch.Tensor:
         """One decode step on device tensors: append k, v ([B][H][d] fp16), then
         attend with q; a single launch when the append needs no flush."""
-        assert k.dtype == torch.float16 and v.dtype == torch.float16 and q.dtype == torch.float16
+        _need_f16(k, v, q)
         if out is None:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         if scale is None:

@@ -181,3 +181,16 @@ def test_rope_decode_validates_before_touching_the_device():
     bad.blocks, bad.k_res, bad.v_res = 0x1001, 0x1000, 0x1000
     assert L.kvq_decode_attention_rope(ctypes.byref(cfg), ctypes.byref(bad), q, out, 1.0,
                                        10000.0, ws, ws_n, None) == kvq.KVQ_EALIGN
+
+
+def test_binding_rejects_bad_tensors_before_any_call():
+    """The binding checks dtype and layout itself (not with asserts, which
+    python -O strips): a wrong dtype or a non-contiguous tensor raises
+    before the library sees a pointer."""
+    import torch
+    with pytest.raises(ValueError):
+        kvq._ptr(torch.zeros(4, 4).t())
+    with pytest.raises(TypeError):
+        kvq._need_f16(torch.zeros(2, dtype=torch.float32))
+    kvq._need_f16(torch.zeros(2, dtype=torch.float16))
+    assert kvq._ptr(torch.zeros(3)) != 0
