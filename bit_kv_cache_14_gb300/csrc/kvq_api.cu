@@ -1,8 +1,9 @@
 // C ABI of libkvq: validation, buffer sizes, host counters, launches.
 // Declarations and contracts: include/kvq.h.
+#include <math.h>
 #include <string.h>
 
-#include <math.h>
+#include <atomic>
 
 #include "kvq_internal.cuh"
 #include "kvq_rope.cuh"
@@ -16,17 +17,19 @@ bool pow2_group(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
+// SM count per device, looked up once; calls from several host threads may
+// race to fill an entry, and all of them store the same value.
 int num_sms_cached() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  if (cache[dev] == 0) {
-    int n = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
       n = 152;
-    cache[dev] = n;
+    cache[dev].store(n, std::memory_order_relaxed);
   }
-  return cache[dev];
+  return n;
 }
 }  // namespace
 
