@@ -1,0 +1,82 @@
+"""The benchmark's GPU-arm JSON line keeps its contract, checked on the CPU:
+bench.main() runs with the GPU leg replaced by fixed figures (and the rank
+reduction on the CPU), and the one line it prints carries every key the
+contract names, with the whole-job value, the roofline of the timed kernel
+(traffic from the committed ncu summary while its source hash matches), the
+end-to-end figure, the launch count, the clocks and the oracle baseline."""
+import contextlib
+import io
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+BYTES = 134348800  # one decode launch on the Llama-2-7B-shaped layer, 4096 + 1 tokens
+
+
+def _fake_gpu(args, w, rank, world):
+    return dict(warmup_steps=1280, elapsed_ms=600.0, total_bytes=args.steps * BYTES,
+                decode_ms=0.0274, timed_launches=args.steps + args.steps // 128,
+                dstate_bytes=BYTES, plain_ms=0.031, e2e_ms=12.0, e2e_bytes=256 * BYTES,
+                n_e2e=256, h2d=196608, d2h=131072,
+                clocks={"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 9},
+                copies=5, cache_bytes=1, prefill_ms=0.65, prompt_bytes_in=536870912,
+                l2=136e6, ws_cache_total=5, append={"store": {"us_median": 3.0, "launches": 9}})
+
+
+@pytest.fixture
+def line(monkeypatch):
+    monkeypatch.setattr(bench, "run_gpu", _fake_gpu)
+    real = bench.max_over_ranks
+    monkeypatch.setattr(bench, "max_over_ranks", lambda v, world, device: real(v, world, "cpu"))
+
+    def run(*argv):
+        monkeypatch.setattr(sys, "argv", ["bench.py", *argv])
+        out = io.StringIO()
+        with contextlib.redirect_stdout(out):
+            bench.main()
+        rows = [r for r in out.getvalue().splitlines() if r.strip()]
+        assert len(rows) == 1
+        return json.loads(rows[0])
+    return run
+
+
+REQUIRED = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+            "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "roofline",
+            "e2e", "gpu_launches", "clocks")
+
+
+@pytest.mark.parametrize("rope", [False, True])
+def test_gpu_line_contract(line, rope):
+    argv = ["--steps", "2000", "--warmup", "5", "--cpu-seconds", "0.5"]
+    if rope:
+        argv += ["--rope-base", "10000"]
+    d = line(*argv)
+    for k in REQUIRED:
+        assert k in d, k
+    assert d["steps"] == 2000 and d["n_gpus"] == 1 and d["scaling"] == "weak"
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] == pytest.approx(2000 * BYTES / 0.6 / 1e9)
+    assert d["config"]["workload"] == "llama2_7b_2bit"
+    assert ("variant" in d["config"]) == rope
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(BYTES / 0.0274e-3 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"])
+    assert r["kernel"] == ("rope_decode_kernel" if rope else "tc_decode_kernel")
+    # from the committed ncu summary while its source hash matches (then at
+    # least the algorithmic bytes), else null
+    assert r["traffic"] is None or r["traffic"] > BYTES
+    e = d["e2e"]
+    assert set(("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")) <= set(e)
+    assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] > 0
+    assert set(("sm_mhz", "sm_max_mhz", "reasons")) <= set(d["clocks"])
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]
