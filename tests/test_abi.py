@@ -194,3 +194,33 @@ def test_binding_rejects_bad_tensors_before_any_call():
         kvq._need_f16(torch.zeros(2, dtype=torch.float32))
     kvq._need_f16(torch.zeros(2, dtype=torch.float16))
     assert kvq._ptr(torch.zeros(3)) != 0
+
+
+def test_binding_block_layout_matches_the_library():
+    """The binding's mirror of the block layout (used to read codes and
+    statistics back) gives the same block size as kvq_cache_sizes, for every
+    supported bits / scheme / group combination."""
+    cases = []
+    for bits in (2, 4):
+        for d in (64, 128):
+            for gv in (16, 32, 64, 128):
+                if d % gv:
+                    continue
+                for G in (16, 32, 64, 128):
+                    cases.append(dict(head_dim=d, bits=bits, v_group=gv, k_group=G,
+                                      residual=G * 2, scheme=kvq.KIVI))
+                for gk in (16, 32, 64, 128):
+                    if d % gk == 0:
+                        for sch in (kvq.INNERQ, kvq.INNERQ_KNORM):
+                            cases.append(dict(head_dim=d, bits=bits, v_group=gv, k_group=gk,
+                                              residual=8, n_sink=2, scheme=sch))
+    for kw in cases:
+        cfg = _cfg(batch=2, n_q_heads=3, n_kv_heads=3, max_ctx=300, **kw)
+        s = kvq.cache_sizes(cfg)
+        view = kvq.QuantizedKVCache.__new__(kvq.QuantizedKVCache)
+        view.cfg = cfg
+        off, bb, rb, ngv, ngk = view._block_layout()
+        BH, cap = 6, 384
+        extra = BH * cfg.head_dim * 4 if cfg.scheme == kvq.INNERQ_KNORM else 0
+        assert s.blocks == BH * (cap // 32) * bb + extra, kw
+        assert rb == cfg.head_dim * cfg.bits // 8 and bb % 128 == 0, kw
