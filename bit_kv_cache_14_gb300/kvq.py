@@ -119,6 +119,9 @@ def make_config(batch, n_q_heads, n_kv_heads, head_dim, bits, scheme, k_group, v
 
 def config_of(w, max_ctx: int | None = None) -> Config:
     """Config of a synth.Workload (max_ctx defaults to prompt + streamed tokens)."""
+    for name in ("v_queue", "meta_f16", "outliers"):
+        if getattr(w, name, False):
+            raise ValueError("%s: a cache-format variant the library does not build yet" % name)
     scheme = INNERQ_KNORM if getattr(w, "k_norm", False) else w.scheme
     return make_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.bits, scheme,
                        w.k_group, w.v_group, w.residual, w.n_sink,

@@ -59,6 +59,9 @@ class Workload:
     data_scale: float = 1.0          # multiplier on every key and value
     first_token_k_mult: float = 1.0
     k_norm: bool = False             # InnerQ: one-shot per-channel key normalization
+    v_queue: bool = False            # KIVI: values leave fp16 one at a time (a queue)
+    meta_f16: bool = False           # scales and zeros stored in fp16
+    outliers: int = 0                # KIVI: fp16 outliers kept per token and tensor
 
     @property
     def group_ratio(self) -> int:

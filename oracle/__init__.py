@@ -245,7 +245,9 @@ class OracleHead:
         cap = w.max_ctx() if cap is None else cap
         return cls(w.head_dim, w.bits, w.scheme, w.k_group, w.v_group, w.residual,
                    w.n_sink, cap, k_norm=getattr(w, "k_norm", False),
-                   v_queue=getattr(w, "v_queue", False))
+                   v_queue=getattr(w, "v_queue", False),
+                   meta_f16=getattr(w, "meta_f16", False),
+                   outliers=getattr(w, "outliers", 0))
 
     # counters
     def save_state(self):

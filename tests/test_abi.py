@@ -224,3 +224,13 @@ def test_binding_block_layout_matches_the_library():
         extra = BH * cfg.head_dim * 4 if cfg.scheme == kvq.INNERQ_KNORM else 0
         assert s.blocks == BH * (cap // 32) * bb + extra, kw
         assert rb == cfg.head_dim * cfg.bits // 8 and bb % 128 == 0, kw
+
+
+def test_config_refuses_variants_the_library_lacks():
+    """Workload fields for cache-format variants that only the oracle has so
+    far are refused, never silently dropped."""
+    base = synth.scaled(synth.WORKLOADS["tiny"])
+    kvq.config_of(base)
+    for kw in (dict(v_queue=True), dict(meta_f16=True), dict(outliers=1)):
+        with pytest.raises(ValueError):
+            kvq.config_of(synth.scaled(base, **kw))
