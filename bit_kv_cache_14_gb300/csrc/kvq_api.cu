@@ -39,6 +39,9 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   if (!cfg || !g) return KVQ_EINVAL;
   const kvq_config &c = *cfg;
   if (c.batch < 1 || c.n_kv_heads < 1 || c.n_q_heads < 1 || c.max_ctx < 1) return KVQ_EINVAL;
+  // at most 2^30 tokens per sequence: every byte size below stays far from
+  // overflow (65535 heads x 2^25 blocks x < 2^15 bytes)
+  if (c.max_ctx > (1LL << 30)) return KVQ_EUNSUPPORTED;
   if (c.n_q_heads % c.n_kv_heads != 0) return KVQ_EINVAL;
   if (c.scheme != KVQ_KIVI && c.scheme != KVQ_INNERQ && c.scheme != KVQ_INNERQ_KNORM)
     return KVQ_EINVAL;

@@ -105,7 +105,8 @@ extern "C" {
  *     when it later leaves the window) is first multiplied, in fp32, by
  *     r_c = 1 / n_c (fp32 division); decode multiplies q by n_c for the
  *     quantized tokens.  Sinks and window stay the raw fp16 keys.
- *   max_ctx: most tokens one sequence will hold (prompt + appended).
+ *   max_ctx: most tokens one sequence will hold (prompt + appended), at most
+ *     2^30 (KVQ_EUNSUPPORTED above).
  */
 typedef struct kvq_config {
   int32_t batch;

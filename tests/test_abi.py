@@ -94,6 +94,8 @@ def test_workspace_bytes():
     (dict(scheme=kvq.INNERQ, k_group=48), kvq.KVQ_EUNSUPPORTED),
     (dict(scheme=kvq.INNERQ_KNORM, k_group=48), kvq.KVQ_EUNSUPPORTED),
     (dict(scheme=3), kvq.KVQ_EINVAL),
+    (dict(max_ctx=(1 << 30) + 1), kvq.KVQ_EUNSUPPORTED),
+    (dict(max_ctx=1 << 62), kvq.KVQ_EUNSUPPORTED),
 ])
 def test_config_validation(kw, code):
     with pytest.raises(kvq.KVQError) as e:
