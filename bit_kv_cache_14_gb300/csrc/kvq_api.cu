@@ -147,6 +147,24 @@ static int check_cache(const Geometry &g, const kvq_cache *c) {
   return KVQ_OK;
 }
 
+// The host counters the library maintains must describe a state it can
+// reach (a corrupted struct must not steer a kernel past the buffers): every
+// call but prefill, which resets them, checks them first.
+static int check_counters(const Geometry &g, const kvq_cache *c) {
+  if (c->n_quant > g.cap || c->n_resid > g.residual || c->n_sink > g.n_sink) return KVQ_EINVAL;
+  if (c->n_quant + c->n_resid + c->n_sink > g.max_ctx) return KVQ_EINVAL;
+  if (g.scheme == KVQ_KIVI && (c->n_resid >= g.residual || c->n_quant % g.residual != 0))
+    return KVQ_EINVAL;
+  if (g.scheme == KVQ_INNERQ && g.residual > 0 && c->ring_head >= g.residual) return KVQ_EINVAL;
+  if (g.scheme == KVQ_INNERQ && g.residual == 0 && c->ring_head != 0) return KVQ_EINVAL;
+  return KVQ_OK;
+}
+
+static int check_state(const Geometry &g, const kvq_cache *c) {
+  const int r = check_cache(g, c);
+  return r != KVQ_OK ? r : check_counters(g, c);
+}
+
 static int from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA; }
 
 }  // namespace kvq
@@ -187,7 +205,7 @@ int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
-  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if ((r = check_cache(g, cache)) != KVQ_OK) return r;  // counters: reset below
   if (T < 0) return KVQ_EINVAL;
   if (T > 0 && (!K || !V)) return KVQ_EINVAL;
   if (T > 0 && (!aligned16(K) || !aligned16(V))) return KVQ_EALIGN;
@@ -221,7 +239,7 @@ int kvq_append(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k, const
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
-  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if ((r = check_state(g, cache)) != KVQ_OK) return r;
   if (!k || !v) return KVQ_EINVAL;
   if (!aligned16(k) || !aligned16(v)) return KVQ_EALIGN;
   if (cache->n_quant + cache->n_resid + cache->n_sink + 1 > g.max_ctx) return KVQ_ECAPACITY;
@@ -257,7 +275,7 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
-  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if ((r = check_state(g, cache)) != KVQ_OK) return r;
   if (!q || !out || !ws) return KVQ_EINVAL;
   if (!aligned16(q) || !aligned16(out) || !aligned16(ws)) return KVQ_EALIGN;
   if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
@@ -279,7 +297,7 @@ int kvq_decode_attention_rope(const kvq_config *cfg, const kvq_cache *cache, con
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
-  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if ((r = check_state(g, cache)) != KVQ_OK) return r;
   if (!q || !out || !ws) return KVQ_EINVAL;
   if (!aligned16(q) || !aligned16(out) || !aligned16(ws)) return KVQ_EALIGN;
   if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
@@ -302,7 +320,7 @@ int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
-  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if ((r = check_state(g, cache)) != KVQ_OK) return r;
   if (!k || !v || !q || !out || !ws) return KVQ_EINVAL;
   if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out) || !aligned16(ws))
     return KVQ_EALIGN;
@@ -341,7 +359,7 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
   if (!h_k || !h_v || !h_q || !h_out || !d_k || !d_v || !d_q || !d_out) return KVQ_EINVAL;
-  if ((r = check_cache(g, cache)) != KVQ_OK) return r;
+  if ((r = check_state(g, cache)) != KVQ_OK) return r;
   if (cache->n_quant + cache->n_resid + cache->n_sink + 1 > g.max_ctx) return KVQ_ECAPACITY;
   if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -141,6 +141,10 @@ typedef struct kvq_sizes {
  *   n_resid   KIVI: fp16 residual tokens (< R); InnerQ: window tokens (<= W)
  *   n_sink    InnerQ: sink tokens held (<= S)
  *   ring_head InnerQ: window slot of the oldest token once the window is full
+ * Every call except kvq_quantize_prefill (which resets them) first checks
+ * that the counters describe a reachable state (n_sink <= S, n_resid <= R or
+ * W, KIVI n_resid < R and n_quant a multiple of R, ring_head < W, n_quant <=
+ * capacity, all tokens <= max_ctx) and returns KVQ_EINVAL otherwise.
  */
 typedef struct kvq_cache {
   void *blocks;

@@ -236,3 +236,31 @@ def test_config_refuses_variants_the_library_lacks():
     for kw in (dict(v_queue=True), dict(meta_f16=True), dict(outliers=1)):
         with pytest.raises(ValueError):
             kvq.config_of(synth.scaled(base, **kw))
+
+
+def test_corrupted_counters_are_rejected_before_any_launch():
+    """Counters that no sequence of calls can produce (too many sinks or
+    residual tokens, a quantized count off the flush grid or past the
+    capacity, a ring head past the window) make every call but prefill return
+    KVQ_EINVAL instead of steering a kernel past the buffers."""
+    L = kvq.lib()
+    q, out = ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)
+    ws = ctypes.c_void_p(0x4000)
+    kivi = _cfg()
+    innerq = _cfg(scheme=kvq.INNERQ, bits=4, k_group=64, v_group=64, residual=32, n_sink=4)
+    for cfg, bad in ((kivi, dict(n_resid=128)), (kivi, dict(n_quant=100)),
+                     (kivi, dict(n_quant=4352 + 128)), (kivi, dict(n_quant=4352, n_resid=1)),
+                     (innerq, dict(n_sink=5)), (innerq, dict(n_resid=33)),
+                     (innerq, dict(ring_head=32))):
+        c = kvq.Cache()
+        for name in ("blocks", "k_meta", "k_mode", "v_mode", "k_res", "v_res", "k_sink",
+                     "v_sink"):
+            setattr(c, name, 0x1000)
+        for k, v in bad.items():
+            setattr(c, k, v)
+        n = kvq.workspace_bytes(cfg)
+        assert L.kvq_decode_attention(ctypes.byref(cfg), ctypes.byref(c), q, out, 1.0, ws, n,
+                                      None) == kvq.KVQ_EINVAL, bad
+        assert L.kvq_decode_attention_rope(ctypes.byref(cfg), ctypes.byref(c), q, out, 1.0,
+                                           10000.0, ws, n, None) == kvq.KVQ_EINVAL, bad
+        assert L.kvq_append(ctypes.byref(cfg), ctypes.byref(c), q, q, None) == kvq.KVQ_EINVAL, bad
