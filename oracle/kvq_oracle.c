@@ -426,6 +426,7 @@ int orc_append(orc_head *s, const uint16_t *k, const uint16_t *v) {
     int64_t nv = held - s->n_vquant;               /* queued fp16 values (queue) */
     if (s->n_resid + 1 == R && s->n_quant + R > s->cap) return -1;
     if (s->v_queue && nv + 1 == R && s->n_vquant + 1 > s->cap) return -1;
+    if (s->v_queue && (nv < 0 || nv >= R)) return -1;  /* not a reachable queue state */
     memcpy(s->k_res + s->n_resid * d, k, row);
     if (!s->v_queue) memcpy(s->v_res + s->n_resid * d, v, row);
     s->n_resid += 1;

@@ -702,15 +702,20 @@ def pin_attention_grid_exact_outliers():
         V[t, vo[int(rng.integers(0, len(vo)))]] = float(rng.choice([-1, 1])) * 96
     K16, V16 = K.astype(np.float16), V.astype(np.float16)
     assert np.array_equal(K16.astype(np.float64), K) and np.array_equal(V16.astype(np.float64), V)
-    h = _outlier_head(d, 2, G, Gv, R, k)
-    h.prefill(K16[:75], V16[:75])
-    for i in range(75, 91):
-        h.append(K16[i], V16[i])
-    assert (h.n_quant, h.n_resid) == (80, 11)
     q = (_randn16(rng, d).astype(np.float32) / 16).astype(np.float16)
     tau = 1 / math.sqrt(d)
-    np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K16[:91], V16[:91], tau), rtol=0,
-                               atol=1e-12)
+    # also combined with the value queue and with fp16 metadata (grid steps
+    # and bases are fp16 values, so both stay lossless)
+    for v_queue, meta_f16 in ((False, False), (True, False), (False, True), (True, True)):
+        h = oracle.OracleHead(d, 2, oracle.KIVI, G, Gv, R, 0, 256, outliers=k, v_queue=v_queue,
+                              meta_f16=meta_f16)
+        h.prefill(K16[:75], V16[:75])
+        for i in range(75, 91):
+            h.append(K16[i], V16[i])
+        assert (h.n_quant, h.n_resid) == (80, 11)
+        assert h.n_vquant == (91 - 15 if v_queue else 80)
+        np.testing.assert_allclose(h.attend(q, tau), _sdpa(q, K16[:91], V16[:91], tau), rtol=0,
+                                   atol=1e-12, err_msg=str((v_queue, meta_f16)))
 
 
 def pin_outlier_isolation_bounds_the_error():
