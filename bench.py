@@ -494,30 +494,32 @@ def run_gpu(args, w, rank, world):
     p1.synchronize()
     plain_ms = p0.elapsed_time(p1) / max(1, n_plain)
 
-    # end to end through the host-buffer entry point (pinned host memory in,
-    # host result out, every step)
+    # end to end through the host-buffer entry point: every step copies one
+    # pinned host block [k | v | q] in and the output rows back out, rotating
+    # over the same cache copies as the timed steps (an HBM-sized working set)
     restore()
-    c0 = caches[0]
-    d_k = torch.empty(ks.shape[1:], dtype=torch.float16, device=dev)
-    d_v, d_q = torch.empty_like(d_k), torch.empty(qs.shape[1:], dtype=torch.float16, device=dev)
+    nin = caches[0].step_input_halves()
+    d_in = torch.empty(nin, dtype=torch.float16, device=dev)
     d_out = torch.empty(qs.shape[1:], dtype=torch.float32, device=dev)
-    h_k = torch.from_numpy(Ks).pin_memory()
-    h_v = torch.from_numpy(Vs).pin_memory()
-    h_q = qs.cpu().pin_memory()
+    qs_host = qs.cpu()
+    h_in = torch.empty((EPOCH, nin), dtype=torch.float16).pin_memory()
+    for e in range(EPOCH):
+        h_in[e] = torch.cat([torch.from_numpy(Ks[e]).reshape(-1),
+                             torch.from_numpy(Vs[e]).reshape(-1), qs_host[e % 8].reshape(-1)])
     h_out = torch.empty(qs.shape[1:], dtype=torch.float32).pin_memory()
-    n_e2e = min(EPOCH, max(K_steps, 16))
+    n_e2e = min(P, max(K_steps, 256))
+    kvn = ks[0].numel()
 
     def host_step(i):
+        c = caches[i % copies]
+        e = (i // copies) % EPOCH
         if rope is None:
-            c0.decode_step_host(h_k[i], h_v[i], h_q[i % 8], h_out, d_k, d_v, d_q, d_out, scale,
-                                stream)
+            c.decode_step_host(h_in[e], h_out, d_in, d_out, scale, stream)
             return
-        # the same copies around the binding's calls: pinned host in, host result out
-        d_k.copy_(h_k[i], non_blocking=True)
-        d_v.copy_(h_v[i], non_blocking=True)
-        d_q.copy_(h_q[i % 8], non_blocking=True)
-        c0.append(d_k, d_v, stream)
-        c0.decode_rope(d_q, rope, d_out, scale, stream)
+        # the same single copy in and out around the binding's two calls
+        d_in.copy_(h_in[e], non_blocking=True)
+        c.append(d_in[:kvn].view(ks.shape[1:]), d_in[kvn:2 * kvn].view(ks.shape[1:]), stream)
+        c.decode_rope(d_in[2 * kvn:].view(qs.shape[1:]), rope, d_out, scale, stream)
         h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -530,13 +532,14 @@ def run_gpu(args, w, rank, world):
         e2e_bytes = 0
         for i in range(n_e2e):
             host_step(i)
-            e2e_bytes += ep_bytes[i]
+            e2e_bytes += ep_bytes[(i // copies) % EPOCH]
         x1.record(stream)
     x1.synchronize()
     e2e_ms = x0.elapsed_time(x1)
-    h2d = 2 * ks[0].numel() * 2 + qs[0].numel() * 2
+    h2d = nin * 2
     d2h = qs[0].numel() * 4
-    assert c0.device_status() == 0
+    for c in caches:
+        assert c.device_status() == 0
 
     # secondary figures: kvq_append alone, plain launches with events around
     # each over one epoch per cache copy, split into steps that store the
@@ -574,6 +577,124 @@ def run_gpu(args, w, rank, world):
                 ws_cache_total=cache_bytes * copies)
 
 
+# ---------------------------------------------------------------------------
+# the other named workloads: decode kernel alone, one line each
+# ---------------------------------------------------------------------------
+
+def prompt_on_device(w, dev):
+    """The workload's prompt K, V ([B][H][T][d] fp16) generated head by head on
+    the host cores (synth's seeded streams) and copied into device tensors."""
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+
+    shape = (w.batch, w.n_kv_heads, w.ctx, w.head_dim)
+    Kd = torch.empty(shape, dtype=torch.float16, device=dev)
+    Vd = torch.empty(shape, dtype=torch.float16, device=dev)
+
+    def one(idx):
+        b, h = divmod(idx, w.n_kv_heads)
+        k, v = synth.head_tokens(w, b, h, 0, w.ctx)
+        Kd[b, h].copy_(torch.from_numpy(k))
+        Vd[b, h].copy_(torch.from_numpy(v))
+
+    with ThreadPoolExecutor(max(1, min(16, len(os.sched_getaffinity(0))))) as ex:
+        list(ex.map(one, range(w.batch * w.n_kv_heads)))
+    return Kd, Vd
+
+
+def measure_config(w, dev, stream, peak):
+    """Prefill once per cache copy, append the workload's streamed token, then
+    time a CUDA graph of decode launches rotating over the copies (enough
+    copies that 3x the L2 is touched between two uses of one, at most 64)."""
+    import torch
+    from bit_kv_cache_14_gb300 import kvq
+
+    cfg = kvq.config_of(w)
+    t0 = time.time()
+    Kd, Vd = prompt_on_device(w, dev)
+    gen_s = time.time() - t0
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = decode_bytes(w, w.ctx, 0, 0)
+    copies = min(64, max(2, math.ceil(3 * l2 / max(1, per_copy)) + 1))
+    caches = [kvq.QuantizedKVCache(cfg, dev) for _ in range(copies)]
+    pre_ms = []
+    with torch.cuda.stream(stream):
+        for c in caches:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            c.prefill(Kd, Vd, stream)
+            e1.record(stream)
+            e1.synchronize()
+            pre_ms.append(e0.elapsed_time(e1))
+    prompt_bytes = 2 * Kd.numel() * 2
+    del Kd, Vd
+    Ks, Vs = synth.streamed(w, max(1, w.n_append))
+    k, v = torch.from_numpy(Ks[0]).to(dev), torch.from_numpy(Vs[0]).to(dev)
+    q = torch.from_numpy(synth.queries(w, 0)).to(dev)
+    outs = [torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in caches]
+    scale = 1.0 / math.sqrt(w.head_dim)
+    with torch.cuda.stream(stream):
+        for c in caches:
+            c.append(k, v, stream)
+    stream.synchronize()
+    c0 = caches[0]
+    nbytes = decode_bytes(w, c0.n_quant, c0.n_resid, c0.n_sink)
+    ideal_s = nbytes / (peak * 1e9)
+    M = max(2 * copies, min(256, int(0.05 / max(ideal_s, 1e-7))))
+    with torch.cuda.stream(stream):
+        for i in range(copies):  # warm the library outside capture
+            caches[i].decode(q, outs[i], scale, stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(M):
+            caches[i % copies].decode(q, outs[i % copies], scale, stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+        stream.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        d0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        d1.record(stream)
+    d1.synchronize()
+    us = d0.elapsed_time(d1) / (reps * M) * 1e3
+    for c in caches:
+        assert c.device_status() == 0
+    gbs = nbytes / (us * 1e-6) / 1e9
+    touched = (copies - 1) * per_copy
+    return {
+        "kernel": kvq.decode_kernel_name(cfg, c0.n_quant),
+        "us": us, "gbs": gbs, "frac": gbs / peak, "algorithmic_bytes_per_launch": nbytes,
+        "state": {"n_quant": c0.n_quant, "n_resid": c0.n_resid, "n_sink": c0.n_sink},
+        "launches_timed": reps * M,
+        "l2_policy": "rotating %d cache copies (%.0f MB touched between uses of one copy vs %.0f "
+                     "MB L2)%s" % (copies, touched / 1e6, l2 / 1e6,
+                                   "" if touched > l2 else
+                                   "; smaller than L2: L2-resident, latency-bound, not an HBM "
+                                   "number"),
+        "prefill": {"ms": float(np.median(pre_ms)), "bytes_in": prompt_bytes,
+                    "gbs_in": prompt_bytes / (float(np.median(pre_ms)) * 1e-3) / 1e9},
+        "host_generation_s": gen_s,
+    }
+
+
+def run_configs(names, peak):
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    stream = torch.cuda.Stream(dev)
+    out = {}
+    for name in names:
+        try:
+            out[name] = measure_config(synth.WORKLOADS[name], dev, stream, peak)
+        except Exception as exc:  # noqa: BLE001 -- one config's failure drops only its line
+            out[name] = {"error": ("%s: %s" % (type(exc).__name__, exc))[:300]}
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -583,6 +704,10 @@ def main():
     ap.add_argument("--workload", default="llama2_7b_2bit", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--skip-cpu", action="store_true", help="omit the cpu_baseline leg")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--configs", default="others",
+                    help="comma-separated workloads whose decode kernel is also timed alone "
+                         "(one GPU only); 'others' = every named workload but the headline one, "
+                         "'none' = skip")
     ap.add_argument("--rope-base", type=float, default=None,
                     help="time the variant whose keys are cached before the rotary embedding "
                          "(kvq_decode_attention_rope with this base) instead of the plain decode")
@@ -659,6 +784,10 @@ def main():
         "gpu_launches": r["timed_launches"],
         "clocks": r["clocks"],
     }
+    if world == 1 and args.configs != "none" and args.rope_base is None:
+        names = ([n for n in synth.WORKLOADS if n != w.name] if args.configs == "others"
+                 else [n for n in args.configs.split(",") if n])
+        line["configs"] = run_configs(names, peak)
     if rank == 0 and world == 1 and not args.skip_cpu:
         rate, threads, desc, _ = oracle_decode_rate(w, seconds=args.cpu_seconds,
                                                     rope_base=args.rope_base)

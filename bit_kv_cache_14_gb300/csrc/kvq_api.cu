@@ -1,6 +1,7 @@
 // C ABI of libkvq: validation, buffer sizes, host counters, launches.
 // Declarations and contracts: include/kvq.h.
 #include <math.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <atomic>
@@ -20,9 +21,9 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 // SM count per device, looked up once; calls from several host threads may
 // race to fill an entry, and all of them store the same value.
 int num_sms_cached() {
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  static std::atomic<int> cache[kMaxDevices];
+  const int dev = device_slot();
+  if (dev < 0) return 152;
   int n = cache[dev].load(std::memory_order_relaxed);
   if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
@@ -34,6 +35,12 @@ int num_sms_cached() {
 }  // namespace
 
 void note_launch(int n) { t_last_launches = n; }
+
+int device_slot() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
 
 int resolve(const kvq_config *cfg, Geometry *g) {
   if (!cfg || !g) return KVQ_EINVAL;
@@ -167,6 +174,17 @@ static int check_state(const Geometry &g, const kvq_cache *c) {
 
 static int from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA; }
 
+int check_decode_call(const Geometry &g, const kvq_cache *cache, const uint16_t *q,
+                      const float *out, float softmax_scale, const void *ws, size_t ws_bytes) {
+  int r;
+  if ((r = check_state(g, cache)) != KVQ_OK) return r;
+  if (!q || !out || !ws) return KVQ_EINVAL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(ws)) return KVQ_EALIGN;
+  if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
+  if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
+  return KVQ_OK;
+}
+
 }  // namespace kvq
 
 using namespace kvq;
@@ -275,11 +293,7 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
-  if ((r = check_state(g, cache)) != KVQ_OK) return r;
-  if (!q || !out || !ws) return KVQ_EINVAL;
-  if (!aligned16(q) || !aligned16(out) || !aligned16(ws)) return KVQ_EALIGN;
-  if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
-  if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
+  if ((r = check_decode_call(g, cache, q, out, softmax_scale, ws, ws_bytes)) != KVQ_OK) return r;
   const DecodePlan plan =
       plan_decode(g, cache->n_quant, cache->n_resid + cache->n_sink, num_sms_cached());
   r = from_cuda(launch_decode(g, ptrs_of(g, cache), plan, cache->n_quant, cache->n_resid,
@@ -351,26 +365,26 @@ int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k
   return KVQ_OK;
 }
 
-int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *h_k,
-                         const uint16_t *h_v, const uint16_t *h_q, float *h_out, uint16_t *d_k,
-                         uint16_t *d_v, uint16_t *d_q, float *d_out, float softmax_scale,
+int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *h_in,
+                         float *h_out, uint16_t *d_in, float *d_out, float softmax_scale,
                          void *ws, size_t ws_bytes, void *stream) {
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
-  if (!h_k || !h_v || !h_q || !h_out || !d_k || !d_v || !d_q || !d_out) return KVQ_EINVAL;
+  if (!h_in || !h_out || !d_in || !d_out) return KVQ_EINVAL;
   if ((r = check_state(g, cache)) != KVQ_OK) return r;
+  if (!aligned16(d_in) || !aligned16(d_out)) return KVQ_EALIGN;
   if (cache->n_quant + cache->n_resid + cache->n_sink + 1 > g.max_ctx) return KVQ_ECAPACITY;
   if (ws_bytes < decode_workspace_bytes(g)) return KVQ_ECAPACITY;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t kv_bytes = (size_t)g.B * g.H * g.d * 2, q_bytes = (size_t)g.B * g.Hq * g.d * 2;
-  const size_t o_bytes = (size_t)g.B * g.Hq * g.d * 4;
-  if (cudaMemcpyAsync(d_k, h_k, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(d_v, h_v, kv_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(d_q, h_q, q_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+  // [k | v | q]: each part is a multiple of 8 halves (d is), so every part
+  // of the device staging buffer stays 16-byte aligned
+  const size_t kv = (size_t)g.B * g.H * g.d, qn = (size_t)g.B * g.Hq * g.d;
+  const size_t in_bytes = (2 * kv + qn) * 2, o_bytes = qn * 4;
+  if (cudaMemcpyAsync(d_in, h_in, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return KVQ_ECUDA;
-  if ((r = kvq_append_decode(cfg, cache, d_k, d_v, d_q, d_out, softmax_scale, ws, ws_bytes,
-                             stream)) != KVQ_OK)
+  if ((r = kvq_append_decode(cfg, cache, d_in, d_in + kv, d_in + 2 * kv, d_out, softmax_scale, ws,
+                             ws_bytes, stream)) != KVQ_OK)
     return r;
   const int launches = kvq_last_launch_count();
   if (cudaMemcpyAsync(h_out, d_out, o_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
@@ -395,6 +409,22 @@ int kvq_get_device_status(kvq_cache *cache, void *stream) {
 }
 
 int kvq_last_launch_count(void) { return t_last_launches; }
+
+int kvq_decode_kernel_name(const kvq_config *cfg, int64_t n_quant, char *buf, size_t len) {
+  if (!buf || len == 0 || n_quant < 0) return KVQ_EINVAL;
+  Geometry g;
+  const int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  int n;
+  if (n_quant > 0 && tc_decode_supported(g))
+    n = tc_variant_name(g, buf, len);
+  else if (n_quant > 0 && gqa_decode_supported(g))
+    n = gqa_variant_name(g, buf, len);
+  else
+    n = snprintf(buf, len, "decode_kernel<d=%d,bits=%d,rg=%d,scheme=%s>", g.d, g.bits, g.Hq / g.H,
+                 g.scheme == KVQ_KIVI ? "kivi" : "innerq");
+  return (n < 0 || (size_t)n >= len) ? KVQ_EINVAL : KVQ_OK;
+}
 
 void kvq_debug_stall_waits(int64_t iterations) {
   set_debug_stall(iterations < 0 ? 0 : (long long)iterations);

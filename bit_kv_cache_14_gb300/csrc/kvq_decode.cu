@@ -365,18 +365,15 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
   const int64_t p0 = (int64_t)bh * a.s_max * RG;
   for (int i = tid; i < a.n_split * RG * D; i += kBlock) a.ws_o[p0 * D + i] = 0.0f;
   for (int i = tid; i < a.n_split * RG * 2; i += kBlock) a.ws_ml[p0 * 2 + i] = 0.0f;
-  if (tid == 0) a.ws_cnt[bh] = 0;
+  if (tid == 0) atomicExch(&a.ws_cnt[bh], 0);  // an atomic, like the tickets it resets
 }
 
 template <int D, int BITS, int RG, int SCHEME>
 cudaError_t launch_t(const DecodeArgs &a, int smem_bytes, cudaStream_t st) {
-  static int configured = 0;
-  if (configured < smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BITS, RG, SCHEME>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-    configured = smem_bytes;
-  }
+  static KernelSetup setup;
+  const cudaError_t e = kernel_setup(setup, decode_kernel<D, BITS, RG, SCHEME>, kBlock, smem_bytes,
+                                     nullptr);
+  if (e != cudaSuccess) return e;
   decode_kernel<D, BITS, RG, SCHEME>
       <<<dim3((unsigned)a.n_split, (unsigned)(a.g.B * a.g.H)), kBlock, smem_bytes, st>>>(a);
   return cudaGetLastError();

@@ -24,6 +24,8 @@
 //    warp publishes its partial (RG rows) and takes a ticket with a relaxed
 //    atomic, and the last ticket's holder merges (fence-free, the same
 //    encoding as the MHA merge).
+#include <stdio.h>
+
 #include "kvq_tc_common.cuh"
 
 namespace kvq {
@@ -95,10 +97,10 @@ __device__ bool merge_strided(const TcArgs &a, int64_t row0, int stride, int n, 
   M = -INFINITY;
   for (int s = lane; s < n; s += 32) {
     const int64_t row = row0 + (int64_t)s * stride;
-    uint2 v = __ldcg(ml + row);
+    uint2 v = ld_relaxed(ml + row);
     for (int it = 0; it < kMergePolls && (v.x == 0u || v.y == 0u); ++it) {
       __nanosleep(32);
-      v = __ldcg(ml + row);
+      v = ld_relaxed(ml + row);
     }
     ok = ok && v.x != 0u && v.y != 0u;
     M = fmaxf(M, __uint_as_float(v.x ^ kEnc));
@@ -110,7 +112,7 @@ __device__ bool merge_strided(const TcArgs &a, int64_t row0, int stride, int n, 
   for (int s0 = 0; s0 < n && ok; s0 += 32) {
     float w = 0.0f;
     if (s0 + lane < n) {
-      const uint2 v = __ldcg(ml + row0 + (int64_t)(s0 + lane) * stride);
+      const uint2 v = ld_relaxed(ml + row0 + (int64_t)(s0 + lane) * stride);
       const float ms = __uint_as_float(v.x ^ kEnc);
       if (ms != -INFINITY) {
         w = exp2f(ms - M);
@@ -126,7 +128,7 @@ __device__ bool merge_strided(const TcArgs &a, int64_t row0, int stride, int n, 
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           o[j] = j0 + j < nb
-                     ? __ldcg(wo + (row0 + (int64_t)(s0 + j0 + j) * stride) * (kD / 4) + lane)
+                     ? ld_relaxed(wo + (row0 + (int64_t)(s0 + j0 + j) * stride) * (kD / 4) + lane)
                      : make_uint4(1, 1, 1, 1);
           mine = mine && o[j].x != 0u && o[j].y != 0u && o[j].z != 0u && o[j].w != 0u;
         }
@@ -150,10 +152,10 @@ __device__ bool merge_strided(const TcArgs &a, int64_t row0, int stride, int n, 
   for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   O = make_float4(acc[0], acc[1], acc[2], acc[3]);
   for (int s = 0; s < n; ++s)
-    reinterpret_cast<uint4 *>(a.ws_o)[(row0 + (int64_t)s * stride) * (kD / 4) + lane] =
-        make_uint4(0, 0, 0, 0);
+    st_relaxed(reinterpret_cast<uint4 *>(a.ws_o) + (row0 + (int64_t)s * stride) * (kD / 4) + lane,
+               make_uint4(0, 0, 0, 0));
   for (int s = lane; s < n; s += 32)
-    reinterpret_cast<uint2 *>(a.ws_ml)[row0 + (int64_t)s * stride] = make_uint2(0, 0);
+    st_relaxed(reinterpret_cast<uint2 *>(a.ws_ml) + row0 + (int64_t)s * stride, make_uint2(0, 0));
   if (!__all_sync(0xffffffffu, ok)) {
     if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
     return false;
@@ -177,7 +179,7 @@ __device__ bool gqa_finish(const TcArgs &a, int bh, int ticket) {
     reinterpret_cast<float4 *>(a.out + ((int64_t)b * a.g.Hq + h * RG + r) * kD)[lane] =
         make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
   }
-  if (lane == 0) a.ws_cnt[bh] = 0;
+  if (lane == 0) atomicExch(&a.ws_cnt[bh], 0);  // an atomic, like the tickets it resets
   return true;
 }
 
@@ -356,10 +358,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
     const int64_t row0 = ((int64_t)bh * a.part_stride + slot) * RG;
 #pragma unroll
     for (int r = 0; r < RG; ++r) {
-      reinterpret_cast<uint4 *>(a.ws_o + (row0 + r) * kD)[lane] = enc4(o[r]);
+      st_relaxed(reinterpret_cast<uint4 *>(a.ws_o + (row0 + r) * kD) + lane, enc4(o[r]));
       if (lane == 0)
-        reinterpret_cast<uint2 *>(a.ws_ml)[row0 + r] =
-            make_uint2(__float_as_uint(m[r]) ^ kEnc, __float_as_uint(l[r]) ^ kEnc);
+        st_relaxed(reinterpret_cast<uint2 *>(a.ws_ml) + row0 + r,
+                   make_uint2(__float_as_uint(m[r]) ^ kEnc, __float_as_uint(l[r]) ^ kEnc));
     }
     pend_ticket = 0;
     if (lane == 0) pend_ticket = atomicAdd(&a.ws_cnt[bh], 1);
@@ -691,33 +693,43 @@ cudaError_t launch_gqa_t(TcArgs &a, int num_sms, cudaStream_t st) {
   using C = GqaCfg<NGV, KM, RG>;
   auto kern = tc_gqa_kernel<NGV, KM, RG>;
   if (a.g.block_bytes != C::BB || tc_fp16_chunk(a.g) != C::CH) return cudaErrorInvalidValue;
-  static int occ = 0;
-  if (occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::smem);
-    if (e != cudaSuccess) return e;
-    int o = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads, C::smem);
-    if (e != cudaSuccess) return e;
-    occ = o < 1 ? 1 : o;
-  }
+  static KernelSetup setup;
+  int occ = 0;
+  const cudaError_t e = kernel_setup(setup, kern, kThreads, C::smem, &occ);
+  if (e != cudaSuccess) return e;
   int64_t nc = (int64_t)num_sms * occ;
   if (nc > kTcMaxBlocks) nc = kTcMaxBlocks;
   if (nc > a.total) nc = a.total;
   if (nc < 1) nc = 1;
   a.nc = (int)nc;
-  kern<<<(unsigned)nc, kThreads, C::smem, st>>>(a);
-  return cudaGetLastError();
+  // every block must be resident: the last ticket's holder waits for the others
+  if (nc > (int64_t)num_sms * occ) return cudaErrorCooperativeLaunchTooLarge;
+  const cudaError_t le = launch_cooperative(kern, (unsigned)nc, kThreads, C::smem, st, a);
+  return le != cudaSuccess ? le : cudaGetLastError();
+}
+
+// The template arguments the dispatch picks for a geometry.
+struct GqaVariant {
+  int ngv, km, rg;
+};
+GqaVariant gqa_variant(const Geometry &g) {
+  return GqaVariant{kD / g.v_group, g.k_group == 32 ? 1 : 0, g.Hq / g.H};
 }
 
 template <int RG>
 cudaError_t launch_gqa_r(TcArgs &a, int num_sms, cudaStream_t st) {
-  const int ngv = kD / a.g.v_group;
-  const int km = a.g.k_group == 32 ? 1 : 0;
-  if (ngv == 4) return km ? launch_gqa_t<4, 1, RG>(a, num_sms, st) : launch_gqa_t<4, 0, RG>(a, num_sms, st);
-  return km ? launch_gqa_t<2, 1, RG>(a, num_sms, st) : launch_gqa_t<2, 0, RG>(a, num_sms, st);
+  const GqaVariant v = gqa_variant(a.g);
+  if (v.ngv == 4)
+    return v.km ? launch_gqa_t<4, 1, RG>(a, num_sms, st) : launch_gqa_t<4, 0, RG>(a, num_sms, st);
+  return v.km ? launch_gqa_t<2, 1, RG>(a, num_sms, st) : launch_gqa_t<2, 0, RG>(a, num_sms, st);
 }
 
 }  // namespace
+
+int gqa_variant_name(const Geometry &g, char *buf, size_t len) {
+  const GqaVariant v = gqa_variant(g);
+  return snprintf(buf, len, "tc_gqa_kernel<ngv=%d,km=%d,rg=%d>", v.ngv, v.km, v.rg);
+}
 
 bool gqa_decode_supported(const Geometry &g) {
   if (g.d != kD || g.bits != 2 || g.scheme != KVQ_KIVI) return false;

@@ -37,6 +37,8 @@
 //    zero points enter as q.zero per key group and sum_t p_t zero_tj per value
 //    group (CUDA cores).  q is normalised by a power of two so no fp16 operand
 //    can overflow (|q| <= 1, scales <= 65504).
+#include <stdio.h>
+
 #include "kvq_tc_common.cuh"
 
 namespace kvq {
@@ -809,15 +811,10 @@ cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   if (a.g.block_bytes != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::BB ||
       tc_fp16_chunk(a.g) != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::CH)
     return cudaErrorInvalidValue;
-  static int occ = 0;
-  if (occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    int o = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kThreads, smem);
-    if (e != cudaSuccess) return e;
-    occ = o < 1 ? 1 : o;
-  }
+  static KernelSetup setup;
+  int occ = 0;
+  const cudaError_t e = kernel_setup(setup, kern, kThreads, smem, &occ);
+  if (e != cudaSuccess) return e;
   int64_t nc = (int64_t)num_sms * occ;
   if (nc > kTcMaxBlocks) nc = kTcMaxBlocks;
   // every working warp gets at least one unit
@@ -827,29 +824,43 @@ cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   nc = (nw + kWarps - 1) / kWarps;
   a.nc = (int)nc;
   a.nw = (int)nw;
-  kern<<<(unsigned)nc, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  // every block must be resident: the merging warps wait for other blocks
+  if (nc > (int64_t)num_sms * occ) return cudaErrorCooperativeLaunchTooLarge;
+  const cudaError_t le = launch_cooperative(kern, (unsigned)nc, kThreads, smem, st, a);
+  return le != cudaSuccess ? le : cudaGetLastError();
+}
+
+// The template arguments the dispatch picks for a geometry (one function, so
+// the launch and kvq_decode_kernel_name cannot disagree).
+struct TcVariant {
+  int ngv, ngk, km;
+};
+TcVariant tc_variant(const Geometry &g) {
+  TcVariant v{kD / g.v_group, 1, 0};
+  if (g.scheme == KVQ_KIVI)
+    v.km = g.k_group == 16 ? 2 : g.k_group == 32 ? 1 : 0;
+  else
+    v.ngk = kD / g.k_group;
+  return v;
 }
 
 template <int BITS, int SCHEME>
 cudaError_t launch_tc_v(TcArgs &a, int num_sms, cudaStream_t st) {
-  const int ngv = kD / a.g.v_group;
+  const TcVariant v = tc_variant(a.g);
   if constexpr (SCHEME == KVQ_KIVI) {
-    const int G = a.g.k_group;
-    if (ngv == 4)
-      return G == 16 ? launch_tc_t<BITS, SCHEME, 4, 1, 2>(a, num_sms, st)
-           : G == 32 ? launch_tc_t<BITS, SCHEME, 4, 1, 1>(a, num_sms, st)
-                     : launch_tc_t<BITS, SCHEME, 4, 1, 0>(a, num_sms, st);
-    return G == 16 ? launch_tc_t<BITS, SCHEME, 2, 1, 2>(a, num_sms, st)
-         : G == 32 ? launch_tc_t<BITS, SCHEME, 2, 1, 1>(a, num_sms, st)
-                   : launch_tc_t<BITS, SCHEME, 2, 1, 0>(a, num_sms, st);
+    if (v.ngv == 4)
+      return v.km == 2 ? launch_tc_t<BITS, SCHEME, 4, 1, 2>(a, num_sms, st)
+           : v.km == 1 ? launch_tc_t<BITS, SCHEME, 4, 1, 1>(a, num_sms, st)
+                       : launch_tc_t<BITS, SCHEME, 4, 1, 0>(a, num_sms, st);
+    return v.km == 2 ? launch_tc_t<BITS, SCHEME, 2, 1, 2>(a, num_sms, st)
+         : v.km == 1 ? launch_tc_t<BITS, SCHEME, 2, 1, 1>(a, num_sms, st)
+                     : launch_tc_t<BITS, SCHEME, 2, 1, 0>(a, num_sms, st);
   } else {
-    const int ngk = kD / a.g.k_group;
-    if (ngv == 4)
-      return ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, 0>(a, num_sms, st)
-                      : launch_tc_t<BITS, SCHEME, 4, 2, 0>(a, num_sms, st);
-    return ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, 0>(a, num_sms, st)
-                    : launch_tc_t<BITS, SCHEME, 2, 2, 0>(a, num_sms, st);
+    if (v.ngv == 4)
+      return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, 0>(a, num_sms, st)
+                        : launch_tc_t<BITS, SCHEME, 4, 2, 0>(a, num_sms, st);
+    return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, 0>(a, num_sms, st)
+                      : launch_tc_t<BITS, SCHEME, 2, 2, 0>(a, num_sms, st);
   }
 }
 
@@ -859,6 +870,12 @@ int g_stall_limit = 0;
 
 void set_debug_stall(long long n) { g_stall_limit = n > (1 << 30) ? (1 << 30) : (int)n; }
 int debug_stall_limit() { return g_stall_limit; }
+
+int tc_variant_name(const Geometry &g, char *buf, size_t len) {
+  const TcVariant v = tc_variant(g);
+  return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d>", g.bits,
+                  g.scheme == KVQ_KIVI ? "kivi" : "innerq", v.ngv, v.ngk, v.km);
+}
 
 bool tc_decode_supported(const Geometry &g) {
   if (g.d != kD || g.Hq != g.H) return false;

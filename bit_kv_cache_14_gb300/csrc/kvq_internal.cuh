@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -74,7 +77,81 @@ __device__ __forceinline__ float *kivi_key_meta(const Geometry &g, const CachePt
 }
 
 int resolve(const kvq_config *cfg, Geometry *g);
+
+// ---- per-device launch set-up ----------------------------------------------
+// Function attributes and occupancy belong to a device: every cache below is
+// indexed by the current device (0 .. kMaxDevices - 1).
+constexpr int kMaxDevices = 64;
+// The current device, or -1 when there is none or its ordinal is too large.
+int device_slot();
+
+// Launch set-up of one kernel: the dynamic shared memory its attribute allows
+// and its resident blocks per SM at that size, per device, filled on first use
+// with the device current.  The fast path is two relaxed loads; the first use
+// (per device and size) takes a lock.
+struct KernelSetup {
+  std::atomic<int> smem[kMaxDevices];  // bytes the attribute allows (0: not set)
+  std::atomic<int> occ[kMaxDevices];   // blocks per SM at occ_smem
+  std::atomic<int> occ_smem[kMaxDevices];
+  std::mutex mu;
+};
+
+// Makes `kern` launchable with smem_bytes of dynamic shared memory and
+// `threads` threads on the current device; *occ (if given) receives its
+// resident blocks per SM there.
+template <typename F>
+cudaError_t kernel_setup(KernelSetup &s, F kern, int threads, int smem_bytes, int *occ) {
+  const int dev = device_slot();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (s.smem[dev].load(std::memory_order_acquire) >= smem_bytes &&
+      (!occ || s.occ_smem[dev].load(std::memory_order_acquire) == smem_bytes)) {
+    if (occ) *occ = s.occ[dev].load(std::memory_order_relaxed);
+    return cudaSuccess;
+  }
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.smem[dev].load(std::memory_order_relaxed) < smem_bytes) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    s.smem[dev].store(smem_bytes, std::memory_order_release);
+  }
+  if (occ) {
+    if (s.occ_smem[dev].load(std::memory_order_relaxed) != smem_bytes) {
+      int n = 0;
+      const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem_bytes);
+      if (e != cudaSuccess) return e;
+      s.occ[dev].store(n > 0 ? n : 1, std::memory_order_relaxed);
+      s.occ_smem[dev].store(smem_bytes, std::memory_order_release);
+    }
+    *occ = s.occ[dev].load(std::memory_order_relaxed);
+  }
+  return cudaSuccess;
+}
+
+// Launch of a persistent grid whose blocks wait on one another (the
+// tensor-core decode merges): cooperative, so the launch fails unless every
+// block can be resident at once, instead of leaving a poll to time out.
+template <typename... P, typename... A>
+cudaError_t launch_cooperative(void (*kern)(P...), unsigned grid, unsigned threads, int smem,
+                               cudaStream_t st, A &&...args) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = dim3(grid);
+  c.blockDim = dim3(threads);
+  c.dynamicSmemBytes = (size_t)smem;
+  c.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  c.attrs = attr;
+  c.numAttrs = 1;
+  return cudaLaunchKernelEx(&c, kern, static_cast<A &&>(args)...);
+}
 CachePtrs ptrs_of(const Geometry &g, const kvq_cache *c);
+// Every check kvq_decode_attention makes before it enqueues anything (cache
+// buffers and counters, pointers, alignment, workspace size, scale); KVQ_OK
+// or the error it would return.
+int check_decode_call(const Geometry &g, const kvq_cache *cache, const uint16_t *q,
+                      const float *out, float softmax_scale, const void *ws, size_t ws_bytes);
 void note_launch(int n);
 
 // ---- launchers (return cudaError_t of the launch) ------------------------
@@ -133,6 +210,11 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
                              float scale, void *ws, int num_sms, cudaStream_t st,
                              const __half *k_new = nullptr, const __half *v_new = nullptr);
 void set_debug_stall(long long iterations);
+
+// Name of the kernel instantiation each tensor-core path launches for g
+// (snprintf semantics).
+int tc_variant_name(const Geometry &g, char *buf, size_t len);
+int gqa_variant_name(const Geometry &g, char *buf, size_t len);
 
 // Tensor-core grouped-query path (head_dim 128, 2-bit KIVI, G >= 32, 2 or 4
 // query heads per KV head, 2 or 4 value groups).

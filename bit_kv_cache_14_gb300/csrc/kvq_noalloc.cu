@@ -13,16 +13,14 @@ static __device__ __align__(256) unsigned char kvq_noalloc_scratch[KVQ_NOALLOC_S
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices] = {nullptr};
+void *g_scratch_addr[kvq::kMaxDevices] = {nullptr};
 
-// Device address of the scratch on the current device; looked up on the
-// first call made with that device current.
+// Device address of the scratch on the current device (its primary
+// context); looked up on the first call made with that device current.
 int scratch_address(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ECUDA;
-  if (dev < 0 || dev >= kMaxDevices) return KVQ_EUNSUPPORTED;
+  const int dev = kvq::device_slot();
+  if (dev < 0) return KVQ_EUNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void *p = nullptr;
@@ -39,13 +37,18 @@ int scratch_address(void **out) {
 extern "C" int kvq_decode_attention_noalloc(const kvq_config *cfg, const kvq_cache *cache,
                                             const uint16_t *q, float *out,
                                             float softmax_scale, void *stream) {
-  if (!cache || !q || !out) return KVQ_EINVAL;
-  size_t need = 0;
-  int r = kvq_workspace_bytes(cfg, &need);
+  kvq::Geometry g;
+  int r = kvq::resolve(cfg, &g);
   if (r != KVQ_OK) return r;
+  const size_t need = kvq::decode_workspace_bytes(g);
   if (need > (size_t)KVQ_NOALLOC_SCRATCH_BYTES) return KVQ_ECAPACITY;
   void *ws = nullptr;
   if ((r = scratch_address(&ws)) != KVQ_OK) return r;
+  // every check of the regular decode first: a rejected call enqueues nothing
+  // and leaves the shared array alone
+  if ((r = kvq::check_decode_call(g, cache, q, out, softmax_scale, ws,
+                                  (size_t)KVQ_NOALLOC_SCRATCH_BYTES)) != KVQ_OK)
+    return r;
   // The scratch must read zero when a decode starts; a successful decode
   // leaves it so, but another call may have stopped early: clear the part
   // this configuration uses.

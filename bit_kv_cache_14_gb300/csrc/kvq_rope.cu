@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(kRBlock, rope_min_blocks<RG, SCHEME>())
   const int64_t p0 = (int64_t)bh * a.s_max * RG;
   for (int i = tid; i < a.n_split * RG * D; i += kRBlock) a.ws_o[p0 * D + i] = 0.0f;
   for (int i = tid; i < a.n_split * RG * 2; i += kRBlock) a.ws_ml[p0 * 2 + i] = 0.0f;
-  if (tid == 0) a.ws_cnt[bh] = 0;
+  if (tid == 0) atomicExch(&a.ws_cnt[bh], 0);  // an atomic, like the tickets it resets
 }
 
 // Splits over the quantized tokens, plus the fp16 split.  A split's block
@@ -537,21 +537,11 @@ void plan_rope(RopeArgs &a, int per_sm, int num_sms) {
 
 template <int D, int BITS, int RG, int SCHEME>
 cudaError_t launch_t(RopeArgs a, int smem_bytes, int num_sms, cudaStream_t st) {
-  static int configured = 0, occ_smem = -1, per_sm = 1;
-  if (configured < smem_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(rope_decode_kernel<D, BITS, RG, SCHEME>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-    if (e != cudaSuccess) return e;
-    configured = smem_bytes;
-  }
-  if (occ_smem != smem_bytes) {
-    int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &n, rope_decode_kernel<D, BITS, RG, SCHEME>, kRBlock, smem_bytes);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
-    occ_smem = smem_bytes;
-  }
+  static KernelSetup setup;
+  int per_sm = 1;
+  const cudaError_t e =
+      kernel_setup(setup, rope_decode_kernel<D, BITS, RG, SCHEME>, kRBlock, smem_bytes, &per_sm);
+  if (e != cudaSuccess) return e;
   plan_rope(a, per_sm, num_sms);
   rope_decode_kernel<D, BITS, RG, SCHEME>
       <<<dim3((unsigned)a.n_split, (unsigned)(a.g.B * a.g.H)), kRBlock, smem_bytes, st>>>(a);

@@ -283,14 +283,50 @@ __device__ __forceinline__ int head_nparts(const TcArgs &a, int bh) {
 
 // Partials are stored XOR-ed with kEnc: no float that arithmetic produces
 // (kEnc is a signalling NaN) encodes to 0, so a zero word means "not
-// written yet" and the zero-filled workspace starts empty.  Writers publish
-// without any fence or atomic.  The head's merger is fixed in advance: the
-// warp in slot 0, whose range holds the head's first unit and so ends in
-// this head (or holds all of it).  After publishing its own partial it polls
-// (bounded) until the others are visible, merges them with the log-sum-exp
-// rule, writes the output row and zeroes the partials again.
+// written yet" and the zero-filled workspace starts empty.  The head's merger
+// is fixed in advance: the warp in slot 0, whose range holds the head's first
+// unit and so ends in this head (or holds all of it).  After publishing its
+// own partial it polls (bounded) until the others are visible, merges them
+// with the log-sum-exp rule, writes the output row and zeroes the partials
+// again.
+//
+// Memory model: every access to a partial word -- the writer's store, the
+// merger's polling loads and its zeroing stores -- is a relaxed access at GPU
+// scope (st.relaxed.gpu / ld.relaxed.gpu), so the accesses are morally strong
+// and there is no data race; the data is its own flag (each 32-bit word is
+// written once per launch, and a non-zero word is the final value), so no
+// release / acquire ordering between words is needed.  The loads are asm
+// volatile with a memory clobber: the compiler cannot hoist them out of the
+// poll loop.  The grids that merge this way are launched cooperatively, so
+// every block of the grid is resident and every poll can end.
 constexpr uint32_t kEnc = 0x7fbadbadu;
 constexpr int kMergePolls = 1 << 22;
+
+__device__ __forceinline__ void st_relaxed(uint4 *p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_relaxed(uint2 *p, uint2 v) {
+  asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_relaxed(const uint2 *p) {
+  uint2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p)
+               : "memory");
+  return v;
+}
 
 __device__ __forceinline__ uint4 enc4(float4 v) {
   return make_uint4(__float_as_uint(v.x) ^ kEnc, __float_as_uint(v.y) ^ kEnc,
@@ -307,10 +343,10 @@ __device__ __forceinline__ void publish_partial(const TcArgs &a, int bh, int slo
                                                 float m, float l) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)bh * a.part_stride + slot;
-  reinterpret_cast<uint4 *>(a.ws_o + row * kD)[lane] = enc4(o);
+  st_relaxed(reinterpret_cast<uint4 *>(a.ws_o + row * kD) + lane, enc4(o));
   if (lane == 0)
-    reinterpret_cast<uint2 *>(a.ws_ml)[row] =
-        make_uint2(__float_as_uint(m) ^ kEnc, __float_as_uint(l) ^ kEnc);
+    st_relaxed(reinterpret_cast<uint2 *>(a.ws_ml) + row,
+               make_uint2(__float_as_uint(m) ^ kEnc, __float_as_uint(l) ^ kEnc));
 }
 
 // Run by the whole warp in slot 0 of head bh after it published its own
@@ -336,11 +372,11 @@ __device__ bool merge_head(const TcArgs &a, int bh) {
     bool all = false;
     for (int it = 0; it < kMergePolls && !all; ++it) {
       if (it > 0) __nanosleep(32);
-      v = lane < nparts ? __ldcg(ml + lane) : make_uint2(1u, 1u);
+      v = lane < nparts ? ld_relaxed(ml + lane) : make_uint2(1u, 1u);
       bool mine = v.x != 0u && v.y != 0u;
 #pragma unroll
       for (int j = 0; j < MB; ++j) {
-        o[j] = j < nparts ? __ldcg(wo + (int64_t)j * (kD / 4) + lane) : make_uint4(1, 1, 1, 1);
+        o[j] = j < nparts ? ld_relaxed(wo + (int64_t)j * (kD / 4) + lane) : make_uint4(1, 1, 1, 1);
         mine = mine && vis4(o[j]);
       }
       all = __all_sync(0xffffffffu, mine);
@@ -368,10 +404,10 @@ __device__ bool merge_head(const TcArgs &a, int bh) {
     // (m, l) of partial s sits in lane s % 32; every load is re-polled
     // (bounded) until its words are non-zero
     auto ml_of = [&](int s) -> uint2 {
-      uint2 v = __ldcg(ml + s);
+      uint2 v = ld_relaxed(ml + s);
       for (int it = 0; it < kMergePolls && (v.x == 0u || v.y == 0u); ++it) {
         __nanosleep(32);
-        v = __ldcg(ml + s);
+        v = ld_relaxed(ml + s);
       }
       return v;
     };
@@ -387,7 +423,7 @@ __device__ bool merge_head(const TcArgs &a, int bh) {
     for (int s0 = 0; s0 < nparts && ok; s0 += 32) {
       float w = 0.0f;
       if (s0 + lane < nparts) {
-        const uint2 v = __ldcg(ml + s0 + lane);
+        const uint2 v = ld_relaxed(ml + s0 + lane);
         const float ms = __uint_as_float(v.x ^ kEnc);
         if (ms != -INFINITY) {
           w = exp2_approx(ms - M);
@@ -402,7 +438,7 @@ __device__ bool merge_head(const TcArgs &a, int bh) {
           bool mine = true;
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            o[j] = j0 + j < nb ? __ldcg(wo + (int64_t)(s0 + j0 + j) * (kD / 4) + lane)
+            o[j] = j0 + j < nb ? ld_relaxed(wo + (int64_t)(s0 + j0 + j) * (kD / 4) + lane)
                                : make_uint4(1, 1, 1, 1);
             mine = mine && vis4(o[j]);
           }
@@ -434,8 +470,10 @@ __device__ bool merge_head(const TcArgs &a, int bh) {
       make_float4(O[0] * inv, O[1] * inv, O[2] * inv, O[3] * inv);
   // leave the workspace as found: partials zero
   for (int s = 0; s < nparts; ++s)
-    reinterpret_cast<uint4 *>(a.ws_o + base * kD)[(int64_t)s * (kD / 4) + lane] = make_uint4(0, 0, 0, 0);
-  for (int s = lane; s < nparts; s += 32) reinterpret_cast<uint2 *>(a.ws_ml)[base + s] = make_uint2(0, 0);
+    st_relaxed(reinterpret_cast<uint4 *>(a.ws_o + base * kD) + (int64_t)s * (kD / 4) + lane,
+               make_uint4(0, 0, 0, 0));
+  for (int s = lane; s < nparts; s += 32)
+    st_relaxed(reinterpret_cast<uint2 *>(a.ws_ml) + base + s, make_uint2(0, 0));
   return true;
 }
 

@@ -35,6 +35,7 @@ EXPORTS = (
     "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
     "kvq_last_launch_count", "kvq_strerror", "kvq_debug_stall_waits",
     "kvq_decode_attention_noalloc", "kvq_append_decode", "kvq_decode_attention_rope",
+    "kvq_decode_kernel_name",
 )
 
 
@@ -82,13 +83,14 @@ def lib():
             L.kvq_quantize_prefill.argtypes = [C, CA, P, P, I64, P]
             L.kvq_append.argtypes = [C, CA, P, P, P]
             L.kvq_decode_attention.argtypes = [C, CA, P, P, ctypes.c_float, P, ctypes.c_size_t, P]
-            L.kvq_decode_step_host.argtypes = [C, CA, P, P, P, P, P, P, P, P, ctypes.c_float, P,
+            L.kvq_decode_step_host.argtypes = [C, CA, P, P, P, P, ctypes.c_float, P,
                                                ctypes.c_size_t, P]
             L.kvq_decode_attention_rope.argtypes = [C, CA, P, P, ctypes.c_float, ctypes.c_double,
                                                     P, ctypes.c_size_t, P]
             L.kvq_decode_attention_noalloc.argtypes = [C, CA, P, P, ctypes.c_float, P]
             L.kvq_append_decode.argtypes = [C, CA, P, P, P, P, ctypes.c_float, P,
                                             ctypes.c_size_t, P]
+            L.kvq_decode_kernel_name.argtypes = [C, I64, ctypes.c_char_p, ctypes.c_size_t]
             L.kvq_get_device_status.argtypes = [CA, P]
             L.kvq_last_launch_count.argtypes = []
             L.kvq_debug_stall_waits.argtypes = [ctypes.c_int64]
@@ -126,6 +128,15 @@ def config_of(w, max_ctx: int | None = None) -> Config:
     return make_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.bits, scheme,
                        w.k_group, w.v_group, w.residual, w.n_sink,
                        w.max_ctx() if max_ctx is None else max_ctx)
+
+
+def decode_kernel_name(cfg: Config, n_quant: int) -> str:
+    """The decode kernel instantiation the library launches for this
+    configuration with n_quant quantized tokens (host only)."""
+    buf = ctypes.create_string_buffer(128)
+    _check(lib().kvq_decode_kernel_name(ctypes.byref(cfg), int(n_quant), buf, len(buf)),
+           "kvq_decode_kernel_name")
+    return buf.value.decode()
 
 
 def cache_sizes(cfg: Config) -> Sizes:
@@ -249,15 +260,26 @@ class QuantizedKVCache:
                "kvq_append_decode")
         return out
 
-    def decode_step_host(self, h_k, h_v, h_q, h_out, d_k, d_v, d_q, d_out, scale=None,
-                         stream=None) -> None:
-        """One append + decode from pinned host tensors through device staging tensors."""
+    def decode_step_host(self, h_in, h_out, d_in, d_out, scale=None, stream=None) -> None:
+        """One append + decode from pinned host tensors: h_in holds the step's
+        k, v ([B][H][d] each) and q ([B][Hq][d]) back to back as fp16 (see
+        step_input_halves), copied in one piece to d_in; the fp32 output
+        [B][Hq][d] comes back to h_out through d_out."""
+        _need_f16(h_in, d_in)
+        n = self.step_input_halves()
+        if h_in.numel() != n or d_in.numel() != n:
+            raise ValueError("step input holds %d halves, expected %d" % (h_in.numel(), n))
         if scale is None:
             scale = 1.0 / math.sqrt(self.cfg.head_dim)
         _check(lib().kvq_decode_step_host(
-            ctypes.byref(self.cfg), ctypes.byref(self.view), _ptr(h_k), _ptr(h_v), _ptr(h_q),
-            _ptr(h_out), _ptr(d_k), _ptr(d_v), _ptr(d_q), _ptr(d_out), float(scale),
-            self.ws.data_ptr(), self.ws_bytes, _stream(stream)), "kvq_decode_step_host")
+            ctypes.byref(self.cfg), ctypes.byref(self.view), _ptr(h_in), _ptr(h_out), _ptr(d_in),
+            _ptr(d_out), float(scale), self.ws.data_ptr(), self.ws_bytes, _stream(stream)),
+            "kvq_decode_step_host")
+
+    def step_input_halves(self) -> int:
+        """fp16 elements of one step's [k | v | q] input block."""
+        c = self.cfg
+        return (2 * c.n_kv_heads + c.n_q_heads) * c.batch * c.head_dim
 
     def device_status(self, stream=None) -> int:
         """Synchronizes, reads and clears the status word.  After an error the

@@ -249,17 +249,20 @@ int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k
                       void *ws, size_t ws_bytes, void *stream);
 
 /*
- * One decode step from HOST buffers: copies h_k, h_v ([B][H][d] fp16) and h_q
- * ([B][n_q_heads][d] fp16) to the device staging buffers d_k, d_v, d_q,
- * appends and attends (kvq_append_decode), and copies the result to h_out
- * ([B][n_q_heads][d] fp32)
- * through d_out -- all enqueued on `stream`, no synchronization.  Host
- * buffers should be pinned for the copies to be asynchronous.
+ * One decode step from HOST buffers, with one copy in and one copy out.
+ *   h_in:  host fp16, the step's inputs back to back: k [B][H][d], then
+ *          v [B][H][d], then q [B][n_q_heads][d] (2*B*H*d + B*n_q_heads*d
+ *          halves).
+ *   d_in:  device staging buffer of the same layout and size (16-byte aligned).
+ *   h_out: host fp32 [B][n_q_heads][d]; d_out: its device staging buffer.
+ * Enqueued on `stream`, no synchronization: one host-to-device copy of h_in,
+ * kvq_append_decode on the staged rows, one device-to-host copy of the output.
+ * Host buffers should be pinned for the copies to be asynchronous.  Errors:
+ * as kvq_append_decode; KVQ_ECUDA when a copy fails to enqueue.
  */
-int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *h_k,
-                         const uint16_t *h_v, const uint16_t *h_q, float *h_out,
-                         uint16_t *d_k, uint16_t *d_v, uint16_t *d_q, float *d_out,
-                         float softmax_scale, void *ws, size_t ws_bytes, void *stream);
+int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t *h_in,
+                         float *h_out, uint16_t *d_in, float *d_out, float softmax_scale,
+                         void *ws, size_t ws_bytes, void *stream);
 
 /*
  * Decode attention that allocates nothing, not even its scratch.  The pages
@@ -275,13 +278,17 @@ int kvq_decode_step_host(const kvq_config *cfg, kvq_cache *cache, const uint16_t
  * The scratch is one file-scope device array of KVQ_NOALLOC_SCRATCH_BYTES
  * (16 MiB) that every GPU which loads the library holds until the process
  * exits.  Configurations whose kvq_workspace_bytes exceeds it are rejected
- * with KVQ_ECAPACITY before anything is enqueued.  The first call on a device
- * (with that device current) looks up the array's device address with
- * cudaGetSymbolAddress; make that first call before any stream capture.
- * Each call clears the part of the scratch its configuration uses (an
- * asynchronous memset of kvq_workspace_bytes on `stream`), then launches the
- * decode.  All calls share
- * the one array: calls whose work can overlap on the GPU (different streams,
+ * with KVQ_ECAPACITY; every other check of kvq_decode_attention runs too, and
+ * a rejected call enqueues nothing and leaves the array alone.  The first call
+ * on a device (with that device current) looks up the array's device address
+ * with cudaGetSymbolAddress and keeps it; make that first call before any
+ * stream capture.  Only the device's primary context (the CUDA runtime's) is
+ * supported: the kept address is not valid in another context, nor after
+ * cudaDeviceReset.  Each call clears the part of the scratch its
+ * configuration uses (an asynchronous memset of kvq_workspace_bytes on
+ * `stream`), then launches the decode, so a call that stopped early (a
+ * timeout) leaves nothing behind for the next one.  All calls share the one
+ * array: calls whose work can overlap on the GPU (different streams,
  * different caches) race and give wrong results; serialize them.
  */
 #define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -303,6 +310,13 @@ int kvq_get_device_status(kvq_cache *cache, void *stream);
  * the workspace are undefined: zero-fill the workspace again.
  * Process-wide; not for production use. */
 void kvq_debug_stall_waits(int64_t iterations);
+
+/* Name of the decode kernel, with its template arguments, that
+ * kvq_decode_attention launches for this configuration when n_quant tokens
+ * are quantized (e.g. "tc_decode_kernel<bits=2,scheme=kivi,ngv=4,ngk=1,km=1>"),
+ * written NUL-terminated into buf[len].  Host only, no CUDA call.  Returns
+ * KVQ_OK, KVQ_EINVAL (null, n_quant < 0, buf too small) or a config error. */
+int kvq_decode_kernel_name(const kvq_config *cfg, int64_t n_quant, char *buf, size_t len);
 
 /* Number of kernel launches the last successful call of this thread enqueued. */
 int kvq_last_launch_count(void);

@@ -33,6 +33,8 @@ def _fake_gpu(args, w, rank, world):
 @pytest.fixture
 def line(monkeypatch):
     monkeypatch.setattr(bench, "run_gpu", _fake_gpu)
+    monkeypatch.setattr(bench, "run_configs",
+                        lambda names, peak: {n: {"us": 1.0, "frac": 0.5} for n in names})
     real = bench.max_over_ranks
     monkeypatch.setattr(bench, "max_over_ranks", lambda v, world, device: real(v, world, "cpu"))
 
@@ -78,5 +80,10 @@ def test_gpu_line_contract(line, rope):
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] > 0
     assert set(("sm_mhz", "sm_max_mhz", "reasons")) <= set(d["clocks"])
+    if rope:
+        assert "configs" not in d
+    else:
+        # the other named workloads, each with its own decode-kernel line
+        assert sorted(d["configs"]) == ["gqa_2bit", "innerq_1m", "kivi_4bit", "tiny"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]

@@ -151,16 +151,14 @@ def test_decode_step_host_matches_device_path():
     for c in (a, b):
         c.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
     shape_q = (w.batch, w.n_q_heads, w.head_dim)
-    d_k = torch.empty(w.batch, w.n_kv_heads, w.head_dim, dtype=torch.float16, device="cuda")
-    d_v, d_q = torch.empty_like(d_k), torch.empty(shape_q, dtype=torch.float16, device="cuda")
+    d_in = torch.empty(a.step_input_halves(), dtype=torch.float16, device="cuda")
     d_out = torch.empty(shape_q, dtype=torch.float32, device="cuda")
     h_out = torch.empty(shape_q, dtype=torch.float32).pin_memory()
     for s in range(4):
         q = synth.queries(w, s)
-        hk = torch.from_numpy(Ks[s]).pin_memory()
-        hv = torch.from_numpy(Vs[s]).pin_memory()
-        hq = torch.from_numpy(q).pin_memory()
-        a.decode_step_host(hk, hv, hq, h_out, d_k, d_v, d_q, d_out)
+        h_in = torch.from_numpy(np.concatenate([Ks[s].ravel(), Vs[s].ravel(), q.ravel()]))
+        h_in = h_in.pin_memory()
+        a.decode_step_host(h_in, h_out, d_in, d_out)
         torch.cuda.synchronize()
         b.append(torch.from_numpy(Ks[s]).cuda(), torch.from_numpy(Vs[s]).cuda())
         ref = b.decode(torch.from_numpy(q).cuda()).cpu()

@@ -1,0 +1,100 @@
+"""Every tensor-core decode instantiation the library can dispatch to, against
+the CPU oracle (all heads, ragged residuals, at least one flush or window
+eviction), and a host-side check that the dispatch table has no entry
+without such a case.
+
+The tensor-core kernels are templates over the code width, the scheme, the
+value groups per head, the key groups per head (InnerQ) or where the KIVI key
+statistics live (G 16 / 32 inside the block, G >= 64 beside it), and for the
+grouped-query kernel the query heads per KV head.  kvq_decode_kernel_name
+reports which instantiation a configuration reaches, so the coverage check
+asks the library itself rather than a copy of its rule.
+"""
+import itertools
+
+import pytest
+import torch
+
+from bit_kv_cache_14_gb300 import build_lib, kvq, synth
+from parity_util import ATOL, run_workload
+
+W = synth.WORKLOADS
+S = synth.scaled
+
+
+def _kivi(bits, ngv, G):
+    base = W["llama2_7b_2bit"] if bits == 2 else W["kivi_4bit"]
+    R = 64 if G <= 64 else 128
+    return S(base, batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, k_group=G, v_group=128 // ngv,
+             residual=R, n_append=R + 10)
+
+
+def _innerq(bits, ngv, ngk):
+    return S(W["innerq_1m"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, bits=bits,
+             k_group=128 // ngk, v_group=128 // ngv, n_append=40)
+
+
+def _gqa(ngv, G, rg):
+    return S(W["gqa_2bit"], batch=2, n_q_heads=2 * rg, n_kv_heads=2, ctx=900, k_group=G,
+             v_group=128 // ngv, residual=128, n_append=140)
+
+
+CASES = {}
+for bits, ngv, G in itertools.product((2, 4), (2, 4), (16, 32, 64)):
+    CASES["tc_kivi_b%d_ngv%d_g%d" % (bits, ngv, G)] = _kivi(bits, ngv, G)
+for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
+    CASES["tc_innerq_b%d_ngv%d_ngk%d" % (bits, ngv, ngk)] = _innerq(bits, ngv, ngk)
+for ngv, G, rg in itertools.product((2, 4), (32, 64), (2, 4)):
+    CASES["gqa_ngv%d_g%d_rg%d" % (ngv, G, rg)] = _gqa(ngv, G, rg)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build_lib.build()
+    yield
+
+
+def _name(w):
+    return kvq.decode_kernel_name(kvq.config_of(w), 1)
+
+
+def dispatched_tensor_core_names():
+    """Every tensor-core instantiation reachable from a valid configuration."""
+    names = set()
+    for d, bits, rg, gk, gv in itertools.product((64, 128), (2, 4), (1, 2, 4, 8),
+                                                 (16, 32, 64, 128), (16, 32, 64, 128)):
+        if gv > d:
+            continue
+        cfgs = [kvq.make_config(2, 2 * rg, 2, d, bits, kvq.KIVI, gk, gv, 128, 0, 4096)]
+        if gk <= d:
+            cfgs += [kvq.make_config(2, 2 * rg, 2, d, bits, s, gk, gv, 32, 4, 4096)
+                     for s in (kvq.INNERQ, kvq.INNERQ_KNORM)]
+        for cfg in cfgs:
+            name = kvq.decode_kernel_name(cfg, 1)
+            if name.startswith("tc_"):
+                names.add(name)
+    return names
+
+
+def test_every_dispatched_instantiation_has_a_parity_case():
+    dispatched = dispatched_tensor_core_names()
+    assert len(dispatched) == 20 + 8, sorted(dispatched)
+    covered = {_name(w) for w in CASES.values()}
+    assert dispatched <= covered, sorted(dispatched - covered)
+    # and each named case reaches the instantiation its name says
+    for name, w in CASES.items():
+        got = _name(w)
+        if name.startswith("gqa"):
+            assert got.startswith("tc_gqa_kernel<"), (name, got)
+        else:
+            assert got.startswith("tc_decode_kernel<"), (name, got)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_instantiation_matches_oracle(name):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    w = CASES[name]
+    worst = run_workload(w, decode_every=max(1, w.n_append // 4))
+    assert worst <= ATOL
