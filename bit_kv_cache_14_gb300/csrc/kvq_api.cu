@@ -67,6 +67,9 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   } else {
     if (!pow2_group(c.k_group) || c.head_dim % c.k_group != 0) return KVQ_EUNSUPPORTED;
   }
+  if ((c.flags & ~(KVQ_META_F16 | KVQ_VALUE_QUEUE | KVQ_RAGGED)) != 0) return KVQ_EINVAL;
+  if (c.outliers < 0 || c.outliers > 8) return KVQ_EINVAL;
+  if (c.scheme != KVQ_KIVI && ((c.flags & KVQ_VALUE_QUEUE) || c.outliers > 0)) return KVQ_EINVAL;
   g->B = c.batch;
   g->H = c.n_kv_heads;
   g->Hq = c.n_q_heads;
@@ -80,6 +83,11 @@ int resolve(const kvq_config *cfg, Geometry *g) {
   g->residual = c.residual;
   g->n_sink = c.n_sink;
   g->max_ctx = c.max_ctx;
+  g->meta16 = (c.flags & KVQ_META_F16) ? 1 : 0;
+  g->msz = g->meta16 ? 2 : 4;
+  g->vq = (c.flags & KVQ_VALUE_QUEUE) ? 1 : 0;
+  g->ragged = (c.flags & KVQ_RAGGED) ? 1 : 0;
+  g->n_out = c.outliers;
   g->cap = (c.max_ctx + kCapAlign - 1) / kCapAlign * kCapAlign;
   g->row_bytes = c.head_dim * c.bits / 8;
   g->v_meta_cols = c.head_dim / c.v_group;
@@ -94,22 +102,27 @@ int resolve(const kvq_config *cfg, Geometry *g) {
     const int64_t vw = g->cap * (c.head_dim / c.v_group) / 32;
     if (vw > g->mode_words) g->mode_words = vw;
   }
-  const int vmeta = kBlockTokens * g->v_meta_cols * (int)sizeof(float);
+  const int vmeta = kBlockTokens * g->v_meta_cols * g->msz;
   g->blk_vc = kBlockTokens * g->row_bytes;
   g->blk_vs = 2 * kBlockTokens * g->row_bytes;
   g->blk_vz = g->blk_vs + vmeta;
   g->blk_ks = g->blk_vz + vmeta;
+  int end;
   if (g->scheme == KVQ_INNERQ) {
-    const int kmeta = kBlockTokens * g->k_meta_cols * (int)sizeof(float);
+    const int kmeta = kBlockTokens * g->k_meta_cols * g->msz;
     g->blk_kz = g->blk_ks + kmeta;
-    g->block_bytes = g->blk_kz + kmeta;
+    end = g->blk_kz + kmeta;
   } else {
-    // G <= 32: the statistics of the block's 32 / G key groups end the block
+    // G <= 32: the statistics of the block's 32 / G key groups follow
     g->blk_kz = g->blk_ks;
-    g->block_bytes = g->blk_ks + (c.k_group <= kBlockTokens
-                                      ? (kBlockTokens / c.k_group) * 2 * c.head_dim * (int)sizeof(float)
-                                      : 0);
+    end = g->blk_ks + (c.k_group <= kBlockTokens
+                           ? (kBlockTokens / c.k_group) * 2 * c.head_dim * g->msz
+                           : 0);
   }
+  // outlier lists: n_out words per token, keys then values
+  g->blk_ko = end;
+  g->blk_vo = g->blk_ko + kBlockTokens * g->n_out * 4;
+  g->block_bytes = g->blk_vo + kBlockTokens * g->n_out * 4;
   g->knorm_off = (int64_t)g->B * g->H * (g->cap / kBlockTokens) * g->block_bytes;
   return KVQ_OK;
 }
@@ -118,7 +131,7 @@ CachePtrs ptrs_of(const Geometry &g, const kvq_cache *c) {
   CachePtrs p;
   p.blocks = static_cast<uint8_t *>(c->blocks);
   p.k_norm = g.knorm ? reinterpret_cast<float *>(p.blocks + g.knorm_off) : nullptr;
-  p.k_meta = c->k_meta;
+  p.k_meta = static_cast<uint8_t *>(c->k_meta);
   p.k_mode = c->k_mode;
   p.v_mode = c->v_mode;
   p.k_res = reinterpret_cast<__half *>(c->k_res);
@@ -126,7 +139,22 @@ CachePtrs ptrs_of(const Geometry &g, const kvq_cache *c) {
   p.k_sink = reinterpret_cast<__half *>(c->k_sink);
   p.v_sink = reinterpret_cast<__half *>(c->v_sink);
   p.status = c->dev_status;
+  p.seq_prompt = g.ragged ? c->seq_prompt : nullptr;
+  p.appended = c->n_appended;
   return p;
+}
+
+// The host counters as a Counts (n_vq: the value queue's count follows from
+// the length).
+static Counts host_counts(const Geometry &g, const kvq_cache *c) {
+  Counts k;
+  k.n_quant = c->n_quant;
+  k.n_resid = c->n_resid;
+  k.n_sink = c->n_sink;
+  k.ring_head = c->ring_head;
+  const int64_t n = c->n_quant + c->n_resid + c->n_sink;
+  k.n_vq = (g.scheme == KVQ_KIVI && g.vq) ? (n >= g.residual ? n - g.residual + 1 : 0) : c->n_quant;
+  return k;
 }
 
 // The buffers a configuration uses must be present and 16-byte aligned.
@@ -150,6 +178,10 @@ static int check_cache(const Geometry &g, const kvq_cache *c) {
       if (!aligned16(c->k_sink) || !aligned16(c->v_sink)) return KVQ_EALIGN;
     }
   }
+  if (g.ragged) {
+    if (!c->seq_prompt) return KVQ_EINVAL;
+    if (!aligned16(c->seq_prompt)) return KVQ_EALIGN;
+  }
   if (c->n_quant < 0 || c->n_resid < 0 || c->n_sink < 0 || c->ring_head < 0) return KVQ_EINVAL;
   return KVQ_OK;
 }
@@ -160,6 +192,7 @@ static int check_cache(const Geometry &g, const kvq_cache *c) {
 static int check_counters(const Geometry &g, const kvq_cache *c) {
   if (c->n_quant > g.cap || c->n_resid > g.residual || c->n_sink > g.n_sink) return KVQ_EINVAL;
   if (c->n_quant + c->n_resid + c->n_sink > g.max_ctx) return KVQ_EINVAL;
+  if (c->n_appended < 0 || c->n_appended > c->n_quant + c->n_resid + c->n_sink) return KVQ_EINVAL;
   if (g.scheme == KVQ_KIVI && (c->n_resid >= g.residual || c->n_quant % g.residual != 0))
     return KVQ_EINVAL;
   if (g.scheme == KVQ_INNERQ && g.residual > 0 && c->ring_head >= g.residual) return KVQ_EINVAL;
@@ -201,11 +234,12 @@ int kvq_cache_sizes(const kvq_config *cfg, kvq_sizes *out) {
   out->blocks = BH * (size_t)(g.cap / kBlockTokens) * g.block_bytes +
                 (g.knorm ? BH * (size_t)g.d * sizeof(float) : 0);
   if (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens)
-    out->k_meta = BH * (size_t)g.k_meta_rows * 2 * g.d * sizeof(float) + kMetaPad;
+    out->k_meta = BH * (size_t)g.k_meta_rows * 2 * g.d * g.msz + kMetaPad;
   if (g.scheme == KVQ_INNERQ) out->k_mode = out->v_mode = BH * (size_t)g.mode_words * 4;
   out->k_res = out->v_res = BH * (size_t)g.residual * g.d * 2;
   out->k_sink = out->v_sink = BH * (size_t)g.n_sink * g.d * 2;
   out->status = sizeof(int32_t);
+  out->seq_prompt = g.ragged ? (size_t)g.B * sizeof(int32_t) : 0;
   return KVQ_OK;
 }
 
@@ -218,38 +252,63 @@ int kvq_workspace_bytes(const kvq_config *cfg, size_t *bytes) {
   return KVQ_OK;
 }
 
-int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K,
-                         const uint16_t *V, int64_t T, void *stream) {
+// Both prefills.  lens (host, ragged only) null: every sequence has T tokens.
+static int prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K, const uint16_t *V,
+                   int64_t T, const int32_t *lens, bool ragged_call, void *stream) {
   Geometry g;
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
+  if (ragged_call && (!g.ragged || !lens)) return KVQ_EINVAL;
   if ((r = check_cache(g, cache)) != KVQ_OK) return r;  // counters: reset below
   if (T < 0) return KVQ_EINVAL;
   if (T > 0 && (!K || !V)) return KVQ_EINVAL;
   if (T > 0 && (!aligned16(K) || !aligned16(V))) return KVQ_EALIGN;
   if (T > g.max_ctx) return KVQ_ECAPACITY;
-  int64_t nq, nr, ns;
-  if (g.scheme == KVQ_KIVI) {
-    nq = T - T % g.residual;
-    nr = T - nq;
-    ns = 0;
-  } else {
-    ns = T < g.n_sink ? T : g.n_sink;
-    const int64_t rest = T - ns;
-    nr = rest < g.residual ? rest : g.residual;
-    nq = rest - nr;
+  int64_t longest = T;
+  if (lens) {
+    longest = 0;
+    for (int b = 0; b < g.B; ++b) {
+      if (lens[b] < 0 || lens[b] > T) return KVQ_EINVAL;
+      if (lens[b] > longest) longest = lens[b];
+    }
   }
+  const Counts c = counts_of(g, longest, 0);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CachePtrs p = ptrs_of(g, cache);
+  p.appended = 0;
   int launches = 0;
-  r = from_cuda(launch_prefill(g, ptrs_of(g, cache), reinterpret_cast<const __half *>(K),
-                               reinterpret_cast<const __half *>(V), T, nq, nr, ns,
-                               static_cast<cudaStream_t>(stream), &launches));
+  if (g.ragged) {
+    // every sequence's prompt length, read by the kernels below and by every
+    // later call
+    if (lens)
+      r = from_cuda(cudaMemcpyAsync(cache->seq_prompt, lens, (size_t)g.B * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, st));
+    else
+      r = from_cuda(launch_fill_i32(cache->seq_prompt, g.B, (int32_t)T, st)), ++launches;
+    if (r != KVQ_OK) return r;
+  }
+  int n = 0;
+  r = from_cuda(launch_prefill(g, p, reinterpret_cast<const __half *>(K),
+                               reinterpret_cast<const __half *>(V), T, c, st, &n));
   if (r != KVQ_OK) return r;
-  cache->n_quant = nq;
-  cache->n_resid = nr;
-  cache->n_sink = ns;
+  cache->n_quant = c.n_quant;
+  cache->n_resid = c.n_resid;
+  cache->n_sink = c.n_sink;
   cache->ring_head = 0;
-  note_launch(launches);
+  cache->n_appended = 0;
+  note_launch(launches + n);
   return KVQ_OK;
+}
+
+int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K,
+                         const uint16_t *V, int64_t T, void *stream) {
+  return prefill(cfg, cache, K, V, T, nullptr, false, stream);
+}
+
+int kvq_quantize_prefill_ragged(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K,
+                                const uint16_t *V, int64_t T_max, const int32_t *lens,
+                                void *stream) {
+  return prefill(cfg, cache, K, V, T_max, lens, true, stream);
 }
 
 int kvq_append(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k, const uint16_t *v,
@@ -264,10 +323,10 @@ int kvq_append(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k, const
   if (g.scheme == KVQ_KIVI && cache->n_resid >= g.residual) return KVQ_EINVAL;
   if (g.scheme == KVQ_INNERQ && g.residual > 0 && cache->ring_head >= g.residual) return KVQ_EINVAL;
   r = from_cuda(launch_append(g, ptrs_of(g, cache), reinterpret_cast<const __half *>(k),
-                              reinterpret_cast<const __half *>(v), cache->n_quant,
-                              cache->n_resid, cache->n_sink, cache->ring_head,
+                              reinterpret_cast<const __half *>(v), host_counts(g, cache),
                               static_cast<cudaStream_t>(stream)));
   if (r != KVQ_OK) return r;
+  cache->n_appended += 1;
   if (g.scheme == KVQ_KIVI) {
     if (cache->n_resid + 1 == g.residual) {
       cache->n_quant += g.residual;
@@ -294,12 +353,13 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
   int r = resolve(cfg, &g);
   if (r != KVQ_OK) return r;
   if ((r = check_decode_call(g, cache, q, out, softmax_scale, ws, ws_bytes)) != KVQ_OK) return r;
-  const DecodePlan plan =
-      plan_decode(g, cache->n_quant, cache->n_resid + cache->n_sink, num_sms_cached());
-  r = from_cuda(launch_decode(g, ptrs_of(g, cache), plan, cache->n_quant, cache->n_resid,
-                              cache->n_sink, cache->ring_head,
-                              reinterpret_cast<const __half *>(q), out, softmax_scale, ws,
-                              num_sms_cached(), static_cast<cudaStream_t>(stream)));
+  const Counts c = host_counts(g, cache);
+  const DecodePlan plan = plan_decode(g, c.n_quant, g.ragged ? (int64_t)g.residual + g.n_sink
+                                                             : c.n_resid + c.n_sink,
+                                      num_sms_cached());
+  r = from_cuda(launch_decode(g, ptrs_of(g, cache), plan, c, reinterpret_cast<const __half *>(q),
+                              out, softmax_scale, ws, num_sms_cached(),
+                              static_cast<cudaStream_t>(stream)));
   if (r != KVQ_OK) return r;
   note_launch(1);
   return KVQ_OK;
@@ -318,6 +378,7 @@ int kvq_decode_attention_rope(const kvq_config *cfg, const kvq_cache *cache, con
   if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
   if (!(rope_base > 0.0) || !isfinite(rope_base)) return KVQ_EINVAL;
   if (!rope_group_supported(g.Hq / g.H) || g.max_ctx > kRopeMaxPositions) return KVQ_EUNSUPPORTED;
+  if (g.meta16 || g.vq || g.n_out || g.ragged) return KVQ_EUNSUPPORTED;
   r = from_cuda(launch_decode_rope(g, ptrs_of(g, cache), cache->n_quant, cache->n_resid,
                                    cache->n_sink, cache->ring_head,
                                    reinterpret_cast<const __half *>(q), out, softmax_scale,
@@ -361,6 +422,7 @@ int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k
                                  reinterpret_cast<const __half *>(v)));
   if (r != KVQ_OK) return r;
   cache->n_resid += 1;
+  cache->n_appended += 1;
   note_launch(1);
   return KVQ_OK;
 }

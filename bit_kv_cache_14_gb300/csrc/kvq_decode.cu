@@ -33,7 +33,7 @@ struct DecodeArgs {
   const __half *q;
   float *out;
   float scale_log2;  // softmax_scale * log2(e): scores live in the exp2 domain
-  int64_t n_quant, n_resid, n_sink;
+  Counts cnt;        // counters (the longest sequence's under KVQ_RAGGED)
   int64_t chunk;
   int n_qsplit, n_split, s_max;
   int sc_max;        // score slots per head in shared memory
@@ -111,6 +111,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
   const int split = blockIdx.x;
   const int64_t bh = blockIdx.y;
   const int b = (int)(bh / g.H), h = (int)(bh % g.H);
+  const Counts cn = seq_counts(g, a.p, a.cnt, b);  // this sequence's counters
 
   const bool fp16_split = split == a.n_qsplit;
   for (int i = tid; i < RG * D; i += kBlock) {
@@ -131,10 +132,10 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
 
   int64_t t0 = 0, n_tok;
   if (fp16_split) {
-    n_tok = a.n_sink + a.n_resid;
+    n_tok = cn.n_sink + cn.n_resid;
   } else {
     t0 = (int64_t)split * a.chunk;
-    const int64_t t1 = min(t0 + a.chunk, a.n_quant);
+    const int64_t t1 = min(t0 + a.chunk, cn.n_quant);
     n_tok = t1 > t0 ? t1 - t0 : 0;
   }
   __syncthreads();
@@ -142,8 +143,8 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
   // ---------------- key pass: scores (exp2 domain) into sc[h][i] ----------
   if (fp16_split) {
     for (int64_t i = tid; i < n_tok; i += kBlock) {
-      const __half *row = i < a.n_sink ? a.p.k_sink + (bh * g.n_sink + i) * D
-                                       : a.p.k_res + (bh * g.residual + (i - a.n_sink)) * D;
+      const __half *row = i < cn.n_sink ? a.p.k_sink + (bh * g.n_sink + i) * D
+                                        : a.p.k_res + (bh * g.residual + (i - cn.n_sink)) * D;
       float s[RG] = {};
 #pragma unroll 4
       for (int c8 = 0; c8 < CH; ++c8) {
@@ -169,16 +170,16 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
       const int ng_here = (int)min((int64_t)ngt, (n_tok - tt + G - 1) / G);
       for (int i = tid; i < ng_here * D; i += kBlock) {
         const int gl = i / D, c = i % D;
-        const float sk = kivi_key_meta(g, a.p, bh, g0 + gl)[c];
+        const float sk = ld_meta(g, kivi_key_meta(g, a.p, bh, g0 + gl), c);
 #pragma unroll
         for (int hh = 0; hh < RG; ++hh) u_s[(gl * RG + hh) * D + c] = q_s[hh * D + c] * sk;
       }
       const int lane = tid & 31, wid = tid >> 5;
       for (int pr = wid; pr < ng_here * RG; pr += kBlock / 32) {
         const int gl = pr / RG, hh = pr % RG;
-        const float *zr = kivi_key_meta(g, a.p, bh, g0 + gl) + D;
+        const uint8_t *zr = kivi_key_meta(g, a.p, bh, g0 + gl) + D * g.msz;
         float s = 0.0f;
-        for (int c = lane; c < D; c += 32) s += q_s[hh * D + c] * zr[c];
+        for (int c = lane; c < D; c += 32) s += q_s[hh * D + c] * ld_meta(g, zr, c);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
         if (lane == 0) bias_s[pr] = s;
@@ -206,6 +207,21 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
             }
           }
         }
+        if (g.n_out > 0) {
+          // dense-and-sparse: an outlier's code is 0, so the dense sum holds
+          // q_c * zero there; its fp16 value replaces it
+          const int64_t t = t0 + i;
+          const uint32_t *ol = tok_outliers(g, a.p, bh, t, g.blk_ko);
+          const uint8_t *zr = kivi_key_meta(g, a.p, bh, t / G) + D * g.msz;
+          for (int e = 0; e < g.n_out; ++e) {
+            const uint32_t w = ol[e];
+            const int c = (int)(w >> 16);
+            const float dv = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))) -
+                             ld_meta(g, zr, c);
+#pragma unroll
+            for (int hh = 0; hh < RG; ++hh) s[hh] += q_s[hh * D + c] * dv;
+          }
+        }
 #pragma unroll
         for (int hh = 0; hh < RG; ++hh) sc[hh * a.sc_max + i] = s[hh];
       }
@@ -216,8 +232,8 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     for (int64_t i = tid; i < n_tok; i += kBlock) {
       const int64_t t = t0 + i;
       const uint32_t *row = reinterpret_cast<const uint32_t *>(code_row(g, a.p, bh, t, 0));
-      const float *ks = tok_meta(g, a.p, bh, t, g.blk_ks, ngk);
-      const float *kz = tok_meta(g, a.p, bh, t, g.blk_kz, ngk);
+      const uint8_t *ks = tok_meta(g, a.p, bh, t, g.blk_ks, ngk);
+      const uint8_t *kz = tok_meta(g, a.p, bh, t, g.blk_kz, ngk);
       float s[RG] = {};
       for (int j = 0; j < ngk; ++j) {
         float part[RG] = {};
@@ -230,7 +246,7 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
             for (int hh = 0; hh < RG; ++hh) part[hh] += q_s[hh * D + w * CPW + k] * u;
           }
         }
-        const float sj = ks[j], zj = kz[j];
+        const float sj = ld_meta(g, ks, j), zj = ld_meta(g, kz, j);
 #pragma unroll
         for (int hh = 0; hh < RG; ++hh) s[hh] += sj * part[hh] + zj * qj_s[hh * ngk + j];
       }
@@ -270,8 +286,9 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
   }
   if (fp16_split) {
     for (int64_t i = tl; i < n_tok; i += TL) {
-      const __half *row = i < a.n_sink ? a.p.v_sink + (bh * g.n_sink + i) * D
-                                       : a.p.v_res + (bh * g.residual + (i - a.n_sink)) * D;
+      // (value queue: the residual token n_quant + r sits in ring slot r)
+      const __half *row = i < cn.n_sink ? a.p.v_sink + (bh * g.n_sink + i) * D
+                                        : a.p.v_res + (bh * g.residual + (i - cn.n_sink)) * D;
       const uint4 raw = reinterpret_cast<const uint4 *>(row)[j];
       const __half2 *hv = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
@@ -290,11 +307,29 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
     const int gv = (8 * j) / g.v_group;
     for (int64_t i = tl; i < n_tok; i += TL) {
       const int64_t t = t0 + i;
+      if (t >= cn.n_vq) {
+        // value queue: the token's key is quantized, its value still fp16 in
+        // ring slot t mod R
+        const uint4 raw = reinterpret_cast<const uint4 *>(
+            a.p.v_res + (bh * g.residual + t % g.residual) * D)[j];
+        const __half2 *hv = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int hh = 0; hh < RG; ++hh) {
+          const float pv = sc[hh * a.sc_max + i];
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const float2 f = __half22float2(hv[k2]);
+            acc[hh][2 * k2] += pv * f.x;
+            acc[hh][2 * k2 + 1] += pv * f.y;
+          }
+        }
+        continue;
+      }
       const uint8_t *row = code_row(g, a.p, bh, t, g.blk_vc);
       const uint32_t word = BITS == 2 ? (uint32_t)reinterpret_cast<const uint16_t *>(row)[j]
                                       : reinterpret_cast<const uint32_t *>(row)[j];
-      const float vs = tok_meta(g, a.p, bh, t, g.blk_vs, ngv)[gv];
-      const float vz = tok_meta(g, a.p, bh, t, g.blk_vz, ngv)[gv];
+      const float vs = ld_meta(g, tok_meta(g, a.p, bh, t, g.blk_vs, ngv), gv);
+      const float vz = ld_meta(g, tok_meta(g, a.p, bh, t, g.blk_vz, ngv), gv);
 #pragma unroll
       for (int hh = 0; hh < RG; ++hh) {
         const float pv = sc[hh * a.sc_max + i];
@@ -302,6 +337,21 @@ __global__ void __launch_bounds__(kBlock) decode_kernel(const DecodeArgs a) {
         zacc[hh] += pv * vz;
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc[hh][k] += ps * code_at<BITS>(word, k);
+      }
+      if (g.n_out > 0) {
+        // this chunk's outliers: code 0 gave p * zero, the fp16 value replaces it
+        const uint32_t *ol = tok_outliers(g, a.p, bh, t, g.blk_vo);
+        for (int e = 0; e < g.n_out; ++e) {
+          const uint32_t w = ol[e];
+          const int c = (int)(w >> 16);
+          if ((c >> 3) != j) continue;
+          const float dv = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))) - vz;
+#pragma unroll
+          for (int hh = 0; hh < RG; ++hh)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (k == (c & 7)) acc[hh][k] += sc[hh * a.sc_max + i] * dv;
+        }
       }
     }
   }
@@ -439,23 +489,21 @@ DecodePlan plan_decode(const Geometry &g, int64_t n_quant, int64_t n_fp16, int n
 }
 
 cudaError_t launch_decode(const Geometry &g, const CachePtrs &p, const DecodePlan &plan,
-                          int64_t n_quant, int64_t n_resid, int64_t n_sink, int64_t ring_head,
-                          const __half *q, float *out, float scale, void *ws, int num_sms,
-                          cudaStream_t st) {
-  (void)ring_head;  // attention does not depend on the order of window tokens
-  if (n_quant > 0 && tc_decode_supported(g))
-    return launch_decode_tc(g, p, n_quant, n_resid, n_sink, q, out, scale, ws, num_sms, st);
-  if (n_quant > 0 && gqa_decode_supported(g))
-    return launch_decode_gqa(g, p, n_quant, n_resid, n_sink, q, out, scale, ws, num_sms, st);
+                          const Counts &c, const __half *q, float *out, float scale, void *ws,
+                          int num_sms, cudaStream_t st) {
+  // (attention does not depend on the order of window tokens: no ring_head)
+  if (c.n_quant > 0 && tc_decode_supported(g))
+    return launch_decode_tc(g, p, c.n_quant, c.n_resid, c.n_sink, q, out, scale, ws, num_sms, st);
+  if (c.n_quant > 0 && gqa_decode_supported(g))
+    return launch_decode_gqa(g, p, c.n_quant, c.n_resid, c.n_sink, q, out, scale, ws, num_sms,
+                             st);
   DecodeArgs a;
   a.g = g;
   a.p = p;
   a.q = q;
   a.out = out;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.n_quant = n_quant;
-  a.n_resid = n_resid;
-  a.n_sink = n_sink;
+  a.cnt = c;
   a.chunk = plan.chunk;
   a.n_qsplit = plan.n_qsplit;
   a.n_split = plan.n_split;

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
       if constexpr (!C::KIN)
         if (lane == 0)
           bulk_g2s(dst + C::off_km,
-                   a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
+                   a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD * g.msz,
                    C::KMB, bar);
     } else if (lane == 0) {
       const int ns = (int)a.n_sink;
@@ -733,6 +733,7 @@ int gqa_variant_name(const Geometry &g, char *buf, size_t len) {
 
 bool gqa_decode_supported(const Geometry &g) {
   if (g.d != kD || g.bits != 2 || g.scheme != KVQ_KIVI) return false;
+  if (g.meta16 || g.vq || g.n_out || g.ragged) return false;
   const int rg = g.Hq / g.H;
   if (rg != 2 && rg != 4) return false;
   const int ngv = kD / g.v_group;

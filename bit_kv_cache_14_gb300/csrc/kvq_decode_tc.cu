@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
                     pol_once);
       if (SCHEME == KVQ_KIVI && !SC::KIN && lane == 0)
         bulk_g2s(dst + SC::off_km,
-                 a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD,
+                 a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD * g.msz,
                  SC::KMB, bar);
       if (first && lane == 0)
         bulk_g2s(dst + SC::off_q, a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD, kD * 2,
@@ -879,6 +879,7 @@ int tc_variant_name(const Geometry &g, char *buf, size_t len) {
 
 bool tc_decode_supported(const Geometry &g) {
   if (g.d != kD || g.Hq != g.H) return false;
+  if (g.meta16 || g.vq || g.n_out || g.ragged) return false;
   const int ngv = kD / g.v_group;
   if (ngv != 2 && ngv != 4) return false;
   if (g.scheme == KVQ_KIVI) return g.k_group >= 16 && g.k_group <= 128;

@@ -31,19 +31,65 @@ struct Geometry {
   int64_t mode_words;   // per head, InnerQ only
   int block_bytes;      // one 32-token block
   int blk_vc, blk_vs, blk_vz, blk_ks, blk_kz;  // byte offsets inside a block
+  int blk_ko, blk_vo;   // outlier lists (KIVI with n_out > 0)
   int knorm;            // InnerQ key normalization (KVQ_INNERQ_KNORM)
   int64_t knorm_off;    // byte offset of the key factors f32 [B][H][d] in blocks
+  int meta16;           // scales and zeros stored in fp16 (KVQ_META_F16)
+  int msz;              // bytes per stored scale / zero: 4 or 2
+  int vq;               // KIVI value queue (KVQ_VALUE_QUEUE)
+  int n_out;            // KIVI outliers per token and tensor (0 = none)
+  int ragged;           // per-sequence prompt lengths (KVQ_RAGGED)
 };
 
 // Device pointers of a cache (same meaning as kvq_cache).
 struct CachePtrs {
   uint8_t *blocks;
-  float *k_meta;
+  uint8_t *k_meta;
   uint32_t *k_mode, *v_mode;
   __half *k_res, *v_res, *k_sink, *v_sink;
   int32_t *status;
   float *k_norm;  // key factors [B*H][d] (KVQ_INNERQ_KNORM), else nullptr
+  const int32_t *seq_prompt;  // KVQ_RAGGED: prompt length per sequence, else nullptr
+  int64_t appended;           // tokens appended to every sequence since the prefill
 };
+
+// Counters of one sequence (the kvq_cache counters, plus the number of
+// values held quantized: n_quant, or under the value queue its own count).
+struct Counts {
+  int64_t n_quant, n_resid, n_sink, ring_head, n_vq;
+};
+
+// The counters of a sequence that received `prompt` tokens at prefill and
+// `appended` single appends since: every counter is a function of those two
+// (KIVI residual = length mod R; InnerQ sinks, then window, then quantized,
+// with one ring step per eviction; value queue max(0, n - R + 1)).
+__host__ __device__ inline Counts counts_of(const Geometry &g, int64_t prompt, int64_t appended) {
+  Counts c;
+  const int64_t n = prompt + appended;
+  if (g.scheme == KVQ_KIVI) {
+    c.n_resid = n % g.residual;
+    c.n_quant = n - c.n_resid;
+    c.n_sink = 0;
+    c.ring_head = 0;
+    c.n_vq = g.vq ? (n >= g.residual ? n - g.residual + 1 : 0) : c.n_quant;
+  } else {
+    c.n_sink = n < g.n_sink ? n : g.n_sink;
+    const int64_t rest = n - c.n_sink;
+    c.n_resid = rest < g.residual ? rest : g.residual;
+    c.n_quant = rest - c.n_resid;
+    const int64_t ps = prompt < g.n_sink ? prompt : g.n_sink, prest = prompt - ps;
+    const int64_t pq = prest - (prest < g.residual ? prest : g.residual);
+    c.ring_head = g.residual > 0 ? (c.n_quant - pq) % g.residual : 0;
+    c.n_vq = c.n_quant;
+  }
+  return c;
+}
+
+// Counters of sequence b: the uniform ones, or (KVQ_RAGGED) its own.
+__device__ __forceinline__ Counts seq_counts(const Geometry &g, const CachePtrs &p,
+                                             const Counts &uniform, int b) {
+  return g.ragged ? counts_of(g, p.seq_prompt[b], p.appended) : uniform;
+}
 
 // ---- addressing of the block layout (include/kvq.h, "Packed layout") ------
 __host__ __device__ __forceinline__ int64_t block_index(const Geometry &g, int64_t bh,
@@ -59,21 +105,42 @@ __device__ __forceinline__ uint8_t *code_row(const Geometry &g, const CachePtrs 
                                              int64_t t, int off) {
   return tok_block(g, p, bh, t) + off + (int)(t % kBlockTokens) * g.row_bytes;
 }
-// Per-token statistics row of token t: `cols` floats at block offset `off`.
-__device__ __forceinline__ float *tok_meta(const Geometry &g, const CachePtrs &p, int64_t bh,
-                                           int64_t t, int off, int cols) {
-  return reinterpret_cast<float *>(tok_block(g, p, bh, t) + off) + (int)(t % kBlockTokens) * cols;
+// Per-token statistics row of token t: `cols` stored values at block offset `off`.
+__device__ __forceinline__ uint8_t *tok_meta(const Geometry &g, const CachePtrs &p, int64_t bh,
+                                             int64_t t, int off, int cols) {
+  return tok_block(g, p, bh, t) + off + (int)(t % kBlockTokens) * cols * g.msz;
 }
-// KIVI key group grp of head bh: scale row (d floats); the zero row follows.
-// G <= 32: at the end of the group's block; G >= 64: in the k_meta array.
-__device__ __forceinline__ float *kivi_key_meta(const Geometry &g, const CachePtrs &p, int64_t bh,
-                                                int64_t grp) {
+// KIVI key group grp of head bh: scale row (d stored values); the zero row
+// follows at + d * msz bytes.  G <= 32: at the end of the group's block;
+// G >= 64: in the k_meta array.
+__device__ __forceinline__ uint8_t *kivi_key_meta(const Geometry &g, const CachePtrs &p,
+                                                  int64_t bh, int64_t grp) {
   if (g.k_group <= kBlockTokens) {
     const int64_t t0 = grp * g.k_group;
-    return reinterpret_cast<float *>(tok_block(g, p, bh, t0) + g.blk_ks) +
-           (int)((t0 % kBlockTokens) / g.k_group) * 2 * g.d;
+    return tok_block(g, p, bh, t0) + g.blk_ks +
+           (int)((t0 % kBlockTokens) / g.k_group) * 2 * g.d * g.msz;
   }
-  return p.k_meta + (bh * g.k_meta_rows + grp) * 2 * g.d;
+  return p.k_meta + (bh * g.k_meta_rows + grp) * 2 * g.d * g.msz;
+}
+// Outlier list of token t (off = g.blk_ko for keys, g.blk_vo for values):
+// n_out words (channel << 16) | fp16 bits, channels ascending.
+__device__ __forceinline__ uint32_t *tok_outliers(const Geometry &g, const CachePtrs &p,
+                                                  int64_t bh, int64_t t, int off) {
+  return reinterpret_cast<uint32_t *>(tok_block(g, p, bh, t) + off) +
+         (int)(t % kBlockTokens) * g.n_out;
+}
+
+// A stored statistic as fp32, and its store (under KVQ_META_F16 the value is
+// already an fp16 value, so the conversion is exact).
+__device__ __forceinline__ float ld_meta(const Geometry &g, const uint8_t *row, int i) {
+  return g.meta16 ? __half2float(reinterpret_cast<const __half *>(row)[i])
+                  : reinterpret_cast<const float *>(row)[i];
+}
+__device__ __forceinline__ void st_meta(const Geometry &g, uint8_t *row, int i, float v) {
+  if (g.meta16)
+    reinterpret_cast<__half *>(row)[i] = __float2half_rn(v);
+  else
+    reinterpret_cast<float *>(row)[i] = v;
 }
 
 int resolve(const kvq_config *cfg, Geometry *g);
@@ -155,12 +222,17 @@ int check_decode_call(const Geometry &g, const kvq_cache *cache, const uint16_t 
 void note_launch(int n);
 
 // ---- launchers (return cudaError_t of the launch) ------------------------
+// Prefill of K, V [B][H][T][d] (T = the row stride; under KVQ_RAGGED each
+// sequence's own prompt length is read from p.seq_prompt) into an empty
+// cache; c = the counters after it (the longest sequence's when ragged).
 cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *K,
-                           const __half *V, int64_t T, int64_t n_quant, int64_t n_resid,
-                           int64_t n_sink, cudaStream_t st, int *launches);
+                           const __half *V, int64_t T, const Counts &c, cudaStream_t st,
+                           int *launches);
+// One appended token per (batch, kv head); c = the counters before it.
 cudaError_t launch_append(const Geometry &g, const CachePtrs &p, const __half *k,
-                          const __half *v, int64_t n_quant, int64_t n_resid,
-                          int64_t n_sink, int64_t ring_head, cudaStream_t st);
+                          const __half *v, const Counts &c, cudaStream_t st);
+// dst[0 .. n) = v.
+cudaError_t launch_fill_i32(int32_t *dst, int n, int32_t v, cudaStream_t st);
 
 // Partial (m, l, o) slots per head in the decode workspace: enough for one
 // per 128 quantized tokens plus the fp16 segment.
@@ -177,7 +249,7 @@ inline int part_slots(const Geometry &g) { return (int)(g.cap / kCapAlign) + 2; 
 constexpr int kTcWarps = 8;
 constexpr int kTcMaxBlocks = 1024;
 inline int tc_fp16_chunk(const Geometry &g) {
-  const int kmb = (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens) ? 2 * g.d * 4 : 0;
+  const int kmb = (g.scheme == KVQ_KIVI && g.k_group > kBlockTokens) ? 2 * g.d * g.msz : 0;
   const int ch = (g.block_bytes + kmb) / (4 * g.d);
   return ch < 8 ? ch : 8;
 }
@@ -196,9 +268,8 @@ struct DecodePlan {
 size_t decode_workspace_bytes(const Geometry &g);
 DecodePlan plan_decode(const Geometry &g, int64_t n_quant, int64_t n_fp16, int num_sms);
 cudaError_t launch_decode(const Geometry &g, const CachePtrs &p, const DecodePlan &plan,
-                          int64_t n_quant, int64_t n_resid, int64_t n_sink,
-                          int64_t ring_head, const __half *q, float *out, float scale,
-                          void *ws, int num_sms, cudaStream_t st);
+                          const Counts &c, const __half *q, float *out, float scale, void *ws,
+                          int num_sms, cudaStream_t st);
 
 // Tensor-core decode path (MHA, head_dim 128, 2 or 4 value groups).
 bool tc_decode_supported(const Geometry &g);

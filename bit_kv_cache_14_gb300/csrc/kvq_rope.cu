@@ -262,7 +262,9 @@ __global__ void __launch_bounds__(kRBlock, rope_min_blocks<RG, SCHEME>())
           for (int gi = 0; gi < NGS; ++gi) {
             float sa = na, sb = nb, za = 0.0f, zb = 0.0f;
             if (SCHEME == KVQ_KIVI) {
-              const float *km = kivi_key_meta(g, a.p, bh, (tb + (int64_t)gi * g.k_group) >> lgk);
+              // (fp32 statistics: the options are refused for this kernel)
+              const float *km = reinterpret_cast<const float *>(
+                  kivi_key_meta(g, a.p, bh, (tb + (int64_t)gi * g.k_group) >> lgk));
               sa = km[2 * pr];
               sb = km[2 * pr + 1];
               za = km[D + 2 * pr];
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(kRBlock, rope_min_blocks<RG, SCHEME>())
         } else {
           const int GK = g.k_group;
           const int ngk = D / GK;
-          const float *ks = tok_meta(g, a.p, bh, t, g.blk_ks, ngk);
-          const float *kz = tok_meta(g, a.p, bh, t, g.blk_kz, ngk);
+          const float *ks = reinterpret_cast<const float *>(tok_meta(g, a.p, bh, t, g.blk_ks, ngk));
+          const float *kz = reinterpret_cast<const float *>(tok_meta(g, a.p, bh, t, g.blk_kz, ngk));
           float accg[RG], zg[RG];
 #pragma unroll
           for (int hh = 0; hh < RG; ++hh) accg[hh] = zg[hh] = 0.0f;

@@ -27,6 +27,9 @@ KVQ_ETIMEOUT = -6
 KIVI = 0
 INNERQ = 1
 INNERQ_KNORM = 2  # InnerQ with the one-shot per-channel key normalization
+META_F16 = 1      # config.flags: scales and zero points stored in fp16
+VALUE_QUEUE = 2   # config.flags: KIVI values leave the fp16 residual one at a time
+RAGGED = 4        # config.flags: every sequence has its own prompt length
 CAP_ALIGN = 128  # token-stride granularity of the cache layout
 
 # Every entry point declared in include/kvq.h.
@@ -35,26 +38,30 @@ EXPORTS = (
     "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
     "kvq_last_launch_count", "kvq_strerror", "kvq_debug_stall_waits",
     "kvq_decode_attention_noalloc", "kvq_append_decode", "kvq_decode_attention_rope",
-    "kvq_decode_kernel_name",
+    "kvq_decode_kernel_name", "kvq_quantize_prefill_ragged",
 )
 
 
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "n_q_heads", "n_kv_heads", "head_dim", "bits", "scheme", "k_group",
-        "v_group", "residual", "n_sink")] + [("max_ctx", ctypes.c_int64)]
+        "v_group", "residual", "n_sink")] + [("max_ctx", ctypes.c_int64),
+                                             ("flags", ctypes.c_uint32),
+                                             ("outliers", ctypes.c_int32)]
 
 
 class Sizes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
-        "blocks", "k_meta", "k_mode", "v_mode", "k_res", "v_res", "k_sink", "v_sink", "status")]
+        "blocks", "k_meta", "k_mode", "v_mode", "k_res", "v_res", "k_sink", "v_sink", "status",
+        "seq_prompt")]
 
 
 class Cache(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "blocks", "k_meta", "k_mode", "v_mode", "k_res", "v_res", "k_sink", "v_sink")] + [
         (n, ctypes.c_int64) for n in ("n_quant", "n_resid", "n_sink", "ring_head")] + [
-        ("dev_status", ctypes.c_void_p)]
+        ("dev_status", ctypes.c_void_p), ("seq_prompt", ctypes.c_void_p),
+        ("n_appended", ctypes.c_int64)]
 
 
 class KVQError(RuntimeError):
@@ -81,6 +88,7 @@ def lib():
             L.kvq_cache_sizes.argtypes = [C, ctypes.POINTER(Sizes)]
             L.kvq_workspace_bytes.argtypes = [C, ctypes.POINTER(ctypes.c_size_t)]
             L.kvq_quantize_prefill.argtypes = [C, CA, P, P, I64, P]
+            L.kvq_quantize_prefill_ragged.argtypes = [C, CA, P, P, I64, P, P]
             L.kvq_append.argtypes = [C, CA, P, P, P]
             L.kvq_decode_attention.argtypes = [C, CA, P, P, ctypes.c_float, P, ctypes.c_size_t, P]
             L.kvq_decode_step_host.argtypes = [C, CA, P, P, P, P, ctypes.c_float, P,
@@ -114,20 +122,21 @@ def _check(code: int, what: str) -> None:
 
 
 def make_config(batch, n_q_heads, n_kv_heads, head_dim, bits, scheme, k_group, v_group,
-                residual, n_sink, max_ctx) -> Config:
+                residual, n_sink, max_ctx, flags=0, outliers=0) -> Config:
     return Config(batch, n_q_heads, n_kv_heads, head_dim, bits, scheme, k_group, v_group,
-                  residual, n_sink, max_ctx)
+                  residual, n_sink, max_ctx, flags, outliers)
 
 
 def config_of(w, max_ctx: int | None = None) -> Config:
     """Config of a synth.Workload (max_ctx defaults to prompt + streamed tokens)."""
-    for name in ("v_queue", "meta_f16", "outliers"):
-        if getattr(w, name, False):
-            raise ValueError("%s: a cache-format variant the library does not build yet" % name)
     scheme = INNERQ_KNORM if getattr(w, "k_norm", False) else w.scheme
+    flags = ((META_F16 if getattr(w, "meta_f16", False) else 0)
+             | (VALUE_QUEUE if getattr(w, "v_queue", False) else 0)
+             | (RAGGED if getattr(w, "ragged", False) else 0))
     return make_config(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.bits, scheme,
                        w.k_group, w.v_group, w.residual, w.n_sink,
-                       w.max_ctx() if max_ctx is None else max_ctx)
+                       w.max_ctx() if max_ctx is None else max_ctx, flags,
+                       getattr(w, "outliers", 0))
 
 
 def decode_kernel_name(cfg: Config, n_quant: int) -> str:
@@ -187,12 +196,16 @@ class QuantizedKVCache:
             setattr(view, name, t.data_ptr() if n else None)
         self.status = torch.zeros(4, dtype=torch.int32, device=self.device)
         view.dev_status = self.status.data_ptr()
+        # per-sequence prompt lengths (KVQ_RAGGED), written by the prefill
+        self.seq_prompt = torch.zeros(max(cfg.batch, 4), dtype=torch.int32, device=self.device)
+        view.seq_prompt = self.seq_prompt.data_ptr() if sizes.seq_prompt else None
         self.view = view
         self.ws_bytes = workspace_bytes(cfg)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=self.device)
         self.sizes = sizes
 
     # counters
+    n_appended = property(lambda self: self.view.n_appended)
     n_quant = property(lambda self: self.view.n_quant)
     n_resid = property(lambda self: self.view.n_resid)
     n_sink = property(lambda self: self.view.n_sink)
@@ -206,6 +219,26 @@ class QuantizedKVCache:
         _check(lib().kvq_quantize_prefill(ctypes.byref(self.cfg), ctypes.byref(self.view),
                                           _ptr(K), _ptr(V), K.shape[2], _stream(stream)),
                "kvq_quantize_prefill")
+
+    def prefill_ragged(self, K: torch.Tensor, V: torch.Tensor, lens, stream=None) -> None:
+        """K, V: fp16 [B][H][T_max][d] on the device; sequence b's prompt is its
+        first lens[b] rows (KVQ_RAGGED)."""
+        _need_f16(K, V)
+        if K.shape != V.shape:
+            raise ValueError("K and V shapes differ: %s vs %s" % (tuple(K.shape), tuple(V.shape)))
+        lens = (ctypes.c_int32 * self.cfg.batch)(*[int(x) for x in lens])
+        _check(lib().kvq_quantize_prefill_ragged(ctypes.byref(self.cfg), ctypes.byref(self.view),
+                                                 _ptr(K), _ptr(V), K.shape[2], lens,
+                                                 _stream(stream)),
+               "kvq_quantize_prefill_ragged")
+
+    def seq_lengths(self):
+        """Tokens each sequence holds (host arithmetic: prompt + appended)."""
+        c = self.cfg
+        if not c.flags & RAGGED:
+            n = self.n_quant + self.n_resid + self.n_sink
+            return [n] * c.batch
+        return [int(x) + self.n_appended for x in self.seq_prompt[: c.batch].tolist()]
 
     def append(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         """k, v: fp16 [B][H][d] on the device."""
@@ -300,17 +333,24 @@ class QuantizedKVCache:
     def _block_layout(self):
         c = self.cfg
         rb = c.head_dim * c.bits // 8
+        m = 2 if c.flags & META_F16 else 4
         ngv = c.head_dim // c.v_group
         ngk = c.head_dim // c.k_group if c.scheme in (INNERQ, INNERQ_KNORM) else 0
         off = {"k_codes": 0, "v_codes": 32 * rb, "v_scale": 64 * rb}
-        off["v_zero"] = off["v_scale"] + 128 * ngv
-        off["k_scale"] = off["v_zero"] + 128 * ngv
-        off["k_zero"] = off["k_scale"] + 128 * ngk
-        bb = off["k_zero"] + 128 * ngk
+        off["v_zero"] = off["v_scale"] + 32 * m * ngv
+        off["k_scale"] = off["v_zero"] + 32 * m * ngv
+        off["k_zero"] = off["k_scale"] + 32 * m * ngk
+        end = off["k_zero"] + 32 * m * ngk
         if c.scheme == KIVI and c.k_group <= 32:
             off["k_stats"] = off["k_scale"]          # 32/G groups x (scale row, zero row)
-            bb = off["k_stats"] + (32 // c.k_group) * 2 * c.head_dim * 4
+            end = off["k_stats"] + (32 // c.k_group) * 2 * c.head_dim * m
+        off["k_outliers"] = end
+        off["v_outliers"] = end + 32 * 4 * c.outliers
+        bb = off["v_outliers"] + 32 * 4 * c.outliers
         return off, bb, rb, ngv, ngk
+
+    def _meta_dtype(self):
+        return torch.float16 if self.cfg.flags & META_F16 else torch.float32
 
     def _block_field(self, name: str, width: int) -> torch.Tensor:
         """Bytes [off, off + 32*width) of every block as [B][H][cap][width] (a copy)."""
@@ -327,26 +367,37 @@ class QuantizedKVCache:
         return self._block_field(which + "_codes", rb)
 
     def meta(self, name: str) -> torch.Tensor:
-        """scale / zero statistics as fp32 [B][H][rows * cols] (a copy): KIVI keys
-        [cap/G][d], per-token statistics [cap][groups]."""
+        """scale / zero statistics as fp32 [B][H][rows * cols] (a copy; fp16
+        statistics are widened exactly): KIVI keys [cap/G][d], per-token
+        statistics [cap][groups]."""
         c = self.cfg
+        dt = self._meta_dtype()
+        m = 2 if dt == torch.float16 else 4
         if name.startswith("k") and c.scheme == KIVI:
             rows = self.cap // c.k_group
             which = 0 if name == "k_scale" else 1
             if c.k_group <= 32:
                 per = 32 // c.k_group
-                f = self._block_field("k_stats", per * 2 * c.head_dim * 4 // 32)
-                f = f.contiguous().view(torch.float32)
+                f = self._block_field("k_stats", per * 2 * c.head_dim * m // 32)
+                f = f.contiguous().view(dt).float()
                 f = f.reshape(c.batch, c.n_kv_heads, self.cap // 32, per, 2, c.head_dim)
                 return f[:, :, :, :, which, :].reshape(c.batch, c.n_kv_heads, -1)
             n = c.batch * c.n_kv_heads * rows * 2 * c.head_dim
-            km = self.bufs["k_meta"][: n * 4].view(torch.float32)
+            km = self.bufs["k_meta"][: n * m].view(dt).float()
             km = km.view(c.batch, c.n_kv_heads, rows, 2, c.head_dim)
             return km[:, :, :, which, :].reshape(c.batch, c.n_kv_heads, -1)
         _, _, _, ngv, ngk = self._block_layout()
         cols = ngk if name.startswith("k") else ngv
-        f = self._block_field(name, 4 * cols).contiguous().view(torch.float32)
+        f = self._block_field(name, m * cols).contiguous().view(dt).float()
         return f.reshape(c.batch, c.n_kv_heads, -1)
+
+    def outlier_lists(self, which: str):
+        """Per-token outlier lists (KIVI with outliers): channels and fp16 bit
+        patterns, each int32 [B][H][cap][outliers] (copies)."""
+        c = self.cfg
+        w = self._block_field(which + "_outliers", 4 * c.outliers).contiguous().view(torch.int32)
+        w = w.reshape(c.batch, c.n_kv_heads, self.cap, c.outliers)
+        return (w >> 16) & 0xFFFF, w & 0xFFFF
 
     def key_norms(self) -> torch.Tensor:
         """Per-channel key factors fp32 [B][H][d] (INNERQ_KNORM), stored after

@@ -33,6 +33,7 @@ _TENSOR_V = 2
 _TENSOR_Q = 3
 _TENSOR_OUTLIER = 7
 _TENSOR_OFFSET = 8
+_TENSOR_LENGTH = 9
 
 
 @dataclasses.dataclass(frozen=True)
@@ -62,6 +63,7 @@ class Workload:
     v_queue: bool = False            # KIVI: values leave fp16 one at a time (a queue)
     meta_f16: bool = False           # scales and zeros stored in fp16
     outliers: int = 0                # KIVI: fp16 outliers kept per token and tensor
+    ragged: bool = False             # every sequence has its own prompt length
 
     @property
     def group_ratio(self) -> int:
@@ -167,6 +169,22 @@ def head_tokens(w: Workload, b: int, h: int, part: int, n: int,
     if w.first_token_k_mult != 1.0 and first_token == 0 and n > 0:
         k[0, :] *= np.float32(w.first_token_k_mult)
     return k.astype(np.float16), v.astype(np.float16)
+
+
+def prompt_lengths(w: Workload) -> np.ndarray:
+    """Prompt length of each sequence, int32 [B]: all ctx, or (ragged) drawn
+    uniformly from [0, ctx] per sequence from the workload's seed, with the
+    first sequence at ctx (the longest) and, from four sequences on, the
+    second empty and the third shorter than the residual / window."""
+    if not w.ragged:
+        return np.full(w.batch, w.ctx, np.int32)
+    rng = _rng(w.seed, _TENSOR_LENGTH)
+    lens = rng.integers(0, w.ctx + 1, size=w.batch).astype(np.int32)
+    lens[0] = w.ctx
+    if w.batch >= 4:
+        lens[1] = 0
+        lens[2] = min(w.ctx, max(0, w.residual - 1))
+    return lens
 
 
 def _threads() -> int:

@@ -34,31 +34,39 @@
  * Packed layout.  cap = max_ctx rounded up to a multiple of 128 is the
  * per-head token capacity.  Every per-token quantity of the quantized region
  * lives in 32-token blocks, so one contiguous read fetches everything a
- * 32-token tile needs except the KIVI key statistics:
+ * 32-token tile needs except the KIVI key statistics for G >= 64.  M below is
+ * f32, or fp16 under KVQ_META_F16 (m = its size in bytes, 4 or 2):
  *   blocks  u8 [B][H][cap/32][block_bytes]; block j of a head holds tokens
  *           32j .. 32j+31 (token t at row i = t mod 32) as
  *             K codes  [32][d*bits/8]    channel c of a row at bits
  *             V codes  [32][d*bits/8]    (c mod (8/bits))*bits of byte c/(8/bits)
- *             V scale  f32 [32][d/v_group]   (per token, channel group)
- *             V zero   f32 [32][d/v_group]
+ *             V scale  M [32][d/v_group]   (per token, channel group)
+ *             V zero   M [32][d/v_group]
  *             InnerQ only:
- *             K scale  f32 [32][d/k_group]   (per token, channel group)
- *             K zero   f32 [32][d/k_group]
+ *             K scale  M [32][d/k_group]   (per token, channel group)
+ *             K zero   M [32][d/k_group]
  *             KIVI with G <= 32 only:
- *             K stats  f32 [32/G][2][d]  per key group of the block: scale
+ *             K stats  M [32/G][2][d]  per key group of the block: scale
  *                      row, then zero (= min) row, one value per channel
- *           block_bytes = 64*d*bits/8 + 256*(d/v_group + (InnerQ ? d/k_group : 0))
- *                         + (KIVI, G <= 32 ? (32/G)*8*d : 0), a multiple of 128.
+ *             KIVI with o = cfg.outliers > 0 only:
+ *             K outliers u32 [32][o]  per token: (channel << 16) | fp16 bits
+ *             V outliers u32 [32][o]  of its o outliers, channels ascending
+ *           block_bytes = 64*d*bits/8 + 64*m*(d/v_group + (InnerQ ? d/k_group : 0))
+ *                         + (KIVI, G <= 32 ? (32/G)*2*m*d : 0) + 256*o,
+ *           a multiple of 128.
  *           KVQ_INNERQ_KNORM: the blocks buffer ends with the key factors
  *             f32 [B][H][d] (n_c above), after the last head's blocks.
  *   KIVI with G >= 64:
- *           k_meta  f32 [B][H][cap/G][2][d]  the same two rows per key group
+ *           k_meta  M [B][H][cap/G][2][d]  the same two rows per key group
  *           (the buffer carries 64 bytes of slack after the last head)
- *   KIVI:   k_res, v_res   fp16 [B][H][R][d]  residual, oldest first
+ *   KIVI:   k_res, v_res   fp16 [B][H][R][d]  residual, oldest first; with
+ *                           KVQ_VALUE_QUEUE, v_res is a ring: the fp16 value
+ *                           of token t sits in slot t mod R
  *   InnerQ: k_mode, v_mode  u32 [B][H][cap*(d/group)/32]  bit i = group
  *                           i % (d/group) of token i / (d/group); 1 = symmetric
  *           k_res, v_res   fp16 [B][H][W][d]   recent window, a ring (see ring_head)
  *           k_sink, v_sink fp16 [B][H][S][d]   first S tokens
+ *   KVQ_RAGGED: seq_prompt int32 [B]  each sequence's prompt length
  *   Quantized tokens occupy slots [0, n_quant) in arrival order.
  */
 #ifndef KVQ_H
@@ -85,6 +93,11 @@ extern "C" {
 #define KVQ_INNERQ 1
 #define KVQ_INNERQ_KNORM 2 /* InnerQ with the one-shot per-channel key normalization */
 
+/* Cache-format options (kvq_config.flags). */
+#define KVQ_META_F16 1u    /* scales and zero points stored in fp16 */
+#define KVQ_VALUE_QUEUE 2u /* KIVI: values leave the fp16 residual one at a time */
+#define KVQ_RAGGED 4u      /* every sequence of the batch has its own length */
+
 /*
  * Cache configuration.
  *   batch, n_q_heads, n_kv_heads: n_q_heads % n_kv_heads == 0; query head hq
@@ -107,6 +120,31 @@ extern "C" {
  *     quantized tokens.  Sinks and window stay the raw fp16 keys.
  *   max_ctx: most tokens one sequence will hold (prompt + appended), at most
  *     2^30 (KVQ_EUNSUPPORTED above).
+ *   flags: any of
+ *     KVQ_META_F16 (pgsm.cn how-to §3.1 stores the residual design without
+ *       fixing the statistics' precision): the fp32 scale and zero of the
+ *       formula are each rounded once to fp16 (IEEE nearest-even) and the
+ *       codes are taken with the stored values, code = clamp(rint((x -
+ *       zero16) / scale16)) (symmetric: q = clamp(rint(x / scale16)), zero =
+ *       -2^(b-1) * scale16), so dequantization uses exactly what is stored; a
+ *       scale that rounds to 0 is a constant group.  Needs |x| small enough
+ *       that every stored value is finite (|x| <= 8192 covers every case).
+ *     KVQ_VALUE_QUEUE (KIVI only; [KIVI] 工作原理, value paragraph: the
+ *       newest values wait in a queue, and once it reaches R the oldest is
+ *       quantized): after n tokens the last min(n, R - 1) values are fp16 and
+ *       the first max(0, n - R + 1) are quantized per token; keys still flush
+ *       every R tokens.
+ *     KVQ_RAGGED: sequences have their own prompt lengths
+ *       (kvq_quantize_prefill_ragged); every append adds one token to every
+ *       sequence.
+ *   outliers (KIVI only; "大模型量化技术原理", KVQuant / 技术原理 四: per
+ *     vector, the outliers are kept apart in fp16 and the rest quantized over
+ *     the narrower range): o in 0..8.  Each token's o largest-magnitude key
+ *     elements and o largest value elements (equal magnitudes: the lower
+ *     channel) are kept as (channel, fp16) lists; the statistics of every key
+ *     group (each channel over its G tokens) and value group come from the
+ *     other elements only (none left: scale 0, zero 0), outlier positions
+ *     store code 0, and decode uses the fp16 value there.
  */
 typedef struct kvq_config {
   int32_t batch;
@@ -120,6 +158,8 @@ typedef struct kvq_config {
   int32_t residual;
   int32_t n_sink;
   int64_t max_ctx;
+  uint32_t flags;
+  int32_t outliers;
 } kvq_config;
 
 /* Byte sizes of the cache buffers for a configuration (0 = unused). */
@@ -129,30 +169,40 @@ typedef struct kvq_sizes {
   size_t k_mode, v_mode;
   size_t k_res, v_res;
   size_t k_sink, v_sink;
-  size_t status; /* one int32 status word */
+  size_t status;     /* one int32 status word */
+  size_t seq_prompt; /* KVQ_RAGGED: int32 per sequence (0 otherwise) */
 } kvq_sizes;
 
 /*
  * Cache view.  The caller allocates every buffer (sizes from kvq_cache_sizes,
  * 16-byte aligned), zero-fills `dev_status` once, and keeps this struct; the
- * library updates the host counters below.  Lengths are uniform across the
- * batch.  Copying the struct together with the buffers checkpoints the cache.
+ * library updates the host counters below.  Copying the struct together with
+ * the buffers checkpoints the cache.
  *   n_quant   tokens in the quantized region (slots [0, n_quant))
  *   n_resid   KIVI: fp16 residual tokens (< R); InnerQ: window tokens (<= W)
  *   n_sink    InnerQ: sink tokens held (<= S)
  *   ring_head InnerQ: window slot of the oldest token once the window is full
- * Every call except kvq_quantize_prefill (which resets them) first checks
- * that the counters describe a reachable state (n_sink <= S, n_resid <= R or
- * W, KIVI n_resid < R and n_quant a multiple of R, ring_head < W, n_quant <=
- * capacity, all tokens <= max_ctx) and returns KVQ_EINVAL otherwise.
+ *   n_appended  tokens appended to every sequence since the prefill
+ * Without KVQ_RAGGED lengths are uniform across the batch and the counters
+ * describe every sequence.  With KVQ_RAGGED they describe the longest
+ * sequence (capacity checks and launch sizes use them); sequence b holds
+ * seq_prompt[b] + n_appended tokens, and its own counters follow from that
+ * length exactly as a uniform cache's would (the device reads seq_prompt).
+ * Every call except the prefills (which reset them) first checks that the
+ * counters describe a reachable state (n_sink <= S, n_resid <= R or W, KIVI
+ * n_resid < R and n_quant a multiple of R, ring_head < W, n_quant <=
+ * capacity, all tokens <= max_ctx, n_appended <= all tokens) and returns
+ * KVQ_EINVAL otherwise.
  */
 typedef struct kvq_cache {
   void *blocks;
-  float *k_meta;
+  void *k_meta;
   uint32_t *k_mode, *v_mode;
   uint16_t *k_res, *v_res, *k_sink, *v_sink;
   int64_t n_quant, n_resid, n_sink, ring_head;
   int32_t *dev_status;
+  int32_t *seq_prompt; /* KVQ_RAGGED: device int32 [B], written by the prefill */
+  int64_t n_appended;
 } kvq_cache;
 
 /* Fills *out with the byte size of each cache buffer.  Returns KVQ_OK,
@@ -181,6 +231,22 @@ int kvq_workspace_bytes(const kvq_config *cfg, size_t *bytes);
  */
 int kvq_quantize_prefill(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K,
                          const uint16_t *V, int64_t T, void *stream);
+
+/*
+ * Prefill of sequences with their own prompt lengths (KVQ_RAGGED; pgsm.cn
+ * how-to §3.1 keeps a residual per sequence).  K, V: device fp16
+ * [B][H][T_max][d], sequence b's prompt in rows [0, lens[b]) (later rows are
+ * not read).  lens: HOST int32 [B], 0 <= lens[b] <= T_max <= max_ctx, copied
+ * to cache->seq_prompt on `stream` (a pageable host copy: the call returns
+ * once lens is no longer needed).  Each sequence is quantized exactly as
+ * kvq_quantize_prefill quantizes a prompt of its length; the host counters
+ * then describe the longest one.  kvq_quantize_prefill on a KVQ_RAGGED cache
+ * gives every sequence the length T.
+ * Errors: as kvq_quantize_prefill; KVQ_EINVAL without KVQ_RAGGED.
+ */
+int kvq_quantize_prefill_ragged(const kvq_config *cfg, kvq_cache *cache, const uint16_t *K,
+                                const uint16_t *V, int64_t T_max, const int32_t *lens,
+                                void *stream);
 
 /*
  * Append one decode token per (batch, kv head).  k, v: device fp16 [B][H][d].
@@ -229,8 +295,8 @@ int kvq_decode_attention(const kvq_config *cfg, const kvq_cache *cache, const ui
  *   kvq_decode_attention (values are not rotated; an empty cache gives zeros).
  *   ws: the decode scratch (kvq_workspace_bytes; zero-filled, left zero).
  * Errors: as kvq_decode_attention; KVQ_EINVAL for rope_base <= 0 or not
- *   finite; KVQ_EUNSUPPORTED for n_q_heads / n_kv_heads = 8 or max_ctx > 2^24
- *   (positions are exact in fp32).
+ *   finite; KVQ_EUNSUPPORTED for n_q_heads / n_kv_heads = 8, max_ctx > 2^24
+ *   (positions are exact in fp32), or any kvq_config.flags / outliers option.
  */
 int kvq_decode_attention_rope(const kvq_config *cfg, const kvq_cache *cache, const uint16_t *q,
                               float *out, float softmax_scale, double rope_base, void *ws,

@@ -22,22 +22,36 @@ def new_cache(w, max_ctx=None):
     return kvq.QuantizedKVCache(kvq.config_of(w, max_ctx), "cuda")
 
 
-def oracle_head(w, b, h, max_ctx):
+def oracle_head(w, b, h, max_ctx, T=None):
+    """Oracle state of head (b, h) after the prefill of its T prompt tokens
+    (default: the workload's ctx)."""
+    T = w.ctx if T is None else int(T)
     head = oracle.OracleHead.for_workload(w, cap=max_ctx)
     K, V = synth.head_tokens(w, b, h, 0, w.ctx)
-    head.prefill(K, V)
+    head.prefill(K[:T], V[:T])
+    head.nq_prefill = head.n_quant  # evictions since the prefill give the window's ring offset
     return head
 
 
+def _same_bits(got, exp, what):
+    assert got.size == exp.size, (what, got.shape, exp.shape)
+    assert np.array_equal(got.reshape(-1).view(np.uint32), exp.reshape(-1).view(np.uint32)), what
+
+
 def check_head_state(cache, w, b, h, head):
-    """Byte-for-byte comparison of one head's cache contents with the oracle."""
-    assert cache.n_quant == head.n_quant, (cache.n_quant, head.n_quant)
-    assert cache.n_resid == head.n_resid
-    n = head.n_quant
+    """Byte-for-byte comparison of one head's cache contents with the oracle.
+    The oracle's counters say which rows of the cache are live (under ragged
+    lengths the host counters describe the longest sequence only)."""
+    ragged = getattr(w, "ragged", False)
+    if not ragged:
+        assert cache.n_quant == head.n_quant, (cache.n_quant, head.n_quant)
+        assert cache.n_resid == head.n_resid
+    n, nvq = head.n_quant, head.n_vquant
+    where = "(b=%d h=%d)" % (b, h)
     kc = cache.codes("k")[b, h, :n].cpu().numpy()
-    vc = cache.codes("v")[b, h, :n].cpu().numpy()
-    assert np.array_equal(kc, head.packed_k()), "key codes differ (b=%d h=%d)" % (b, h)
-    assert np.array_equal(vc, head.packed_v()), "value codes differ (b=%d h=%d)" % (b, h)
+    vc = cache.codes("v")[b, h, :nvq].cpu().numpy()
+    assert np.array_equal(kc, head.packed_k()), "key codes differ " + where
+    assert np.array_equal(vc, head.packed_v()), "value codes differ " + where
     ks_o, kz_o = head.k_meta()
     vs_o, vz_o = head.v_meta()
     ks = cache.meta("k_scale")[b, h, : ks_o.size].cpu().numpy()
@@ -46,28 +60,49 @@ def check_head_state(cache, w, b, h, head):
     vz = cache.meta("v_zero")[b, h, : vz_o.size].cpu().numpy()
     for got, exp, name in ((ks, ks_o, "k_scale"), (kz, kz_o, "k_zero"), (vs, vs_o, "v_scale"),
                            (vz, vz_o, "v_zero")):
-        assert np.array_equal(got.view(np.uint32), exp.reshape(-1).view(np.uint32)), \
-            "%s differs (b=%d h=%d)" % (name, b, h)
+        _same_bits(got, exp, "%s differs %s" % (name, where))
+    if getattr(w, "outliers", 0):
+        for which, rows, oidx, oval in (("k", n, head.k_oidx, head.k_oval),
+                                        ("v", nvq, head.v_oidx, head.v_oval)):
+            idx, bits = cache.outlier_lists(which)
+            idx = idx[b, h, :rows].cpu().numpy()
+            bits = bits[b, h, :rows].cpu().numpy()
+            assert np.array_equal(idx, oidx[:rows].astype(np.int32)), \
+                "%s outlier channels differ %s" % (which, where)
+            assert np.array_equal(bits, oval[:rows].astype(np.int32)), \
+                "%s outlier values differ %s" % (which, where)
     if getattr(w, "k_norm", False):
         kn = cache.key_norms()[b, h].cpu().numpy()
         assert np.array_equal(kn.view(np.uint32), head.key_norms().view(np.uint32)), \
-            "key factors differ (b=%d h=%d)" % (b, h)
+            "key factors differ " + where
     kr_o, vr_o = head.residual_tokens()
     nr = head.n_resid
     if w.scheme == synth.KIVI:
-        kr = cache.fp16_rows("k_res", w.residual)[b, h, :nr].cpu().numpy()
-        vr = cache.fp16_rows("v_res", w.residual)[b, h, :nr].cpu().numpy()
+        R = w.residual
+        kr = cache.fp16_rows("k_res", R)[b, h, :nr].cpu().numpy()
+        if getattr(w, "v_queue", False):
+            # the queue's values, oldest first: token t sits in ring slot t mod R
+            vr_o = head.value_queue()
+            slots = [(nvq + i) % R for i in range(len(vr_o))]
+            vr = cache.fp16_rows("v_res", R)[b, h].cpu().numpy()[slots]
+        else:
+            vr = cache.fp16_rows("v_res", R)[b, h, :nr].cpu().numpy()
     else:
-        # window ring: slot (ring_head + i) % W holds the i-th oldest token
+        # window ring: slot (ring_head + i) % W holds the i-th oldest token, and
+        # the ring moves one slot per eviction since the prefill
         W = w.residual
-        order = [(cache.ring_head + i) % W for i in range(nr)] if nr == W else list(range(nr))
+        ring_head = (head.n_quant - head.nq_prefill) % W if W > 0 else 0
+        if not ragged:
+            assert cache.ring_head == ring_head
+        order = [(ring_head + i) % W for i in range(nr)] if nr == W else list(range(nr))
         if W > 0:
             kr = cache.fp16_rows("k_res", W)[b, h].cpu().numpy()[order]
             vr = cache.fp16_rows("v_res", W)[b, h].cpu().numpy()[order]
         else:
             kr = vr = np.zeros((0, w.head_dim), np.float16)
         ns = head.n_sink_used
-        assert cache.n_sink == ns
+        if not ragged:
+            assert cache.n_sink == ns
         if ns:
             ksk_o, vsk_o = head.sink_tokens()
             ksk = cache.fp16_rows("k_sink", w.n_sink)[b, h, :ns].cpu().numpy()
@@ -84,8 +119,9 @@ def check_head_state(cache, w, b, h, head):
             if nbits % 32:
                 mask = np.uint32((1 << (nbits % 32)) - 1)
                 assert (words[full] & mask) == (exp[full] & mask), "%s mode tail" % which
-    assert np.array_equal(kr.view(np.uint16), kr_o.view(np.uint16)), "key residual differs"
-    assert np.array_equal(vr.view(np.uint16), vr_o.view(np.uint16)), "value residual differs"
+    assert np.array_equal(kr.view(np.uint16), kr_o.view(np.uint16)), "key residual differs " + where
+    assert np.array_equal(vr.view(np.uint16), vr_o.view(np.uint16)), \
+        "value residual differs " + where
 
 
 def check_decode(out, q, w, b, h, head, tau, rope_base=None):
@@ -116,10 +152,14 @@ def run_workload(w, heads=None, n_append=None, decode_every=None, max_ctx=None,
     if heads is None:
         heads = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
     K, V = synth.prompt(w)
+    lens = synth.prompt_lengths(w)
     cache = new_cache(w, max_ctx)
-    cache.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
+    if getattr(w, "ragged", False):
+        cache.prefill_ragged(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda(), lens)
+    else:
+        cache.prefill(torch.from_numpy(K).cuda(), torch.from_numpy(V).cuda())
     del K, V
-    heads_o = {bh: oracle_head(w, bh[0], bh[1], max_ctx) for bh in heads}
+    heads_o = {bh: oracle_head(w, bh[0], bh[1], max_ctx, lens[bh[0]]) for bh in heads}
     torch.cuda.synchronize()
     for (b, h), ho in heads_o.items():
         check_head_state(cache, w, b, h, ho)

@@ -201,7 +201,7 @@ def test_binding_rejects_bad_tensors_before_any_call():
 def test_binding_block_layout_matches_the_library():
     """The binding's mirror of the block layout (used to read codes and
     statistics back) gives the same block size as kvq_cache_sizes, for every
-    supported bits / scheme / group combination."""
+    supported bits / scheme / group combination and cache-format option."""
     cases = []
     for bits in (2, 4):
         for d in (64, 128):
@@ -209,13 +209,17 @@ def test_binding_block_layout_matches_the_library():
                 if d % gv:
                     continue
                 for G in (16, 32, 64, 128):
-                    cases.append(dict(head_dim=d, bits=bits, v_group=gv, k_group=G,
-                                      residual=G * 2, scheme=kvq.KIVI))
+                    for flags in (0, kvq.META_F16, kvq.VALUE_QUEUE | kvq.RAGGED):
+                        for o in (0, 1, 8):
+                            cases.append(dict(head_dim=d, bits=bits, v_group=gv, k_group=G,
+                                              residual=G * 2, scheme=kvq.KIVI, flags=flags,
+                                              outliers=o))
                 for gk in (16, 32, 64, 128):
                     if d % gk == 0:
                         for sch in (kvq.INNERQ, kvq.INNERQ_KNORM):
-                            cases.append(dict(head_dim=d, bits=bits, v_group=gv, k_group=gk,
-                                              residual=8, n_sink=2, scheme=sch))
+                            for flags in (0, kvq.META_F16 | kvq.RAGGED):
+                                cases.append(dict(head_dim=d, bits=bits, v_group=gv, k_group=gk,
+                                                  residual=8, n_sink=2, scheme=sch, flags=flags))
     for kw in cases:
         cfg = _cfg(batch=2, n_q_heads=3, n_kv_heads=3, max_ctx=300, **kw)
         s = kvq.cache_sizes(cfg)
@@ -226,16 +230,71 @@ def test_binding_block_layout_matches_the_library():
         extra = BH * cfg.head_dim * 4 if cfg.scheme == kvq.INNERQ_KNORM else 0
         assert s.blocks == BH * (cap // 32) * bb + extra, kw
         assert rb == cfg.head_dim * cfg.bits // 8 and bb % 128 == 0, kw
+        assert s.seq_prompt == (2 * 4 if cfg.flags & kvq.RAGGED else 0), kw
+        m = 2 if cfg.flags & kvq.META_F16 else 4
+        if cfg.scheme == kvq.KIVI and cfg.k_group > 32:
+            assert s.k_meta == BH * (cap // cfg.k_group) * 2 * cfg.head_dim * m + 64, kw
 
 
-def test_config_refuses_variants_the_library_lacks():
-    """Workload fields for cache-format variants that only the oracle has so
-    far are refused, never silently dropped."""
+def test_format_options_sizes_and_refusals():
+    """fp16 statistics cut the Llama-2-7B layer's 2-bit tokens from 128 to 96
+    bytes per token-head (codes 64 + statistics 32); outlier lists add 8 bytes
+    per outlier (key and value word); options outside their scheme, unknown
+    flag bits and more than 8 outliers are refused; the pre-RoPE decode
+    refuses every option."""
+    per_tok = lambda s: s.blocks / (8 * 32 * 4352)  # noqa: E731
+    assert per_tok(kvq.cache_sizes(_cfg(max_ctx=4300))) == 128
+    assert per_tok(kvq.cache_sizes(_cfg(max_ctx=4300, flags=kvq.META_F16))) == 96
+    assert per_tok(kvq.cache_sizes(_cfg(max_ctx=4300, outliers=2))) == 128 + 16
+    for kw in (dict(flags=8), dict(outliers=9), dict(outliers=-1),
+               dict(scheme=kvq.INNERQ, k_group=64, residual=32, n_sink=4, outliers=1),
+               dict(scheme=kvq.INNERQ, k_group=64, residual=32, n_sink=4,
+                    flags=kvq.VALUE_QUEUE)):
+        with pytest.raises(kvq.KVQError) as e:
+            kvq.cache_sizes(_cfg(**kw))
+        assert e.value.code == kvq.KVQ_EINVAL, kw
+    # the workload fields map onto the options
     base = synth.scaled(synth.WORKLOADS["tiny"])
-    kvq.config_of(base)
-    for kw in (dict(v_queue=True), dict(meta_f16=True), dict(outliers=1)):
-        with pytest.raises(ValueError):
-            kvq.config_of(synth.scaled(base, **kw))
+    cfg = kvq.config_of(synth.scaled(base, v_queue=True, meta_f16=True, outliers=1, ragged=True))
+    assert cfg.flags == kvq.META_F16 | kvq.VALUE_QUEUE | kvq.RAGGED and cfg.outliers == 1
+    L = kvq.lib()
+    c = kvq.Cache()
+    for name in ("blocks", "k_meta", "k_res", "v_res"):
+        setattr(c, name, 0x1000)
+    for kw in (dict(flags=kvq.META_F16), dict(outliers=1)):
+        cfg = _cfg(**kw)
+        assert L.kvq_decode_attention_rope(ctypes.byref(cfg), ctypes.byref(c),
+                                           ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000), 1.0,
+                                           10000.0, ctypes.c_void_p(0x4000), 1 << 40,
+                                           None) == kvq.KVQ_EUNSUPPORTED
+
+
+def test_ragged_prefill_validates_on_the_host():
+    """The ragged prefill needs the option, a seq_prompt buffer and lengths in
+    [0, T_max]; each is checked before anything is enqueued."""
+    L = kvq.lib()
+    c = kvq.Cache()
+    for name in ("blocks", "k_meta", "k_res", "v_res"):
+        setattr(c, name, 0x1000)
+    lens = (ctypes.c_int32 * 8)(*([100] * 8))
+    K = ctypes.c_void_p(0x2000)
+    plain = _cfg()
+    assert L.kvq_quantize_prefill_ragged(ctypes.byref(plain), ctypes.byref(c), K, K, 100, lens,
+                                         None) == kvq.KVQ_EINVAL
+    rag = _cfg(flags=kvq.RAGGED)
+    assert L.kvq_quantize_prefill_ragged(ctypes.byref(rag), ctypes.byref(c), K, K, 100, lens,
+                                         None) == kvq.KVQ_EINVAL   # no seq_prompt buffer
+    c.seq_prompt = 0x1000
+    assert L.kvq_quantize_prefill_ragged(ctypes.byref(rag), ctypes.byref(c), K, K, 100, None,
+                                         None) == kvq.KVQ_EINVAL
+    bad = (ctypes.c_int32 * 8)(*([100] * 7 + [101]))
+    assert L.kvq_quantize_prefill_ragged(ctypes.byref(rag), ctypes.byref(c), K, K, 100, bad,
+                                         None) == kvq.KVQ_EINVAL
+    neg = (ctypes.c_int32 * 8)(*([100] * 7 + [-1]))
+    assert L.kvq_quantize_prefill_ragged(ctypes.byref(rag), ctypes.byref(c), K, K, 100, neg,
+                                         None) == kvq.KVQ_EINVAL
+    assert L.kvq_quantize_prefill_ragged(ctypes.byref(rag), ctypes.byref(c), K, K, 5000, lens,
+                                         None) == kvq.KVQ_ECAPACITY
 
 
 def test_corrupted_counters_are_rejected_before_any_launch():
