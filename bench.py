@@ -46,17 +46,49 @@ EPOCH = 256  # streamed appends per replayed epoch
 # bytes of one decode step (algorithmic: what the kernel must read)
 # ---------------------------------------------------------------------------
 
-def decode_bytes(w, n_quant, n_resid, n_sink):
-    """Codes + fp32 scale/zero + fp16 residual/sink rows, all heads."""
-    BH, d, b = w.batch * w.n_kv_heads, w.head_dim, w.bits
-    codes = 2 * n_quant * d * b // 8
+def head_counts(w, n, prompt=None):
+    """(n_quant, n_resid, n_sink, n_vq) of one sequence holding n tokens (the
+    cache's counting rules: KIVI residual n mod R, value queue max(0, n-R+1);
+    InnerQ sinks, then window, then quantized)."""
     if w.scheme == synth.KIVI:
-        kmeta = (n_quant // w.k_group) * d * 8
+        nr = n % w.residual
+        nq = n - nr
+        nvq = max(0, n - w.residual + 1) if w.v_queue else nq
+        return nq, nr, 0, nvq
+    ns = min(n, w.n_sink)
+    nw = min(n - ns, w.residual)
+    return n - ns - nw, nw, ns, n - ns - nw
+
+
+def head_bytes(w, nq, nr, ns, nvq=None):
+    """Algorithmic bytes one decode reads for one KV head: key and value codes,
+    their scales and zeros (fp32, or fp16 with fp16 statistics), outlier lists
+    (4 bytes an entry), and the fp16 rows (sinks, residual / window, and under
+    the value queue the values still waiting)."""
+    nvq = nq if nvq is None else nvq
+    d, b = w.head_dim, w.bits
+    m = 2 if w.meta_f16 else 4
+    if w.scheme == synth.KIVI:
+        kmeta = (nq // w.k_group) * d * 2 * m
     else:
-        kmeta = n_quant * (d // w.k_group) * 8
-    vmeta = n_quant * (d // w.v_group) * 8
-    fp16 = (n_resid + n_sink) * d * 2 * 2
-    return BH * (codes + kmeta + vmeta + fp16)
+        kmeta = nq * (d // w.k_group) * 2 * m
+    keys = nq * d * b // 8 + kmeta + nq * w.outliers * 4 + (nr + ns) * d * 2
+    n = nq + nr + ns
+    values = nvq * d * b // 8 + nvq * (d // w.v_group) * 2 * m + nvq * w.outliers * 4 + \
+        (n - nvq) * d * 2
+    return keys + values
+
+
+def decode_bytes(w, n_quant, n_resid, n_sink):
+    """All heads at uniform counters (the value queue's count follows)."""
+    n = n_quant + n_resid + n_sink
+    nvq = head_counts(w, n)[3] if w.v_queue else n_quant
+    return w.batch * w.n_kv_heads * head_bytes(w, n_quant, n_resid, n_sink, nvq)
+
+
+def decode_bytes_ragged(w, lengths):
+    """All heads, each sequence with its own length."""
+    return w.n_kv_heads * sum(head_bytes(w, *head_counts(w, int(n))) for n in lengths)
 
 
 def kivi_states(w, n0, r0, steps):
@@ -613,8 +645,9 @@ def measure_config(w, dev, stream, peak):
     t0 = time.time()
     Kd, Vd = prompt_on_device(w, dev)
     gen_s = time.time() - t0
+    lens = synth.prompt_lengths(w)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_copy = decode_bytes(w, w.ctx, 0, 0)
+    per_copy = decode_bytes_ragged(w, lens) if w.ragged else decode_bytes(w, w.ctx, 0, 0)
     copies = min(64, max(2, math.ceil(3 * l2 / max(1, per_copy)) + 1))
     caches = [kvq.QuantizedKVCache(cfg, dev) for _ in range(copies)]
     pre_ms = []
@@ -622,11 +655,15 @@ def measure_config(w, dev, stream, peak):
         for c in caches:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            c.prefill(Kd, Vd, stream)
+            if w.ragged:
+                c.prefill_ragged(Kd, Vd, lens, stream)
+            else:
+                c.prefill(Kd, Vd, stream)
             e1.record(stream)
             e1.synchronize()
             pre_ms.append(e0.elapsed_time(e1))
-    prompt_bytes = 2 * Kd.numel() * 2
+    prompt_bytes = 2 * Kd.numel() * 2 if not w.ragged else \
+        2 * int(np.sum(lens)) * w.n_kv_heads * w.head_dim * 2
     del Kd, Vd
     Ks, Vs = synth.streamed(w, max(1, w.n_append))
     k, v = torch.from_numpy(Ks[0]).to(dev), torch.from_numpy(Vs[0]).to(dev)
@@ -638,7 +675,8 @@ def measure_config(w, dev, stream, peak):
             c.append(k, v, stream)
     stream.synchronize()
     c0 = caches[0]
-    nbytes = decode_bytes(w, c0.n_quant, c0.n_resid, c0.n_sink)
+    nbytes = (decode_bytes_ragged(w, c0.seq_lengths()) if w.ragged
+              else decode_bytes(w, c0.n_quant, c0.n_resid, c0.n_sink))
     ideal_s = nbytes / (peak * 1e9)
     M = max(2 * copies, min(256, int(0.05 / max(ideal_s, 1e-7))))
     with torch.cuda.stream(stream):
@@ -680,14 +718,21 @@ def measure_config(w, dev, stream, peak):
     }
 
 
-def run_configs(names, peak):
+# Cache-format options timed on the headline layer (decode kernel alone).
+FORMATS = {"meta_f16": dict(meta_f16=True), "outliers_2": dict(outliers=2),
+           "value_queue": dict(v_queue=True), "ragged": dict(ragged=True)}
+
+
+def run_configs(names, peak, base=None):
+    """names: workloads (base None) or, with a base workload, FORMATS keys."""
     import torch
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     stream = torch.cuda.Stream(dev)
     out = {}
     for name in names:
+        w = synth.WORKLOADS[name] if base is None else synth.scaled(base, **FORMATS[name])
         try:
-            out[name] = measure_config(synth.WORKLOADS[name], dev, stream, peak)
+            out[name] = measure_config(w, dev, stream, peak)
         except Exception as exc:  # noqa: BLE001 -- one config's failure drops only its line
             out[name] = {"error": ("%s: %s" % (type(exc).__name__, exc))[:300]}
         torch.cuda.synchronize(dev)
@@ -708,6 +753,10 @@ def main():
                     help="comma-separated workloads whose decode kernel is also timed alone "
                          "(one GPU only); 'others' = every named workload but the headline one, "
                          "'none' = skip")
+    ap.add_argument("--formats", default="all",
+                    help="comma-separated cache-format options timed on the headline workload "
+                         "(decode kernel alone; one GPU only): " + ", ".join(sorted(FORMATS)) +
+                         "; 'all' or 'none'")
     ap.add_argument("--rope-base", type=float, default=None,
                     help="time the variant whose keys are cached before the rotary embedding "
                          "(kvq_decode_attention_rope with this base) instead of the plain decode")
@@ -788,6 +837,10 @@ def main():
         names = ([n for n in synth.WORKLOADS if n != w.name] if args.configs == "others"
                  else [n for n in args.configs.split(",") if n])
         line["configs"] = run_configs(names, peak)
+    if world == 1 and args.formats != "none" and args.rope_base is None:
+        names = (sorted(FORMATS) if args.formats == "all"
+                 else [n for n in args.formats.split(",") if n])
+        line["formats"] = run_configs(names, peak, base=w)
     if rank == 0 and world == 1 and not args.skip_cpu:
         rate, threads, desc, _ = oracle_decode_rate(w, seconds=args.cpu_seconds,
                                                     rope_base=args.rope_base)

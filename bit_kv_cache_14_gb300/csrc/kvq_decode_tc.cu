@@ -39,830 +39,11 @@
 //    can overflow (|q| <= 1, scales <= 65504).
 #include <stdio.h>
 
-#include "kvq_tc_common.cuh"
+#include "kvq_decode_tc.cuh"
 
 namespace kvq {
 
 namespace {
-
-// Work units: a quantized tile is one unit, an fp16 chunk kChunkUnits (its
-// dot products run on the CUDA cores in a long dependent chain), and every
-// head starts with kHeadUnits units that hold no data.  They fall to the
-// warp that holds the head's first unit: the warp that changes heads there
-// and merges the head's partials at the end, both costs of about a tile.
-constexpr int kHeadUnits = 2;
-constexpr int kChunkUnits = 2;
-
-// What unit range [x0, x1) holds of head bh: its U units are HU empty ones,
-// S_h quantized tiles of kTile tokens, then F_h = nch * UPC fp16 units; a
-// chunk belongs to the warp that holds its first unit.
-__device__ __forceinline__ Seg warp_seg(const TcArgs &a, int bh, int x0, int x1) {
-  Seg s;
-  const int base = bh * a.U;
-  const int ua = max(x0, base) - base, ub = min(x1, base + a.U) - base;
-  const int qa = max(ua - a.HU, 0), qb = min(ub - a.HU, a.S_h);
-  s.tq0 = qa * kTile;
-  s.tq1 = qa < qb ? (int)min((int64_t)qb * kTile, a.n_quant) : s.tq0;
-  const int fa = max(ua - a.HU - a.S_h, 0), fb = min(ub - a.HU - a.S_h, a.F_h);
-  s.c0 = (fa + a.UPC - 1) / a.UPC;
-  s.c1 = fa < fb ? min((fb + a.UPC - 1) / a.UPC, a.nch) : s.c0;
-  return s;
-}
-
-template <int BITS, int SCHEME, int NGV, int NGK, int KM>
-__global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM>;
-  constexpr bool G16 = SCHEME == KVQ_KIVI && KM == 2;
-  constexpr int RB = SC::RB;  // packed bytes per token row
-  constexpr int nslot = SC::nslot;
-  constexpr int SLOT = SC::bytes;
-  const Geometry &g = a.g;
-  constexpr TcLayout Ly = tc_layout(SLOT, nslot, SC::SBB);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-  uint8_t *wring = smem + Ly.ring + warp * nslot * SLOT;
-  uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
-  uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB + warp * SC::SBB);
-  const uint32_t wring_s = smem_u32(wring), wbars_s = smem_u32(wbars);  // shared-window addresses
-
-  // Warp-level stream-K: warp gw of the grid owns units [x0, x1) of the
-  // concatenated per-head unit lists (units of one tile or fp16 chunk).
-  const int gw = (int)blockIdx.x * kWarps + warp;
-  if (gw >= a.nw) return;
-  const int x0 = (int)((int64_t)gw * a.total / a.nw);
-  const int x1 = (int)((int64_t)(gw + 1) * a.total / a.nw);
-  const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
-  // fp16 tokens per chunk: a chunk's K and V rows fill the slot up to the query
-  constexpr int CH = SC::CH;
-
-  // Each warp owns its ring and barriers; nothing below synchronises warps.
-  // Ring bytes are only read where a copy wrote them (rows past a segment's
-  // end are masked), so the ring needs no clearing; the zero block does.
-  if (lane < 16) sBw[SC::sb_zero + lane] = 0u;
-  if (lane == 0) {
-    for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncwarp();
-
-  // ---- producer: this warp's items in the order the consumer visits them:
-  // per head, its quantized tiles, then its fp16 chunks.
-  int pc_bh = bh_first, pc_ph = 0, pc_lt = 0, pc_n = 0, issued = 0, ps = 0;
-  const uint64_t pol_once = l2_evict_first();  // cache blocks are read once
-  Seg pc_seg = warp_seg(a, pc_bh, x0, x1);
-  pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
-  auto pc_settle = [&]() {
-    while (pc_bh >= 0 && pc_lt >= pc_n) {
-      if (pc_ph == 0) {
-        pc_ph = 1;
-        pc_n = pc_seg.c1 - pc_seg.c0;
-      } else {
-        if (++pc_bh > bh_last) {
-          pc_bh = -1;
-          return;
-        }
-        pc_ph = 0;
-        pc_seg = warp_seg(a, pc_bh, x0, x1);
-        pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
-      }
-      pc_lt = 0;
-    }
-  };
-  // Called by the whole warp; lane 0 posts the byte count and issues the
-  // copies of the next item of this warp.  A quantized tile: its cache block
-  // and, for KIVI G >= 64, its key group's statistics.  An fp16 chunk: its K
-  // rows, then its V rows (sink rows before residual / window rows).  The
-  // query row rides along with the warp's first item of each phase of a head.
-  auto issue_next = [&]() {
-    if (pc_bh < 0) return;
-    const bool first = pc_lt == 0;
-    uint8_t *dst = wring + ps * SLOT;
-    uint64_t *bar = &wbars[ps];
-    const uint32_t dst_s = wring_s + ps * SLOT, bar_s = wbars_s + 8 * ps;
-    ps = ps + 1 == nslot ? 0 : ps + 1;
-    if (pc_ph == 0) {
-      // a cache block: the common case, issued without a branch on the lane
-      const int tok0 = pc_seg.tq0 + kTile * pc_lt;
-      bulk_g2s_pred(lane == 0, bar_s, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)), dst_s,
-                    a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB, SC::BB,
-                    pol_once);
-      if (SCHEME == KVQ_KIVI && !SC::KIN && lane == 0)
-        bulk_g2s(dst + SC::off_km,
-                 a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD * g.msz,
-                 SC::KMB, bar);
-      if (first && lane == 0)
-        bulk_g2s(dst + SC::off_q, a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD, kD * 2,
-                 bar);
-    } else if (lane == 0) {
-      const __half *qrow = a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD;
-      const int ns = (int)a.n_sink;
-      const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
-      const int s0 = min(i0, ns), s1 = min(i1, ns);            // sink rows
-      const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;  // residual / window rows
-      bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2 + (first ? kD * 2 : 0)));
-      if (s1 > s0) {
-        const int64_t row = (int64_t)pc_bh * g.n_sink + s0;
-        bulk_g2s(dst, a.p.k_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
-        bulk_g2s(dst + CH * kD * 2, a.p.v_sink + row * kD, (uint32_t)((s1 - s0) * kD * 2), bar);
-      }
-      if (r1 > r0) {
-        // a fused append's new row is not in the residual yet: it comes from
-        // the step's input rows
-        const int rn = (a.new_row >= 0 && r1 - 1 == a.new_row) ? r1 - 1 : r1;
-        const int64_t row = (int64_t)pc_bh * g.residual + r0;
-        const int o = (s1 - s0) * kD * 2;
-        if (rn > r0) {
-          bulk_g2s(dst + o, a.p.k_res + row * kD, (uint32_t)((rn - r0) * kD * 2), bar);
-          bulk_g2s(dst + CH * kD * 2 + o, a.p.v_res + row * kD,
-                   (uint32_t)((rn - r0) * kD * 2), bar);
-        }
-        if (rn < r1) {
-          const int on = o + (rn - r0) * kD * 2;
-          bulk_g2s(dst + on, a.k_new + (int64_t)pc_bh * kD, kD * 2, bar);
-          bulk_g2s(dst + CH * kD * 2 + on, a.v_new + (int64_t)pc_bh * kD, kD * 2, bar);
-        }
-      }
-      if (first) bulk_g2s(dst + SC::off_q, qrow, kD * 2, bar);
-    }
-    ++issued;
-    ++pc_lt;
-    pc_settle();
-  };
-  pc_settle();
-  for (int s = 0; s < nslot; ++s) issue_next();
-
-  // ---- per-head constants (each warp for itself) --------------------------
-  float pow2E = 1.0f;  // scores = raw * 2^(E+24) (q normalised by 2^-E, codes by 2^-24)
-  float q4[4];         // q of channels 4*lane .. 4*lane+3 (exp2 domain)
-  // KIVI key operand: this lane builds the channel pairs (c, c + kHalf) of
-  // c = b_clo and c = b_clo + 1 (even positions p and p + 1 of word W), whose
-  // B-fragment words sit next to each other at b_sidx, b_sidx + 1
-  constexpr int kHalf = BITS == 2 ? 8 : 4;  // channel offset of the high half of a pair
-  int b_clo, b_sidx;
-  float qn_lo[2], qn_hi[2], qf_lo[2], qf_hi[2];
-  {
-    int W, p, tg, kb;
-    if (BITS == 2) {
-      W = lane >> 2;
-      p = 2 * (lane & 3);
-      b_clo = 16 * W + p;
-      tg = W >> 1;
-      kb = 4 * (W & 1) + (p >> 1);
-    } else {
-      W = lane >> 1;
-      p = 2 * (lane & 1);
-      b_clo = 8 * W + p;
-      tg = W >> 2;
-      kb = 2 * (W & 3) + (p >> 1);
-    }
-    b_sidx = tg * 16 + kb * 2;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) qn_lo[r] = qn_hi[r] = qf_lo[r] = qf_hi[r] = 0.0f;
-  }
-  // InnerQ: fixed key operand and per-group sums of q
-  uint32_t bqi[8][2];
-  float Qj[NGK];
-
-  // Per-head constants from the query row that rode along with the head's
-  // first tile of this warp.
-  auto start_head = [&](const uint8_t *slot, int cur_bh) {
-    const __half *qh = reinterpret_cast<const __half *>(slot + SC::off_q);
-    const uint2 qr = reinterpret_cast<const uint2 *>(qh)[lane];
-    const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
-    const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
-    q4[0] = q01.x * a.scale_log2;
-    q4[1] = q01.y * a.scale_log2;
-    q4[2] = q23.x * a.scale_log2;
-    q4[3] = q23.y * a.scale_log2;
-    // InnerQ with normalized keys: the per-channel factors go into q (the
-    // quantized tokens only; the fp16 rows reload the raw query)
-    const float *knr = SCHEME == KVQ_INNERQ && g.knorm ? a.p.k_norm + (int64_t)cur_bh * kD : nullptr;
-    if (knr) {
-      const float4 n4 = reinterpret_cast<const float4 *>(knr)[lane];
-      q4[0] *= n4.x;
-      q4[1] *= n4.y;
-      q4[2] *= n4.z;
-      q4[3] *= n4.w;
-    }
-    float mx = fmaxf(fmaxf(fabsf(q4[0]), fabsf(q4[1])), fmaxf(fabsf(q4[2]), fabsf(q4[3])));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    int E = 0;
-    if (mx > 0.0f && mx < INFINITY) frexpf(mx, &E);
-    pow2E = ldexpf(1.0f, E) * kSub;
-    const float inv = ldexpf(1.0f, -E);
-    auto qf = [&](int c) { return __half2float(qh[c]) * a.scale_log2 * (knr ? knr[c] : 1.0f); };
-    if (SCHEME == KVQ_KIVI) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int c = b_clo + r;
-        const int p = BITS == 2 ? (c & 7) : (c & 3);
-        const float invf = inv * inv_pos_factor<BITS>(p);
-        qf_lo[r] = qf(c);
-        qf_hi[r] = qf(c + kHalf);
-        qn_lo[r] = qf_lo[r] * invf;
-        qn_hi[r] = qf_hi[r] * invf;
-      }
-    } else {
-      const int GK = kD / NGK;
-      const float s4 = (q4[0] + q4[1]) + (q4[2] + q4[3]);
-#pragma unroll
-      for (int j = 0; j < NGK; ++j) {
-        float sj = (4 * lane) / GK == j ? s4 : 0.0f;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sj += __shfl_xor_sync(0xffffffffu, sj, off);
-        Qj[j] = sj;
-      }
-      // columns n = gid = (group j = gid/2, part = gid%2); zero for gid >= 2*NGK
-      const int jn = gid >> 1, part = gid & 1;
-#pragma unroll
-      for (int kb = 0; kb < 8; ++kb)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          int clo, chi, p;
-          key_pair<BITS>(tig, kb, r, clo, chi, p);
-          const float invf = inv * inv_pos_factor<BITS>(p);
-          const float vlo = (clo / GK == jn) ? qf(clo) * invf : 0.0f;
-          const float vhi = (chi / GK == jn) ? qf(chi) * invf : 0.0f;
-          uint32_t hi, lo;
-          split2(vlo, vhi, hi, lo);
-          bqi[kb][r] = gid < 2 * NGK ? (part ? lo : hi) : 0u;
-        }
-    }
-  };
-
-  // ---- per-warp online-softmax state ----------------------------------------
-  float m_run = -INFINITY, l_lane = 0.0f, z_lane[NGV];
-  float dv[8][4];
-  auto reset_state = [&]() {
-    m_run = -INFINITY;
-    l_lane = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NGV; ++j) z_lane[j] = 0.0f;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) dv[mt][r] = 0.0f;
-  };
-  reset_state();
-
-  // Warp state -> partial `slot` of head bh.  The quantized-token state
-  // (online softmax over MMA fragments; lanes hold one token each for l and
-  // z) and the fp16-token state (mf, lf, af: a lane owns channels 4*lane ..
-  // 4*lane + 3) are joined with the log-sum-exp rule; the quantized output
-  // row goes through the warp's operand area to reach the lane layout.
-  int pend_bh = -1;  // head this warp merges (slot 0), once it has published
-  auto flush = [&](int bh, int slot, float mf, float lf, const float (&af)[4]) -> bool {
-    float l = l_lane;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    float Z[NGV];
-#pragma unroll
-    for (int j = 0; j < NGV; ++j) {
-      float z = z_lane[j];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-      Z[j] = z;
-    }
-    float *so = reinterpret_cast<float *>(sBw);
-    const int gc = (gid * NGV) >> 3;  // value group of this thread's 16 channels
-    if (tig == gc) {
-      float zc = Z[0];
-#pragma unroll
-      for (int j = 1; j < NGV; ++j)
-        if (j == gc) zc = Z[j];
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const float invf = kSub * kSlackScale / pos_factor<BITS>(BITS == 2 ? mt : (mt & 3));
-        so[16 * gid + mt] = fmaf(dv[mt][0] + dv[mt][1], invf, zc);
-        so[16 * gid + 8 + mt] = fmaf(dv[mt][2] + dv[mt][3], invf, zc);
-      }
-    }
-    __syncwarp();
-    const float4 oq = reinterpret_cast<const float4 *>(so)[lane];
-    __syncwarp();
-    const float m = fmaxf(m_run, mf);
-    const float wq = m_run == -INFINITY ? 0.0f : exp2_approx(m_run - m);
-    const float wf = mf == -INFINITY ? 0.0f : exp2_approx(mf - m);
-    float4 o;
-    o.x = fmaf(oq.x, wq, af[0] * wf);
-    o.y = fmaf(oq.y, wq, af[1] * wf);
-    o.z = fmaf(oq.z, wq, af[2] * wf);
-    o.w = fmaf(oq.w, wq, af[3] * wf);
-    const float lt = fmaf(l, wq, lf * wf);
-    reset_state();
-    // a merge still owed (a head this warp held whole) comes first; the
-    // merge of the warp's last head waits until after the tile loop
-    if (pend_bh >= 0 && !merge_head<8>(a, pend_bh)) return false;
-    publish_partial(a, bh, slot, o, m, lt);
-    pend_bh = slot == 0 ? bh : -1;
-    return true;
-  };
-
-  int done = 0;          // items whose copies completed
-  int cs = 0;            // ring slot of the next item
-  uint32_t cph = 0;      // its barrier phase parity
-  // Waits for the next ring slot.  One verdict per warp: every lane takes
-  // the same path; false (status word set) on timeout.
-  auto wait_slot = [&](int &s_out) -> bool {
-    const int s = cs;
-    const uint32_t par = cph;
-    if (++cs == nslot) {
-      cs = 0;
-      cph ^= 1u;
-    }
-    const bool ok = bar_wait(wbars_s + 8 * s, par, a.wait_limit);
-    if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
-      return false;
-    }
-    ++done;
-    s_out = s;
-    return true;
-  };
-  bool aborted = false;
-  if (a.stall_limit > 0) {
-    // debug: the warp's first wait is on a barrier nothing completes
-    const bool ok = bar_wait(&wbars[nslot], 0u, a.stall_limit);
-    if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ETIMEOUT);
-      aborted = true;
-    }
-  }
-  for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
-    const Seg sg = warp_seg(a, bh, x0, x1);
-    const int tq0 = sg.tq0, tq1 = sg.tq1;
-    // fp16 sink + residual / window chunks of this warp's segment
-    const int nchk = sg.c1 - sg.c0;
-    const int base = bh * a.U;
-    if (tq1 > tq0) {
-      const int nt = (tq1 - tq0 + kTile - 1) / kTile;
-      for (int lt = 0; lt < nt; ++lt) {
-        int s;
-        if (!wait_slot(s)) {
-          aborted = true;
-          break;
-        }
-        const uint8_t *slot = wring + s * SLOT;
-        if (lt == 0) start_head(slot, bh);
-        const int tok0 = tq0 + kTile * lt;
-        const int n = min(kTile, tq1 - tok0);
-        auto tile = [&](auto full_c) {
-          constexpr bool FULL = decltype(full_c)::value;
-          const uint8_t *kc = slot;
-          const uint8_t *vc = slot + SC::off_vc;
-          // ------------- keys: two 16-token MMA tiles ------------------------
-          float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-          float bias0 = 0.0f, bias1 = 0.0f;
-          // key operand words of MMA k-block kb for key group gl (loaded next
-          // to their use to keep few registers live)
-          auto bk_at = [&](int gl, int kb) -> uint2 {
-            if (SCHEME == KVQ_KIVI) {
-              // lanes of columns >= 2 read the zero block: no divergent branch
-              const uint32_t *src = gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + SC::sb_zero;
-              return *reinterpret_cast<const uint2 *>(src + 2 * kb);
-            } else {
-              return make_uint2(bqi[kb][0], bqi[kb][1]);
-            }
-          };
-          bool two_groups = false;
-          if (SCHEME == KVQ_KIVI) {
-            // q~ = q * scale (normalised, position factor divided out) as fp16
-            // hi/lo in B-fragment order, and q . zero, per key group of the tile
-            const float *km = reinterpret_cast<const float *>(slot + SC::off_km);
-            two_groups = G16 && (FULL || n > 16);
-  #pragma unroll
-            for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
-              if (gl == 1 && !two_groups) break;
-              const float *ks = km + gl * 2 * kD, *kz = ks + kD;
-              const float2 s_lo = *reinterpret_cast<const float2 *>(ks + b_clo);
-              const float2 s_hi = *reinterpret_cast<const float2 *>(ks + b_clo + kHalf);
-              const float2 z_lo = *reinterpret_cast<const float2 *>(kz + b_clo);
-              const float2 z_hi = *reinterpret_cast<const float2 *>(kz + b_clo + kHalf);
-              uint32_t h0, l0, h1, l1;
-              split2(qn_lo[0] * s_lo.x, qn_hi[0] * s_hi.x, h0, l0);
-              split2(qn_lo[1] * s_lo.y, qn_hi[1] * s_hi.y, h1, l1);
-              *reinterpret_cast<uint2 *>(sBw + gl * 128 + b_sidx) = make_uint2(h0, h1);
-              *reinterpret_cast<uint2 *>(sBw + gl * 128 + 64 + b_sidx) = make_uint2(l0, l1);
-              float bz = fmaf(qf_lo[0], z_lo.x, fmaf(qf_hi[0], z_hi.x, fmaf(qf_lo[1], z_lo.y, qf_hi[1] * z_hi.y)));
-  #pragma unroll
-              for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
-              if (gl == 0) bias0 = bz;
-              bias1 = bz;
-            }
-            __syncwarp();
-          }
-          if (BITS == 2) {
-            const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
-            const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
-            const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
-            const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
-            if (!two_groups) {
-  #pragma unroll
-              for (int m = 0; m < 2; ++m) {
-                const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
-                const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
-                const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
-                const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
-  #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const uint2 b = bk_at(0, 4 * m + j);
-                  mma16816(d0, ext<2>(w00, s00, 2 * j), ext<2>(w01, s01, 2 * j),
-                           ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1), b.x, b.y);
-                  mma16816(d1, ext<2>(w10, s10, 2 * j), ext<2>(w11, s11, 2 * j),
-                           ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1), b.x, b.y);
-                }
-              }
-            } else {
-  #pragma unroll
-              for (int t2 = 0; t2 < 2; ++t2) {
-                const uint2 wa = t2 ? wa1 : wa0, wb = t2 ? wb1 : wb0;
-  #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                  const uint32_t w0 = m ? wa.y : wa.x, w1 = m ? wb.y : wb.x;
-                  const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
-  #pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const uint2 b = bk_at(t2, 4 * m + j);
-                    if (t2 == 0)
-                      mma16816(d0, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
-                    else
-                      mma16816(d1, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
-                  }
-                }
-              }
-            }
-          } else {
-            // 4-bit keys: G >= 32 always gives one key group per tile here
-            // (the 4-bit group-16 case takes the same path with two groups)
-  #pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2) {
-              const int gl = two_groups ? t2 : 0;
-              const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid) * RB + 16 * tig);
-              const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid + 8) * RB + 16 * tig);
-              const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
-  #pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
-  #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  const uint2 b = bk_at(gl, 2 * m + j);
-                  if (t2 == 0)
-                    mma16816(d0, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
-                  else
-                    mma16816(d1, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
-                }
-              }
-            }
-          }
-          // ------------- scores -> one token per lane ------------------------
-          float ra0, rb0, ra1, rb1;
-          if (SCHEME == KVQ_KIVI) {
-            ra0 = d0[0] + d0[1];
-            rb0 = d0[2] + d0[3];
-            ra1 = d1[0] + d1[1];
-            rb1 = d1[2] + d1[3];
-          } else {
-            const float *ks = reinterpret_cast<const float *>(slot + SC::off_ks);
-            const float *kz = reinterpret_cast<const float *>(slot + SC::off_kz);
-            const int jj = tig < NGK ? tig : NGK - 1;
-            float qj = Qj[0];
-  #pragma unroll
-            for (int j = 1; j < NGK; ++j)
-              if (j == jj) qj = Qj[j];
-            auto term = [&](int row, float dd) {
-              return fmaf(ks[row * NGK + jj], dd * pow2E, kz[row * NGK + jj] * qj);
-            };
-            ra0 = term(gid, d0[0] + d0[1]);
-            rb0 = term(gid + 8, d0[2] + d0[3]);
-            ra1 = term(gid + 16, d1[0] + d1[1]);
-            rb1 = term(gid + 24, d1[2] + d1[3]);
-            if (tig >= NGK) ra0 = rb0 = ra1 = rb1 = 0.0f;
-  #pragma unroll
-            for (int off = 1; off < NGK; off <<= 1) {
-              ra0 += __shfl_xor_sync(0xffffffffu, ra0, off);
-              rb0 += __shfl_xor_sync(0xffffffffu, rb0, off);
-              ra1 += __shfl_xor_sync(0xffffffffu, ra1, off);
-              rb1 += __shfl_xor_sync(0xffffffffu, rb1, off);
-            }
-          }
-          const int t = lane;
-          const int src = 4 * (t & 7);
-          const float xa0 = __shfl_sync(0xffffffffu, ra0, src), xb0 = __shfl_sync(0xffffffffu, rb0, src);
-          const float xa1 = __shfl_sync(0xffffffffu, ra1, src), xb1 = __shfl_sync(0xffffffffu, rb1, src);
-          float score = t < 16 ? ((t & 8) ? xb0 : xa0) : ((t & 8) ? xb1 : xa1);
-          if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
-          const bool valid = FULL || t < n;
-          score = valid ? score : -INFINITY;
-          // lazy rescaling: the reference m_run moves only when a score passes
-          // it by more than kSlack (one vote, no reduction on most tiles)
-          if (__any_sync(0xffffffffu, score > m_run + kSlack)) {
-            float mt_ = score;
-  #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
-            const float alpha = exp2_approx(m_run - mt_);
-            l_lane *= alpha;
-  #pragma unroll
-            for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
-  #pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-  #pragma unroll
-              for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
-            m_run = mt_;
-          }
-          const float p = exp2_approx(score - m_run);  // <= 2^kSlack
-          const float pv = p * kInvSlack;          // value operand scale: stays in fp16 range
-          l_lane += p;
-          {
-            const float *vz = reinterpret_cast<const float *>(slot + SC::off_vz) + t * NGV;
-            float zr[NGV];
-            if (NGV == 4) {
-              const float4 z4 = *reinterpret_cast<const float4 *>(vz);
-              zr[0] = z4.x;
-              zr[1] = z4.y;
-              zr[2 % NGV] = z4.z;
-              zr[3 % NGV] = z4.w;
-            } else {
-              const float2 z2 = *reinterpret_cast<const float2 *>(vz);
-              zr[0] = z2.x;
-              zr[1 % NGV] = z2.y;
-            }
-  #pragma unroll
-            for (int j = 0; j < NGV; ++j)
-              z_lane[j] = (FULL || p > 0.0f) ? fmaf(p, zr[j], z_lane[j]) : z_lane[j];
-          }
-          // ------------- values: B = p * scale (hi/lo), A = codes ------------
-          // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) of k-block kb carry
-          // tokens 16kb + tig + {0, 4} and + {8, 12} (code rows 4 apart hit
-          // distinct banks).  Each token's lane writes its operand row
-          // B[t][(j, hi/lo)] = p_t * scale_tj * 2^-8 as fp16 hi + lo into the
-          // warp's operand area (the key operand is consumed by now), laid out
-          // [column][kb][tig][4 tokens] so each lane then loads the fragment of
-          // a k-block with one 64-bit load.
-          {
-            const float *vsr = reinterpret_cast<const float *>(slot + SC::off_vs) + t * NGV;
-            float sv[NGV];
-            if (NGV == 4) {
-              const float4 s4 = *reinterpret_cast<const float4 *>(vsr);
-              sv[0] = s4.x;
-              sv[1] = s4.y;
-              sv[2 % NGV] = s4.z;
-              sv[3 % NGV] = s4.w;
-            } else {
-              const float2 s2 = *reinterpret_cast<const float2 *>(vsr);
-              sv[0] = s2.x;
-              sv[1 % NGV] = s2.y;
-            }
-            __syncwarp();  // every lane's key-operand loads are done
-            __half *orow = reinterpret_cast<__half *>(sBw) + 16 * (t >> 4) + 4 * (t & 3) + ((t & 15) >> 2);
-  #pragma unroll
-            for (int j = 0; j < NGV; ++j) {
-              const float x = valid ? pv * sv[j] : 0.0f;
-              const __half h = __float2half_rn(x);
-              orow[64 * j] = h;
-              orow[64 * j + 32] = __float2half_rn(x - __half2float(h));
-            }
-            __syncwarp();
-          }
-          const bool bact = gid < 2 * NGV;
-          const uint32_t *bsrc = sBw + 16 * gid + 2 * tig;
-          const int nkb = (FULL || n > 16) ? 2 : 1;
-          for (int kb = 0; kb < nkb; ++kb) {
-            const int tk0 = 16 * kb + tig, tk1 = tk0 + 4, tk2 = tk0 + 8, tk3 = tk0 + 12;
-            const uint2 bw = *reinterpret_cast<const uint2 *>(bsrc + 8 * kb);
-            const uint32_t bv0 = bact ? bw.x : 0u;
-            const uint32_t bv1 = bact ? bw.y : 0u;
-            if (BITS == 2) {
-              const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * gid);
-              const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * gid);
-              const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vc + tk2 * RB + 4 * gid);
-              const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vc + tk3 * RB + 4 * gid);
-              const uint32_t xa_ = __byte_perm(w0, w1, 0x5410), ya_ = __byte_perm(w0, w1, 0x7632);
-              const uint32_t xb_ = __byte_perm(w2, w3, 0x5410), yb_ = __byte_perm(w2, w3, 0x7632);
-              const uint32_t xas = shifted<2>(xa_), yas = shifted<2>(ya_);
-              const uint32_t xbs = shifted<2>(xb_), ybs = shifted<2>(yb_);
-  #pragma unroll
-              for (int mt = 0; mt < 8; ++mt)
-                mma16816(dv[mt], ext<2>(xa_, xas, mt), ext<2>(ya_, yas, mt), ext<2>(xb_, xbs, mt),
-                         ext<2>(yb_, ybs, mt), bv0, bv1);
-            } else {
-              const uint2 w0 = *reinterpret_cast<const uint2 *>(vc + tk0 * RB + 8 * gid);
-              const uint2 w1 = *reinterpret_cast<const uint2 *>(vc + tk1 * RB + 8 * gid);
-              const uint2 w2 = *reinterpret_cast<const uint2 *>(vc + tk2 * RB + 8 * gid);
-              const uint2 w3 = *reinterpret_cast<const uint2 *>(vc + tk3 * RB + 8 * gid);
-              // [0]: channels 16gid+0..3, [1]: +4..7, [2]: +8..11, [3]: +12..15
-              const uint32_t xa4[4] = {__byte_perm(w0.x, w1.x, 0x5410), __byte_perm(w0.x, w1.x, 0x7632),
-                                       __byte_perm(w0.y, w1.y, 0x5410), __byte_perm(w0.y, w1.y, 0x7632)};
-              const uint32_t xb4[4] = {__byte_perm(w2.x, w3.x, 0x5410), __byte_perm(w2.x, w3.x, 0x7632),
-                                       __byte_perm(w2.y, w3.y, 0x5410), __byte_perm(w2.y, w3.y, 0x7632)};
-              uint32_t sa4[4], sb4[4];
-  #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                sa4[i] = shifted<4>(xa4[i]);
-                sb4[i] = shifted<4>(xb4[i]);
-              }
-  #pragma unroll
-              for (int mt = 0; mt < 8; ++mt) {
-                const int lo = mt < 4 ? 0 : 1, hi = mt < 4 ? 2 : 3, pos = mt & 3;
-                mma16816(dv[mt], ext<4>(xa4[lo], sa4[lo], pos), ext<4>(xa4[hi], sa4[hi], pos),
-                         ext<4>(xb4[lo], sb4[lo], pos), ext<4>(xb4[hi], sb4[hi], pos), bv0, bv1);
-              }
-            }
-          }
-        };
-        if (n == kTile)
-          tile(std::true_type{});
-        else
-          tile(std::false_type{});
-        __syncwarp();
-        issue_next();  // refill the slot just consumed
-      }
-      if (aborted) break;
-    }
-    // fp16 chunks; a lane owns channels 4*lane .. 4*lane + 3.  A warp whose
-    // range holds only a head's empty unit still publishes (an empty
-    // partial): the head's partial count includes every warp it touches.
-    float mf = -INFINITY, lf = 0.0f, af[4] = {0.f, 0.f, 0.f, 0.f};
-    float pow2F = 1.0f;  // fp16 scores = MMA result * 2^F (q normalised by 2^-F)
-    {
-      for (int lt = 0; lt < nchk; ++lt) {
-        int s;
-        if (!wait_slot(s)) {
-          aborted = true;
-          break;
-        }
-        const uint8_t *slot = wring + s * SLOT;
-        if (lt == 0) {
-          const uint2 qr = reinterpret_cast<const uint2 *>(slot + SC::off_q)[lane];
-          const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
-          const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
-          q4[0] = q01.x * a.scale_log2;
-          q4[1] = q01.y * a.scale_log2;
-          q4[2] = q23.x * a.scale_log2;
-          q4[3] = q23.y * a.scale_log2;
-          // key-score operand of the fp16 rows: q / 2^F as fp16 hi/lo.  With
-          // channels 16kb + 4tig .. + 3 on k-pairs (2tig, 2tig+1), (2tig+8,
-          // 2tig+9) of k-block kb, lane L's own 4 channels are the B words of
-          // (kb, tig) = (L >> 2, L & 3).
-          float mx = fmaxf(fmaxf(fabsf(q4[0]), fabsf(q4[1])), fmaxf(fabsf(q4[2]), fabsf(q4[3])));
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-          int F = 0;
-          if (mx > 0.0f && mx < INFINITY) frexpf(mx, &F);
-          pow2F = ldexpf(1.0f, F);
-          const float inv = ldexpf(1.0f, -F);
-          uint32_t h0, l0, h1, l1;
-          split2(q4[0] * inv, q4[1] * inv, h0, l0);
-          split2(q4[2] * inv, q4[3] * inv, h1, l1);
-          __syncwarp();  // the quantized tiles' operand loads are done
-          *reinterpret_cast<uint2 *>(sBw + (lane & 3) * 16 + 2 * (lane >> 2)) = make_uint2(h0, h1);
-          *reinterpret_cast<uint2 *>(sBw + (4 + (lane & 3)) * 16 + 2 * (lane >> 2)) = make_uint2(l0, l1);
-          __syncwarp();
-        }
-        const int i0 = (sg.c0 + lt) * CH;
-        const int nv = min(CH, (int)a.n_fp16 - i0);  // valid rows of the chunk
-        if (a.new_row >= 0) {
-          // fused append: the warp holding the new token stores it in the residual
-          const int tn = (int)a.n_sink + a.new_row - i0;
-          if (tn >= 0 && tn < nv) {
-            const int half = lane >> 4, j = lane & 15;
-            const uint4 v4 = reinterpret_cast<const uint4 *>(slot + half * CH * kD * 2 + tn * kD * 2)[j];
-            __half *dstrow = (half ? a.p.v_res : a.p.k_res) + ((int64_t)bh * g.residual + a.new_row) * kD;
-            reinterpret_cast<uint4 *>(dstrow)[j] = v4;
-          }
-        }
-        const uint2 *vr = reinterpret_cast<const uint2 *>(slot + CH * kD * 2);
-        // scores on the tensor cores: A = the chunk's K rows (token rows 0..7;
-        // rows 8..15 zero), B = the query operand; rows past the chunk's valid
-        // ones are masked below.  Lane (gid, 0) ends with token gid's score.
-        float sp;
-        {
-          const uint2 *ka = reinterpret_cast<const uint2 *>(slot + gid * kD * 2) + tig;
-          const uint32_t *bq = gid < 2 ? sBw + (gid * 4 + tig) * 16 : sBw + SC::sb_zero;
-          float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int kb = 0; kb < 8; ++kb) {
-            const uint2 av = ka[4 * kb];
-            const uint2 bv = *reinterpret_cast<const uint2 *>(bq + 2 * kb);
-            mma16816((kb & 1) ? e1 : e0, av.x, 0u, av.y, 0u, bv.x, bv.y);
-          }
-          sp = __shfl_sync(0xffffffffu, (e0[0] + e0[1]) + (e1[0] + e1[1]), lane & ~3) * pow2F;
-        }
-        const int row = gid;
-        const float sc = row < nv ? sp : -INFINITY;
-        float mc = sc;
-        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 4));
-        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 8));
-        mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, 16));
-        const float mn = fmaxf(mf, mc);
-        const float al = exp2_approx(mf - mn);
-        const float pr = exp2_approx(sc - mn);  // 0 for rows past the chunk's end
-        float ps_ = pr;
-        ps_ += __shfl_xor_sync(0xffffffffu, ps_, 4);
-        ps_ += __shfl_xor_sync(0xffffffffu, ps_, 8);
-        ps_ += __shfl_xor_sync(0xffffffffu, ps_, 16);
-        lf = fmaf(lf, al, ps_);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) af[i] *= al;
-        mf = mn;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (t < CH && t < nv) {
-            // row t's probability sits in lanes whose bits 4,3,2 spell t
-            const float pt = __shfl_sync(0xffffffffu, pr, ((t >> 2) << 4) | (((t >> 1) & 1) << 3) | ((t & 1) << 2));
-            const uint2 vw = vr[t * (kD / 4) + lane];
-            const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
-            const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
-            af[0] = fmaf(pt, v01.x, af[0]);
-            af[1] = fmaf(pt, v01.y, af[1]);
-            af[2] = fmaf(pt, v23.x, af[2]);
-            af[3] = fmaf(pt, v23.y, af[3]);
-          }
-        }
-        __syncwarp();
-        issue_next();
-      }
-      if (aborted) break;
-    }
-    if (!flush(bh, gw - owner_of(base, a.total, a.nw), mf, lf, af)) {
-      aborted = true;
-      break;
-    }
-  }
-  if (!aborted && pend_bh >= 0 && !merge_head<24>(a, pend_bh)) aborted = true;
-  if (aborted) {
-    // give up this warp's work; its copies complete first
-    if (lane == 0)
-      for (int i = done; i < issued; ++i)
-        bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
-  }
-}
-
-template <int BITS, int SCHEME, int NGV, int NGK, int KM>
-cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
-  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM>;
-  constexpr int smem = SlotCfg<BITS, SCHEME, NGV, NGK, KM>::smem;
-  if (a.g.block_bytes != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::BB ||
-      tc_fp16_chunk(a.g) != SlotCfg<BITS, SCHEME, NGV, NGK, KM>::CH)
-    return cudaErrorInvalidValue;
-  static KernelSetup setup;
-  int occ = 0;
-  const cudaError_t e = kernel_setup(setup, kern, kThreads, smem, &occ);
-  if (e != cudaSuccess) return e;
-  int64_t nc = (int64_t)num_sms * occ;
-  if (nc > kTcMaxBlocks) nc = kTcMaxBlocks;
-  // every working warp gets at least one unit
-  int64_t nw = nc * kWarps;
-  if (nw > a.total) nw = a.total;
-  if (nw < 1) nw = 1;
-  nc = (nw + kWarps - 1) / kWarps;
-  a.nc = (int)nc;
-  a.nw = (int)nw;
-  // every block must be resident: the merging warps wait for other blocks
-  if (nc > (int64_t)num_sms * occ) return cudaErrorCooperativeLaunchTooLarge;
-  const cudaError_t le = launch_cooperative(kern, (unsigned)nc, kThreads, smem, st, a);
-  return le != cudaSuccess ? le : cudaGetLastError();
-}
-
-// The template arguments the dispatch picks for a geometry (one function, so
-// the launch and kvq_decode_kernel_name cannot disagree).
-struct TcVariant {
-  int ngv, ngk, km;
-};
-TcVariant tc_variant(const Geometry &g) {
-  TcVariant v{kD / g.v_group, 1, 0};
-  if (g.scheme == KVQ_KIVI)
-    v.km = g.k_group == 16 ? 2 : g.k_group == 32 ? 1 : 0;
-  else
-    v.ngk = kD / g.k_group;
-  return v;
-}
-
-template <int BITS, int SCHEME>
-cudaError_t launch_tc_v(TcArgs &a, int num_sms, cudaStream_t st) {
-  const TcVariant v = tc_variant(a.g);
-  if constexpr (SCHEME == KVQ_KIVI) {
-    if (v.ngv == 4)
-      return v.km == 2 ? launch_tc_t<BITS, SCHEME, 4, 1, 2>(a, num_sms, st)
-           : v.km == 1 ? launch_tc_t<BITS, SCHEME, 4, 1, 1>(a, num_sms, st)
-                       : launch_tc_t<BITS, SCHEME, 4, 1, 0>(a, num_sms, st);
-    return v.km == 2 ? launch_tc_t<BITS, SCHEME, 2, 1, 2>(a, num_sms, st)
-         : v.km == 1 ? launch_tc_t<BITS, SCHEME, 2, 1, 1>(a, num_sms, st)
-                     : launch_tc_t<BITS, SCHEME, 2, 1, 0>(a, num_sms, st);
-  } else {
-    if (v.ngv == 4)
-      return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, 0>(a, num_sms, st)
-                        : launch_tc_t<BITS, SCHEME, 4, 2, 0>(a, num_sms, st);
-    return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, 0>(a, num_sms, st)
-                      : launch_tc_t<BITS, SCHEME, 2, 2, 0>(a, num_sms, st);
-  }
-}
 
 int g_stall_limit = 0;
 
@@ -873,13 +54,13 @@ int debug_stall_limit() { return g_stall_limit; }
 
 int tc_variant_name(const Geometry &g, char *buf, size_t len) {
   const TcVariant v = tc_variant(g);
-  return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d>", g.bits,
-                  g.scheme == KVQ_KIVI ? "kivi" : "innerq", v.ngv, v.ngk, v.km);
+  return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d,mf=%d>",
+                  g.bits, g.scheme == KVQ_KIVI ? "kivi" : "innerq", v.ngv, v.ngk, v.km, g.meta16);
 }
 
 bool tc_decode_supported(const Geometry &g) {
   if (g.d != kD || g.Hq != g.H) return false;
-  if (g.meta16 || g.vq || g.n_out || g.ragged) return false;
+  if (g.vq || g.n_out || g.ragged) return false;
   const int ngv = kD / g.v_group;
   if (ngv != 2 && ngv != 4) return false;
   if (g.scheme == KVQ_KIVI) return g.k_group >= 16 && g.k_group <= 128;
@@ -928,11 +109,7 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * 2;
   a.wait_limit = 1 << 24;
   a.stall_limit = g_stall_limit;
-  if (g.bits == 2)
-    return g.scheme == KVQ_KIVI ? launch_tc_v<2, KVQ_KIVI>(a, num_sms, st)
-                                : launch_tc_v<2, KVQ_INNERQ>(a, num_sms, st);
-  return g.scheme == KVQ_KIVI ? launch_tc_v<4, KVQ_KIVI>(a, num_sms, st)
-                              : launch_tc_v<4, KVQ_INNERQ>(a, num_sms, st);
+  return g.meta16 ? launch_tc_f16(a, num_sms, st) : launch_tc_mf<0>(a, num_sms, st);
 }
 
 }  // namespace kvq

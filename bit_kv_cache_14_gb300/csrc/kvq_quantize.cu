@@ -25,7 +25,6 @@ namespace kvq {
 namespace {
 
 constexpr int kQuantBlock = 256;
-constexpr int kMaxOutliers = 8;
 
 __device__ __forceinline__ void load8(const __half *p, float (&x)[8]) {
   const uint4 raw = *reinterpret_cast<const uint4 *>(p);

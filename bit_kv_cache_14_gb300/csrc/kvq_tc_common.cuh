@@ -13,22 +13,8 @@
 
 namespace kvq {
 
-namespace {
-
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnit = 128;    // tokens per stream-K work unit (grouped-query kernel)
-constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
-constexpr int kD = 128;
-constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
-// Lazy online softmax: probabilities are taken against a running reference
-// that may sit up to kSlack (log2 units) below the true maximum, so p <= 2^8;
-// the value operand carries p * 2^-8 and the output row multiplies it back.
-constexpr float kSlack = 8.0f;
-constexpr float kSlackScale = 256.0f;
-constexpr float kInvSlack = 1.0f / 256.0f;
-constexpr int kDrainLimit = 1 << 26;
-
+// Launch arguments of the tensor-core decode kernels (one definition for
+// every translation unit that launches them).
 struct TcArgs {
   Geometry g;
   CachePtrs p;
@@ -53,6 +39,28 @@ struct TcArgs {
   int stall_limit;  // debug: > 0 = first wait on a barrier nothing completes
 };
 
+// The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), built in
+// its own translation unit.
+cudaError_t launch_tc_f16(TcArgs &a, int num_sms, cudaStream_t st);
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnit = 128;    // tokens per stream-K work unit (grouped-query kernel)
+constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
+constexpr int kD = 128;
+constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
+// Lazy online softmax: probabilities are taken against a running reference
+// that may sit up to kSlack (log2 units) below the true maximum, so p <= 2^8;
+// the value operand carries p * 2^-8 and the output row multiplies it back.
+constexpr float kSlack = 8.0f;
+constexpr float kSlackScale = 256.0f;
+constexpr float kInvSlack = 1.0f / 256.0f;
+constexpr int kDrainLimit = 1 << 26;
+
+
+
 struct TcLayout {
   int ring, sB, bars, total;
 };
@@ -75,18 +83,20 @@ __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int 
 // transpose the output row at a head's end, and 64 bytes that stay zero.
 // KM (KIVI): 2 = G 16, two key groups per tile, statistics inside the block;
 // 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
-// from the separate key-statistics array.
-template <int BITS, int SCHEME, int NGV, int NGK, int KM>
+// from the separate key-statistics array.  MF: statistics stored in fp16
+// (MSZ = 2 bytes each) instead of fp32.
+template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF = 0>
 struct SlotCfg {
+  static constexpr int MSZ = MF ? 2 : 4;
   static constexpr int RB = kD * BITS / 8;
   static constexpr int off_vc = kTile * RB;
   static constexpr int off_vs = 2 * kTile * RB;
-  static constexpr int off_vz = off_vs + kTile * NGV * 4;
-  static constexpr int off_ks = off_vz + kTile * NGV * 4;  // InnerQ
-  static constexpr int off_kz = off_ks + kTile * NGK * 4;  // InnerQ
+  static constexpr int off_vz = off_vs + kTile * NGV * MSZ;
+  static constexpr int off_ks = off_vz + kTile * NGV * MSZ;  // InnerQ
+  static constexpr int off_kz = off_ks + kTile * NGK * MSZ;  // InnerQ
   static constexpr bool KIN = SCHEME == KVQ_KIVI && KM >= 1;
-  static constexpr int KGB = (KM == 2 ? 2 : 1) * 2 * kD * 4;  // KIVI key statistics of a tile
-  static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks + (KIN ? KGB : 0) : off_kz + kTile * NGK * 4;
+  static constexpr int KGB = (KM == 2 ? 2 : 1) * 2 * kD * MSZ;  // KIVI key statistics of a tile
+  static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks + (KIN ? KGB : 0) : off_kz + kTile * NGK * MSZ;
   static constexpr int KMB = SCHEME == KVQ_KIVI && !KIN ? KGB : 0;  // separate copy
   static constexpr int off_km = KIN ? off_ks : BB;
   static constexpr int off_q = BB + KMB;
@@ -100,6 +110,47 @@ struct SlotCfg {
   static constexpr int smem = tc_layout(bytes, nslot, SBB).total;
 };
 
+// Stored statistics as fp32: element i of a row at `base`, the pair (i, i +
+// 1) (i even), and N consecutive values (a per-token row of N groups).
+template <int MF>
+__device__ __forceinline__ float ld_stat(const uint8_t *base, int i) {
+  if (MF) return __half2float(reinterpret_cast<const __half *>(base)[i]);
+  return reinterpret_cast<const float *>(base)[i];
+}
+template <int MF>
+__device__ __forceinline__ float2 ld_stat2(const uint8_t *base, int i) {
+  if (MF) return __half22float2(reinterpret_cast<const __half2 *>(base)[i >> 1]);
+  return reinterpret_cast<const float2 *>(base)[i >> 1];
+}
+template <int MF, int N>
+__device__ __forceinline__ void ld_stat_row(const uint8_t *base, float (&out)[N]) {
+  static_assert(N == 2 || N == 4, "rows of 2 or 4 groups");
+  if (MF) {
+    if (N == 4) {
+      const uint2 w = *reinterpret_cast<const uint2 *>(base);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+      out[0] = a.x;
+      out[1] = a.y;
+      out[2 % N] = b.x;
+      out[3 % N] = b.y;
+    } else {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(base));
+      out[0] = a.x;
+      out[1 % N] = a.y;
+    }
+  } else if (N == 4) {
+    const float4 a = *reinterpret_cast<const float4 *>(base);
+    out[0] = a.x;
+    out[1] = a.y;
+    out[2 % N] = a.z;
+    out[3 % N] = a.w;
+  } else {
+    const float2 a = *reinterpret_cast<const float2 *>(base);
+    out[0] = a.x;
+    out[1 % N] = a.y;
+  }
+}
 
 // ---- PTX helpers --------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -34,7 +34,8 @@ def _fake_gpu(args, w, rank, world):
 def line(monkeypatch):
     monkeypatch.setattr(bench, "run_gpu", _fake_gpu)
     monkeypatch.setattr(bench, "run_configs",
-                        lambda names, peak: {n: {"us": 1.0, "frac": 0.5} for n in names})
+                        lambda names, peak, base=None: {n: {"us": 1.0, "frac": 0.5}
+                                                        for n in names})
     real = bench.max_over_ranks
     monkeypatch.setattr(bench, "max_over_ranks", lambda v, world, device: real(v, world, "cpu"))
 
@@ -52,6 +53,25 @@ def line(monkeypatch):
 REQUIRED = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
             "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "roofline",
             "e2e", "gpu_launches", "clocks")
+
+
+def test_decode_bytes_match_the_layout_arithmetic():
+    """Bytes per decode (the roofline's numerator) for the Llama layer: 128 B
+    per quantized token-head (64 of codes, 64 of fp32 statistics), 96 with
+    fp16 statistics, + 16 with two outliers per token and tensor, 512 per fp16
+    token-head; the value queue keeps up to R - 1 values fp16 (256 B each
+    instead of 64); ragged sequences each count their own tokens."""
+    w = bench.synth.WORKLOADS["llama2_7b_2bit"]
+    S = bench.synth.scaled
+    assert bench.decode_bytes(w, 4096, 1, 0) == BYTES
+    assert bench.decode_bytes(S(w, meta_f16=True), 4096, 1, 0) == 256 * (4096 * 96 + 512)
+    assert bench.decode_bytes(S(w, outliers=2), 4096, 1, 0) == 256 * (4096 * 144 + 512)
+    vq = S(w, v_queue=True)
+    # 4097 tokens, R = 128: values of tokens 3970 .. 4096 (127) still fp16
+    assert bench.decode_bytes(vq, 4096, 1, 0) == 256 * (4096 * 64 + 3970 * 64 + 256 + 127 * 256)
+    rg = S(w, ragged=True)
+    assert bench.decode_bytes_ragged(rg, [4097] * 8) == BYTES
+    assert bench.decode_bytes_ragged(rg, [0] * 8) == 0
 
 
 @pytest.mark.parametrize("rope", [False, True])
@@ -85,5 +105,7 @@ def test_gpu_line_contract(line, rope):
     else:
         # the other named workloads, each with its own decode-kernel line
         assert sorted(d["configs"]) == ["gqa_2bit", "innerq_1m", "kivi_4bit", "tiny"]
+        # and each cache-format option on the headline layer
+        assert sorted(d["formats"]) == ["meta_f16", "outliers_2", "ragged", "value_queue"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]

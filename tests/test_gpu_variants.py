@@ -22,16 +22,16 @@ W = synth.WORKLOADS
 S = synth.scaled
 
 
-def _kivi(bits, ngv, G):
+def _kivi(bits, ngv, G, mf=False):
     base = W["llama2_7b_2bit"] if bits == 2 else W["kivi_4bit"]
     R = 64 if G <= 64 else 128
     return S(base, batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, k_group=G, v_group=128 // ngv,
-             residual=R, n_append=R + 10)
+             residual=R, n_append=R + 10, meta_f16=mf)
 
 
-def _innerq(bits, ngv, ngk):
+def _innerq(bits, ngv, ngk, mf=False):
     return S(W["innerq_1m"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, bits=bits,
-             k_group=128 // ngk, v_group=128 // ngv, n_append=40)
+             k_group=128 // ngk, v_group=128 // ngv, n_append=40, meta_f16=mf)
 
 
 def _gqa(ngv, G, rg):
@@ -40,10 +40,12 @@ def _gqa(ngv, G, rg):
 
 
 CASES = {}
-for bits, ngv, G in itertools.product((2, 4), (2, 4), (16, 32, 64)):
-    CASES["tc_kivi_b%d_ngv%d_g%d" % (bits, ngv, G)] = _kivi(bits, ngv, G)
-for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
-    CASES["tc_innerq_b%d_ngv%d_ngk%d" % (bits, ngv, ngk)] = _innerq(bits, ngv, ngk)
+for mf in (False, True):
+    sfx = "_f16" if mf else ""
+    for bits, ngv, G in itertools.product((2, 4), (2, 4), (16, 32, 64)):
+        CASES["tc_kivi_b%d_ngv%d_g%d%s" % (bits, ngv, G, sfx)] = _kivi(bits, ngv, G, mf)
+    for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
+        CASES["tc_innerq_b%d_ngv%d_ngk%d%s" % (bits, ngv, ngk, sfx)] = _innerq(bits, ngv, ngk, mf)
 for ngv, G, rg in itertools.product((2, 4), (32, 64), (2, 4)):
     CASES["gqa_ngv%d_g%d_rg%d" % (ngv, G, rg)] = _gqa(ngv, G, rg)
 
@@ -65,10 +67,13 @@ def dispatched_tensor_core_names():
                                                  (16, 32, 64, 128), (16, 32, 64, 128)):
         if gv > d:
             continue
-        cfgs = [kvq.make_config(2, 2 * rg, 2, d, bits, kvq.KIVI, gk, gv, 128, 0, 4096)]
-        if gk <= d:
-            cfgs += [kvq.make_config(2, 2 * rg, 2, d, bits, s, gk, gv, 32, 4, 4096)
-                     for s in (kvq.INNERQ, kvq.INNERQ_KNORM)]
+        cfgs = []
+        for fl in (0, kvq.META_F16):
+            cfgs.append(kvq.make_config(2, 2 * rg, 2, d, bits, kvq.KIVI, gk, gv, 128, 0, 4096,
+                                        fl))
+            if gk <= d:
+                cfgs += [kvq.make_config(2, 2 * rg, 2, d, bits, s, gk, gv, 32, 4, 4096, fl)
+                         for s in (kvq.INNERQ, kvq.INNERQ_KNORM)]
         for cfg in cfgs:
             name = kvq.decode_kernel_name(cfg, 1)
             if name.startswith("tc_"):
@@ -78,7 +83,8 @@ def dispatched_tensor_core_names():
 
 def test_every_dispatched_instantiation_has_a_parity_case():
     dispatched = dispatched_tensor_core_names()
-    assert len(dispatched) == 20 + 8, sorted(dispatched)
+    # MHA: 20 shapes with fp32 and with fp16 statistics; grouped-query: 8
+    assert len(dispatched) == 2 * 20 + 8, sorted(dispatched)
     covered = {_name(w) for w in CASES.values()}
     assert dispatched <= covered, sorted(dispatched - covered)
     # and each named case reaches the instantiation its name says
