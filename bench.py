@@ -366,6 +366,7 @@ def run_gpu(args, w, rank, world):
     cfg = kvq.config_of(w, max_ctx)
     K, V = synth.prompt(w)
     Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
+    torch.cuda.synchronize(dev)  # (copied on the default stream; the prefill uses `stream`)
     del K, V
     prompt_bytes_in = 2 * Kd.numel() * 2
 
@@ -631,6 +632,8 @@ def prompt_on_device(w, dev):
 
     with ThreadPoolExecutor(max(1, min(16, len(os.sched_getaffinity(0))))) as ex:
         list(ex.map(one, range(w.batch * w.n_kv_heads)))
+    # the copies ran on the default stream; the prefill runs on another one
+    torch.cuda.synchronize(dev)
     return Kd, Vd
 
 

@@ -325,6 +325,42 @@ __device__ __forceinline__ uint32_t sym_code(float x, float scale, int bits) {
   return (uint32_t)((int)r + half);
 }
 
+// The same codes with one reciprocal per group instead of one division per
+// element, and bit for bit the same: the product d * rn(1 / scale) differs
+// from the IEEE quotient rn(d / scale) by at most 3 * 2^-24 of its magnitude
+// (three roundings), under 2^-16 while |d / scale| < 64, so rint gives the
+// same integer for both unless the product lies within kTieGuard (2^-12) of a
+// half-integer; there -- and for a quotient out of that range -- the IEEE
+// division decides.
+constexpr float kTieGuard = 1.0f / 4096.0f;
+__device__ __forceinline__ float rint_quotient(float d, float scale, float inv) {
+  const float r = __fmul_rn(d, inv);
+  const float f = __fsub_rn(r, floorf(r));
+  if (!(fabsf(r) < 64.0f) || fabsf(__fsub_rn(f, 0.5f)) < kTieGuard)
+    return rintf(__fdiv_rn(d, scale));
+  return rintf(r);
+}
+__device__ __forceinline__ uint32_t asym_code_inv(float x, float mn, float scale, float inv,
+                                                  int bits) {
+  if (scale == 0.0f) return 0u;
+  float r = rint_quotient(__fsub_rn(x, mn), scale, inv);
+  r = fminf(fmaxf(r, 0.0f), (float)((1 << bits) - 1));
+  return (uint32_t)r;
+}
+// Symmetric (a scale of 0, possible only for fp16 statistics, gives q = 0).
+__device__ __forceinline__ uint32_t sym_code_inv(float x, float scale, float inv, int bits) {
+  const int half = 1 << (bits - 1);
+  if (scale == 0.0f) return (uint32_t)half;
+  const float lim = (float)(half - 1);
+  float r = rint_quotient(x, scale, inv);
+  r = fminf(fmaxf(r, -lim), lim);
+  return (uint32_t)((int)r + half);
+}
+// rn(1 / scale), 0 for a zero scale (then no code uses it).
+__device__ __forceinline__ float recip_or_zero(float scale) {
+  return scale == 0.0f ? 0.0f : __fdiv_rn(1.0f, scale);
+}
+
 // InnerQ mode rule: symmetric iff not constant and |max + min| <= (max - min)/(2^b - 1).
 __device__ __forceinline__ bool choose_symmetric(float mn, float mx, int bits) {
   if (mx == mn) return false;

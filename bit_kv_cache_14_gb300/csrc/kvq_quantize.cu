@@ -69,9 +69,72 @@ __device__ __forceinline__ Stats sym_stats(float mn, float mx, int bits, bool f1
   return Stats{s, __fmul_rn(-(float)(1 << (bits - 1)), s)};
 }
 
-// Symmetric code; a scale of 0 (an fp16 scale that rounded to zero) gives q = 0.
-__device__ __forceinline__ uint32_t sym_code_z(float x, float scale, int bits) {
-  return scale == 0.0f ? (uint32_t)(1 << (bits - 1)) : sym_code(x, scale, bits);
+// ---- codes of 8 elements ---------------------------------------------------
+// The product r = d * rn(1 / scale) is rounded to an integer by adding 1.5 *
+// 2^23 (round to nearest even, |r| < 2^22), clamped in that domain and read
+// from the low mantissa bits: about ten instructions an element.  A lane whose
+// product lies within kTieGuard of a half-integer for any element (rare; or a
+// product out of range) redoes its 8 codes with asym_code_inv / sym_code_inv,
+// where the IEEE quotient decides: the codes are exactly those of the formula.
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kMagicBits = 0x4B400000;
+
+__device__ __forceinline__ float magic_round(float r, bool &tie) {
+  const float m = __fadd_rn(r, kMagic);
+  tie |= !(fabsf(__fsub_rn(r, __fsub_rn(m, kMagic))) < 0.5f - kTieGuard);
+  return m;
+}
+
+// Asymmetric codes; z / s / inv hold one value per element (PER, the KIVI
+// key channels) or one for all 8 (a per-token group).  om: outliers, code 0.
+template <int BITS, bool PER>
+__device__ __forceinline__ uint32_t pack_asym(const float (&x)[8], uint32_t om, const float *z,
+                                              const float *s, const float *inv) {
+  constexpr float top = (float)((1 << BITS) - 1);
+  bool tie = false;
+  uint32_t w = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int i = PER ? e : 0;
+    bool te = false;
+    const float m = magic_round(__fmul_rn(__fsub_rn(x[e], z[i]), inv[i]), te);
+    const float mc = fminf(fmaxf(m, kMagic), kMagic + top);
+    const uint32_t c = (uint32_t)(__float_as_int(mc) - kMagicBits);
+    if (!((om >> e) & 1u)) {  // (an outlier's product does not count)
+      w |= c << (e * BITS);
+      tie |= te;
+    }
+  }
+  if (tie) {
+    w = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = PER ? e : 0;
+      if (!((om >> e) & 1u)) w |= asym_code_inv(x[e], z[i], s[i], inv[i], BITS) << (e * BITS);
+    }
+  }
+  return w;
+}
+
+// Symmetric codes of one group: q + 2^(b-1), q = clamp(rint(x / scale)).
+template <int BITS>
+__device__ __forceinline__ uint32_t pack_sym(const float (&x)[8], float s, float inv) {
+  constexpr int half = 1 << (BITS - 1);
+  constexpr float lim = (float)(half - 1);
+  bool tie = false;
+  uint32_t w = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float m = magic_round(__fmul_rn(x[e], inv), tie);
+    const float mc = fminf(fmaxf(m, kMagic - lim), kMagic + lim);
+    w |= (uint32_t)(__float_as_int(mc) - kMagicBits + half) << (e * BITS);
+  }
+  if (tie) {
+    w = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w |= sym_code_inv(x[e], s, inv, BITS) << (e * BITS);
+  }
+  return w;
 }
 
 // ---- dense-and-sparse outliers ---------------------------------------------
@@ -138,7 +201,8 @@ constexpr int kMaskBytes = 128 * 16;  // G <= 128 rows, d / 8 <= 16 chunks
 // its list, and skipped by the statistics (code 0 at their positions).
 __device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int64_t bh,
                                       const __half *src, int64_t t0, float *s_scale,
-                                      float *s_mn, float *s_pmn, float *s_pmx, uint8_t *s_om) {
+                                      float *s_mn, float *s_inv, float *s_pmn, float *s_pmx,
+                                      uint8_t *s_om) {
   const int d = g.d, G = g.k_group;
   const int chunks = d / 8, lanes = blockDim.x / chunks;
   const int j = threadIdx.x % chunks, r0 = threadIdx.x / chunks;
@@ -201,6 +265,7 @@ __device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int
     }
     s_scale[c] = st.scale;
     s_mn[c] = st.zero;
+    s_inv[c] = recip_or_zero(st.scale);
     uint8_t *km = kivi_key_meta(g, p, bh, t0 / G);
     st_meta(g, km, c, st.scale);
     st_meta(g, km + d * g.msz, c, st.zero);
@@ -211,12 +276,10 @@ __device__ void key_group_per_channel(const Geometry &g, const CachePtrs &p, int
     float x[8];
     load8(src + (int64_t)i * d + 8 * jj, x);
     const uint32_t om = g.n_out > 0 ? s_om[it] : 0u;
-    uint32_t w = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int c = 8 * jj + k;
-      if (!((om >> k) & 1u)) w |= asym_code(x[k], s_mn[c], s_scale[c], g.bits) << (k * g.bits);
-    }
+    const int c0 = 8 * jj;
+    const uint32_t w =
+        g.bits == 2 ? pack_asym<2, true>(x, om, s_mn + c0, s_scale + c0, s_inv + c0)
+                    : pack_asym<4, true>(x, om, s_mn + c0, s_scale + c0, s_inv + c0);
     store_chunk(code_row(g, p, bh, t0 + i, 0), jj, w, g.bits);
   }
   __syncthreads();
@@ -287,12 +350,14 @@ struct ChunkQ {
 
 // Per-token group quantization of the 8 values x of this lane; the group is
 // `lanes` consecutive, aligned lanes (lanes = group / 8, a power of two <= 16;
-// it may differ between lanes of a warp).  Every lane of the warp must call it:
-// the butterfly always runs its four full-mask rounds and each lane only
-// combines the rounds inside its own group.  om: this lane's outliers (they
-// take no part in the statistics and store code 0); a group left without an
-// element stores scale 0 and zero 0.
-__device__ __forceinline__ ChunkQ quant_chunk(const float (&x)[8], int lanes, int bits,
+// it may differ between lanes of a warp).  Every lane of the warp must call it
+// with the same `rounds` (a power of two >= every calling lane's `lanes`): the
+// butterfly runs its full-mask rounds up to it and each lane only combines the
+// rounds inside its own group.  om: this lane's outliers (they take no part in
+// the statistics and store code 0); a group left without an element stores
+// scale 0 and zero 0.
+template <int BITS>
+__device__ __forceinline__ ChunkQ quant_chunk(const float (&x)[8], int lanes, int rounds,
                                               bool allow_sym, bool f16, uint32_t om) {
   float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
@@ -301,8 +366,7 @@ __device__ __forceinline__ ChunkQ quant_chunk(const float (&x)[8], int lanes, in
     mn = fminf(mn, x[k]);
     mx = fmaxf(mx, x[k]);
   }
-#pragma unroll
-  for (int off = 1; off < 16; off <<= 1) {
+  for (int off = 1; off < rounds; off <<= 1) {
     const float omn = __shfl_xor_sync(0xffffffffu, mn, off);
     const float omx = __shfl_xor_sync(0xffffffffu, mx, off);
     if (off < lanes) {
@@ -319,22 +383,21 @@ __device__ __forceinline__ ChunkQ quant_chunk(const float (&x)[8], int lanes, in
   }
   mn = canon_zero(mn);
   mx = canon_zero(mx);
-  r.sym = allow_sym && choose_symmetric(mn, mx, bits);
-  if (r.sym) {
-    const Stats st = sym_stats(mn, mx, bits, f16);
-    r.scale = st.scale;
-    r.zero = st.zero;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) r.codes |= sym_code_z(x[k], r.scale, bits) << (k * bits);
-  } else {
-    const Stats st = asym_stats(mn, mx, bits, f16);
-    r.scale = st.scale;
-    r.zero = st.zero;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (!((om >> k) & 1u)) r.codes |= asym_code(x[k], r.zero, r.scale, bits) << (k * bits);
-  }
+  r.sym = allow_sym && choose_symmetric(mn, mx, BITS);
+  const Stats st = r.sym ? sym_stats(mn, mx, BITS, f16) : asym_stats(mn, mx, BITS, f16);
+  r.scale = st.scale;
+  r.zero = st.zero;
+  const float inv = recip_or_zero(r.scale);
+  r.codes = r.sym ? pack_sym<BITS>(x, r.scale, inv)
+                  : pack_asym<BITS, false>(x, om, &r.zero, &r.scale, &inv);
   return r;
+}
+
+// quant_chunk for a width known only at run time.
+__device__ __forceinline__ ChunkQ quant_chunk_b(const float (&x)[8], int lanes, int rounds,
+                                                int bits, bool allow_sym, bool f16, uint32_t om) {
+  return bits == 2 ? quant_chunk<2>(x, lanes, rounds, allow_sym, f16, om)
+                   : quant_chunk<4>(x, lanes, rounds, allow_sym, f16, om);
 }
 
 // Where one per-token quantization writes: block offsets of the code rows
@@ -379,103 +442,314 @@ __device__ __forceinline__ void quant_value_token(const Geometry &g, const Cache
                    valid);
   }
   const int lanes = g.v_group / 8;
-  const ChunkQ q = quant_chunk(x, lanes, g.bits, false, g.meta16, om);
+  const ChunkQ q = quant_chunk_b(x, lanes, lanes, g.bits, false, g.meta16, om);
   if (valid) store_token(g, p, dst, bh, t, j, lanes, q);
 }
 
-// Prefill, per-token groups: the quantized tokens of every head of X
-// [B*H][T][d] (InnerQ keys and values from row n_sink on; KIVI values from
-// row 0, the first n_vq of them) into slots [0, n).  blockIdx.y = head,
-// blockIdx.z = 0 keys / 1 values (keys only under InnerQ).  A block takes
-// kTokIter rounds of kQuantBlock / (d/8) tokens.
-constexpr int kTokIter = 4;
+// ---- prefill of per-token groups, one lane per (token, group) --------------
+// Codes of n_el elements of one group, two at a time with the packed fp32x2
+// IEEE operations (each component rounded exactly as the scalar one), the
+// rint by the 1.5 * 2^23 addition; `tie` collects |r - rint(r)| close to 1/2
+// (the caller then redoes the group with the IEEE quotient).  CLAMP: clamp to
+// the code range (needed only when the stored statistics are rounded to fp16:
+// with fp32 statistics every product already lies in range).
+template <int BITS, bool SYM, bool CLAMP>
+__device__ __forceinline__ uint32_t codes_pair(float2 x, float2 nz, float2 inv, float &tie_max) {
+  constexpr int half = 1 << (BITS - 1);
+  constexpr float lo = SYM ? -(float)(half - 1) : 0.0f;
+  constexpr float hi = SYM ? (float)(half - 1) : (float)((1 << BITS) - 1);
+  const float2 d = SYM ? x : __fadd2_rn(x, nz);
+  const float2 r = __fmul2_rn(d, inv);
+  float2 m = __fadd2_rn(r, make_float2(kMagic, kMagic));
+  const float2 ri = __fadd2_rn(m, make_float2(-kMagic, -kMagic));  // rint(r), exact
+  const float2 e = __fadd2_rn(r, make_float2(-ri.x, -ri.y));
+  tie_max = fmaxf(tie_max, fmaxf(fabsf(e.x), fabsf(e.y)));
+  if (CLAMP || SYM) {
+    m.x = fminf(fmaxf(m.x, kMagic + lo), kMagic + hi);
+    m.y = fminf(fmaxf(m.y, kMagic + lo), kMagic + hi);
+  }
+  const uint32_t c0 = (uint32_t)(__float_as_int(m.x) - kMagicBits + (SYM ? half : 0));
+  const uint32_t c1 = (uint32_t)(__float_as_int(m.y) - kMagicBits + (SYM ? half : 0));
+  return c0 | (c1 << BITS);
+}
+
+// Outliers of one token row spread over `nl` aligned consecutive lanes, each
+// holding GC elements (lane position li, channels li*GC ..): the k largest
+// magnitudes, equal ones to the lower channel (k rounds of a maximum over the
+// row's lanes).  Sets taken[] (this lane's outlier bits) and writes the row's
+// list (channels ascending) to `list` when valid.  Every lane calls it.
+template <int GC>
+__device__ __forceinline__ void row_outliers(const float *x, int li, int nl, int k,
+                                             uint32_t (&taken)[(GC + 31) / 32], uint32_t *list,
+                                             bool valid) {
+#pragma unroll
+  for (int w = 0; w < (GC + 31) / 32; ++w) taken[w] = 0u;
+  for (int r = 0; r < k; ++r) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < GC; ++e)
+      if (!((taken[e >> 5] >> (e & 31)) & 1u))
+        m = max(m, ((uint32_t)__half_as_ushort(__float2half_rn(fabsf(x[e]))) << 8) |
+                       (uint32_t)(255 - (li * GC + e)));
+    for (int off = 1; off < 8; off <<= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, m, off);
+      if (off < nl) m = max(m, o);
+    }
+    const int c = 255 - (int)(m & 255u);
+    if (c / GC == li) taken[(c % GC) >> 5] |= 1u << ((c % GC) & 31);
+  }
+  int cnt = 0;
+#pragma unroll
+  for (int w = 0; w < (GC + 31) / 32; ++w) cnt += __popc(taken[w]);
+  int pre = cnt;
+  for (int dlt = 1; dlt < nl; dlt <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, pre, dlt, nl);
+    if (li >= dlt) pre += y;
+  }
+  int pos = pre - cnt;
+  if (!valid) return;
+#pragma unroll
+  for (int e = 0; e < GC; ++e)
+    if ((taken[e >> 5] >> (e & 31)) & 1u)
+      list[pos++] = ((uint32_t)(li * GC + e) << 16) |
+                    (uint32_t)__half_as_ushort(__float2half_rn(x[e]));
+}
+
+// Prefill of per-token groups: every lane quantizes one (token, group) of
+// GL 16-byte chunks (GC = 8 GL channels) -- its statistics once, no shuffle
+// but for outliers -- and a warp covers 32 / (d / GC) whole tokens, so the
+// InnerQ mode bits of a warp are one 32-bit word (a ballot).  KIND 0: InnerQ
+// keys (from row n_sink on; normalized under KVQ_INNERQ_KNORM), 1: InnerQ
+// values, 2: KIVI values (from row 0, the first n_vq of them; outliers).
+template <int BITS, int GL, int KIND>
 __global__ void __launch_bounds__(kQuantBlock)
-    per_token_prefill_kernel(Geometry g, CachePtrs p, const __half *K, const __half *V,
-                             int64_t T, Counts uni) {
-  const bool is_key = blockIdx.z == 0 && g.scheme == KVQ_INNERQ;
-  const TokenDst dst = is_key ? key_dst(g, p) : value_dst(g, p);
-  const __half *X = is_key ? K : V;
+    group_prefill_kernel(Geometry g, CachePtrs p, const __half *X, int64_t T, Counts uni) {
+  constexpr int GC = GL * 8;
+  constexpr bool KEY = KIND == 0, MODE = KIND != 2;
+  __shared__ float s_rk[kMaxHeadDim];  // reciprocal key factors (KVQ_INNERQ_KNORM)
+  const int d = g.d, ng = d / GC, tpw = 32 / ng;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t bh = blockIdx.y;
   const Counts c = seq_counts(g, p, uni, (int)(bh / g.H));
   const int64_t src0 = c.n_sink;
-  const int64_t n_tok = (g.scheme == KVQ_KIVI) ? c.n_vq : c.n_quant;
-  const int chunks = g.d / 8;
-  const int tpr = kQuantBlock / chunks;  // tokens per round
-  const int64_t tok0 = (int64_t)blockIdx.x * tpr * kTokIter;
-  if (tok0 >= n_tok) return;  // (uniform per block)
-  const int lt = threadIdx.x / chunks, j = threadIdx.x - lt * chunks;
-  const int lanes = dst.group / 8;
-
-  // Mode bits of this block's tokens, assembled in shared memory (at most
-  // kTokIter * kQuantBlock * 8 / 16 bits: groups of >= 16 channels).
-  __shared__ uint32_t s_bits[kTokIter * kQuantBlock / 64 + 2];
-  const int ng = dst.meta_cols;
-  const int64_t bit0 = tok0 * ng;
-  const int64_t wbase = bit0 >> 5;
-  if (dst.mode) {
-    for (int i = threadIdx.x; i < kTokIter * kQuantBlock / 64 + 2; i += blockDim.x) s_bits[i] = 0;
+  const int64_t n_tok = KIND == 2 ? c.n_vq : c.n_quant;
+  const bool norm = KEY && g.knorm;
+  if (norm) {
+    for (int i = threadIdx.x; i < d; i += blockDim.x)
+      s_rk[i] = __fdiv_rn(1.0f, p.k_norm[bh * d + i]);
     __syncthreads();
   }
-
-  for (int it = 0; it < kTokIter; ++it) {
-    const int64_t t = tok0 + (int64_t)it * tpr + lt;
-    const bool valid = t < n_tok;
-    float x[8];
-    if (valid) {
-      load8(X + (bh * T + src0 + t) * g.d + 8 * j, x);
-      if (is_key && g.knorm) normalize8(p.k_norm + bh * g.d, 8 * j, x);
-    } else {
+  const int64_t tw = ((int64_t)blockIdx.x * (kQuantBlock / 32) + warp) * tpw;  // first token
+  if (tw >= n_tok) return;  // (whole warps)
+  const int gi = lane % ng;
+  const int64_t t = tw + lane / ng;
+  const bool valid = t < n_tok;
+  float x[GC];
+  {
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        X + (bh * T + src0 + (valid ? t : tw)) * d + gi * GC);
+    uint4 raw[GL];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) x[k] = 0.0f;
-    }
-    if (!dst.mode) {  // KIVI values (outliers, fp16 statistics)
-      quant_value_token(g, p, bh, t, j, chunks, x, valid);
-      continue;
-    }
-    const ChunkQ q = quant_chunk(x, lanes, g.bits, true, g.meta16, 0u);
-    if (valid) {
-      store_token(g, p, dst, bh, t, j, lanes, q);
-      if ((j & (lanes - 1)) == 0) {
-        const int gi = j / lanes;
-        if (q.sym) {
-          const int64_t bit = t * ng + gi;
-          atomicOr(&s_bits[(bit >> 5) - wbase], 1u << (bit & 31));
-        }
+    for (int k = 0; k < GL; ++k) raw[k] = src[k];
+#pragma unroll
+    for (int k = 0; k < GL; ++k) {
+      const __half2 *h = reinterpret_cast<const __half2 *>(&raw[k]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(h[i]);
+        x[8 * k + 2 * i] = f.x;
+        x[8 * k + 2 * i + 1] = f.y;
       }
     }
   }
-  if (!dst.mode) return;
-  __syncthreads();
-  // Write back the words this block owns.  Blocks own disjoint bit ranges;
-  // the block holding the last token also owns the rest of its last word.
-  const int64_t tok_end = min(tok0 + (int64_t)tpr * kTokIter, n_tok);
-  int64_t bit1 = tok_end * ng;
-  if (tok_end == n_tok) bit1 = (bit1 + 31) & ~(int64_t)31;
-  const int64_t wlast = (bit1 - 1) >> 5;
-  uint32_t *words = dst.mode + bh * g.mode_words;
-  for (int64_t w = wbase + threadIdx.x; w <= wlast; w += blockDim.x) {
-    const int64_t lo = max(bit0, w * 32) - w * 32, hi = min(bit1, w * 32 + 32) - w * 32;
-    const uint32_t mask = (hi - lo == 32) ? 0xffffffffu : (((1u << (hi - lo)) - 1u) << lo);
-    const uint32_t bits = s_bits[w - wbase] & mask;
-    if (mask == 0xffffffffu) {
-      words[w] = bits;
-    } else {
-      atomicAnd(&words[w], ~mask);
-      atomicOr(&words[w], bits);
+  if (norm) {
+#pragma unroll
+    for (int e = 0; e < GC; ++e) x[e] = __fmul_rn(x[e], s_rk[gi * GC + e]);
+  }
+  uint32_t taken[(GC + 31) / 32];
+#pragma unroll
+  for (int w = 0; w < (GC + 31) / 32; ++w) taken[w] = 0u;
+  if (KIND == 2 && g.n_out > 0)
+    row_outliers<GC>(x, gi, ng, g.n_out, taken,
+                     valid ? tok_outliers(g, p, bh, t, g.blk_vo) : nullptr, valid);
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < GC; ++e) {
+    if ((taken[e >> 5] >> (e & 31)) & 1u) continue;
+    mn = fminf(mn, x[e]);
+    mx = fmaxf(mx, x[e]);
+  }
+  bool sym = false;
+  Stats st{0.0f, 0.0f};
+  if (!(mn > mx)) {  // (else no inlier: scale 0, zero 0)
+    mn = canon_zero(mn);
+    mx = canon_zero(mx);
+    sym = MODE && choose_symmetric(mn, mx, BITS);
+    st = sym ? sym_stats(mn, mx, BITS, g.meta16) : asym_stats(mn, mx, BITS, g.meta16);
+  }
+  const float inv = recip_or_zero(st.scale);
+  constexpr int WPG = GC * BITS / 32;  // code words of a group
+  uint32_t cw[WPG];
+  {
+    float tie = 0.0f;
+    const bool clamp = g.meta16 || (KIND == 2 && g.n_out > 0);
+    const float2 nz = make_float2(-st.zero, -st.zero), iv = make_float2(inv, inv);
+#pragma unroll
+    for (int w = 0; w < WPG; ++w) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < 16 / BITS; ++i) {
+        const int e = w * (32 / BITS) + 2 * i;
+        const float2 xv = make_float2(x[e], x[e + 1]);
+        // (outliers: their products may leave the code range before they are
+        // cleared, so they clamp as fp16 statistics do)
+        const uint32_t cc =
+            sym ? (clamp ? codes_pair<BITS, true, true>(xv, nz, iv, tie)
+                         : codes_pair<BITS, true, false>(xv, nz, iv, tie))
+                : (clamp ? codes_pair<BITS, false, true>(xv, nz, iv, tie)
+                         : codes_pair<BITS, false, false>(xv, nz, iv, tie));
+        word |= cc << (2 * i * BITS);
+      }
+      cw[w] = word;
     }
+    if (!(tie < 0.5f - kTieGuard)) {
+      // a product close to a tie (or out of range): the IEEE quotient decides
+#pragma unroll
+      for (int w = 0; w < WPG; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 32 / BITS; ++i) {
+          const int e = w * (32 / BITS) + i;
+          word |= (sym ? sym_code_inv(x[e], st.scale, inv, BITS)
+                       : asym_code_inv(x[e], st.zero, st.scale, inv, BITS))
+                  << (i * BITS);
+        }
+        cw[w] = word;
+      }
+    }
+  }
+  // outliers store code 0
+#pragma unroll
+  for (int e = 0; e < GC; ++e)
+    if ((taken[e >> 5] >> (e & 31)) & 1u) cw[e / (32 / BITS)] &= ~(((1u << BITS) - 1u) << ((e % (32 / BITS)) * BITS));
+  const TokenDst dst = KEY ? key_dst(g, p) : value_dst(g, p);
+  if (valid) {
+    uint8_t *blk = tok_block(g, p, bh, t);
+    const int row = (int)(t % kBlockTokens);
+    uint32_t *code = reinterpret_cast<uint32_t *>(blk + dst.off_codes + row * g.row_bytes) + gi * WPG;
+    if (WPG == 1) {
+      code[0] = cw[0];
+    } else if (WPG == 2) {
+      *reinterpret_cast<uint2 *>(code) = make_uint2(cw[0], cw[1 % WPG]);
+    } else {
+#pragma unroll
+      for (int w = 0; w < WPG; w += 4)
+        *reinterpret_cast<uint4 *>(code + w) =
+            make_uint4(cw[w % WPG], cw[(w + 1) % WPG], cw[(w + 2) % WPG], cw[(w + 3) % WPG]);
+    }
+    st_meta(g, blk + dst.off_scale + row * ng * g.msz, gi, st.scale);
+    st_meta(g, blk + dst.off_zero + row * ng * g.msz, gi, st.zero);
+  }
+  if (MODE) {
+    // the warp's 32 mode bits are one word: tokens tw .. tw + tpw, groups in order
+    const uint32_t bits = __ballot_sync(0xffffffffu, valid && sym);
+    if (lane == 0) dst.mode[bh * g.mode_words + (tw * ng >> 5)] = bits;
   }
 }
 
-// Prefill, KIVI keys: one block per (G-token group, head).
+// One KIVI key group (G tokens of src, row stride D) quantized per channel by
+// ONE warp, with no shared memory and no block barrier: lane (rs, j) holds the
+// 8 channels of chunk j (a 16-byte load per row) for the rows rs, rs + RL,
+// ... (RL = 32 / (D/8) row slices); the per-channel minimum and maximum are
+// combined over the slices by shuffles, each lane takes its 8 channels'
+// statistics and reciprocals, and a second pass over the same rows (L1 hits)
+// packs the codes.  With outliers each row's are found by the 16 (or 8) lanes
+// of its slice, listed in the first pass, and found again in the second.
+template <int D, int BITS>
+__device__ __forceinline__ void key_group_warp(const Geometry &g, const CachePtrs &p, int64_t bh,
+                                               const __half *src, int64_t t0) {
+  constexpr int CH = D / 8, RL = 32 / CH;
+  const int lane = threadIdx.x & 31, j = lane % CH, rs = lane / CH;
+  const int G = g.k_group;
+  float mn[8], mx[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mn[e] = INFINITY;
+    mx[e] = -INFINITY;
+  }
+  for (int i = rs; i < G; i += RL) {
+    float x[8];
+    load8(src + (int64_t)i * D + 8 * j, x);
+    uint32_t om = 0;
+    if (g.n_out > 0) {
+      om = outlier_mask(x, j, CH, g.n_out);
+      store_outliers(tok_outliers(g, p, bh, t0 + i, g.blk_ko), x, j, CH, om, true);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if ((om >> e) & 1u) continue;
+      mn[e] = fminf(mn[e], x[e]);
+      mx[e] = fmaxf(mx[e], x[e]);
+    }
+  }
+#pragma unroll
+  for (int off = CH; off < 32; off <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      mn[e] = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], off));
+      mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], off));
+    }
+  float sc[8], zr[8], inv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    // no inlier in the group (every element an outlier): scale 0, zero 0
+    const Stats st = mn[e] > mx[e] ? Stats{0.0f, 0.0f}
+                                   : asym_stats(canon_zero(mn[e]), canon_zero(mx[e]), BITS,
+                                                g.meta16);
+    sc[e] = st.scale;
+    zr[e] = st.zero;
+    inv[e] = recip_or_zero(st.scale);
+  }
+  if (rs == 0) {
+    uint8_t *km = kivi_key_meta(g, p, bh, t0 / G);
+    if (g.meta16) {
+      __half2 hs[4], hz[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hs[e] = __floats2half2_rn(sc[2 * e], sc[2 * e + 1]);
+        hz[e] = __floats2half2_rn(zr[2 * e], zr[2 * e + 1]);
+      }
+      reinterpret_cast<uint4 *>(km)[j] = *reinterpret_cast<const uint4 *>(hs);
+      reinterpret_cast<uint4 *>(km + D * 2)[j] = *reinterpret_cast<const uint4 *>(hz);
+    } else {
+      float4 *ks = reinterpret_cast<float4 *>(km) + 2 * j;
+      float4 *kz = reinterpret_cast<float4 *>(km + D * 4) + 2 * j;
+      ks[0] = make_float4(sc[0], sc[1], sc[2], sc[3]);
+      ks[1] = make_float4(sc[4], sc[5], sc[6], sc[7]);
+      kz[0] = make_float4(zr[0], zr[1], zr[2], zr[3]);
+      kz[1] = make_float4(zr[4], zr[5], zr[6], zr[7]);
+    }
+  }
+  for (int i = rs; i < G; i += RL) {
+    float x[8];
+    load8(src + (int64_t)i * D + 8 * j, x);
+    const uint32_t om = g.n_out > 0 ? outlier_mask(x, j, CH, g.n_out) : 0u;
+    const uint32_t w = pack_asym<BITS, true>(x, om, zr, sc, inv);
+    store_chunk(code_row(g, p, bh, t0 + i, 0), j, w, BITS);
+  }
+}
+
+// Prefill, KIVI keys: one warp per (head, G-token group), 8 warps a block.
+template <int D, int BITS>
 __global__ void __launch_bounds__(kQuantBlock)
-    kivi_key_prefill_kernel(Geometry g, CachePtrs p, const __half *K, int64_t T, Counts uni) {
-  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim], s_pmn[kKeyPart], s_pmx[kKeyPart];
-  __shared__ uint8_t s_om[kMaskBytes];
-  const int64_t bh = blockIdx.y;
-  const int64_t t0 = (int64_t)blockIdx.x * g.k_group;
+    kivi_key_prefill_kernel(Geometry g, CachePtrs p, const __half *K, int64_t T, Counts uni,
+                            int64_t groups_per_head) {
+  const int64_t gi = (int64_t)blockIdx.x * (kQuantBlock / 32) + (threadIdx.x >> 5);
+  if (gi >= (int64_t)g.B * g.H * groups_per_head) return;  // (whole warps)
+  const int64_t bh = gi / groups_per_head;
+  const int64_t t0 = (gi - bh * groups_per_head) * g.k_group;
   if (t0 >= seq_counts(g, p, uni, (int)(bh / g.H)).n_quant) return;  // (ragged: shorter)
-  key_group_per_channel(g, p, bh, K + (bh * T + t0) * g.d, t0, s_scale, s_mn, s_pmn, s_pmx,
-                        s_om);
+  key_group_warp<D, BITS>(g, p, bh, K + (bh * T + t0) * D, t0);
 }
 
 // fp16 rows of a prefill, every head: blockIdx.z = 0 the residual / window
@@ -525,7 +799,8 @@ __global__ void prefill_rows_kernel(Geometry g, CachePtrs p, const __half *K, co
 // oldest (token n_vq) is quantized into value slot n_vq.
 __global__ void __launch_bounds__(kQuantBlock)
     kivi_append_kernel(Geometry g, CachePtrs p, const __half *k, const __half *v, Counts uni) {
-  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim], s_pmn[kKeyPart], s_pmx[kKeyPart];
+  __shared__ float s_scale[kMaxHeadDim], s_mn[kMaxHeadDim], s_inv[kMaxHeadDim];
+  __shared__ float s_pmn[kKeyPart], s_pmx[kKeyPart];
   __shared__ uint8_t s_om[kMaskBytes];
   const int64_t bh = blockIdx.x;
   const int d = g.d, R = g.residual;
@@ -545,8 +820,8 @@ __global__ void __launch_bounds__(kQuantBlock)
   if (flush) {
     for (int grp = 0; grp < R / g.k_group; ++grp)
       key_group_per_channel(g, p, bh, kr + (int64_t)grp * g.k_group * d,
-                            c.n_quant + (int64_t)grp * g.k_group, s_scale, s_mn, s_pmn, s_pmx,
-                            s_om);
+                            c.n_quant + (int64_t)grp * g.k_group, s_scale, s_mn, s_inv, s_pmn,
+                            s_pmx, s_om);
     if (!g.vq) {
       const int tpr = blockDim.x / chunks;
       for (int t0 = 0; t0 < R; t0 += tpr) {
@@ -613,7 +888,7 @@ __global__ void __launch_bounds__(32)
     // consecutive and never straddle the key/value boundary (chunks is a
     // multiple of both group widths).
     const int lanes = (valid ? dst.group : 8) / 8;
-    const ChunkQ q = quant_chunk(x, lanes, g.bits, true, g.meta16, 0u);
+    const ChunkQ q = quant_chunk_b(x, lanes, 16, g.bits, true, g.meta16, 0u);
     if (valid) {
       store_token(g, p, dst, bh, n_quant, j, lanes, q);
       if ((j & (lanes - 1)) == 0) {
@@ -640,6 +915,40 @@ __global__ void fill_i32_kernel(int32_t *dst, int n, int32_t v) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) dst[i] = v;
 }
 
+// group_prefill_kernel for a kind, group width and code width known at run
+// time.
+template <int BITS, int KIND>
+cudaError_t launch_group_prefill_b(const Geometry &g, const CachePtrs &p, const __half *X,
+                                   int64_t T, const Counts &c, int group, int64_t n_tok,
+                                   cudaStream_t st) {
+  const int ng = g.d / group, tpb = (kQuantBlock / 32) * (32 / ng);
+  const dim3 grid((unsigned)((n_tok + tpb - 1) / tpb), (unsigned)(g.B * g.H));
+  switch (group) {
+    case 16: group_prefill_kernel<BITS, 2, KIND><<<grid, kQuantBlock, 0, st>>>(g, p, X, T, c); break;
+    case 32: group_prefill_kernel<BITS, 4, KIND><<<grid, kQuantBlock, 0, st>>>(g, p, X, T, c); break;
+    case 64: group_prefill_kernel<BITS, 8, KIND><<<grid, kQuantBlock, 0, st>>>(g, p, X, T, c); break;
+    case 128: group_prefill_kernel<BITS, 16, KIND><<<grid, kQuantBlock, 0, st>>>(g, p, X, T, c); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t launch_group_prefill_k(const Geometry &g, const CachePtrs &p, const __half *X,
+                                   int64_t T, const Counts &c, int group, int64_t n_tok,
+                                   cudaStream_t st) {
+  return g.bits == 2 ? launch_group_prefill_b<2, KIND>(g, p, X, T, c, group, n_tok, st)
+                     : launch_group_prefill_b<4, KIND>(g, p, X, T, c, group, n_tok, st);
+}
+
+cudaError_t launch_group_prefill(const Geometry &g, const CachePtrs &p, const __half *X,
+                                 int64_t T, const Counts &c, int kind, int group, int64_t n_tok,
+                                 cudaStream_t st) {
+  if (kind == 0) return launch_group_prefill_k<0>(g, p, X, T, c, group, n_tok, st);
+  if (kind == 1) return launch_group_prefill_k<1>(g, p, X, T, c, group, n_tok, st);
+  return launch_group_prefill_k<2>(g, p, X, T, c, group, n_tok, st);
+}
+
 int copy_blocks(int64_t total_vec) {
   int64_t b = (total_vec + 255) / 256;
   return (int)(b < 1 ? 1 : (b > 65535 ? 65535 : b));
@@ -657,8 +966,6 @@ cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *
                            int *launches) {
   const int64_t BH = (int64_t)g.B * g.H;
   const int chunks = g.d / 8;
-  const int tpb = kQuantBlock / chunks;
-  const int64_t per_block = (int64_t)tpb * kTokIter;
   int n = 0;
   if (g.scheme == KVQ_INNERQ && g.knorm) {
     // key factors over the whole prompt, before any key is quantized
@@ -674,21 +981,26 @@ cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *
   }
   if (g.scheme == KVQ_KIVI) {
     if (c.n_quant > 0) {
-      kivi_key_prefill_kernel<<<dim3((unsigned)(c.n_quant / g.k_group), (unsigned)BH),
-                                kQuantBlock, 0, st>>>(g, p, K, T, c);
+      const int64_t gph = c.n_quant / g.k_group;
+      const int64_t warps = BH * gph, per = kQuantBlock / 32;
+      const unsigned blocks = (unsigned)((warps + per - 1) / per);
+      auto kern = g.d == 64 ? (g.bits == 2 ? kivi_key_prefill_kernel<64, 2>
+                                           : kivi_key_prefill_kernel<64, 4>)
+                            : (g.bits == 2 ? kivi_key_prefill_kernel<128, 2>
+                                           : kivi_key_prefill_kernel<128, 4>);
+      kern<<<blocks, kQuantBlock, 0, st>>>(g, p, K, T, c, gph);
       ++n;
     }
     if (c.n_vq > 0) {
-      per_token_prefill_kernel<<<dim3((unsigned)((c.n_vq + per_block - 1) / per_block),
-                                      (unsigned)BH, 1),
-                                 kQuantBlock, 0, st>>>(g, p, K, V, T, c);
+      const cudaError_t e = launch_group_prefill(g, p, V, T, c, 2, g.v_group, c.n_vq, st);
+      if (e != cudaSuccess) return e;
       ++n;
     }
   } else if (c.n_quant > 0) {
-    per_token_prefill_kernel<<<dim3((unsigned)((c.n_quant + per_block - 1) / per_block),
-                                    (unsigned)BH, 2),
-                               kQuantBlock, 0, st>>>(g, p, K, V, T, c);
-    ++n;
+    cudaError_t e = launch_group_prefill(g, p, K, T, c, 0, g.k_group, c.n_quant, st);
+    if (e == cudaSuccess) e = launch_group_prefill(g, p, V, T, c, 1, g.v_group, c.n_quant, st);
+    if (e != cudaSuccess) return e;
+    n += 2;
   }
   // fp16 rows: residual / window keys and values (up to R rows: the value
   // queue holds at most R - 1), sinks
