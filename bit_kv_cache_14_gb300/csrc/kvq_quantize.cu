@@ -473,13 +473,34 @@ __device__ __forceinline__ uint32_t codes_pair(float2 x, float2 nz, float2 inv, 
   return c0 | (c1 << BITS);
 }
 
-// Outliers of one token row spread over `nl` aligned consecutive lanes, each
-// holding GC elements (lane position li, channels li*GC ..): the k largest
-// magnitudes, equal ones to the lower channel (k rounds of a maximum over the
-// row's lanes).  Sets taken[] (this lane's outlier bits) and writes the row's
-// list (channels ascending) to `list` when valid.  Every lane calls it.
+// Codes of an element pair against per-lane parameters: r = (x + nz) * inv,
+// rint by the 1.5 * 2^23 addition, clamped to [lo, hi], plus off (asymmetric:
+// nz = -zero, [0, 2^b - 1], off 0; symmetric: nz = 0, [-(2^(b-1) - 1),
+// 2^(b-1) - 1], off 2^(b-1)) -- one branch-free path for both modes.
+template <int BITS>
+__device__ __forceinline__ uint32_t codes_pair_any(float2 x, float2 nz, float2 inv, float lo,
+                                                   float hi, int off, float &tie_max) {
+  const float2 r = __fmul2_rn(__fadd2_rn(x, nz), inv);
+  float2 m = __fadd2_rn(r, make_float2(kMagic, kMagic));
+  const float2 ri = __fadd2_rn(m, make_float2(-kMagic, -kMagic));  // rint(r), exact
+  const float2 e = __fadd2_rn(r, make_float2(-ri.x, -ri.y));
+  tie_max = fmaxf(tie_max, fmaxf(fabsf(e.x), fabsf(e.y)));
+  m.x = fminf(fmaxf(m.x, kMagic + lo), kMagic + hi);
+  m.y = fminf(fmaxf(m.y, kMagic + lo), kMagic + hi);
+  const uint32_t c0 = (uint32_t)(__float_as_int(m.x) - kMagicBits + off);
+  const uint32_t c1 = (uint32_t)(__float_as_int(m.y) - kMagicBits + off);
+  return c0 | (c1 << BITS);
+}
+
+// Outliers of one token row of raw fp16 values spread over `nl` aligned
+// consecutive lanes, each holding GC of them (lane position li, channels
+// li*GC ..): the k largest magnitudes, equal ones to the lower channel (k
+// rounds of a maximum over the row's lanes of (|x| bits, 255 - channel)).
+// Sets taken[] (this lane's outlier bits) and writes the row's list
+// ((channel << 16) | fp16 bits, channels ascending) to `list` when valid.
+// Every lane calls it.
 template <int GC>
-__device__ __forceinline__ void row_outliers(const float *x, int li, int nl, int k,
+__device__ __forceinline__ void row_outliers(const __half *xh, int li, int nl, int k,
                                              uint32_t (&taken)[(GC + 31) / 32], uint32_t *list,
                                              bool valid) {
 #pragma unroll
@@ -489,7 +510,7 @@ __device__ __forceinline__ void row_outliers(const float *x, int li, int nl, int
 #pragma unroll
     for (int e = 0; e < GC; ++e)
       if (!((taken[e >> 5] >> (e & 31)) & 1u))
-        m = max(m, ((uint32_t)__half_as_ushort(__float2half_rn(fabsf(x[e]))) << 8) |
+        m = max(m, ((uint32_t)(__half_as_ushort(xh[e]) & 0x7fffu) << 8) |
                        (uint32_t)(255 - (li * GC + e)));
     for (int off = 1; off < 8; off <<= 1) {
       const uint32_t o = __shfl_xor_sync(0xffffffffu, m, off);
@@ -511,20 +532,21 @@ __device__ __forceinline__ void row_outliers(const float *x, int li, int nl, int
 #pragma unroll
   for (int e = 0; e < GC; ++e)
     if ((taken[e >> 5] >> (e & 31)) & 1u)
-      list[pos++] = ((uint32_t)(li * GC + e) << 16) |
-                    (uint32_t)__half_as_ushort(__float2half_rn(x[e]));
+      list[pos++] = ((uint32_t)(li * GC + e) << 16) | (uint32_t)__half_as_ushort(xh[e]);
 }
 
 // Prefill of per-token groups: every lane quantizes one (token, group) of
 // GL 16-byte chunks (GC = 8 GL channels) -- its statistics once, no shuffle
-// but for outliers -- and a warp covers 32 / (d / GC) whole tokens, so the
-// InnerQ mode bits of a warp are one 32-bit word (a ballot).  KIND 0: InnerQ
-// keys (from row n_sink on; normalized under KVQ_INNERQ_KNORM), 1: InnerQ
-// values, 2: KIVI values (from row 0, the first n_vq of them; outliers).
+// but for outliers, one branch-free code path for both modes -- and a warp
+// covers 32 / (d / GC) whole tokens, so the InnerQ mode bits of a warp are
+// one 32-bit word (a ballot).  The row stays in registers as its raw fp16
+// pairs.  KIND 0: InnerQ keys (from row n_sink on; normalized under
+// KVQ_INNERQ_KNORM), 1: InnerQ values, 2: KIVI values (from row 0, the first
+// n_vq of them; outliers).
 template <int BITS, int GL, int KIND>
 __global__ void __launch_bounds__(kQuantBlock)
     group_prefill_kernel(Geometry g, CachePtrs p, const __half *X, int64_t T, Counts uni) {
-  constexpr int GC = GL * 8;
+  constexpr int GC = GL * 8, NP = GC / 2;  // elements, element pairs
   constexpr bool KEY = KIND == 0, MODE = KIND != 2;
   __shared__ float s_rk[kMaxHeadDim];  // reciprocal key factors (KVQ_INNERQ_KNORM)
   const int d = g.d, ng = d / GC, tpw = 32 / ng;
@@ -544,40 +566,58 @@ __global__ void __launch_bounds__(kQuantBlock)
   const int gi = lane % ng;
   const int64_t t = tw + lane / ng;
   const bool valid = t < n_tok;
-  float x[GC];
+  __half2 xh[NP];
   {
     const uint4 *src = reinterpret_cast<const uint4 *>(
         X + (bh * T + src0 + (valid ? t : tw)) * d + gi * GC);
-    uint4 raw[GL];
-#pragma unroll
-    for (int k = 0; k < GL; ++k) raw[k] = src[k];
 #pragma unroll
     for (int k = 0; k < GL; ++k) {
-      const __half2 *h = reinterpret_cast<const __half2 *>(&raw[k]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __half22float2(h[i]);
-        x[8 * k + 2 * i] = f.x;
-        x[8 * k + 2 * i + 1] = f.y;
-      }
+      const uint4 raw = src[k];
+      xh[4 * k] = *reinterpret_cast<const __half2 *>(&raw.x);
+      xh[4 * k + 1] = *reinterpret_cast<const __half2 *>(&raw.y);
+      xh[4 * k + 2] = *reinterpret_cast<const __half2 *>(&raw.z);
+      xh[4 * k + 3] = *reinterpret_cast<const __half2 *>(&raw.w);
     }
   }
-  if (norm) {
-#pragma unroll
-    for (int e = 0; e < GC; ++e) x[e] = __fmul_rn(x[e], s_rk[gi * GC + e]);
-  }
+  // element pair i as fp32 (normalized keys: times the reciprocal factors)
+  auto pair = [&](int i) -> float2 {
+    const float2 f = __half22float2(xh[i]);
+    if (!norm) return f;
+    return __fmul2_rn(f, make_float2(s_rk[gi * GC + 2 * i], s_rk[gi * GC + 2 * i + 1]));
+  };
   uint32_t taken[(GC + 31) / 32];
 #pragma unroll
   for (int w = 0; w < (GC + 31) / 32; ++w) taken[w] = 0u;
-  if (KIND == 2 && g.n_out > 0)
-    row_outliers<GC>(x, gi, ng, g.n_out, taken,
+  const bool outl = KIND == 2 && g.n_out > 0;
+  if (outl)
+    row_outliers<GC>(reinterpret_cast<const __half *>(xh), gi, ng, g.n_out, taken,
                      valid ? tok_outliers(g, p, bh, t, g.blk_vo) : nullptr, valid);
-  float mn = INFINITY, mx = -INFINITY;
+  float mn, mx;
+  if (!norm && !outl) {
+    __half2 a = xh[0], b = xh[0];
 #pragma unroll
-  for (int e = 0; e < GC; ++e) {
-    if ((taken[e >> 5] >> (e & 31)) & 1u) continue;
-    mn = fminf(mn, x[e]);
-    mx = fmaxf(mx, x[e]);
+    for (int i = 1; i < NP; ++i) {
+      a = __hmin2(a, xh[i]);
+      b = __hmax2(b, xh[i]);
+    }
+    const float2 fa = __half22float2(a), fb = __half22float2(b);
+    mn = fminf(fa.x, fa.y);
+    mx = fmaxf(fb.x, fb.y);
+  } else {
+    mn = INFINITY;
+    mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      const float2 f = pair(i);
+      if (!((taken[(2 * i) >> 5] >> ((2 * i) & 31)) & 1u)) {
+        mn = fminf(mn, f.x);
+        mx = fmaxf(mx, f.x);
+      }
+      if (!((taken[(2 * i + 1) >> 5] >> ((2 * i + 1) & 31)) & 1u)) {
+        mn = fminf(mn, f.y);
+        mx = fmaxf(mx, f.y);
+      }
+    }
   }
   bool sym = false;
   Stats st{0.0f, 0.0f};
@@ -589,49 +629,46 @@ __global__ void __launch_bounds__(kQuantBlock)
   }
   const float inv = recip_or_zero(st.scale);
   constexpr int WPG = GC * BITS / 32;  // code words of a group
+  constexpr int PPW = 16 / BITS;       // element pairs a code word holds
   uint32_t cw[WPG];
   {
+    constexpr int half = 1 << (BITS - 1);
+    const float lo = sym ? -(float)(half - 1) : 0.0f;
+    const float hi = sym ? (float)(half - 1) : (float)((1 << BITS) - 1);
+    const int off = sym ? half : 0;
+    const float nzv = sym ? 0.0f : -st.zero;
+    const float2 nz = make_float2(nzv, nzv), iv = make_float2(inv, inv);
     float tie = 0.0f;
-    const bool clamp = g.meta16 || (KIND == 2 && g.n_out > 0);
-    const float2 nz = make_float2(-st.zero, -st.zero), iv = make_float2(inv, inv);
 #pragma unroll
     for (int w = 0; w < WPG; ++w) {
       uint32_t word = 0;
 #pragma unroll
-      for (int i = 0; i < 16 / BITS; ++i) {
-        const int e = w * (32 / BITS) + 2 * i;
-        const float2 xv = make_float2(x[e], x[e + 1]);
-        // (outliers: their products may leave the code range before they are
-        // cleared, so they clamp as fp16 statistics do)
-        const uint32_t cc =
-            sym ? (clamp ? codes_pair<BITS, true, true>(xv, nz, iv, tie)
-                         : codes_pair<BITS, true, false>(xv, nz, iv, tie))
-                : (clamp ? codes_pair<BITS, false, true>(xv, nz, iv, tie)
-                         : codes_pair<BITS, false, false>(xv, nz, iv, tie));
-        word |= cc << (2 * i * BITS);
-      }
+      for (int i = 0; i < PPW; ++i)
+        word |= codes_pair_any<BITS>(pair(w * PPW + i), nz, iv, lo, hi, off, tie) << (2 * i * BITS);
       cw[w] = word;
     }
     if (!(tie < 0.5f - kTieGuard)) {
       // a product close to a tie (or out of range): the IEEE quotient decides
-#pragma unroll
       for (int w = 0; w < WPG; ++w) {
         uint32_t word = 0;
-#pragma unroll
-        for (int i = 0; i < 32 / BITS; ++i) {
-          const int e = w * (32 / BITS) + i;
-          word |= (sym ? sym_code_inv(x[e], st.scale, inv, BITS)
-                       : asym_code_inv(x[e], st.zero, st.scale, inv, BITS))
-                  << (i * BITS);
+        for (int i = 0; i < PPW; ++i) {
+          const float2 f = pair(w * PPW + i);
+          const uint32_t c0 = sym ? sym_code_inv(f.x, st.scale, inv, BITS)
+                                  : asym_code_inv(f.x, st.zero, st.scale, inv, BITS);
+          const uint32_t c1 = sym ? sym_code_inv(f.y, st.scale, inv, BITS)
+                                  : asym_code_inv(f.y, st.zero, st.scale, inv, BITS);
+          word |= (c0 | (c1 << BITS)) << (2 * i * BITS);
         }
         cw[w] = word;
       }
     }
   }
-  // outliers store code 0
+  if (outl) {  // outliers store code 0
 #pragma unroll
-  for (int e = 0; e < GC; ++e)
-    if ((taken[e >> 5] >> (e & 31)) & 1u) cw[e / (32 / BITS)] &= ~(((1u << BITS) - 1u) << ((e % (32 / BITS)) * BITS));
+    for (int e = 0; e < GC; ++e)
+      if ((taken[e >> 5] >> (e & 31)) & 1u)
+        cw[e / (32 / BITS)] &= ~(((1u << BITS) - 1u) << ((e % (32 / BITS)) * BITS));
+  }
   const TokenDst dst = KEY ? key_dst(g, p) : value_dst(g, p);
   if (valid) {
     uint8_t *blk = tok_block(g, p, bh, t);
@@ -672,24 +709,48 @@ __device__ __forceinline__ void key_group_warp(const Geometry &g, const CachePtr
   const int lane = threadIdx.x & 31, j = lane % CH, rs = lane / CH;
   const int G = g.k_group;
   float mn[8], mx[8];
+  if (g.n_out == 0) {
+    // raw fp16 keys: the minimum and maximum on half2 pairs (exact)
+    __half2 hmn[4], hmx[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    mn[e] = INFINITY;
-    mx[e] = -INFINITY;
-  }
-  for (int i = rs; i < G; i += RL) {
-    float x[8];
-    load8(src + (int64_t)i * D + 8 * j, x);
-    uint32_t om = 0;
-    if (g.n_out > 0) {
-      om = outlier_mask(x, j, CH, g.n_out);
-      store_outliers(tok_outliers(g, p, bh, t0 + i, g.blk_ko), x, j, CH, om, true);
+    for (int e = 0; e < 4; ++e) {
+      hmn[e] = __float2half2_rn(INFINITY);
+      hmx[e] = __float2half2_rn(-INFINITY);
+    }
+    for (int i = rs; i < G; i += RL) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(src + (int64_t)i * D + 8 * j);
+      const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hmn[e] = __hmin2(hmn[e], h[e]);
+        hmx[e] = __hmax2(hmx[e], h[e]);
+      }
     }
 #pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = __half22float2(hmn[e]), b = __half22float2(hmx[e]);
+      mn[2 * e] = a.x;
+      mn[2 * e + 1] = a.y;
+      mx[2 * e] = b.x;
+      mx[2 * e + 1] = b.y;
+    }
+  } else {
+#pragma unroll
     for (int e = 0; e < 8; ++e) {
-      if ((om >> e) & 1u) continue;
-      mn[e] = fminf(mn[e], x[e]);
-      mx[e] = fmaxf(mx[e], x[e]);
+      mn[e] = INFINITY;
+      mx[e] = -INFINITY;
+    }
+    for (int i = rs; i < G; i += RL) {
+      float x[8];
+      load8(src + (int64_t)i * D + 8 * j, x);
+      const uint32_t om = outlier_mask(x, j, CH, g.n_out);
+      store_outliers(tok_outliers(g, p, bh, t0 + i, g.blk_ko), x, j, CH, om, true);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if ((om >> e) & 1u) continue;
+        mn[e] = fminf(mn[e], x[e]);
+        mx[e] = fmaxf(mx[e], x[e]);
+      }
     }
   }
 #pragma unroll
@@ -730,12 +791,41 @@ __device__ __forceinline__ void key_group_warp(const Geometry &g, const CachePtr
       kz[1] = make_float4(zr[4], zr[5], zr[6], zr[7]);
     }
   }
+  float2 nz[4], iv[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    nz[e] = make_float2(-zr[2 * e], -zr[2 * e + 1]);
+    iv[e] = make_float2(inv[2 * e], inv[2 * e + 1]);
+  }
+  // codes leave their range only for outliers or fp16-rounded statistics
+  const bool clamp = g.meta16 || g.n_out > 0;
+  // the group's rows are consecutive token rows of one block (G <= 32) or of
+  // G / 32 consecutive blocks of the head
+  uint8_t *blk0 = tok_block(g, p, bh, t0);
+  const int r0 = (int)(t0 % kBlockTokens);
   for (int i = rs; i < G; i += RL) {
     float x[8];
     load8(src + (int64_t)i * D + 8 * j, x);
     const uint32_t om = g.n_out > 0 ? outlier_mask(x, j, CH, g.n_out) : 0u;
-    const uint32_t w = pack_asym<BITS, true>(x, om, zr, sc, inv);
-    store_chunk(code_row(g, p, bh, t0 + i, 0), j, w, BITS);
+    float tie = 0.0f;
+    uint32_t w = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 xv = make_float2(x[2 * e], x[2 * e + 1]);
+      const uint32_t cc = clamp ? codes_pair<BITS, false, true>(xv, nz[e], iv[e], tie)
+                                : codes_pair<BITS, false, false>(xv, nz[e], iv[e], tie);
+      w |= cc << (2 * e * BITS);
+    }
+    if (!(tie < 0.5f - kTieGuard)) w = pack_asym<BITS, true>(x, 0u, zr, sc, inv);
+    if (om) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if ((om >> e) & 1u) w &= ~(((1u << BITS) - 1u) << (e * BITS));
+    }
+    const int row = r0 + i;
+    store_chunk(blk0 + (int64_t)(row / kBlockTokens) * g.block_bytes +
+                    (row % kBlockTokens) * g.row_bytes,
+                j, w, BITS);
   }
 }
 
