@@ -404,8 +404,10 @@ int kvq_append_decode(const kvq_config *cfg, kvq_cache *cache, const uint16_t *k
   if (!(softmax_scale == softmax_scale)) return KVQ_EINVAL;
   // One launch when the append only stores the new token (KIVI, no flush)
   // and the decode runs on the tensor-core path; two launches otherwise.
+  // (not under the value queue, whose append may quantize a value, nor with
+  // per-sequence lengths, whose residual slots differ between sequences)
   const bool fuse = g.scheme == KVQ_KIVI && cache->n_resid + 1 < g.residual &&
-                    cache->n_quant > 0 && tc_decode_supported(g);
+                    cache->n_quant > 0 && !g.vq && !g.ragged && tc_decode_supported(g);
   if (!fuse) {
     if ((r = kvq_append(cfg, cache, k, v, stream)) != KVQ_OK) return r;
     if ((r = kvq_decode_attention(cfg, cache, q, out, softmax_scale, ws, ws_bytes, stream)) !=

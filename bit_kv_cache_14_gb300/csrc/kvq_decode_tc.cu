@@ -54,13 +54,13 @@ int debug_stall_limit() { return g_stall_limit; }
 
 int tc_variant_name(const Geometry &g, char *buf, size_t len) {
   const TcVariant v = tc_variant(g);
-  return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d,mf=%d>",
-                  g.bits, g.scheme == KVQ_KIVI ? "kivi" : "innerq", v.ngv, v.ngk, v.km, g.meta16);
+  return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d,mf=%d,out=%d>",
+                  g.bits, g.scheme == KVQ_KIVI ? "kivi" : "innerq", v.ngv, v.ngk, v.km, g.meta16,
+                  g.n_out > 0 ? 1 : 0);
 }
 
 bool tc_decode_supported(const Geometry &g) {
   if (g.d != kD || g.Hq != g.H) return false;
-  if (g.vq || g.n_out || g.ragged) return false;
   const int ngv = kD / g.v_group;
   if (ngv != 2 && ngv != 4) return false;
   if (g.scheme == KVQ_KIVI) return g.k_group >= 16 && g.k_group <= 128;
@@ -84,13 +84,23 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.n_quant = n_quant;
   a.n_fp16 = n_resid + n_sink;
   a.n_sink = n_sink;
+  const int64_t n_all = n_quant + n_resid + n_sink;
+  a.n_vq = (g.scheme == KVQ_KIVI && g.vq) ? (n_all >= g.residual ? n_all - g.residual + 1 : 0)
+                                           : n_quant;
   a.S_h = (int)((n_quant + kTile - 1) / kTile);
   // fp16 rows travel in chunks of CH tokens (K and V rows fill a ring slot up
-  // to its query row; the kernel's SlotCfg::CH is the same expression)
+  // to its query row; without outlier lists the kernel's SlotCfg::CH is the
+  // same expression)
   const int CH = tc_fp16_chunk(g);
+  a.CH = CH;
   a.CPU = 1;
   a.UPC = kChunkUnits;
-  a.nch = (int)((a.n_fp16 + CH - 1) / CH);
+  // per-sequence lengths: the counters are the longest sequence's, and any
+  // sequence may hold up to R - 1 (KIVI) or S + W (InnerQ) fp16 tokens
+  const int64_t fp16_units = g.ragged ? (g.scheme == KVQ_KIVI ? g.residual - 1
+                                                               : (int64_t)g.residual + g.n_sink)
+                                      : a.n_fp16;
+  a.nch = (int)((fp16_units + CH - 1) / CH);
   a.F_h = a.nch * a.UPC;
   a.HU = kHeadUnits;
   a.U = a.HU + a.S_h + a.F_h;
@@ -109,6 +119,7 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * 2;
   a.wait_limit = 1 << 24;
   a.stall_limit = g_stall_limit;
+  if (g.n_out > 0) return launch_tc_out(a, num_sms, st);
   return g.meta16 ? launch_tc_f16(a, num_sms, st) : launch_tc_mf<0>(a, num_sms, st);
 }
 

@@ -19,26 +19,43 @@ namespace {
 constexpr int kHeadUnits = 2;
 constexpr int kChunkUnits = 2;
 
+// Counters of head bh: the launch's, or (per-sequence lengths) its
+// sequence's own; nf = fp16 tokens (sinks + residual / window), nvq = tokens
+// whose values are quantized (the value queue keeps [nvq, nq) in fp16).
+struct HeadCnt {
+  int nq, nf, ns, nvq;
+};
+__device__ __forceinline__ HeadCnt head_cnt(const TcArgs &a, int bh) {
+  if (!a.g.ragged) return HeadCnt{(int)a.n_quant, (int)a.n_fp16, (int)a.n_sink, (int)a.n_vq};
+  const Counts c = counts_of(a.g, a.p.seq_prompt[bh / a.g.H], a.p.appended);
+  return HeadCnt{(int)c.n_quant, (int)(c.n_resid + c.n_sink), (int)c.n_sink, (int)c.n_vq};
+}
+
 // What unit range [x0, x1) holds of head bh: its U units are HU empty ones,
 // S_h quantized tiles of kTile tokens, then F_h = nch * UPC fp16 units; a
-// chunk belongs to the warp that holds its first unit.
-__device__ __forceinline__ Seg warp_seg(const TcArgs &a, int bh, int x0, int x1) {
+// chunk belongs to the warp that holds its first unit.  (Per-sequence lengths:
+// the unit layout is the longest sequence's, with room for the most fp16
+// tokens a sequence can hold; a shorter head's units past its own tokens are
+// empty.)
+__device__ __forceinline__ Seg warp_seg(const TcArgs &a, const HeadCnt &hc, int bh, int x0,
+                                        int x1) {
   Seg s;
   const int base = bh * a.U;
   const int ua = max(x0, base) - base, ub = min(x1, base + a.U) - base;
   const int qa = max(ua - a.HU, 0), qb = min(ub - a.HU, a.S_h);
   s.tq0 = qa * kTile;
-  s.tq1 = qa < qb ? (int)min((int64_t)qb * kTile, a.n_quant) : s.tq0;
+  s.tq1 = qa < qb ? max(min(qb * kTile, hc.nq), s.tq0) : s.tq0;
   const int fa = max(ua - a.HU - a.S_h, 0), fb = min(ub - a.HU - a.S_h, a.F_h);
+  const int nch = (hc.nf + a.CH - 1) / a.CH;
   s.c0 = (fa + a.UPC - 1) / a.UPC;
-  s.c1 = fa < fb ? min((fb + a.UPC - 1) / a.UPC, a.nch) : s.c0;
+  s.c1 = fa < fb ? max(min((fb + a.UPC - 1) / a.UPC, nch), s.c0) : s.c0;
   return s;
 }
 
-template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF>
+template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF, int OUT>
 __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF>;
+  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
   constexpr bool G16 = SCHEME == KVQ_KIVI && KM == 2;
   constexpr int RB = SC::RB;  // packed bytes per token row
   constexpr int nslot = SC::nslot;
@@ -59,13 +76,21 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   const int x0 = (int)((int64_t)gw * a.total / a.nw);
   const int x1 = (int)((int64_t)(gw + 1) * a.total / a.nw);
   const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
-  // fp16 tokens per chunk: a chunk's K and V rows fill the slot up to the query
-  constexpr int CH = SC::CH;
+  // fp16 tokens per chunk: a chunk's K and V rows fill the slot up to the
+  // query (with outlier lists the block size, so CH, is a run-time value)
+  const int CH = OUT ? a.CH : SC::CH;
+  const int BBr = OUT ? g.block_bytes : SC::BB;  // bytes of a cache block
+  const int n_out = OUT ? g.n_out : 0;
+  float *qf_s = reinterpret_cast<float *>(sBw + SC::sb_xtra);  // OUT: q, score domain
+  float *xo_s = qf_s + kD;  // OUT: outliers' value corrections, m_run frame
 
   // Each warp owns its ring and barriers; nothing below synchronises warps.
   // Ring bytes are only read where a copy wrote them (rows past a segment's
   // end are masked), so the ring needs no clearing; the zero block does.
   if (lane < 16) sBw[SC::sb_zero + lane] = 0u;
+  if (OUT)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xo_s[4 * lane + i] = 0.0f;
   if (lane == 0) {
     for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -77,7 +102,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // per head, its quantized tiles, then its fp16 chunks.
   int pc_bh = bh_first, pc_ph = 0, pc_lt = 0, pc_n = 0, issued = 0, ps = 0;
   const uint64_t pol_once = l2_evict_first();  // cache blocks are read once
-  Seg pc_seg = warp_seg(a, pc_bh, x0, x1);
+  HeadCnt pc_hc = head_cnt(a, pc_bh);
+  Seg pc_seg = warp_seg(a, pc_hc, pc_bh, x0, x1);
   pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
   auto pc_settle = [&]() {
     while (pc_bh >= 0 && pc_lt >= pc_n) {
@@ -90,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           return;
         }
         pc_ph = 0;
-        pc_seg = warp_seg(a, pc_bh, x0, x1);
+        pc_hc = head_cnt(a, pc_bh);
+        pc_seg = warp_seg(a, pc_hc, pc_bh, x0, x1);
         pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
       }
       pc_lt = 0;
@@ -111,8 +138,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     if (pc_ph == 0) {
       // a cache block: the common case, issued without a branch on the lane
       const int tok0 = pc_seg.tq0 + kTile * pc_lt;
-      bulk_g2s_pred(lane == 0, bar_s, (uint32_t)(SC::BB + SC::KMB + (first ? kD * 2 : 0)), dst_s,
-                    a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * SC::BB, SC::BB,
+      bulk_g2s_pred(lane == 0, bar_s, (uint32_t)(BBr + SC::KMB + (first ? kD * 2 : 0)), dst_s,
+                    a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * BBr, BBr,
                     pol_once);
       if (SCHEME == KVQ_KIVI && !SC::KIN && lane == 0)
         bulk_g2s(dst + SC::off_km,
@@ -123,8 +150,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
                  bar);
     } else if (lane == 0) {
       const __half *qrow = a.q + ((int64_t)(pc_bh / g.H) * g.Hq + pc_bh % g.H) * kD;
-      const int ns = (int)a.n_sink;
-      const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
+      const int ns = pc_hc.ns;
+      const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, pc_hc.nf);
       const int s0 = min(i0, ns), s1 = min(i1, ns);            // sink rows
       const int r0 = max(i0, ns) - ns, r1 = max(i1, ns) - ns;  // residual / window rows
       bar_expect_tx(bar, (uint32_t)(2 * (i1 - i0) * kD * 2 + (first ? kD * 2 : 0)));
@@ -212,6 +239,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       q4[2] *= n4.z;
       q4[3] *= n4.w;
     }
+    if (OUT) {
+      // the query in the score domain, for the outliers' key corrections
+      __syncwarp();
+      reinterpret_cast<float4 *>(qf_s)[lane] = make_float4(q4[0], q4[1], q4[2], q4[3]);
+      __syncwarp();
+    }
     float mx = fmaxf(fmaxf(fabsf(q4[0]), fabsf(q4[1])), fmaxf(fabsf(q4[2]), fabsf(q4[3])));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -262,9 +295,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // ---- per-warp online-softmax state ----------------------------------------
   float m_run = -INFINITY, l_lane = 0.0f, z_lane[NGV];
   float dv[8][4];
+  // value queue: p_t * v_t of tokens whose key is quantized but whose value
+  // is still fp16 (channels 4*lane .. 4*lane + 3, m_run frame)
+  float xv[4];
   auto reset_state = [&]() {
     m_run = -INFINITY;
     l_lane = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) xv[i] = 0.0f;
 #pragma unroll
     for (int j = 0; j < NGV; ++j) z_lane[j] = 0.0f;
 #pragma unroll
@@ -307,7 +345,20 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       }
     }
     __syncwarp();
-    const float4 oq = reinterpret_cast<const float4 *>(so)[lane];
+    float4 oq = reinterpret_cast<const float4 *>(so)[lane];
+    oq.x += xv[0];
+    oq.y += xv[1];
+    oq.z += xv[2];
+    oq.w += xv[3];
+    if (OUT) {
+      // the outliers' value corrections (every lane's atomics are done)
+      const float4 xo = reinterpret_cast<const float4 *>(xo_s)[lane];
+      oq.x += xo.x;
+      oq.y += xo.y;
+      oq.z += xo.z;
+      oq.w += xo.w;
+      reinterpret_cast<float4 *>(xo_s)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     __syncwarp();
     const float m = fmaxf(m_run, mf);
     const float wq = m_run == -INFINITY ? 0.0f : exp2_approx(m_run - m);
@@ -358,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     }
   }
   for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
-    const Seg sg = warp_seg(a, bh, x0, x1);
+    const HeadCnt hc = head_cnt(a, bh);
+    const Seg sg = warp_seg(a, hc, bh, x0, x1);
     const int tq0 = sg.tq0, tq1 = sg.tq1;
     // fp16 sink + residual / window chunks of this warp's segment
     const int nchk = sg.c1 - sg.c0;
@@ -526,7 +578,22 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           float score = t < 16 ? ((t & 8) ? xb0 : xa0) : ((t & 8) ? xb1 : xa1);
           if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
           const bool valid = FULL || t < n;
+          if (OUT && valid) {
+            // dense-and-sparse keys: an outlier's code is 0, so the dense score
+            // holds q_c * zero_c there; its fp16 value replaces it
+            const uint32_t *ol = reinterpret_cast<const uint32_t *>(slot + g.blk_ko) + t * n_out;
+            const uint8_t *kz = slot + SC::off_km + ((G16 ? (t >> 4) : 0) * 2 + 1) * kD * SC::MSZ;
+            for (int e = 0; e < n_out; ++e) {
+              const uint32_t w = ol[e];
+              const int c = (int)(w >> 16);
+              const float v = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+              score = fmaf(qf_s[c], v - ld_stat<MF>(kz, c), score);
+            }
+          }
           score = valid ? score : -INFINITY;
+          // value queue: tokens [vq_from, ...) of the head keep fp16 values
+          const int vq_from = hc.nvq - tok0;
+          const bool valid_v = valid && t < vq_from;
           // lazy rescaling: the reference m_run moves only when a score passes
           // it by more than kSlack (one vote, no reduction on most tiles)
           if (__any_sync(0xffffffffu, score > m_run + kSlack)) {
@@ -537,6 +604,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             l_lane *= alpha;
   #pragma unroll
             for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) xv[i] *= alpha;
+            if (OUT) {
+              __syncwarp();  // the previous tiles' corrections are in
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) xo_s[4 * lane + i] *= alpha;
+              __syncwarp();
+            }
   #pragma unroll
             for (int mt = 0; mt < 8; ++mt)
   #pragma unroll
@@ -551,7 +626,37 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             ld_stat_row<MF, NGV>(slot + SC::off_vz + t * NGV * SC::MSZ, zr);
   #pragma unroll
             for (int j = 0; j < NGV; ++j)
-              z_lane[j] = (FULL || p > 0.0f) ? fmaf(p, zr[j], z_lane[j]) : z_lane[j];
+              z_lane[j] = valid_v ? fmaf(p, zr[j], z_lane[j]) : z_lane[j];
+            if (OUT && valid_v) {
+              // dense-and-sparse values: code 0 gave p * zero, the fp16 value
+              // replaces it (channel c of an arbitrary lane: shared atomics)
+              const uint32_t *ol = reinterpret_cast<const uint32_t *>(slot + g.blk_vo) + t * n_out;
+              for (int e = 0; e < n_out; ++e) {
+                const uint32_t w = ol[e];
+                const int c = (int)(w >> 16);
+                const float v = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+                float zc = zr[0];
+  #pragma unroll
+                for (int j = 1; j < NGV; ++j)
+                  if (j == c / (kD / NGV)) zc = zr[j];
+                atomicAdd(&xo_s[c], p * (v - zc));
+              }
+            }
+          }
+          if (vq_from < n) {
+            // (warp-uniform) the tile's value-queue tokens: p_t * v_t from their
+            // fp16 ring rows, on CUDA cores
+            for (int tt = max(vq_from, 0); tt < n; ++tt) {
+              const float pt = __shfl_sync(0xffffffffu, p, tt);
+              const int64_t slot_v = ((int64_t)bh * g.residual + (tok0 + tt) % g.residual) * kD;
+              const uint2 vw = reinterpret_cast<const uint2 *>(a.p.v_res + slot_v)[lane];
+              const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
+              const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
+              xv[0] = fmaf(pt, v01.x, xv[0]);
+              xv[1] = fmaf(pt, v01.y, xv[1]);
+              xv[2] = fmaf(pt, v23.x, xv[2]);
+              xv[3] = fmaf(pt, v23.y, xv[3]);
+            }
           }
           // ------------- values: B = p * scale (hi/lo), A = codes ------------
           // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) of k-block kb carry
@@ -568,7 +673,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             __half *orow = reinterpret_cast<__half *>(sBw) + 16 * (t >> 4) + 4 * (t & 3) + ((t & 15) >> 2);
   #pragma unroll
             for (int j = 0; j < NGV; ++j) {
-              const float x = valid ? pv * sv[j] : 0.0f;
+              const float x = valid_v ? pv * sv[j] : 0.0f;
               const __half h = __float2half_rn(x);
               orow[64 * j] = h;
               orow[64 * j + 32] = __float2half_rn(x - __half2float(h));
@@ -671,10 +776,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           __syncwarp();
         }
         const int i0 = (sg.c0 + lt) * CH;
-        const int nv = min(CH, (int)a.n_fp16 - i0);  // valid rows of the chunk
+        const int nv = min(CH, hc.nf - i0);  // valid rows of the chunk
         if (a.new_row >= 0) {
           // fused append: the warp holding the new token stores it in the residual
-          const int tn = (int)a.n_sink + a.new_row - i0;
+          const int tn = hc.ns + a.new_row - i0;
           if (tn >= 0 && tn < nv) {
             const int half = lane >> 4, j = lane & 15;
             const uint4 v4 = reinterpret_cast<const uint4 *>(slot + half * CH * kD * 2 + tn * kD * 2)[j];
@@ -749,12 +854,17 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   }
 }
 
-template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF>
+template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF, int OUT>
 cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
-  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF>;
-  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM, MF>;
+  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
+  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
   constexpr int smem = SC::smem;
-  if (a.g.block_bytes != SC::BB || tc_fp16_chunk(a.g) != SC::CH || a.g.meta16 != MF)
+  if (a.g.meta16 != MF || (a.g.n_out > 0) != (OUT != 0)) return cudaErrorInvalidValue;
+  // the block and the fp16 chunk fit the slot (the block size, and so the
+  // chunk, is compile-time without outlier lists)
+  if (OUT ? (a.g.block_bytes > SC::BBX || a.g.n_out > kMaxOutliers ||
+             2 * a.CH * kD * 2 > SC::off_q)
+          : (a.g.block_bytes != SC::BB || a.CH != SC::CH))
     return cudaErrorInvalidValue;
   static KernelSetup setup;
   int occ = 0;
@@ -789,34 +899,38 @@ TcVariant tc_variant(const Geometry &g) {
   return v;
 }
 
-template <int BITS, int SCHEME, int MF>
+template <int BITS, int SCHEME, int MF, int OUT>
 cudaError_t launch_tc_v(TcArgs &a, int num_sms, cudaStream_t st) {
   const TcVariant v = tc_variant(a.g);
   if constexpr (SCHEME == KVQ_KIVI) {
     if (v.ngv == 4)
-      return v.km == 2 ? launch_tc_t<BITS, SCHEME, 4, 1, 2, MF>(a, num_sms, st)
-           : v.km == 1 ? launch_tc_t<BITS, SCHEME, 4, 1, 1, MF>(a, num_sms, st)
-                       : launch_tc_t<BITS, SCHEME, 4, 1, 0, MF>(a, num_sms, st);
-    return v.km == 2 ? launch_tc_t<BITS, SCHEME, 2, 1, 2, MF>(a, num_sms, st)
-         : v.km == 1 ? launch_tc_t<BITS, SCHEME, 2, 1, 1, MF>(a, num_sms, st)
-                     : launch_tc_t<BITS, SCHEME, 2, 1, 0, MF>(a, num_sms, st);
+      return v.km == 2 ? launch_tc_t<BITS, SCHEME, 4, 1, 2, MF, OUT>(a, num_sms, st)
+           : v.km == 1 ? launch_tc_t<BITS, SCHEME, 4, 1, 1, MF, OUT>(a, num_sms, st)
+                       : launch_tc_t<BITS, SCHEME, 4, 1, 0, MF, OUT>(a, num_sms, st);
+    return v.km == 2 ? launch_tc_t<BITS, SCHEME, 2, 1, 2, MF, OUT>(a, num_sms, st)
+         : v.km == 1 ? launch_tc_t<BITS, SCHEME, 2, 1, 1, MF, OUT>(a, num_sms, st)
+                     : launch_tc_t<BITS, SCHEME, 2, 1, 0, MF, OUT>(a, num_sms, st);
   } else {
     if (v.ngv == 4)
-      return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, 0, MF>(a, num_sms, st)
-                        : launch_tc_t<BITS, SCHEME, 4, 2, 0, MF>(a, num_sms, st);
-    return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, 0, MF>(a, num_sms, st)
-                      : launch_tc_t<BITS, SCHEME, 2, 2, 0, MF>(a, num_sms, st);
+      return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 4, 4, 0, MF, OUT>(a, num_sms, st)
+                        : launch_tc_t<BITS, SCHEME, 4, 2, 0, MF, OUT>(a, num_sms, st);
+    return v.ngk == 4 ? launch_tc_t<BITS, SCHEME, 2, 4, 0, MF, OUT>(a, num_sms, st)
+                      : launch_tc_t<BITS, SCHEME, 2, 2, 0, MF, OUT>(a, num_sms, st);
   }
 }
 
-// Every instantiation of one statistics width, dispatched on bits and scheme.
-template <int MF>
+// Every instantiation of one statistics width, dispatched on bits and scheme
+// (OUT: KIVI with outlier lists).
+template <int MF, int OUT = 0>
 cudaError_t launch_tc_mf(TcArgs &a, int num_sms, cudaStream_t st) {
+  if (OUT)
+    return a.g.bits == 2 ? launch_tc_v<2, KVQ_KIVI, MF, OUT>(a, num_sms, st)
+                         : launch_tc_v<4, KVQ_KIVI, MF, OUT>(a, num_sms, st);
   if (a.g.bits == 2)
-    return a.g.scheme == KVQ_KIVI ? launch_tc_v<2, KVQ_KIVI, MF>(a, num_sms, st)
-                                  : launch_tc_v<2, KVQ_INNERQ, MF>(a, num_sms, st);
-  return a.g.scheme == KVQ_KIVI ? launch_tc_v<4, KVQ_KIVI, MF>(a, num_sms, st)
-                                : launch_tc_v<4, KVQ_INNERQ, MF>(a, num_sms, st);
+    return a.g.scheme == KVQ_KIVI ? launch_tc_v<2, KVQ_KIVI, MF, OUT>(a, num_sms, st)
+                                  : launch_tc_v<2, KVQ_INNERQ, MF, OUT>(a, num_sms, st);
+  return a.g.scheme == KVQ_KIVI ? launch_tc_v<4, KVQ_KIVI, MF, OUT>(a, num_sms, st)
+                                : launch_tc_v<4, KVQ_INNERQ, MF, OUT>(a, num_sms, st);
 }
 
 }  // namespace

@@ -37,11 +37,14 @@ struct TcArgs {
   int part_stride;
   int wait_limit;   // poll cap of every pipeline wait
   int stall_limit;  // debug: > 0 = first wait on a barrier nothing completes
+  int64_t n_vq;     // values held quantized (the value queue's count; else n_quant)
+  int CH;           // fp16 tokens per chunk (tc_fp16_chunk)
 };
 
-// The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), built in
-// its own translation unit.
+// The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), and with
+// outlier lists (KIVI), each built in its own translation unit.
 cudaError_t launch_tc_f16(TcArgs &a, int num_sms, cudaStream_t st);
+cudaError_t launch_tc_out(TcArgs &a, int num_sms, cudaStream_t st);
 
 namespace {
 
@@ -85,7 +88,12 @@ __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int 
 // 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
 // from the separate key-statistics array.  MF: statistics stored in fp16
 // (MSZ = 2 bytes each) instead of fp32.
-template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF = 0>
+// OUT: the block carries outlier lists (up to kMaxOutliers words per token
+// and tensor), so its size is known only at run time: the slot reserves room
+// for the largest, and the per-warp area adds the query in the score domain
+// and the outliers' value corrections (128 floats each).
+constexpr int kMaxOutliers = 8;
+template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF = 0, int OUT = 0>
 struct SlotCfg {
   static constexpr int MSZ = MF ? 2 : 4;
   static constexpr int RB = kD * BITS / 8;
@@ -97,14 +105,17 @@ struct SlotCfg {
   static constexpr bool KIN = SCHEME == KVQ_KIVI && KM >= 1;
   static constexpr int KGB = (KM == 2 ? 2 : 1) * 2 * kD * MSZ;  // KIVI key statistics of a tile
   static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks + (KIN ? KGB : 0) : off_kz + kTile * NGK * MSZ;
+  static constexpr int BBX = BB + (OUT ? 2 * kTile * kMaxOutliers * 4 : 0);  // room in the slot
   static constexpr int KMB = SCHEME == KVQ_KIVI && !KIN ? KGB : 0;  // separate copy
-  static constexpr int off_km = KIN ? off_ks : BB;
-  static constexpr int off_q = BB + KMB;
+  static constexpr int off_km = KIN ? off_ks : BBX;
+  static constexpr int off_q = BBX + KMB;
   static constexpr int bytes = off_q + kD * 2;
   static constexpr int CH = off_q / (4 * kD) < 8 ? off_q / (4 * kD) : 8;  // fp16 tokens per chunk
   // per warp: KIVI key operand (512 B per group; also the 512 B output
-  // transpose at a head's end) + 64 zero bytes
-  static constexpr int SBB = (SCHEME == KVQ_KIVI && KM == 2 ? 1024 : 512) + 64;
+  // transpose at a head's end), the outlier extras, 64 zero bytes
+  static constexpr int SBO = (SCHEME == KVQ_KIVI && KM == 2 ? 1024 : 512);
+  static constexpr int SBB = SBO + (OUT ? 1024 : 0) + 64;
+  static constexpr int sb_xtra = SBO / 4;       // word offset of the extras (OUT)
   static constexpr int sb_zero = SBB / 4 - 16;  // word offset of the zero block
   static constexpr int nslot = tc_layout(bytes, 3, SBB).total <= 112 * 1024 ? 3 : 2;
   static constexpr int smem = tc_layout(bytes, nslot, SBB).total;

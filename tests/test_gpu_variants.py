@@ -22,11 +22,11 @@ W = synth.WORKLOADS
 S = synth.scaled
 
 
-def _kivi(bits, ngv, G, mf=False):
+def _kivi(bits, ngv, G, mf=False, out=0):
     base = W["llama2_7b_2bit"] if bits == 2 else W["kivi_4bit"]
     R = 64 if G <= 64 else 128
     return S(base, batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, k_group=G, v_group=128 // ngv,
-             residual=R, n_append=R + 10, meta_f16=mf)
+             residual=R, n_append=R + 10, meta_f16=mf, outliers=out)
 
 
 def _innerq(bits, ngv, ngk, mf=False):
@@ -46,6 +46,10 @@ for mf in (False, True):
         CASES["tc_kivi_b%d_ngv%d_g%d%s" % (bits, ngv, G, sfx)] = _kivi(bits, ngv, G, mf)
     for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
         CASES["tc_innerq_b%d_ngv%d_ngk%d%s" % (bits, ngv, ngk, sfx)] = _innerq(bits, ngv, ngk, mf)
+    # with outlier lists (KIVI only); 1, 2 and 8 outliers per token spread over the shapes
+    for i, (bits, ngv, G) in enumerate(itertools.product((2, 4), (2, 4), (16, 32, 64))):
+        CASES["tc_kivi_b%d_ngv%d_g%d%s_out" % (bits, ngv, G, sfx)] = _kivi(bits, ngv, G, mf,
+                                                                         (1, 2, 8)[i % 3])
 for ngv, G, rg in itertools.product((2, 4), (32, 64), (2, 4)):
     CASES["gqa_ngv%d_g%d_rg%d" % (ngv, G, rg)] = _gqa(ngv, G, rg)
 
@@ -69,8 +73,9 @@ def dispatched_tensor_core_names():
             continue
         cfgs = []
         for fl in (0, kvq.META_F16):
-            cfgs.append(kvq.make_config(2, 2 * rg, 2, d, bits, kvq.KIVI, gk, gv, 128, 0, 4096,
-                                        fl))
+            for o in (0, 2):
+                cfgs.append(kvq.make_config(2, 2 * rg, 2, d, bits, kvq.KIVI, gk, gv, 128, 0, 4096,
+                                            fl, o))
             if gk <= d:
                 cfgs += [kvq.make_config(2, 2 * rg, 2, d, bits, s, gk, gv, 32, 4, 4096, fl)
                          for s in (kvq.INNERQ, kvq.INNERQ_KNORM)]
@@ -83,8 +88,9 @@ def dispatched_tensor_core_names():
 
 def test_every_dispatched_instantiation_has_a_parity_case():
     dispatched = dispatched_tensor_core_names()
-    # MHA: 20 shapes with fp32 and with fp16 statistics; grouped-query: 8
-    assert len(dispatched) == 2 * 20 + 8, sorted(dispatched)
+    # MHA: 20 shapes with fp32 and with fp16 statistics, the 12 KIVI ones
+    # also with outlier lists; grouped-query: 8
+    assert len(dispatched) == 2 * 20 + 2 * 12 + 8, sorted(dispatched)
     covered = {_name(w) for w in CASES.values()}
     assert dispatched <= covered, sorted(dispatched - covered)
     # and each named case reaches the instantiation its name says
