@@ -54,9 +54,9 @@ int debug_stall_limit() { return g_stall_limit; }
 
 int tc_variant_name(const Geometry &g, char *buf, size_t len) {
   const TcVariant v = tc_variant(g);
-  return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d,mf=%d,out=%d>",
+  return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d,mf=%d,ext=%d>",
                   g.bits, g.scheme == KVQ_KIVI ? "kivi" : "innerq", v.ngv, v.ngk, v.km, g.meta16,
-                  g.n_out > 0 ? 1 : 0);
+                  (g.n_out > 0 || g.vq || g.ragged) ? 1 : 0);
 }
 
 bool tc_decode_supported(const Geometry &g) {
@@ -119,7 +119,7 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * 2;
   a.wait_limit = 1 << 24;
   a.stall_limit = g_stall_limit;
-  if (g.n_out > 0) return launch_tc_out(a, num_sms, st);
+  if (g.n_out > 0 || g.vq || g.ragged) return launch_tc_ext(a, num_sms, st);
   return g.meta16 ? launch_tc_f16(a, num_sms, st) : launch_tc_mf<0>(a, num_sms, st);
 }
 

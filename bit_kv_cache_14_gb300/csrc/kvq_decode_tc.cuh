@@ -25,8 +25,9 @@ constexpr int kChunkUnits = 2;
 struct HeadCnt {
   int nq, nf, ns, nvq;
 };
+template <int EXT>
 __device__ __forceinline__ HeadCnt head_cnt(const TcArgs &a, int bh) {
-  if (!a.g.ragged) return HeadCnt{(int)a.n_quant, (int)a.n_fp16, (int)a.n_sink, (int)a.n_vq};
+  if (!EXT || !a.g.ragged) return HeadCnt{(int)a.n_quant, (int)a.n_fp16, (int)a.n_sink, (int)a.n_vq};
   const Counts c = counts_of(a.g, a.p.seq_prompt[bh / a.g.H], a.p.appended);
   return HeadCnt{(int)c.n_quant, (int)(c.n_resid + c.n_sink), (int)c.n_sink, (int)c.n_vq};
 }
@@ -37,21 +38,29 @@ __device__ __forceinline__ HeadCnt head_cnt(const TcArgs &a, int bh) {
 // the unit layout is the longest sequence's, with room for the most fp16
 // tokens a sequence can hold; a shorter head's units past its own tokens are
 // empty.)
+template <int EXT>
 __device__ __forceinline__ Seg warp_seg(const TcArgs &a, const HeadCnt &hc, int bh, int x0,
                                         int x1) {
   Seg s;
   const int base = bh * a.U;
   const int ua = max(x0, base) - base, ub = min(x1, base + a.U) - base;
   const int qa = max(ua - a.HU, 0), qb = min(ub - a.HU, a.S_h);
-  s.tq0 = qa * kTile;
-  s.tq1 = qa < qb ? max(min(qb * kTile, hc.nq), s.tq0) : s.tq0;
   const int fa = max(ua - a.HU - a.S_h, 0), fb = min(ub - a.HU - a.S_h, a.F_h);
-  const int nch = (hc.nf + a.CH - 1) / a.CH;
+  s.tq0 = qa * kTile;
   s.c0 = (fa + a.UPC - 1) / a.UPC;
-  s.c1 = fa < fb ? max(min((fb + a.UPC - 1) / a.UPC, nch), s.c0) : s.c0;
+  if (!EXT) {
+    s.tq1 = qa < qb ? (int)min((int64_t)qb * kTile, a.n_quant) : s.tq0;
+    s.c1 = fa < fb ? min((fb + a.UPC - 1) / a.UPC, a.nch) : s.c0;
+  } else {
+    const int nch = (hc.nf + a.CH - 1) / a.CH;
+    s.tq1 = qa < qb ? max(min(qb * kTile, hc.nq), s.tq0) : s.tq0;
+    s.c1 = fa < fb ? max(min((fb + a.UPC - 1) / a.UPC, nch), s.c0) : s.c0;
+  }
   return s;
 }
 
+// OUT = 1: the extended kernel -- per-sequence lengths, the value queue and
+// outlier lists, each a run-time option; OUT = 0 compiles none of them.
 template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF, int OUT>
 __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -102,8 +111,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // per head, its quantized tiles, then its fp16 chunks.
   int pc_bh = bh_first, pc_ph = 0, pc_lt = 0, pc_n = 0, issued = 0, ps = 0;
   const uint64_t pol_once = l2_evict_first();  // cache blocks are read once
-  HeadCnt pc_hc = head_cnt(a, pc_bh);
-  Seg pc_seg = warp_seg(a, pc_hc, pc_bh, x0, x1);
+  HeadCnt pc_hc = head_cnt<OUT>(a, pc_bh);
+  Seg pc_seg = warp_seg<OUT>(a, pc_hc, pc_bh, x0, x1);
   pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
   auto pc_settle = [&]() {
     while (pc_bh >= 0 && pc_lt >= pc_n) {
@@ -116,8 +125,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           return;
         }
         pc_ph = 0;
-        pc_hc = head_cnt(a, pc_bh);
-        pc_seg = warp_seg(a, pc_hc, pc_bh, x0, x1);
+        pc_hc = head_cnt<OUT>(a, pc_bh);
+        pc_seg = warp_seg<OUT>(a, pc_hc, pc_bh, x0, x1);
         pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
       }
       pc_lt = 0;
@@ -346,11 +355,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     }
     __syncwarp();
     float4 oq = reinterpret_cast<const float4 *>(so)[lane];
-    oq.x += xv[0];
-    oq.y += xv[1];
-    oq.z += xv[2];
-    oq.w += xv[3];
     if (OUT) {
+      oq.x += xv[0];
+      oq.y += xv[1];
+      oq.z += xv[2];
+      oq.w += xv[3];
       // the outliers' value corrections (every lane's atomics are done)
       const float4 xo = reinterpret_cast<const float4 *>(xo_s)[lane];
       oq.x += xo.x;
@@ -409,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     }
   }
   for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
-    const HeadCnt hc = head_cnt(a, bh);
-    const Seg sg = warp_seg(a, hc, bh, x0, x1);
+    const HeadCnt hc = head_cnt<OUT>(a, bh);
+    const Seg sg = warp_seg<OUT>(a, hc, bh, x0, x1);
     const int tq0 = sg.tq0, tq1 = sg.tq1;
     // fp16 sink + residual / window chunks of this warp's segment
     const int nchk = sg.c1 - sg.c0;
@@ -592,8 +601,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           }
           score = valid ? score : -INFINITY;
           // value queue: tokens [vq_from, ...) of the head keep fp16 values
-          const int vq_from = hc.nvq - tok0;
-          const bool valid_v = valid && t < vq_from;
+          const int vq_from = OUT ? hc.nvq - tok0 : kTile;
+          const bool valid_v = OUT ? valid && t < vq_from : valid;
           // lazy rescaling: the reference m_run moves only when a score passes
           // it by more than kSlack (one vote, no reduction on most tiles)
           if (__any_sync(0xffffffffu, score > m_run + kSlack)) {
@@ -604,9 +613,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             l_lane *= alpha;
   #pragma unroll
             for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
-  #pragma unroll
-            for (int i = 0; i < 4; ++i) xv[i] *= alpha;
             if (OUT) {
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) xv[i] *= alpha;
               __syncwarp();  // the previous tiles' corrections are in
   #pragma unroll
               for (int i = 0; i < 4; ++i) xo_s[4 * lane + i] *= alpha;
@@ -626,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             ld_stat_row<MF, NGV>(slot + SC::off_vz + t * NGV * SC::MSZ, zr);
   #pragma unroll
             for (int j = 0; j < NGV; ++j)
-              z_lane[j] = valid_v ? fmaf(p, zr[j], z_lane[j]) : z_lane[j];
+              z_lane[j] = (OUT ? valid_v : (FULL || p > 0.0f)) ? fmaf(p, zr[j], z_lane[j])
+                                                                : z_lane[j];
             if (OUT && valid_v) {
               // dense-and-sparse values: code 0 gave p * zero, the fp16 value
               // replaces it (channel c of an arbitrary lane: shared atomics)
@@ -643,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
               }
             }
           }
-          if (vq_from < n) {
+          if (OUT && vq_from < n) {
             // (warp-uniform) the tile's value-queue tokens: p_t * v_t from their
             // fp16 ring rows, on CUDA cores
             for (int tt = max(vq_from, 0); tt < n; ++tt) {
@@ -859,7 +869,8 @@ cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
   auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
   constexpr int smem = SC::smem;
-  if (a.g.meta16 != MF || (a.g.n_out > 0) != (OUT != 0)) return cudaErrorInvalidValue;
+  const bool ext = a.g.n_out > 0 || a.g.vq || a.g.ragged;
+  if (a.g.meta16 != MF || ext != (OUT != 0)) return cudaErrorInvalidValue;
   // the block and the fp16 chunk fit the slot (the block size, and so the
   // chunk, is compile-time without outlier lists)
   if (OUT ? (a.g.block_bytes > SC::BBX || a.g.n_out > kMaxOutliers ||
@@ -920,12 +931,9 @@ cudaError_t launch_tc_v(TcArgs &a, int num_sms, cudaStream_t st) {
 }
 
 // Every instantiation of one statistics width, dispatched on bits and scheme
-// (OUT: KIVI with outlier lists).
+// (OUT: the extended kernel).
 template <int MF, int OUT = 0>
 cudaError_t launch_tc_mf(TcArgs &a, int num_sms, cudaStream_t st) {
-  if (OUT)
-    return a.g.bits == 2 ? launch_tc_v<2, KVQ_KIVI, MF, OUT>(a, num_sms, st)
-                         : launch_tc_v<4, KVQ_KIVI, MF, OUT>(a, num_sms, st);
   if (a.g.bits == 2)
     return a.g.scheme == KVQ_KIVI ? launch_tc_v<2, KVQ_KIVI, MF, OUT>(a, num_sms, st)
                                   : launch_tc_v<2, KVQ_INNERQ, MF, OUT>(a, num_sms, st);

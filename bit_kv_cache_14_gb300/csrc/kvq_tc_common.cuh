@@ -41,10 +41,11 @@ struct TcArgs {
   int CH;           // fp16 tokens per chunk (tc_fp16_chunk)
 };
 
-// The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), and with
-// outlier lists (KIVI), each built in its own translation unit.
+// The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), and the
+// extended one (outlier lists, the value queue, per-sequence lengths), each
+// built in its own translation unit.
 cudaError_t launch_tc_f16(TcArgs &a, int num_sms, cudaStream_t st);
-cudaError_t launch_tc_out(TcArgs &a, int num_sms, cudaStream_t st);
+cudaError_t launch_tc_ext(TcArgs &a, int num_sms, cudaStream_t st);
 
 namespace {
 
@@ -88,10 +89,11 @@ __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int 
 // 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
 // from the separate key-statistics array.  MF: statistics stored in fp16
 // (MSZ = 2 bytes each) instead of fp32.
-// OUT: the block carries outlier lists (up to kMaxOutliers words per token
-// and tensor), so its size is known only at run time: the slot reserves room
-// for the largest, and the per-warp area adds the query in the score domain
-// and the outliers' value corrections (128 floats each).
+// OUT (the extended kernel): the block may carry outlier lists (up to
+// kMaxOutliers words per token and tensor), so its size is known only at run
+// time: the slot reserves room for the largest, and the per-warp area adds
+// the query in the score domain and the outliers' value corrections (128
+// floats each).
 constexpr int kMaxOutliers = 8;
 template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF = 0, int OUT = 0>
 struct SlotCfg {
@@ -130,8 +132,9 @@ __device__ __forceinline__ float ld_stat(const uint8_t *base, int i) {
 }
 template <int MF>
 __device__ __forceinline__ float2 ld_stat2(const uint8_t *base, int i) {
-  if (MF) return __half22float2(reinterpret_cast<const __half2 *>(base)[i >> 1]);
-  return reinterpret_cast<const float2 *>(base)[i >> 1];
+  // (byte offset i * size: i is even, so the pair is aligned)
+  if (MF) return __half22float2(*reinterpret_cast<const __half2 *>(base + i * 2));
+  return *reinterpret_cast<const float2 *>(base + i * 4);
 }
 template <int MF, int N>
 __device__ __forceinline__ void ld_stat_row(const uint8_t *base, float (&out)[N]) {

@@ -29,9 +29,10 @@ def _kivi(bits, ngv, G, mf=False, out=0):
              residual=R, n_append=R + 10, meta_f16=mf, outliers=out)
 
 
-def _innerq(bits, ngv, ngk, mf=False):
-    return S(W["innerq_1m"], batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, bits=bits,
-             k_group=128 // ngk, v_group=128 // ngv, n_append=40, meta_f16=mf)
+def _innerq(bits, ngv, ngk, mf=False, ragged=False):
+    return S(W["innerq_1m"], batch=4 if ragged else 2, n_q_heads=2, n_kv_heads=2, ctx=700,
+             bits=bits, k_group=128 // ngk, v_group=128 // ngv, n_append=40, meta_f16=mf,
+             ragged=ragged)
 
 
 def _gqa(ngv, G, rg):
@@ -46,10 +47,14 @@ for mf in (False, True):
         CASES["tc_kivi_b%d_ngv%d_g%d%s" % (bits, ngv, G, sfx)] = _kivi(bits, ngv, G, mf)
     for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
         CASES["tc_innerq_b%d_ngv%d_ngk%d%s" % (bits, ngv, ngk, sfx)] = _innerq(bits, ngv, ngk, mf)
-    # with outlier lists (KIVI only); 1, 2 and 8 outliers per token spread over the shapes
+    # the extended kernel: KIVI with outlier lists (1, 2 and 8 per token spread
+    # over the shapes), InnerQ with per-sequence lengths
     for i, (bits, ngv, G) in enumerate(itertools.product((2, 4), (2, 4), (16, 32, 64))):
         CASES["tc_kivi_b%d_ngv%d_g%d%s_out" % (bits, ngv, G, sfx)] = _kivi(bits, ngv, G, mf,
                                                                          (1, 2, 8)[i % 3])
+    for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
+        CASES["tc_innerq_b%d_ngv%d_ngk%d%s_ragged" % (bits, ngv, ngk, sfx)] = _innerq(
+            bits, ngv, ngk, mf, ragged=True)
 for ngv, G, rg in itertools.product((2, 4), (32, 64), (2, 4)):
     CASES["gqa_ngv%d_g%d_rg%d" % (ngv, G, rg)] = _gqa(ngv, G, rg)
 
@@ -72,11 +77,12 @@ def dispatched_tensor_core_names():
         if gv > d:
             continue
         cfgs = []
-        for fl in (0, kvq.META_F16):
+        for fl in (0, kvq.META_F16, kvq.META_F16 | kvq.RAGGED, kvq.RAGGED,
+                   kvq.VALUE_QUEUE):
             for o in (0, 2):
                 cfgs.append(kvq.make_config(2, 2 * rg, 2, d, bits, kvq.KIVI, gk, gv, 128, 0, 4096,
                                             fl, o))
-            if gk <= d:
+            if gk <= d and not fl & kvq.VALUE_QUEUE:
                 cfgs += [kvq.make_config(2, 2 * rg, 2, d, bits, s, gk, gv, 32, 4, 4096, fl)
                          for s in (kvq.INNERQ, kvq.INNERQ_KNORM)]
         for cfg in cfgs:
@@ -88,9 +94,9 @@ def dispatched_tensor_core_names():
 
 def test_every_dispatched_instantiation_has_a_parity_case():
     dispatched = dispatched_tensor_core_names()
-    # MHA: 20 shapes with fp32 and with fp16 statistics, the 12 KIVI ones
-    # also with outlier lists; grouped-query: 8
-    assert len(dispatched) == 2 * 20 + 2 * 12 + 8, sorted(dispatched)
+    # MHA: 20 shapes with fp32 and with fp16 statistics, each plain and
+    # extended (outlier lists, value queue, per-sequence lengths); grouped-query: 8
+    assert len(dispatched) == 2 * 2 * 20 + 8, sorted(dispatched)
     covered = {_name(w) for w in CASES.values()}
     assert dispatched <= covered, sorted(dispatched - covered)
     # and each named case reaches the instantiation its name says
