@@ -326,12 +326,13 @@ __device__ __forceinline__ uint32_t sym_code(float x, float scale, int bits) {
 }
 
 // The same codes with one reciprocal per group instead of one division per
-// element, and bit for bit the same: the product d * rn(1 / scale) differs
-// from the IEEE quotient rn(d / scale) by at most 3 * 2^-24 of its magnitude
-// (three roundings), under 2^-16 while |d / scale| < 64, so rint gives the
-// same integer for both unless the product lies within kTieGuard (2^-12) of a
-// half-integer; there -- and for a quotient out of that range -- the IEEE
-// division decides.
+// element, and bit for bit the same: with inv the hardware reciprocal of the
+// scale (rcp.approx: at most 1 ulp, a relative error below 2^-23), the
+// product rn(d * inv) differs from the IEEE quotient rn(d / scale) by less
+// than 2^-21 of its magnitude, under 2^-15 while |d / scale| < 64, so rint
+// gives the same integer for both unless the product lies within kTieGuard
+// (2^-12) of a half-integer; there -- and for a quotient out of that range --
+// the IEEE division decides.
 constexpr float kTieGuard = 1.0f / 4096.0f;
 __device__ __forceinline__ float rint_quotient(float d, float scale, float inv) {
   const float r = __fmul_rn(d, inv);
@@ -356,9 +357,14 @@ __device__ __forceinline__ uint32_t sym_code_inv(float x, float scale, float inv
   r = fminf(fmaxf(r, -lim), lim);
   return (uint32_t)((int)r + half);
 }
-// rn(1 / scale), 0 for a zero scale (then no code uses it).
+// The reciprocal of a scale for the products above (the hardware
+// approximation; scales are normal numbers), 0 for a zero scale (then no
+// code uses it).
 __device__ __forceinline__ float recip_or_zero(float scale) {
-  return scale == 0.0f ? 0.0f : __fdiv_rn(1.0f, scale);
+  if (scale == 0.0f) return 0.0f;
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(scale));
+  return r;
 }
 
 // InnerQ mode rule: symmetric iff not constant and |max + min| <= (max - min)/(2^b - 1).

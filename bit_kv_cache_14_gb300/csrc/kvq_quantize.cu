@@ -70,7 +70,7 @@ __device__ __forceinline__ Stats sym_stats(float mn, float mx, int bits, bool f1
 }
 
 // ---- codes of 8 elements ---------------------------------------------------
-// The product r = d * rn(1 / scale) is rounded to an integer by adding 1.5 *
+// The product r = d * (1 / scale) is rounded to an integer by adding 1.5 *
 // 2^23 (round to nearest even, |r| < 2^22), clamped in that domain and read
 // from the low mantissa bits: about ten instructions an element.  A lane whose
 // product lies within kTieGuard of a half-integer for any element (rare; or a
@@ -639,13 +639,28 @@ __global__ void __launch_bounds__(kQuantBlock)
     const float nzv = sym ? 0.0f : -st.zero;
     const float2 nz = make_float2(nzv, nzv), iv = make_float2(inv, inv);
     float tie = 0.0f;
+    if (MODE || g.meta16 || outl) {
+      // both modes (per-lane range and offset), or codes that can leave
+      // their range: the clamped path
 #pragma unroll
-    for (int w = 0; w < WPG; ++w) {
-      uint32_t word = 0;
+      for (int w = 0; w < WPG; ++w) {
+        uint32_t word = 0;
 #pragma unroll
-      for (int i = 0; i < PPW; ++i)
-        word |= codes_pair_any<BITS>(pair(w * PPW + i), nz, iv, lo, hi, off, tie) << (2 * i * BITS);
-      cw[w] = word;
+        for (int i = 0; i < PPW; ++i)
+          word |= codes_pair_any<BITS>(pair(w * PPW + i), nz, iv, lo, hi, off, tie)
+                  << (2 * i * BITS);
+        cw[w] = word;
+      }
+    } else {
+      // KIVI values with fp32 statistics: every product lies in the code range
+#pragma unroll
+      for (int w = 0; w < WPG; ++w) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < PPW; ++i)
+          word |= codes_pair<BITS, false, false>(pair(w * PPW + i), nz, iv, tie) << (2 * i * BITS);
+        cw[w] = word;
+      }
     }
     if (!(tie < 0.5f - kTieGuard)) {
       // a product close to a tie (or out of range): the IEEE quotient decides
@@ -1095,7 +1110,10 @@ cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *
   // fp16 rows: residual / window keys and values (up to R rows: the value
   // queue holds at most R - 1), sinks
   const int max_rows = g.residual > g.n_sink ? g.residual : g.n_sink;
-  if (max_rows > 0 && T > 0) {
+  // (uniform lengths: nothing to copy when the prompt left no fp16 row)
+  const int64_t n_all = c.n_quant + c.n_resid + c.n_sink;
+  const bool rows = g.ragged || c.n_resid > 0 || c.n_sink > 0 || c.n_vq < n_all;
+  if (max_rows > 0 && T > 0 && rows) {
     prefill_rows_kernel<<<dim3(copy_blocks(BH * max_rows * chunks), 1, g.n_sink > 0 ? 4 : 2), 256,
                           0, st>>>(g, p, K, V, T, c, max_rows);
     ++n;
