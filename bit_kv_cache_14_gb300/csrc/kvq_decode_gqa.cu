@@ -47,10 +47,13 @@ struct GqaCfg {
   static constexpr int bytes = BB + KMB;  // one slot (no query rows in the ring)
   static constexpr int CH = bytes / (4 * kD) < 8 ? bytes / (4 * kD) : 8;
   static constexpr int WPG = 8 / NGV;     // 16-channel code words per value group
-  // per warp: key operand (8 columns x 64 words, also the output transpose of
-  // RG x 128 floats) + 64 zero bytes; query table [c][4] fp32 + 2^E per head
-  static constexpr int SBB = 8 * 64 * 4 + 64;
-  static constexpr int sb_zero = SBB / 4 - 16;
+  // per warp: key operand (8 columns, each a row of KROW words: lane group
+  // tig's 2-word fragment of k-step kk at tig * KTIG + 2 kk; the padding puts
+  // the four lane groups and the eight columns a half-warp reads on distinct
+  // banks), also the value operand (2 NGV blocks of 64 words) and the output
+  // transpose of RG x 128 floats; query table [c][4] fp32 + 2^E per head
+  static constexpr int KTIG = 18, KROW = 72;
+  static constexpr int SBB = 8 * KROW * 4;
   static constexpr int QTB = kD * 4 * 4 + 16;
   __host__ __device__ static constexpr int lay(int nslot, int what) {
     // what: 0 sB offset, 1 QT offset, 2 bars offset, 3 total
@@ -183,6 +186,14 @@ __device__ bool gqa_finish(const TcArgs &a, int bh, int ticket) {
   return true;
 }
 
+// Position of q_r[c] in the query table: channel c = 16 W + 8 e + p (p < 8)
+// belongs to key-operand pair ip = 8 W + p of lane ip mod 32, pass m = ip / 32;
+// the table is [m][r / 2][lane][r mod 2][e].
+__device__ __forceinline__ int qt_index(int c, int r) {
+  const int ip = 8 * (c >> 4) + (c & 7), e = (c >> 3) & 1;
+  return (((ip >> 5) * 2 + (r >> 1)) * 32 + (ip & 31)) * 4 + (r & 1) * 2 + e;
+}
+
 template <int NGV, int KM, int RG>
 __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -204,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
   block_range(a, blockIdx.x, x0, x1);
   const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
 
-  if (lane < 16) sBw[C::sb_zero + lane] = 0u;
   if (lane == 0) {
     for (int s = 0; s <= nslot; ++s) bar_init(&wbars[s], 1);  // [nslot]: never completed
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -215,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
   // ---- producer: per head, quantized tiles lt = warp, warp + 8, ..., then
   // fp16 chunks lt = warp, warp + 8, ... of this block's segments
   int pc_bh = bh_first, pc_ph = 0, pc_lt = warp, pc_n = 0, issued = 0, ps = 0;
+  const uint8_t *pc_src = nullptr, *pc_meta = nullptr;  // next block / key statistics
   const uint64_t pol_once = l2_evict_first();  // cache blocks are read once
   const uint32_t wring_s = smem_u32(wring), wbars_s = smem_u32(wbars);
   Seg pc_seg = seg_in(a, pc_bh, x0, x1);
@@ -243,16 +254,21 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
     const uint32_t dst_s = wring_s + ps * SLOT, bar_s = wbars_s + 8 * ps;
     ps = ps + 1 == nslot ? 0 : ps + 1;
     if (pc_ph == 0) {
-      // a cache block: posted by one lane without a branch
-      const int tok0 = pc_seg.tq0 + kTile * pc_lt;
-      bulk_g2s_pred(lane == 0, bar_s, (uint32_t)(C::BB + C::KMB), dst_s,
-                    a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * C::BB, C::BB,
-                    pol_once);
-      if constexpr (!C::KIN)
-        if (lane == 0)
-          bulk_g2s(dst + C::off_km,
-                   a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD * g.msz,
-                   C::KMB, bar);
+      // a cache block: posted by one lane without a branch.  The warp's blocks
+      // of one head are kWarps apart, and so are their key-statistics rows
+      // (kWarps * kTile tokens is a whole number of key groups).
+      if (pc_lt == warp) {
+        const int tok0 = pc_seg.tq0 + kTile * pc_lt;
+        pc_src = a.p.blocks + ((int64_t)pc_bh * (g.cap / kTile) + tok0 / kTile) * C::BB;
+        if constexpr (!C::KIN)
+          pc_meta = a.p.k_meta + ((int64_t)pc_bh * g.k_meta_rows + tok0 / g.k_group) * 2 * kD * g.msz;
+      }
+      bulk_g2s_pred(lane == 0, bar_s, (uint32_t)(C::BB + C::KMB), dst_s, pc_src, C::BB, pol_once);
+      pc_src += kWarps * C::BB;
+      if constexpr (!C::KIN) {
+        if (lane == 0) bulk_g2s(dst + C::off_km, pc_meta, C::KMB, bar);
+        pc_meta += (kWarps * kTile / g.k_group) * 2 * kD * g.msz;
+      }
     } else if (lane == 0) {
       const int ns = (int)a.n_sink;
       const int i0 = (pc_seg.c0 + pc_lt) * CH, i1 = min(i0 + CH, (int)a.n_fp16);
@@ -279,8 +295,11 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
   pc_settle();
   for (int s = 0; s < nslot; ++s) issue_next();
 
-  // ---- per-head query table: QT[c][r] = q_r[c] * scale_log2 * 2^-E_r, and
-  // 2^E_r; loaded with plain loads when the warp starts a head
+  // ---- per-head query table: q_r[c] * scale_log2 * 2^-E_r at qt_index(c, r),
+  // then 2^E_r at [4 kD + r]; written with plain stores when the warp starts a
+  // head.  The order serves the key-operand build: the lane that builds
+  // channel pair (c, c + 8) finds (q_r[c], q_r[c + 8]) for r = 0, 1 in one
+  // float4 and for r = 2, 3 in the next 32 lanes' float4 row.
   float pow2 = 1.0f;  // 2^E of this lane's softmax head (tig)
   int q_head = -1;
   auto load_q = [&](int bh) {
@@ -312,38 +331,55 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
     }
     __syncwarp();  // the previous head's readers are done with the table
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float4 t;
-      t.x = qv[0][i];
-      t.y = RG > 1 ? qv[RG > 1 ? 1 : 0][i] : 0.0f;
-      t.z = RG > 2 ? qv[RG > 2 ? 2 : 0][i] : 0.0f;
-      t.w = RG > 3 ? qv[RG > 3 ? 3 : 0][i] : 0.0f;
-      reinterpret_cast<float4 *>(QT)[4 * lane + i] = t;
-    }
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int r = 0; r < RG; ++r) QT[qt_index(4 * lane + i, r)] = qv[r][i];
     if (lane < RG) QT[4 * kD + lane] = e2[lane < RG ? lane : 0];
     __syncwarp();
     pow2 = tig < RG ? QT[4 * kD + tig] : 1.0f;
     q_head = bh;
   };
 
-  // key-operand channel pairs this lane builds (as in the MHA kernel)
-  int b_clo[2], b_sidx[2];
+  // key-operand channel pairs this lane builds (as in the MHA kernel), and
+  // the factor 4^-p that undoes the code position p of the low channel
+  int b_clo[2];
+  uint32_t *b_dst[2];
+  float2 b_ipf[2];
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     const int ip = lane + 32 * m;
     const int W = ip >> 3, p = ip & 7;
     b_clo[m] = 16 * W + p;
-    b_sidx[m] = (W >> 1) * 16 + (4 * (W & 1) + (p >> 1)) * 2 + (p & 1);
+    b_dst[m] = sBw + (W >> 1) * C::KTIG + (4 * (W & 1) + (p >> 1)) * 2 + (p & 1);
+    const float f = inv_pos_factor<2>(p);
+    b_ipf[m] = make_float2(f, f);
   }
+  // value operand: the writer's columns (r = tig, hi / lo) and the reader's
+  // column gid sit at column slot n ^ (n >> 2), which keeps the writers' 32-bit
+  // stores (columns 0, 2, 4, 6 or 1, 3, 5, 7) and each half-warp's 64-bit
+  // loads (columns 0-3 or 4-7) on distinct banks
+  const int wofs = 2 * (gid & 3) + (gid >> 2);  // word of token pair (gid, gid + 8)
+  uint32_t *const v_hi = sBw + (2 * tig + (tig >> 1)) * 8 + wofs;
+  uint32_t *const v_lo = sBw + (2 * tig + 1 - (tig >> 1)) * 8 + wofs;
+  const uint32_t *const v_rd = sBw + (gid ^ (gid >> 2)) * 8 + 2 * tig;
+  // value codes: this lane's rows take code position P + off of each word
+  // (P the tile's base position), read in place by a mask: positions 0-3 from
+  // the token pair's half words, 4-7 from them shifted down a byte
+  const int v_off = gid / WPG;
+  const uint32_t vm0 = 0x00030003u << (2 * v_off), vm1 = vm0 << 4;
+  const float2 neg1 = make_float2(-1.0f, -1.0f);
+  const bool head_lane = tig < RG;
 
   // ---- online-softmax state: lane (gid, tig) holds head tig ---------------
-  float m_run = -INFINITY, l_lane = 0.0f, z_lane[NGV];
+  // (lanes of absent heads keep a finite reference, so their weights are 0)
+  float m_run = -INFINITY;
+  float2 l2, z2[NGV / 2];
   float dv[8][4];
   auto reset_state = [&]() {
-    m_run = -INFINITY;
-    l_lane = 0.0f;
+    m_run = head_lane ? -INFINITY : 0.0f;
+    l2 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < NGV; ++j) z_lane[j] = 0.0f;
+    for (int j = 0; j < NGV / 2; ++j) z2[j] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -371,25 +407,26 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
 
   // quantized state -> partial `slot` of head bh
   auto flush_quant = [&](int bh, int slot) -> bool {
-    float l = l_lane, Z[NGV];
+    float l = l2.x + l2.y, Z[NGV];
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
 #pragma unroll
     for (int j = 0; j < NGV; ++j) {
-      float z = z_lane[j];
+      float z = (j & 1) ? z2[j / 2].y : z2[j / 2].x;
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
       Z[j] = z;
     }
     float *so = reinterpret_cast<float *>(sBw);
     __syncwarp();
-    if (tig < RG) {
+    if (head_lane) {
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int j = mt / WPG, m = mt % WPG;
-        const int W = j * WPG + gid % WPG, p = m * NGV + gid / WPG;
-        const int P = m * NGV;  // extraction position of this tile
-        const float f = kSub * kSlackScale / pos_factor<2>(P);
+        const int W = j * WPG + gid % WPG, p = m * NGV + v_off;
+        // the code sat at position (m NGV mod 4) + off of its source half word
+        const int ps = ((m * NGV) & 3) + v_off;
+        const float f = __int_as_float((127 + 32 - 2 * ps) << 23);  // 2^24 * 2^8 / 4^ps
         so[tig * kD + 16 * W + p] = fmaf(dv[mt][0] + dv[mt][1], f, Z[j]);
         so[tig * kD + 16 * W + 8 + p] = fmaf(dv[mt][2] + dv[mt][3], f, Z[j]);
       }
@@ -436,7 +473,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
     const int tq0 = sg.tq0, tq1 = sg.tq1;
     if (tq1 > tq0) {
       if (q_head != bh) load_q(bh);
-      const int nt = (tq1 - tq0 + kTile - 1) / kTile;
+      // every tile is whole: the quantized length is a multiple of the key
+      // group (>= 32), which the launch checks
+      const int nt = (tq1 - tq0) / kTile;
       for (int lt = warp; lt < nt; lt += kWarps) {
         int s;
         if (!wait_slot(s)) {
@@ -444,32 +483,36 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
           break;
         }
         const uint8_t *slot = wring + s * SLOT;
-        const int tok0 = tq0 + kTile * lt;
-        const int n = min(kTile, tq1 - tok0);
         const uint8_t *kc = slot;
         const uint8_t *vc = slot + C::off_vc;
         // ---- key operand: columns (r, hi/lo) of QT * scale / 4^p, and the
         // per-head bias sum_c QT * zero, for this tile's key group
         const float *ks = reinterpret_cast<const float *>(slot + C::off_km), *kz = ks + kD;
-        float bpart[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 bacc[RG];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) bacc[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
           const int clo = b_clo[m], chi = clo + 8;
-          const float ipf = inv_pos_factor<2>(clo & 7);
-          const float slo = ks[clo] * ipf, shi = ks[chi] * ipf;
-          const float zlo = kz[clo], zhi = kz[chi];
-          const float4 ql = reinterpret_cast<const float4 *>(QT)[clo];
-          const float4 qh = reinterpret_cast<const float4 *>(QT)[chi];
-          const float qlo[4] = {ql.x, ql.y, ql.z, ql.w}, qhi[4] = {qh.x, qh.y, qh.z, qh.w};
+          const float2 s2 = __fmul2_rn(make_float2(ks[clo], ks[chi]), b_ipf[m]);
+          const float2 zz = make_float2(kz[clo], kz[chi]);
+          const float4 q01 = reinterpret_cast<const float4 *>(QT)[(2 * m) * 32 + lane];
+          const float4 q23 = RG > 2 ? reinterpret_cast<const float4 *>(QT)[(2 * m + 1) * 32 + lane] : q01;
 #pragma unroll
           for (int r = 0; r < RG; ++r) {
-            uint32_t hi, lo;
-            split2(qlo[r] * slo, qhi[r] * shi, hi, lo);
-            sBw[(2 * r) * 64 + b_sidx[m]] = hi;
-            sBw[(2 * r + 1) * 64 + b_sidx[m]] = lo;
-            bpart[r] = fmaf(qlo[r], zlo, fmaf(qhi[r], zhi, bpart[r]));
+            const float4 &qq = r < 2 ? q01 : q23;
+            const float2 qr = (r & 1) ? make_float2(qq.z, qq.w) : make_float2(qq.x, qq.y);
+            const float2 x = __fmul2_rn(qr, s2);
+            const __half2 h = __float22half2_rn(x);
+            b_dst[m][(2 * r) * C::KROW] = h2u(h);
+            b_dst[m][(2 * r + 1) * C::KROW] =
+                h2u(__float22half2_rn(__ffma2_rn(__half22float2(h), neg1, x)));
+            bacc[r] = __ffma2_rn(qr, zz, bacc[r]);
           }
         }
+        float bpart[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) bpart[r] = r < RG ? bacc[r < RG ? r : 0].x + bacc[r < RG ? r : 0].y : 0.0f;
         // reduce-scatter of the 4 bias sums: lane L ends with head (L >> 3)
         {
           const bool h4 = lane & 16;
@@ -490,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
         // ---- keys: D[token][(r, hi/lo)]
         float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
         {
-          const uint32_t *bsrc = gid < 2 * RG ? sBw + gid * 64 + tig * 16 : sBw + C::sb_zero;
+          const uint32_t *bsrc = sBw + gid * C::KROW + tig * C::KTIG;
           const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
           const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
           const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
@@ -512,46 +555,64 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
           }
         }
         // ---- scores of head tig for tokens gid, gid + 8, gid + 16, gid + 24
-        float sc[4];
-        sc[0] = fmaf(d0[0] + d0[1], kSub, bias) * pow2;
-        sc[1] = fmaf(d0[2] + d0[3], kSub, bias) * pow2;
-        sc[2] = fmaf(d1[0] + d1[1], kSub, bias) * pow2;
-        sc[3] = fmaf(d1[2] + d1[3], kSub, bias) * pow2;
-        bool grow = false;
+        const float2 ksub2 = make_float2(kSub, kSub), bias2 = make_float2(bias, bias);
+        const float2 pw2 = make_float2(pow2, pow2);
+        const float2 s01 =
+            __fmul2_rn(__ffma2_rn(make_float2(d0[0] + d0[1], d0[2] + d0[3]), ksub2, bias2), pw2);
+        const float2 s23 =
+            __fmul2_rn(__ffma2_rn(make_float2(d1[0] + d1[1], d1[2] + d1[3]), ksub2, bias2), pw2);
+        float sc[4] = {s01.x, s01.y, s23.x, s23.y};
+        if constexpr (RG < 4) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const bool valid = tig < RG && gid + 8 * i < n;
-          sc[i] = valid ? sc[i] : -INFINITY;
-          grow = grow || sc[i] > m_run + kSlack;
+          for (int i = 0; i < 4; ++i) sc[i] = head_lane ? sc[i] : -INFINITY;
         }
+        const float lim = m_run + kSlack;
+        const bool grow = sc[0] > lim || sc[1] > lim || sc[2] > lim || sc[3] > lim;
         if (__any_sync(0xffffffffu, grow)) {
           float mt_ = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
 #pragma unroll
           for (int off = 4; off < 32; off <<= 1) mt_ = fmaxf(mt_, __shfl_xor_sync(0xffffffffu, mt_, off));
           if (mt_ > m_run) {
             const float alpha = exp2_approx(m_run - mt_);
-            l_lane *= alpha;
+            const float2 al2 = make_float2(alpha, alpha);
+            l2 = __fmul2_rn(l2, al2);
 #pragma unroll
-            for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
+            for (int j = 0; j < NGV / 2; ++j) z2[j] = __fmul2_rn(z2[j], al2);
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-              for (int r = 0; r < 4; ++r) dv[mt][r] *= alpha;
+            for (int mt = 0; mt < 8; ++mt) {
+              const float2 x = __fmul2_rn(make_float2(dv[mt][0], dv[mt][1]), al2);
+              const float2 y = __fmul2_rn(make_float2(dv[mt][2], dv[mt][3]), al2);
+              dv[mt][0] = x.x;
+              dv[mt][1] = x.y;
+              dv[mt][2] = y.x;
+              dv[mt][3] = y.y;
+            }
             m_run = mt_;
           }
         }
-        float pv[4];
+        // weights 2^(s - m) (0 for an absent head: its reference is finite)
+        float2 pv[2];
         {
+          const float2 mr = make_float2(m_run, m_run);
           const float *vz = reinterpret_cast<const float *>(slot + C::off_vz);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float p = sc[i] == -INFINITY ? 0.0f : exp2_approx(sc[i] - m_run);
-            pv[i] = p * kInvSlack;
-            l_lane += p;
-            if (p > 0.0f) {
-              const float *zr = vz + (gid + 8 * i) * NGV;
+          for (int k = 0; k < 2; ++k) {
+            const float2 e = __ffma2_rn(mr, neg1, make_float2(sc[2 * k], sc[2 * k + 1]));
+            const float2 p = make_float2(exp2_approx(e.x), exp2_approx(e.y));
+            l2 = __fadd2_rn(l2, p);
+            pv[k] = __fmul2_rn(p, make_float2(kInvSlack, kInvSlack));
 #pragma unroll
-              for (int j = 0; j < NGV; ++j) z_lane[j] = fmaf(p, zr[j], z_lane[j]);
+            for (int h = 0; h < 2; ++h) {
+              const float pi = h ? p.y : p.x;
+              const float2 pp = make_float2(pi, pi);
+              const float *zr = vz + (gid + 8 * (2 * k + h)) * NGV;
+              if constexpr (NGV == 4) {
+                const float4 z4 = *reinterpret_cast<const float4 *>(zr);
+                z2[0] = __ffma2_rn(pp, make_float2(z4.x, z4.y), z2[0]);
+                z2[1] = __ffma2_rn(pp, make_float2(z4.z, z4.w), z2[1]);
+              } else {
+                z2[0] = __ffma2_rn(pp, *reinterpret_cast<const float2 *>(zr), z2[0]);
+              }
             }
           }
         }
@@ -560,55 +621,66 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
         // tokens 16kb + tig + {0, 8} and + {4, 12}.  The operand B[t][(r,
         // hi/lo)] = p_tr * scale_tj * 2^-8 is written once, by the lane that
         // holds p_tr (head tig, tokens gid + 8i): a token pair (t, t + 8) of one
-        // column is one 32-bit word, at [j][kb][column][tig'][2 words] in the
-        // warp's operand area (the key operand is consumed by now); each lane
-        // then loads its fragment of (kb, j) with one 64-bit load.
+        // column is one 32-bit word, at [j][kb][column slot][tig'][2 words] in
+        // the warp's operand area (the key operand is consumed by now); each
+        // lane then loads its fragment of (kb, j) with one 64-bit load.
         {
           const float *vs = reinterpret_cast<const float *>(slot + C::off_vs);
-          const int wofs = 2 * (gid & 3) + (gid >> 2);  // word of token pair (gid, gid + 8)
           __syncwarp();  // every lane's key-operand loads are done
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
-            const float pa = pv[2 * kb], pb = pv[2 * kb + 1];
-            const float *sa = vs + (gid + 16 * kb) * NGV, *sb = sa + 8 * NGV;
+            // tokens a = gid + 16 kb and b = a + 8: products taken in pairs of
+            // value groups (j, j + 1), then packed per group as (a, b)
+            const float2 paa = make_float2(pv[kb].x, pv[kb].x), pbb = make_float2(pv[kb].y, pv[kb].y);
+            float2 sa[NGV / 2], sb[NGV / 2];
+            const float *ra = vs + (gid + 16 * kb) * NGV, *rb = ra + 8 * NGV;
+            if constexpr (NGV == 4) {
+              const float4 x = *reinterpret_cast<const float4 *>(ra);
+              const float4 y = *reinterpret_cast<const float4 *>(rb);
+              sa[0] = make_float2(x.x, x.y), sa[1] = make_float2(x.z, x.w);
+              sb[0] = make_float2(y.x, y.y), sb[1] = make_float2(y.z, y.w);
+            } else {
+              sa[0] = *reinterpret_cast<const float2 *>(ra);
+              sb[0] = *reinterpret_cast<const float2 *>(rb);
+            }
 #pragma unroll
-            for (int j = 0; j < NGV; ++j) {
-              const float xa = pa > 0.0f ? pa * sa[j] : 0.0f;
-              const float xb = pb > 0.0f ? pb * sb[j] : 0.0f;
-              uint32_t h, l;
-              split2(xa, xb, h, l);
-              uint32_t *cell = sBw + ((j * 2 + kb) * 8 + 2 * tig) * 8 + wofs;
-              cell[0] = h;
-              cell[8] = l;
+            for (int jp = 0; jp < NGV / 2; ++jp) {
+              const float2 xa = __fmul2_rn(paa, sa[jp]), xb = __fmul2_rn(pbb, sb[jp]);
+              const __half2 h0 = __floats2half2_rn(xa.x, xb.x), h1 = __floats2half2_rn(xa.y, xb.y);
+              const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+              const float2 ea = __ffma2_rn(make_float2(f0.x, f1.x), neg1, xa);
+              const float2 eb = __ffma2_rn(make_float2(f0.y, f1.y), neg1, xb);
+              v_hi[(4 * jp + kb) * 64] = h2u(h0);
+              v_lo[(4 * jp + kb) * 64] = h2u(__floats2half2_rn(ea.x, eb.x));
+              v_hi[(4 * jp + 2 + kb) * 64] = h2u(h1);
+              v_lo[(4 * jp + 2 + kb) * 64] = h2u(__floats2half2_rn(ea.y, eb.y));
             }
           }
           __syncwarp();
         }
         {
-          const bool bact = gid < 2 * RG;
-          const int sh = 2 * (gid / WPG);  // this lane's code position offset
-          const int nkb = n > 16 ? 2 : 1;
-          for (int kb = 0; kb < nkb; ++kb) {
-            const int tk0 = 16 * kb + tig, tk1 = tk0 + 8, tk2 = tk0 + 4, tk3 = tk0 + 12;
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint8_t *vr = vc + (16 * kb + tig) * RB + 4 * (gid % WPG);
 #pragma unroll
             for (int j = 0; j < NGV; ++j) {
-              const uint2 bw = *reinterpret_cast<const uint2 *>(sBw + ((j * 2 + kb) * 8 + gid) * 8 + 2 * tig);
-              const uint32_t bv0 = bact ? bw.x : 0u;
-              const uint32_t bv1 = bact ? bw.y : 0u;
-              const int W = j * WPG + gid % WPG;
-              const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vc + tk0 * RB + 4 * W);
-              const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vc + tk1 * RB + 4 * W);
-              const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vc + tk2 * RB + 4 * W);
-              const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vc + tk3 * RB + 4 * W);
-              const uint32_t ya = __byte_perm(w0, w1, 0x5410) >> sh, yb = __byte_perm(w0, w1, 0x7632) >> sh;
-              const uint32_t yc = __byte_perm(w2, w3, 0x5410) >> sh, yd = __byte_perm(w2, w3, 0x7632) >> sh;
-              const uint32_t sa = shifted<2>(ya), sb = shifted<2>(yb);
-              const uint32_t sc_ = shifted<2>(yc), sd = shifted<2>(yd);
-#pragma unroll
-              for (int m = 0; m < WPG; ++m) {
-                const int P = m * NGV;
-                mma16816(dv[j * WPG + m], ext<2>(ya, sa, P), ext<2>(yb, sb, P), ext<2>(yc, sc_, P),
-                         ext<2>(yd, sd, P), bv0, bv1);
+              const uint2 bw = *reinterpret_cast<const uint2 *>(v_rd + (j * 2 + kb) * 64);
+              const uint8_t *vw = vr + 4 * j * WPG;
+              const uint32_t w0 = *reinterpret_cast<const uint32_t *>(vw);
+              const uint32_t w1 = *reinterpret_cast<const uint32_t *>(vw + 8 * RB);
+              const uint32_t w2 = *reinterpret_cast<const uint32_t *>(vw + 4 * RB);
+              const uint32_t w3 = *reinterpret_cast<const uint32_t *>(vw + 12 * RB);
+              const uint32_t ya = __byte_perm(w0, w1, 0x5410), yb = __byte_perm(w0, w1, 0x7632);
+              const uint32_t yc = __byte_perm(w2, w3, 0x5410), yd = __byte_perm(w2, w3, 0x7632);
+              const uint32_t za = ya >> 8, zb = yb >> 8, zc = yc >> 8, zd = yd >> 8;
+              if constexpr (WPG == 2) {
+                mma16816(dv[2 * j], ya & vm0, yb & vm0, yc & vm0, yd & vm0, bw.x, bw.y);
+                mma16816(dv[2 * j + 1], za & vm0, zb & vm0, zc & vm0, zd & vm0, bw.x, bw.y);
+              } else {
+                mma16816(dv[4 * j], ya & vm0, yb & vm0, yc & vm0, yd & vm0, bw.x, bw.y);
+                mma16816(dv[4 * j + 1], ya & vm1, yb & vm1, yc & vm1, yd & vm1, bw.x, bw.y);
+                mma16816(dv[4 * j + 2], za & vm0, zb & vm0, zc & vm0, zd & vm0, bw.x, bw.y);
+                mma16816(dv[4 * j + 3], za & vm1, zb & vm1, zc & vm1, zd & vm1, bw.x, bw.y);
               }
             }
           }
@@ -631,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
       for (int r = 0; r < RG; ++r) {
         const float e = QT[4 * kD + r];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) qq[r][i] = QT[4 * (4 * lane + i) + r] * e;
+        for (int i = 0; i < 4; ++i) qq[r][i] = QT[qt_index(4 * lane + i, r)] * e;
         mf[r] = -INFINITY;
         lf[r] = 0.0f;
 #pragma unroll
@@ -753,6 +825,7 @@ cudaError_t launch_decode_gqa(const Geometry &g, const CachePtrs &p, int64_t n_q
   a.v_new = nullptr;
   a.new_row = -1;
   a.scale_log2 = scale * 1.4426950408889634f;
+  if (n_quant % kTile != 0) return cudaErrorInvalidValue;  // the kernel takes whole tiles only
   a.n_quant = n_quant;
   a.n_fp16 = n_resid + n_sink;
   a.n_sink = n_sink;
