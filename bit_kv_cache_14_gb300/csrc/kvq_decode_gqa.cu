@@ -48,11 +48,12 @@ struct GqaCfg {
   static constexpr int CH = bytes / (4 * kD) < 8 ? bytes / (4 * kD) : 8;
   static constexpr int WPG = 8 / NGV;     // 16-channel code words per value group
   // per warp: key operand (8 columns, each a row of KROW words: lane group
-  // tig's 2-word fragment of k-step kk at tig * KTIG + 2 kk; the padding puts
-  // the four lane groups and the eight columns a half-warp reads on distinct
-  // banks), also the value operand (2 NGV blocks of 64 words) and the output
-  // transpose of RG x 128 floats; query table [c][4] fp32 + 2^E per head
-  static constexpr int KTIG = 18, KROW = 72;
+  // tig's 2-word fragment of k-step kk at tig * KTIG + 2 kk; the pitches put
+  // the 16 fragments a half-warp reads, and the 32 words one store writes,
+  // on distinct banks), also the value operand (2 NGV blocks of 64 words) and
+  // the output transpose of RG x 128 floats; query table [c][4] fp32 + 2^E
+  // per head
+  static constexpr int KTIG = 24, KROW = 98;
   static constexpr int SBB = 8 * KROW * 4;
   static constexpr int QTB = kD * 4 * 4 + 16;
   __host__ __device__ static constexpr int lay(int nslot, int what) {
@@ -186,11 +187,17 @@ __device__ bool gqa_finish(const TcArgs &a, int bh, int ticket) {
   return true;
 }
 
+// Key-operand pair ip (0..63: lane ip mod 32, pass ip / 32) builds channels
+// c = 16 W + p and c + 8 with p = ip mod 8 and W = kw_of(ip / 8): bits 1 and 2
+// of ip / 8 swapped, so one pass writes the fragments of lane groups 0 and 2
+// (or 1 and 3).  The map is its own inverse.
+__device__ __forceinline__ int kw_of(int q) { return (q & 1) | ((q & 2) << 1) | ((q & 4) >> 1); }
+
 // Position of q_r[c] in the query table: channel c = 16 W + 8 e + p (p < 8)
-// belongs to key-operand pair ip = 8 W + p of lane ip mod 32, pass m = ip / 32;
-// the table is [m][r / 2][lane][r mod 2][e].
+// belongs to key-operand pair ip = 8 kw_of(W) + p; the table is
+// [ip / 32][r / 2][ip mod 32][r mod 2][e].
 __device__ __forceinline__ int qt_index(int c, int r) {
-  const int ip = 8 * (c >> 4) + (c & 7), e = (c >> 3) & 1;
+  const int ip = 8 * kw_of(c >> 4) + (c & 7), e = (c >> 3) & 1;
   return (((ip >> 5) * 2 + (r >> 1)) * 32 + (ip & 31)) * 4 + (r & 1) * 2 + e;
 }
 
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     const int ip = lane + 32 * m;
-    const int W = ip >> 3, p = ip & 7;
+    const int W = kw_of(ip >> 3), p = ip & 7;
     b_clo[m] = 16 * W + p;
     b_dst[m] = sBw + (W >> 1) * C::KTIG + (4 * (W & 1) + (p >> 1)) * 2 + (p & 1);
     const float f = inv_pos_factor<2>(p);
@@ -531,27 +538,40 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
         const float bias = __shfl_sync(0xffffffffu, bpart[0], (tig & 3) << 3);
         __syncwarp();
         // ---- keys: D[token][(r, hi/lo)]
-        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        // (two accumulators per 16-token half, one per code word, keep the
+        // dependent MMA chains four long)
+        float d0[4], d1[4];
         {
+          float e0[2][4] = {}, e1[2][4] = {};
           const uint32_t *bsrc = sBw + gid * C::KROW + tig * C::KTIG;
           const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
           const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
           const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
           const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
+          uint32_t w[2][4], sw[2][4];
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
-            const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
-            const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
-            const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
+            w[m][0] = m ? wa0.y : wa0.x, w[m][1] = m ? wb0.y : wb0.x;
+            w[m][2] = m ? wa1.y : wa1.x, w[m][3] = m ? wb1.y : wb1.x;
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
+            for (int i = 0; i < 4; ++i) sw[m][i] = shifted<2>(w[m][i]);
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
               const uint2 b = *reinterpret_cast<const uint2 *>(bsrc + 2 * (4 * m + jj));
-              mma16816(d0, ext<2>(w00, s00, 2 * jj), ext<2>(w01, s01, 2 * jj),
-                       ext<2>(w00, s00, 2 * jj + 1), ext<2>(w01, s01, 2 * jj + 1), b.x, b.y);
-              mma16816(d1, ext<2>(w10, s10, 2 * jj), ext<2>(w11, s11, 2 * jj),
-                       ext<2>(w10, s10, 2 * jj + 1), ext<2>(w11, s11, 2 * jj + 1), b.x, b.y);
+              mma16816(e0[m], ext<2>(w[m][0], sw[m][0], 2 * jj), ext<2>(w[m][1], sw[m][1], 2 * jj),
+                       ext<2>(w[m][0], sw[m][0], 2 * jj + 1), ext<2>(w[m][1], sw[m][1], 2 * jj + 1),
+                       b.x, b.y);
+              mma16816(e1[m], ext<2>(w[m][2], sw[m][2], 2 * jj), ext<2>(w[m][3], sw[m][3], 2 * jj),
+                       ext<2>(w[m][2], sw[m][2], 2 * jj + 1), ext<2>(w[m][3], sw[m][3], 2 * jj + 1),
+                       b.x, b.y);
             }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            d0[i] = e0[0][i] + e0[1][i];
+            d1[i] = e1[0][i] + e1[1][i];
           }
         }
         // ---- scores of head tig for tokens gid, gid + 8, gid + 16, gid + 24
