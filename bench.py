@@ -167,9 +167,11 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-DECODE_SOURCES = ("kvq_decode.cu", "kvq_decode_tc.cu", "kvq_decode_gqa.cu", "kvq_tc_common.cuh",
+# sources of the timed kernels (their hash ties a committed ncu summary to them)
+DECODE_SOURCES = ("kvq_decode_tc.cuh", "kvq_decode_tc.cu", "kvq_tc_common.cuh", "kvq_rope.cuh",
                   "kvq_internal.cuh")
-ROPE_SOURCES = ("kvq_rope.cu", "kvq_rope.cuh", "kvq_internal.cuh")
+ROPE_SOURCES = ("kvq_decode_tc.cuh", "kvq_decode_tc_rope.cu", "kvq_tc_common.cuh", "kvq_rope.cuh",
+                "kvq_internal.cuh")
 
 
 def decode_source_sha(names=DECODE_SOURCES):
@@ -182,17 +184,14 @@ def decode_source_sha(names=DECODE_SOURCES):
     return h.hexdigest()[:16]
 
 
-def decode_kernel_name(w):
-    """Which decode kernel the library launches for this shape: head_dim 128
-    with 2 or 4 value groups -> the tensor-core kernels (MHA; grouped-query for
-    2-bit KIVI, G >= 32, 2 or 4 query heads per KV head), else the general one."""
-    if w.head_dim == 128 and 128 // w.v_group in (2, 4):
-        if w.n_q_heads == w.n_kv_heads:
-            return "tc_decode_kernel"
-        if (w.bits == 2 and w.scheme == synth.KIVI and w.k_group >= 32
-                and w.n_q_heads // w.n_kv_heads in (2, 4)):
-            return "tc_gqa_kernel"
-    return "decode_kernel"
+def decode_kernel_name(w, rope=False):
+    """The decode kernel the library launches for this shape (its own answer,
+    kvq_decode_kernel_name / kvq_rope_kernel_name, without the template
+    arguments)."""
+    from bit_kv_cache_14_gb300 import kvq
+    cfg = kvq.config_of(w)
+    name = kvq.rope_kernel_name(cfg, 1) if rope else kvq.decode_kernel_name(cfg, 1)
+    return name.split("<")[0]
 
 
 def profiled_traffic(workload, per_launch_units, rope=False):
@@ -907,7 +906,7 @@ def main():
         "us_per_step": elapsed_ms / args.steps * 1e3,
         "roofline": {"bound": "hbm", "achieved": decode_gbs, "peak": peak, "unit": "GB/s",
                      "frac": decode_gbs / peak, "traffic": traffic,
-                     "kernel": "rope_decode_kernel" if rope else decode_kernel_name(w),
+                     "kernel": decode_kernel_name(w, rope),
                      "kernel_us": r["decode_ms"] * 1e3,
                      "algorithmic_bytes_per_launch": r["dstate_bytes"],
                      "peak_kind": peak_kind},

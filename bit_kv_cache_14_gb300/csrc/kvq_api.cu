@@ -379,11 +379,17 @@ int kvq_decode_attention_rope(const kvq_config *cfg, const kvq_cache *cache, con
   if (!(rope_base > 0.0) || !isfinite(rope_base)) return KVQ_EINVAL;
   if (!rope_group_supported(g.Hq / g.H) || g.max_ctx > kRopeMaxPositions) return KVQ_EUNSUPPORTED;
   if (g.meta16 || g.vq || g.n_out || g.ragged) return KVQ_EUNSUPPORTED;
-  r = from_cuda(launch_decode_rope(g, ptrs_of(g, cache), cache->n_quant, cache->n_resid,
-                                   cache->n_sink, cache->ring_head,
-                                   reinterpret_cast<const __half *>(q), out, softmax_scale,
-                                   rope_base, ws, num_sms_cached(),
-                                   static_cast<cudaStream_t>(stream)));
+  if (cache->n_quant > 0 && tc_rope_supported(g))
+    r = from_cuda(launch_decode_tc_rope(g, ptrs_of(g, cache), cache->n_quant, cache->n_resid,
+                                        reinterpret_cast<const __half *>(q), out, softmax_scale,
+                                        rope_base, ws, num_sms_cached(),
+                                        static_cast<cudaStream_t>(stream)));
+  else
+    r = from_cuda(launch_decode_rope(g, ptrs_of(g, cache), cache->n_quant, cache->n_resid,
+                                     cache->n_sink, cache->ring_head,
+                                     reinterpret_cast<const __half *>(q), out, softmax_scale,
+                                     rope_base, ws, num_sms_cached(),
+                                     static_cast<cudaStream_t>(stream)));
   if (r != KVQ_OK) return r;
   note_launch(1);
   return KVQ_OK;
@@ -487,6 +493,20 @@ int kvq_decode_kernel_name(const kvq_config *cfg, int64_t n_quant, char *buf, si
   else
     n = snprintf(buf, len, "decode_kernel<d=%d,bits=%d,rg=%d,scheme=%s>", g.d, g.bits, g.Hq / g.H,
                  g.scheme == KVQ_KIVI ? "kivi" : "innerq");
+  return (n < 0 || (size_t)n >= len) ? KVQ_EINVAL : KVQ_OK;
+}
+
+int kvq_rope_kernel_name(const kvq_config *cfg, int64_t n_quant, char *buf, size_t len) {
+  if (!buf || len == 0 || n_quant < 0) return KVQ_EINVAL;
+  Geometry g;
+  const int r = resolve(cfg, &g);
+  if (r != KVQ_OK) return r;
+  int n;
+  if (n_quant > 0 && tc_rope_supported(g))
+    n = tc_rope_variant_name(g, buf, len);
+  else
+    n = snprintf(buf, len, "rope_decode_kernel<d=%d,bits=%d,rg=%d,scheme=%s>", g.d, g.bits,
+                 g.Hq / g.H, g.scheme == KVQ_KIVI ? "kivi" : "innerq");
   return (n < 0 || (size_t)n >= len) ? KVQ_EINVAL : KVQ_OK;
 }
 

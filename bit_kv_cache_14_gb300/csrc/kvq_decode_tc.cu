@@ -68,11 +68,9 @@ bool tc_decode_supported(const Geometry &g) {
   return ngk == 2 || ngk == 4;
 }
 
-cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_quant,
-                             int64_t n_resid, int64_t n_sink, const __half *q, float *out,
-                             float scale, void *ws, int num_sms, cudaStream_t st,
-                             const __half *k_new, const __half *v_new) {
-  TcArgs a;
+cudaError_t tc_fill_args(TcArgs &a, const Geometry &g, const CachePtrs &p, int64_t n_quant,
+                         int64_t n_resid, int64_t n_sink, const __half *q, float *out, float scale,
+                         void *ws, const __half *k_new, const __half *v_new) {
   a.g = g;
   a.p = p;
   a.q = q;
@@ -119,6 +117,19 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * 2;
   a.wait_limit = 1 << 24;
   a.stall_limit = g_stall_limit;
+  a.qpos = 0;
+  a.c1 = a.c2 = a.c3 = 0.0f;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_quant,
+                             int64_t n_resid, int64_t n_sink, const __half *q, float *out,
+                             float scale, void *ws, int num_sms, cudaStream_t st,
+                             const __half *k_new, const __half *v_new) {
+  TcArgs a;
+  const cudaError_t e =
+      tc_fill_args(a, g, p, n_quant, n_resid, n_sink, q, out, scale, ws, k_new, v_new);
+  if (e != cudaSuccess) return e;
   if (g.n_out > 0 || g.vq || g.ragged) return launch_tc_ext(a, num_sms, st);
   return g.meta16 ? launch_tc_f16(a, num_sms, st) : launch_tc_mf<0>(a, num_sms, st);
 }

@@ -4,6 +4,7 @@
 // kvq_decode_tc.cu for the design.
 #pragma once
 
+#include "kvq_rope.cuh"
 #include "kvq_tc_common.cuh"
 
 namespace kvq {
@@ -61,18 +62,37 @@ __device__ __forceinline__ Seg warp_seg(const TcArgs &a, const HeadCnt &hc, int 
 
 // OUT = 1: the extended kernel -- per-sequence lengths, the value queue and
 // outlier lists, each a run-time option; OUT = 0 compiles none of them.
-template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF, int OUT>
+// RP = 1: the rotary form (keys cached before RoPE; KIVI, key groups of 32 or
+// more, fp32 statistics, no options): key scores on the CUDA cores, one token
+// per lane, the rest as above.
+template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF, int OUT, int RP = 0>
 __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
+  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT, RP>;
+  static_assert(!RP || (SCHEME == KVQ_KIVI && KM <= 1 && MF == 0 && OUT == 0),
+                "the rotary form: KIVI, one key group per tile, fp32 statistics, no options");
   constexpr bool G16 = SCHEME == KVQ_KIVI && KM == 2;
   constexpr int RB = SC::RB;  // packed bytes per token row
   constexpr int nslot = SC::nslot;
   constexpr int SLOT = SC::bytes;
   const Geometry &g = a.g;
-  constexpr TcLayout Ly = tc_layout(SLOT, nslot, SC::SBB);
+  constexpr TcLayout Ly = tc_layout(SLOT, nslot, SC::SBB, SC::CSB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  // The rotary form's table: entry [L][j] = (cos j theta_2L, cos j theta_2L+1,
+  // sin j theta_2L, sin j theta_2L+1) for token offsets j < 32 (pair-pair L =
+  // channels 4L .. 4L + 3), built once by the block.
+  const float4 *cs_tab = reinterpret_cast<const float4 *>(smem);
+  if constexpr (RP != 0) {
+    float4 *tab = reinterpret_cast<float4 *>(smem);
+    for (int i = tid; i < 32 * 32; i += kThreads) {
+      const int L = i >> 5, j = i & 31;
+      const float2 r0 = rope_cos_sin((float)j, a.theta[2 * L], a.c1, a.c2, a.c3);
+      const float2 r1 = rope_cos_sin((float)j, a.theta[2 * L + 1], a.c1, a.c2, a.c3);
+      tab[i] = make_float4(r0.x, r1.x, r0.y, r1.y);
+    }
+    __syncthreads();
+  }
   uint8_t *wring = smem + Ly.ring + warp * nslot * SLOT;
   uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + Ly.bars) + warp * (nslot + 1);
   uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB + warp * SC::SBB);
@@ -301,6 +321,102 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     }
   };
 
+  // ---- the rotary form's key scores (RP) -------------------------------------
+  // Token t (lane t) of the tile at `slot`, token 0 at position tok0: with the
+  // anchor A = R(qpos - tok0) q, score = k_t . R(-t) A, and per channel pair
+  // (a, b) that is cos(t theta) X + sin(t theta) Y with X = k_a A_a + k_b A_b,
+  // Y = k_a A_b - k_b A_a (the rotation moved onto the query: RoPE rotations
+  // compose).  Lane L first writes the weights of its pair-pair L (channels
+  // 4L .. 4L + 3) into the warp's area, the dequantization k = code * scale +
+  // zero folded in; then every lane runs its own token through the 32
+  // pair-pairs, two pairs per packed instruction.  A code is read in place:
+  // masked inside its 16-bit half and OR-ed into the mantissa of 2^23, minus
+  // 2^23, the code at bit offset o reads as code * 2^o; the weights carry 2^-o.
+  auto rope_score = [&](const uint8_t *slot, int t, int tok0) -> float {
+    float4 *wt = reinterpret_cast<float4 *>(sBw);
+    auto pow2i = [](int e) { return __int_as_float((127 + e) << 23); };
+    {
+      const float delta0 = (float)(a.qpos - tok0);
+      const float2 r0 = rope_cos_sin(delta0, a.theta[2 * lane], a.c1, a.c2, a.c3);
+      const float2 r1 = rope_cos_sin(delta0, a.theta[2 * lane + 1], a.c1, a.c2, a.c3);
+      const float a0a = r0.x * q4[0] - r0.y * q4[1], a0b = r0.y * q4[0] + r0.x * q4[1];
+      const float a1a = r1.x * q4[2] - r1.y * q4[3], a1b = r1.y * q4[2] + r1.x * q4[3];
+      const float4 sc4 = reinterpret_cast<const float4 *>(slot + SC::off_km)[lane];
+      const float4 zr4 = reinterpret_cast<const float4 *>(slot + SC::off_km + kD * 4)[lane];
+      const int o = BITS == 2 ? 8 * (lane & 1) : 0;  // offset of channel 4L in its half
+      const float f0 = pow2i(-o), f1 = pow2i(-(o + BITS));
+      const float f2 = pow2i(-(o + 2 * BITS)), f3 = pow2i(-(o + 3 * BITS));
+      // [L]: X weights of the a channels (pairs 2L, 2L + 1), then of the b
+      // channels; [32 + L]: the same for Y; [64 + L]: the zeros' X, Y terms
+      wt[lane] = make_float4(sc4.x * a0a * f0, sc4.z * a1a * f2, sc4.y * a0b * f1, sc4.w * a1b * f3);
+      wt[32 + lane] =
+          make_float4(sc4.x * a0b * f0, sc4.z * a1b * f2, -(sc4.y * a0a) * f1, -(sc4.w * a1a) * f3);
+      wt[64 + lane] = make_float4(fmaf(zr4.x, a0a, zr4.y * a0b), fmaf(zr4.z, a1a, zr4.w * a1b),
+                                  fmaf(zr4.x, a0b, -(zr4.y * a0a)), fmaf(zr4.z, a1b, -(zr4.w * a1a)));
+      __syncwarp();
+    }
+    constexpr int NW = SC::RB / 4;  // code words of a token row
+    uint32_t wd[NW];
+    const uint4 *row = reinterpret_cast<const uint4 *>(slot + t * SC::RB);
+#pragma unroll
+    for (int v = 0; v < NW / 4; ++v) {
+      const uint4 x = row[v];
+      wd[4 * v] = x.x;
+      wd[4 * v + 1] = x.y;
+      wd[4 * v + 2] = x.z;
+      wd[4 * v + 3] = x.w;
+    }
+    constexpr uint32_t M = (1u << BITS) - 1u;
+    const uint32_t magic = 0x4B000000u;  // 2^23
+    const float2 unmagic = make_float2(-8388608.0f, -8388608.0f);
+    const float4 *cst = cs_tab + t;
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int L = 0; L < 32; ++L) {
+      const int bit0 = 4 * L * BITS;  // first bit of channel 4L in the row
+      const uint32_t w = wd[bit0 >> 5];
+      const uint32_t h = (bit0 & 16) ? (w >> 16) : w;
+      const int o = bit0 & 15;
+      const float2 u = __fadd2_rn(make_float2(__uint_as_float(and_or(h, M << o, magic)),
+                                              __uint_as_float(and_or(h, M << (o + 2 * BITS), magic))),
+                                  unmagic);  // channels 4L, 4L + 2
+      const float2 v = __fadd2_rn(make_float2(__uint_as_float(and_or(h, M << (o + BITS), magic)),
+                                              __uint_as_float(and_or(h, M << (o + 3 * BITS), magic))),
+                                  unmagic);  // channels 4L + 1, 4L + 3
+      const float4 wa = wt[L], wb = wt[32 + L], wz = wt[64 + L], c = cst[32 * L];
+      const float2 X = __ffma2_rn(u, make_float2(wa.x, wa.y),
+                                  __ffma2_rn(v, make_float2(wa.z, wa.w), make_float2(wz.x, wz.y)));
+      const float2 Y = __ffma2_rn(u, make_float2(wb.x, wb.y),
+                                  __ffma2_rn(v, make_float2(wb.z, wb.w), make_float2(wz.z, wz.w)));
+      acc = __ffma2_rn(make_float2(c.x, c.y), X, __ffma2_rn(make_float2(c.z, c.w), Y, acc));
+    }
+    return acc.x + acc.y;
+  };
+  // The rotary form's fp16 rows: row tt of the chunk that starts at fp16
+  // index i0 is the token at position n_quant + i0 + tt (KIVI keeps no
+  // sinks).  Each lane turns the query by R(qpos - position) on its channels
+  // 4 lane .. 4 lane + 3 and the warp sums; returns the score of row gid
+  // (rows past nv: 0).
+  auto rope_chunk_score = [&](const uint8_t *slot, int i0, int nv) -> float {
+    const float2 th0 = a.theta[2 * lane], th1 = a.theta[2 * lane + 1];
+    const uint2 *kr = reinterpret_cast<const uint2 *>(slot);
+    float sp = 0.0f;
+    for (int tt = 0; tt < nv; ++tt) {
+      const uint2 kw = kr[tt * (kD / 4) + lane];
+      const float2 k01 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.x));
+      const float2 k23 = __half22float2(*reinterpret_cast<const __half2 *>(&kw.y));
+      const float delta = (float)(a.qpos - ((int)a.n_quant + i0 + tt));
+      const float2 r0 = rope_cos_sin(delta, th0, a.c1, a.c2, a.c3);
+      const float2 r1 = rope_cos_sin(delta, th1, a.c1, a.c2, a.c3);
+      float x = fmaf(k01.x, r0.x * q4[0] - r0.y * q4[1], k01.y * (r0.y * q4[0] + r0.x * q4[1]));
+      x = fmaf(k23.x, r1.x * q4[2] - r1.y * q4[3], fmaf(k23.y, r1.y * q4[2] + r1.x * q4[3], x));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      sp = gid == tt ? x : sp;
+    }
+    return sp;
+  };
+
   // ---- per-warp online-softmax state ----------------------------------------
   float m_run = -INFINITY, l_lane = 0.0f, z_lane[NGV];
   float dv[8][4];
@@ -440,152 +556,158 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           constexpr bool FULL = decltype(full_c)::value;
           const uint8_t *kc = slot;
           const uint8_t *vc = slot + SC::off_vc;
-          // ------------- keys: two 16-token MMA tiles ------------------------
-          float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-          float bias0 = 0.0f, bias1 = 0.0f;
-          // key operand words of MMA k-block kb for key group gl (loaded next
-          // to their use to keep few registers live)
-          auto bk_at = [&](int gl, int kb) -> uint2 {
+          const int t = lane;
+          float score;
+          if constexpr (RP != 0) {
+            score = rope_score(slot, t, tok0);
+          } else {
+            // ------------- keys: two 16-token MMA tiles ------------------------
+            float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+            float bias0 = 0.0f, bias1 = 0.0f;
+            // key operand words of MMA k-block kb for key group gl (loaded next
+            // to their use to keep few registers live)
+            auto bk_at = [&](int gl, int kb) -> uint2 {
+              if (SCHEME == KVQ_KIVI) {
+                // lanes of columns >= 2 read the zero block: no divergent branch
+                const uint32_t *src = gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + SC::sb_zero;
+                return *reinterpret_cast<const uint2 *>(src + 2 * kb);
+              } else {
+                return make_uint2(bqi[kb][0], bqi[kb][1]);
+              }
+            };
+            bool two_groups = false;
             if (SCHEME == KVQ_KIVI) {
-              // lanes of columns >= 2 read the zero block: no divergent branch
-              const uint32_t *src = gid < 2 ? sBw + gl * 128 + (gid * 4 + tig) * 16 : sBw + SC::sb_zero;
-              return *reinterpret_cast<const uint2 *>(src + 2 * kb);
-            } else {
-              return make_uint2(bqi[kb][0], bqi[kb][1]);
+              // q~ = q * scale (normalised, position factor divided out) as fp16
+              // hi/lo in B-fragment order, and q . zero, per key group of the tile
+              const uint8_t *km = slot + SC::off_km;
+              two_groups = G16 && (FULL || n > 16);
+    #pragma unroll
+              for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
+                if (gl == 1 && !two_groups) break;
+                const uint8_t *ks = km + gl * 2 * kD * SC::MSZ, *kz = ks + kD * SC::MSZ;
+                const float2 s_lo = ld_stat2<MF>(ks, b_clo);
+                const float2 s_hi = ld_stat2<MF>(ks, b_clo + kHalf);
+                const float2 z_lo = ld_stat2<MF>(kz, b_clo);
+                const float2 z_hi = ld_stat2<MF>(kz, b_clo + kHalf);
+                uint32_t h0, l0, h1, l1;
+                split2(qn_lo[0] * s_lo.x, qn_hi[0] * s_hi.x, h0, l0);
+                split2(qn_lo[1] * s_lo.y, qn_hi[1] * s_hi.y, h1, l1);
+                *reinterpret_cast<uint2 *>(sBw + gl * 128 + b_sidx) = make_uint2(h0, h1);
+                *reinterpret_cast<uint2 *>(sBw + gl * 128 + 64 + b_sidx) = make_uint2(l0, l1);
+                float bz = fmaf(qf_lo[0], z_lo.x, fmaf(qf_hi[0], z_hi.x, fmaf(qf_lo[1], z_lo.y, qf_hi[1] * z_hi.y)));
+    #pragma unroll
+                for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
+                if (gl == 0) bias0 = bz;
+                bias1 = bz;
+              }
+              __syncwarp();
             }
-          };
-          bool two_groups = false;
-          if (SCHEME == KVQ_KIVI) {
-            // q~ = q * scale (normalised, position factor divided out) as fp16
-            // hi/lo in B-fragment order, and q . zero, per key group of the tile
-            const uint8_t *km = slot + SC::off_km;
-            two_groups = G16 && (FULL || n > 16);
-  #pragma unroll
-            for (int gl = 0; gl < (G16 ? 2 : 1); ++gl) {
-              if (gl == 1 && !two_groups) break;
-              const uint8_t *ks = km + gl * 2 * kD * SC::MSZ, *kz = ks + kD * SC::MSZ;
-              const float2 s_lo = ld_stat2<MF>(ks, b_clo);
-              const float2 s_hi = ld_stat2<MF>(ks, b_clo + kHalf);
-              const float2 z_lo = ld_stat2<MF>(kz, b_clo);
-              const float2 z_hi = ld_stat2<MF>(kz, b_clo + kHalf);
-              uint32_t h0, l0, h1, l1;
-              split2(qn_lo[0] * s_lo.x, qn_hi[0] * s_hi.x, h0, l0);
-              split2(qn_lo[1] * s_lo.y, qn_hi[1] * s_hi.y, h1, l1);
-              *reinterpret_cast<uint2 *>(sBw + gl * 128 + b_sidx) = make_uint2(h0, h1);
-              *reinterpret_cast<uint2 *>(sBw + gl * 128 + 64 + b_sidx) = make_uint2(l0, l1);
-              float bz = fmaf(qf_lo[0], z_lo.x, fmaf(qf_hi[0], z_hi.x, fmaf(qf_lo[1], z_lo.y, qf_hi[1] * z_hi.y)));
-  #pragma unroll
-              for (int off = 16; off > 0; off >>= 1) bz += __shfl_xor_sync(0xffffffffu, bz, off);
-              if (gl == 0) bias0 = bz;
-              bias1 = bz;
-            }
-            __syncwarp();
-          }
-          if (BITS == 2) {
-            const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
-            const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
-            const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
-            const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
-            if (!two_groups) {
-  #pragma unroll
-              for (int m = 0; m < 2; ++m) {
-                const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
-                const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
-                const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
-                const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
-  #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const uint2 b = bk_at(0, 4 * m + j);
-                  mma16816(d0, ext<2>(w00, s00, 2 * j), ext<2>(w01, s01, 2 * j),
-                           ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1), b.x, b.y);
-                  mma16816(d1, ext<2>(w10, s10, 2 * j), ext<2>(w11, s11, 2 * j),
-                           ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1), b.x, b.y);
+            if (BITS == 2) {
+              const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
+              const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
+              const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
+              const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
+              if (!two_groups) {
+    #pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                  const uint32_t w00 = m ? wa0.y : wa0.x, w01 = m ? wb0.y : wb0.x;
+                  const uint32_t w10 = m ? wa1.y : wa1.x, w11 = m ? wb1.y : wb1.x;
+                  const uint32_t s00 = shifted<2>(w00), s01 = shifted<2>(w01);
+                  const uint32_t s10 = shifted<2>(w10), s11 = shifted<2>(w11);
+    #pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const uint2 b = bk_at(0, 4 * m + j);
+                    mma16816(d0, ext<2>(w00, s00, 2 * j), ext<2>(w01, s01, 2 * j),
+                             ext<2>(w00, s00, 2 * j + 1), ext<2>(w01, s01, 2 * j + 1), b.x, b.y);
+                    mma16816(d1, ext<2>(w10, s10, 2 * j), ext<2>(w11, s11, 2 * j),
+                             ext<2>(w10, s10, 2 * j + 1), ext<2>(w11, s11, 2 * j + 1), b.x, b.y);
+                  }
+                }
+              } else {
+    #pragma unroll
+                for (int t2 = 0; t2 < 2; ++t2) {
+                  const uint2 wa = t2 ? wa1 : wa0, wb = t2 ? wb1 : wb0;
+    #pragma unroll
+                  for (int m = 0; m < 2; ++m) {
+                    const uint32_t w0 = m ? wa.y : wa.x, w1 = m ? wb.y : wb.x;
+                    const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
+    #pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                      const uint2 b = bk_at(t2, 4 * m + j);
+                      if (t2 == 0)
+                        mma16816(d0, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
+                                 ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
+                      else
+                        mma16816(d1, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
+                                 ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
+                    }
+                  }
                 }
               }
             } else {
-  #pragma unroll
+              // 4-bit keys: G >= 32 always gives one key group per tile here
+              // (the 4-bit group-16 case takes the same path with two groups)
+    #pragma unroll
               for (int t2 = 0; t2 < 2; ++t2) {
-                const uint2 wa = t2 ? wa1 : wa0, wb = t2 ? wb1 : wb0;
-  #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                  const uint32_t w0 = m ? wa.y : wa.x, w1 = m ? wb.y : wb.x;
-                  const uint32_t s0 = shifted<2>(w0), s1 = shifted<2>(w1);
-  #pragma unroll
-                  for (int j = 0; j < 4; ++j) {
-                    const uint2 b = bk_at(t2, 4 * m + j);
+                const int gl = two_groups ? t2 : 0;
+                const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid) * RB + 16 * tig);
+                const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid + 8) * RB + 16 * tig);
+                const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
+    #pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                  const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
+    #pragma unroll
+                  for (int j = 0; j < 2; ++j) {
+                    const uint2 b = bk_at(gl, 2 * m + j);
                     if (t2 == 0)
-                      mma16816(d0, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
+                      mma16816(d0, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
+                               ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
                     else
-                      mma16816(d1, ext<2>(w0, s0, 2 * j), ext<2>(w1, s1, 2 * j),
-                               ext<2>(w0, s0, 2 * j + 1), ext<2>(w1, s1, 2 * j + 1), b.x, b.y);
+                      mma16816(d1, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
+                               ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
                   }
                 }
               }
             }
-          } else {
-            // 4-bit keys: G >= 32 always gives one key group per tile here
-            // (the 4-bit group-16 case takes the same path with two groups)
-  #pragma unroll
-            for (int t2 = 0; t2 < 2; ++t2) {
-              const int gl = two_groups ? t2 : 0;
-              const uint4 wa = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid) * RB + 16 * tig);
-              const uint4 wb = *reinterpret_cast<const uint4 *>(kc + (16 * t2 + gid + 8) * RB + 16 * tig);
-              const uint32_t A0[4] = {wa.x, wa.y, wa.z, wa.w}, A1[4] = {wb.x, wb.y, wb.z, wb.w};
-  #pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                const uint32_t s0 = shifted<4>(A0[m]), s1 = shifted<4>(A1[m]);
-  #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  const uint2 b = bk_at(gl, 2 * m + j);
-                  if (t2 == 0)
-                    mma16816(d0, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
-                  else
-                    mma16816(d1, ext<4>(A0[m], s0, 2 * j), ext<4>(A1[m], s1, 2 * j),
-                             ext<4>(A0[m], s0, 2 * j + 1), ext<4>(A1[m], s1, 2 * j + 1), b.x, b.y);
-                }
+            // ------------- scores -> one token per lane ------------------------
+            float ra0, rb0, ra1, rb1;
+            if (SCHEME == KVQ_KIVI) {
+              ra0 = d0[0] + d0[1];
+              rb0 = d0[2] + d0[3];
+              ra1 = d1[0] + d1[1];
+              rb1 = d1[2] + d1[3];
+            } else {
+              const uint8_t *ks = slot + SC::off_ks;
+              const uint8_t *kz = slot + SC::off_kz;
+              const int jj = tig < NGK ? tig : NGK - 1;
+              float qj = Qj[0];
+    #pragma unroll
+              for (int j = 1; j < NGK; ++j)
+                if (j == jj) qj = Qj[j];
+              auto term = [&](int row, float dd) {
+                return fmaf(ld_stat<MF>(ks, row * NGK + jj), dd * pow2E,
+                            ld_stat<MF>(kz, row * NGK + jj) * qj);
+              };
+              ra0 = term(gid, d0[0] + d0[1]);
+              rb0 = term(gid + 8, d0[2] + d0[3]);
+              ra1 = term(gid + 16, d1[0] + d1[1]);
+              rb1 = term(gid + 24, d1[2] + d1[3]);
+              if (tig >= NGK) ra0 = rb0 = ra1 = rb1 = 0.0f;
+    #pragma unroll
+              for (int off = 1; off < NGK; off <<= 1) {
+                ra0 += __shfl_xor_sync(0xffffffffu, ra0, off);
+                rb0 += __shfl_xor_sync(0xffffffffu, rb0, off);
+                ra1 += __shfl_xor_sync(0xffffffffu, ra1, off);
+                rb1 += __shfl_xor_sync(0xffffffffu, rb1, off);
               }
             }
+          
+            const int src = 4 * (t & 7);
+            const float xa0 = __shfl_sync(0xffffffffu, ra0, src), xb0 = __shfl_sync(0xffffffffu, rb0, src);
+            const float xa1 = __shfl_sync(0xffffffffu, ra1, src), xb1 = __shfl_sync(0xffffffffu, rb1, src);
+            score = t < 16 ? ((t & 8) ? xb0 : xa0) : ((t & 8) ? xb1 : xa1);
+            if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
           }
-          // ------------- scores -> one token per lane ------------------------
-          float ra0, rb0, ra1, rb1;
-          if (SCHEME == KVQ_KIVI) {
-            ra0 = d0[0] + d0[1];
-            rb0 = d0[2] + d0[3];
-            ra1 = d1[0] + d1[1];
-            rb1 = d1[2] + d1[3];
-          } else {
-            const uint8_t *ks = slot + SC::off_ks;
-            const uint8_t *kz = slot + SC::off_kz;
-            const int jj = tig < NGK ? tig : NGK - 1;
-            float qj = Qj[0];
-  #pragma unroll
-            for (int j = 1; j < NGK; ++j)
-              if (j == jj) qj = Qj[j];
-            auto term = [&](int row, float dd) {
-              return fmaf(ld_stat<MF>(ks, row * NGK + jj), dd * pow2E,
-                          ld_stat<MF>(kz, row * NGK + jj) * qj);
-            };
-            ra0 = term(gid, d0[0] + d0[1]);
-            rb0 = term(gid + 8, d0[2] + d0[3]);
-            ra1 = term(gid + 16, d1[0] + d1[1]);
-            rb1 = term(gid + 24, d1[2] + d1[3]);
-            if (tig >= NGK) ra0 = rb0 = ra1 = rb1 = 0.0f;
-  #pragma unroll
-            for (int off = 1; off < NGK; off <<= 1) {
-              ra0 += __shfl_xor_sync(0xffffffffu, ra0, off);
-              rb0 += __shfl_xor_sync(0xffffffffu, rb0, off);
-              ra1 += __shfl_xor_sync(0xffffffffu, ra1, off);
-              rb1 += __shfl_xor_sync(0xffffffffu, rb1, off);
-            }
-          }
-          const int t = lane;
-          const int src = 4 * (t & 7);
-          const float xa0 = __shfl_sync(0xffffffffu, ra0, src), xb0 = __shfl_sync(0xffffffffu, rb0, src);
-          const float xa1 = __shfl_sync(0xffffffffu, ra1, src), xb1 = __shfl_sync(0xffffffffu, rb1, src);
-          float score = t < 16 ? ((t & 8) ? xb0 : xa0) : ((t & 8) ? xb1 : xa1);
-          if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
           const bool valid = FULL || t < n;
           if (OUT && valid) {
             // dense-and-sparse keys: an outlier's code is 0, so the dense score
@@ -802,7 +924,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         // rows 8..15 zero), B = the query operand; rows past the chunk's valid
         // ones are masked below.  Lane (gid, 0) ends with token gid's score.
         float sp;
-        {
+        if constexpr (RP != 0) {
+          sp = rope_chunk_score(slot, i0, nv);
+        } else {
           const uint2 *ka = reinterpret_cast<const uint2 *>(slot + gid * kD * 2) + tig;
           const uint32_t *bq = gid < 2 ? sBw + (gid * 4 + tig) * 16 : sBw + SC::sb_zero;
           float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -864,10 +988,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   }
 }
 
-template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF, int OUT>
+template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF, int OUT, int RP = 0>
 cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
-  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
-  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM, MF, OUT>;
+  using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT, RP>;
+  auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM, MF, OUT, RP>;
   constexpr int smem = SC::smem;
   const bool ext = a.g.n_out > 0 || a.g.vq || a.g.ragged;
   if (a.g.meta16 != MF || ext != (OUT != 0)) return cudaErrorInvalidValue;

@@ -50,7 +50,6 @@ constexpr int kSub = 32;                // tokens per sub-tile: one per lane
 constexpr int kRChunkMin = 128;         // quantized tokens per split: at least this
 constexpr int kRChunkCap = 2048;        // ... and at most this
 constexpr int kRBlockFixed = 128;       // a block's fixed work, in token-equivalents
-constexpr float kInvTwoPi = 0.15915494309189535f;
 
 struct RopeArgs {
   Geometry g;
@@ -94,16 +93,7 @@ __host__ __device__ inline RSmem rope_smem(int D, int RG, int NGS, int sc_max) {
 
 // cos and sin of delta * theta (delta a non-negative integer below 2^24).
 __device__ __forceinline__ float2 rope_cs(float delta, float2 th, const RopeArgs &a) {
-  const float p = __fmul_rn(delta, th.x);
-  const float e = fmaf(delta, th.x, -p) + delta * th.y;  // p + e = delta * theta
-  const float k = rintf(p * kInvTwoPi);
-  float r = fmaf(-k, a.c1, p);
-  r = fmaf(-k, a.c2, r);
-  r = fmaf(-k, a.c3, r);
-  r += e;
-  float s, c;
-  __sincosf(r, &s, &c);
-  return make_float2(c, s);
+  return rope_cos_sin(delta, th, a.c1, a.c2, a.c3);
 }
 
 // x < 2^16: its value as a float, exactly.
@@ -589,15 +579,7 @@ cudaError_t launch_decode_rope(const Geometry &g, const CachePtrs &p, int64_t n_
   a.s_max = part_slots(g);
   a.sc_max = kRChunkCap > g.residual + g.n_sink ? kRChunkCap : g.residual + g.n_sink;
   // theta_i = base^(-2i/d) as hi + lo; 2 pi in three parts
-  for (int i = 0; i < g.d / 2; ++i) {
-    const double th = pow(rope_base, -2.0 * i / g.d);
-    const float hi = (float)th;
-    a.theta[i] = make_float2(hi, (float)(th - (double)hi));
-  }
-  const double two_pi = 2.0 * M_PI;
-  a.c1 = (float)two_pi;
-  a.c2 = (float)(two_pi - (double)a.c1);
-  a.c3 = (float)(two_pi - (double)a.c1 - (double)a.c2);
+  rope_constants(rope_base, g.d, a.theta, a.c1, a.c2, a.c3);
   // workspace: counters, then (m, l) and o rows (the general decode layout)
   const int64_t parts = BH * a.s_max * rg;
   char *base = static_cast<char *>(ws);

@@ -39,7 +39,18 @@ struct TcArgs {
   int stall_limit;  // debug: > 0 = first wait on a barrier nothing completes
   int64_t n_vq;     // values held quantized (the value queue's count; else n_quant)
   int CH;           // fp16 tokens per chunk (tc_fp16_chunk)
+  // keys cached before RoPE (the rotary form of the MHA kernel only): the
+  // query's position, 2 pi = c1 + c2 + c3, theta_i = theta[i].x + .y
+  int qpos;
+  float c1, c2, c3;
+  float2 theta[64];
 };
+
+// Common arguments of the MHA tensor-core decode (work split, workspace);
+// k_new / v_new: a fused append's rows, or null.
+cudaError_t tc_fill_args(TcArgs &a, const Geometry &g, const CachePtrs &p, int64_t n_quant,
+                         int64_t n_resid, int64_t n_sink, const __half *q, float *out, float scale,
+                         void *ws, const __half *k_new, const __half *v_new);
 
 // The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), and the
 // extended one (outlier lists, the value queue, per-sequence lengths), each
@@ -69,9 +80,12 @@ struct TcLayout {
   int ring, sB, bars, total;
 };
 
-__host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int sb_bytes) {
+// pre: bytes the block keeps ahead of the rings (the rotary form's cos / sin
+// table)
+__host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int sb_bytes,
+                                                 int pre = 0) {
   TcLayout L{};
-  L.ring = 0;
+  L.ring = pre;
   L.sB = L.ring + kWarps * nslot * slot_bytes;  // per warp: key operand + zero block
   L.bars = L.sB + kWarps * sb_bytes;            // per warp: nslot + 1 mbarriers
   L.total = L.bars + kWarps * (nslot + 1) * 8;
@@ -94,8 +108,12 @@ __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int 
 // time: the slot reserves room for the largest, and the per-warp area adds
 // the query in the score domain and the outliers' value corrections (128
 // floats each).
+// RP (the rotary form, keys cached before RoPE): the key scores run on the
+// CUDA cores, so the per-warp area holds the tile's per-pair key weights
+// (3 x 32 float4) instead of the key operand, and the block keeps a 32 x 32
+// float4 table of cos / sin ahead of the rings.
 constexpr int kMaxOutliers = 8;
-template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF = 0, int OUT = 0>
+template <int BITS, int SCHEME, int NGV, int NGK, int KM, int MF = 0, int OUT = 0, int RP = 0>
 struct SlotCfg {
   static constexpr int MSZ = MF ? 2 : 4;
   static constexpr int RB = kD * BITS / 8;
@@ -115,12 +133,13 @@ struct SlotCfg {
   static constexpr int CH = off_q / (4 * kD) < 8 ? off_q / (4 * kD) : 8;  // fp16 tokens per chunk
   // per warp: KIVI key operand (512 B per group; also the 512 B output
   // transpose at a head's end), the outlier extras, 64 zero bytes
-  static constexpr int SBO = (SCHEME == KVQ_KIVI && KM == 2 ? 1024 : 512);
+  static constexpr int SBO = RP ? 3 * 32 * 16 : (SCHEME == KVQ_KIVI && KM == 2 ? 1024 : 512);
   static constexpr int SBB = SBO + (OUT ? 1024 : 0) + 64;
   static constexpr int sb_xtra = SBO / 4;       // word offset of the extras (OUT)
   static constexpr int sb_zero = SBB / 4 - 16;  // word offset of the zero block
-  static constexpr int nslot = tc_layout(bytes, 3, SBB).total <= 112 * 1024 ? 3 : 2;
-  static constexpr int smem = tc_layout(bytes, nslot, SBB).total;
+  static constexpr int CSB = RP ? 32 * 32 * 16 : 0;  // the rotary form's cos / sin table
+  static constexpr int nslot = tc_layout(bytes, 3, SBB, CSB).total <= 112 * 1024 ? 3 : 2;
+  static constexpr int smem = tc_layout(bytes, nslot, SBB, CSB).total;
 };
 
 // Stored statistics as fp32: element i of a row at `base`, the pair (i, i +
@@ -245,6 +264,13 @@ template <int BITS>
 __device__ __forceinline__ uint32_t ext(uint32_t w, uint32_t ws, int p) {
   if (BITS == 2) return p <= 4 ? (w & (0x00030003u << (2 * p))) : (ws & (0x00030003u << (2 * (p - 5))));
   return p <= 1 ? (w & (0x000F000Fu << (4 * p))) : (ws & (0x000F000Fu << (4 * (p - 2))));
+}
+
+// (x & m) | c in one instruction.
+__device__ __forceinline__ uint32_t and_or(uint32_t x, uint32_t m, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(x), "r"(m), "r"(c));
+  return d;
 }
 
 template <int BITS>

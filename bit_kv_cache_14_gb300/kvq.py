@@ -38,7 +38,7 @@ EXPORTS = (
     "kvq_decode_attention", "kvq_decode_step_host", "kvq_get_device_status",
     "kvq_last_launch_count", "kvq_strerror", "kvq_debug_stall_waits",
     "kvq_decode_attention_noalloc", "kvq_append_decode", "kvq_decode_attention_rope",
-    "kvq_decode_kernel_name", "kvq_quantize_prefill_ragged",
+    "kvq_decode_kernel_name", "kvq_quantize_prefill_ragged", "kvq_rope_kernel_name",
 )
 
 
@@ -99,6 +99,7 @@ def lib():
             L.kvq_append_decode.argtypes = [C, CA, P, P, P, P, ctypes.c_float, P,
                                             ctypes.c_size_t, P]
             L.kvq_decode_kernel_name.argtypes = [C, I64, ctypes.c_char_p, ctypes.c_size_t]
+            L.kvq_rope_kernel_name.argtypes = [C, I64, ctypes.c_char_p, ctypes.c_size_t]
             L.kvq_get_device_status.argtypes = [CA, P]
             L.kvq_last_launch_count.argtypes = []
             L.kvq_debug_stall_waits.argtypes = [ctypes.c_int64]
@@ -145,6 +146,15 @@ def decode_kernel_name(cfg: Config, n_quant: int) -> str:
     buf = ctypes.create_string_buffer(128)
     _check(lib().kvq_decode_kernel_name(ctypes.byref(cfg), int(n_quant), buf, len(buf)),
            "kvq_decode_kernel_name")
+    return buf.value.decode()
+
+
+def rope_kernel_name(cfg: Config, n_quant: int) -> str:
+    """The kernel kvq_decode_attention_rope launches for this configuration
+    with n_quant quantized tokens (host only)."""
+    buf = ctypes.create_string_buffer(128)
+    _check(lib().kvq_rope_kernel_name(ctypes.byref(cfg), int(n_quant), buf, len(buf)),
+           "kvq_rope_kernel_name")
     return buf.value.decode()
 
 

@@ -384,6 +384,13 @@ void kvq_debug_stall_waits(int64_t iterations);
  * KVQ_OK, KVQ_EINVAL (null, n_quant < 0, buf too small) or a config error. */
 int kvq_decode_kernel_name(const kvq_config *cfg, int64_t n_quant, char *buf, size_t len);
 
+/* The same for kvq_decode_attention_rope (e.g.
+ * "tc_decode_kernel<bits=2,scheme=kivi,ngv=4,km=1,rope=1>": the tensor-core
+ * form, taken for head_dim 128, one query head per KV head, KIVI with key
+ * groups of 32 or more and no cache options; other shapes name
+ * "rope_decode_kernel<...>").  Host only, no CUDA call; same returns. */
+int kvq_rope_kernel_name(const kvq_config *cfg, int64_t n_quant, char *buf, size_t len);
+
 /* Number of kernel launches the last successful call of this thread enqueued. */
 int kvq_last_launch_count(void);
 

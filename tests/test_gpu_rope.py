@@ -50,6 +50,19 @@ CASES = {
                                n_append=40),
 }
 
+# the tensor-core form: every instantiation (bits x value groups x key
+# statistics inside the block (G 32) or beside it (G 64)), ragged residuals,
+# flushes between the decodes
+TC_CASES = {}
+for _bits in (2, 4):
+    for _ngv in (2, 4):
+        for _g in (32, 64):
+            TC_CASES["tc_b%d_ngv%d_g%d" % (_bits, _ngv, _g)] = S(
+                W["llama2_7b_2bit"] if _bits == 2 else W["kivi_4bit"], batch=2, n_q_heads=2,
+                n_kv_heads=2, ctx=700, k_group=_g, v_group=128 // _ngv, residual=64,
+                n_append=74)
+CASES.update(TC_CASES)
+
 
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_rope_small_workload_all_heads(name):

@@ -116,3 +116,26 @@ def test_instantiation_matches_oracle(name):
     w = CASES[name]
     worst = run_workload(w, decode_every=max(1, w.n_append // 4))
     assert worst <= ATOL
+
+
+def test_every_rotary_instantiation_has_a_parity_case():
+    """The tensor-core form of the decode over keys cached before RoPE: every
+    instantiation a valid configuration reaches is one of the rotary parity
+    cases in test_gpu_rope.py, and the other shapes name the general kernel."""
+    import test_gpu_rope
+    dispatched = set()
+    for d, bits, rg, gk, gv in itertools.product((64, 128), (2, 4), (1, 2, 4), (16, 32, 64, 128),
+                                                 (16, 32, 64, 128)):
+        if gv > d:
+            continue
+        for fl in (0, kvq.META_F16):
+            cfg = kvq.make_config(2, 2 * rg, 2, d, bits, kvq.KIVI, gk, gv, 128, 0, 4096, fl)
+            name = kvq.rope_kernel_name(cfg, 1)
+            if name.startswith("tc_"):
+                dispatched.add(name)
+                assert d == 128 and rg == 1 and gk >= 32 and not fl, name
+            else:
+                assert name.startswith("rope_decode_kernel<"), name
+    assert len(dispatched) == 8, sorted(dispatched)
+    covered = {kvq.rope_kernel_name(kvq.config_of(w), 1) for w in test_gpu_rope.TC_CASES.values()}
+    assert dispatched == covered, sorted(dispatched ^ covered)
