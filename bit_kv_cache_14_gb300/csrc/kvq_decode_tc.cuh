@@ -370,9 +370,21 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     const uint32_t magic = 0x4B000000u;  // 2^23
     const float2 unmagic = make_float2(-8388608.0f, -8388608.0f);
     const float4 *cst = cs_tab + t;
-    float2 acc = make_float2(0.0f, 0.0f);
+    // four independent accumulators (pair-pairs L mod 4) keep the dependent
+    // chains short; each step's shared loads are issued a step ahead
+    float2 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.0f, 0.0f);
+    float4 wa = wt[0], wb = wt[32], wz = wt[64], c = cst[0];
 #pragma unroll
     for (int L = 0; L < 32; ++L) {
+      float4 wa_n, wb_n, wz_n, c_n;
+      if (L + 1 < 32) {
+        wa_n = wt[L + 1];
+        wb_n = wt[33 + L];
+        wz_n = wt[65 + L];
+        c_n = cst[32 * (L + 1)];
+      }
       const int bit0 = 4 * L * BITS;  // first bit of channel 4L in the row
       const uint32_t w = wd[bit0 >> 5];
       const uint32_t h = (bit0 & 16) ? (w >> 16) : w;
@@ -383,14 +395,20 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       const float2 v = __fadd2_rn(make_float2(__uint_as_float(and_or(h, M << (o + BITS), magic)),
                                               __uint_as_float(and_or(h, M << (o + 3 * BITS), magic))),
                                   unmagic);  // channels 4L + 1, 4L + 3
-      const float4 wa = wt[L], wb = wt[32 + L], wz = wt[64 + L], c = cst[32 * L];
       const float2 X = __ffma2_rn(u, make_float2(wa.x, wa.y),
                                   __ffma2_rn(v, make_float2(wa.z, wa.w), make_float2(wz.x, wz.y)));
       const float2 Y = __ffma2_rn(u, make_float2(wb.x, wb.y),
                                   __ffma2_rn(v, make_float2(wb.z, wb.w), make_float2(wz.z, wz.w)));
-      acc = __ffma2_rn(make_float2(c.x, c.y), X, __ffma2_rn(make_float2(c.z, c.w), Y, acc));
+      acc[L & 3] = __ffma2_rn(make_float2(c.x, c.y), X, __ffma2_rn(make_float2(c.z, c.w), Y, acc[L & 3]));
+      if (L + 1 < 32) {
+        wa = wa_n;
+        wb = wb_n;
+        wz = wz_n;
+        c = c_n;
+      }
     }
-    return acc.x + acc.y;
+    const float2 s01 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+    return s01.x + s01.y;
   };
   // The rotary form's fp16 rows: row tt of the chunk that starts at fp16
   // index i0 is the token at position n_quant + i0 + tt (KIVI keeps no
