@@ -172,6 +172,7 @@ DECODE_SOURCES = ("kvq_decode_tc.cuh", "kvq_decode_tc.cu", "kvq_tc_common.cuh", 
                   "kvq_internal.cuh")
 ROPE_SOURCES = ("kvq_decode_tc.cuh", "kvq_decode_tc_rope.cu", "kvq_tc_common.cuh", "kvq_rope.cuh",
                 "kvq_internal.cuh")
+GQA_SOURCES = ("kvq_decode_gqa.cu", "kvq_tc_common.cuh", "kvq_internal.cuh")
 
 
 def decode_source_sha(names=DECODE_SOURCES):
@@ -194,7 +195,7 @@ def decode_kernel_name(w, rope=False):
     return name.split("<")[0]
 
 
-def profiled_traffic(workload, per_launch_units, rope=False):
+def profiled_traffic(workload, per_launch_units, rope=False, kernel="tc_decode_kernel"):
     """DRAM bytes per decode launch from the committed ncu summary, or None when
     the kernel source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", ("decode_rope_%s.md" if rope else "decode_%s.md")
@@ -205,8 +206,9 @@ def profiled_traffic(workload, per_launch_units, rope=False):
         return None
     sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
     tb = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not sha or not tb or sha.group(1) != decode_source_sha(ROPE_SOURCES if rope
-                                                             else DECODE_SOURCES):
+    sources = (ROPE_SOURCES if rope else GQA_SOURCES if kernel == "tc_gqa_kernel"
+               else DECODE_SOURCES)
+    if not sha or not tb or sha.group(1) != decode_source_sha(sources):
         return None
     return float(tb.group(1))
 
@@ -892,7 +894,7 @@ def main():
     value = whole_job_gbs(r["total_bytes"], world, elapsed_ms)
     decode_gbs = r["dstate_bytes"] / (r["decode_ms"] * 1e-3) / 1e9
     rope = args.rope_base is not None
-    traffic = profiled_traffic(w.name, 1, rope=rope)
+    traffic = profiled_traffic(w.name, 1, rope=rope, kernel=decode_kernel_name(w, rope))
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": r["warmup_steps"], "ms_per_step": elapsed_ms / args.steps,
