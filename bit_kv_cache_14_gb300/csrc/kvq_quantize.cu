@@ -717,14 +717,24 @@ __global__ void __launch_bounds__(kQuantBlock)
 // statistics and reciprocals, and a second pass over the same rows (L1 hits)
 // packs the codes.  With outliers each row's are found by the 16 (or 8) lanes
 // of its slice, listed in the first pass, and found again in the second.
-template <int D, int BITS>
+// GT > 0 (the group size, 16 or 32, known at compile time; no outliers): each
+// lane issues the loads of all its rows at once for the first pass, so a warp
+// has the whole group in flight; the second pass reads them again from L1.
+template <int D, int BITS, int GT = 0>
 __device__ __forceinline__ void key_group_warp(const Geometry &g, const CachePtrs &p, int64_t bh,
                                                const __half *src, int64_t t0) {
   constexpr int CH = D / 8, RL = 32 / CH;
+  constexpr int NR = GT > 0 ? GT / RL : 1;  // rows a lane holds (GT > 0)
   const int lane = threadIdx.x & 31, j = lane % CH, rs = lane / CH;
-  const int G = g.k_group;
+  const int G = GT > 0 ? GT : g.k_group;
+  uint4 held[NR];
+  if constexpr (GT > 0) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      held[r] = *reinterpret_cast<const uint4 *>(src + (int64_t)(rs + r * RL) * D + 8 * j);
+  }
   float mn[8], mx[8];
-  if (g.n_out == 0) {
+  if (GT > 0 || g.n_out == 0) {
     // raw fp16 keys: the minimum and maximum on half2 pairs (exact)
     __half2 hmn[4], hmx[4];
 #pragma unroll
@@ -732,14 +742,20 @@ __device__ __forceinline__ void key_group_warp(const Geometry &g, const CachePtr
       hmn[e] = __float2half2_rn(INFINITY);
       hmx[e] = __float2half2_rn(-INFINITY);
     }
-    for (int i = rs; i < G; i += RL) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(src + (int64_t)i * D + 8 * j);
+    auto fold = [&](const uint4 &raw) {
       const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         hmn[e] = __hmin2(hmn[e], h[e]);
         hmx[e] = __hmax2(hmx[e], h[e]);
       }
+    };
+    if constexpr (GT > 0) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) fold(held[r]);
+    } else {
+      for (int i = rs; i < G; i += RL)
+        fold(*reinterpret_cast<const uint4 *>(src + (int64_t)i * D + 8 * j));
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -821,7 +837,7 @@ __device__ __forceinline__ void key_group_warp(const Geometry &g, const CachePtr
   for (int i = rs; i < G; i += RL) {
     float x[8];
     load8(src + (int64_t)i * D + 8 * j, x);
-    const uint32_t om = g.n_out > 0 ? outlier_mask(x, j, CH, g.n_out) : 0u;
+    const uint32_t om = GT == 0 && g.n_out > 0 ? outlier_mask(x, j, CH, g.n_out) : 0u;
     float tie = 0.0f;
     uint32_t w = 0;
 #pragma unroll
@@ -845,7 +861,7 @@ __device__ __forceinline__ void key_group_warp(const Geometry &g, const CachePtr
 }
 
 // Prefill, KIVI keys: one warp per (head, G-token group), 8 warps a block.
-template <int D, int BITS>
+template <int D, int BITS, int GT>
 __global__ void __launch_bounds__(kQuantBlock)
     kivi_key_prefill_kernel(Geometry g, CachePtrs p, const __half *K, int64_t T, Counts uni,
                             int64_t groups_per_head) {
@@ -854,7 +870,7 @@ __global__ void __launch_bounds__(kQuantBlock)
   const int64_t bh = gi / groups_per_head;
   const int64_t t0 = (gi - bh * groups_per_head) * g.k_group;
   if (t0 >= seq_counts(g, p, uni, (int)(bh / g.H)).n_quant) return;  // (ragged: shorter)
-  key_group_warp<D, BITS>(g, p, bh, K + (bh * T + t0) * D, t0);
+  key_group_warp<D, BITS, GT>(g, p, bh, K + (bh * T + t0) * D, t0);
 }
 
 // fp16 rows of a prefill, every head: blockIdx.z = 0 the residual / window
@@ -1089,10 +1105,19 @@ cudaError_t launch_prefill(const Geometry &g, const CachePtrs &p, const __half *
       const int64_t gph = c.n_quant / g.k_group;
       const int64_t warps = BH * gph, per = kQuantBlock / 32;
       const unsigned blocks = (unsigned)((warps + per - 1) / per);
-      auto kern = g.d == 64 ? (g.bits == 2 ? kivi_key_prefill_kernel<64, 2>
-                                           : kivi_key_prefill_kernel<64, 4>)
-                            : (g.bits == 2 ? kivi_key_prefill_kernel<128, 2>
-                                           : kivi_key_prefill_kernel<128, 4>);
+      // groups of 16 or 32 tokens without outliers: the register-resident form
+      const int gt = g.n_out > 0 ? 0 : g.k_group == 32 ? 32 : g.k_group == 16 ? 16 : 0;
+      auto pick = [&](auto d_c, auto b_c) {
+        constexpr int D = decltype(d_c)::value, B = decltype(b_c)::value;
+        return gt == 32 ? kivi_key_prefill_kernel<D, B, 32>
+             : gt == 16 ? kivi_key_prefill_kernel<D, B, 16> : kivi_key_prefill_kernel<D, B, 0>;
+      };
+      using I64 = std::integral_constant<int, 64>;
+      using I128 = std::integral_constant<int, 128>;
+      using B2 = std::integral_constant<int, 2>;
+      using B4 = std::integral_constant<int, 4>;
+      auto kern = g.d == 64 ? (g.bits == 2 ? pick(I64{}, B2{}) : pick(I64{}, B4{}))
+                            : (g.bits == 2 ? pick(I128{}, B2{}) : pick(I128{}, B4{}));
       kern<<<blocks, kQuantBlock, 0, st>>>(g, p, K, T, c, gph);
       ++n;
     }
