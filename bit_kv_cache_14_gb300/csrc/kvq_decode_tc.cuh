@@ -795,17 +795,30 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           }
           if (OUT && vq_from < n) {
             // (warp-uniform) the tile's value-queue tokens: p_t * v_t from their
-            // fp16 ring rows, on CUDA cores
-            for (int tt = max(vq_from, 0); tt < n; ++tt) {
-              const float pt = __shfl_sync(0xffffffffu, p, tt);
-              const int64_t slot_v = ((int64_t)bh * g.residual + (tok0 + tt) % g.residual) * kD;
-              const uint2 vw = reinterpret_cast<const uint2 *>(a.p.v_res + slot_v)[lane];
-              const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.x));
-              const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw.y));
-              xv[0] = fmaf(pt, v01.x, xv[0]);
-              xv[1] = fmaf(pt, v01.y, xv[1]);
-              xv[2] = fmaf(pt, v23.x, xv[2]);
-              xv[3] = fmaf(pt, v23.y, xv[3]);
+            // fp16 ring rows (slot t mod R), on CUDA cores, in token order; the
+            // rows of four tokens are loaded before their products
+            const int t_first = max(vq_from, 0);
+            const uint2 *ring = reinterpret_cast<const uint2 *>(a.p.v_res + (int64_t)bh * g.residual * kD);
+            int rs = (int)((tok0 + t_first) % g.residual);
+            for (int tt0 = t_first; tt0 < n; tt0 += 4) {
+              uint2 vw[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                vw[u] = tt0 + u < n ? ring[(int64_t)rs * (kD / 4) + lane] : make_uint2(0u, 0u);
+                rs = rs + 1 == g.residual ? 0 : rs + 1;
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float pt = __shfl_sync(0xffffffffu, p, (tt0 + u) & 31);
+                if (tt0 + u < n) {
+                  const float2 v01 = __half22float2(*reinterpret_cast<const __half2 *>(&vw[u].x));
+                  const float2 v23 = __half22float2(*reinterpret_cast<const __half2 *>(&vw[u].y));
+                  xv[0] = fmaf(pt, v01.x, xv[0]);
+                  xv[1] = fmaf(pt, v01.y, xv[1]);
+                  xv[2] = fmaf(pt, v23.x, xv[2]);
+                  xv[3] = fmaf(pt, v23.y, xv[3]);
+                }
+              }
             }
           }
           // ------------- values: B = p * scale (hi/lo), A = codes ------------
