@@ -60,6 +60,111 @@ __device__ __forceinline__ Seg warp_seg(const TcArgs &a, const HeadCnt &hc, int 
   return s;
 }
 
+// Per-sequence lengths (the extended kernel): every head holds only its own
+// sequence's tiles and chunks -- kHeadUnits empty units, S quantized tiles,
+// F = chunks * UPC fp16 units -- heads in batch order, so the warps' equal
+// ranges are equal work (with the uniform layout every head would take the
+// longest sequence's units).  A head's first unit is a prefix sum over the
+// batch that each warp takes itself (ragged_locate); its span follows from
+// that and its counters.
+struct HeadSpan {
+  int base, U, S, F;
+};
+
+template <int EXT>
+__device__ __forceinline__ HeadSpan span_at(const TcArgs &a, int base, const HeadCnt &hc) {
+  if (!EXT) return HeadSpan{base, a.U, a.S_h, a.F_h};
+  const int S = (hc.nq + kTile - 1) / kTile, F = (hc.nf + a.CH - 1) / a.CH * a.UPC;
+  return HeadSpan{base, a.HU + S + F, S, F};
+}
+
+// Units of one head of sequence b.
+__device__ __forceinline__ int seq_units(const TcArgs &a, int b) {
+  const Counts c = counts_of(a.g, a.p.seq_prompt[b], a.p.appended);
+  return a.HU + (int)((c.n_quant + kTile - 1) / kTile) +
+         (int)((c.n_resid + c.n_sink + a.CH - 1) / a.CH) * a.UPC;
+}
+
+// Run by the whole warp: the units of every head (`total`) and, for x >= 0,
+// the head bh that holds unit x and its first unit (returned).
+__device__ int ragged_locate(const TcArgs &a, int x, int &bh, int &total) {
+  const int lane = threadIdx.x & 31, B = a.g.B, H = a.g.H;
+  int base = 0;
+  bh = -1;
+  int acc = 0;  // units of the sequences before this round
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    const int uh = b < B ? seq_units(a, b) : 0;
+    const int ub = H * uh;  // units of sequence b, all its heads
+    int inc = ub;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    const int tot = __shfl_sync(0xffffffffu, inc, 31);
+    if (bh < 0 && x >= acc && x < acc + tot) {  // (warp-uniform)
+      const int L = __ffs(__ballot_sync(0xffffffffu, acc + inc > x)) - 1;
+      const int start = acc + __shfl_sync(0xffffffffu, inc - ub, L);
+      const int U = __shfl_sync(0xffffffffu, uh, L);
+      const int h = (x - start) / U;
+      bh = (b0 + L) * H + h;
+      base = start + h * U;
+    }
+    acc += tot;
+  }
+  total = acc;
+  return base;
+}
+
+// The extended kernel's unit layout for warp gw: the units' total, the
+// working warps (every one owns at least one unit, so the warps touching a
+// head are consecutive: its partial slots), the warp's range, its first and
+// last heads and the first unit of the first.  Uniform lengths: the launch's.
+struct ExtRange {
+  int total, nw, x0, x1, bh_first, bh_last, base_first;
+};
+__device__ ExtRange ext_range(const TcArgs &a, int gw) {
+  ExtRange r;
+  r.total = a.total;
+  r.nw = a.nw;
+  int t_;
+  if (a.g.ragged) {
+    ragged_locate(a, -1, r.bh_first, r.total);
+    r.nw = min(a.nw, r.total);
+  }
+  r.x0 = (int)((int64_t)gw * r.total / r.nw);
+  r.x1 = (int)((int64_t)(gw + 1) * r.total / r.nw);
+  if (gw >= r.nw) return r;
+  if (a.g.ragged) {
+    r.base_first = ragged_locate(a, r.x0, r.bh_first, t_);
+    ragged_locate(a, r.x1 - 1, r.bh_last, t_);
+  } else {
+    r.bh_first = r.x0 / a.U;
+    r.bh_last = (r.x1 - 1) / a.U;
+    r.base_first = r.bh_first * a.U;
+  }
+  return r;
+}
+
+// warp_seg for a head whose first unit is head_base (the extended kernel).
+template <int EXT>
+__device__ __forceinline__ Seg warp_seg_at(const TcArgs &a, const HeadCnt &hc, int head_base,
+                                           int x0, int x1) {
+  const HeadSpan hs = span_at<EXT>(a, head_base, hc);
+  Seg s;
+  const int base = hs.base;
+  const int ua = max(x0, base) - base, ub = min(x1, base + hs.U) - base;
+  const int qa = max(ua - a.HU, 0), qb = min(ub - a.HU, hs.S);
+  const int fa = max(ua - a.HU - hs.S, 0), fb = min(ub - a.HU - hs.S, hs.F);
+  const int nch = (hc.nf + a.CH - 1) / a.CH;
+  s.tq0 = qa * kTile;
+  s.c0 = (fa + a.UPC - 1) / a.UPC;
+  s.tq1 = qa < qb ? max(min(qb * kTile, hc.nq), s.tq0) : s.tq0;
+  s.c1 = fa < fb ? max(min((fb + a.UPC - 1) / a.UPC, nch), s.c0) : s.c0;
+  return s;
+}
+
 // OUT = 1: the extended kernel -- per-sequence lengths, the value queue and
 // outlier lists, each a run-time option; OUT = 0 compiles none of them.
 // RP = 1: the rotary form (keys cached before RoPE; KIVI, key groups of 32 or
@@ -102,9 +207,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // concatenated per-head unit lists (units of one tile or fp16 chunk).
   const int gw = (int)blockIdx.x * kWarps + warp;
   if (gw >= a.nw) return;
-  const int x0 = (int)((int64_t)gw * a.total / a.nw);
-  const int x1 = (int)((int64_t)(gw + 1) * a.total / a.nw);
-  const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
+  // (OUT: per-sequence lengths lay the heads out by their own units)
+  ExtRange rx{};
+  if constexpr (OUT != 0) {
+    rx = ext_range(a, gw);
+    if (gw >= rx.nw) return;
+  }
+  const int x0 = OUT ? rx.x0 : (int)((int64_t)gw * a.total / a.nw);
+  const int x1 = OUT ? rx.x1 : (int)((int64_t)(gw + 1) * a.total / a.nw);
+  const int bh_first = OUT ? rx.bh_first : x0 / a.U, bh_last = OUT ? rx.bh_last : (x1 - 1) / a.U;
   // fp16 tokens per chunk: a chunk's K and V rows fill the slot up to the
   // query (with outlier lists the block size, so CH, is a run-time value)
   const int CH = OUT ? a.CH : SC::CH;
@@ -132,7 +243,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   int pc_bh = bh_first, pc_ph = 0, pc_lt = 0, pc_n = 0, issued = 0, ps = 0;
   const uint64_t pol_once = l2_evict_first();  // cache blocks are read once
   HeadCnt pc_hc = head_cnt<OUT>(a, pc_bh);
-  Seg pc_seg = warp_seg<OUT>(a, pc_hc, pc_bh, x0, x1);
+  int pc_base = OUT ? rx.base_first : 0;  // (OUT) first unit of head pc_bh
+  Seg pc_seg = OUT ? warp_seg_at<OUT>(a, pc_hc, pc_base, x0, x1)
+                   : warp_seg<OUT>(a, pc_hc, pc_bh, x0, x1);
   pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
   auto pc_settle = [&]() {
     while (pc_bh >= 0 && pc_lt >= pc_n) {
@@ -140,13 +253,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         pc_ph = 1;
         pc_n = pc_seg.c1 - pc_seg.c0;
       } else {
+        if constexpr (OUT != 0) pc_base += span_at<OUT>(a, pc_base, pc_hc).U;
         if (++pc_bh > bh_last) {
           pc_bh = -1;
           return;
         }
         pc_ph = 0;
         pc_hc = head_cnt<OUT>(a, pc_bh);
-        pc_seg = warp_seg<OUT>(a, pc_hc, pc_bh, x0, x1);
+        pc_seg = OUT ? warp_seg_at<OUT>(a, pc_hc, pc_base, x0, x1)
+                     : warp_seg<OUT>(a, pc_hc, pc_bh, x0, x1);
         pc_n = (pc_seg.tq1 - pc_seg.tq0 + kTile - 1) / kTile;
       }
       pc_lt = 0;
@@ -461,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // 4*lane + 3) are joined with the log-sum-exp rule; the quantized output
   // row goes through the warp's operand area to reach the lane layout.
   int pend_bh = -1;  // head this warp merges (slot 0), once it has published
+  int pend_np = 0, cur_np = 0;  // (OUT) its partial count, the current head's
   auto flush = [&](int bh, int slot, float mf, float lf, const float (&af)[4]) -> bool {
     float l = l_lane;
 #pragma unroll
@@ -515,9 +631,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     reset_state();
     // a merge still owed (a head this warp held whole) comes first; the
     // merge of the warp's last head waits until after the tile loop
-    if (pend_bh >= 0 && !merge_head<8>(a, pend_bh)) return false;
+    if (pend_bh >= 0 && !merge_head<8>(a, pend_bh, OUT ? pend_np : -1)) return false;
     publish_partial(a, bh, slot, o, m, lt);
     pend_bh = slot == 0 ? bh : -1;
+    if constexpr (OUT != 0) pend_np = cur_np;
     return true;
   };
 
@@ -551,13 +668,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       aborted = true;
     }
   }
+  int base_t = OUT ? rx.base_first : 0;  // (OUT) first unit of head bh
   for (int bh = bh_first; bh <= bh_last && !aborted; ++bh) {
     const HeadCnt hc = head_cnt<OUT>(a, bh);
-    const Seg sg = warp_seg<OUT>(a, hc, bh, x0, x1);
+    const Seg sg = OUT ? warp_seg_at<OUT>(a, hc, base_t, x0, x1)
+                       : warp_seg<OUT>(a, hc, bh, x0, x1);
     const int tq0 = sg.tq0, tq1 = sg.tq1;
     // fp16 sink + residual / window chunks of this warp's segment
     const int nchk = sg.c1 - sg.c0;
-    const int base = bh * a.U;
+    const int base = OUT ? base_t : bh * a.U;
     if (tq1 > tq0) {
       const int nt = (tq1 - tq0 + kTile - 1) / kTile;
       for (int lt = 0; lt < nt; ++lt) {
@@ -1005,12 +1124,26 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       }
       if (aborted) break;
     }
-    if (!flush(bh, gw - owner_of(base, a.total, a.nw), mf, lf, af)) {
+    if constexpr (OUT != 0) {
+      // partials of the head: one per warp whose range touches it
+      const int U = span_at<OUT>(a, base, hc).U;
+      cur_np = owner_of(base + U - 1, rx.total, rx.nw) - owner_of(base, rx.total, rx.nw) + 1;
+      base_t += U;
+      if (cur_np > a.part_stride) {
+        // (cannot happen: a head's partials are at most its units) never
+        // touch rows past the head's slots
+        if (lane == 0 && a.p.status) atomicExch(a.p.status, KVQ_ECAPACITY);
+        aborted = true;
+        break;
+      }
+    }
+    if (!flush(bh, gw - owner_of(base, OUT ? rx.total : a.total, OUT ? rx.nw : a.nw), mf, lf,
+               af)) {
       aborted = true;
       break;
     }
   }
-  if (!aborted && pend_bh >= 0 && !merge_head<24>(a, pend_bh)) aborted = true;
+  if (!aborted && pend_bh >= 0 && !merge_head<24>(a, pend_bh, OUT ? pend_np : -1)) aborted = true;
   if (aborted) {
     // give up this warp's work; its copies complete first
     if (lane == 0)

@@ -442,14 +442,15 @@ __device__ __forceinline__ void publish_partial(const TcArgs &a, int bh, int slo
 
 // Run by the whole warp in slot 0 of head bh after it published its own
 // partial (a lane reads back only what it wrote itself there): merges the
-// head's partials and writes the output row.  Returns false if they did not
+// head's partials (nparts_given, or by the uniform unit layout) and writes
+// the output row.  Returns false if they did not
 // all appear within the poll bound (status word set).
 // MB: partial rows fetched in one round of loads when nparts <= MB (the
 // kernel's last call can afford many registers).
 template <int MB>
-__device__ bool merge_head(const TcArgs &a, int bh) {
+__device__ bool merge_head(const TcArgs &a, int bh, int nparts_given = -1) {
   const int lane = threadIdx.x & 31;
-  const int nparts = head_nparts(a, bh);
+  const int nparts = nparts_given >= 0 ? nparts_given : head_nparts(a, bh);
   const int64_t base = (int64_t)bh * a.part_stride;
   const uint2 *ml = reinterpret_cast<const uint2 *>(a.ws_ml) + base;
   const uint4 *wo = reinterpret_cast<const uint4 *>(a.ws_o + base * kD);
