@@ -56,7 +56,7 @@ int tc_variant_name(const Geometry &g, char *buf, size_t len) {
   const TcVariant v = tc_variant(g);
   return snprintf(buf, len, "tc_decode_kernel<bits=%d,scheme=%s,ngv=%d,ngk=%d,km=%d,mf=%d,ext=%d>",
                   g.bits, g.scheme == KVQ_KIVI ? "kivi" : "innerq", v.ngv, v.ngk, v.km, g.meta16,
-                  (g.n_out > 0 || g.vq || g.ragged) ? 1 : 0);
+                  tc_ext_kind(g));
 }
 
 bool tc_decode_supported(const Geometry &g) {
@@ -130,7 +130,9 @@ cudaError_t launch_decode_tc(const Geometry &g, const CachePtrs &p, int64_t n_qu
   const cudaError_t e =
       tc_fill_args(a, g, p, n_quant, n_resid, n_sink, q, out, scale, ws, k_new, v_new);
   if (e != cudaSuccess) return e;
-  if (g.n_out > 0 || g.vq || g.ragged) return launch_tc_ext(a, num_sms, st);
+  const int kind = tc_ext_kind(g);
+  if (kind == 1) return launch_tc_ext(a, num_sms, st);
+  if (kind == 2) return launch_tc_rag(a, num_sms, st);
   return g.meta16 ? launch_tc_f16(a, num_sms, st) : launch_tc_mf<0>(a, num_sms, st);
 }
 

@@ -26,11 +26,20 @@ constexpr int kChunkUnits = 2;
 struct HeadCnt {
   int nq, nf, ns, nvq;
 };
+// The counters of a sequence with n = prompt + appended tokens: counts_of's
+// rules in 32-bit arithmetic (a cache holds at most 2^30 tokens).
+__device__ __forceinline__ HeadCnt seq_cnt(const Geometry &g, int n) {
+  if (g.scheme == KVQ_KIVI) {
+    const int nr = n % g.residual;
+    return HeadCnt{n - nr, nr, 0, g.vq ? (n >= g.residual ? n - g.residual + 1 : 0) : n - nr};
+  }
+  const int ns = min(n, g.n_sink), rest = n - ns, nr = min(rest, g.residual);
+  return HeadCnt{rest - nr, nr + ns, ns, rest - nr};
+}
 template <int EXT>
 __device__ __forceinline__ HeadCnt head_cnt(const TcArgs &a, int bh) {
   if (!EXT || !a.g.ragged) return HeadCnt{(int)a.n_quant, (int)a.n_fp16, (int)a.n_sink, (int)a.n_vq};
-  const Counts c = counts_of(a.g, a.p.seq_prompt[bh / a.g.H], a.p.appended);
-  return HeadCnt{(int)c.n_quant, (int)(c.n_resid + c.n_sink), (int)c.n_sink, (int)c.n_vq};
+  return seq_cnt(a.g, a.p.seq_prompt[bh / a.g.H] + (int)a.p.appended);
 }
 
 // What unit range [x0, x1) holds of head bh: its U units are HU empty ones,
@@ -80,9 +89,8 @@ __device__ __forceinline__ HeadSpan span_at(const TcArgs &a, int base, const Hea
 
 // Units of one head of sequence b.
 __device__ __forceinline__ int seq_units(const TcArgs &a, int b) {
-  const Counts c = counts_of(a.g, a.p.seq_prompt[b], a.p.appended);
-  return a.HU + (int)((c.n_quant + kTile - 1) / kTile) +
-         (int)((c.n_resid + c.n_sink + a.CH - 1) / a.CH) * a.UPC;
+  const HeadCnt c = seq_cnt(a.g, a.p.seq_prompt[b] + (int)a.p.appended);
+  return a.HU + (c.nq + kTile - 1) / kTile + (c.nf + a.CH - 1) / a.CH * a.UPC;
 }
 
 // Run by the whole warp: the units of every head (`total`) and, for x >= 0,
@@ -129,6 +137,34 @@ __device__ ExtRange ext_range(const TcArgs &a, int gw) {
   r.total = a.total;
   r.nw = a.nw;
   int t_;
+  if (a.g.ragged && a.g.B <= 32) {
+    // one pass: lane b holds sequence b's units; their prefix sum gives the
+    // total, then both ends of the warp's range
+    const int lane = threadIdx.x & 31, H = a.g.H;
+    const int uh = lane < a.g.B ? seq_units(a, lane) : 0, ub = H * uh;
+    int inc = ub;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    r.total = __shfl_sync(0xffffffffu, inc, 31);
+    r.nw = min(a.nw, r.total);
+    r.x0 = (int)((int64_t)gw * r.total / r.nw);
+    r.x1 = (int)((int64_t)(gw + 1) * r.total / r.nw);
+    if (gw >= r.nw) return r;
+    auto head_of = [&](int x, int &bh) {
+      const int L = __ffs(__ballot_sync(0xffffffffu, inc > x)) - 1;
+      const int start = __shfl_sync(0xffffffffu, inc - ub, L);
+      const int U = __shfl_sync(0xffffffffu, uh, L);
+      const int h = (x - start) / U;
+      bh = L * H + h;
+      return start + h * U;
+    };
+    r.base_first = head_of(r.x0, r.bh_first);
+    head_of(r.x1 - 1, r.bh_last);
+    return r;
+  }
   if (a.g.ragged) {
     ragged_locate(a, -1, r.bh_first, r.total);
     r.nw = min(a.nw, r.total);
@@ -166,7 +202,8 @@ __device__ __forceinline__ Seg warp_seg_at(const TcArgs &a, const HeadCnt &hc, i
 }
 
 // OUT = 1: the extended kernel -- per-sequence lengths, the value queue and
-// outlier lists, each a run-time option; OUT = 0 compiles none of them.
+// outlier lists, each a run-time option; OUT = 2: per-sequence lengths only;
+// OUT = 0 compiles none of them.
 // RP = 1: the rotary form (keys cached before RoPE; KIVI, key groups of 32 or
 // more, fp32 statistics, no options): key scores on the CUDA cores, one token
 // per lane, the rest as above.
@@ -176,6 +213,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT, RP>;
   static_assert(!RP || (SCHEME == KVQ_KIVI && KM <= 1 && MF == 0 && OUT == 0),
                 "the rotary form: KIVI, one key group per tile, fp32 statistics, no options");
+  // OUT: 0 = no options; 1 = outlier lists and the value queue compiled in
+  // (and per-sequence lengths, if the cache has them); 2 = per-sequence
+  // lengths only.  XO: the outlier and value-queue code.
+  constexpr bool XO = OUT == 1;
   constexpr bool G16 = SCHEME == KVQ_KIVI && KM == 2;
   constexpr int RB = SC::RB;  // packed bytes per token row
   constexpr int nslot = SC::nslot;
@@ -218,9 +259,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   const int bh_first = OUT ? rx.bh_first : x0 / a.U, bh_last = OUT ? rx.bh_last : (x1 - 1) / a.U;
   // fp16 tokens per chunk: a chunk's K and V rows fill the slot up to the
   // query (with outlier lists the block size, so CH, is a run-time value)
-  const int CH = OUT ? a.CH : SC::CH;
-  const int BBr = OUT ? g.block_bytes : SC::BB;  // bytes of a cache block
-  const int n_out = OUT ? g.n_out : 0;
+  const int CH = XO ? a.CH : SC::CH;
+  const int BBr = XO ? g.block_bytes : SC::BB;  // bytes of a cache block
+  const int n_out = XO ? g.n_out : 0;
   float *qf_s = reinterpret_cast<float *>(sBw + SC::sb_xtra);  // OUT: q, score domain
   float *xo_s = qf_s + kD;  // OUT: outliers' value corrections, m_run frame
 
@@ -228,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // Ring bytes are only read where a copy wrote them (rows past a segment's
   // end are masked), so the ring needs no clearing; the zero block does.
   if (lane < 16) sBw[SC::sb_zero + lane] = 0u;
-  if (OUT)
+  if (XO)
 #pragma unroll
     for (int i = 0; i < 4; ++i) xo_s[4 * lane + i] = 0.0f;
   if (lane == 0) {
@@ -383,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
       q4[2] *= n4.z;
       q4[3] *= n4.w;
     }
-    if (OUT) {
+    if (XO) {
       // the query in the score domain, for the outliers' key corrections
       __syncwarp();
       reinterpret_cast<float4 *>(qf_s)[lane] = make_float4(q4[0], q4[1], q4[2], q4[3]);
@@ -605,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     }
     __syncwarp();
     float4 oq = reinterpret_cast<const float4 *>(so)[lane];
-    if (OUT) {
+    if (XO) {
       oq.x += xv[0];
       oq.y += xv[1];
       oq.z += xv[2];
@@ -846,7 +887,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             if (SCHEME == KVQ_KIVI) score = fmaf(score, pow2E, t < 16 ? bias0 : bias1);
           }
           const bool valid = FULL || t < n;
-          if (OUT && valid) {
+          if (XO && valid) {
             // dense-and-sparse keys: an outlier's code is 0, so the dense score
             // holds q_c * zero_c there; its fp16 value replaces it
             const uint32_t *ol = reinterpret_cast<const uint32_t *>(slot + g.blk_ko) + t * n_out;
@@ -860,8 +901,8 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           }
           score = valid ? score : -INFINITY;
           // value queue: tokens [vq_from, ...) of the head keep fp16 values
-          const int vq_from = OUT ? hc.nvq - tok0 : kTile;
-          const bool valid_v = OUT ? valid && t < vq_from : valid;
+          const int vq_from = XO ? hc.nvq - tok0 : kTile;
+          const bool valid_v = XO ? valid && t < vq_from : valid;
           // lazy rescaling: the reference m_run moves only when a score passes
           // it by more than kSlack (one vote, no reduction on most tiles)
           if (__any_sync(0xffffffffu, score > m_run + kSlack)) {
@@ -872,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             l_lane *= alpha;
   #pragma unroll
             for (int j = 0; j < NGV; ++j) z_lane[j] *= alpha;
-            if (OUT) {
+            if (XO) {
   #pragma unroll
               for (int i = 0; i < 4; ++i) xv[i] *= alpha;
               __syncwarp();  // the previous tiles' corrections are in
@@ -894,9 +935,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
             ld_stat_row<MF, NGV>(slot + SC::off_vz + t * NGV * SC::MSZ, zr);
   #pragma unroll
             for (int j = 0; j < NGV; ++j)
-              z_lane[j] = (OUT ? valid_v : (FULL || p > 0.0f)) ? fmaf(p, zr[j], z_lane[j])
+              z_lane[j] = (XO ? valid_v : (FULL || p > 0.0f)) ? fmaf(p, zr[j], z_lane[j])
                                                                 : z_lane[j];
-            if (OUT && valid_v) {
+            if (XO && valid_v) {
               // dense-and-sparse values: code 0 gave p * zero, the fp16 value
               // replaces it (channel c of an arbitrary lane: shared atomics)
               const uint32_t *ol = reinterpret_cast<const uint32_t *>(slot + g.blk_vo) + t * n_out;
@@ -912,7 +953,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
               }
             }
           }
-          if (OUT && vq_from < n) {
+          if (XO && vq_from < n) {
             // (warp-uniform) the tile's value-queue tokens: p_t * v_t from their
             // fp16 ring rows (slot t mod R), on CUDA cores, in token order; the
             // rows of four tokens are loaded before their products
@@ -1157,11 +1198,10 @@ cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   using SC = SlotCfg<BITS, SCHEME, NGV, NGK, KM, MF, OUT, RP>;
   auto kern = tc_decode_kernel<BITS, SCHEME, NGV, NGK, KM, MF, OUT, RP>;
   constexpr int smem = SC::smem;
-  const bool ext = a.g.n_out > 0 || a.g.vq || a.g.ragged;
-  if (a.g.meta16 != MF || ext != (OUT != 0)) return cudaErrorInvalidValue;
+  if (a.g.meta16 != MF || tc_ext_kind(a.g) != OUT) return cudaErrorInvalidValue;
   // the block and the fp16 chunk fit the slot (the block size, and so the
   // chunk, is compile-time without outlier lists)
-  if (OUT ? (a.g.block_bytes > SC::BBX || a.g.n_out > kMaxOutliers ||
+  if (OUT == 1 ? (a.g.block_bytes > SC::BBX || a.g.n_out > kMaxOutliers ||
              2 * a.CH * kD * 2 > SC::off_q)
           : (a.g.block_bytes != SC::BB || a.CH != SC::CH))
     return cudaErrorInvalidValue;

@@ -52,11 +52,21 @@ cudaError_t tc_fill_args(TcArgs &a, const Geometry &g, const CachePtrs &p, int64
                          int64_t n_resid, int64_t n_sink, const __half *q, float *out, float scale,
                          void *ws, const __half *k_new, const __half *v_new);
 
-// The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), and the
-// extended one (outlier lists, the value queue, per-sequence lengths), each
-// built in its own translation unit.
+// The MHA tensor-core decode with fp16 statistics (KVQ_META_F16), the
+// extended one (outlier lists, the value queue, per-sequence lengths) and
+// the one with per-sequence lengths only, each built in its own translation
+// unit.
 cudaError_t launch_tc_f16(TcArgs &a, int num_sms, cudaStream_t st);
 cudaError_t launch_tc_ext(TcArgs &a, int num_sms, cudaStream_t st);
+cudaError_t launch_tc_rag(TcArgs &a, int num_sms, cudaStream_t st);
+
+// The MHA tensor-core family a cache takes: 0 = no options; 1 = outlier
+// lists or the value queue (per-sequence lengths too, if the cache has them);
+// 2 = per-sequence lengths only.
+inline int tc_ext_kind(const Geometry &g) {
+  if (g.n_out > 0 || g.vq) return 1;
+  return g.ragged ? 2 : 0;
+}
 
 namespace {
 
@@ -103,7 +113,8 @@ __host__ __device__ constexpr TcLayout tc_layout(int slot_bytes, int nslot, int 
 // 1 = G 32, one group, inside the block; 0 = G >= 64, the tile's group read
 // from the separate key-statistics array.  MF: statistics stored in fp16
 // (MSZ = 2 bytes each) instead of fp32.
-// OUT (the extended kernel): the block may carry outlier lists (up to
+// OUT = 1 (the extended kernel with outliers or the value queue): the block
+// may carry outlier lists (up to
 // kMaxOutliers words per token and tensor), so its size is known only at run
 // time: the slot reserves room for the largest, and the per-warp area adds
 // the query in the score domain and the outliers' value corrections (128
@@ -125,7 +136,7 @@ struct SlotCfg {
   static constexpr bool KIN = SCHEME == KVQ_KIVI && KM >= 1;
   static constexpr int KGB = (KM == 2 ? 2 : 1) * 2 * kD * MSZ;  // KIVI key statistics of a tile
   static constexpr int BB = SCHEME == KVQ_KIVI ? off_ks + (KIN ? KGB : 0) : off_kz + kTile * NGK * MSZ;
-  static constexpr int BBX = BB + (OUT ? 2 * kTile * kMaxOutliers * 4 : 0);  // room in the slot
+  static constexpr int BBX = BB + (OUT == 1 ? 2 * kTile * kMaxOutliers * 4 : 0);  // room in the slot
   static constexpr int KMB = SCHEME == KVQ_KIVI && !KIN ? KGB : 0;  // separate copy
   static constexpr int off_km = KIN ? off_ks : BBX;
   static constexpr int off_q = BBX + KMB;
@@ -134,7 +145,7 @@ struct SlotCfg {
   // per warp: KIVI key operand (512 B per group; also the 512 B output
   // transpose at a head's end), the outlier extras, 64 zero bytes
   static constexpr int SBO = RP ? 3 * 32 * 16 : (SCHEME == KVQ_KIVI && KM == 2 ? 1024 : 512);
-  static constexpr int SBB = SBO + (OUT ? 1024 : 0) + 64;
+  static constexpr int SBB = SBO + (OUT == 1 ? 1024 : 0) + 64;
   static constexpr int sb_xtra = SBO / 4;       // word offset of the extras (OUT)
   static constexpr int sb_zero = SBB / 4 - 16;  // word offset of the zero block
   static constexpr int CSB = RP ? 32 * 32 * 16 : 0;  // the rotary form's cos / sin table

@@ -22,11 +22,12 @@ W = synth.WORKLOADS
 S = synth.scaled
 
 
-def _kivi(bits, ngv, G, mf=False, out=0):
+def _kivi(bits, ngv, G, mf=False, out=0, ragged=False):
     base = W["llama2_7b_2bit"] if bits == 2 else W["kivi_4bit"]
     R = 64 if G <= 64 else 128
-    return S(base, batch=2, n_q_heads=2, n_kv_heads=2, ctx=700, k_group=G, v_group=128 // ngv,
-             residual=R, n_append=R + 10, meta_f16=mf, outliers=out)
+    return S(base, batch=4 if ragged else 2, n_q_heads=2, n_kv_heads=2, ctx=700, k_group=G,
+             v_group=128 // ngv, residual=R, n_append=R + 10, meta_f16=mf, outliers=out,
+             ragged=ragged)
 
 
 def _innerq(bits, ngv, ngk, mf=False, ragged=False):
@@ -48,10 +49,12 @@ for mf in (False, True):
     for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
         CASES["tc_innerq_b%d_ngv%d_ngk%d%s" % (bits, ngv, ngk, sfx)] = _innerq(bits, ngv, ngk, mf)
     # the extended kernel: KIVI with outlier lists (1, 2 and 8 per token spread
-    # over the shapes), InnerQ with per-sequence lengths
+    # over the shapes); per-sequence lengths only: KIVI and InnerQ
     for i, (bits, ngv, G) in enumerate(itertools.product((2, 4), (2, 4), (16, 32, 64))):
         CASES["tc_kivi_b%d_ngv%d_g%d%s_out" % (bits, ngv, G, sfx)] = _kivi(bits, ngv, G, mf,
                                                                          (1, 2, 8)[i % 3])
+        CASES["tc_kivi_b%d_ngv%d_g%d%s_ragged" % (bits, ngv, G, sfx)] = _kivi(bits, ngv, G, mf,
+                                                                            ragged=True)
     for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
         CASES["tc_innerq_b%d_ngv%d_ngk%d%s_ragged" % (bits, ngv, ngk, sfx)] = _innerq(
             bits, ngv, ngk, mf, ragged=True)
@@ -94,9 +97,10 @@ def dispatched_tensor_core_names():
 
 def test_every_dispatched_instantiation_has_a_parity_case():
     dispatched = dispatched_tensor_core_names()
-    # MHA: 20 shapes with fp32 and with fp16 statistics, each plain and
-    # extended (outlier lists, value queue, per-sequence lengths); grouped-query: 8
-    assert len(dispatched) == 2 * 2 * 20 + 8, sorted(dispatched)
+    # MHA: 20 shapes with fp32 and with fp16 statistics, each plain and with
+    # per-sequence lengths only, and the 12 KIVI shapes extended (outlier lists,
+    # value queue; InnerQ has neither); grouped-query: 8
+    assert len(dispatched) == 2 * (2 * 20 + 12) + 8, sorted(dispatched)
     covered = {_name(w) for w in CASES.values()}
     assert dispatched <= covered, sorted(dispatched - covered)
     # and each named case reaches the instantiation its name says
