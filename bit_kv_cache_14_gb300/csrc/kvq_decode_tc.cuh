@@ -19,6 +19,7 @@ namespace {
 // and merges the head's partials at the end, both costs of about a tile.
 constexpr int kHeadUnits = 2;
 constexpr int kChunkUnits = 2;
+constexpr int kMinWarpUnits = 6;
 
 // Counters of head bh: the launch's, or (per-sequence lengths) its
 // sequence's own; nf = fp16 tokens (sinks + residual / window), nvq = tokens
@@ -244,9 +245,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   uint32_t *sBw = reinterpret_cast<uint32_t *>(smem + Ly.sB + warp * SC::SBB);
   const uint32_t wring_s = smem_u32(wring), wbars_s = smem_u32(wbars);  // shared-window addresses
 
-  // Warp-level stream-K: warp gw of the grid owns units [x0, x1) of the
+  // Warp-level stream-K: logical warp gw owns units [x0, x1) of the
   // concatenated per-head unit lists (units of one tile or fp16 chunk).
-  const int gw = (int)blockIdx.x * kWarps + warp;
+  // When fewer warps than the grid holds have work, logical warps go
+  // round-robin over the blocks, so every SM gets about the same number.
+  const int gw = a.nw < (int)gridDim.x * kWarps ? warp * (int)gridDim.x + (int)blockIdx.x
+                                                : (int)blockIdx.x * kWarps + warp;
   if (gw >= a.nw) return;
   // (OUT: per-sequence lengths lay the heads out by their own units)
   ExtRange rx{};
@@ -1211,11 +1215,19 @@ cudaError_t launch_tc_t(TcArgs &a, int num_sms, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   int64_t nc = (int64_t)num_sms * occ;
   if (nc > kTcMaxBlocks) nc = kTcMaxBlocks;
-  // every working warp gets at least one unit
+  // every working warp gets at least kMinWarpUnits units (or all of them):
+  // a head's partials are the warps its units span, and its merger reads
+  // them in rounds, so cutting small batches across the whole grid costs
+  // more in merging than the extra warps bring
   int64_t nw = nc * kWarps;
-  if (nw > a.total) nw = a.total;
+  if (nw > (a.total + kMinWarpUnits - 1) / kMinWarpUnits)
+    nw = (a.total + kMinWarpUnits - 1) / kMinWarpUnits;
   if (nw < 1) nw = 1;
-  nc = (nw + kWarps - 1) / kWarps;
+  // blocks: enough for the working warps, rounded up to a whole number per
+  // SM (the working warps spread over them, see the kernel)
+  const int64_t need = (nw + kWarps - 1) / kWarps;
+  const int64_t per = ((need + num_sms - 1) / num_sms) * num_sms;
+  if (per < nc) nc = per;
   a.nc = (int)nc;
   a.nw = (int)nw;
   // every block must be resident: the merging warps wait for other blocks
