@@ -1,5 +1,5 @@
-// Grouped-query decode attention on the tensor cores: head_dim 128, 2-bit
-// KIVI codes, RG = 2 or 4 query heads per KV head.
+// Grouped-query decode attention on the tensor cores: head_dim 128, 2- or
+// 4-bit KIVI codes, RG = 2 or 4 query heads per KV head.
 //
 // Same computation as the MHA kernel (softmax(scale * q.K^T) V over the
 // packed cache, dequantization folded into both GEMVs -- "大模型量化技术原理：
@@ -32,9 +32,9 @@ namespace kvq {
 
 namespace {
 
-template <int NGV, int KM, int RG>
+template <int BITS, int NGV, int KM, int RG>
 struct GqaCfg {
-  static constexpr int RB = kD * 2 / 8;  // 32 bytes per 2-bit row
+  static constexpr int RB = kD * BITS / 8;  // bytes per token row of codes
   static constexpr int off_vc = kTile * RB;
   static constexpr int off_vs = 2 * kTile * RB;
   static constexpr int off_vz = off_vs + kTile * NGV * 4;
@@ -46,9 +46,16 @@ struct GqaCfg {
   static constexpr int off_km = KIN ? off_ks : BB;
   static constexpr int bytes = BB + KMB;  // one slot (no query rows in the ring)
   static constexpr int CH = bytes / (4 * kD) < 8 ? bytes / (4 * kD) : 8;
-  static constexpr int WPG = 8 / NGV;     // 16-channel code words per value group
+  // code words: a 32-bit word holds CPW channels, PH per 16-bit half (the
+  // low half channels 0..PH-1 of the word, the high half PH..CPW-1)
+  static constexpr int CPW = 32 / BITS, PH = 16 / BITS;
+  static constexpr int KWL = kD / CPW / 4;      // key words per lane group (2 or 4)
+  static constexpr int SPW = 8 / KWL;           // key k-steps per word
+  static constexpr int WPG = kD / NGV / CPW;    // code words per value group
+  static constexpr int NV = 8 / WPG;            // code positions dealt over a tile's rows
+  static constexpr int MPJ = PH / NV;           // value MMAs per value group and k-block
   // per warp: key operand (8 columns, each a row of KROW words: lane group
-  // tig's 2-word fragment of k-step kk at tig * KTIG + 2 kk; the pitches put
+  // tig's 2-word fragment of k-step s at tig * KTIG + 2 s; the pitches put
   // the 16 fragments a half-warp reads, and the 32 words one store writes,
   // on distinct banks), also the value operand (2 NGV blocks of 64 words) and
   // the output transpose of RG x 128 floats; query table [c][4] fp32 + 2^E
@@ -63,8 +70,13 @@ struct GqaCfg {
          : what == 2 ? kWarps * nslot * bytes + kWarps * (SBB + QTB)
                      : kWarps * nslot * bytes + kWarps * (SBB + QTB) + kWarps * (nslot + 1) * 8;
   }
-  static constexpr int nslot = lay(3, 3) <= 112 * 1024 ? 3 : 2;
+  // two blocks per SM where two ring slots fit in half the shared memory
+  // (2-bit), else one block per SM with three slots (4-bit: 6 KB blocks)
+  static constexpr int MINB = lay(2, 3) <= 112 * 1024 ? 2 : 1;
+  static constexpr int nslot = MINB == 2 ? (lay(3, 3) <= 112 * 1024 ? 3 : 2) : 3;
   static constexpr int smem = lay(nslot, 3);
+  static_assert(smem <= 227 * 1024, "shared memory");
+  static_assert(MPJ * NGV == 8, "eight value MMAs per k-block");
 };
 
 // Partial slots of head bh (RG rows each): 8 per block holding quantized
@@ -188,28 +200,37 @@ __device__ bool gqa_finish(const TcArgs &a, int bh, int ticket) {
 }
 
 // Key-operand pair ip (0..63: lane ip mod 32, pass ip / 32) builds channels
-// c = 16 W + p and c + 8 with p = ip mod 8 and W = kw_of(ip / 8): bits 1 and 2
-// of ip / 8 swapped, so one pass writes the fragments of lane groups 0 and 2
-// (or 1 and 3).  The map is its own inverse.
-__device__ __forceinline__ int kw_of(int q) { return (q & 1) | ((q & 2) << 1) | ((q & 4) >> 1); }
+// c = CPW W + p and c + PH of code word W at position p.  2-bit: p = ip mod 8,
+// W = kw_of(ip / 8) with bits 1 and 2 swapped; 4-bit: p = ip mod 4, W =
+// kw_of(ip / 4) with bits 2 and 3 swapped.  Either way one pass writes the
+// fragments of lane groups 0 and 2 (or 1 and 3); the map is its own inverse.
+template <int BITS>
+__device__ __forceinline__ int kw_of(int q) {
+  if (BITS == 2) return (q & 1) | ((q & 2) << 1) | ((q & 4) >> 1);
+  return (q & 3) | ((q & 4) << 1) | ((q & 8) >> 1);
+}
 
-// Position of q_r[c] in the query table: channel c = 16 W + 8 e + p (p < 8)
-// belongs to key-operand pair ip = 8 kw_of(W) + p; the table is
+// Position of q_r[c] in the query table: channel c = CPW W + PH e + p (p <
+// PH) belongs to key-operand pair ip = PH kw_of(W) + p; the table is
 // [ip / 32][r / 2][ip mod 32][r mod 2][e].
+template <int BITS>
 __device__ __forceinline__ int qt_index(int c, int r) {
-  const int ip = 8 * kw_of(c >> 4) + (c & 7), e = (c >> 3) & 1;
+  constexpr int CPW = 32 / BITS, PH = 16 / BITS;
+  const int ip = PH * kw_of<BITS>(c / CPW) + (c % PH), e = (c / PH) & 1;
   return (((ip >> 5) * 2 + (r >> 1)) * 32 + (ip & 31)) * 4 + (r & 1) * 2 + e;
 }
 
-template <int NGV, int KM, int RG>
-__global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
+template <int BITS, int NGV, int KM, int RG>
+__global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG>::MINB))
+    tc_gqa_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  using C = GqaCfg<NGV, KM, RG>;
+  using C = GqaCfg<BITS, NGV, KM, RG>;
   constexpr int RB = C::RB;
   constexpr int nslot = C::nslot;
   constexpr int SLOT = C::bytes;
   constexpr int CH = C::CH;
-  constexpr int WPG = C::WPG;
+  constexpr int WPG = C::WPG, MPJ = C::MPJ, NV = C::NV, CPW = C::CPW, PH = C::PH;
+  constexpr int KWL = C::KWL, SPW = C::SPW;
   const Geometry &g = a.g;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
@@ -340,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int r = 0; r < RG; ++r) QT[qt_index(4 * lane + i, r)] = qv[r][i];
+      for (int r = 0; r < RG; ++r) QT[qt_index<BITS>(4 * lane + i, r)] = qv[r][i];
     if (lane < RG) QT[4 * kD + lane] = e2[lane < RG ? lane : 0];
     __syncwarp();
     pow2 = tig < RG ? QT[4 * kD + tig] : 1.0f;
@@ -348,17 +369,18 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
   };
 
   // key-operand channel pairs this lane builds (as in the MHA kernel), and
-  // the factor 4^-p that undoes the code position p of the low channel
+  // the factor 1 / pos_factor(p) that undoes the code position p; lane group
+  // tig holds words W = KWL tig + w, k-step SPW w + p / 2, register p mod 2
   int b_clo[2];
   uint32_t *b_dst[2];
   float2 b_ipf[2];
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     const int ip = lane + 32 * m;
-    const int W = kw_of(ip >> 3), p = ip & 7;
-    b_clo[m] = 16 * W + p;
-    b_dst[m] = sBw + (W >> 1) * C::KTIG + (4 * (W & 1) + (p >> 1)) * 2 + (p & 1);
-    const float f = inv_pos_factor<2>(p);
+    const int W = kw_of<BITS>(ip / PH), p = ip % PH;
+    b_clo[m] = CPW * W + p;
+    b_dst[m] = sBw + (W / KWL) * C::KTIG + (SPW * (W % KWL) + (p >> 1)) * 2 + (p & 1);
+    const float f = inv_pos_factor<BITS>(p);
     b_ipf[m] = make_float2(f, f);
   }
   // value operand: the writer's columns (r = tig, hi / lo) and the reader's
@@ -369,11 +391,12 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
   uint32_t *const v_hi = sBw + (2 * tig + (tig >> 1)) * 8 + wofs;
   uint32_t *const v_lo = sBw + (2 * tig + 1 - (tig >> 1)) * 8 + wofs;
   const uint32_t *const v_rd = sBw + (gid ^ (gid >> 2)) * 8 + 2 * tig;
-  // value codes: this lane's rows take code position P + off of each word
-  // (P the tile's base position), read in place by a mask: positions 0-3 from
-  // the token pair's half words, 4-7 from them shifted down a byte
+  // value codes: this lane's rows take code position NV m + v_off of each
+  // half word (m the MMA's index in its value group), read in place by a
+  // mask: the low half of the positions (0-3 of 2-bit, 0-1 of 4-bit) from the
+  // token pair's half words, the high half from them shifted down a byte
   const int v_off = gid / WPG;
-  const uint32_t vm0 = 0x00030003u << (2 * v_off), vm1 = vm0 << 4;
+  const uint32_t vm0 = (BITS == 2 ? 0x00030003u : 0x000F000Fu) << (BITS * v_off), vm1 = vm0 << 4;
   const float2 neg1 = make_float2(-1.0f, -1.0f);
   const bool head_lane = tig < RG;
 
@@ -429,13 +452,14 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
     if (head_lane) {
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const int j = mt / WPG, m = mt % WPG;
-        const int W = j * WPG + gid % WPG, p = m * NGV + v_off;
-        // the code sat at position (m NGV mod 4) + off of its source half word
-        const int ps = ((m * NGV) & 3) + v_off;
-        const float f = __int_as_float((127 + 32 - 2 * ps) << 23);  // 2^24 * 2^8 / 4^ps
-        so[tig * kD + 16 * W + p] = fmaf(dv[mt][0] + dv[mt][1], f, Z[j]);
-        so[tig * kD + 16 * W + 8 + p] = fmaf(dv[mt][2] + dv[mt][3], f, Z[j]);
+        const int j = mt / MPJ, m = mt % MPJ;
+        const int W = j * WPG + gid % WPG, p = m * NV + v_off;
+        // the code sat at position ps of its source half word (the high
+        // positions after the shift by a byte): 2^24 * 2^8 / pos_factor
+        const int ps = p % (PH / 2);
+        const float f = __int_as_float((127 + 32 - BITS * ps) << 23);
+        so[tig * kD + CPW * W + p] = fmaf(dv[mt][0] + dv[mt][1], f, Z[j]);
+        so[tig * kD + CPW * W + PH + p] = fmaf(dv[mt][2] + dv[mt][3], f, Z[j]);
       }
     }
     __syncwarp();
@@ -492,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
         const uint8_t *slot = wring + s * SLOT;
         const uint8_t *kc = slot;
         const uint8_t *vc = slot + C::off_vc;
-        // ---- key operand: columns (r, hi/lo) of QT * scale / 4^p, and the
+        // ---- key operand: columns (r, hi/lo) of QT * scale / pos_factor(p), and the
         // per-head bias sum_c QT * zero, for this tile's key group
         const float *ks = reinterpret_cast<const float *>(slot + C::off_km), *kz = ks + kD;
         float2 bacc[RG];
@@ -500,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
         for (int r = 0; r < RG; ++r) bacc[r] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          const int clo = b_clo[m], chi = clo + 8;
+          const int clo = b_clo[m], chi = clo + PH;
           const float2 s2 = __fmul2_rn(make_float2(ks[clo], ks[chi]), b_ipf[m]);
           const float2 zz = make_float2(kz[clo], kz[chi]);
           const float4 q01 = reinterpret_cast<const float4 *>(QT)[(2 * m) * 32 + lane];
@@ -544,29 +568,36 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
         {
           float e0[2][4] = {}, e1[2][4] = {};
           const uint32_t *bsrc = sBw + gid * C::KROW + tig * C::KTIG;
-          const uint2 wa0 = *reinterpret_cast<const uint2 *>(kc + gid * RB + 8 * tig);
-          const uint2 wb0 = *reinterpret_cast<const uint2 *>(kc + (gid + 8) * RB + 8 * tig);
-          const uint2 wa1 = *reinterpret_cast<const uint2 *>(kc + (gid + 16) * RB + 8 * tig);
-          const uint2 wb1 = *reinterpret_cast<const uint2 *>(kc + (gid + 24) * RB + 8 * tig);
-          uint32_t w[2][4], sw[2][4];
+          // rows gid, gid + 8, gid + 16, gid + 24: this lane group's KWL words
+          uint32_t w[KWL][4], sw[KWL][4];
 #pragma unroll
-          for (int m = 0; m < 2; ++m) {
-            w[m][0] = m ? wa0.y : wa0.x, w[m][1] = m ? wb0.y : wb0.x;
-            w[m][2] = m ? wa1.y : wa1.x, w[m][3] = m ? wb1.y : wb1.x;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) sw[m][i] = shifted<2>(w[m][i]);
+          for (int i = 0; i < 4; ++i) {
+            const uint8_t *row = kc + (gid + 8 * i) * RB + 4 * KWL * tig;
+            if constexpr (KWL == 2) {
+              const uint2 x = *reinterpret_cast<const uint2 *>(row);
+              w[0][i] = x.x, w[1][i] = x.y;
+            } else {
+              const uint4 x = *reinterpret_cast<const uint4 *>(row);
+              w[0][i] = x.x, w[1][i] = x.y, w[2][i] = x.z, w[3][i] = x.w;
+            }
           }
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
+          for (int m = 0; m < KWL; ++m)
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              const uint2 b = *reinterpret_cast<const uint2 *>(bsrc + 2 * (4 * m + jj));
-              mma16816(e0[m], ext<2>(w[m][0], sw[m][0], 2 * jj), ext<2>(w[m][1], sw[m][1], 2 * jj),
-                       ext<2>(w[m][0], sw[m][0], 2 * jj + 1), ext<2>(w[m][1], sw[m][1], 2 * jj + 1),
-                       b.x, b.y);
-              mma16816(e1[m], ext<2>(w[m][2], sw[m][2], 2 * jj), ext<2>(w[m][3], sw[m][3], 2 * jj),
-                       ext<2>(w[m][2], sw[m][2], 2 * jj + 1), ext<2>(w[m][3], sw[m][3], 2 * jj + 1),
-                       b.x, b.y);
+            for (int i = 0; i < 4; ++i) sw[m][i] = shifted<BITS>(w[m][i]);
+#pragma unroll
+          for (int jj = 0; jj < SPW; ++jj)
+#pragma unroll
+            for (int m = 0; m < KWL; ++m) {
+              const uint2 b = *reinterpret_cast<const uint2 *>(bsrc + 2 * (SPW * m + jj));
+              float(&f0)[4] = e0[m & 1];
+              float(&f1)[4] = e1[m & 1];
+              mma16816(f0, ext<BITS>(w[m][0], sw[m][0], 2 * jj), ext<BITS>(w[m][1], sw[m][1], 2 * jj),
+                       ext<BITS>(w[m][0], sw[m][0], 2 * jj + 1),
+                       ext<BITS>(w[m][1], sw[m][1], 2 * jj + 1), b.x, b.y);
+              mma16816(f1, ext<BITS>(w[m][2], sw[m][2], 2 * jj), ext<BITS>(w[m][3], sw[m][3], 2 * jj),
+                       ext<BITS>(w[m][2], sw[m][2], 2 * jj + 1),
+                       ext<BITS>(w[m][3], sw[m][3], 2 * jj + 1), b.x, b.y);
             }
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -693,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
               const uint32_t ya = __byte_perm(w0, w1, 0x5410), yb = __byte_perm(w0, w1, 0x7632);
               const uint32_t yc = __byte_perm(w2, w3, 0x5410), yd = __byte_perm(w2, w3, 0x7632);
               const uint32_t za = ya >> 8, zb = yb >> 8, zc = yc >> 8, zd = yd >> 8;
-              if constexpr (WPG == 2) {
+              if constexpr (MPJ == 2) {
                 mma16816(dv[2 * j], ya & vm0, yb & vm0, yc & vm0, yd & vm0, bw.x, bw.y);
                 mma16816(dv[2 * j + 1], za & vm0, zb & vm0, zc & vm0, zd & vm0, bw.x, bw.y);
               } else {
@@ -723,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
       for (int r = 0; r < RG; ++r) {
         const float e = QT[4 * kD + r];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) qq[r][i] = QT[qt_index(4 * lane + i, r)] * e;
+        for (int i = 0; i < 4; ++i) qq[r][i] = QT[qt_index<BITS>(4 * lane + i, r)] * e;
         mf[r] = -INFINITY;
         lf[r] = 0.0f;
 #pragma unroll
@@ -780,10 +811,10 @@ __global__ void __launch_bounds__(kThreads, 2) tc_gqa_kernel(const TcArgs a) {
       bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
 }
 
-template <int NGV, int KM, int RG>
+template <int BITS, int NGV, int KM, int RG>
 cudaError_t launch_gqa_t(TcArgs &a, int num_sms, cudaStream_t st) {
-  using C = GqaCfg<NGV, KM, RG>;
-  auto kern = tc_gqa_kernel<NGV, KM, RG>;
+  using C = GqaCfg<BITS, NGV, KM, RG>;
+  auto kern = tc_gqa_kernel<BITS, NGV, KM, RG>;
   if (a.g.block_bytes != C::BB || tc_fp16_chunk(a.g) != C::CH) return cudaErrorInvalidValue;
   static KernelSetup setup;
   int occ = 0;
@@ -802,29 +833,32 @@ cudaError_t launch_gqa_t(TcArgs &a, int num_sms, cudaStream_t st) {
 
 // The template arguments the dispatch picks for a geometry.
 struct GqaVariant {
-  int ngv, km, rg;
+  int bits, ngv, km, rg;
 };
 GqaVariant gqa_variant(const Geometry &g) {
-  return GqaVariant{kD / g.v_group, g.k_group == 32 ? 1 : 0, g.Hq / g.H};
+  return GqaVariant{g.bits, kD / g.v_group, g.k_group == 32 ? 1 : 0, g.Hq / g.H};
 }
 
-template <int RG>
-cudaError_t launch_gqa_r(TcArgs &a, int num_sms, cudaStream_t st) {
+template <int BITS, int RG>
+cudaError_t launch_gqa_br(TcArgs &a, int num_sms, cudaStream_t st) {
   const GqaVariant v = gqa_variant(a.g);
   if (v.ngv == 4)
-    return v.km ? launch_gqa_t<4, 1, RG>(a, num_sms, st) : launch_gqa_t<4, 0, RG>(a, num_sms, st);
-  return v.km ? launch_gqa_t<2, 1, RG>(a, num_sms, st) : launch_gqa_t<2, 0, RG>(a, num_sms, st);
+    return v.km ? launch_gqa_t<BITS, 4, 1, RG>(a, num_sms, st)
+                : launch_gqa_t<BITS, 4, 0, RG>(a, num_sms, st);
+  return v.km ? launch_gqa_t<BITS, 2, 1, RG>(a, num_sms, st)
+              : launch_gqa_t<BITS, 2, 0, RG>(a, num_sms, st);
 }
 
 }  // namespace
 
 int gqa_variant_name(const Geometry &g, char *buf, size_t len) {
   const GqaVariant v = gqa_variant(g);
-  return snprintf(buf, len, "tc_gqa_kernel<ngv=%d,km=%d,rg=%d>", v.ngv, v.km, v.rg);
+  return snprintf(buf, len, "tc_gqa_kernel<bits=%d,ngv=%d,km=%d,rg=%d>", v.bits, v.ngv, v.km,
+                  v.rg);
 }
 
 bool gqa_decode_supported(const Geometry &g) {
-  if (g.d != kD || g.bits != 2 || g.scheme != KVQ_KIVI) return false;
+  if (g.d != kD || (g.bits != 2 && g.bits != 4) || g.scheme != KVQ_KIVI) return false;
   if (g.meta16 || g.vq || g.n_out || g.ragged) return false;
   const int rg = g.Hq / g.H;
   if (rg != 2 && rg != 4) return false;
@@ -875,7 +909,9 @@ cudaError_t launch_decode_gqa(const Geometry &g, const CachePtrs &p, int64_t n_q
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * rg * 2;
   a.wait_limit = 1 << 24;
   a.stall_limit = debug_stall_limit();
-  return rg == 4 ? launch_gqa_r<4>(a, num_sms, st) : launch_gqa_r<2>(a, num_sms, st);
+  if (g.bits == 4)
+    return rg == 4 ? launch_gqa_br<4, 4>(a, num_sms, st) : launch_gqa_br<4, 2>(a, num_sms, st);
+  return rg == 4 ? launch_gqa_br<2, 4>(a, num_sms, st) : launch_gqa_br<2, 2>(a, num_sms, st);
 }
 
 }  // namespace kvq

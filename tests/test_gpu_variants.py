@@ -36,9 +36,9 @@ def _innerq(bits, ngv, ngk, mf=False, ragged=False):
              ragged=ragged)
 
 
-def _gqa(ngv, G, rg):
-    return S(W["gqa_2bit"], batch=2, n_q_heads=2 * rg, n_kv_heads=2, ctx=900, k_group=G,
-             v_group=128 // ngv, residual=128, n_append=140)
+def _gqa(bits, ngv, G, rg):
+    return S(W["gqa_2bit"], batch=2, n_q_heads=2 * rg, n_kv_heads=2, ctx=900, bits=bits,
+             k_group=G, v_group=128 // ngv, residual=128, n_append=140)
 
 
 CASES = {}
@@ -58,8 +58,8 @@ for mf in (False, True):
     for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
         CASES["tc_innerq_b%d_ngv%d_ngk%d%s_ragged" % (bits, ngv, ngk, sfx)] = _innerq(
             bits, ngv, ngk, mf, ragged=True)
-for ngv, G, rg in itertools.product((2, 4), (32, 64), (2, 4)):
-    CASES["gqa_ngv%d_g%d_rg%d" % (ngv, G, rg)] = _gqa(ngv, G, rg)
+for bits, ngv, G, rg in itertools.product((2, 4), (2, 4), (32, 64), (2, 4)):
+    CASES["gqa_b%d_ngv%d_g%d_rg%d" % (bits, ngv, G, rg)] = _gqa(bits, ngv, G, rg)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -99,8 +99,8 @@ def test_every_dispatched_instantiation_has_a_parity_case():
     dispatched = dispatched_tensor_core_names()
     # MHA: 20 shapes with fp32 and with fp16 statistics, each plain and with
     # per-sequence lengths only, and the 12 KIVI shapes extended (outlier lists,
-    # value queue; InnerQ has neither); grouped-query: 8
-    assert len(dispatched) == 2 * (2 * 20 + 12) + 8, sorted(dispatched)
+    # value queue; InnerQ has neither); grouped-query: 8 for each code width
+    assert len(dispatched) == 2 * (2 * 20 + 12) + 16, sorted(dispatched)
     covered = {_name(w) for w in CASES.values()}
     assert dispatched <= covered, sorted(dispatched - covered)
     # and each named case reaches the instantiation its name says

@@ -122,13 +122,18 @@ GQA_CASES = [synth.WORKLOADS["gqa_2bit"],
              synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=2, n_q_heads=8, n_kv_heads=4,
                           ctx=900, k_group=64, v_group=64),
              synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=1, n_q_heads=4, n_kv_heads=1,
-                          ctx=1 << 20)]
+                          ctx=1 << 20),
+             synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=2, n_q_heads=8, n_kv_heads=2,
+                          ctx=900, bits=4),
+             synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=1, n_q_heads=4, n_kv_heads=1,
+                          ctx=1 << 20, bits=4, k_group=64)]
 
 
-@pytest.mark.parametrize("w", GQA_CASES, ids=lambda w: "%s_B%d_T%d" % (w.name, w.batch, w.ctx))
+@pytest.mark.parametrize("w", GQA_CASES,
+                         ids=lambda w: "%s_B%d_T%d_b%d" % (w.name, w.batch, w.ctx, w.bits))
 def test_gqa_split_never_exceeds_the_partial_slots(w):
     """Block counts up to 8 resident blocks on each of 152 SMs (the kernel
-    fits at most 2: 112 KB of shared memory per block)."""
+    fits at most 2: 112 KB of shared memory per block; 4-bit codes, 1)."""
     cfg = kvq.config_of(w)
     stride = _part_stride(cfg)
     BH = cfg.batch * cfg.n_kv_heads
