@@ -392,7 +392,7 @@ def run_gpu(args, w, rank, world):
             pre_ms.append(e0.elapsed_time(e1))
     del Kd, Vd
     n0, r0, s0 = caches[0].n_quant, caches[0].n_resid, caches[0].n_sink
-    states = [(c.n_quant, c.n_resid, c.n_sink, c.ring_head) for c in caches]
+    states = [(c.n_quant, c.n_resid, c.n_sink, c.ring_head, c.n_appended) for c in caches]
 
     Ks, Vs = synth.streamed(w, EPOCH)
     ks = torch.from_numpy(Ks).to(dev)
@@ -403,7 +403,8 @@ def run_gpu(args, w, rank, world):
 
     def restore():
         for c, st in zip(caches, states):
-            c.view.n_quant, c.view.n_resid, c.view.n_sink, c.view.ring_head = st
+            (c.view.n_quant, c.view.n_resid, c.view.n_sink, c.view.ring_head,
+             c.view.n_appended) = st
 
     rope = args.rope_base
 
@@ -815,16 +816,30 @@ FORMATS = {"meta_f16": dict(meta_f16=True), "outliers_2": dict(outliers=2),
            "value_queue": dict(v_queue=True), "ragged": dict(ragged=True)}
 
 
+# Derived shapes of the named workloads (decode kernel alone): the
+# grouped-query layer with 4-bit codes.
+VARIANTS = {"gqa_4bit": ("gqa_2bit", dict(bits=4))}
+
+
 def run_configs(names, peak, base=None):
-    """names: workloads (base None) or, with a base workload, FORMATS keys."""
+    """names: workloads (base None), FORMATS keys (a base workload), or
+    VARIANTS keys (base "variants")."""
     import torch
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     stream = torch.cuda.Stream(dev)
     out = {}
     for name in names:
-        w = synth.WORKLOADS[name] if base is None else synth.scaled(base, **FORMATS[name])
+        if base is None:
+            w = synth.WORKLOADS[name]
+        elif base == "variants":
+            w = synth.scaled(synth.WORKLOADS[VARIANTS[name][0]], **VARIANTS[name][1])
+        else:
+            w = synth.scaled(base, **FORMATS[name])
         try:
             out[name] = measure_config(w, dev, stream, peak)
+            if base == "variants":
+                out[name]["workload"] = "%s with %s" % (VARIANTS[name][0], ", ".join(
+                    "%s=%s" % kv for kv in sorted(VARIANTS[name][1].items())))
         except Exception as exc:  # noqa: BLE001 -- one config's failure drops only its line
             out[name] = {"error": ("%s: %s" % (type(exc).__name__, exc))[:300]}
         torch.cuda.synchronize(dev)
@@ -849,6 +864,9 @@ def main():
                     help="comma-separated cache-format options timed on the headline workload "
                          "(decode kernel alone; one GPU only): " + ", ".join(sorted(FORMATS)) +
                          "; 'all' or 'none'")
+    ap.add_argument("--variants", default="all",
+                    help="comma-separated derived shapes timed alone (one GPU only): " +
+                         ", ".join(sorted(VARIANTS)) + "; 'all' or 'none'")
     ap.add_argument("--rope-base", type=float, default=None,
                     help="time the variant whose keys are cached before the rotary embedding "
                          "(kvq_decode_attention_rope with this base) instead of the plain decode")
@@ -940,6 +958,10 @@ def main():
         names = (sorted(FORMATS) if args.formats == "all"
                  else [n for n in args.formats.split(",") if n])
         line["formats"] = run_configs(names, peak, base=w)
+    if world == 1 and args.variants != "none" and args.rope_base is None:
+        names = (sorted(VARIANTS) if args.variants == "all"
+                 else [n for n in args.variants.split(",") if n])
+        line["variants"] = run_configs(names, peak, base="variants")
     if rank == 0 and world == 1 and not args.skip_cpu:
         rate, threads, desc, _ = oracle_decode_rate(w, seconds=args.cpu_seconds,
                                                     rope_base=args.rope_base)
