@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG>::MINB))
   float *QT = reinterpret_cast<float *>(smem + C::lay(nslot, 1) + warp * C::QTB);
   uint64_t *wbars = reinterpret_cast<uint64_t *>(smem + C::lay(nslot, 2)) + warp * (nslot + 1);
 
+  grid_dep_trigger();  // the next decode's blocks may take the SMs this grid leaves
   int x0, x1;
   block_range(a, blockIdx.x, x0, x1);
   const int bh_first = x0 / a.U, bh_last = (x1 - 1) / a.U;
@@ -321,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG>::MINB))
     pc_settle();
   };
   pc_settle();
+  grid_dep_wait();  // the previous grid on the stream has drained: device data from here on
   for (int s = 0; s < nslot; ++s) issue_next();
 
   // ---- per-head query table: q_r[c] * scale_log2 * 2^-E_r at qt_index(c, r),

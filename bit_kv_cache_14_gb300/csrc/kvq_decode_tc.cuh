@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   constexpr TcLayout Ly = tc_layout(SLOT, nslot, SC::SBB, SC::CSB);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  grid_dep_trigger();  // the next decode's blocks may take the SMs this grid leaves
   // The rotary form's table: entry [L][j] = (cos j theta_2L, cos j theta_2L+1,
   // sin j theta_2L, sin j theta_2L+1) for token offsets j < 32 (pair-pair L =
   // channels 4L .. 4L + 3), built once by the block.
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
   // (OUT: per-sequence lengths lay the heads out by their own units)
   ExtRange rx{};
   if constexpr (OUT != 0) {
+    grid_dep_wait();  // the per-sequence counters are device data
     rx = ext_range(a, gw);
     if (gw >= rx.nw) return;
   }
@@ -373,6 +375,9 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
     pc_settle();
   };
   pc_settle();
+  // the previous grid on the stream has drained: device data from here on
+  // (under per-sequence lengths the wait came before the counters' reads)
+  if constexpr (OUT == 0) grid_dep_wait();
   for (int s = 0; s < nslot; ++s) issue_next();
 
   // ---- per-head constants (each warp for itself) --------------------------

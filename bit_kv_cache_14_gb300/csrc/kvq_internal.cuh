@@ -206,11 +206,16 @@ cudaError_t launch_cooperative(void (*kern)(P...), unsigned grid, unsigned threa
   c.blockDim = dim3(threads);
   c.dynamicSmemBytes = (size_t)smem;
   c.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  // programmatic dependent launch: the kernel may start while the previous
+  // grid on the stream drains; it waits for it (griddepcontrol.wait) before
+  // its first access to global memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   c.attrs = attr;
-  c.numAttrs = 1;
+  c.numAttrs = 2;
   return cudaLaunchKernelEx(&c, kern, static_cast<A &&>(args)...);
 }
 CachePtrs ptrs_of(const Geometry &g, const kvq_cache *c);

@@ -235,6 +235,17 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, uint32_t parity, int lim
   return bar_wait(smem_u32(bar), parity, limit);
 }
 
+// Programmatic dependent launch (the launch attribute set by
+// launch_cooperative).  grid_dep_trigger: the next launch on the stream may
+// start its blocks as this grid's blocks leave the SMs.  grid_dep_wait: wait
+// until the previous grid on the stream has completed and its writes are
+// visible; nothing before it may read or write global memory that another
+// kernel writes (a launch without the attribute returns at once).
+__device__ __forceinline__ void grid_dep_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
                                          uint64_t *bar) {
   asm volatile(
