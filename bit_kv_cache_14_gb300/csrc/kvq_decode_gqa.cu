@@ -457,9 +457,9 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG>::MINB))
         const int j = mt / MPJ, m = mt % MPJ;
         const int W = j * WPG + gid % WPG, p = m * NV + v_off;
         // the code sat at position ps of its source half word (the high
-        // positions after the shift by a byte): 2^24 * 2^8 / pos_factor
+        // positions after the shift by a byte): 2^24 * 2^kSlack / pos_factor
         const int ps = p % (PH / 2);
-        const float f = __int_as_float((127 + 32 - BITS * ps) << 23);
+        const float f = __int_as_float((127 + 24 + kSlackLog2 - BITS * ps) << 23);
         so[tig * kD + CPW * W + p] = fmaf(dv[mt][0] + dv[mt][1], f, Z[j]);
         so[tig * kD + CPW * W + PH + p] = fmaf(dv[mt][2] + dv[mt][3], f, Z[j]);
       }
@@ -672,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG>::MINB))
         // ---- values: per value group j, its 16-row tiles and columns (r, hi/lo)
         // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) of k-block kb carry
         // tokens 16kb + tig + {0, 8} and + {4, 12}.  The operand B[t][(r,
-        // hi/lo)] = p_tr * scale_tj * 2^-8 is written once, by the lane that
+        // hi/lo)] = p_tr * scale_tj * 2^-kSlack is written once, by the lane that
         // holds p_tr (head tig, tokens gid + 8i): a token pair (t, t + 8) of one
         // column is one 32-bit word, at [j][kb][column slot][tig'][2 words] in
         // the warp's operand area (the key operand is consumed by now); each

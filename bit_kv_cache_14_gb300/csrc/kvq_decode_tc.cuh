@@ -994,7 +994,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
           // MMA k pairs (2tig, 2tig+1) and (2tig+8, 2tig+9) of k-block kb carry
           // tokens 16kb + tig + {0, 4} and + {8, 12} (code rows 4 apart hit
           // distinct banks).  Each token's lane writes its operand row
-          // B[t][(j, hi/lo)] = p_t * scale_tj * 2^-8 as fp16 hi + lo into the
+          // B[t][(j, hi/lo)] = p_t * scale_tj * 2^-kSlack as fp16 hi + lo into the
           // warp's operand area (the key operand is consumed by now), laid out
           // [column][kb][tig][4 tokens] so each lane then loads the fragment of
           // a k-block with one 64-bit load.

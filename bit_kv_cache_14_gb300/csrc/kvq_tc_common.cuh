@@ -77,11 +77,19 @@ constexpr int kTile = 32;     // tokens per warp tile (two 16-token MMA tiles)
 constexpr int kD = 128;
 constexpr float kSub = 16777216.0f;  // 2^24: undoes the subnormal scale of the code operands
 // Lazy online softmax: probabilities are taken against a running reference
-// that may sit up to kSlack (log2 units) below the true maximum, so p <= 2^8;
-// the value operand carries p * 2^-8 and the output row multiplies it back.
-constexpr float kSlack = 8.0f;
-constexpr float kSlackScale = 256.0f;
-constexpr float kInvSlack = 1.0f / 256.0f;
+// that may sit up to kSlack (log2 units) below the true maximum, so p <=
+// 2^kSlack; the value operand carries p * 2^-kSlack * scale (at most the
+// value scale: within fp16 range) and the output row multiplies it back.
+// The slack is small because the operand's fp16 hi + lo split is exact to
+// about 2^-22 only above fp16's normal minimum 2^-14: a weight p whose
+// p * 2^-kSlack * scale falls below it keeps only an absolute 2^-25, and
+// over thousands of tokens those errors add up to an offset of the output
+// (on a head whose softmax is held by a few tokens, 2e-3 with a slack of 8).
+// A larger reference jump costs one rescale of the accumulators.
+constexpr int kSlackLog2 = 2;
+constexpr float kSlack = (float)kSlackLog2;
+constexpr float kSlackScale = (float)(1 << kSlackLog2);
+constexpr float kInvSlack = 1.0f / kSlackScale;
 constexpr int kDrainLimit = 1 << 26;
 
 
