@@ -741,13 +741,13 @@ __global__ void __launch_bounds__(kThreads, 2) tc_decode_kernel(const TcArgs a) 
         const int n = min(kTile, tq1 - tok0);
         auto tile = [&](auto full_c) {
           constexpr bool FULL = decltype(full_c)::value;
-          const uint8_t *kc = slot;
           const uint8_t *vc = slot + SC::off_vc;
           const int t = lane;
           float score;
           if constexpr (RP != 0) {
             score = rope_score(slot, t, tok0);
           } else {
+            const uint8_t *kc = slot;
             // ------------- keys: two 16-token MMA tiles ------------------------
             float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
             float bias0 = 0.0f, bias1 = 0.0f;
