@@ -91,7 +91,7 @@ def _gqa_max_parts(cfg, BH, n_quant, n_fp16, blocks):
     cap = (cfg.max_ctx + 127) // 128 * 128
     block_bytes = s.blocks // (BH * (cap // 32))
     ch = _fp16_chunk(cfg)
-    kmb = 2 * 128 * 4 if cfg.k_group > 32 else 0
+    kmb = 2 * 128 * 4 if cfg.scheme == kvq.KIVI and cfg.k_group > 32 else 0
     cpu = max(1, (128 // 32) * (block_bytes + kmb) // (ch * 4 * 128))
     nch = -(-n_fp16 // ch) if n_fp16 else 0
     S_h, F_h = -(-n_quant // 128), -(-nch // cpu)
@@ -126,7 +126,11 @@ GQA_CASES = [synth.WORKLOADS["gqa_2bit"],
              synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=2, n_q_heads=8, n_kv_heads=2,
                           ctx=900, bits=4),
              synth.scaled(synth.WORKLOADS["gqa_2bit"], batch=1, n_q_heads=4, n_kv_heads=1,
-                          ctx=1 << 20, bits=4, k_group=64)]
+                          ctx=1 << 20, bits=4, k_group=64),
+             synth.scaled(synth.WORKLOADS["innerq_1m"], batch=2, n_q_heads=8, n_kv_heads=2,
+                          ctx=700),
+             synth.scaled(synth.WORKLOADS["innerq_1m"], batch=1, n_q_heads=8, n_kv_heads=4,
+                          bits=2, k_group=32)]
 
 
 @pytest.mark.parametrize("w", GQA_CASES,
