@@ -818,8 +818,10 @@ FORMATS = {"meta_f16": dict(meta_f16=True), "outliers_2": dict(outliers=2),
 
 
 # Derived shapes of the named workloads (decode kernel alone): the
-# grouped-query layer with 4-bit codes.
-VARIANTS = {"gqa_4bit": ("gqa_2bit", dict(bits=4))}
+# grouped-query layer with 4-bit codes, and the InnerQ cache on the
+# grouped-query layer's shape (B64, 32 query / 8 KV heads, 16384 tokens).
+VARIANTS = {"gqa_4bit": ("gqa_2bit", dict(bits=4)),
+            "innerq_gqa": ("innerq_1m", dict(batch=64, n_q_heads=32, n_kv_heads=8, ctx=16384))}
 
 
 def run_configs(names, peak, base=None):

@@ -109,6 +109,6 @@ def test_gpu_line_contract(line, rope):
         # and each cache-format option on the headline layer
         assert sorted(d["formats"]) == ["meta_f16", "outliers_2", "ragged", "value_queue"]
         # and the derived shapes (the grouped-query layer with 4-bit codes)
-        assert sorted(d["variants"]) == ["gqa_4bit"]
+        assert sorted(d["variants"]) == ["gqa_4bit", "innerq_gqa"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]

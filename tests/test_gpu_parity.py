@@ -223,10 +223,12 @@ def _sample_heads(w, n=3):
     return sorted(set(picks))[:n]
 
 
-# the named workloads, and the grouped-query layer with 4-bit codes (the
-# benchmark's derived shape)
+# the named workloads, the grouped-query layer with 4-bit codes and the
+# InnerQ cache on the grouped-query layer's shape (the benchmark's derived
+# shapes)
 FULL_SIZE = {n: W[n] for n in ("llama2_7b_2bit", "kivi_4bit", "gqa_2bit", "innerq_1m")}
 FULL_SIZE["gqa_4bit"] = S(W["gqa_2bit"], bits=4)
+FULL_SIZE["innerq_gqa"] = S(W["innerq_1m"], batch=64, n_q_heads=32, n_kv_heads=8, ctx=16384)
 
 
 @pytest.mark.slow
