@@ -44,8 +44,8 @@ bool gqa_decode_supported(const Geometry &g) {
   if (rg != 2 && rg != 4) return false;
   const int ngv = kD / g.v_group;
   if (ngv != 2 && ngv != 4) return false;
-  if (g.scheme == KVQ_INNERQ)  // channel groups of 32 or 64; not the folded key normalization
-    return !g.knorm && (g.k_group == 32 || g.k_group == 64);
+  if (g.scheme == KVQ_INNERQ)  // channel groups of 32 or 64
+    return g.k_group == 32 || g.k_group == 64;
   return g.scheme == KVQ_KIVI && g.k_group >= 32 && g.k_group <= 128;
 }
 

@@ -372,19 +372,35 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
 #pragma unroll
   for (int gq = 0; gq < (NGK > 0 ? NGK : 1); ++gq) qsum[gq] = 0.0f;
   int q_head = -1;
-  auto load_q = [&](int bh) {
+  // query head r of KV head bh, this lane's channels 4 lane .. 4 lane + 3,
+  // times scale_log2
+  auto raw_q = [&](int bh, int r, float (&v)[4]) {
     const int b = bh / g.H, h = bh % g.H;
+    const uint2 qr =
+        __ldg(reinterpret_cast<const uint2 *>(a.q + ((int64_t)b * g.Hq + h * RG + r) * kD) + lane);
+    const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
+    const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
+    v[0] = q01.x * a.scale_log2;
+    v[1] = q01.y * a.scale_log2;
+    v[2] = q23.x * a.scale_log2;
+    v[3] = q23.y * a.scale_log2;
+  };
+  // InnerQ with normalized keys: the per-channel factors go into the table's
+  // query (the codes' side; the fp16 rows take the raw query)
+  const bool knorm = INQ && g.knorm;
+  auto load_q = [&](int bh) {
     float qv[RG][4];
 #pragma unroll
-    for (int r = 0; r < RG; ++r) {
-      const uint2 qr = __ldg(reinterpret_cast<const uint2 *>(
-                                 a.q + ((int64_t)b * g.Hq + h * RG + r) * kD) + lane);
-      const float2 q01 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.x));
-      const float2 q23 = __half22float2(*reinterpret_cast<const __half2 *>(&qr.y));
-      qv[r][0] = q01.x * a.scale_log2;
-      qv[r][1] = q01.y * a.scale_log2;
-      qv[r][2] = q23.x * a.scale_log2;
-      qv[r][3] = q23.y * a.scale_log2;
+    for (int r = 0; r < RG; ++r) raw_q(bh, r, qv[r]);
+    if (knorm) {
+      const float4 n4 = reinterpret_cast<const float4 *>(a.p.k_norm + (int64_t)bh * kD)[lane];
+#pragma unroll
+      for (int r = 0; r < RG; ++r) {
+        qv[r][0] *= n4.x;
+        qv[r][1] *= n4.y;
+        qv[r][2] *= n4.z;
+        qv[r][3] *= n4.w;
+      }
     }
     float e2[RG];
 #pragma unroll
@@ -917,9 +933,13 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
 #pragma unroll
       for (int r = 0; r < RG; ++r) {
         const float e = QT[4 * kD + r];
+        if (knorm) {
+          raw_q(bh, r, qq[r]);
+        } else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          qq[r][i] = QT[INQ ? iq_index<BITS>(4 * lane + i, r) : qt_index<BITS>(4 * lane + i, r)] * e;
+          for (int i = 0; i < 4; ++i)
+            qq[r][i] = QT[INQ ? iq_index<BITS>(4 * lane + i, r) : qt_index<BITS>(4 * lane + i, r)] * e;
+        }
         mf[r] = -INFINITY;
         lf[r] = 0.0f;
 #pragma unroll

@@ -36,12 +36,12 @@ def _innerq(bits, ngv, ngk, mf=False, ragged=False):
              ragged=ragged)
 
 
-def _gqa_iq(bits, ngv, ngk, rg):
+def _gqa_iq(bits, ngv, ngk, rg, knorm=False):
     # 700 prompt tokens: 4 sinks, a 32-token window, 664 quantized (a short
     # last tile), and every append moves one more token into the quantized
     # region
     return S(W["innerq_1m"], batch=2, n_q_heads=2 * rg, n_kv_heads=2, ctx=700, bits=bits,
-             k_group=128 // ngk, v_group=128 // ngv, n_append=40)
+             k_group=128 // ngk, v_group=128 // ngv, n_append=40, k_norm=knorm)
 
 
 def _gqa(bits, ngv, G, rg):
@@ -71,6 +71,10 @@ for bits, ngv, G, rg in itertools.product((2, 4), (2, 4), (32, 64), (2, 4)):
     # InnerQ keys: the same four axes, with G read as 128 / key channel groups
     CASES["gqa_innerq_b%d_ngv%d_ngk%d_rg%d" % (bits, ngv, 128 // G, rg)] = _gqa_iq(
         bits, ngv, 128 // G, rg)
+# InnerQ's folded key normalization on the grouped-query kernel (a run-time
+# flag of the same instantiations)
+CASES["gqa_innerq_knorm_b2_ngv4_ngk4_rg2"] = _gqa_iq(2, 4, 4, 2, knorm=True)
+CASES["gqa_innerq_knorm_b4_ngv2_ngk2_rg4"] = _gqa_iq(4, 2, 2, 4, knorm=True)
 
 
 @pytest.fixture(scope="module", autouse=True)
