@@ -92,6 +92,15 @@ EDGE = {
     # InnerQ without sinks
     "innerq_no_sink": S(W["innerq_1m"], batch=1, n_q_heads=2, n_kv_heads=2, ctx=300, n_sink=0,
                         n_append=10),
+    # the grouped-query kernel's corners: quantized tokens arriving one at a
+    # time (a single short tile of 1, 2, ... tokens), no fp16 rows at all, and
+    # a KIVI prompt shorter than R that reaches its first flush
+    "innerq_gqa_prompt_lt_sink": S(W["innerq_1m"], batch=2, n_q_heads=8, n_kv_heads=2, ctx=2,
+                                   n_append=50),
+    "innerq_gqa_no_window_no_sink": S(W["innerq_1m"], batch=2, n_q_heads=8, n_kv_heads=2, ctx=300,
+                                      residual=0, n_sink=0, n_append=10),
+    "kivi_gqa_short_prompt": S(W["gqa_2bit"], batch=2, n_q_heads=8, n_kv_heads=2, ctx=100,
+                               n_append=40),
 }
 
 
