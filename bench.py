@@ -173,7 +173,8 @@ DECODE_SOURCES = ("kvq_decode_tc.cuh", "kvq_decode_tc.cu", "kvq_tc_common.cuh", 
 ROPE_SOURCES = ("kvq_decode_tc.cuh", "kvq_decode_tc_rope.cu", "kvq_tc_common.cuh", "kvq_rope.cuh",
                 "kvq_internal.cuh")
 GQA_SOURCES = ("kvq_decode_gqa.cuh", "kvq_decode_gqa.cu", "kvq_decode_gqa_iq.cu",
-               "kvq_tc_common.cuh", "kvq_internal.cuh")
+               "kvq_decode_gqa_f16.cu", "kvq_decode_gqa_iq16.cu", "kvq_tc_common.cuh",
+               "kvq_internal.cuh")
 
 
 def decode_source_sha(names=DECODE_SOURCES):

@@ -8,38 +8,30 @@ namespace {
 
 // The template arguments the dispatch picks for a geometry.
 struct GqaVariant {
-  int bits, ngv, km, rg, ngk;  // ngk: InnerQ key channel groups (0: KIVI)
+  int bits, ngv, km, rg, ngk, mf;  // ngk: InnerQ key channel groups (0: KIVI)
 };
 GqaVariant gqa_variant(const Geometry &g) {
+  const int mf = g.meta16 ? 1 : 0;
   if (g.scheme == KVQ_INNERQ)
-    return GqaVariant{g.bits, kD / g.v_group, 0, g.Hq / g.H, kD / g.k_group};
-  return GqaVariant{g.bits, kD / g.v_group, g.k_group == 32 ? 1 : 0, g.Hq / g.H, 0};
-}
-
-template <int BITS, int RG>
-cudaError_t launch_gqa_br(TcArgs &a, int num_sms, cudaStream_t st) {
-  const GqaVariant v = gqa_variant(a.g);
-  if (v.ngv == 4)
-    return v.km ? launch_gqa_t<BITS, 4, 1, RG>(a, num_sms, st)
-                : launch_gqa_t<BITS, 4, 0, RG>(a, num_sms, st);
-  return v.km ? launch_gqa_t<BITS, 2, 1, RG>(a, num_sms, st)
-              : launch_gqa_t<BITS, 2, 0, RG>(a, num_sms, st);
+    return GqaVariant{g.bits, kD / g.v_group, 0, g.Hq / g.H, kD / g.k_group, mf};
+  return GqaVariant{g.bits, kD / g.v_group, g.k_group == 32 ? 1 : 0, g.Hq / g.H, 0, mf};
 }
 
 }  // namespace
 
 int gqa_variant_name(const Geometry &g, char *buf, size_t len) {
   const GqaVariant v = gqa_variant(g);
+  const char *mf = v.mf ? ",mf=1" : "";
   if (v.ngk)
-    return snprintf(buf, len, "tc_gqa_kernel<bits=%d,scheme=innerq,ngv=%d,ngk=%d,rg=%d>", v.bits,
-                    v.ngv, v.ngk, v.rg);
-  return snprintf(buf, len, "tc_gqa_kernel<bits=%d,ngv=%d,km=%d,rg=%d>", v.bits, v.ngv, v.km,
-                  v.rg);
+    return snprintf(buf, len, "tc_gqa_kernel<bits=%d,scheme=innerq,ngv=%d,ngk=%d,rg=%d%s>", v.bits,
+                    v.ngv, v.ngk, v.rg, mf);
+  return snprintf(buf, len, "tc_gqa_kernel<bits=%d,ngv=%d,km=%d,rg=%d%s>", v.bits, v.ngv, v.km,
+                  v.rg, mf);
 }
 
 bool gqa_decode_supported(const Geometry &g) {
   if (g.d != kD || (g.bits != 2 && g.bits != 4)) return false;
-  if (g.meta16 || g.vq || g.n_out || g.ragged) return false;
+  if (g.vq || g.n_out || g.ragged) return false;
   const int rg = g.Hq / g.H;
   if (rg != 2 && rg != 4) return false;
   const int ngv = kD / g.v_group;
@@ -92,10 +84,9 @@ cudaError_t launch_decode_gqa(const Geometry &g, const CachePtrs &p, int64_t n_q
   a.ws_o = a.ws_ml + (size_t)BH * a.part_stride * rg * 2;
   a.wait_limit = 1 << 24;
   a.stall_limit = debug_stall_limit();
-  if (g.scheme == KVQ_INNERQ) return launch_gqa_innerq(a, num_sms, st);
-  if (g.bits == 4)
-    return rg == 4 ? launch_gqa_br<4, 4>(a, num_sms, st) : launch_gqa_br<4, 2>(a, num_sms, st);
-  return rg == 4 ? launch_gqa_br<2, 4>(a, num_sms, st) : launch_gqa_br<2, 2>(a, num_sms, st);
+  if (g.scheme == KVQ_INNERQ)
+    return g.meta16 ? launch_gqa_innerq_f16(a, num_sms, st) : launch_gqa_innerq(a, num_sms, st);
+  return g.meta16 ? launch_gqa_kivi_f16(a, num_sms, st) : launch_kivi<0>(a, num_sms, st);
 }
 
 }  // namespace kvq

@@ -36,19 +36,20 @@ namespace {
 
 // NGK = 0: KIVI keys (per-channel statistics over G tokens; KM = 1 when G =
 // 32 puts them inside the block); NGK = 2 or 4: InnerQ keys (per token, NGK
-// groups of channels; KM unused).
-template <int BITS, int NGV, int KM, int RG, int NGK = 0>
+// groups of channels; KM unused).  MF: statistics stored in fp16.
+template <int BITS, int NGV, int KM, int RG, int NGK = 0, int MF = 0>
 struct GqaCfg {
   static constexpr bool INQ = NGK > 0;
+  static constexpr int MSZ = MF ? 2 : 4;    // bytes per stored statistic
   static constexpr int RB = kD * BITS / 8;  // bytes per token row of codes
   static constexpr int off_vc = kTile * RB;
   static constexpr int off_vs = 2 * kTile * RB;
-  static constexpr int off_vz = off_vs + kTile * NGV * 4;
-  static constexpr int off_ks = off_vz + kTile * NGV * 4;
-  static constexpr int off_kz = off_ks + kTile * NGK * 4;  // InnerQ: [token][group]
+  static constexpr int off_vz = off_vs + kTile * NGV * MSZ;
+  static constexpr int off_ks = off_vz + kTile * NGV * MSZ;
+  static constexpr int off_kz = off_ks + kTile * NGK * MSZ;  // InnerQ: [token][group]
   static constexpr bool KIN = !INQ && KM >= 1;  // KIVI G = 32: key statistics inside the block
-  static constexpr int KGB = 2 * kD * 4;
-  static constexpr int BB = INQ ? off_kz + kTile * NGK * 4 : off_ks + (KIN ? KGB : 0);
+  static constexpr int KGB = 2 * kD * MSZ;
+  static constexpr int BB = INQ ? off_kz + kTile * NGK * MSZ : off_ks + (KIN ? KGB : 0);
   static constexpr int KMB = (INQ || KIN) ? 0 : KGB;
   static constexpr int off_km = KIN ? off_ks : BB;
   static constexpr int bytes = BB + KMB;  // one slot (no query rows in the ring)
@@ -256,11 +257,11 @@ __device__ __forceinline__ int iq_index(int c, int r) {
   return (r * 32 + L) * 4 + 2 * (c & 1) + h;
 }
 
-template <int BITS, int NGV, int KM, int RG, int NGK = 0>
-__global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MINB))
+template <int BITS, int NGV, int KM, int RG, int NGK = 0, int MF = 0>
+__global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK, MF>::MINB))
     tc_gqa_kernel(const TcArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  using C = GqaCfg<BITS, NGV, KM, RG, NGK>;
+  using C = GqaCfg<BITS, NGV, KM, RG, NGK, MF>;
   constexpr bool INQ = C::INQ;
   constexpr int RB = C::RB;
   constexpr int nslot = C::nslot;
@@ -614,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
           }
           // per-token scales and zeros: [token][group] rows, read per group
           // next to their use
-          const float *ksr = reinterpret_cast<const float *>(slot + C::off_ks) + gid * NGK;
+          const uint8_t *ksr = slot + C::off_ks + gid * NGK * C::MSZ;
           __syncwarp();
           // ---- keys: per channel group, D_g[token][(r, hi/lo)] over its
           // k-steps, weighted by the token's scale of that group
@@ -656,24 +657,17 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
               mma16816(e0, w[0] & M0, w[1] & M0, w[0] & M1, w[1] & M1, b.x, b.y);
               mma16816(e1, w[2] & M0, w[3] & M0, w[2] & M1, w[3] & M1, b.x, b.y);
             }
-            acc[0] = fmaf(ksr[gq], e0[0] + e0[1], acc[0]);
-            acc[1] = fmaf(ksr[8 * NGK + gq], e0[2] + e0[3], acc[1]);
-            acc[2] = fmaf(ksr[16 * NGK + gq], e1[0] + e1[1], acc[2]);
-            acc[3] = fmaf(ksr[24 * NGK + gq], e1[2] + e1[3], acc[3]);
+            acc[0] = fmaf(ld_stat<MF>(ksr, gq), e0[0] + e0[1], acc[0]);
+            acc[1] = fmaf(ld_stat<MF>(ksr, 8 * NGK + gq), e0[2] + e0[3], acc[1]);
+            acc[2] = fmaf(ld_stat<MF>(ksr, 16 * NGK + gq), e1[0] + e1[1], acc[2]);
+            acc[3] = fmaf(ld_stat<MF>(ksr, 24 * NGK + gq), e1[2] + e1[3], acc[3]);
           }
           // ---- scores: (sum_g scale * D_g * 2^24 + sum_g zero * q-sum_g) * 2^E;
           // tokens past the head's quantized end (a short last tile) -inf
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float *kzr = reinterpret_cast<const float *>(slot + C::off_kz) + (gid + 8 * i) * NGK;
             float zk[NGK];
-            if constexpr (NGK == 4) {
-              const float4 b4 = *reinterpret_cast<const float4 *>(kzr);
-              zk[0] = b4.x, zk[1] = b4.y, zk[2] = b4.z, zk[3] = b4.w;
-            } else {
-              const float2 b2 = *reinterpret_cast<const float2 *>(kzr);
-              zk[0] = b2.x, zk[1] = b2.y;
-            }
+            ld_stat_row<MF, NGK>(slot + C::off_kz + (gid + 8 * i) * NGK * C::MSZ, zk);
             float zt = 0.0f;
 #pragma unroll
             for (int gq = 0; gq < NGK; ++gq) zt = fmaf(zk[gq], qsum[gq], zt);
@@ -683,15 +677,16 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
         } else {
           // ---- key operand: columns (r, hi/lo) of QT * scale / pos_factor(p), and the
           // per-head bias sum_c QT * zero, for this tile's key group
-          const float *ks = reinterpret_cast<const float *>(slot + C::off_km), *kz = ks + kD;
+          const uint8_t *ks = slot + C::off_km, *kz = ks + kD * C::MSZ;
           float2 bacc[RG];
 #pragma unroll
           for (int r = 0; r < RG; ++r) bacc[r] = make_float2(0.f, 0.f);
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
             const int clo = b_clo[m], chi = clo + PH;
-            const float2 s2 = __fmul2_rn(make_float2(ks[clo], ks[chi]), b_ipf[m]);
-            const float2 zz = make_float2(kz[clo], kz[chi]);
+            const float2 s2 =
+                __fmul2_rn(make_float2(ld_stat<MF>(ks, clo), ld_stat<MF>(ks, chi)), b_ipf[m]);
+            const float2 zz = make_float2(ld_stat<MF>(kz, clo), ld_stat<MF>(kz, chi));
             const float4 q01 = reinterpret_cast<const float4 *>(QT)[(2 * m) * 32 + lane];
             const float4 q23 = RG > 2 ? reinterpret_cast<const float4 *>(QT)[(2 * m + 1) * 32 + lane] : q01;
 #pragma unroll
@@ -811,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
         float2 pv[2];
         {
           const float2 mr = make_float2(m_run, m_run);
-          const float *vz = reinterpret_cast<const float *>(slot + C::off_vz);
+          const uint8_t *vz = slot + C::off_vz;
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
             const float2 e = __ffma2_rn(mr, neg1, make_float2(sc[2 * k], sc[2 * k + 1]));
@@ -822,20 +817,16 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
             for (int h = 0; h < 2; ++h) {
               const float pi = h ? p.y : p.x;
               const float2 pp = make_float2(pi, pi);
-              const float *zr = vz + (gid + 8 * (2 * k + h)) * NGV;
+              float zv[NGV];
+              ld_stat_row<MF, NGV>(vz + (gid + 8 * (2 * k + h)) * NGV * C::MSZ, zv);
               // (a token past a short tile's end has weight 0; its statistics
               // need not be finite)
               const bool okz = full || tok0 + gid + 8 * (2 * k + h) < tq1;
-              if constexpr (NGV == 4) {
-                float4 z4 = *reinterpret_cast<const float4 *>(zr);
-                if (!okz) z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                z2[0] = __ffma2_rn(pp, make_float2(z4.x, z4.y), z2[0]);
-                z2[1] = __ffma2_rn(pp, make_float2(z4.z, z4.w), z2[1]);
-              } else {
-                float2 z = *reinterpret_cast<const float2 *>(zr);
-                if (!okz) z = make_float2(0.f, 0.f);
-                z2[0] = __ffma2_rn(pp, z, z2[0]);
-              }
+#pragma unroll
+              for (int j = 0; j < NGV; ++j) zv[j] = okz ? zv[j] : 0.0f;
+#pragma unroll
+              for (int jp = 0; jp < NGV / 2; ++jp)
+                z2[jp] = __ffma2_rn(pp, make_float2(zv[2 * jp], zv[2 * jp + 1]), z2[jp]);
             }
           }
         }
@@ -848,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
         // the warp's operand area (the key operand is consumed by now); each
         // lane then loads its fragment of (kb, j) with one 64-bit load.
         {
-          const float *vs = reinterpret_cast<const float *>(slot + C::off_vs);
+          const uint8_t *vs = slot + C::off_vs;
           __syncwarp();  // every lane's key-operand loads are done
 #pragma unroll
           for (int kb = 0; kb < 2; ++kb) {
@@ -856,15 +847,15 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
             // value groups (j, j + 1), then packed per group as (a, b)
             const float2 paa = make_float2(pv[kb].x, pv[kb].x), pbb = make_float2(pv[kb].y, pv[kb].y);
             float2 sa[NGV / 2], sb[NGV / 2];
-            const float *ra = vs + (gid + 16 * kb) * NGV, *rb = ra + 8 * NGV;
-            if constexpr (NGV == 4) {
-              const float4 x = *reinterpret_cast<const float4 *>(ra);
-              const float4 y = *reinterpret_cast<const float4 *>(rb);
-              sa[0] = make_float2(x.x, x.y), sa[1] = make_float2(x.z, x.w);
-              sb[0] = make_float2(y.x, y.y), sb[1] = make_float2(y.z, y.w);
-            } else {
-              sa[0] = *reinterpret_cast<const float2 *>(ra);
-              sb[0] = *reinterpret_cast<const float2 *>(rb);
+            {
+              float xa[NGV], xb[NGV];
+              ld_stat_row<MF, NGV>(vs + (gid + 16 * kb) * NGV * C::MSZ, xa);
+              ld_stat_row<MF, NGV>(vs + (gid + 16 * kb + 8) * NGV * C::MSZ, xb);
+#pragma unroll
+              for (int jp = 0; jp < NGV / 2; ++jp) {
+                sa[jp] = make_float2(xa[2 * jp], xa[2 * jp + 1]);
+                sb[jp] = make_float2(xb[2 * jp], xb[2 * jp + 1]);
+              }
             }
             if (!full) {
               const bool oka = tok0 + gid + 16 * kb < tq1, okb = tok0 + gid + 16 * kb + 8 < tq1;
@@ -996,10 +987,10 @@ __global__ void __launch_bounds__(kThreads, (GqaCfg<BITS, NGV, KM, RG, NGK>::MIN
       bar_wait(&wbars[i % nslot], (uint32_t)((i / nslot) & 1), kDrainLimit);
 }
 
-template <int BITS, int NGV, int KM, int RG, int NGK = 0>
+template <int BITS, int NGV, int KM, int RG, int NGK = 0, int MF = 0>
 cudaError_t launch_gqa_t(TcArgs &a, int num_sms, cudaStream_t st) {
-  using C = GqaCfg<BITS, NGV, KM, RG, NGK>;
-  auto kern = tc_gqa_kernel<BITS, NGV, KM, RG, NGK>;
+  using C = GqaCfg<BITS, NGV, KM, RG, NGK, MF>;
+  auto kern = tc_gqa_kernel<BITS, NGV, KM, RG, NGK, MF>;
   if (a.g.block_bytes != C::BB || tc_fp16_chunk(a.g) != C::CH) return cudaErrorInvalidValue;
   static KernelSetup setup;
   int occ = 0;
@@ -1016,10 +1007,54 @@ cudaError_t launch_gqa_t(TcArgs &a, int num_sms, cudaStream_t st) {
   return le != cudaSuccess ? le : cudaGetLastError();
 }
 
+// The instantiation the geometry names, for statistics in fp32 (MF = 0) or
+// fp16 (MF = 1): KIVI keys (value groups, key statistics inside the block or
+// not) and InnerQ keys (value groups, key channel groups), over the code width
+// and the query heads per KV head.
+template <int MF, int BITS, int RG>
+cudaError_t launch_kivi_br(TcArgs &a, int num_sms, cudaStream_t st) {
+  const int ngv = kD / a.g.v_group, km = a.g.k_group == 32 ? 1 : 0;
+  if (ngv == 4)
+    return km ? launch_gqa_t<BITS, 4, 1, RG, 0, MF>(a, num_sms, st)
+              : launch_gqa_t<BITS, 4, 0, RG, 0, MF>(a, num_sms, st);
+  return km ? launch_gqa_t<BITS, 2, 1, RG, 0, MF>(a, num_sms, st)
+            : launch_gqa_t<BITS, 2, 0, RG, 0, MF>(a, num_sms, st);
+}
+template <int MF>
+cudaError_t launch_kivi(TcArgs &a, int num_sms, cudaStream_t st) {
+  const int rg = a.g.Hq / a.g.H;
+  if (a.g.bits == 4)
+    return rg == 4 ? launch_kivi_br<MF, 4, 4>(a, num_sms, st) : launch_kivi_br<MF, 4, 2>(a, num_sms, st);
+  return rg == 4 ? launch_kivi_br<MF, 2, 4>(a, num_sms, st) : launch_kivi_br<MF, 2, 2>(a, num_sms, st);
+}
+template <int MF, int BITS, int RG>
+cudaError_t launch_innerq_br(TcArgs &a, int num_sms, cudaStream_t st) {
+  const int ngv = kD / a.g.v_group, ngk = kD / a.g.k_group;
+  if (ngv == 4)
+    return ngk == 4 ? launch_gqa_t<BITS, 4, 0, RG, 4, MF>(a, num_sms, st)
+                    : launch_gqa_t<BITS, 4, 0, RG, 2, MF>(a, num_sms, st);
+  return ngk == 4 ? launch_gqa_t<BITS, 2, 0, RG, 4, MF>(a, num_sms, st)
+                  : launch_gqa_t<BITS, 2, 0, RG, 2, MF>(a, num_sms, st);
+}
+template <int MF>
+cudaError_t launch_innerq(TcArgs &a, int num_sms, cudaStream_t st) {
+  const int rg = a.g.Hq / a.g.H;
+  if (a.g.bits == 4)
+    return rg == 4 ? launch_innerq_br<MF, 4, 4>(a, num_sms, st)
+                   : launch_innerq_br<MF, 4, 2>(a, num_sms, st);
+  return rg == 4 ? launch_innerq_br<MF, 2, 4>(a, num_sms, st)
+                 : launch_innerq_br<MF, 2, 2>(a, num_sms, st);
+}
+
 }  // namespace
 
-// InnerQ keys (kvq_decode_gqa_iq.cu): the launch of the instantiation the
-// geometry names, with the arguments launch_decode_gqa filled in.
+// The other families' launches, each in a translation unit of its own so the
+// instantiations compile in parallel (arguments filled in by
+// launch_decode_gqa): InnerQ keys (kvq_decode_gqa_iq.cu), KIVI keys with fp16
+// statistics (kvq_decode_gqa_f16.cu), InnerQ keys with fp16 statistics
+// (kvq_decode_gqa_iq16.cu).
 cudaError_t launch_gqa_innerq(TcArgs &a, int num_sms, cudaStream_t st);
+cudaError_t launch_gqa_kivi_f16(TcArgs &a, int num_sms, cudaStream_t st);
+cudaError_t launch_gqa_innerq_f16(TcArgs &a, int num_sms, cudaStream_t st);
 
 }  // namespace kvq

@@ -294,7 +294,7 @@ int gqa_variant_name(const Geometry &g, char *buf, size_t len);
 
 // Tensor-core grouped-query path (head_dim 128, 2 or 4 query heads per KV
 // head, 2 or 4 value groups; 2- or 4-bit KIVI with G >= 32, or InnerQ with
-// key channel groups of 32 or 64).
+// key channel groups of 32 or 64; statistics in fp32 or fp16).
 bool gqa_decode_supported(const Geometry &g);
 cudaError_t launch_decode_gqa(const Geometry &g, const CachePtrs &p, int64_t n_quant,
                               int64_t n_resid, int64_t n_sink, const __half *q, float *out,

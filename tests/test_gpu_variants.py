@@ -36,17 +36,17 @@ def _innerq(bits, ngv, ngk, mf=False, ragged=False):
              ragged=ragged)
 
 
-def _gqa_iq(bits, ngv, ngk, rg, knorm=False):
+def _gqa_iq(bits, ngv, ngk, rg, knorm=False, mf=False):
     # 700 prompt tokens: 4 sinks, a 32-token window, 664 quantized (a short
     # last tile), and every append moves one more token into the quantized
     # region
     return S(W["innerq_1m"], batch=2, n_q_heads=2 * rg, n_kv_heads=2, ctx=700, bits=bits,
-             k_group=128 // ngk, v_group=128 // ngv, n_append=40, k_norm=knorm)
+             k_group=128 // ngk, v_group=128 // ngv, n_append=40, k_norm=knorm, meta_f16=mf)
 
 
-def _gqa(bits, ngv, G, rg):
+def _gqa(bits, ngv, G, rg, mf=False):
     return S(W["gqa_2bit"], batch=2, n_q_heads=2 * rg, n_kv_heads=2, ctx=900, bits=bits,
-             k_group=G, v_group=128 // ngv, residual=128, n_append=140)
+             k_group=G, v_group=128 // ngv, residual=128, n_append=140, meta_f16=mf)
 
 
 CASES = {}
@@ -66,11 +66,13 @@ for mf in (False, True):
     for bits, ngv, ngk in itertools.product((2, 4), (2, 4), (2, 4)):
         CASES["tc_innerq_b%d_ngv%d_ngk%d%s_ragged" % (bits, ngv, ngk, sfx)] = _innerq(
             bits, ngv, ngk, mf, ragged=True)
-for bits, ngv, G, rg in itertools.product((2, 4), (2, 4), (32, 64), (2, 4)):
-    CASES["gqa_b%d_ngv%d_g%d_rg%d" % (bits, ngv, G, rg)] = _gqa(bits, ngv, G, rg)
-    # InnerQ keys: the same four axes, with G read as 128 / key channel groups
-    CASES["gqa_innerq_b%d_ngv%d_ngk%d_rg%d" % (bits, ngv, 128 // G, rg)] = _gqa_iq(
-        bits, ngv, 128 // G, rg)
+for mf in (False, True):
+    sfx = "_f16" if mf else ""
+    for bits, ngv, G, rg in itertools.product((2, 4), (2, 4), (32, 64), (2, 4)):
+        CASES["gqa_b%d_ngv%d_g%d_rg%d%s" % (bits, ngv, G, rg, sfx)] = _gqa(bits, ngv, G, rg, mf)
+        # InnerQ keys: the same four axes, with G read as 128 / key channel groups
+        CASES["gqa_innerq_b%d_ngv%d_ngk%d_rg%d%s" % (bits, ngv, 128 // G, rg, sfx)] = _gqa_iq(
+            bits, ngv, 128 // G, rg, mf=mf)
 # InnerQ's folded key normalization on the grouped-query kernel (a run-time
 # flag of the same instantiations)
 CASES["gqa_innerq_knorm_b2_ngv4_ngk4_rg2"] = _gqa_iq(2, 4, 4, 2, knorm=True)
@@ -115,8 +117,8 @@ def test_every_dispatched_instantiation_has_a_parity_case():
     # MHA: 20 shapes with fp32 and with fp16 statistics, each plain and with
     # per-sequence lengths only, and the 12 KIVI shapes extended (outlier lists,
     # value queue; InnerQ has neither); grouped-query: 8 for each code width
-    # with KIVI keys, 8 with InnerQ keys
-    assert len(dispatched) == 2 * (2 * 20 + 12) + 32, sorted(dispatched)
+    # with KIVI keys, 8 with InnerQ keys, each with fp32 and fp16 statistics
+    assert len(dispatched) == 2 * (2 * 20 + 12) + 64, sorted(dispatched)
     covered = {_name(w) for w in CASES.values()}
     assert dispatched <= covered, sorted(dispatched - covered)
     # and each named case reaches the instantiation its name says
