@@ -130,11 +130,16 @@ GQA_CASES = [synth.WORKLOADS["gqa_2bit"],
              synth.scaled(synth.WORKLOADS["innerq_1m"], batch=2, n_q_heads=8, n_kv_heads=2,
                           ctx=700),
              synth.scaled(synth.WORKLOADS["innerq_1m"], batch=1, n_q_heads=8, n_kv_heads=4,
-                          bits=2, k_group=32)]
+                          bits=2, k_group=32),
+             # fp16 statistics: smaller blocks, so other chunk and unit counts
+             synth.scaled(synth.WORKLOADS["gqa_2bit"], meta_f16=True),
+             synth.scaled(synth.WORKLOADS["innerq_1m"], batch=2, n_q_heads=8, n_kv_heads=2,
+                          ctx=700, meta_f16=True)]
 
 
 @pytest.mark.parametrize("w", GQA_CASES,
-                         ids=lambda w: "%s_B%d_T%d_b%d" % (w.name, w.batch, w.ctx, w.bits))
+                         ids=lambda w: "%s_B%d_T%d_b%d%s" % (w.name, w.batch, w.ctx, w.bits,
+                                                             "_f16" if w.meta_f16 else ""))
 def test_gqa_split_never_exceeds_the_partial_slots(w):
     """Block counts up to 8 resident blocks on each of 152 SMs (the kernel
     fits at most 2: 112 KB of shared memory per block; 4-bit codes, 1)."""
